@@ -1,0 +1,253 @@
+"""Pins for the fp64 oracle: checks against facts that do not come from the
+oracle itself. Each pin takes an ``oracle.Oracle`` and raises AssertionError
+when the oracle disagrees. test_oracle_pins.py runs them on the real oracle;
+test_oracle_mutants.py runs them on deliberately broken copies and expects a
+failure from at least one.
+
+What pins what:
+  * windows            hand-worked window tables (tests/golden/windows.json)
+  * landmarks          torch adaptive_avg_pool1d/2d in float64 (library
+                       routine); m=1 gives the mean query; m=N in 2-D gives Q
+  * scores             numpy matmul
+  * top-k              brute-force ranking by counting, with planted exact ties
+  * LV                 scipy softmax attention of each landmark over all keys
+  * routing            numpy argmax (first index on ties) and sorted margins
+  * attention          k=N reduces the method to plain softmax attention over
+                       [Lq; K] with values [LV; V], whatever the routes
+  * weights            softmax weights sum to 1
+  * permutation        permuting K,V rows permutes the experts' indices and
+                       leaves LV, routes and outputs unchanged
+  * hand example       a 4-token, d=2 case worked out in closed form
+"""
+from __future__ import annotations
+
+import json
+import math
+import os
+
+import numpy as np
+from scipy.special import softmax
+
+import synth
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def _f64(a):
+    return synth.bf16_to_f64(a)
+
+
+def _rand(shape, seed, tag, scale=1.0):
+    return synth.normal_bf16(shape, seed, tag, scale)
+
+
+def pin_window_tables(o):
+    g = json.load(open(os.path.join(GOLDEN, "windows.json")))
+    for key, gh, p in (("14->5", 14, 5), ("32->7", 32, 7), ("40->7", 40, 7)):
+        bounds = g["axis_bounds"][key]
+        for i in range(p * p):
+            r, c = divmod(i, p)
+            (y0, y1), (x0, x1) = bounds[r], bounds[c]
+            want = [y * gh + x for y in range(y0, y1) for x in range(x0, x1)]
+            got = o.window(gh * gh, gh, gh, p * p, i).tolist()
+            assert got == want, f"{key} window {i}: {got} != {want}"
+    od = g["one_d"]
+    for i, (a, b) in enumerate(od["bounds"]):
+        assert o.window(od["N"], 0, 0, od["m"], i).tolist() == list(range(a, b))
+    for i in range(64):  # divisible case: exactly N/m tokens each
+        assert o.window(4096, 0, 0, 64, i).tolist() == list(range(64 * i, 64 * i + 64))
+
+
+def pin_landmarks_adaptive_pool(o):
+    import torch
+    import torch.nn.functional as F
+
+    q = _rand((2, 3, 196, 64), 11, 0)
+    lq = o.landmarks(q, 14, 14, 25)
+    t = torch.from_numpy(_f64(q)).reshape(6, 14, 14, 64).permute(0, 3, 1, 2)
+    ref = F.adaptive_avg_pool2d(t, (5, 5)).permute(0, 2, 3, 1).reshape(2, 3, 25, 64).numpy()
+    assert np.max(np.abs(lq - ref)) < 1e-12
+    q = _rand((1, 2, 1600, 64), 12, 0)
+    lq = o.landmarks(q, 40, 40, 49)
+    t = torch.from_numpy(_f64(q)).reshape(2, 40, 40, 64).permute(0, 3, 1, 2)
+    ref = F.adaptive_avg_pool2d(t, (7, 7)).permute(0, 2, 3, 1).reshape(1, 2, 49, 64).numpy()
+    assert np.max(np.abs(lq - ref)) < 1e-12
+    q = _rand((1, 2, 1000, 64), 13, 0)  # 1-D, m does not divide N
+    lq = o.landmarks(q, 0, 0, 7)
+    t = torch.from_numpy(_f64(q)).reshape(2, 1000, 64).permute(0, 2, 1)
+    ref = F.adaptive_avg_pool1d(t, 7).permute(0, 2, 1).reshape(1, 2, 7, 64).numpy()
+    assert np.max(np.abs(lq - ref)) < 1e-12
+
+
+def pin_landmarks_special(o):
+    q = _rand((1, 2, 196, 64), 14, 0)
+    mean = _f64(q).mean(axis=2, keepdims=True)
+    assert np.max(np.abs(o.landmarks(q, 0, 0, 1) - mean)) < 1e-12
+    assert np.max(np.abs(o.landmarks(q, 14, 14, 1) - mean)) < 1e-12
+    assert np.array_equal(o.landmarks(q, 14, 14, 196), _f64(q))  # m = N: one token per window
+
+
+def pin_scores(o):
+    q, k = _rand((2, 1, 300, 64), 15, 0), _rand((2, 1, 300, 64), 15, 1)
+    lq = o.landmarks(q, 0, 0, 10)
+    for bh in range(2):
+        ref = (lq.reshape(2, 10, 64)[bh] @ _f64(k).reshape(2, 300, 64)[bh].T) / 8.0
+        for i in (0, 9):
+            assert np.max(np.abs(o.scores(lq, k, bh, i) - ref[i])) < 1e-12
+
+
+def _brute_topk(s, kk):
+    """Key j is selected iff fewer than kk keys beat it, where j' beats j when
+    s[j'] > s[j], or s[j'] == s[j] and j' < j."""
+    n = len(s)
+    sel = []
+    for j in range(n):
+        beats = sum(1 for jj in range(n) if s[jj] > s[j] or (s[jj] == s[j] and jj < j))
+        if beats < kk:
+            sel.append(j)
+    order = sorted(range(n), key=lambda j: (-s[j], j))
+    gap = s[order[kk - 1]] - s[order[kk]] if kk < n else math.inf
+    return sel, gap
+
+
+def pin_topk_bruteforce(o):
+    N = 40
+    q, k, v = _rand((1, 2, N, 64), 16, 0), _rand((1, 2, N, 64), 16, 1), _rand((1, 2, N, 64), 16, 2)
+    k = k.copy()
+    k[0, 0, 7] = k[0, 0, 3]  # exact ties: duplicate rows...
+    k[0, 0, 30] = k[0, 0, 3]
+    k[0, 1, 5] = 0  # ...and zero rows (score exactly 0)
+    k[0, 1, 25] = 0
+    lq = o.landmarks(q, 0, 0, 4)
+    for kk in (1, 2, 3, 7, 20, N - 1, N):
+        _, e, gap = o.scan(lq, k, v, kk)
+        for bh in range(2):
+            for i in range(4):
+                s = o.scores(lq, k, bh, i).tolist()
+                sel, g = _brute_topk(s, kk)
+                assert e[bh, i].tolist() == sel, (kk, bh, i)
+                assert g == gap[bh, i] or (math.isinf(g) and math.isinf(gap[bh, i]))
+    # a landmark equal to a duplicated key direction: force the tie to straddle the cut
+    lq2 = np.zeros((1, 2, 4, 64))
+    lq2[0, 0, :] = _f64(k[0, 0, 3])
+    _, e, gap = o.scan(lq2, k, v, 2)
+    s = o.scores(lq2, k, 0, 0).tolist()
+    sel, _ = _brute_topk(s, 2)
+    assert e[0, 0].tolist() == sel and sel == [3, 7]
+
+
+def pin_lv_textbook(o):
+    q, k, v = _rand((1, 3, 257, 64), 17, 0), _rand((1, 3, 257, 64), 17, 1, 2.0), _rand((1, 3, 257, 64), 17, 2)
+    lq = o.landmarks(q, 0, 0, 5) * 4.0  # sharper softmax
+    lv, _, _ = o.scan(lq, k, v, 3, want_idx=False, want_gap=False)
+    K, V = _f64(k).reshape(3, 257, 64), _f64(v).reshape(3, 257, 64)
+    for bh in range(3):
+        w = softmax(lq.reshape(3, 5, 64)[bh] @ K[bh].T / 8.0, axis=-1)
+        assert np.max(np.abs(lv[bh] - w @ V[bh])) < 1e-12
+
+
+def pin_route_argmax(o):
+    q = _rand((2, 2, 150, 64), 18, 0)
+    lq = o.landmarks(q, 0, 0, 6)
+    r, g = o.route(q, lq)
+    t = np.einsum("bhnc,bhic->bhni", _f64(q), lq) / 8.0
+    assert np.array_equal(r.reshape(2, 2, 150), np.argmax(t, axis=-1))
+    ts = np.sort(t, axis=-1)
+    assert np.max(np.abs(g.reshape(2, 2, 150) - (ts[..., -1] - ts[..., -2]))) < 1e-12
+    which = np.array([0, 151, 599])
+    r2, _ = o.route(q, lq, which=which)
+    assert np.array_equal(r2, r.reshape(-1)[which])
+
+
+def pin_attention_k_equals_n(o):
+    N, m = 60, 4
+    q, k, v = _rand((1, 2, N, 64), 19, 0, 2.0), _rand((1, 2, N, 64), 19, 1), _rand((1, 2, N, 64), 19, 2)
+    r = o.forward(q, k, v, 0, 0, m, N)
+    assert np.array_equal(r["expert_idx"][0], np.broadcast_to(np.arange(N), (2, m, N)))
+    Q, K, V = _f64(q)[0], _f64(k)[0], _f64(v)[0]
+    for h in range(2):
+        keys = np.concatenate([r["lq"][0, h], K[h]])
+        vals = np.concatenate([r["lv"][0, h], V[h]])
+        w = softmax(Q[h] @ keys.T / 8.0, axis=-1)
+        assert np.max(np.abs(r["out"][0, h] - w @ vals)) < 1e-12
+    # with every key in every expert the routes cannot matter
+    other = (r["route"] + 1) % m
+    out2, _ = o.attend(q, r["lq"], r["lv"], k, v, r["expert_idx"], other)
+    assert np.max(np.abs(out2 - r["out"].reshape(2, N, 64))) < 1e-12
+
+
+def pin_weights_sum_to_one(o):
+    q, k, v = synth.make_inputs("tiny")
+    r = o.forward(q, k, v, 14, 14, 25, 25)
+    assert np.max(np.abs(r["wsum"] - 1.0)) < 1e-12
+
+
+def pin_permutation(o):
+    N = 128
+    q, k, v = _rand((1, 2, N, 64), 20, 0), _rand((1, 2, N, 64), 20, 1), _rand((1, 2, N, 64), 20, 2)
+    rng = np.random.default_rng(5)
+    pi = rng.permutation(N)
+    kp, vp = k[:, :, pi], v[:, :, pi]  # row j of the permuted inputs is row pi[j]
+    a = o.forward(q, k, v, 0, 0, 8, 10)
+    b = o.forward(q, kp, vp, 0, 0, 8, 10)
+    inv = np.argsort(pi)
+    mapped = np.sort(inv[a["expert_idx"]], axis=-1)  # old key j now sits at inv[j]
+    assert np.array_equal(mapped, b["expert_idx"])
+    assert np.array_equal(a["route"], b["route"])
+    assert np.max(np.abs(a["lv"] - b["lv"])) < 1e-12
+    assert np.max(np.abs(a["out"] - b["out"])) < 1e-12
+
+
+def pin_hand_example(o):
+    """N=4 tokens, d=2, 1-D windows of 2 (m=2), k=1; tau = 1/sqrt(2).
+
+    Q = (2,0),(0,0),(0,4),(0,0) -> Lq_0 = (1,0), Lq_1 = (0,2).
+    K = (1,0),(0,1),(-1,0),(0,0);  V = (1,0),(0,1),(0,0),(0,0).
+    Landmark 0 logits (t,0,-t,0): expert {0}, gap t,
+        LV_0 = (e^t, 1) / (e^t + e^-t + 2).
+    Landmark 1 logits (0,2t,0,0): expert {1}, gap 2t,
+        LV_1 = (1, e^2t) / (3 + e^2t).
+    Routes: q0 -> 0 (margin 2t); q1, q3 tie at 0 -> 0 (margin 0); q2 -> 1 (8t).
+    Outputs (one softmax over [Lq_0, Lq_1, routed key]):
+        q0: logits (2t, 0, 2t)  -> (e^2t LV_0 + LV_1 + e^2t v0) / (2 e^2t + 1)
+        q1, q3: all 0           -> (LV_0 + LV_1 + v0) / 3
+        q2: logits (0, 8t, 4t)  -> (LV_0 + e^8t LV_1 + e^4t v1) / (1 + e^8t + e^4t)
+    """
+    t = 1.0 / math.sqrt(2.0)
+    bf = lambda rows: synth.f64_to_bf16(np.array(rows, dtype=np.float64)).reshape(1, 1, 4, 2)
+    q = bf([[2, 0], [0, 0], [0, 4], [0, 0]])
+    k = bf([[1, 0], [0, 1], [-1, 0], [0, 0]])
+    v = bf([[1, 0], [0, 1], [0, 0], [0, 0]])
+    r = o.forward(q, k, v, 0, 0, 2, 1)
+    e = math.exp
+    lv0 = np.array([e(t), 1.0]) / (e(t) + e(-t) + 2)
+    lv1 = np.array([1.0, e(2 * t)]) / (3 + e(2 * t))
+    v0, v1 = np.array([1.0, 0.0]), np.array([0.0, 1.0])
+    assert np.array_equal(r["lq"][0, 0], [[1.0, 0.0], [0.0, 2.0]])
+    assert r["expert_idx"][0, 0].tolist() == [[0], [1]]
+    assert np.allclose(r["gap"][0, 0], [t, 2 * t], rtol=0, atol=1e-15)
+    assert np.allclose(r["lv"][0, 0], [lv0, lv1], rtol=0, atol=1e-15)
+    assert r["route"][0, 0].tolist() == [0, 0, 1, 0]
+    assert np.allclose(r["rgap"][0, 0], [2 * t, 0, 8 * t, 0], rtol=0, atol=1e-14)
+    want = np.array([
+        (e(2 * t) * lv0 + lv1 + e(2 * t) * v0) / (2 * e(2 * t) + 1),
+        (lv0 + lv1 + v0) / 3,
+        (lv0 + e(8 * t) * lv1 + e(4 * t) * v1) / (1 + e(8 * t) + e(4 * t)),
+        (lv0 + lv1 + v0) / 3,
+    ])
+    assert np.max(np.abs(r["out"][0, 0] - want)) < 1e-14
+
+
+ALL_PINS = [
+    pin_window_tables,
+    pin_landmarks_adaptive_pool,
+    pin_landmarks_special,
+    pin_scores,
+    pin_topk_bruteforce,
+    pin_lv_textbook,
+    pin_route_argmax,
+    pin_attention_k_equals_n,
+    pin_weights_sum_to_one,
+    pin_permutation,
+    pin_hand_example,
+]
