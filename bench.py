@@ -1,0 +1,426 @@
+#!/usr/bin/env python
+"""MiTA forward pass on GB300: queries/s and the roofline fraction.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl mita|reference]
+                    [--config long1m] [--no-sweep] [--no-cpu] [--no-e2e]
+
+One step = one full forward pass (landmark pooling, landmark scan with expert
+selection, routing, grouping, expert attention) over one synthetic batch
+already resident in HBM. value = B*H*N queries / device time per step. With
+N GPUs (torchrun) every rank runs an independent replica on its own inputs
+(the heads are independent problems; there is no exchange step), the time is
+the max over ranks, and value counts the queries of all ranks (weak scaling).
+
+--impl reference times the fp64 CPU oracle on the host cores instead, on a
+bounded sample of the same workload (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "MiTA fwd queries/s at N=4K-1M, d=64; achieved fraction of roofline"
+DEFAULT_CONFIG = "long1m"
+SWEEP = ("lra", "long64k", "long256k")
+PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+STAGES = ("pool", "scan", "select", "route", "group", "expert")
+KERNEL_SOURCES = {"pool": "pool.cu", "scan": "scan_simt.cu", "select": "select.cu", "route": "route_simt.cu",
+                  "group": "group.cu", "expert": "expert_simt.cu"}
+
+
+def describe(name):
+    c = synth.CONFIGS[name]
+    grid = f"{c['grid_h']}x{c['grid_w']} grid" if c["grid_h"] else f"1-D windows of {c['N'] // c['m']}"
+    rec = {"iid": "Q,K,V i.i.d. N(0,1)",
+           "outliers": "Q,K,V i.i.d. N(0,1), 1% of key rows x4",
+           "clusters": f"K,Q from {c.get('clusters')} Gaussian clusters (sigma 0.3), V N(0,1)",
+           "runs": f"K,Q from {c.get('clusters')} clusters in runs of 16-256 tokens, V N(0,1)"}[c["recipe"]]
+    return f"{name}: B={c['B']} H={c['H']} N={c['N']} d=64 m={c['m']} k={c['k']}, {grid}; {rec}; seed 0"
+
+
+# ---------------------------------------------------------------------------
+# Algorithmic work per stage (the roofline numerators), per call.
+# Whole pass: FLOPs = B*H*(4 m N d + 4 N (m+k) d); bytes = B*H*(3 N d + N d)*2
+# + B*H*m*k*2*d*2 (Q,K,V read once, gathered expert rows, output written).
+# ---------------------------------------------------------------------------
+def work(c):
+    BH, N, d, m, k = c["B"] * c["H"], c["N"], 64, c["m"], c["k"]
+    row = N * d * 2
+    return {
+        "total": {"flops": BH * (4 * m * N * d + 4 * N * (m + k) * d),
+                  "bytes": BH * (4 * row + m * k * 2 * d * 2)},
+        "pool": {"flops": 0, "bytes": BH * row},
+        "scan": {"flops": BH * 4 * m * N * d, "bytes": BH * 2 * row},
+        "route": {"flops": BH * 2 * N * m * d, "bytes": BH * row},
+        "expert": {"flops": BH * 4 * N * (m + k) * d, "bytes": BH * (2 * row + m * k * 2 * d * 2)},
+    }
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        j = json.load(open(p))
+        return {k: float(j[k]) for k in PEAKS_FALLBACK}, "measured"
+    return dict(PEAKS_FALLBACK), "fallback"
+
+
+def roofline_time(w, peaks, sustained):
+    tf = peaks["bf16_tflops_sustained" if sustained else "bf16_tflops"] * 1e12
+    return max(w["flops"] / tf, w["bytes"] / (peaks["hbm_gbs"] * 1e9))
+
+
+def kernel_traffic(stage, workload):
+    """DRAM bytes per launch of a stage's kernel from a committed ncu summary,
+    or None when absent or taken on a different version of the kernel source."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    t = json.load(open(p)).get(stage)
+    if not t or t.get("workload") != workload:
+        return None
+    src = os.path.join(ROOT, "mixture_top_forward_gb300", "csrc", KERNEL_SOURCES[stage])
+    if hashlib.sha256(open(src, "rb").read()).hexdigest()[:16] != t.get("source_sha"):
+        return None
+    return t.get("bytes_per_launch")
+
+
+# ---------------------------------------------------------------------------
+# Clock sampling during the timed region.
+# ---------------------------------------------------------------------------
+class Clocks:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.path = tempfile.mktemp(prefix="clocks", suffix=".csv")
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={gpu_index}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 7:
+                continue
+            try:
+                rows.append((float(f[0]), float(f[1]), f[3:7]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        reasons = sorted({names[i] for _, _, r in rows for i in range(4) if r[i].lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing on a bounded sample of one head.
+# ---------------------------------------------------------------------------
+def oracle_head_time(name, q, k, v, n_landmarks, n_queries, seed=1):
+    """Seconds the oracle needs for one whole head, estimated from a sample:
+    pooling of the head in full, the scan of `n_landmarks` landmarks (values
+    and expert selection) and routing + attention of `n_queries` queries,
+    each scaled to the full head (m landmarks, N queries). The attention of
+    the sampled queries runs on the scanned landmarks' experts and values,
+    with same-shaped stand-ins for the rest (the work does not depend on the
+    values)."""
+    import oracle
+
+    c = synth.CONFIGS[name]
+    N, m, kk, gh, gw = c["N"], c["m"], c["k"], c["grid_h"], c["grid_w"]
+    rng = np.random.default_rng(seed)
+    qs, ks, vs = q[:1, :1], k[:1, :1], v[:1, :1]
+    t0 = time.perf_counter()
+    lq = oracle.landmarks(qs, gh, gw, m)
+    t1 = time.perf_counter()
+    nl = min(m, n_landmarks)
+    which_l = np.sort(rng.choice(m, size=nl, replace=False))
+    lv_s, e_s, _ = oracle.scan(lq, ks, vs, kk, which=which_l)
+    t2 = time.perf_counter()
+    lv = np.zeros((1, 1, m, 64))
+    e = np.tile(np.arange(kk, dtype=np.int32), (1, 1, m, 1))
+    lv[0, 0, which_l] = lv_s
+    e[0, 0, which_l] = e_s
+    nq = min(N, n_queries)
+    which_q = np.sort(rng.choice(N, size=nq, replace=False))
+    r_s, _ = oracle.route(qs, lq, which=which_q)
+    route = np.zeros((1, 1, N), np.int32)
+    route[0, 0, which_q] = r_s
+    t3 = time.perf_counter()
+    oracle.attend(qs, lq, lv, ks, vs, e, route, which=which_q)
+    t4 = time.perf_counter()
+    t_head = (t1 - t0) + (t2 - t1) * m / nl + (t4 - t2) * N / nq
+    sample = (f"1 head of {name}: pooling of all {N} tokens, scan of {nl}/{m} landmarks, routing+attention of "
+              f"{nq}/{N} queries, scaled to the head")
+    return t_head, sample, t4 - t0
+
+
+def cpu_baseline(name, q, k, v, budget_landmarks=256, budget_queries=131072):
+    import oracle
+
+    t_head, sample, wall = oracle_head_time(name, q, k, v, budget_landmarks, budget_queries)
+    c = synth.CONFIGS[name]
+    return {"value": c["N"] / t_head, "unit": "queries/s", "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": sample, "wall_s": round(wall, 2)}
+
+
+# ---------------------------------------------------------------------------
+# GPU arm.
+# ---------------------------------------------------------------------------
+def run_gpu(args, rank, world):
+    import torch
+
+    import mixture_top_forward_gb300 as M
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    M.load(build_if_missing=False)
+    name = args.config
+    c = synth.CONFIGS[name]
+    B, H, N, m, kk, gh, gw = c["B"], c["H"], c["N"], c["m"], c["k"], c["grid_h"], c["grid_w"]
+    q, k, v = synth.make_inputs(c, seed=rank)
+
+    def dev_bf16(a):
+        return torch.from_numpy(a.view(np.int16)).to(dev).view(torch.bfloat16)
+
+    Q, K, V = dev_bf16(q), dev_bf16(k), dev_bf16(v)
+    out = torch.empty_like(Q)
+    eidx = torch.empty((B, H, m, kk), dtype=torch.int32, device=dev)
+    route = torch.empty((B, H, N), dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        M.mita_forward(Q, K, V, gh, gw, m, kk, out=out, expert_idx=eidx, route=route, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    assert M.mita_sync_status(stream) == 0, M.mita_last_error()
+    M.mita_profile_read(stream)  # discard
+    clocks = Clocks(dev.index) if rank == 0 else None
+    time.sleep(0.3 if clocks else 0)
+    M.mita_profile_enable(True)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    M.mita_profile_enable(False)
+    ms = ev0.elapsed_time(ev1)
+    stages = M.mita_profile_read(stream)
+    clk = clocks.stop() if clocks else None
+    assert M.mita_sync_status(stream) == 0, M.mita_last_error()
+    if world > 1:
+        t = torch.tensor([ms], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    ms_step = ms / args.steps
+    queries = B * H * N
+    value = queries * world / (ms_step / 1e3)
+
+    peaks, peak_src = load_peaks()
+    w = work(c)
+    t_roof = roofline_time(w["total"], peaks, sustained=True)
+    stage_ms = {s: stages[s][0] / args.steps for s in STAGES}
+    launches = sum(stages[s][1] for s in STAGES)
+    dom = max(("pool", "scan", "route", "expert"), key=lambda s: stage_ms[s])
+    wd = w[dom]
+    t_dom = stage_ms[dom] / 1e3
+    tensor = wd["flops"] / (peaks["bf16_tflops_sustained"] * 1e12) >= wd["bytes"] / (peaks["hbm_gbs"] * 1e9)
+    if tensor:
+        ach = wd["flops"] / t_dom / 1e12
+        roof = {"bound": "tensor", "achieved": ach, "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s"}
+    else:
+        ach = wd["bytes"] / t_dom / 1e9
+        roof = {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["traffic"] = kernel_traffic(dom, name)
+    roof["kernel"] = dom
+    roof["peak_source"] = f"{peak_src} ({'sustained bf16' if tensor else 'copy bandwidth'})"
+
+    res = {
+        "metric": METRIC, "value": value, "unit": "queries/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": describe(name), "B": B, "H": H, "N": N, "d": 64, "m": m, "k": kk,
+                   "l2": f"inputs ({3 * Q.numel() * 2 / 1e9:.2f} GB) larger than L2, no flush",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "roofline": roof,
+        "roofline_whole_pass": {"t_roof_us": t_roof * 1e6, "t_us": ms_step * 1e3, "frac": t_roof / (ms_step / 1e3),
+                                "flops": w["total"]["flops"], "bytes": w["total"]["bytes"],
+                                "peak_source": f"{peak_src} (sustained bf16, copy bandwidth)"},
+        "stage_ms": stage_ms,
+        "gpu_launches": launches,
+        "clocks": clk,
+    }
+    del Q, K, V, out
+    torch.cuda.empty_cache()
+
+    if rank == 0 and not args.no_e2e:
+        res["e2e"] = e2e(args, M, q, k, v, c, stream)
+    if rank == 0 and not args.no_sweep:
+        res["sweep"] = sweep(args, M, dev, stream, peaks)
+    if rank == 0 and not args.no_cpu and world == 1:
+        res["cpu_baseline"] = cpu_baseline(name, q, k, v)
+    return res
+
+
+def e2e(args, M, q, k, v, c, stream):
+    """Same metric through the host-buffer entry point: each step copies the
+    inputs from pinned host memory and the results back."""
+    import torch
+
+    pin = lambda a: torch.from_numpy(a).pin_memory().numpy()
+    qh, kh, vh = pin(q), pin(k), pin(v)
+    out = pin(np.empty_like(q))
+    eidx = pin(np.empty((c["B"], c["H"], c["m"], c["k"]), np.int32))
+    route = pin(np.empty((c["B"], c["H"], c["N"]), np.int32))
+    args_ = (c["grid_h"], c["grid_w"], c["m"], c["k"])
+    for _ in range(max(1, min(args.warmup, 3))):
+        M.mita_forward_host(qh, kh, vh, *args_, out=out, expert_idx=eidx, route=route, stream=stream.cuda_stream)
+    n = max(3, min(args.steps, 10))
+    t0 = time.perf_counter()
+    for _ in range(n):
+        M.mita_forward_host(qh, kh, vh, *args_, out=out, expert_idx=eidx, route=route, stream=stream.cuda_stream)
+    dt = (time.perf_counter() - t0) / n
+    return {"value": c["B"] * c["H"] * c["N"] / dt, "unit": "queries/s",
+            "h2d_bytes_per_step": int(qh.nbytes + kh.nbytes + vh.nbytes),
+            "d2h_bytes_per_step": int(out.nbytes + eidx.nbytes + route.nbytes), "steps": n,
+            "ms_per_step": dt * 1e3}
+
+
+def sweep(args, M, dev, stream, peaks):
+    """The other long-sequence workloads of the metric (N=4K..256K)."""
+    import torch
+
+    res = {}
+    for name in SWEEP:
+        if name == args.config:
+            continue
+        c = synth.CONFIGS[name]
+        q, k, v = synth.make_inputs(c)
+        to = lambda a: torch.from_numpy(a.view(np.int16)).to(dev).view(torch.bfloat16)
+        Q, K, V = to(q), to(k), to(v)
+        out = torch.empty_like(Q)
+        e = torch.empty((c["B"], c["H"], c["m"], c["k"]), dtype=torch.int32, device=dev)
+        r = torch.empty((c["B"], c["H"], c["N"]), dtype=torch.int32, device=dev)
+        a = (c["grid_h"], c["grid_w"], c["m"], c["k"])
+        for _ in range(3):
+            M.mita_forward(Q, K, V, *a, out=out, expert_idx=e, route=r, stream=stream)
+        torch.cuda.synchronize()
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        n = 10
+        ev0.record(stream)
+        for _ in range(n):
+            M.mita_forward(Q, K, V, *a, out=out, expert_idx=e, route=r, stream=stream)
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        ms = ev0.elapsed_time(ev1) / n
+        t_roof = roofline_time(work(c)["total"], peaks, sustained=True)
+        res[name] = {"queries_per_s": c["B"] * c["H"] * c["N"] / (ms / 1e3), "ms_per_step": ms,
+                     "roofline_frac": t_roof / (ms / 1e3)}
+        del Q, K, V, out
+        torch.cuda.empty_cache()
+    return res
+
+
+# ---------------------------------------------------------------------------
+# Reference arm: the fp64 oracle on the host cores.
+# ---------------------------------------------------------------------------
+def run_reference(args, rank, world):
+    import oracle
+
+    if rank != 0:
+        return None
+    name = args.config
+    c = synth.CONFIGS[name]
+    q, k, v = synth.make_inputs(c)
+    for _ in range(args.warmup):
+        oracle_head_time(name, q, k, v, 2, 512)
+    times, sample = [], ""
+    for s in range(args.steps):
+        t_head, sample, _ = oracle_head_time(name, q, k, v, 16, 8192, seed=100 + s)
+        times.append(t_head)
+    t = statistics.median(times)
+    value = c["N"] / t
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "queries/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": t * 1e3 * c["B"] * c["H"],
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": describe(name), "B": c["B"], "H": c["H"], "N": c["N"], "d": 64, "m": c["m"],
+                   "k": c["k"]},
+        "cpu_baseline": {"value": value, "unit": "queries/s", "cores": oracle.num_threads(), "kind": "oracle",
+                         "sample": sample + "; each step one such sample, median over steps"},
+        "e2e": {"value": value, "unit": "queries/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("mita", "reference"), default="mita")
+    ap.add_argument("--config", default=DEFAULT_CONFIG, choices=sorted(synth.CONFIGS))
+    ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "mita":
+        ap.error("--warmup must be >= 3")
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        res = run_reference(args, rank, world)
+    else:
+        if world > 1:
+            import torch
+
+            torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+            torch.distributed.init_process_group("nccl")
+        res = run_gpu(args, rank, world)
+        if world > 1:
+            import torch
+
+            torch.distributed.destroy_process_group()
+    if rank == 0 and res is not None:
+        print(json.dumps(res), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,143 @@
+/*
+ * mita.h -- C ABI of libmita.so, a GB300 (sm_103a) implementation of the
+ * forward pass of Mixture-of-Top-k Attention (MiTA).
+ *
+ * The method (described in prose in "NeurIPS 2026 | Mixture-of-Top-k 注意力：
+ * 从快权重统一高效注意力…" (shuwu5.cn), section "MiTA：用少量地标查询，同时完成
+ * 压缩与专家构造"; the same steps in "NeurIPS'26：注意力也是FFN？…"
+ * (pro-axy-igame.com), section "用少量地标查询，同时构造全局概括与细节专家", and in
+ * the Figure 3 and Algorithm 1 captions of "And attention is also FFN? …"
+ * (en.roboind.com)), per head (b,h), with tau = 1/sqrt(d):
+ *   1. landmarks   Lq_i = mean of the query rows in local window i (i < m);
+ *   2. scan        s_ij = tau <Lq_i, K_j> over all N keys;
+ *                  shared expert value LV_i = sum_j softmax_j(s_i.) V_j;
+ *                  routed expert E_i = the k keys with the largest s_ij;
+ *   3. routing     e(n) = argmax_i tau <q_n, Lq_i>;
+ *   4. attention   out_n = softmax over the m logits tau<q_n, Lq_i> and the k
+ *                  logits tau<q_n, K_j> (j in E_e(n)) together, applied to
+ *                  the values [LV_1..LV_m ; V_j, j in E_e(n)].
+ *
+ * Conventions shared by every entry point
+ *   Q, K, V, out  bf16, layout [B][H][N][d], contiguous, 16-byte aligned.
+ *   d             must be 64 (MITA_ERR_UNSUPPORTED otherwise).
+ *   grid_h,grid_w both 0: 1-D landmarks over contiguous windows
+ *                 [floor(i N/m), ceil((i+1) N/m)).
+ *                 both > 0: 2-D adaptive pooling of a grid_h x grid_w token
+ *                 grid (row-major, grid_h*grid_w == N) onto a p x p landmark
+ *                 grid, m = p*p (a non-square m is MITA_ERR_UNSUPPORTED);
+ *                 landmark (r,c) pools rows [floor(r gh/p), ceil((r+1) gh/p))
+ *                 and columns [floor(c gw/p), ceil((c+1) gw/p)).
+ *   m, k          1 <= m <= min(N, MITA_MAX_M), 1 <= k <= min(N, MITA_MAX_K).
+ *   expert_idx    int32 [B][H][m][k]: E_i in ascending key order. Ties in s
+ *                 go to the lower key index.
+ *   route         int32 [B][H][N]: e(n) in [0, m). Ties go to the lower
+ *                 landmark index.
+ *   B*H == 0      is an empty problem: nothing is read or written, MITA_OK.
+ *   Ownership     the caller owns every buffer passed in; the library never
+ *                 frees or retains them. The library owns a cached scratch
+ *                 workspace per (device, stream), grown on demand with
+ *                 cudaMalloc and freed by mita_release_workspace().
+ *   Streams       device entry points enqueue all work on `stream` (a
+ *                 cudaStream_t; NULL = the legacy default stream) and return
+ *                 without synchronising, except when the workspace must grow.
+ *                 Calls on different streams use different workspaces.
+ *   Errors        a negative MITA_ERR_* code; mita_last_error() gives the
+ *                 message. Argument errors are found before anything is
+ *                 launched. A fault inside a kernel surfaces, as with any CUDA
+ *                 call, at the caller's next synchronisation; waits inside the
+ *                 kernels are bounded and report MITA_ERR_TIMEOUT through
+ *                 mita_sync_status() instead of hanging.
+ */
+#ifndef MITA_H
+#define MITA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MITA_OK 0
+#define MITA_ERR_INVALID_ARG (-1) /* null/misaligned pointer, bad size or grid */
+#define MITA_ERR_UNSUPPORTED (-2) /* valid for the method, not built here (d != 64, non-square 2-D m, limits) */
+#define MITA_ERR_ALLOC (-3)       /* workspace allocation failed */
+#define MITA_ERR_CUDA (-4)        /* a CUDA runtime call or launch failed */
+#define MITA_ERR_TIMEOUT (-5)     /* a bounded device-side wait gave up */
+
+#define MITA_MAX_M 1024
+#define MITA_MAX_K 1024
+
+/*
+ * The MiTA forward pass, stages 1-4 above, on device buffers.
+ * Q, K, V: device, bf16 [B][H][N][d] (read only). out: device, bf16
+ * [B][H][N][d]. expert_idx: device, int32 [B][H][m][k]. route: device, int32
+ * [B][H][N]. Returns MITA_OK or a MITA_ERR_* code; asynchronous on `stream`.
+ */
+int mita_forward(const void* Q, const void* K, const void* V, int B, int H, int N, int d, int grid_h, int grid_w,
+                 int m, int k, void* out, int32_t* expert_idx, int32_t* route, void* stream);
+
+/*
+ * mita_forward with two optional extra device outputs (either may be NULL):
+ * lq, float32 [B][H][m][d], the landmark queries of stage 1, and lv,
+ * float32 [B][H][m][d], the shared-expert values LV of stage 2.
+ */
+int mita_forward_aux(const void* Q, const void* K, const void* V, int B, int H, int N, int d, int grid_h, int grid_w,
+                     int m, int k, void* out, int32_t* expert_idx, int32_t* route, float* lq, float* lv,
+                     void* stream);
+
+/*
+ * mita_forward on HOST buffers (same shapes and dtypes; bf16 as uint16 bit
+ * patterns). Copies the inputs to the device, runs the forward pass on
+ * `stream`, copies out, expert_idx and route back, and returns after the
+ * stream has finished. Host buffers may be pageable; pinned buffers copy
+ * faster. Device staging buffers are part of the cached workspace.
+ */
+int mita_forward_host(const uint16_t* Q, const uint16_t* K, const uint16_t* V, int B, int H, int N, int d,
+                      int grid_h, int grid_w, int m, int k, uint16_t* out, int32_t* expert_idx, int32_t* route,
+                      void* stream);
+
+/*
+ * Bytes of scratch one mita_forward call of this shape holds in the
+ * workspace (device buffers only; excludes mita_forward_host staging).
+ * Returns 0 for an invalid or empty shape.
+ */
+size_t mita_workspace_bytes(int B, int H, int N, int d, int grid_h, int grid_w, int m, int k);
+
+/*
+ * Waits for `stream`, then reports and clears the device-side status word of
+ * the current device: MITA_OK, MITA_ERR_TIMEOUT when a bounded wait inside a
+ * kernel gave up since the last check, or MITA_ERR_CUDA when the stream
+ * itself failed.
+ */
+int mita_sync_status(void* stream);
+
+/*
+ * Stage timing (off by default). While enabled on a host thread, every
+ * forward call made from that thread records CUDA events on its stream around
+ * each stage: 0 landmark pooling, 1 landmark scan, 2 expert merge/selection,
+ * 3 routing, 4 grouping, 5 expert attention. mita_profile_read() waits for
+ * `stream`, adds the elapsed times of all recorded calls on it to stage_ms
+ * and the number of kernels each stage launched to stage_launches (arrays of
+ * at least max_stages entries, either may be NULL), forgets those records and
+ * returns the number of stages (6), or a MITA_ERR_* code.
+ */
+int mita_profile_enable(int on);
+int mita_profile_read(double* stage_ms, int64_t* stage_launches, int max_stages, void* stream);
+/* Name of stage i, or NULL. */
+const char* mita_stage_name(int i);
+
+/* Message for the last non-zero return on this host thread ("" if none). */
+const char* mita_last_error(void);
+
+/*
+ * Frees every cached workspace of every device. Synchronises each device that
+ * holds one; call it when no mita_* work is in flight.
+ */
+void mita_release_workspace(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MITA_H */

@@ -1,0 +1,98 @@
+// Grouping queries by expert: a counting sort on the routes.
+//
+// The pages process queries grouped by expert so that every query of one
+// routed expert shares the same gathered keys and values
+// ("NeurIPS 2026 | Mixture-of-Top-k 注意力" (shuwu5.cn), end of section
+// "MiTA：用少量地标查询，同时完成压缩与专家构造"; Algorithm 1 caption of
+// "And attention is also FFN? …" (en.roboind.com)).
+//
+//  1. the routing kernel has already counted queries per (head, expert);
+//  2. offsets_kernel (one CTA per head): exclusive scan of the counts gives
+//     each expert's segment of `perm`; it also cuts every segment into work
+//     items of at most `qtile` queries for the attention kernel;
+//  3. scatter_kernel (one CTA per 256 queries): counts its queries per expert
+//     in shared memory, reserves a range of each expert's segment with one
+//     global atomic per (CTA, expert), and writes the query indices there.
+// The order of queries inside a segment depends on CTA timing; it does not
+// affect any result, because every query's attention is computed on its own.
+#include "mita_internal.cuh"
+
+namespace mita {
+
+namespace {
+
+constexpr int GT = 1024;  // threads of the offsets kernel (>= MITA_MAX_M_INTERNAL)
+constexpr int SCT = 256;  // queries per scatter CTA
+
+__global__ void __launch_bounds__(GT) offsets_kernel(int m, int64_t N, int qtile, int64_t max_items,
+                                                     int* __restrict__ counts, int* __restrict__ expoff,
+                                                     int* __restrict__ cursor, int4* __restrict__ items,
+                                                     int* __restrict__ nitems) {
+    __shared__ int sc[GT];
+    __shared__ int st[GT];
+    const int64_t bh = blockIdx.x;
+    const int e = threadIdx.x;
+    const int c = e < m ? counts[bh * m + e] : 0;
+    const int tiles = (c + qtile - 1) / qtile;
+    sc[e] = c;
+    st[e] = tiles;
+    __syncthreads();
+    for (int o = 1; o < GT; o <<= 1) {  // inclusive Hillis-Steele scans
+        const int a = e >= o ? sc[e - o] : 0;
+        const int b = e >= o ? st[e - o] : 0;
+        __syncthreads();
+        sc[e] += a;
+        st[e] += b;
+        __syncthreads();
+    }
+    if (e < m) {
+        const int off = sc[e] - c;
+        expoff[bh * (m + 1) + e] = off;
+        cursor[bh * m + e] = off;
+        counts[bh * m + e] = 0;  // ready for the next call
+        const int ib = st[e] - tiles;
+        for (int t = 0; t < tiles; ++t) {
+            const int start = t * qtile;
+            items[bh * max_items + ib + t] = make_int4(e, off + start, min(qtile, c - start), 0);
+        }
+    }
+    if (e == m - 1) {
+        expoff[bh * (m + 1) + m] = sc[e];
+        nitems[bh] = st[e];
+    }
+}
+
+__global__ void __launch_bounds__(SCT) scatter_kernel(const int32_t* __restrict__ route, int64_t N, int m,
+                                                      int64_t nblocks, int* __restrict__ cursor,
+                                                      int* __restrict__ perm) {
+    __shared__ int sh[MITA_MAX_M_INTERNAL];
+    const int64_t blk = blockIdx.x % nblocks;
+    const int64_t bh = blockIdx.x / nblocks;
+    const int64_t n = blk * SCT + threadIdx.x;
+    const bool valid = n < N;
+    for (int e = threadIdx.x; e < m; e += SCT) sh[e] = 0;
+    __syncthreads();
+    int e = 0, rank = 0;
+    if (valid) {
+        e = route[bh * N + n];
+        rank = atomicAdd(&sh[e], 1);
+    }
+    __syncthreads();
+    for (int x = threadIdx.x; x < m; x += SCT)
+        if (sh[x]) sh[x] = atomicAdd(&cursor[bh * m + x], sh[x]);
+    __syncthreads();
+    if (valid) perm[bh * N + sh[e] + rank] = static_cast<int>(n);
+}
+
+}  // namespace
+
+cudaError_t launch_group(const Plan& p, const Work& w, const int32_t* route, cudaStream_t st) {
+    offsets_kernel<<<static_cast<unsigned>(p.s.BH), GT, 0, st>>>(p.s.m, p.s.N, p.qtile, p.max_items, w.counts,
+                                                                 w.expoff, w.cursor, w.items, w.nitems);
+    const int64_t nblocks = (p.s.N + SCT - 1) / SCT;
+    scatter_kernel<<<static_cast<unsigned>(p.s.BH * nblocks), SCT, 0, st>>>(route, p.s.N, p.s.m, nblocks, w.cursor,
+                                                                            w.perm);
+    return cudaGetLastError();
+}
+
+}  // namespace mita

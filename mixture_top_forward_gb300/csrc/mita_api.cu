@@ -1,0 +1,422 @@
+// C ABI of libmita.so: argument checks, workspace, and the launch sequence
+// of the forward pass (declared and documented in include/mita.h).
+#include <algorithm>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <utility>
+#include <vector>
+
+#include "mita.h"
+#include "mita_internal.cuh"
+
+static_assert(MITA_MAX_M <= MITA_MAX_M_INTERNAL, "routing/grouping tables hold MITA_MAX_M experts");
+static_assert(MITA_MAX_K <= MITA_SORT_MAX, "the expert sort holds MITA_MAX_K indices");
+
+namespace mita {
+
+namespace {
+
+thread_local char g_err[512] = "";
+
+int fail(int code, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof g_err, fmt, ap);
+    va_end(ap);
+    return code;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+    return fail(MITA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+int isqrt_exact(int m) {
+    int p = 0;
+    while ((p + 1) * (p + 1) <= m) ++p;
+    return p * p == m ? p : -1;
+}
+
+// Validates the arguments common to every entry point and fills `s`.
+// Returns MITA_OK, or an error code with the message set.
+int check_shape(int B, int H, int N, int d, int gh, int gw, int m, int k, Shape* s, bool* empty) {
+    *empty = false;
+    if (B < 0 || H < 0) return fail(MITA_ERR_INVALID_ARG, "B=%d, H=%d must be >= 0", B, H);
+    if (static_cast<int64_t>(B) * H == 0) {
+        *empty = true;
+        return MITA_OK;
+    }
+    if (N < 1) return fail(MITA_ERR_INVALID_ARG, "N=%d must be >= 1", N);
+    if (d != D) return fail(MITA_ERR_UNSUPPORTED, "d=%d: only d=64 is built", d);
+    if (m < 1 || m > N) return fail(MITA_ERR_INVALID_ARG, "m=%d must be in [1, N=%d]", m, N);
+    if (k < 1 || k > N) return fail(MITA_ERR_INVALID_ARG, "k=%d must be in [1, N=%d]", k, N);
+    if (m > MITA_MAX_M) return fail(MITA_ERR_UNSUPPORTED, "m=%d exceeds MITA_MAX_M=%d", m, MITA_MAX_M);
+    if (k > MITA_MAX_K) return fail(MITA_ERR_UNSUPPORTED, "k=%d exceeds MITA_MAX_K=%d", k, MITA_MAX_K);
+    int p = 0;
+    if (gh != 0 || gw != 0) {
+        if (gh < 1 || gw < 1 || static_cast<int64_t>(gh) * gw != N)
+            return fail(MITA_ERR_INVALID_ARG, "grid %dx%d does not tile N=%d", gh, gw, N);
+        p = isqrt_exact(m);
+        if (p < 0) return fail(MITA_ERR_UNSUPPORTED, "2-D pooling needs a square m, got m=%d", m);
+        if (p > gh || p > gw) return fail(MITA_ERR_INVALID_ARG, "landmark grid %dx%d exceeds the token grid", p, p);
+    }
+    const int64_t BH = static_cast<int64_t>(B) * H;
+    if (BH * N > (static_cast<int64_t>(1) << 40))
+        return fail(MITA_ERR_UNSUPPORTED, "B*H*N=%lld is too large", static_cast<long long>(BH * N));
+    *s = Shape{BH, N, gh, gw, p, m, k};
+    return MITA_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// ---------------------------------------------------------------------------
+// Workspace cache, one buffer per (device, stream, purpose).
+// ---------------------------------------------------------------------------
+struct Slot {
+    void* ptr = nullptr;
+    size_t bytes = 0;
+};
+std::mutex g_ws_mu;
+std::map<std::pair<int, std::pair<uintptr_t, int>>, Slot> g_ws;
+
+int workspace(cudaStream_t st, int purpose, size_t bytes, void** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    std::lock_guard<std::mutex> lk(g_ws_mu);
+    Slot& s = g_ws[{dev, {reinterpret_cast<uintptr_t>(st), purpose}}];
+    if (s.bytes < bytes) {
+        if (s.ptr) {
+            e = cudaStreamSynchronize(st);
+            if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+            cudaFree(s.ptr);
+            s.ptr = nullptr;
+            s.bytes = 0;
+        }
+        const size_t want = bytes + bytes / 8;  // some headroom for growth
+        e = cudaMalloc(&s.ptr, want);
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            s.ptr = nullptr;
+            return fail(MITA_ERR_ALLOC, "cudaMalloc(%zu) for the workspace: %s", want, cudaGetErrorString(e));
+        }
+        s.bytes = want;
+        e = cudaMemsetAsync(s.ptr, 0, want, st);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
+    }
+    *out = s.ptr;
+    return MITA_OK;
+}
+
+}  // namespace
+
+bool make_plan(const Shape& s, Plan* p) {
+    Plan P{};
+    P.s = s;
+    // scan: 32 landmarks per CTA; enough key chunks for ~8 CTAs per SM, at
+    // least 1024 keys per chunk
+    P.ltile = 32;
+    const int64_t ltiles = (s.m + P.ltile - 1) / P.ltile;
+    const int64_t target = 152 * 8;
+    int64_t chunks = (target + s.BH * ltiles - 1) / (s.BH * ltiles);
+    chunks = std::max<int64_t>(1, std::min<int64_t>(chunks, s.N / 1024));
+    P.chunk_len = (s.N + chunks - 1) / chunks;
+    P.chunks = static_cast<int>((s.N + P.chunk_len - 1) / P.chunk_len);
+    const int64_t room = ((P.chunk_len + 31) / 32) * 32 + 32;  // a chunk never needs more
+    int64_t cap = ((2 * static_cast<int64_t>(s.k) + 64 + 31) / 32) * 32;
+    cap = std::min(cap, room);
+    cap = std::max<int64_t>(cap, s.k + 32);
+    P.cap = static_cast<int>(cap);
+    P.rblock = 256;
+    P.nrblocks = (s.N + P.rblock - 1) / P.rblock;
+    P.qtile = 128;
+    P.max_items = (s.N + P.qtile - 1) / P.qtile + s.m;
+
+    const size_t BH = static_cast<size_t>(s.BH), m = static_cast<size_t>(s.m);
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const size_t o = off;
+        off += align256(bytes);
+        return o;
+    };
+    P.off_status = take(sizeof(int));
+    P.off_lq32 = take(BH * m * D * sizeof(float));
+    P.off_lqhi = take(BH * m * D * 2);
+    P.off_lqlo = take(BH * m * D * 2);
+    P.off_lv32 = take(BH * m * D * sizeof(float));
+    P.off_lvbf = take(BH * m * D * 2);
+    P.off_part = take(BH * P.chunks * m * 68 * sizeof(float));
+    P.off_cand = take(BH * P.chunks * m * static_cast<size_t>(P.cap) * sizeof(uint64_t));
+    P.off_ccount = take(BH * P.chunks * m * sizeof(int));
+    P.off_counts = take(BH * m * sizeof(int));
+    P.off_expoff = take(BH * (m + 1) * sizeof(int));
+    P.off_cursor = take(BH * m * sizeof(int));
+    P.off_perm = take(BH * static_cast<size_t>(s.N) * sizeof(int));
+    P.off_items = take(BH * static_cast<size_t>(P.max_items) * sizeof(int4));
+    P.off_nitems = take(BH * sizeof(int));
+    P.total = off;
+    if (P.max_items * s.BH > 0x7FFFFFFFLL || s.BH * P.nrblocks > 0x7FFFFFFFLL) return false;
+    *p = P;
+    return true;
+}
+
+Work carve(const Plan& p, void* base) {
+    char* b = static_cast<char*>(base);
+    Work w;
+    w.status = reinterpret_cast<int*>(b + p.off_status);
+    w.lq32 = reinterpret_cast<float*>(b + p.off_lq32);
+    w.lqhi = reinterpret_cast<__nv_bfloat16*>(b + p.off_lqhi);
+    w.lqlo = reinterpret_cast<__nv_bfloat16*>(b + p.off_lqlo);
+    w.lv32 = reinterpret_cast<float*>(b + p.off_lv32);
+    w.lvbf = reinterpret_cast<__nv_bfloat16*>(b + p.off_lvbf);
+    w.part = reinterpret_cast<float*>(b + p.off_part);
+    w.cand = reinterpret_cast<uint64_t*>(b + p.off_cand);
+    w.ccount = reinterpret_cast<int*>(b + p.off_ccount);
+    w.counts = reinterpret_cast<int*>(b + p.off_counts);
+    w.expoff = reinterpret_cast<int*>(b + p.off_expoff);
+    w.cursor = reinterpret_cast<int*>(b + p.off_cursor);
+    w.perm = reinterpret_cast<int*>(b + p.off_perm);
+    w.items = reinterpret_cast<int4*>(b + p.off_items);
+    w.nitems = reinterpret_cast<int*>(b + p.off_nitems);
+    return w;
+}
+
+namespace {
+
+// ---------------------------------------------------------------------------
+// Stage timing: per host thread, events recorded between stages.
+// ---------------------------------------------------------------------------
+constexpr int kStages = 6;
+const char* const kStageNames[kStages] = {"pool", "scan", "select", "route", "group", "expert"};
+const int kStageLaunches[kStages] = {1, 1, 1, 1, 2, 1};
+
+struct Recorded {
+    cudaStream_t stream;
+    cudaEvent_t ev[kStages + 1];
+};
+thread_local bool t_profile = false;
+thread_local std::vector<Recorded> t_records;
+
+struct StageMarks {
+    Recorded rec{};
+    bool on = false;
+    explicit StageMarks(cudaStream_t st) {
+        if (!t_profile) return;
+        rec.stream = st;
+        for (auto& e : rec.ev)
+            if (cudaEventCreate(&e) != cudaSuccess) return;
+        on = true;
+    }
+    void mark(int i) {
+        if (on) cudaEventRecord(rec.ev[i], rec.stream);
+    }
+    void commit() {
+        if (on) t_records.push_back(rec);
+        on = false;
+    }
+    ~StageMarks() {
+        if (on)
+            for (auto& e : rec.ev) cudaEventDestroy(e);
+    }
+};
+
+// The four stages on a prepared workspace.
+int run_forward(const Plan& P, const Work& W, const __nv_bfloat16* Q, const __nv_bfloat16* K,
+                const __nv_bfloat16* V, __nv_bfloat16* out, int32_t* expert_idx, int32_t* route, float* lq_out,
+                float* lv_out, cudaStream_t st) {
+    cudaError_t e;
+    const size_t mrows = static_cast<size_t>(P.s.BH) * P.s.m;
+    if ((e = cudaMemsetAsync(W.counts, 0, mrows * sizeof(int), st)) != cudaSuccess)
+        return cuda_fail(e, "cudaMemsetAsync");
+    StageMarks marks(st);
+    marks.mark(0);
+    if ((e = launch_pool(P, W, Q, st)) != cudaSuccess) return cuda_fail(e, "landmark pooling launch");
+    marks.mark(1);
+    if ((e = launch_scan(P, W, K, V, st)) != cudaSuccess) return cuda_fail(e, "landmark scan launch");
+    marks.mark(2);
+    if ((e = launch_select(P, W, expert_idx, st)) != cudaSuccess) return cuda_fail(e, "expert selection launch");
+    marks.mark(3);
+    if ((e = launch_route(P, W, Q, route, st)) != cudaSuccess) return cuda_fail(e, "routing launch");
+    marks.mark(4);
+    if ((e = launch_group(P, W, route, st)) != cudaSuccess) return cuda_fail(e, "grouping launch");
+    marks.mark(5);
+    if ((e = launch_expert(P, W, Q, K, V, expert_idx, out, st)) != cudaSuccess)
+        return cuda_fail(e, "expert attention launch");
+    marks.mark(6);
+    marks.commit();
+    if (lq_out && (e = cudaMemcpyAsync(lq_out, W.lq32, mrows * D * sizeof(float), cudaMemcpyDeviceToDevice, st)) !=
+                      cudaSuccess)
+        return cuda_fail(e, "copy of Lq");
+    if (lv_out && (e = cudaMemcpyAsync(lv_out, W.lv32, mrows * D * sizeof(float), cudaMemcpyDeviceToDevice, st)) !=
+                      cudaSuccess)
+        return cuda_fail(e, "copy of LV");
+    return MITA_OK;
+}
+
+}  // namespace
+}  // namespace mita
+
+using namespace mita;
+
+extern "C" int mita_forward_aux(const void* Q, const void* K, const void* V, int B, int H, int N, int d, int grid_h,
+                                int grid_w, int m, int k, void* out, int32_t* expert_idx, int32_t* route, float* lq,
+                                float* lv, void* stream) {
+    g_err[0] = 0;
+    Shape s;
+    bool empty;
+    int rc = check_shape(B, H, N, d, grid_h, grid_w, m, k, &s, &empty);
+    if (rc != MITA_OK || empty) return rc;
+    if (!Q || !K || !V || !out || !expert_idx || !route)
+        return fail(MITA_ERR_INVALID_ARG, "a required pointer is NULL");
+    if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(out))
+        return fail(MITA_ERR_INVALID_ARG, "Q, K, V and out must be 16-byte aligned");
+    Plan P;
+    if (!make_plan(s, &P)) return fail(MITA_ERR_UNSUPPORTED, "problem too large for the launch grids");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    void* base = nullptr;
+    if ((rc = workspace(st, 0, P.total, &base)) != MITA_OK) return rc;
+    Work W = carve(P, base);
+    return run_forward(P, W, static_cast<const __nv_bfloat16*>(Q), static_cast<const __nv_bfloat16*>(K),
+                       static_cast<const __nv_bfloat16*>(V), static_cast<__nv_bfloat16*>(out), expert_idx, route, lq,
+                       lv, st);
+}
+
+extern "C" int mita_forward(const void* Q, const void* K, const void* V, int B, int H, int N, int d, int grid_h,
+                            int grid_w, int m, int k, void* out, int32_t* expert_idx, int32_t* route, void* stream) {
+    return mita_forward_aux(Q, K, V, B, H, N, d, grid_h, grid_w, m, k, out, expert_idx, route, nullptr, nullptr,
+                            stream);
+}
+
+extern "C" int mita_forward_host(const uint16_t* Q, const uint16_t* K, const uint16_t* V, int B, int H, int N, int d,
+                                 int grid_h, int grid_w, int m, int k, uint16_t* out, int32_t* expert_idx,
+                                 int32_t* route, void* stream) {
+    g_err[0] = 0;
+    Shape s;
+    bool empty;
+    int rc = check_shape(B, H, N, d, grid_h, grid_w, m, k, &s, &empty);
+    if (rc != MITA_OK || empty) return rc;
+    if (!Q || !K || !V || !out || !expert_idx || !route)
+        return fail(MITA_ERR_INVALID_ARG, "a required pointer is NULL");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const size_t tok = static_cast<size_t>(s.BH) * s.N * D * 2;
+    const size_t eb = static_cast<size_t>(s.BH) * s.m * s.k * sizeof(int32_t);
+    const size_t rb = static_cast<size_t>(s.BH) * s.N * sizeof(int32_t);
+    size_t off = 0;
+    const size_t oq = off; off += align256(tok);
+    const size_t ok_ = off; off += align256(tok);
+    const size_t ov = off; off += align256(tok);
+    const size_t oo = off; off += align256(tok);
+    const size_t oe = off; off += align256(eb);
+    const size_t orr = off; off += align256(rb);
+    void* stage = nullptr;
+    if ((rc = workspace(st, 1, off, &stage)) != MITA_OK) return rc;
+    char* sb = static_cast<char*>(stage);
+    cudaError_t e;
+    if ((e = cudaMemcpyAsync(sb + oq, Q, tok, cudaMemcpyHostToDevice, st)) != cudaSuccess ||
+        (e = cudaMemcpyAsync(sb + ok_, K, tok, cudaMemcpyHostToDevice, st)) != cudaSuccess ||
+        (e = cudaMemcpyAsync(sb + ov, V, tok, cudaMemcpyHostToDevice, st)) != cudaSuccess)
+        return cuda_fail(e, "host-to-device copy");
+    rc = mita_forward_aux(sb + oq, sb + ok_, sb + ov, B, H, N, d, grid_h, grid_w, m, k, sb + oo,
+                          reinterpret_cast<int32_t*>(sb + oe), reinterpret_cast<int32_t*>(sb + orr), nullptr, nullptr,
+                          stream);
+    if (rc != MITA_OK) return rc;
+    if ((e = cudaMemcpyAsync(out, sb + oo, tok, cudaMemcpyDeviceToHost, st)) != cudaSuccess ||
+        (e = cudaMemcpyAsync(expert_idx, sb + oe, eb, cudaMemcpyDeviceToHost, st)) != cudaSuccess ||
+        (e = cudaMemcpyAsync(route, sb + orr, rb, cudaMemcpyDeviceToHost, st)) != cudaSuccess)
+        return cuda_fail(e, "device-to-host copy");
+    if ((e = cudaStreamSynchronize(st)) != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+    return MITA_OK;
+}
+
+extern "C" size_t mita_workspace_bytes(int B, int H, int N, int d, int grid_h, int grid_w, int m, int k) {
+    Shape s;
+    bool empty;
+    char saved[sizeof g_err];
+    memcpy(saved, g_err, sizeof g_err);
+    const int rc = check_shape(B, H, N, d, grid_h, grid_w, m, k, &s, &empty);
+    memcpy(g_err, saved, sizeof g_err);
+    if (rc != MITA_OK || empty) return 0;
+    Plan P;
+    if (!make_plan(s, &P)) return 0;
+    return P.total;
+}
+
+extern "C" int mita_sync_status(void* stream) {
+    g_err[0] = 0;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+    int dev = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    int status = MITA_OK;
+    std::lock_guard<std::mutex> lk(g_ws_mu);
+    for (auto& kv : g_ws) {
+        if (kv.first.first != dev || kv.first.second.second != 0 || !kv.second.ptr) continue;
+        if (reinterpret_cast<cudaStream_t>(kv.first.second.first) != st) continue;
+        int word = 0;
+        if ((e = cudaMemcpy(&word, kv.second.ptr, sizeof(int), cudaMemcpyDeviceToHost)) != cudaSuccess)
+            return cuda_fail(e, "status read");
+        if (word != 0) {
+            status = word;
+            const int zero = 0;
+            cudaMemcpy(kv.second.ptr, &zero, sizeof(int), cudaMemcpyHostToDevice);
+        }
+    }
+    if (status != MITA_OK) return fail(status, "a bounded device-side wait gave up (status %d)", status);
+    return MITA_OK;
+}
+
+extern "C" int mita_profile_enable(int on) {
+    t_profile = on != 0;
+    return MITA_OK;
+}
+
+extern "C" int mita_profile_read(double* stage_ms, int64_t* stage_launches, int max_stages, void* stream) {
+    g_err[0] = 0;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+    const int n = std::min(max_stages, kStages);
+    std::vector<Recorded> keep;
+    int rc = MITA_OK;
+    for (auto& r : t_records) {
+        if (r.stream != st) {
+            keep.push_back(r);
+            continue;
+        }
+        for (int i = 0; i < n; ++i) {
+            float ms = 0.f;
+            if (rc == MITA_OK && (e = cudaEventElapsedTime(&ms, r.ev[i], r.ev[i + 1])) != cudaSuccess)
+                rc = cuda_fail(e, "cudaEventElapsedTime");
+            if (stage_ms) stage_ms[i] += ms;
+            if (stage_launches) stage_launches[i] += kStageLaunches[i];
+        }
+        for (auto& ev : r.ev) cudaEventDestroy(ev);
+    }
+    t_records.swap(keep);
+    return rc == MITA_OK ? kStages : rc;
+}
+
+extern "C" const char* mita_stage_name(int i) { return (i >= 0 && i < kStages) ? kStageNames[i] : nullptr; }
+
+extern "C" const char* mita_last_error(void) { return g_err; }
+
+extern "C" void mita_release_workspace(void) {
+    std::lock_guard<std::mutex> lk(g_ws_mu);
+    int cur = 0;
+    cudaGetDevice(&cur);
+    for (auto& kv : g_ws) {
+        if (!kv.second.ptr) continue;
+        cudaSetDevice(kv.first.first);
+        cudaDeviceSynchronize();
+        cudaFree(kv.second.ptr);
+        kv.second.ptr = nullptr;
+        kv.second.bytes = 0;
+    }
+    g_ws.clear();
+    cudaSetDevice(cur);
+}

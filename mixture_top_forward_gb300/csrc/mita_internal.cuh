@@ -1,0 +1,129 @@
+// Internal declarations shared by the kernels of libmita.so.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+// Largest m and k the kernels' shared-memory tables hold (the public limits
+// MITA_MAX_M / MITA_MAX_K in mita.h must not exceed these).
+#define MITA_MAX_M_INTERNAL 1024
+#define MITA_SORT_MAX 1024
+
+namespace mita {
+
+constexpr int D = 64;  // head dimension the kernels are built for
+
+// ----------------------------------------------------------------------------
+// Problem shape and the workspace plan of one call.
+// ----------------------------------------------------------------------------
+struct Shape {
+    int64_t BH;     // B*H heads
+    int64_t N;      // tokens per head
+    int gh, gw;     // token grid (0,0 = 1-D)
+    int p;          // landmark grid side for 2-D (m = p*p), 0 for 1-D
+    int m, k;       // landmarks, keys per routed expert
+};
+
+struct Plan {
+    Shape s;
+    // landmark scan
+    int ltile;          // landmarks per scan CTA
+    int chunks;         // key chunks per head
+    int64_t chunk_len;  // keys per chunk (last one may be shorter)
+    int cap;            // candidate slots per (head, chunk, landmark)
+    // routing / grouping
+    int rblock;         // queries per routing CTA
+    int64_t nrblocks;   // routing CTAs per head
+    // expert attention
+    int qtile;          // queries per expert work item
+    int64_t max_items;  // work items per head, upper bound
+    // workspace layout (byte offsets)
+    size_t off_status, off_lq32, off_lqhi, off_lqlo, off_lv32, off_lvbf, off_part, off_cand, off_ccount,
+        off_counts, off_expoff, off_cursor, off_perm, off_items, off_nitems, total;
+};
+
+// Builds the plan; returns false if a size does not fit the int ranges used.
+bool make_plan(const Shape& s, Plan* p);
+
+// Workspace pointers derived from a plan.
+struct Work {
+    int* status;            // device status word (MITA_ERR_TIMEOUT etc.)
+    float* lq32;            // [BH][m][64]
+    __nv_bfloat16* lqhi;    // [BH][m][64]  bf16(Lq)
+    __nv_bfloat16* lqlo;    // [BH][m][64]  bf16(Lq - bf16(Lq))
+    float* lv32;            // [BH][m][64]
+    __nv_bfloat16* lvbf;    // [BH][m][64]
+    float* part;            // [BH][chunks][m][68]: max, sum, -, -, o[64]
+    uint64_t* cand;         // [BH][chunks][m][cap] composite top-k keys
+    int* ccount;            // [BH][chunks][m]
+    int* counts;            // [BH][m] queries routed to each expert
+    int* expoff;            // [BH][m+1] exclusive prefix of counts
+    int* cursor;            // [BH][m] scatter cursors
+    int* perm;              // [BH][N] queries grouped by expert
+    int4* items;            // [BH][max_items] (expert, start, len, -)
+    int* nitems;            // [BH]
+};
+
+Work carve(const Plan& p, void* base);
+
+// ----------------------------------------------------------------------------
+// Device helpers.
+// ----------------------------------------------------------------------------
+// Top-k order key: larger score first, then lower key index. The float is
+// mapped to an order-preserving unsigned integer (-0 folded onto +0), the
+// index is stored inverted so that a lower index compares larger.
+__device__ __forceinline__ uint64_t topk_key(float s, uint32_t j) {
+    uint32_t u = __float_as_uint(s);
+    if ((u << 1) == 0) u = 0;  // -0 -> +0
+    u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+    return (static_cast<uint64_t>(u) << 32) | static_cast<uint64_t>(0xFFFFFFFFu - j);
+}
+__device__ __forceinline__ uint32_t topk_key_index(uint64_t key) {
+    return 0xFFFFFFFFu - static_cast<uint32_t>(key & 0xFFFFFFFFu);
+}
+
+__device__ __forceinline__ void unpack_bf16x8(const uint4& raw, float* f) {
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw);
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+        float2 x = __bfloat1622float2(h[t]);
+        f[2 * t] = x.x;
+        f[2 * t + 1] = x.y;
+    }
+}
+
+__device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
+    uint4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
+}
+
+__device__ __forceinline__ float warp_max(float x) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+    return x;
+}
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    return x;
+}
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+// ----------------------------------------------------------------------------
+// Launchers (each returns cudaGetLastError() of its launches).
+// ----------------------------------------------------------------------------
+cudaError_t launch_pool(const Plan& p, const Work& w, const __nv_bfloat16* Q, cudaStream_t st);
+cudaError_t launch_scan(const Plan& p, const Work& w, const __nv_bfloat16* K, const __nv_bfloat16* V,
+                        cudaStream_t st);
+cudaError_t launch_select(const Plan& p, const Work& w, int32_t* expert_idx, cudaStream_t st);
+cudaError_t launch_route(const Plan& p, const Work& w, const __nv_bfloat16* Q, int32_t* route, cudaStream_t st);
+cudaError_t launch_group(const Plan& p, const Work& w, const int32_t* route, cudaStream_t st);
+cudaError_t launch_expert(const Plan& p, const Work& w, const __nv_bfloat16* Q, const __nv_bfloat16* K,
+                          const __nv_bfloat16* V, const int32_t* expert_idx, __nv_bfloat16* out, cudaStream_t st);
+
+}  // namespace mita

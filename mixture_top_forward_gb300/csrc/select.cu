@@ -1,0 +1,161 @@
+// Stage 2, merge: per (head, landmark), combine the scan's per-chunk results.
+//
+//  * shared-expert value: the chunks' softmax partials (max_c, sum_c, o_c)
+//    are merged by rescaling to the common maximum (log-sum-exp merge), giving
+//    LV_i = softmax(s_i) V over all N keys;
+//  * routed expert: the k largest top-k keys over all chunks' candidate
+//    buffers, found by radix select on the 64-bit keys (8 bits per pass,
+//    256-bin shared-memory histogram), then written as key indices in
+//    ascending order (bitonic sort in shared memory).
+// Each chunk's buffer holds at least min(chunk length, k) of its best keys,
+// so the union always contains the global top k.
+#include "mita_internal.cuh"
+
+namespace mita {
+
+namespace {
+
+constexpr int ST = 256;  // threads per CTA
+
+__global__ void __launch_bounds__(ST) select_kernel(int m, int k, int chunks, int cap,
+                                                    const float* __restrict__ part,
+                                                    const uint64_t* __restrict__ cand,
+                                                    const int* __restrict__ ccount, float* __restrict__ lv32,
+                                                    __nv_bfloat16* __restrict__ lvbf,
+                                                    int32_t* __restrict__ expert_idx) {
+    __shared__ unsigned hist[256];
+    __shared__ int cnts[64];
+    __shared__ int sel[MITA_SORT_MAX];
+    __shared__ int nsel;
+    __shared__ int s_digit;
+    __shared__ unsigned s_above;
+
+    const int i = static_cast<int>(blockIdx.x % static_cast<unsigned>(m));
+    const int64_t bh = blockIdx.x / static_cast<unsigned>(m);
+    const int tid = threadIdx.x;
+
+    // ---- shared-expert value ------------------------------------------------
+    if (tid < D) {
+        float M = -INFINITY;
+        for (int c = 0; c < chunks; ++c) M = fmaxf(M, part[((bh * chunks + c) * m + i) * 68]);
+        float L = 0.f, O = 0.f;
+        for (int c = 0; c < chunks; ++c) {
+            const float* pp = part + ((bh * chunks + c) * m + i) * 68;
+            const float f = exp2f((pp[0] - M) * kLog2e);
+            L += pp[1] * f;
+            O += pp[4 + tid] * f;
+        }
+        const float v = O / L;
+        lv32[(bh * m + i) * D + tid] = v;
+        lvbf[(bh * m + i) * D + tid] = __float2bfloat16_rn(v);
+    }
+
+    // ---- routed expert: k largest keys over all chunk buffers ---------------
+    // chunk counts (chunks may exceed 64: then they are re-read from global)
+    int total = 0;
+    for (int c = 0; c < chunks; ++c) {
+        const int n = ccount[(bh * chunks + c) * m + i];
+        if (c < 64 && tid == 0) cnts[c] = n;
+        total += n;
+    }
+    __syncthreads();
+    auto count_of = [&](int c) { return c < 64 ? cnts[c] : ccount[(bh * chunks + c) * m + i]; };
+    auto buf_of = [&](int c) { return cand + ((bh * chunks + c) * m + i) * static_cast<int64_t>(cap); };
+
+    uint64_t kth = 0;  // keep every key >= kth
+    if (total > k) {
+        uint64_t prefix = 0, mask = 0;
+        unsigned remaining = static_cast<unsigned>(k);
+        for (int shift = 56; shift >= 0; shift -= 8) {
+            hist[tid] = 0;
+            __syncthreads();
+            for (int c = 0; c < chunks; ++c) {
+                const uint64_t* b = buf_of(c);
+                const int n = count_of(c);
+                for (int e = tid; e < n; e += ST) {
+                    const uint64_t x = b[e];
+                    if ((x & mask) == prefix) atomicAdd(&hist[(x >> shift) & 255u], 1u);
+                }
+            }
+            __syncthreads();
+            if (tid < 32) {  // warp 0 finds the digit holding the k-th largest
+                const int lane = tid;
+                unsigned cc[8], tot = 0;
+#pragma unroll
+                for (int t = 0; t < 8; ++t) {
+                    cc[t] = hist[255 - 8 * lane - t];
+                    tot += cc[t];
+                }
+                unsigned incl = tot;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const unsigned y = __shfl_up_sync(0xffffffffu, incl, o);
+                    if (lane >= o) incl += y;
+                }
+                const unsigned excl = incl - tot;
+                if (excl < remaining && remaining <= incl) {
+                    unsigned run = excl;
+                    for (int t = 0; t < 8; ++t) {
+                        if (run + cc[t] >= remaining) {
+                            s_digit = 255 - 8 * lane - t;
+                            s_above = run;
+                            break;
+                        }
+                        run += cc[t];
+                    }
+                }
+            }
+            __syncthreads();
+            remaining -= s_above;
+            prefix |= static_cast<uint64_t>(s_digit) << shift;
+            mask |= 0xFFull << shift;
+            __syncthreads();
+        }
+        kth = prefix;
+    }
+
+    // ---- gather the selected indices and sort them ascending ----------------
+    if (tid == 0) nsel = 0;
+    __syncthreads();
+    for (int c = 0; c < chunks; ++c) {
+        const uint64_t* b = buf_of(c);
+        const int n = count_of(c);
+        for (int e = tid; e < n; e += ST) {
+            const uint64_t x = b[e];
+            if (x >= kth) sel[atomicAdd(&nsel, 1)] = static_cast<int>(topk_key_index(x));
+        }
+    }
+    __syncthreads();
+    int n2 = 1;
+    while (n2 < k) n2 <<= 1;
+    for (int t = k + tid; t < n2; t += ST) sel[t] = 0x7FFFFFFF;
+    __syncthreads();
+    for (int size = 2; size <= n2; size <<= 1) {
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            for (int t = tid; t < n2 / 2; t += ST) {
+                const int lo = 2 * t - (t & (stride - 1));
+                const int hi = lo + stride;
+                const bool up = (lo & size) == 0;
+                const int a = sel[lo], b = sel[hi];
+                if ((a > b) == up) {
+                    sel[lo] = b;
+                    sel[hi] = a;
+                }
+            }
+            __syncthreads();
+        }
+    }
+    int32_t* dst = expert_idx + (bh * m + i) * static_cast<int64_t>(k);
+    for (int t = tid; t < k; t += ST) dst[t] = sel[t];
+}
+
+}  // namespace
+
+cudaError_t launch_select(const Plan& p, const Work& w, int32_t* expert_idx, cudaStream_t st) {
+    const unsigned grid = static_cast<unsigned>(p.s.BH * p.s.m);
+    select_kernel<<<grid, ST, 0, st>>>(p.s.m, p.s.k, p.chunks, p.cap, w.part, w.cand, w.ccount, w.lv32, w.lvbf,
+                                      expert_idx);
+    return cudaGetLastError();
+}
+
+}  // namespace mita

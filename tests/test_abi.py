@@ -1,0 +1,69 @@
+"""The C-ABI library on the host: it loads, exports every function the header
+declares, and rejects bad arguments before touching a device."""
+import ctypes
+
+import pytest
+
+import mixture_top_forward_gb300 as M
+
+FAKE = 0x100000  # 16-byte aligned, never dereferenced: validation fails first
+
+
+@pytest.fixture(scope="module")
+def lib():
+    M.build()
+    return M.load()
+
+
+def test_exports_every_declared_function(lib):
+    names = M.declared_functions()
+    assert {"mita_forward", "mita_forward_aux", "mita_forward_host", "mita_last_error",
+            "mita_release_workspace"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def _fwd(lib, B=1, H=1, N=196, d=64, gh=14, gw=14, m=25, k=25, q=FAKE, kp=FAKE, v=FAKE, out=FAKE, e=FAKE, r=FAKE):
+    return lib.mita_forward(q, kp, v, B, H, N, d, gh, gw, m, k, out, e, r, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(d=65), M.MITA_ERR_UNSUPPORTED),
+    (dict(d=128), M.MITA_ERR_UNSUPPORTED),
+    (dict(m=0), M.MITA_ERR_INVALID_ARG),
+    (dict(m=197), M.MITA_ERR_INVALID_ARG),
+    (dict(k=0), M.MITA_ERR_INVALID_ARG),
+    (dict(k=197), M.MITA_ERR_INVALID_ARG),
+    (dict(m=24), M.MITA_ERR_UNSUPPORTED),            # non-square m with a 2-D grid
+    (dict(gh=14, gw=13), M.MITA_ERR_INVALID_ARG),     # grid does not tile N
+    (dict(gh=0, gw=14), M.MITA_ERR_INVALID_ARG),
+    (dict(N=0), M.MITA_ERR_INVALID_ARG),
+    (dict(B=-1), M.MITA_ERR_INVALID_ARG),
+    (dict(N=4096, gh=0, gw=0, m=1025), M.MITA_ERR_UNSUPPORTED),
+    (dict(N=4096, gh=0, gw=0, k=1025), M.MITA_ERR_UNSUPPORTED),
+    (dict(q=0), M.MITA_ERR_INVALID_ARG),
+    (dict(out=0), M.MITA_ERR_INVALID_ARG),
+    (dict(q=FAKE + 8), M.MITA_ERR_INVALID_ARG),      # misaligned
+])
+def test_rejects_bad_arguments(lib, kw, code):
+    assert _fwd(lib, **kw) == code
+    assert M.mita_last_error() != ""
+
+
+def test_empty_problem_is_a_no_op(lib):
+    assert _fwd(lib, B=0) == M.MITA_OK
+    assert _fwd(lib, H=0, q=0, out=0) == M.MITA_OK
+
+
+def test_workspace_bytes(lib):
+    assert M.mita_workspace_bytes(1, 1, 196, 64, 14, 14, 25, 25) > 0
+    assert M.mita_workspace_bytes(1, 1, 196, 65, 14, 14, 25, 25) == 0
+    small = M.mita_workspace_bytes(1, 8, 65536, 64, 0, 0, 256, 256)
+    big = M.mita_workspace_bytes(1, 8, 1 << 20, 64, 0, 0, 256, 256)
+    assert 0 < small < big < 2 << 30
+
+
+def test_stage_names(lib):
+    names = [M.mita_stage_name(i) for i in range(6)]
+    assert names == ["pool", "scan", "select", "route", "group", "expert"]
+    assert M.mita_stage_name(6) is None

@@ -1,0 +1,138 @@
+"""Parity of the CUDA path with the fp64 oracle (acceptance rule in parity.py).
+
+Small configs and edge cases are compared element by element with the full
+oracle; the large configs run in exactly the launch configuration bench.py
+times (mita_forward on the whole problem) and are checked on a few heads:
+every landmark's expert set and shared-expert value, and routes and outputs of
+sampled queries."""
+import numpy as np
+import pytest
+
+import parity
+import synth
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    import torch
+
+    import mixture_top_forward_gb300 as M
+
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    M.load(build_if_missing=False)
+
+
+def _cfg_args(name):
+    c = synth.CONFIGS[name]
+    return c["grid_h"], c["grid_w"], c["m"], c["k"]
+
+
+@pytest.mark.parametrize("name", ["tiny", "deit", "seg1024", "seg1600"])
+def test_config_full_oracle(orc, name):
+    q, k, v = synth.make_inputs(name)
+    rep = parity.full_parity(orc, q, k, v, *_cfg_args(name))
+    print(name, rep)
+
+
+@pytest.mark.parametrize("name,heads,nq", [
+    ("lra", (0, 131, 255), 4096),
+    ("long64k", (0, 7), 8192),
+    ("long256k", (0, 5), 8192),
+    ("long1m", (3,), 8192),
+])
+def test_config_sampled(orc, name, heads, nq):
+    q, k, v = synth.make_inputs(name)
+    gpu = parity.run_gpu(q, k, v, *_cfg_args(name), full_out=False)
+    rep = parity.sampled_parity(orc, q, k, v, *_cfg_args(name), gpu, heads, nq)
+    print(name, rep)
+
+
+def _rand(B, H, N, seed, scale=1.0):
+    return [synth.normal_bf16((B, H, N, 64), seed, t, scale) for t in range(3)]
+
+
+@pytest.mark.parametrize("B,H,N,gh,gw,m,k", [
+    (2, 3, 1000, 0, 0, 7, 13),      # ragged windows and tiles
+    (1, 2, 196, 14, 14, 25, 196),   # k = N: every key in every expert
+    (1, 2, 196, 14, 14, 196, 3),    # m = N: one token per window
+    (2, 2, 300, 0, 0, 1, 5),        # m = 1: one landmark, every route 0
+    (1, 3, 777, 0, 0, 33, 1),       # k = 1
+    (1, 1, 1, 0, 0, 1, 1),          # a single token
+    (1, 2, 5000, 0, 0, 300, 700),   # several landmark tiles, k > 512
+    (3, 1, 2500, 50, 50, 16, 1024), # 2-D 4x4 landmarks, k = MITA_MAX_K
+])
+def test_edge_shapes(orc, B, H, N, gh, gw, m, k):
+    q, kk_, v = _rand(B, H, N, 100 + N + m + k, 2.0)
+    rep = parity.full_parity(orc, q, kk_, v, gh, gw, m, k)
+    print(rep)
+
+
+def test_ascending_scores_force_compaction(orc):
+    """Scores that grow along the sequence make every key beat the running
+    threshold, so every chunk buffer overflows and compacts repeatedly."""
+    B, H, N, m, k = 1, 2, 40000, 4, 64
+    q = synth.normal_bf16((B, H, N, 64), 7, 0, 0.1)
+    q = synth.f64_to_bf16(synth.bf16_to_f64(q) + 1.0)  # queries (and landmarks) near the all-ones direction
+    ramp = np.linspace(-2.0, 2.0, N)[None, None, :, None]
+    noise = synth.bf16_to_f64(synth.normal_bf16((B, H, N, 64), 7, 1, 0.01))
+    kk_ = synth.f64_to_bf16(ramp + noise)
+    v = synth.normal_bf16((B, H, N, 64), 7, 2)
+    rep = parity.full_parity(orc, q, kk_, v, 0, 0, m, k)
+    print(rep)
+
+
+def test_exact_ties_go_to_lower_index(orc):
+    """Duplicated key rows tie exactly; the lower index must win. With every
+    row repeated 8 times, k = 12 cuts through the second-best group of ties."""
+    B, H, N, m, k = 1, 1, 4096, 8, 12
+    q, kk_, v = _rand(B, H, N, 31)
+    kk_ = kk_.copy()
+    src = np.arange(0, N, 8)
+    for r in range(1, 8):  # every key row repeated 8 times in a row
+        kk_[:, :, src + r] = kk_[:, :, src]
+    gpu = parity.run_gpu(q, kk_, v, 0, 0, m, k)
+    ora = orc.forward(q, kk_, v, 0, 0, m, k)
+    # ties are exact, so each expert must be the oracle's (same tie rule)
+    assert np.array_equal(gpu["expert_idx"], ora["expert_idx"])
+    parity.full_parity(orc, q, kk_, v, 0, 0, m, k, gpu=gpu)
+
+
+def test_empty_batch():
+    import torch
+
+    import mixture_top_forward_gb300 as M
+
+    Q = torch.empty((0, 4, 196, 64), dtype=torch.bfloat16, device="cuda")
+    out, e, r = M.mita_forward(Q, Q, Q, 14, 14, 25, 25)
+    assert out.shape == Q.shape and e.shape == (0, 4, 25, 25) and r.shape == (0, 4, 196)
+
+
+def test_host_entry_point_matches_device(orc):
+    import torch
+
+    import mixture_top_forward_gb300 as M
+
+    q, k, v = synth.make_inputs("tiny")
+    out_h, e_h, r_h = M.mita_forward_host(q, k, v, 14, 14, 25, 25)
+    out_d, e_d, r_d = M.mita_forward(parity.to_device(q), parity.to_device(k), parity.to_device(v), 14, 14, 25, 25)
+    torch.cuda.synchronize()
+    assert np.array_equal(out_h, out_d.view(torch.int16).cpu().numpy().view(np.uint16))
+    assert np.array_equal(e_h, e_d.cpu().numpy()) and np.array_equal(r_h, r_d.cpu().numpy())
+
+
+def test_repeatable(orc):
+    """Two calls give bit-identical results (no order-dependent arithmetic)."""
+    import torch
+
+    import mixture_top_forward_gb300 as M
+
+    q, k, v = synth.make_inputs("seg1024")
+    Q, K, V = parity.to_device(q), parity.to_device(k), parity.to_device(v)
+    a = M.mita_forward(Q, K, V, 32, 32, 49, 49)
+    b = M.mita_forward(Q, K, V, 32, 32, 49, 49)
+    torch.cuda.synchronize()
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)
