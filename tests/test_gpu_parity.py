@@ -51,7 +51,9 @@ def test_config_sampled(orc, name, heads, nq):
 
 
 def _rand(B, H, N, seed, scale=1.0):
-    return [synth.normal_bf16((B, H, N, 64), seed, t, scale) for t in range(3)]
+    """Q and K at `scale` (sharper softmaxes), V at unit scale: outputs stay
+    below 4 in magnitude, where bf16's half-ulp is below the 2e-2 bound."""
+    return [synth.normal_bf16((B, H, N, 64), seed, t, scale if t < 2 else 1.0) for t in range(3)]
 
 
 @pytest.mark.parametrize("B,H,N,gh,gw,m,k", [
