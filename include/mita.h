@@ -98,6 +98,37 @@ int mita_forward_host(const uint16_t* Q, const uint16_t* K, const uint16_t* V, i
                       void* stream);
 
 /*
+ * mita_forward for callers that cannot allocate device memory. (The paper has
+ * no counterpart: this entry point exists for library users, not for the
+ * method.) Some callers must not call cudaMalloc: a framework that owns all
+ * device memory through its own pool (a direct cudaMalloc would bypass its
+ * accounting, and can fail once the pool has reserved the device), or a
+ * latency-critical loop that cannot afford the device-wide synchronisation
+ * cudaMalloc and cudaFree imply. This variant allocates nothing: no
+ * cudaMalloc, no cudaFree, no allocating library call. Its scratch is one
+ * static device array of MITA_NOALLOC_SCRATCH_BYTES (32 MiB), which every GPU
+ * that loads the library holds until the process exits.
+ *
+ * Same arguments, layouts and results as mita_forward (the caller still
+ * provides Q, K, V, out, expert_idx and route). A shape whose scratch
+ * (mita_workspace_bytes) exceeds MITA_NOALLOC_SCRATCH_BYTES is rejected with
+ * MITA_ERR_UNSUPPORTED before anything is enqueued; the ViT-sized workloads
+ * (N up to a few thousand tokens, m and k in the tens) fit.
+ *
+ * The first call on a device looks up the array's device address with
+ * cudaGetSymbolAddress (with that device current); make that first call
+ * before any stream capture. Every call on a device shares the one array and
+ * finds the previous call's contents in it (it clears what must start at
+ * zero), so calls whose work overlaps on the GPU -- concurrent streams, or
+ * several host threads -- race; order them on one stream. Stage timing is
+ * not recorded for these calls, and a device-side timeout in them is not
+ * reported by mita_sync_status (the kernels still exit instead of hanging).
+ */
+#define MITA_NOALLOC_SCRATCH_BYTES (32 << 20)
+int mita_forward_noalloc(const void* Q, const void* K, const void* V, int B, int H, int N, int d, int grid_h,
+                         int grid_w, int m, int k, void* out, int32_t* expert_idx, int32_t* route, void* stream);
+
+/*
  * Bytes of scratch one mita_forward call of this shape holds in the
  * workspace (device buffers only; excludes mita_forward_host staging).
  * Returns 0 for an invalid or empty shape.

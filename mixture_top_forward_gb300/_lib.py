@@ -57,6 +57,8 @@ def load(path: str | None = None, build_if_missing: bool = True) -> ctypes.CDLL:
         lib.mita_forward.restype = ci
         lib.mita_forward_aux.argtypes = [vp, vp, vp] + [ci] * 8 + [vp, vp, vp, vp, vp, vp]
         lib.mita_forward_aux.restype = ci
+        lib.mita_forward_noalloc.argtypes = [vp, vp, vp] + [ci] * 8 + [vp, vp, vp, vp]
+        lib.mita_forward_noalloc.restype = ci
         lib.mita_forward_host.argtypes = [vp, vp, vp] + [ci] * 8 + [vp, vp, vp, vp]
         lib.mita_forward_host.restype = ci
         lib.mita_workspace_bytes.argtypes = [ci] * 8
@@ -130,6 +132,20 @@ def mita_forward(Q, K, V, grid_h: int, grid_w: int, m: int, k: int, out=None, ex
                              _dev_ptr(V, "torch.bfloat16", "V"), B, H, N, d, grid_h, grid_w, m, k,
                              _dev_ptr(out, "torch.bfloat16", "out"), _dev_ptr(expert_idx, "torch.int32", "expert_idx"),
                              _dev_ptr(route, "torch.int32", "route"), _stream(stream))
+    _raise(rc)
+    return out, expert_idx, route
+
+
+def mita_forward_noalloc(Q, K, V, grid_h: int, grid_w: int, m: int, k: int, out, expert_idx, route, stream=None):
+    """mita_forward through the no-allocation entry point: the library uses
+    its static device scratch instead of its workspace, so the caller must
+    pass every output buffer (nothing is allocated on this path)."""
+    B, H, N, d = _shape(Q, m, k, grid_h, grid_w)
+    rc = load().mita_forward_noalloc(_dev_ptr(Q, "torch.bfloat16", "Q"), _dev_ptr(K, "torch.bfloat16", "K"),
+                                     _dev_ptr(V, "torch.bfloat16", "V"), B, H, N, d, grid_h, grid_w, m, k,
+                                     _dev_ptr(out, "torch.bfloat16", "out"),
+                                     _dev_ptr(expert_idx, "torch.int32", "expert_idx"),
+                                     _dev_ptr(route, "torch.int32", "route"), _stream(stream))
     _raise(rc)
     return out, expert_idx, route
 

@@ -420,3 +420,73 @@ extern "C" void mita_release_workspace(void) {
     g_ws.clear();
     cudaSetDevice(cur);
 }
+
+// ---------------------------------------------------------------------------
+// Forward pass without allocation (see mita_forward_noalloc in mita.h).
+// Its scratch is this file-scope device array: the CUDA runtime reserves it
+// on every device that loads the library's module, until the process exits.
+// ---------------------------------------------------------------------------
+static __device__ __align__(256) unsigned char g_noalloc_scratch[MITA_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+
+std::mutex g_noalloc_mu;
+std::map<int, void*> g_noalloc_addr;  // device -> device address of g_noalloc_scratch
+
+// Device address of the static scratch on the current device. In host code
+// the array's name is only a host-side stand-in, so the address is asked
+// from the runtime once per device, with that device current.
+int noalloc_scratch(void** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    auto it = g_noalloc_addr.find(dev);
+    if (it == g_noalloc_addr.end()) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess || p == nullptr)
+            return fail(MITA_ERR_CUDA, "cudaGetSymbolAddress of the static scratch on device %d: %s", dev,
+                        cudaGetErrorString(e));
+        it = g_noalloc_addr.emplace(dev, p).first;
+    }
+    *out = it->second;
+    return MITA_OK;
+}
+
+}  // namespace
+
+extern "C" int mita_forward_noalloc(const void* Q, const void* K, const void* V, int B, int H, int N, int d,
+                                    int grid_h, int grid_w, int m, int k, void* out, int32_t* expert_idx,
+                                    int32_t* route, void* stream) {
+    g_err[0] = 0;
+    Shape s;
+    bool empty;
+    int rc = check_shape(B, H, N, d, grid_h, grid_w, m, k, &s, &empty);
+    if (rc != MITA_OK || empty) return rc;
+    if (!Q || !K || !V || !out || !expert_idx || !route)
+        return fail(MITA_ERR_INVALID_ARG, "a required pointer is NULL");
+    if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(out))
+        return fail(MITA_ERR_INVALID_ARG, "Q, K, V and out must be 16-byte aligned");
+    Plan P;
+    if (!make_plan(s, &P)) return fail(MITA_ERR_UNSUPPORTED, "problem too large for the launch grids");
+    if (P.total > static_cast<size_t>(MITA_NOALLOC_SCRATCH_BYTES))
+        return fail(MITA_ERR_UNSUPPORTED,
+                    "this shape needs %zu bytes of scratch; mita_forward_noalloc has %d (MITA_NOALLOC_SCRATCH_BYTES)",
+                    P.total, MITA_NOALLOC_SCRATCH_BYTES);
+    void* base = nullptr;
+    if ((rc = noalloc_scratch(&base)) != MITA_OK) return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    Work W = carve(P, base);
+    // The array keeps the previous call's contents; the status word must start
+    // at zero (the per-expert counters are cleared by the forward sequence).
+    cudaError_t e = cudaMemsetAsync(W.status, 0, sizeof(int), st);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
+    const bool prof = t_profile;  // stage timing would create events: keep it off here
+    t_profile = false;
+    rc = run_forward(P, W, static_cast<const __nv_bfloat16*>(Q), static_cast<const __nv_bfloat16*>(K),
+                     static_cast<const __nv_bfloat16*>(V), static_cast<__nv_bfloat16*>(out), expert_idx, route,
+                     nullptr, nullptr, st);
+    t_profile = prof;
+    return rc;
+}
