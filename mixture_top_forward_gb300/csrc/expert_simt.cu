@@ -9,8 +9,9 @@
 // is what the key loop below does: the m+k pairs stream through shared memory
 // in blocks of 32, with a running max and rescaled accumulators.
 //
-// One CTA per work item (head, expert, <= 128 queries of that expert), one
-// thread per query; key/value rows are read from shared memory as broadcasts.
+// One CTA per work item (expert, start, <= 128 queries, head) of the flat
+// item list, one thread per query; key/value rows are read from shared
+// memory as broadcasts. Used where experts hold few queries.
 #include "mita_internal.cuh"
 
 namespace mita {
@@ -22,16 +23,15 @@ constexpr int EB = 32;   // keys per staged block
 
 __global__ void __launch_bounds__(ET) expert_simt_kernel(
     const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restrict__ K, const __nv_bfloat16* __restrict__ V,
-    int64_t N, int m, int k, int64_t max_items, const int4* __restrict__ items, const int* __restrict__ nitems,
+    int64_t N, int m, int k, const int4* __restrict__ items, const int* __restrict__ nitems,
     const int* __restrict__ perm, const int32_t* __restrict__ expert_idx, const float* __restrict__ lq32,
     const float* __restrict__ lv32, __nv_bfloat16* __restrict__ out) {
     __shared__ __align__(16) float Ks[EB][D];
     __shared__ __align__(16) float Vs[EB][D];
-    const int64_t it = blockIdx.x % max_items;
-    const int64_t bh = blockIdx.x / max_items;
-    if (it >= nitems[bh]) return;
-    const int4 item = items[bh * max_items + it];
+    if (static_cast<int>(blockIdx.x) >= *nitems) return;
+    const int4 item = items[blockIdx.x];
     const int e = item.x, start = item.y, len = item.z;
+    const int64_t bh = item.w;
     const int t = threadIdx.x;
     const bool valid = t < len;
     const int n = valid ? perm[bh * N + start + t] : 0;
@@ -133,10 +133,10 @@ __global__ void __launch_bounds__(ET) expert_simt_kernel(
 
 }  // namespace
 
-cudaError_t launch_expert(const Plan& p, const Work& w, const __nv_bfloat16* Q, const __nv_bfloat16* K,
+cudaError_t launch_expert_simt(const Plan& p, const Work& w, const __nv_bfloat16* Q, const __nv_bfloat16* K,
                           const __nv_bfloat16* V, const int32_t* expert_idx, __nv_bfloat16* out, cudaStream_t st) {
     const unsigned grid = static_cast<unsigned>(p.s.BH * p.max_items);
-    expert_simt_kernel<<<grid, ET, 0, st>>>(Q, K, V, p.s.N, p.s.m, p.s.k, p.max_items, w.items, w.nitems, w.perm,
+    expert_simt_kernel<<<grid, ET, 0, st>>>(Q, K, V, p.s.N, p.s.m, p.s.k, w.items, w.nitems, w.perm,
                                             expert_idx, w.lq32, w.lv32, out);
     return cudaGetLastError();
 }

@@ -9,7 +9,9 @@
 //  1. the routing kernel has already counted queries per (head, expert);
 //  2. offsets_kernel (one CTA per head): exclusive scan of the counts gives
 //     each expert's segment of `perm`; it also cuts every segment into work
-//     items of at most `qtile` queries for the attention kernel;
+//     items (expert, start, length <= qtile, head) for the attention kernel,
+//     appended to one flat list: each head reserves its range with one global
+//     atomic, and keeps its items in expert order inside it;
 //  3. scatter_kernel (one CTA per 256 queries): counts its queries per expert
 //     in shared memory, reserves a range of each expert's segment with one
 //     global atomic per (CTA, expert), and writes the query indices there.
@@ -24,12 +26,12 @@ namespace {
 constexpr int GT = 1024;  // threads of the offsets kernel (>= MITA_MAX_M_INTERNAL)
 constexpr int SCT = 256;  // queries per scatter CTA
 
-__global__ void __launch_bounds__(GT) offsets_kernel(int m, int64_t N, int qtile, int64_t max_items,
-                                                     int* __restrict__ counts, int* __restrict__ expoff,
-                                                     int* __restrict__ cursor, int4* __restrict__ items,
-                                                     int* __restrict__ nitems) {
+__global__ void __launch_bounds__(GT) offsets_kernel(int m, int64_t N, int qtile, int* __restrict__ counts,
+                                                     int* __restrict__ expoff, int* __restrict__ cursor,
+                                                     int4* __restrict__ items, int* __restrict__ nitems) {
     __shared__ int sc[GT];
     __shared__ int st[GT];
+    __shared__ int base;
     const int64_t bh = blockIdx.x;
     const int e = threadIdx.x;
     const int c = e < m ? counts[bh * m + e] : 0;
@@ -45,20 +47,21 @@ __global__ void __launch_bounds__(GT) offsets_kernel(int m, int64_t N, int qtile
         st[e] += b;
         __syncthreads();
     }
+    if (e == m - 1) {
+        expoff[bh * (m + 1) + m] = sc[e];
+        base = atomicAdd(nitems, st[e]);
+    }
+    __syncthreads();
     if (e < m) {
         const int off = sc[e] - c;
         expoff[bh * (m + 1) + e] = off;
         cursor[bh * m + e] = off;
         counts[bh * m + e] = 0;  // ready for the next call
-        const int ib = st[e] - tiles;
+        const int ib = base + st[e] - tiles;
         for (int t = 0; t < tiles; ++t) {
             const int start = t * qtile;
-            items[bh * max_items + ib + t] = make_int4(e, off + start, min(qtile, c - start), 0);
+            items[ib + t] = make_int4(e, off + start, min(qtile, c - start), static_cast<int>(bh));
         }
-    }
-    if (e == m - 1) {
-        expoff[bh * (m + 1) + m] = sc[e];
-        nitems[bh] = st[e];
     }
 }
 
@@ -87,8 +90,8 @@ __global__ void __launch_bounds__(SCT) scatter_kernel(const int32_t* __restrict_
 }  // namespace
 
 cudaError_t launch_group(const Plan& p, const Work& w, const int32_t* route, cudaStream_t st) {
-    offsets_kernel<<<static_cast<unsigned>(p.s.BH), GT, 0, st>>>(p.s.m, p.s.N, p.qtile, p.max_items, w.counts,
-                                                                 w.expoff, w.cursor, w.items, w.nitems);
+    offsets_kernel<<<static_cast<unsigned>(p.s.BH), GT, 0, st>>>(p.s.m, p.s.N, p.qtile, w.counts, w.expoff,
+                                                                 w.cursor, w.items, w.nitems);
     const int64_t nblocks = (p.s.N + SCT - 1) / SCT;
     scatter_kernel<<<static_cast<unsigned>(p.s.BH * nblocks), SCT, 0, st>>>(route, p.s.N, p.s.m, nblocks, w.cursor,
                                                                             w.perm);

@@ -114,6 +114,27 @@ int workspace(cudaStream_t st, int purpose, size_t bytes, void** out) {
 
 }  // namespace
 
+int device_sms() {
+    static std::mutex mu;
+    static std::map<int, int> cache;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    std::lock_guard<std::mutex> lk(mu);
+    auto it = cache.find(dev);
+    if (it != cache.end()) return it->second;
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+    cache[dev] = n;
+    return n;
+}
+
+cudaError_t launch_expert(const Plan& p, const Work& w, const __nv_bfloat16* Q, const __nv_bfloat16* K,
+                          const __nv_bfloat16* V, const int32_t* expert_idx, __nv_bfloat16* out, cudaStream_t st) {
+    // tensor cores when the experts hold enough queries to fill 128-row tiles
+    if (expert_tc_supported(p) && p.s.N >= 32LL * p.s.m) return launch_expert_tc(p, w, Q, K, V, expert_idx, out, st);
+    return launch_expert_simt(p, w, Q, K, V, expert_idx, out, st);
+}
+
 bool make_plan(const Shape& s, Plan* p) {
     Plan P{};
     P.s = s;
@@ -157,7 +178,7 @@ bool make_plan(const Shape& s, Plan* p) {
     P.off_cursor = take(BH * m * sizeof(int));
     P.off_perm = take(BH * static_cast<size_t>(s.N) * sizeof(int));
     P.off_items = take(BH * static_cast<size_t>(P.max_items) * sizeof(int4));
-    P.off_nitems = take(BH * sizeof(int));
+    P.off_nitems = take(sizeof(int));
     P.total = off;
     if (P.max_items * s.BH > 0x7FFFFFFFLL || s.BH * P.nrblocks > 0x7FFFFFFFLL) return false;
     *p = P;
@@ -230,7 +251,8 @@ int run_forward(const Plan& P, const Work& W, const __nv_bfloat16* Q, const __nv
                 float* lv_out, cudaStream_t st) {
     cudaError_t e;
     const size_t mrows = static_cast<size_t>(P.s.BH) * P.s.m;
-    if ((e = cudaMemsetAsync(W.counts, 0, mrows * sizeof(int), st)) != cudaSuccess)
+    if ((e = cudaMemsetAsync(W.counts, 0, mrows * sizeof(int), st)) != cudaSuccess ||
+        (e = cudaMemsetAsync(W.nitems, 0, sizeof(int), st)) != cudaSuccess)
         return cuda_fail(e, "cudaMemsetAsync");
     StageMarks marks(st);
     marks.mark(0);

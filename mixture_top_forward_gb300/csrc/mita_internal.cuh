@@ -61,8 +61,8 @@ struct Work {
     int* expoff;            // [BH][m+1] exclusive prefix of counts
     int* cursor;            // [BH][m] scatter cursors
     int* perm;              // [BH][N] queries grouped by expert
-    int4* items;            // [BH][max_items] (expert, start, len, -)
-    int* nitems;            // [BH]
+    int4* items;            // [BH*max_items] flat list: (expert, start, len, head)
+    int* nitems;            // number of items in the flat list
 };
 
 Work carve(const Plan& p, void* base);
@@ -125,5 +125,15 @@ cudaError_t launch_route(const Plan& p, const Work& w, const __nv_bfloat16* Q, i
 cudaError_t launch_group(const Plan& p, const Work& w, const int32_t* route, cudaStream_t st);
 cudaError_t launch_expert(const Plan& p, const Work& w, const __nv_bfloat16* Q, const __nv_bfloat16* K,
                           const __nv_bfloat16* V, const int32_t* expert_idx, __nv_bfloat16* out, cudaStream_t st);
+cudaError_t launch_expert_simt(const Plan& p, const Work& w, const __nv_bfloat16* Q, const __nv_bfloat16* K,
+                               const __nv_bfloat16* V, const int32_t* expert_idx, __nv_bfloat16* out,
+                               cudaStream_t st);
+cudaError_t launch_expert_tc(const Plan& p, const Work& w, const __nv_bfloat16* Q, const __nv_bfloat16* K,
+                             const __nv_bfloat16* V, const int32_t* expert_idx, __nv_bfloat16* out,
+                             cudaStream_t st);
+bool expert_tc_supported(const Plan& p);
+
+// Number of SMs of the current device (cached per device).
+int device_sms();
 
 }  // namespace mita
