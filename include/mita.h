@@ -106,7 +106,7 @@ int mita_forward_host(const uint16_t* Q, const uint16_t* K, const uint16_t* V, i
  * latency-critical loop that cannot afford the device-wide synchronisation
  * cudaMalloc and cudaFree imply. This variant allocates nothing: no
  * cudaMalloc, no cudaFree, no allocating library call. Its scratch is one
- * static device array of MITA_NOALLOC_SCRATCH_BYTES (32 MiB), which every GPU
+ * static device array of MITA_NOALLOC_SCRATCH_BYTES (64 MiB), which every GPU
  * that loads the library holds until the process exits.
  *
  * Same arguments, layouts and results as mita_forward (the caller still
@@ -124,7 +124,7 @@ int mita_forward_host(const uint16_t* Q, const uint16_t* K, const uint16_t* V, i
  * not recorded for these calls, and a device-side timeout in them is not
  * reported by mita_sync_status (the kernels still exit instead of hanging).
  */
-#define MITA_NOALLOC_SCRATCH_BYTES (32 << 20)
+#define MITA_NOALLOC_SCRATCH_BYTES (64 << 20)
 int mita_forward_noalloc(const void* Q, const void* K, const void* V, int B, int H, int N, int d, int grid_h,
                          int grid_w, int m, int k, void* out, int32_t* expert_idx, int32_t* route, void* stream);
 

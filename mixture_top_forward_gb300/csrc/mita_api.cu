@@ -135,29 +135,93 @@ cudaError_t launch_expert(const Plan& p, const Work& w, const __nv_bfloat16* Q, 
     return launch_expert_simt(p, w, Q, K, V, expert_idx, out, st);
 }
 
+namespace {
+
+int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+int64_t round_up(int64_t a, int64_t b) { return cdiv(a, b) * b; }
+
+// Chunking and candidate capacity of one scan level. prevS = samples of the
+// pilot whose threshold this level starts from (0: none, every key is kept).
+ScanLevel scan_level(const Shape& s, int64_t S, int64_t stride, int64_t prevS, int64_t min_chunk, int sms) {
+    ScanLevel L{};
+    L.S = S;
+    L.stride = stride;
+    int64_t chunks = std::max<int64_t>(1, cdiv(sms, s.BH));  // about one wave of CTAs
+    chunks = std::min(chunks, cdiv(S, min_chunk));
+    if (prevS == 0) chunks = std::max(chunks, cdiv(S, 2048));  // bound what an unfiltered chunk keeps
+    L.chunk_len = round_up(cdiv(S, chunks), 128);
+    L.chunks = static_cast<int>(cdiv(S, L.chunk_len));
+    // A chunk holds at most min(chunk_len, S) keys: with that capacity it never
+    // compacts. A filtered level expects ~k * chunk_len / prevS survivors per
+    // landmark; give it 1.5x that (compaction handles the rest, and needs
+    // room for k plus one 128-key tile).
+    const int64_t room = round_up(std::min(L.chunk_len, S), 32);
+    int64_t cap = room;
+    if (prevS > 0) {
+        const int64_t expect = cdiv(static_cast<int64_t>(s.k) * L.chunk_len, prevS);
+        cap = std::max<int64_t>(round_up(expect + expect / 2 + 64, 32), s.k + 128);
+        cap = std::min(cap, room);
+    }
+    L.cap = static_cast<int>(cap);
+    return L;
+}
+
+}  // namespace
+
 bool make_plan(const Shape& s, Plan* p) {
     Plan P{};
     P.s = s;
-    // scan: 32 landmarks per CTA; enough key chunks for ~8 CTAs per SM, at
-    // least 1024 keys per chunk
-    P.ltile = 32;
-    const int64_t ltiles = (s.m + P.ltile - 1) / P.ltile;
-    const int64_t target = 152 * 8;
-    int64_t chunks = (target + s.BH * ltiles - 1) / (s.BH * ltiles);
-    chunks = std::max<int64_t>(1, std::min<int64_t>(chunks, s.N / 1024));
-    P.chunk_len = (s.N + chunks - 1) / chunks;
-    P.chunks = static_cast<int>((s.N + P.chunk_len - 1) / P.chunk_len);
-    const int64_t room = ((P.chunk_len + 31) / 32) * 32 + 32;  // a chunk never needs more
-    int64_t cap = ((2 * static_cast<int64_t>(s.k) + 64 + 31) / 32) * 32;
-    cap = std::min(cap, room);
-    cap = std::max<int64_t>(cap, s.k + 32);
-    P.cap = static_cast<int>(cap);
+    const int sms = device_sms();
+    P.scan_tc = s.m <= 256;
+    if (P.scan_tc) {
+        // Pilots: strided samples, the first of max(2k, min(N/8, 8k)) keys,
+        // then up to 16x larger, the last of about N/8 keys; each starts from
+        // the previous level's threshold. The main scan then keeps about 8k
+        // candidates per landmark and head.
+        int64_t prevS = 0;
+        const int64_t K8 = 8LL * s.k;
+        int64_t t = std::max<int64_t>(2LL * s.k, std::min<int64_t>(s.N / 8, K8));
+        if (8 * t <= s.N) {
+            while (P.nlev < 3) {
+                const int64_t stride = s.N / t;
+                const int64_t S = cdiv(s.N, stride);
+                P.lev[P.nlev++] = scan_level(s, S, stride, prevS, 512, sms);
+                prevS = S;
+                const int64_t next = std::min<int64_t>(16 * t, s.N / 8);
+                if (next <= t) break;
+                t = next;
+            }
+        }
+        P.lev[P.nlev++] = scan_level(s, s.N, 1, prevS, 512, sms);
+    } else {
+        // CUDA-core scan: 32 landmarks per CTA, ~8 CTAs per SM, >= 1024 keys per chunk
+        const int64_t ltiles = cdiv(s.m, 32);
+        int64_t chunks = cdiv(static_cast<int64_t>(sms) * 8, s.BH * ltiles);
+        chunks = std::max<int64_t>(1, std::min<int64_t>(chunks, s.N / 1024));
+        ScanLevel L{};
+        L.S = s.N;
+        L.stride = 1;
+        L.chunk_len = cdiv(s.N, chunks);
+        L.chunks = static_cast<int>(cdiv(s.N, L.chunk_len));
+        const int64_t room = round_up(L.chunk_len, 32) + 32;
+        int64_t cap = round_up(2LL * s.k + 64, 32);
+        cap = std::min(cap, room);
+        cap = std::max<int64_t>(cap, s.k + 32);
+        L.cap = static_cast<int>(cap);
+        P.nlev = 1;
+        P.lev[0] = L;
+    }
     P.rblock = 256;
     P.nrblocks = (s.N + P.rblock - 1) / P.rblock;
     P.qtile = 128;
     P.max_items = (s.N + P.qtile - 1) / P.qtile + s.m;
 
     const size_t BH = static_cast<size_t>(s.BH), m = static_cast<size_t>(s.m);
+    size_t cand = 0, cnts = 0;
+    for (int l = 0; l < P.nlev; ++l) {
+        cand = std::max(cand, BH * P.lev[l].chunks * m * static_cast<size_t>(P.lev[l].cap));
+        cnts = std::max(cnts, BH * P.lev[l].chunks * m);
+    }
     size_t off = 0;
     auto take = [&](size_t bytes) {
         const size_t o = off;
@@ -170,9 +234,10 @@ bool make_plan(const Shape& s, Plan* p) {
     P.off_lqlo = take(BH * m * D * 2);
     P.off_lv32 = take(BH * m * D * sizeof(float));
     P.off_lvbf = take(BH * m * D * 2);
-    P.off_part = take(BH * P.chunks * m * 68 * sizeof(float));
-    P.off_cand = take(BH * P.chunks * m * static_cast<size_t>(P.cap) * sizeof(uint64_t));
-    P.off_ccount = take(BH * P.chunks * m * sizeof(int));
+    P.off_part = take(BH * P.lev[P.nlev - 1].chunks * m * 68 * sizeof(float));
+    P.off_cand = take(cand * sizeof(uint64_t));
+    P.off_ccount = take(cnts * sizeof(int));
+    P.off_theta = take(BH * m * sizeof(uint64_t));
     P.off_counts = take(BH * m * sizeof(int));
     P.off_expoff = take(BH * (m + 1) * sizeof(int));
     P.off_cursor = take(BH * m * sizeof(int));
@@ -181,6 +246,8 @@ bool make_plan(const Shape& s, Plan* p) {
     P.off_nitems = take(sizeof(int));
     P.total = off;
     if (P.max_items * s.BH > 0x7FFFFFFFLL || s.BH * P.nrblocks > 0x7FFFFFFFLL) return false;
+    for (int l = 0; l < P.nlev; ++l)
+        if (s.BH * P.lev[l].chunks * 32 > 0x7FFFFFFFLL) return false;
     *p = P;
     return true;
 }
@@ -197,6 +264,7 @@ Work carve(const Plan& p, void* base) {
     w.part = reinterpret_cast<float*>(b + p.off_part);
     w.cand = reinterpret_cast<uint64_t*>(b + p.off_cand);
     w.ccount = reinterpret_cast<int*>(b + p.off_ccount);
+    w.theta = reinterpret_cast<uint64_t*>(b + p.off_theta);
     w.counts = reinterpret_cast<int*>(b + p.off_counts);
     w.expoff = reinterpret_cast<int*>(b + p.off_expoff);
     w.cursor = reinterpret_cast<int*>(b + p.off_cursor);
@@ -213,11 +281,10 @@ namespace {
 // ---------------------------------------------------------------------------
 constexpr int kStages = 6;
 const char* const kStageNames[kStages] = {"pool", "scan", "select", "route", "group", "expert"};
-const int kStageLaunches[kStages] = {1, 1, 1, 1, 2, 1};
-
 struct Recorded {
     cudaStream_t stream;
     cudaEvent_t ev[kStages + 1];
+    int launches[kStages];
 };
 thread_local bool t_profile = false;
 thread_local std::vector<Recorded> t_records;
@@ -235,8 +302,11 @@ struct StageMarks {
     void mark(int i) {
         if (on) cudaEventRecord(rec.ev[i], rec.stream);
     }
-    void commit() {
-        if (on) t_records.push_back(rec);
+    void commit(const int* launches) {
+        if (on) {
+            for (int i = 0; i < kStages; ++i) rec.launches[i] = launches[i];
+            t_records.push_back(rec);
+        }
         on = false;
     }
     ~StageMarks() {
@@ -258,7 +328,18 @@ int run_forward(const Plan& P, const Work& W, const __nv_bfloat16* Q, const __nv
     marks.mark(0);
     if ((e = launch_pool(P, W, Q, st)) != cudaSuccess) return cuda_fail(e, "landmark pooling launch");
     marks.mark(1);
-    if ((e = launch_scan(P, W, K, V, st)) != cudaSuccess) return cuda_fail(e, "landmark scan launch");
+    if (P.scan_tc) {
+        if (P.nlev > 1 && (e = cudaMemsetAsync(W.theta, 0, mrows * sizeof(uint64_t), st)) != cudaSuccess)
+            return cuda_fail(e, "cudaMemsetAsync");
+        for (int l = 0; l + 1 < P.nlev; ++l) {
+            if ((e = launch_scan_tc(P, W, K, V, l, st)) != cudaSuccess) return cuda_fail(e, "pilot scan launch");
+            if ((e = launch_pilot_select(P, W, l, st)) != cudaSuccess) return cuda_fail(e, "pilot select launch");
+        }
+        if ((e = launch_scan_tc(P, W, K, V, P.nlev - 1, st)) != cudaSuccess)
+            return cuda_fail(e, "landmark scan launch");
+    } else if ((e = launch_scan(P, W, K, V, st)) != cudaSuccess) {
+        return cuda_fail(e, "landmark scan launch");
+    }
     marks.mark(2);
     if ((e = launch_select(P, W, expert_idx, st)) != cudaSuccess) return cuda_fail(e, "expert selection launch");
     marks.mark(3);
@@ -269,7 +350,8 @@ int run_forward(const Plan& P, const Work& W, const __nv_bfloat16* Q, const __nv
     if ((e = launch_expert(P, W, Q, K, V, expert_idx, out, st)) != cudaSuccess)
         return cuda_fail(e, "expert attention launch");
     marks.mark(6);
-    marks.commit();
+    const int launches[kStages] = {1, P.scan_tc ? 2 * P.nlev - 1 : 1, 1, 1, 2, 1};
+    marks.commit(launches);
     if (lq_out && (e = cudaMemcpyAsync(lq_out, W.lq32, mrows * D * sizeof(float), cudaMemcpyDeviceToDevice, st)) !=
                       cudaSuccess)
         return cuda_fail(e, "copy of Lq");
@@ -415,7 +497,7 @@ extern "C" int mita_profile_read(double* stage_ms, int64_t* stage_launches, int 
             if (rc == MITA_OK && (e = cudaEventElapsedTime(&ms, r.ev[i], r.ev[i + 1])) != cudaSuccess)
                 rc = cuda_fail(e, "cudaEventElapsedTime");
             if (stage_ms) stage_ms[i] += ms;
-            if (stage_launches) stage_launches[i] += kStageLaunches[i];
+            if (stage_launches) stage_launches[i] += r.launches[i];
         }
         for (auto& ev : r.ev) cudaEventDestroy(ev);
     }

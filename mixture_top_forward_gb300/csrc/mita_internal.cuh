@@ -25,13 +25,22 @@ struct Shape {
     int m, k;       // landmarks, keys per routed expert
 };
 
+// One scan over (a sample of) every head's keys.
+struct ScanLevel {
+    int64_t S;          // keys scanned per head (samples 0..S-1)
+    int64_t stride;     // sample s is key s * stride
+    int64_t chunk_len;  // samples per chunk (last one may be shorter)
+    int chunks;         // chunks per head (one CTA each)
+    int cap;            // candidate slots per (head, chunk, landmark)
+};
+
 struct Plan {
     Shape s;
-    // landmark scan
-    int ltile;          // landmarks per scan CTA
-    int chunks;         // key chunks per head
-    int64_t chunk_len;  // keys per chunk (last one may be shorter)
-    int cap;            // candidate slots per (head, chunk, landmark)
+    // landmark scan: pilot levels on strided samples, then the main scan
+    // (lev[nlev-1], stride 1); scan_tc selects the tensor-core kernels
+    bool scan_tc;
+    int nlev;
+    ScanLevel lev[4];
     // routing / grouping
     int rblock;         // queries per routing CTA
     int64_t nrblocks;   // routing CTAs per head
@@ -39,7 +48,7 @@ struct Plan {
     int qtile;          // queries per expert work item
     int64_t max_items;  // work items per head, upper bound
     // workspace layout (byte offsets)
-    size_t off_status, off_lq32, off_lqhi, off_lqlo, off_lv32, off_lvbf, off_part, off_cand, off_ccount,
+    size_t off_status, off_lq32, off_lqhi, off_lqlo, off_lv32, off_lvbf, off_part, off_cand, off_ccount, off_theta,
         off_counts, off_expoff, off_cursor, off_perm, off_items, off_nitems, total;
 };
 
@@ -57,6 +66,7 @@ struct Work {
     float* part;            // [BH][chunks][m][68]: max, sum, -, -, o[64]
     uint64_t* cand;         // [BH][chunks][m][cap] composite top-k keys
     int* ccount;            // [BH][chunks][m]
+    uint64_t* theta;        // [BH][m] top-k thresholds from the pilot scans
     int* counts;            // [BH][m] queries routed to each expert
     int* expoff;            // [BH][m+1] exclusive prefix of counts
     int* cursor;            // [BH][m] scatter cursors
@@ -120,7 +130,10 @@ constexpr float kLog2e = 1.4426950408889634f;
 cudaError_t launch_pool(const Plan& p, const Work& w, const __nv_bfloat16* Q, cudaStream_t st);
 cudaError_t launch_scan(const Plan& p, const Work& w, const __nv_bfloat16* K, const __nv_bfloat16* V,
                         cudaStream_t st);
+cudaError_t launch_scan_tc(const Plan& p, const Work& w, const __nv_bfloat16* K, const __nv_bfloat16* V, int level,
+                           cudaStream_t st);
 cudaError_t launch_select(const Plan& p, const Work& w, int32_t* expert_idx, cudaStream_t st);
+cudaError_t launch_pilot_select(const Plan& p, const Work& w, int level, cudaStream_t st);
 cudaError_t launch_route(const Plan& p, const Work& w, const __nv_bfloat16* Q, int32_t* route, cudaStream_t st);
 cudaError_t launch_group(const Plan& p, const Work& w, const int32_t* route, cudaStream_t st);
 cudaError_t launch_expert(const Plan& p, const Work& w, const __nv_bfloat16* Q, const __nv_bfloat16* K,

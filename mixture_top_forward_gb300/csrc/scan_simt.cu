@@ -137,8 +137,9 @@ __global__ void __launch_bounds__(SW * 32) scan_simt_kernel(
 cudaError_t launch_scan(const Plan& p, const Work& w, const __nv_bfloat16* K, const __nv_bfloat16* V,
                         cudaStream_t st) {
     const int ltiles = (p.s.m + LT - 1) / LT;
-    const unsigned grid = static_cast<unsigned>(p.s.BH * p.chunks * ltiles);
-    scan_simt_kernel<<<grid, SW * 32, 0, st>>>(K, V, p.s.N, p.s.m, p.s.k, p.chunks, p.chunk_len, p.cap, ltiles,
+    const ScanLevel& L = p.lev[0];
+    const unsigned grid = static_cast<unsigned>(p.s.BH * L.chunks * ltiles);
+    scan_simt_kernel<<<grid, SW * 32, 0, st>>>(K, V, p.s.N, p.s.m, p.s.k, L.chunks, L.chunk_len, L.cap, ltiles,
                                                w.lq32, w.part, w.cand, w.ccount);
     return cudaGetLastError();
 }

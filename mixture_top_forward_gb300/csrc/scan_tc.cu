@@ -1,0 +1,405 @@
+// Stage 2 on the tensor cores: the landmark scan, and the sample pilots that
+// give it its top-k thresholds.
+//
+// "NeurIPS 2026 | Mixture-of-Top-k 注意力" (shuwu5.cn), section
+// "MiTA：用少量地标查询，同时完成压缩与专家构造": each landmark query is matched
+// against every key; its k best keys form its routed expert, and the same
+// landmark's cross-attention over the whole sequence gives the shared-expert
+// value LV_i. One pass over K and V does both.
+//
+// One CTA per (head, chunk of keys); it holds all m <= 256 landmark queries
+// (NL = 1 or 2 tiles of 128 rows) in shared memory as a bf16 hi/lo pair,
+// hi = bf16(Lq), lo = bf16(Lq - hi), so that S = Lq_hi K^T + Lq_lo K^T (two
+// accumulating MMAs) matches the fp32 landmark to ~2^-16 relative: exact
+// enough for the top-k comparisons.
+//   warp 0 lane 0: TMA producer of 128-key tiles of K (3-4 stage ring);
+//   warp 3 lane 0: TMA producer of V tiles (2-3 stages; full scans only);
+//   warp 1 lane 0: MMA issuer: S_L = Lq_L K^T into TMEM per landmark tile L,
+//                  and one tile later O_L += P_L V (full scans only);
+//   warp 2:        TMEM allocation;
+//   warps 4..:     one warpgroup per landmark tile, one thread per landmark.
+//                  A thread loads its 128 scores, offers them to its
+//                  landmark's candidate buffer (topk.cuh: append when the
+//                  64-bit order key reaches the threshold, warp-cooperative
+//                  compaction on overflow) and, in full scans, runs the online
+//                  softmax (lazy running max), writes P (bf16) and leaves a
+//                  (max, sum, o[64]) partial at the end of the chunk.
+// Keys are read through a 3-D tensor map (row, head) whose row stride may be
+// > 1: a pilot scan reads every stride-th key of each head. A pilot does only
+// the top-k part; its k-th best order key (select.cu) is a lower bound of the
+// true k-th best of the whole head, because the sample keys are keys of the
+// head, so the next scan may start from it and still keep every key of the
+// true top k. Every wait is bounded (umma.cuh).
+#include "tensormap.cuh"
+#include "topk.cuh"
+#include "umma.cuh"
+
+namespace mita {
+
+namespace {
+
+using namespace umma;
+
+constexpr float kC = 0.125f * kLog2e;  // tau * log2(e)
+constexpr float kLazy = 8.0f;
+constexpr uint32_t kIdescS = idesc_bf16(128, 128, false);
+constexpr uint32_t kIdescPV = idesc_bf16(128, 64, true);
+
+struct ScanArgs {
+    const __nv_bfloat16* lqhi;
+    const __nv_bfloat16* lqlo;
+    const uint64_t* theta;  // [BH][m] starting thresholds, or null (0: accept everything)
+    float* part;            // [BH][chunks][m][68], full scans only
+    uint64_t* cand;         // [BH][chunks][m][cap]
+    int* ccount;            // [BH][chunks][m]
+    int* status;
+    int64_t S;          // keys (samples) per head in this scan
+    int64_t stride;     // key index of sample s is s * stride
+    int64_t chunk_len;  // multiple of 128
+    int chunks, cap, m, k;
+};
+
+template <bool FULL, int NL>
+struct Cfg {
+    static constexpr int KST = FULL ? (NL == 2 ? 3 : 4) : 4;  // K ring stages
+    static constexpr int VST = FULL ? (NL == 2 ? 2 : 3) : 0;  // V ring stages
+    static constexpr int NT = 128 + NL * 128;
+    static constexpr size_t OFF_LQLO = NL * 16384;
+    static constexpr size_t OFF_K = 2 * NL * 16384;
+    static constexpr size_t OFF_V = OFF_K + KST * 16384;
+    static constexpr size_t OFF_P = OFF_V + VST * 16384;
+    static constexpr size_t OFF_HIST = OFF_P + (FULL ? NL * 32768 : 0);
+    static constexpr size_t SMEM = OFF_HIST + NL * 4 * 1024 + 1024;
+    static constexpr uint32_t TCOLS = NL * 256;  // per tile L: S at L*256, O at L*256 + 128
+};
+
+// Score of an order key (the inverse of topk_key's float mapping); -inf for 0.
+__device__ __forceinline__ float key_score(uint64_t key) {
+    if (key == 0) return -INFINITY;
+    uint32_t u = static_cast<uint32_t>(key >> 32);
+    u = (u & 0x80000000u) ? (u & 0x7FFFFFFFu) : ~u;
+    return __uint_as_float(u);
+}
+
+// Issues O_L += P_L V for every landmark tile L of key tile i (MMA thread).
+template <class C, int NL>
+__device__ __forceinline__ bool issue_pv(const ScanArgs& a, uint8_t* base, uint32_t tb, int i, uint64_t* vfull,
+                                         uint64_t* vempty, uint64_t* pfull, uint64_t* pvdone) {
+    const int vs = i % C::VST;
+    if (!mbar_wait(&vfull[vs], (i / C::VST) & 1, a.status)) return false;
+    const uint32_t va = smem_u32(base + C::OFF_V + vs * 16384);
+    for (int l = 0; l < NL; ++l) {
+        if (!mbar_wait(&pfull[l], i & 1, a.status)) return false;
+        tc_fence_after();
+        const uint32_t pa = smem_u32(base + C::OFF_P + l * 32768);
+        const uint32_t tO = tb + l * 256 + 128;
+#pragma unroll
+        for (int s = 0; s < 8; ++s)
+            mma_ss(tO, sdesc_sw128(pa + (s >> 2) * 16384 + (s & 3) * 32), sdesc_sw128(va + s * 2048), kIdescPV,
+                   (i > 0 || s > 0) ? 1u : 0u);
+        mma_commit(&pvdone[l]);
+    }
+    mma_commit(&vempty[vs]);
+    return true;
+}
+
+template <bool FULL, int NL>
+__global__ void __launch_bounds__(Cfg<FULL, NL>::NT, 1)
+    scan_tc_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv, ScanArgs a) {
+    using C = Cfg<FULL, NL>;
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ uint64_t kfull[C::KST], kempty[C::KST];
+    __shared__ uint64_t vfull[C::VST > 0 ? C::VST : 1], vempty[C::VST > 0 ? C::VST : 1];
+    __shared__ uint64_t sfull[NL], sfree[NL], pfull[NL], pvdone[NL];
+    __shared__ uint32_t tmem_base;
+    uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int c = static_cast<int>(blockIdx.x % static_cast<unsigned>(a.chunks));
+    const int64_t bh = blockIdx.x / static_cast<unsigned>(a.chunks);
+    const int64_t s0 = static_cast<int64_t>(c) * a.chunk_len;
+    const int64_t s1 = min(a.S, s0 + a.chunk_len);
+    const int T = static_cast<int>((s1 - s0 + 127) / 128);
+
+    if (tid == 0) {
+        for (int i = 0; i < C::KST; ++i) {
+            mbar_init(&kfull[i], 1);
+            mbar_init(&kempty[i], 1);
+        }
+        for (int i = 0; i < C::VST; ++i) {
+            mbar_init(&vfull[i], 1);
+            mbar_init(&vempty[i], 1);
+        }
+        for (int l = 0; l < NL; ++l) {
+            mbar_init(&sfull[l], 1);
+            mbar_init(&sfree[l], 1);
+            mbar_init(&pfull[l], 1);
+            mbar_init(&pvdone[l], 1);
+        }
+        fence_barrier_init();
+    }
+    if (warp == 2) tmem_alloc(&tmem_base, C::TCOLS);
+    {   // landmark queries of this head, hi and lo, rows >= m zero
+        const uint32_t hb = smem_u32(base), lb = smem_u32(base + C::OFF_LQLO);
+        for (int x = tid; x < NL * 128 * 8; x += C::NT) {
+            const int row = x >> 3, ch = x & 7;
+            const uint32_t off = swz128(row, ch);
+            if (row < a.m) {
+                const int64_t src = (bh * a.m + row) * D + ch * 8;
+                cp_async16(hb + off, a.lqhi + src);
+                cp_async16(lb + off, a.lqlo + src);
+            } else {
+                *reinterpret_cast<uint4*>(base + off) = make_uint4(0, 0, 0, 0);
+                *reinterpret_cast<uint4*>(base + C::OFF_LQLO + off) = make_uint4(0, 0, 0, 0);
+            }
+        }
+        cp_async_wait_all();
+        fence_proxy_async();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tb = tmem_base;
+
+    if (warp == 0) {
+        // ---------------- K producer ----------------
+        if (lane == 0) {
+            for (int i = 0; i < T; ++i) {
+                const int st = i % C::KST;
+                if (i >= C::KST && !mbar_wait(&kempty[st], ((i / C::KST) & 1) ^ 1, a.status)) break;
+                mbar_arrive_expect_tx(&kfull[st], 16384);
+                tma_load_3d(base + C::OFF_K + st * 16384, &tk, 0, static_cast<int>(s0 + i * 128),
+                            static_cast<int>(bh), &kfull[st]);
+            }
+        }
+    } else if (warp == 3) {
+        // ---------------- V producer ----------------
+        if constexpr (FULL) {
+          if (lane == 0) {
+            for (int i = 0; i < T; ++i) {
+                const int st = i % C::VST;
+                if (i >= C::VST && !mbar_wait(&vempty[st], ((i / C::VST) & 1) ^ 1, a.status)) break;
+                mbar_arrive_expect_tx(&vfull[st], 16384);
+                tma_load_3d(base + C::OFF_V + st * 16384, &tv, 0, static_cast<int>(s0 + i * 128),
+                            static_cast<int>(bh), &vfull[st]);
+            }
+          }
+        }
+    } else if (warp == 1) {
+        // ---------------- MMA issuer ----------------
+        if (lane == 0) {
+            const uint32_t hi = smem_u32(base), lo = smem_u32(base + C::OFF_LQLO);
+            bool ok = true;
+            for (int i = 0; i < T && ok; ++i) {
+                const int st = i % C::KST;
+                if (!mbar_wait(&kfull[st], (i / C::KST) & 1, a.status)) break;
+                tc_fence_after();
+                const uint32_t ka = smem_u32(base + C::OFF_K + st * 16384);
+                for (int l = 0; l < NL && ok; ++l) {
+                    if (i > 0) {
+                        if (!mbar_wait(&sfree[l], (i - 1) & 1, a.status)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                    }
+                    const uint32_t tS = tb + l * 256;
+#pragma unroll
+                    for (int s = 0; s < 4; ++s)
+                        mma_ss(tS, sdesc_sw128(hi + l * 16384 + s * 32), sdesc_sw128(ka + s * 32), kIdescS, s > 0);
+#pragma unroll
+                    for (int s = 0; s < 4; ++s)
+                        mma_ss(tS, sdesc_sw128(lo + l * 16384 + s * 32), sdesc_sw128(ka + s * 32), kIdescS, 1u);
+                    mma_commit(&sfull[l]);
+                }
+                if (!ok) break;
+                mma_commit(&kempty[st]);
+                if constexpr (FULL) {
+                    if (i > 0) ok = issue_pv<C, NL>(a, base, tb, i - 1, vfull, vempty, pfull, pvdone);
+                }
+            }
+            if constexpr (FULL) {
+                if (ok && T > 0) issue_pv<C, NL>(a, base, tb, T - 1, vfull, vempty, pfull, pvdone);
+            }
+        }
+    } else if (warp >= 4) {
+        // ---------------- landmark rows: top-k filter and softmax ----------------
+        const int L = (warp - 4) >> 2;
+        const int t = tid - 128 - L * 128;
+        const int li = L * 128 + t;
+        const bool row_ok = li < a.m;
+        const int bar_id = 1 + L;
+        const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+        const uint32_t tS = tb + L * 256, tO = tS + 128;
+        const int64_t slot = (bh * a.chunks + c) * a.m + (row_ok ? li : 0);
+        uint64_t* buf = a.cand + slot * static_cast<int64_t>(a.cap);
+        uint64_t theta = (a.theta && row_ok) ? a.theta[bh * a.m + li] : 0;
+        float theta_s = key_score(theta);
+        int cnt = 0;
+        unsigned* hist = reinterpret_cast<unsigned*>(base + C::OFF_HIST + (warp - 4) * 1024);
+        uint8_t* pb = base + C::OFF_P + L * 32768;
+        float mrun = -INFINITY, lrun = 0.f;
+        bool ok = true;
+        for (int i = 0; i < T; ++i) {
+            ok = named_bar_and(bar_id, 128, mbar_wait(&sfull[L], i & 1, a.status));
+            if (!ok) break;
+            tc_fence_after();
+            float s[128];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) tmem_ld32(tS + lane_off + q * 32, s + q * 32);
+            tmem_ld_wait();
+            tc_fence_before();
+            named_bar(bar_id, 128);
+            if (t == 0) mbar_arrive(&sfree[L]);
+            const int64_t col0 = s0 + static_cast<int64_t>(i) * 128;
+            const int nvalid = static_cast<int>(s1 - col0 < 128 ? s1 - col0 : 128);
+
+            // top-k candidates (compaction first if this tile could overflow a buffer)
+            unsigned need = __ballot_sync(0xffffffffu, row_ok && cnt + nvalid > a.cap);
+            while (need) {
+                const int src = __ffs(need) - 1;
+                need &= need - 1;
+                uint64_t* b = reinterpret_cast<uint64_t*>(
+                    __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(buf), src));
+                const int bc = __shfl_sync(0xffffffffu, cnt, src);
+                const uint64_t kth = warp_compact_topk(b, bc, a.k, hist);
+                if (lane == src) {
+                    cnt = a.k;
+                    theta = kth + 1;
+                    theta_s = key_score(kth);
+                }
+            }
+            if (row_ok) {
+#pragma unroll
+                for (int col = 0; col < 128; ++col) {
+                    const float sc = s[col] * 0.125f;
+                    if (col < nvalid && sc >= theta_s) {
+                        const uint64_t key = topk_key(sc, static_cast<uint32_t>((col0 + col) * a.stride));
+                        if (key >= theta) buf[cnt++] = key;
+                    }
+                }
+            }
+            if (FULL) {
+                float bmax = -INFINITY;
+#pragma unroll
+                for (int col = 0; col < 128; ++col) {
+                    s[col] = col < nvalid ? s[col] * kC : -INFINITY;
+                    bmax = fmaxf(bmax, s[col]);
+                }
+                const float mnew = (bmax > mrun + kLazy) ? bmax : mrun;
+                const float alpha = exp2f(mrun - mnew);
+                float sum = 0.f;
+#pragma unroll
+                for (int col = 0; col < 128; ++col) {
+                    s[col] = exp2f(s[col] - mnew);
+                    sum += s[col];
+                }
+                lrun = lrun * alpha + sum;
+                if (i > 0) {
+                    ok = named_bar_and(bar_id, 128, mbar_wait(&pvdone[L], (i - 1) & 1, a.status));
+                    if (!ok) break;
+                    tc_fence_after();
+                    if (__any_sync(0xffffffffu, alpha != 1.f)) {
+                        float o[32];
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            tmem_ld32(tO + lane_off + h * 32, o);
+                            tmem_ld_wait();
+#pragma unroll
+                            for (int q = 0; q < 32; ++q) o[q] *= alpha;
+                            tmem_st32(tO + lane_off + h * 32, o);
+                        }
+                        tmem_st_wait();
+                    }
+                }
+#pragma unroll
+                for (int g = 0; g < 16; ++g) {
+                    uint4 pk;
+                    __nv_bfloat162* h2 = reinterpret_cast<__nv_bfloat162*>(&pk);
+#pragma unroll
+                    for (int u = 0; u < 4; ++u)
+                        h2[u] = __floats2bfloat162_rn(s[8 * g + 2 * u], s[8 * g + 2 * u + 1]);
+                    *reinterpret_cast<uint4*>(pb + (g >> 3) * 16384 + swz128(t, g & 7)) = pk;
+                }
+                fence_proxy_async();
+                tc_fence_before();
+                named_bar(bar_id, 128);
+                if (t == 0) mbar_arrive(&pfull[L]);
+                mrun = mnew;
+            }
+        }
+        if (FULL && ok && T > 0) {
+            ok = named_bar_and(bar_id, 128, mbar_wait(&pvdone[L], (T - 1) & 1, a.status));
+            if (ok) {
+                tc_fence_after();
+                float o[64];
+                tmem_ld32(tO + lane_off, o);
+                tmem_ld32(tO + lane_off + 32, o + 32);
+                tmem_ld_wait();
+                if (row_ok) {
+                    float* pp = a.part + slot * 68;
+                    pp[0] = mrun / kLog2e;  // running max in natural-log units of tau <Lq, K>
+                    pp[1] = lrun;
+#pragma unroll
+                    for (int q = 0; q < 64; q += 4)
+                        *reinterpret_cast<float4*>(pp + 4 + q) = make_float4(o[q], o[q + 1], o[q + 2], o[q + 3]);
+                }
+            }
+        }
+        if (row_ok) a.ccount[slot] = cnt;
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 2) tmem_free(tb, C::TCOLS);
+}
+
+template <bool FULL, int NL>
+cudaError_t launch_one(const CUtensorMap& tk, const CUtensorMap& tv, const ScanArgs& a, int64_t BH,
+                       cudaStream_t st) {
+    using C = Cfg<FULL, NL>;
+    cudaError_t e = cudaFuncSetAttribute(scan_tc_kernel<FULL, NL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(C::SMEM));
+    if (e != cudaSuccess) return e;
+    const unsigned grid = static_cast<unsigned>(BH * a.chunks);
+    scan_tc_kernel<FULL, NL><<<grid, C::NT, C::SMEM, st>>>(tk, tv, a);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_scan_tc(const Plan& p, const Work& w, const __nv_bfloat16* K, const __nv_bfloat16* V, int level,
+                           cudaStream_t st) {
+    const ScanLevel& L = p.lev[level];
+    const bool full = level == p.nlev - 1;
+    CUtensorMap tk, tv;
+    if (!make_head_tmap(&tk, K, static_cast<uint64_t>(L.S), static_cast<uint64_t>(p.s.BH),
+                        static_cast<uint64_t>(L.stride), static_cast<uint64_t>(p.s.N), 128))
+        return cudaErrorInvalidValue;
+    if (full) {
+        if (!make_head_tmap(&tv, V, static_cast<uint64_t>(p.s.N), static_cast<uint64_t>(p.s.BH), 1,
+                            static_cast<uint64_t>(p.s.N), 128))
+            return cudaErrorInvalidValue;
+    } else {
+        tv = tk;
+    }
+    ScanArgs a;
+    a.lqhi = w.lqhi;
+    a.lqlo = w.lqlo;
+    a.theta = level > 0 ? w.theta : nullptr;
+    a.part = w.part;
+    a.cand = w.cand;
+    a.ccount = w.ccount;
+    a.status = w.status;
+    a.S = L.S;
+    a.stride = L.stride;
+    a.chunk_len = L.chunk_len;
+    a.chunks = L.chunks;
+    a.cap = L.cap;
+    a.m = p.s.m;
+    a.k = p.s.k;
+    const bool two = p.s.m > 128;
+    if (full) return two ? launch_one<true, 2>(tk, tv, a, p.s.BH, st) : launch_one<true, 1>(tk, tv, a, p.s.BH, st);
+    return two ? launch_one<false, 2>(tk, tv, a, p.s.BH, st) : launch_one<false, 1>(tk, tv, a, p.s.BH, st);
+}
+
+}  // namespace mita

@@ -9,6 +9,10 @@
 //    ascending order (bitonic sort in shared memory).
 // Each chunk's buffer holds at least min(chunk length, k) of its best keys,
 // so the union always contains the global top k.
+//
+// The pilot variant (after a scan of a strided key sample) only finds each
+// landmark's k-th largest sample key and raises the landmark's threshold to
+// it: k keys of the head reach that value, so the true k-th best does too.
 #include "mita_internal.cuh"
 
 namespace mita {
@@ -17,12 +21,13 @@ namespace {
 
 constexpr int ST = 256;  // threads per CTA
 
+template <bool PILOT>
 __global__ void __launch_bounds__(ST) select_kernel(int m, int k, int chunks, int cap,
                                                     const float* __restrict__ part,
                                                     const uint64_t* __restrict__ cand,
                                                     const int* __restrict__ ccount, float* __restrict__ lv32,
                                                     __nv_bfloat16* __restrict__ lvbf,
-                                                    int32_t* __restrict__ expert_idx) {
+                                                    int32_t* __restrict__ expert_idx, uint64_t* __restrict__ theta) {
     __shared__ unsigned hist[256];
     __shared__ int cnts[64];
     __shared__ int sel[MITA_SORT_MAX];
@@ -35,7 +40,7 @@ __global__ void __launch_bounds__(ST) select_kernel(int m, int k, int chunks, in
     const int tid = threadIdx.x;
 
     // ---- shared-expert value ------------------------------------------------
-    if (tid < D) {
+    if (!PILOT && tid < D) {
         float M = -INFINITY;
         for (int c = 0; c < chunks; ++c) M = fmaxf(M, part[((bh * chunks + c) * m + i) * 68]);
         float L = 0.f, O = 0.f;
@@ -63,7 +68,7 @@ __global__ void __launch_bounds__(ST) select_kernel(int m, int k, int chunks, in
     auto buf_of = [&](int c) { return cand + ((bh * chunks + c) * m + i) * static_cast<int64_t>(cap); };
 
     uint64_t kth = 0;  // keep every key >= kth
-    if (total > k) {
+    if (total > k || (PILOT && total == k)) {
         uint64_t prefix = 0, mask = 0;
         unsigned remaining = static_cast<unsigned>(k);
         for (int shift = 56; shift >= 0; shift -= 8) {
@@ -113,6 +118,13 @@ __global__ void __launch_bounds__(ST) select_kernel(int m, int k, int chunks, in
         }
         kth = prefix;
     }
+    if (PILOT) {
+        if (tid == 0 && total >= k) {
+            const uint64_t old = theta[bh * m + i];
+            theta[bh * m + i] = kth > old ? kth : old;
+        }
+        return;
+    }
 
     // ---- gather the selected indices and sort them ascending ----------------
     if (tid == 0) nsel = 0;
@@ -153,8 +165,17 @@ __global__ void __launch_bounds__(ST) select_kernel(int m, int k, int chunks, in
 
 cudaError_t launch_select(const Plan& p, const Work& w, int32_t* expert_idx, cudaStream_t st) {
     const unsigned grid = static_cast<unsigned>(p.s.BH * p.s.m);
-    select_kernel<<<grid, ST, 0, st>>>(p.s.m, p.s.k, p.chunks, p.cap, w.part, w.cand, w.ccount, w.lv32, w.lvbf,
-                                      expert_idx);
+    const ScanLevel& L = p.lev[p.nlev - 1];
+    select_kernel<false><<<grid, ST, 0, st>>>(p.s.m, p.s.k, L.chunks, L.cap, w.part, w.cand, w.ccount, w.lv32,
+                                             w.lvbf, expert_idx, nullptr);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_pilot_select(const Plan& p, const Work& w, int level, cudaStream_t st) {
+    const unsigned grid = static_cast<unsigned>(p.s.BH * p.s.m);
+    const ScanLevel& L = p.lev[level];
+    select_kernel<true><<<grid, ST, 0, st>>>(p.s.m, p.s.k, L.chunks, L.cap, nullptr, w.cand, w.ccount, nullptr,
+                                            nullptr, nullptr, w.theta);
     return cudaGetLastError();
 }
 

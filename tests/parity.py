@@ -9,7 +9,10 @@
 * Outputs: compared with the oracle conditioned on the GPU's own routes and
   expert sets (so legal near-tie choices cost nothing): max-abs <= 2e-2 and
   mean-abs <= 2e-3 over all compared elements.
-* Lq and LV (diagnostic): within 1e-4 and 2e-3 of the oracle.
+* Lq and LV (diagnostic): within 1e-4 and 1e-2 of the oracle. LV's bound
+  comes from the tensor-core P.V product: the softmax weights enter it as
+  bf16 (relative rounding 2^-9 each), so |LV error| <= max|V| * 2^-8 or so,
+  about 1e-2 for unit-normal values.
 All gaps and logits are tau-scaled, tau = 1/sqrt(d).
 """
 from __future__ import annotations
@@ -20,7 +23,7 @@ import synth
 
 GAP = 1e-3
 OUT_MAX, OUT_MEAN = 2e-2, 2e-3
-LQ_TOL, LV_TOL = 1e-4, 2e-3
+LQ_TOL, LV_TOL = 1e-4, 1e-2
 
 
 def to_device(a):

@@ -138,3 +138,19 @@ def test_repeatable(orc):
     torch.cuda.synchronize()
     for x, y in zip(a, b):
         assert torch.equal(x, y)
+
+
+def test_pilot_blind_spot_forces_compaction(orc):
+    """Every key at an odd index outscores every key at an even index. At
+    N = 65536 the pilot samples are strided by even steps, so they see only
+    the weaker half and leave a low threshold: the main scan's candidate
+    buffers overflow and must compact, and the result must still be exact."""
+    B, H, N, m, k = 1, 1, 65536, 4, 64
+    noise = synth.bf16_to_f64(synth.normal_bf16((B, H, N, 64), 41, 0))
+    q = synth.f64_to_bf16(1.0 + 0.1 * noise)
+    sign = np.where(np.arange(N) % 2 == 1, 1.0, -1.0)[None, None, :, None]
+    kn = synth.bf16_to_f64(synth.normal_bf16((B, H, N, 64), 41, 1))
+    kk_ = synth.f64_to_bf16(0.5 * sign + 0.05 * kn)
+    v = synth.normal_bf16((B, H, N, 64), 41, 2)
+    rep = parity.full_parity(orc, q, kk_, v, 0, 0, m, k)
+    print(rep)
