@@ -128,6 +128,11 @@ int device_sms() {
     return n;
 }
 
+cudaError_t launch_route(const Plan& p, const Work& w, const __nv_bfloat16* Q, int32_t* route, cudaStream_t st) {
+    if (route_tc_supported(p)) return launch_route_tc(p, w, Q, route, st);
+    return launch_route_simt(p, w, Q, route, st);
+}
+
 cudaError_t launch_expert(const Plan& p, const Work& w, const __nv_bfloat16* Q, const __nv_bfloat16* K,
                           const __nv_bfloat16* V, const int32_t* expert_idx, __nv_bfloat16* out, cudaStream_t st) {
     // tensor cores when the experts hold enough queries to fill 128-row tiles

@@ -135,6 +135,10 @@ cudaError_t launch_scan_tc(const Plan& p, const Work& w, const __nv_bfloat16* K,
 cudaError_t launch_select(const Plan& p, const Work& w, int32_t* expert_idx, cudaStream_t st);
 cudaError_t launch_pilot_select(const Plan& p, const Work& w, int level, cudaStream_t st);
 cudaError_t launch_route(const Plan& p, const Work& w, const __nv_bfloat16* Q, int32_t* route, cudaStream_t st);
+cudaError_t launch_route_simt(const Plan& p, const Work& w, const __nv_bfloat16* Q, int32_t* route,
+                              cudaStream_t st);
+cudaError_t launch_route_tc(const Plan& p, const Work& w, const __nv_bfloat16* Q, int32_t* route, cudaStream_t st);
+bool route_tc_supported(const Plan& p);
 cudaError_t launch_group(const Plan& p, const Work& w, const int32_t* route, cudaStream_t st);
 cudaError_t launch_expert(const Plan& p, const Work& w, const __nv_bfloat16* Q, const __nv_bfloat16* K,
                           const __nv_bfloat16* V, const int32_t* expert_idx, __nv_bfloat16* out, cudaStream_t st);

@@ -72,7 +72,7 @@ __global__ void __launch_bounds__(RT) route_simt_kernel(const __nv_bfloat16* __r
 
 }  // namespace
 
-cudaError_t launch_route(const Plan& p, const Work& w, const __nv_bfloat16* Q, int32_t* route, cudaStream_t st) {
+cudaError_t launch_route_simt(const Plan& p, const Work& w, const __nv_bfloat16* Q, int32_t* route, cudaStream_t st) {
     const int64_t nblocks = (p.s.N + RT - 1) / RT;
     const unsigned grid = static_cast<unsigned>(p.s.BH * nblocks);
     route_simt_kernel<<<grid, RT, 0, st>>>(Q, p.s.N, p.s.m, nblocks, w.lq32, route, w.counts);

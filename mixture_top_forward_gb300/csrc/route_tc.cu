@@ -1,0 +1,204 @@
+// Stage 3 on the tensor cores: routing.
+//
+// "NeurIPS 2026 | Mixture-of-Top-k 注意力" (shuwu5.cn), section
+// "MiTA：用少量地标查询，同时完成压缩与专家构造": each query picks the expert of
+// the landmark query it matches best (s = 1), reusing the query-to-landmark
+// logits: e(n) = argmax_i <q_n, Lq_i> (tau > 0 does not change the argmax),
+// ties to the lowest i.
+//
+// Persistent CTAs, each over a contiguous range of 128-query tiles (so the
+// head, and with it the landmark operand, changes rarely).
+//   warp 4 lane 0: TMA loads of Q tiles (4-stage ring) and of the head's
+//                  landmark queries (bf16 hi/lo pair, m_pad <= 256 rows), and
+//                  the MMAs D = Q Lq_hi^T + Q Lq_lo^T (M = 128, N = m_pad,
+//                  exact to ~2^-16 of the fp32 landmarks) into one of two TMEM
+//                  buffers;
+//   warps 0-3:     one query row per thread: argmax over the m logits, the
+//                  route, and a shared-memory histogram of the head's routes
+//                  that is added to the per-head expert counts.
+// Every wait is bounded (umma.cuh).
+#include <algorithm>
+
+#include "tensormap.cuh"
+#include "umma.cuh"
+
+namespace mita {
+
+namespace {
+
+using namespace umma;
+
+constexpr int QST = 4;  // Q tile stages
+constexpr size_t OFF_LO = 32768;
+constexpr size_t OFF_Q = 65536;
+constexpr size_t SMEM = OFF_Q + QST * 16384 + 1024;
+
+struct RouteArgs {
+    int32_t* route;
+    int* counts;
+    int* status;
+    int64_t N, tiles_per_head, total_tiles;
+    int m, m_pad;
+};
+
+__global__ void __launch_bounds__(160, 1) route_tc_kernel(const __grid_constant__ CUtensorMap tq,
+                                                          const __grid_constant__ CUtensorMap thi,
+                                                          const __grid_constant__ CUtensorMap tlo, RouteArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ uint64_t qfull[QST], qempty[QST], dfull[2], dfree[2], lqbar;
+    __shared__ uint32_t tmem_base;
+    __shared__ int hist[256];
+    uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int64_t t0 = a.total_tiles * blockIdx.x / gridDim.x;
+    const int64_t t1 = a.total_tiles * (blockIdx.x + 1) / gridDim.x;
+    const int nt = static_cast<int>(t1 - t0);
+
+    if (tid == 0) {
+        for (int i = 0; i < QST; ++i) {
+            mbar_init(&qfull[i], 1);
+            mbar_init(&qempty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&dfull[i], 1);
+            mbar_init(&dfree[i], 1);
+        }
+        mbar_init(&lqbar, 1);
+        fence_barrier_init();
+    }
+    for (int e = tid; e < 256; e += blockDim.x) hist[e] = 0;
+    if (warp == 0) tmem_alloc(&tmem_base, 512);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tb = tmem_base;
+
+    if (warp == 4) {
+        if (lane == 0) {
+            const uint32_t idesc = idesc_bf16(128, a.m_pad, false);
+            const uint32_t hi = smem_u32(base), lo = smem_u32(base + OFF_LO);
+            auto load_q = [&](int t) {
+                const int st = t % QST;
+                const int64_t g = t0 + t;
+                const int64_t bh = g / a.tiles_per_head, tile = g % a.tiles_per_head;
+                mbar_arrive_expect_tx(&qfull[st], 16384);
+                tma_load_2d(base + OFF_Q + st * 16384, &tq, 0, static_cast<int>(bh * a.N + tile * 128), &qfull[st]);
+            };
+            for (int t = 0; t < nt && t < QST; ++t) load_q(t);
+            int64_t cur = -1;
+            uint32_t lq_phase = 0;
+            for (int t = 0; t < nt; ++t) {
+                const int64_t bh = (t0 + t) / a.tiles_per_head;
+                if (bh != cur) {  // restage the landmarks once the MMAs reading them are done
+                    if (t > 0 && !mbar_wait(&dfull[(t - 1) & 1], ((t - 1) >> 1) & 1, a.status)) break;
+                    mbar_arrive_expect_tx(&lqbar, 2u * a.m_pad * 128u);
+                    tma_load_2d(base, &thi, 0, static_cast<int>(bh * a.m), &lqbar);
+                    tma_load_2d(base + OFF_LO, &tlo, 0, static_cast<int>(bh * a.m), &lqbar);
+                    if (!mbar_wait(&lqbar, lq_phase, a.status)) break;
+                    lq_phase ^= 1;
+                    cur = bh;
+                }
+                const int st = t % QST;
+                if (!mbar_wait(&qfull[st], (t / QST) & 1, a.status)) break;
+                if (t >= 2 && !mbar_wait(&dfree[t & 1], ((t >> 1) - 1) & 1, a.status)) break;
+                tc_fence_after();
+                const uint32_t qa = smem_u32(base + OFF_Q + st * 16384);
+                const uint32_t d = tb + (t & 1) * 256;
+#pragma unroll
+                for (int s = 0; s < 4; ++s)
+                    mma_ss(d, sdesc_sw128(qa + s * 32), sdesc_sw128(hi + s * 32), idesc, s > 0);
+#pragma unroll
+                for (int s = 0; s < 4; ++s) mma_ss(d, sdesc_sw128(qa + s * 32), sdesc_sw128(lo + s * 32), idesc, 1u);
+                mma_commit(&dfull[t & 1]);
+                mma_commit(&qempty[st]);
+                // refill the stage of the previous tile (its MMAs were issued earlier)
+                if (t >= 1 && t - 1 + QST < nt) {
+                    const int ps = (t - 1) % QST;
+                    if (!mbar_wait(&qempty[ps], ((t - 1) / QST) & 1, a.status)) break;
+                    load_q(t - 1 + QST);
+                }
+            }
+        }
+    } else {
+        // ---------------- argmax warpgroup (warps 0-3) ----------------
+        const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+        int64_t cur = -1;
+        for (int t = 0; t < nt; ++t) {
+            const int64_t g = t0 + t;
+            const int64_t bh = g / a.tiles_per_head, tile = g % a.tiles_per_head;
+            if (bh != cur) {
+                named_bar(1, 128);
+                if (cur >= 0)
+                    for (int e = tid; e < a.m; e += 128)
+                        if (hist[e]) atomicAdd(&a.counts[cur * a.m + e], hist[e]);
+                named_bar(1, 128);
+                for (int e = tid; e < a.m; e += 128) hist[e] = 0;
+                cur = bh;
+            }
+            if (!named_bar_and(1, 128, mbar_wait(&dfull[t & 1], (t >> 1) & 1, a.status))) {
+                cur = -1;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t d = tb + (t & 1) * 256 + lane_off;
+            float best = -INFINITY;
+            int arg = 0;
+            for (int c0 = 0; c0 < a.m_pad; c0 += 32) {
+                float v[32];
+                tmem_ld32(d + c0, v);
+                tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    if (c0 + j < a.m && v[j] > best) {
+                        best = v[j];
+                        arg = c0 + j;
+                    }
+                }
+            }
+            tc_fence_before();
+            named_bar(1, 128);
+            if (tid == 0) mbar_arrive(&dfree[t & 1]);
+            const int64_t n = tile * 128 + tid;
+            if (n < a.N) {
+                a.route[bh * a.N + n] = arg;
+                atomicAdd(&hist[arg], 1);
+            }
+        }
+        named_bar(1, 128);
+        if (cur >= 0)
+            for (int e = tid; e < a.m; e += 128)
+                if (hist[e]) atomicAdd(&a.counts[cur * a.m + e], hist[e]);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_free(tb, 512);
+}
+
+}  // namespace
+
+bool route_tc_supported(const Plan& p) { return p.s.m <= 256 && p.s.BH * p.s.N < (int64_t(1) << 31); }
+
+cudaError_t launch_route_tc(const Plan& p, const Work& w, const __nv_bfloat16* Q, int32_t* route, cudaStream_t st) {
+    RouteArgs a;
+    a.route = route;
+    a.counts = w.counts;
+    a.status = w.status;
+    a.N = p.s.N;
+    a.tiles_per_head = (p.s.N + 127) / 128;
+    a.total_tiles = a.tiles_per_head * p.s.BH;
+    a.m = p.s.m;
+    a.m_pad = (p.s.m + 15) / 16 * 16;
+    CUtensorMap tq, thi, tlo;
+    const uint64_t mrows = static_cast<uint64_t>(p.s.BH) * p.s.m;
+    if (!make_row_tmap(&tq, Q, static_cast<uint64_t>(p.s.BH * p.s.N), 128) ||
+        !make_row_tmap(&thi, w.lqhi, mrows, a.m_pad) || !make_row_tmap(&tlo, w.lqlo, mrows, a.m_pad))
+        return cudaErrorInvalidValue;
+    cudaError_t e = cudaFuncSetAttribute(route_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(SMEM));
+    if (e != cudaSuccess) return e;
+    const int64_t grid = std::min<int64_t>(device_sms(), a.total_tiles);
+    route_tc_kernel<<<static_cast<unsigned>(grid), 160, SMEM, st>>>(tq, thi, tlo, a);
+    return cudaGetLastError();
+}
+
+}  // namespace mita
