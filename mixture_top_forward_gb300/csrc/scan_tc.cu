@@ -12,12 +12,13 @@
 // hi = bf16(Lq), lo = bf16(Lq - hi), so that S = Lq_hi K^T + Lq_lo K^T (two
 // accumulating MMAs) matches the fp32 landmark to ~2^-16 relative: exact
 // enough for the top-k comparisons.
-//   warp 0 lane 0: TMA producer of 128-key tiles of K (3-4 stage ring);
-//   warp 3 lane 0: TMA producer of V tiles (2-3 stages; full scans only);
+//   warp 0:        TMEM allocation; lane 0: TMA producer of 128-key tiles of
+//                  K (3-4 stage ring); lane 1: TMA producer of V tiles (2-3
+//                  stages; full scans only);
 //   warp 1 lane 0: MMA issuer: S_L = Lq_L K^T into TMEM per landmark tile L,
 //                  and one tile later O_L += P_L V (full scans only);
-//   warp 2:        TMEM allocation;
-//   warps 4..:     one warpgroup per landmark tile, one thread per landmark.
+//   warps 2..:     one warpgroup (4 consecutive warps: warp w reads TMEM lane
+//                  quarter w % 4) per landmark tile, one thread per landmark.
 //                  A thread loads its 128 scores, offers them to its
 //                  landmark's candidate buffer (topk.cuh: append when the
 //                  64-bit order key reaches the threshold, warp-cooperative
@@ -42,7 +43,7 @@ using namespace umma;
 
 constexpr float kC = 0.125f * kLog2e;  // tau * log2(e)
 constexpr float kLazy = 8.0f;
-constexpr uint32_t kIdescS = idesc_bf16(128, 128, false);
+constexpr uint32_t kIdescS = idesc_bf16(128, 64, false);
 constexpr uint32_t kIdescPV = idesc_bf16(128, 64, true);
 
 struct ScanArgs {
@@ -61,16 +62,19 @@ struct ScanArgs {
 
 template <bool FULL, int NL>
 struct Cfg {
-    static constexpr int KST = FULL ? (NL == 2 ? 3 : 4) : 4;  // K ring stages
-    static constexpr int VST = FULL ? (NL == 2 ? 2 : 3) : 0;  // V ring stages
-    static constexpr int NT = 128 + NL * 128;
+    static constexpr int KT = 64;                     // keys per tile
+    static constexpr int TB = KT * 128;               // bytes of one K or V tile
+    static constexpr int KST = 6;                     // K ring stages
+    static constexpr int VST = FULL ? 4 : 0;          // V ring stages
+    static constexpr int NT = 64 + NL * 128;
     static constexpr size_t OFF_LQLO = NL * 16384;
     static constexpr size_t OFF_K = 2 * NL * 16384;
-    static constexpr size_t OFF_V = OFF_K + KST * 16384;
-    static constexpr size_t OFF_P = OFF_V + VST * 16384;
-    static constexpr size_t OFF_HIST = OFF_P + (FULL ? NL * 32768 : 0);
+    static constexpr size_t OFF_V = OFF_K + KST * TB;
+    static constexpr size_t OFF_P = OFF_V + VST * TB;  // [NL][2] tiles of 128 x 64 bf16
+    static constexpr size_t OFF_HIST = OFF_P + (FULL ? NL * 2 * 16384 : 0);
     static constexpr size_t SMEM = OFF_HIST + NL * 4 * 1024 + 1024;
-    static constexpr uint32_t TCOLS = NL * 256;  // per tile L: S at L*256, O at L*256 + 128
+    // TMEM per landmark tile L (256 columns apart): S buffers at +0 and +64, O at +128
+    static constexpr uint32_t TCOLS = NL * 256;
 };
 
 // Score of an order key (the inverse of topk_key's float mapping); -inf for 0.
@@ -81,25 +85,30 @@ __device__ __forceinline__ float key_score(uint64_t key) {
     return __uint_as_float(u);
 }
 
-// Issues O_L += P_L V for every landmark tile L of key tile i (MMA thread).
+struct Bars {
+    uint64_t* vfull;
+    uint64_t* vempty;
+    uint64_t* pfull;   // [NL][2]
+    uint64_t* pvdone;  // [NL][2]
+};
+
+// Issues O_L += P_L(i) V(i) for every landmark tile L of key tile i (MMA thread).
 template <class C, int NL>
-__device__ __forceinline__ bool issue_pv(const ScanArgs& a, uint8_t* base, uint32_t tb, int i, uint64_t* vfull,
-                                         uint64_t* vempty, uint64_t* pfull, uint64_t* pvdone) {
-    const int vs = i % C::VST;
-    if (!mbar_wait(&vfull[vs], (i / C::VST) & 1, a.status)) return false;
-    const uint32_t va = smem_u32(base + C::OFF_V + vs * 16384);
+__device__ __forceinline__ bool issue_pv(const ScanArgs& a, uint8_t* base, uint32_t tb, int i, const Bars& b) {
+    const int vs = i % C::VST, pbuf = i & 1;
+    if (!mbar_wait(&b.vfull[vs], (i / C::VST) & 1, a.status)) return false;
+    const uint32_t va = smem_u32(base + C::OFF_V + vs * C::TB);
     for (int l = 0; l < NL; ++l) {
-        if (!mbar_wait(&pfull[l], i & 1, a.status)) return false;
+        if (!mbar_wait(&b.pfull[l * 2 + pbuf], (i >> 1) & 1, a.status)) return false;
         tc_fence_after();
-        const uint32_t pa = smem_u32(base + C::OFF_P + l * 32768);
+        const uint32_t pa = smem_u32(base + C::OFF_P + (l * 2 + pbuf) * 16384);
         const uint32_t tO = tb + l * 256 + 128;
 #pragma unroll
-        for (int s = 0; s < 8; ++s)
-            mma_ss(tO, sdesc_sw128(pa + (s >> 2) * 16384 + (s & 3) * 32), sdesc_sw128(va + s * 2048), kIdescPV,
-                   (i > 0 || s > 0) ? 1u : 0u);
-        mma_commit(&pvdone[l]);
+        for (int s = 0; s < 4; ++s)
+            mma_ss(tO, sdesc_sw128(pa + s * 32), sdesc_sw128(va + s * 2048), kIdescPV, (i > 0 || s > 0) ? 1u : 0u);
+        mma_commit(&b.pvdone[l * 2 + pbuf]);
     }
-    mma_commit(&vempty[vs]);
+    mma_commit(&b.vempty[vs]);
     return true;
 }
 
@@ -107,10 +116,11 @@ template <bool FULL, int NL>
 __global__ void __launch_bounds__(Cfg<FULL, NL>::NT, 1)
     scan_tc_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv, ScanArgs a) {
     using C = Cfg<FULL, NL>;
+    constexpr int KT = C::KT;
     extern __shared__ uint8_t smem_raw[];
     __shared__ uint64_t kfull[C::KST], kempty[C::KST];
     __shared__ uint64_t vfull[C::VST > 0 ? C::VST : 1], vempty[C::VST > 0 ? C::VST : 1];
-    __shared__ uint64_t sfull[NL], sfree[NL], pfull[NL], pvdone[NL];
+    __shared__ uint64_t sfull[NL * 2], sfree[NL * 2], pfull[NL * 2], pvdone[NL * 2];
     __shared__ uint32_t tmem_base;
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
@@ -119,7 +129,7 @@ __global__ void __launch_bounds__(Cfg<FULL, NL>::NT, 1)
     const int64_t bh = blockIdx.x / static_cast<unsigned>(a.chunks);
     const int64_t s0 = static_cast<int64_t>(c) * a.chunk_len;
     const int64_t s1 = min(a.S, s0 + a.chunk_len);
-    const int T = static_cast<int>((s1 - s0 + 127) / 128);
+    const int T = static_cast<int>((s1 - s0 + KT - 1) / KT);
 
     if (tid == 0) {
         for (int i = 0; i < C::KST; ++i) {
@@ -130,7 +140,7 @@ __global__ void __launch_bounds__(Cfg<FULL, NL>::NT, 1)
             mbar_init(&vfull[i], 1);
             mbar_init(&vempty[i], 1);
         }
-        for (int l = 0; l < NL; ++l) {
+        for (int l = 0; l < NL * 2; ++l) {
             mbar_init(&sfull[l], 1);
             mbar_init(&sfree[l], 1);
             mbar_init(&pfull[l], 1);
@@ -138,7 +148,7 @@ __global__ void __launch_bounds__(Cfg<FULL, NL>::NT, 1)
         }
         fence_barrier_init();
     }
-    if (warp == 2) tmem_alloc(&tmem_base, C::TCOLS);
+    if (warp == 0) tmem_alloc(&tmem_base, C::TCOLS);
     {   // landmark queries of this head, hi and lo, rows >= m zero
         const uint32_t hb = smem_u32(base), lb = smem_u32(base + C::OFF_LQLO);
         for (int x = tid; x < NL * 128 * 8; x += C::NT) {
@@ -160,30 +170,30 @@ __global__ void __launch_bounds__(Cfg<FULL, NL>::NT, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tb = tmem_base;
+    const Bars bars{vfull, vempty, pfull, pvdone};
 
     if (warp == 0) {
-        // ---------------- K producer ----------------
+        // ---------------- K producer (lane 0) ----------------
         if (lane == 0) {
             for (int i = 0; i < T; ++i) {
                 const int st = i % C::KST;
                 if (i >= C::KST && !mbar_wait(&kempty[st], ((i / C::KST) & 1) ^ 1, a.status)) break;
-                mbar_arrive_expect_tx(&kfull[st], 16384);
-                tma_load_3d(base + C::OFF_K + st * 16384, &tk, 0, static_cast<int>(s0 + i * 128),
+                mbar_arrive_expect_tx(&kfull[st], C::TB);
+                tma_load_3d(base + C::OFF_K + st * C::TB, &tk, 0, static_cast<int>(s0 + i * KT),
                             static_cast<int>(bh), &kfull[st]);
             }
         }
-    } else if (warp == 3) {
-        // ---------------- V producer ----------------
         if constexpr (FULL) {
-          if (lane == 0) {
-            for (int i = 0; i < T; ++i) {
-                const int st = i % C::VST;
-                if (i >= C::VST && !mbar_wait(&vempty[st], ((i / C::VST) & 1) ^ 1, a.status)) break;
-                mbar_arrive_expect_tx(&vfull[st], 16384);
-                tma_load_3d(base + C::OFF_V + st * 16384, &tv, 0, static_cast<int>(s0 + i * 128),
-                            static_cast<int>(bh), &vfull[st]);
+            // ---------------- V producer (lane 1) ----------------
+            if (lane == 1) {
+                for (int i = 0; i < T; ++i) {
+                    const int st = i % C::VST;
+                    if (i >= C::VST && !mbar_wait(&vempty[st], ((i / C::VST) & 1) ^ 1, a.status)) break;
+                    mbar_arrive_expect_tx(&vfull[st], C::TB);
+                    tma_load_3d(base + C::OFF_V + st * C::TB, &tv, 0, static_cast<int>(s0 + i * KT),
+                                static_cast<int>(bh), &vfull[st]);
+                }
             }
-          }
         }
     } else if (warp == 1) {
         // ---------------- MMA issuer ----------------
@@ -191,68 +201,85 @@ __global__ void __launch_bounds__(Cfg<FULL, NL>::NT, 1)
             const uint32_t hi = smem_u32(base), lo = smem_u32(base + C::OFF_LQLO);
             bool ok = true;
             for (int i = 0; i < T && ok; ++i) {
-                const int st = i % C::KST;
+                const int st = i % C::KST, sb = i & 1;
                 if (!mbar_wait(&kfull[st], (i / C::KST) & 1, a.status)) break;
                 tc_fence_after();
-                const uint32_t ka = smem_u32(base + C::OFF_K + st * 16384);
+                const uint32_t ka = smem_u32(base + C::OFF_K + st * C::TB);
                 for (int l = 0; l < NL && ok; ++l) {
-                    if (i > 0) {
-                        if (!mbar_wait(&sfree[l], (i - 1) & 1, a.status)) {
+                    if (i >= 2) {  // the rows have read S buffer sb of tile i-2
+                        if (!mbar_wait(&sfree[l * 2 + sb], ((i >> 1) - 1) & 1, a.status)) {
                             ok = false;
                             break;
                         }
                         tc_fence_after();
                     }
-                    const uint32_t tS = tb + l * 256;
+                    const uint32_t tS = tb + l * 256 + sb * KT;
 #pragma unroll
                     for (int s = 0; s < 4; ++s)
                         mma_ss(tS, sdesc_sw128(hi + l * 16384 + s * 32), sdesc_sw128(ka + s * 32), kIdescS, s > 0);
 #pragma unroll
                     for (int s = 0; s < 4; ++s)
                         mma_ss(tS, sdesc_sw128(lo + l * 16384 + s * 32), sdesc_sw128(ka + s * 32), kIdescS, 1u);
-                    mma_commit(&sfull[l]);
+                    mma_commit(&sfull[l * 2 + sb]);
                 }
                 if (!ok) break;
                 mma_commit(&kempty[st]);
                 if constexpr (FULL) {
-                    if (i > 0) ok = issue_pv<C, NL>(a, base, tb, i - 1, vfull, vempty, pfull, pvdone);
+                    if (i > 0) ok = issue_pv<C, NL>(a, base, tb, i - 1, bars);
                 }
             }
             if constexpr (FULL) {
-                if (ok && T > 0) issue_pv<C, NL>(a, base, tb, T - 1, vfull, vempty, pfull, pvdone);
+                if (ok && T > 0) issue_pv<C, NL>(a, base, tb, T - 1, bars);
             }
         }
-    } else if (warp >= 4) {
+    } else {
         // ---------------- landmark rows: top-k filter and softmax ----------------
-        const int L = (warp - 4) >> 2;
-        const int t = tid - 128 - L * 128;
+        const int L = (warp - 2) >> 2;
+        const int t = (warp & 3) * 32 + lane;  // TMEM lane = landmark row in the tile
         const int li = L * 128 + t;
         const bool row_ok = li < a.m;
         const int bar_id = 1 + L;
         const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-        const uint32_t tS = tb + L * 256, tO = tS + 128;
+        const uint32_t tO = tb + L * 256 + 128;
         const int64_t slot = (bh * a.chunks + c) * a.m + (row_ok ? li : 0);
         uint64_t* buf = a.cand + slot * static_cast<int64_t>(a.cap);
         uint64_t theta = (a.theta && row_ok) ? a.theta[bh * a.m + li] : 0;
         float theta_s = key_score(theta);
         int cnt = 0;
-        unsigned* hist = reinterpret_cast<unsigned*>(base + C::OFF_HIST + (warp - 4) * 1024);
-        uint8_t* pb = base + C::OFF_P + L * 32768;
+        unsigned* hist = reinterpret_cast<unsigned*>(base + C::OFF_HIST + (warp - 2) * 1024);
         float mrun = -INFINITY, lrun = 0.f;
         bool ok = true;
         for (int i = 0; i < T; ++i) {
-            ok = named_bar_and(bar_id, 128, mbar_wait(&sfull[L], i & 1, a.status));
+            const int sb = i & 1;
+            ok = named_bar_and(bar_id, 128, mbar_wait(&sfull[L * 2 + sb], (i >> 1) & 1, a.status));
             if (!ok) break;
             tc_fence_after();
-            float s[128];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) tmem_ld32(tS + lane_off + q * 32, s + q * 32);
+            float s[KT];
+            tmem_ld32(tb + L * 256 + sb * KT + lane_off, s);
+            tmem_ld32(tb + L * 256 + sb * KT + lane_off + 32, s + 32);
             tmem_ld_wait();
             tc_fence_before();
             named_bar(bar_id, 128);
-            if (t == 0) mbar_arrive(&sfree[L]);
-            const int64_t col0 = s0 + static_cast<int64_t>(i) * 128;
-            const int nvalid = static_cast<int>(s1 - col0 < 128 ? s1 - col0 : 128);
+            if (t == 0) mbar_arrive(&sfree[L * 2 + sb]);
+            const int64_t col0 = s0 + static_cast<int64_t>(i) * KT;
+            const int nvalid = static_cast<int>(s1 - col0 < KT ? s1 - col0 : KT);
+            if (nvalid < KT) {  // last, partial tile of the chunk (warp-uniform)
+#pragma unroll
+                for (int col = 0; col < KT; ++col) s[col] = col < nvalid ? s[col] : -INFINITY;
+            }
+            // raw maxima per 16-column group; a group can only hold a candidate
+            // if its maximum reaches the threshold (s_raw >= 8 theta_s is exact:
+            // tau = 1/8 is a power of two)
+            float gm[KT / 16];
+            float bmax = -INFINITY;
+#pragma unroll
+            for (int g = 0; g < KT / 16; ++g) {
+                float x = s[16 * g];
+#pragma unroll
+                for (int j = 1; j < 16; ++j) x = fmaxf(x, s[16 * g + j]);
+                gm[g] = x;
+                bmax = fmaxf(bmax, x);
+            }
 
             // top-k candidates (compaction first if this tile could overflow a buffer)
             unsigned need = __ballot_sync(0xffffffffu, row_ok && cnt + nvalid > a.cap);
@@ -269,80 +296,97 @@ __global__ void __launch_bounds__(Cfg<FULL, NL>::NT, 1)
                     theta_s = key_score(kth);
                 }
             }
-            if (row_ok) {
+            // masked columns hold -inf: never let them through, even while the
+            // threshold is still -inf (every finite score passes -FLT_MAX)
+            const float thr = fmaxf(theta_s * 8.0f, -3.402823466e38f);
+            if (row_ok && bmax >= thr) {
 #pragma unroll
-                for (int col = 0; col < 128; ++col) {
-                    const float sc = s[col] * 0.125f;
-                    if (col < nvalid && sc >= theta_s) {
-                        const uint64_t key = topk_key(sc, static_cast<uint32_t>((col0 + col) * a.stride));
-                        if (key >= theta) buf[cnt++] = key;
+                for (int g = 0; g < KT / 16; ++g) {
+                    if (gm[g] >= thr) {
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            const int col = 16 * g + j;
+                            if (s[col] >= thr) {
+                                const uint64_t key =
+                                    topk_key(s[col] * 0.125f, static_cast<uint32_t>((col0 + col) * a.stride));
+                                if (key >= theta) buf[cnt++] = key;
+                            }
+                        }
                     }
                 }
             }
-            if (FULL) {
-                float bmax = -INFINITY;
-#pragma unroll
-                for (int col = 0; col < 128; ++col) {
-                    s[col] = col < nvalid ? s[col] * kC : -INFINITY;
-                    bmax = fmaxf(bmax, s[col]);
-                }
-                const float mnew = (bmax > mrun + kLazy) ? bmax : mrun;
+            if constexpr (FULL) {
+                const float bm2 = bmax * kC;
+                const float mnew = (bm2 > mrun + kLazy) ? bm2 : mrun;
                 const float alpha = exp2f(mrun - mnew);
                 float sum = 0.f;
 #pragma unroll
-                for (int col = 0; col < 128; ++col) {
-                    s[col] = exp2f(s[col] - mnew);
+                for (int col = 0; col < KT; ++col) {
+                    s[col] = exp2f(fmaf(s[col], kC, -mnew));
                     sum += s[col];
                 }
                 lrun = lrun * alpha + sum;
-                if (i > 0) {
-                    ok = named_bar_and(bar_id, 128, mbar_wait(&pvdone[L], (i - 1) & 1, a.status));
+                const int pb = L * 2 + sb;
+                // the P buffer of this tile was last read by PV(i-2); rescaling O
+                // (rare: the running max grew by more than 2^8) needs PV(i-1) done
+                const bool rescale = !named_bar_and(bar_id, 128, alpha == 1.f) && i > 0;
+                if (rescale) {
+                    ok = named_bar_and(bar_id, 128, mbar_wait(&pvdone[L * 2 + (sb ^ 1)], ((i - 1) >> 1) & 1, a.status));
                     if (!ok) break;
-                    tc_fence_after();
-                    if (__any_sync(0xffffffffu, alpha != 1.f)) {
-                        float o[32];
-#pragma unroll
-                        for (int h = 0; h < 2; ++h) {
-                            tmem_ld32(tO + lane_off + h * 32, o);
-                            tmem_ld_wait();
-#pragma unroll
-                            for (int q = 0; q < 32; ++q) o[q] *= alpha;
-                            tmem_st32(tO + lane_off + h * 32, o);
-                        }
-                        tmem_st_wait();
-                    }
                 }
+                if (i >= 2) {
+                    ok = named_bar_and(bar_id, 128, mbar_wait(&pvdone[pb], ((i >> 1) - 1) & 1, a.status));
+                    if (!ok) break;
+                }
+                tc_fence_after();
+                if (rescale) {
+                    float o[32];
 #pragma unroll
-                for (int g = 0; g < 16; ++g) {
+                    for (int h = 0; h < 2; ++h) {
+                        tmem_ld32(tO + lane_off + h * 32, o);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int q = 0; q < 32; ++q) o[q] *= alpha;
+                        tmem_st32(tO + lane_off + h * 32, o);
+                    }
+                    tmem_st_wait();
+                }
+                uint8_t* pdst = base + C::OFF_P + pb * 16384;
+#pragma unroll
+                for (int g = 0; g < KT / 8; ++g) {
                     uint4 pk;
                     __nv_bfloat162* h2 = reinterpret_cast<__nv_bfloat162*>(&pk);
 #pragma unroll
                     for (int u = 0; u < 4; ++u)
                         h2[u] = __floats2bfloat162_rn(s[8 * g + 2 * u], s[8 * g + 2 * u + 1]);
-                    *reinterpret_cast<uint4*>(pb + (g >> 3) * 16384 + swz128(t, g & 7)) = pk;
+                    *reinterpret_cast<uint4*>(pdst + swz128(t, g)) = pk;
                 }
                 fence_proxy_async();
                 tc_fence_before();
                 named_bar(bar_id, 128);
-                if (t == 0) mbar_arrive(&pfull[L]);
+                if (t == 0) mbar_arrive(&pfull[pb]);
                 mrun = mnew;
             }
         }
-        if (FULL && ok && T > 0) {
-            ok = named_bar_and(bar_id, 128, mbar_wait(&pvdone[L], (T - 1) & 1, a.status));
-            if (ok) {
-                tc_fence_after();
-                float o[64];
-                tmem_ld32(tO + lane_off, o);
-                tmem_ld32(tO + lane_off + 32, o + 32);
-                tmem_ld_wait();
-                if (row_ok) {
-                    float* pp = a.part + slot * 68;
-                    pp[0] = mrun / kLog2e;  // running max in natural-log units of tau <Lq, K>
-                    pp[1] = lrun;
+        if constexpr (FULL) {
+            if (ok && T > 0) {
+                ok = named_bar_and(bar_id, 128,
+                                   mbar_wait(&pvdone[L * 2 + ((T - 1) & 1)], ((T - 1) >> 1) & 1, a.status));
+                if (ok) {
+                    tc_fence_after();
+                    float o[64];
+                    tmem_ld32(tO + lane_off, o);
+                    tmem_ld32(tO + lane_off + 32, o + 32);
+                    tmem_ld_wait();
+                    if (row_ok) {
+                        float* pp = a.part + slot * 68;
+                        pp[0] = mrun / kLog2e;  // running max in natural-log units of tau <Lq, K>
+                        pp[1] = lrun;
 #pragma unroll
-                    for (int q = 0; q < 64; q += 4)
-                        *reinterpret_cast<float4*>(pp + 4 + q) = make_float4(o[q], o[q + 1], o[q + 2], o[q + 3]);
+                        for (int q = 0; q < 64; q += 4)
+                            *reinterpret_cast<float4*>(pp + 4 + q) =
+                                make_float4(o[q], o[q + 1], o[q + 2], o[q + 3]);
+                    }
                 }
             }
         }
@@ -350,7 +394,7 @@ __global__ void __launch_bounds__(Cfg<FULL, NL>::NT, 1)
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 2) tmem_free(tb, C::TCOLS);
+    if (warp == 0) tmem_free(tb, C::TCOLS);
 }
 
 template <bool FULL, int NL>
@@ -373,11 +417,11 @@ cudaError_t launch_scan_tc(const Plan& p, const Work& w, const __nv_bfloat16* K,
     const bool full = level == p.nlev - 1;
     CUtensorMap tk, tv;
     if (!make_head_tmap(&tk, K, static_cast<uint64_t>(L.S), static_cast<uint64_t>(p.s.BH),
-                        static_cast<uint64_t>(L.stride), static_cast<uint64_t>(p.s.N), 128))
+                        static_cast<uint64_t>(L.stride), static_cast<uint64_t>(p.s.N), 64))
         return cudaErrorInvalidValue;
     if (full) {
         if (!make_head_tmap(&tv, V, static_cast<uint64_t>(p.s.N), static_cast<uint64_t>(p.s.BH), 1,
-                            static_cast<uint64_t>(p.s.N), 128))
+                            static_cast<uint64_t>(p.s.N), 64))
             return cudaErrorInvalidValue;
     } else {
         tv = tk;
