@@ -142,8 +142,8 @@ __global__ void __launch_bounds__(Cfg<FULL, NL>::NT, 1)
         }
         for (int l = 0; l < NL * 2; ++l) {
             mbar_init(&sfull[l], 1);
-            mbar_init(&sfree[l], 1);
-            mbar_init(&pfull[l], 1);
+            mbar_init(&sfree[l], 128);  // every row thread arrives after reading S
+            mbar_init(&pfull[l], 128);  // every row thread arrives after writing its P row
             mbar_init(&pvdone[l], 1);
         }
         fence_barrier_init();
@@ -238,7 +238,6 @@ __global__ void __launch_bounds__(Cfg<FULL, NL>::NT, 1)
         const int t = (warp & 3) * 32 + lane;  // TMEM lane = landmark row in the tile
         const int li = L * 128 + t;
         const bool row_ok = li < a.m;
-        const int bar_id = 1 + L;
         const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
         const uint32_t tO = tb + L * 256 + 128;
         const int64_t slot = (bh * a.chunks + c) * a.m + (row_ok ? li : 0);
@@ -251,7 +250,9 @@ __global__ void __launch_bounds__(Cfg<FULL, NL>::NT, 1)
         bool ok = true;
         for (int i = 0; i < T; ++i) {
             const int sb = i & 1;
-            ok = named_bar_and(bar_id, 128, mbar_wait(&sfull[L * 2 + sb], (i >> 1) & 1, a.status));
+            // waits are made warp-uniform (TMEM loads and stores are warp-wide);
+            // the warps of the group run on their own, so nothing blocks unboundedly
+            ok = __all_sync(0xffffffffu, mbar_wait(&sfull[L * 2 + sb], (i >> 1) & 1, a.status));
             if (!ok) break;
             tc_fence_after();
             float s[KT];
@@ -259,8 +260,7 @@ __global__ void __launch_bounds__(Cfg<FULL, NL>::NT, 1)
             tmem_ld32(tb + L * 256 + sb * KT + lane_off + 32, s + 32);
             tmem_ld_wait();
             tc_fence_before();
-            named_bar(bar_id, 128);
-            if (t == 0) mbar_arrive(&sfree[L * 2 + sb]);
+            mbar_arrive(&sfree[L * 2 + sb]);
             const int64_t col0 = s0 + static_cast<int64_t>(i) * KT;
             const int nvalid = static_cast<int>(s1 - col0 < KT ? s1 - col0 : KT);
             if (nvalid < KT) {  // last, partial tile of the chunk (warp-uniform)
@@ -303,14 +303,18 @@ __global__ void __launch_bounds__(Cfg<FULL, NL>::NT, 1)
 #pragma unroll
                 for (int g = 0; g < KT / 16; ++g) {
                     if (gm[g] >= thr) {
+                        unsigned msk = 0;
 #pragma unroll
-                        for (int j = 0; j < 16; ++j) {
-                            const int col = 16 * g + j;
-                            if (s[col] >= thr) {
-                                const uint64_t key =
-                                    topk_key(s[col] * 0.125f, static_cast<uint32_t>((col0 + col) * a.stride));
-                                if (key >= theta) buf[cnt++] = key;
-                            }
+                        for (int j = 0; j < 16; ++j) msk |= (s[16 * g + j] >= thr ? 1u : 0u) << j;
+                        while (msk) {
+                            const int j = __ffs(msk) - 1;
+                            msk &= msk - 1;
+                            float v = s[16 * g];
+#pragma unroll
+                            for (int jj = 1; jj < 16; ++jj) v = (j == jj) ? s[16 * g + jj] : v;
+                            const uint64_t key =
+                                topk_key(v * 0.125f, static_cast<uint32_t>((col0 + 16 * g + j) * a.stride));
+                            if (key >= theta) buf[cnt++] = key;
                         }
                     }
                 }
@@ -327,15 +331,16 @@ __global__ void __launch_bounds__(Cfg<FULL, NL>::NT, 1)
                 }
                 lrun = lrun * alpha + sum;
                 const int pb = L * 2 + sb;
-                // the P buffer of this tile was last read by PV(i-2); rescaling O
-                // (rare: the running max grew by more than 2^8) needs PV(i-1) done
-                const bool rescale = !named_bar_and(bar_id, 128, alpha == 1.f) && i > 0;
+                // this warp's rows of O need rescaling only when a running max
+                // grew by more than 2^8 (rare); that needs PV(i-1) done
+                const bool rescale = i > 0 && __any_sync(0xffffffffu, alpha != 1.f);
                 if (rescale) {
-                    ok = named_bar_and(bar_id, 128, mbar_wait(&pvdone[L * 2 + (sb ^ 1)], ((i - 1) >> 1) & 1, a.status));
+                    ok = __all_sync(0xffffffffu,
+                                    mbar_wait(&pvdone[L * 2 + (sb ^ 1)], ((i - 1) >> 1) & 1, a.status));
                     if (!ok) break;
                 }
-                if (i >= 2) {
-                    ok = named_bar_and(bar_id, 128, mbar_wait(&pvdone[pb], ((i >> 1) - 1) & 1, a.status));
+                if (i >= 2) {  // the P buffer of this tile was last read by PV(i-2)
+                    ok = __all_sync(0xffffffffu, mbar_wait(&pvdone[pb], ((i >> 1) - 1) & 1, a.status));
                     if (!ok) break;
                 }
                 tc_fence_after();
@@ -363,15 +368,13 @@ __global__ void __launch_bounds__(Cfg<FULL, NL>::NT, 1)
                 }
                 fence_proxy_async();
                 tc_fence_before();
-                named_bar(bar_id, 128);
-                if (t == 0) mbar_arrive(&pfull[pb]);
+                mbar_arrive(&pfull[pb]);
                 mrun = mnew;
             }
         }
         if constexpr (FULL) {
             if (ok && T > 0) {
-                ok = named_bar_and(bar_id, 128,
-                                   mbar_wait(&pvdone[L * 2 + ((T - 1) & 1)], ((T - 1) >> 1) & 1, a.status));
+                ok = __all_sync(0xffffffffu, mbar_wait(&pvdone[L * 2 + ((T - 1) & 1)], ((T - 1) >> 1) & 1, a.status));
                 if (ok) {
                     tc_fence_after();
                     float o[64];
