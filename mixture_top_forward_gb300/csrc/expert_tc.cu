@@ -7,25 +7,32 @@
 // (K_j, V_j, j in E_e) under one softmax over all m+k logits; the page's
 // implementation groups queries by expert and combines by online softmax.
 //
-// Work: persistent CTAs walk a contiguous range of the flat, expert-ordered
-// item list (<= 128 queries of one expert per item). Whenever the expert
-// changes, the CTA stages the expert's key list [Lq_0..Lq_{m-1}, K_e] and
-// value list [LV_0..LV_{m-1}, V_e] (bf16, 128-byte swizzled rows, zero padded
-// to whole 128-row blocks) in shared memory with cp.async gathers. NWG
-// warpgroups each take one item of a round (consecutive items of the same
-// expert) and run it on their own:
-//   Q rows (gathered by the grouping permutation) -> shared memory;
-//   for each 128-key block j: S = Q . keys_j^T into TMEM (4 MMAs, K = 64);
-//   each thread owns one query row: it loads its 128 logits, updates the
-//   running max (kept while it grows by < 2^8, so O rarely needs rescaling),
-//   forms p = 2^(s tau log2e - max) in registers and writes P (bf16) to
-//   shared memory; O += P . values_j into TMEM (8 MMAs, N = 64).
-//   The next block's S MMA is issued as soon as every thread has read S.
-//   Epilogue: O / rowsum -> bf16 -> the query's output row.
-// MMAs are issued by one thread of the warpgroup and tracked with tcgen05
-// commits on mbarriers; every wait is bounded (umma.cuh), and its outcome is
-// made uniform over the warpgroup before anyone acts on it, so a timeout ends
-// the item in every thread and the kernel still reaches its TMEM release.
+// Persistent CTAs walk a contiguous range of the flat, expert-ordered item
+// list (<= 128 queries of one expert per item), in rounds of up to two items
+// of the same expert, one per row warpgroup. The expert's key list
+// [Lq_0..Lq_{m-1}, K_e] and value list [LV_0..LV_{m-1}, V_e] (bf16, 128-byte
+// swizzled rows, zero padded to whole 64-row blocks) stay in shared memory
+// while consecutive rounds share the expert.
+//   warp 0:         producer: gathers the key/value lists when the expert
+//                   changes (the shared rows only when the head changes) and
+//                   each item's query rows (through the grouping permutation),
+//                   all with cp.async;
+//   warps 1, 2 (lane 0): one MMA issuer per warpgroup: per 64-key block j of its
+//                   item, S = Q keys_j^T into one of two TMEM buffers, and one
+//                   block later O += P_j values_j into the warpgroup's TMEM
+//                   accumulator;
+//   warps 3-6, 7-10: one warpgroup per item (4 consecutive warps cover the 4
+//                   TMEM lane quarters), one thread per query row: load the
+//                   64 logits, update the running max (kept while it grows by
+//                   < 2^8, so O rarely needs rescaling), p = 2^(s tau log2e -
+//                   max) in registers, P (bf16) into shared memory once the
+//                   previous block's P.V is done; at the end O / rowsum ->
+//                   bf16 -> the query's row. Query rows are double-buffered, so
+//                   the producer gathers the next item while this one runs.
+// Handshakes are mbarriers, each completed exactly once per event its waiter
+// consumes; row threads arrive individually (128-arrival barriers) and make
+// their waits warp-uniform, so no named barrier can block forever. Every
+// wait is bounded (umma.cuh).
 #include "umma.cuh"
 
 namespace mita {
@@ -36,7 +43,10 @@ using namespace umma;
 
 constexpr float kC = 0.125f * kLog2e;  // tau * log2(e), tau = 1/sqrt(64)
 constexpr float kLazy = 8.0f;          // keep the running max while the new one is within 2^8
-constexpr uint32_t kIdescS = idesc_bf16(128, 128, false);
+constexpr int KB = 64;                 // keys per block
+constexpr int NWG = 2;                 // row warpgroups
+constexpr int NT = 32 * (1 + NWG) + NWG * 128;  // producer, one issuer warp per group, rows
+constexpr uint32_t kIdescS = idesc_bf16(128, KB, false);
 constexpr uint32_t kIdescPV = idesc_bf16(128, 64, true);
 
 struct Args {
@@ -55,231 +65,332 @@ struct Args {
     int m, k, nblk;
 };
 
+struct Layout {
+    uint8_t* keys;  // nblk * 8 KB
+    uint8_t* vals;  // nblk * 8 KB
+    uint8_t* q;     // [NWG][2] * 16 KB: query rows, double-buffered per warpgroup
+    uint8_t* p;     // [NWG] * 16 KB: P of the current block
+};
+
+__device__ __forceinline__ Layout layout(uint8_t* base, int nblk) {
+    Layout L;
+    L.keys = base;
+    L.vals = L.keys + nblk * 8192;
+    L.q = L.vals + nblk * 8192;
+    L.p = L.q + NWG * 2 * 16384;
+    return L;
+}
+
+// The round starting at item r of [r, i1): one item, or two consecutive items
+// of the same expert.
+__device__ __forceinline__ int round_size(const Args& a, int r, int i1, int4& it0, int4& it1) {
+    it0 = a.items[r];
+    it1 = it0;
+    if (r + 1 < i1) {
+        it1 = a.items[r + 1];
+        if (it1.x == it0.x && it1.w == it0.w) return 2;
+    }
+    return 1;
+}
+
 __device__ __forceinline__ void zero16(uint8_t* p) { *reinterpret_cast<uint4*>(p) = make_uint4(0, 0, 0, 0); }
 
-// Stages the key and value lists of expert (bh, e); all NT threads call it.
-template <int NT>
-__device__ void stage_expert(const Args& a, int64_t bh, int e, uint8_t* keys, uint8_t* vals) {
-    const int rows = a.nblk * 128;
-    const int32_t* sel = a.expert_idx + (bh * a.m + e) * static_cast<int64_t>(a.k);
-    const uint32_t kb = smem_u32(keys), vb = smem_u32(vals);
-    for (int x = threadIdx.x; x < rows * 8; x += NT) {
-        const int row = x >> 3, c = x & 7;
-        const uint32_t off = swz128(row, c);
-        if (row < a.m) {
-            const int64_t src = (bh * a.m + row) * D + c * 8;
-            cp_async16(kb + off, a.lqhi + src);
-            cp_async16(vb + off, a.lvbf + src);
-        } else if (row < a.m + a.k) {
-            const int64_t src = (bh * a.N + sel[row - a.m]) * D + c * 8;
-            cp_async16(kb + off, a.K + src);
-            cp_async16(vb + off, a.V + src);
-        } else {
-            zero16(keys + off);
-            zero16(vals + off);
-        }
-    }
-    cp_async_wait_all();
-    fence_proxy_async();
-}
-
-// One work item on warpgroup `wg` (thread t = its query row).
-__device__ void run_item(const Args& a, int4 it, int wg, int t, uint8_t* keys, uint8_t* vals, uint8_t* qb,
-                         uint8_t* pb, uint64_t* barS, uint64_t* barO, uint32_t tS, uint32_t tO, uint32_t& ps,
-                         uint32_t& po) {
-    const int e = it.x, start = it.y, len = it.z;
-    const int64_t bh = it.w;
-    (void)e;
-    const uint32_t lane_off = static_cast<uint32_t>((t >> 5) * 32) << 16;
-    const uint32_t qa = smem_u32(qb), pa = smem_u32(pb), ka = smem_u32(keys), va = smem_u32(vals);
-    const int nkeys = a.m + a.k;
-    int n = 0;
-    if (t < len) {
-        n = a.perm[bh * a.N + start + t];
-        const __nv_bfloat16* src = a.Q + (bh * a.N + n) * D;
-#pragma unroll
-        for (int c = 0; c < 8; ++c) cp_async16(qa + swz128(t, c), src + c * 8);
-    } else {
-#pragma unroll
-        for (int c = 0; c < 8; ++c) zero16(qb + swz128(t, c));
-    }
-    cp_async_wait_all();
-    fence_proxy_async();
-    named_bar(1 + wg, 128);
-
-    auto issue_s = [&](int j) {
-#pragma unroll
-        for (int s = 0; s < 4; ++s)
-            mma_ss(tS, sdesc_sw128(qa + s * 32), sdesc_sw128(ka + j * 16384 + s * 32), kIdescS, s > 0);
-        mma_commit(barS);
-    };
-    auto issue_pv = [&](int j) {
-#pragma unroll
-        for (int s = 0; s < 8; ++s)
-            mma_ss(tO, sdesc_sw128(pa + (s >> 2) * 16384 + (s & 3) * 32), sdesc_sw128(va + j * 16384 + s * 2048),
-                   kIdescPV, (j > 0 || s > 0) ? 1u : 0u);
-        mma_commit(barO);
-    };
-
-    if (t == 0) {
-        tc_fence_after();
-        issue_s(0);
-    }
-    float mrun = -INFINITY, lrun = 0.f;
-    for (int j = 0; j < a.nblk; ++j) {
-        if (!named_bar_and(1 + wg, 128, mbar_wait(barS, ps, a.status))) return;
-        ps ^= 1;
-        tc_fence_after();
-        float s[128];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) tmem_ld32(tS + lane_off + q * 32, s + q * 32);
-        tmem_ld_wait();
-        tc_fence_before();
-        named_bar(1 + wg, 128);
-        if (t == 0 && j + 1 < a.nblk) {
-            tc_fence_after();
-            issue_s(j + 1);
-        }
-        const int valid = min(128, nkeys - j * 128);
-        float bmax = -INFINITY;
-#pragma unroll
-        for (int c = 0; c < 128; ++c) {
-            s[c] = c < valid ? s[c] * kC : -INFINITY;
-            bmax = fmaxf(bmax, s[c]);
-        }
-        const float mnew = (bmax > mrun + kLazy) ? bmax : mrun;
-        const float alpha = exp2f(mrun - mnew);  // 0 on the first block, 1 when the max is kept
-        float sum = 0.f;
-#pragma unroll
-        for (int c = 0; c < 128; ++c) {
-            s[c] = exp2f(s[c] - mnew);
-            sum += s[c];
-        }
-        lrun = lrun * alpha + sum;
-        if (j > 0) {
-            if (!named_bar_and(1 + wg, 128, mbar_wait(barO, po, a.status))) return;
-            po ^= 1;
-            tc_fence_after();
-            if (__any_sync(0xffffffffu, alpha != 1.f)) {  // rescale this warp's rows of O
-                float o[32];
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    tmem_ld32(tO + lane_off + h * 32, o);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int c = 0; c < 32; ++c) o[c] *= alpha;
-                    tmem_st32(tO + lane_off + h * 32, o);
-                }
-                tmem_st_wait();
-            }
-        }
-#pragma unroll
-        for (int g = 0; g < 16; ++g) {
-            uint4 pk;
-            __nv_bfloat162* h2 = reinterpret_cast<__nv_bfloat162*>(&pk);
-#pragma unroll
-            for (int u = 0; u < 4; ++u) h2[u] = __floats2bfloat162_rn(s[8 * g + 2 * u], s[8 * g + 2 * u + 1]);
-            *reinterpret_cast<uint4*>(pb + (g >> 3) * 16384 + swz128(t, g & 7)) = pk;
-        }
-        fence_proxy_async();
-        tc_fence_before();
-        named_bar(1 + wg, 128);
-        if (t == 0) {
-            tc_fence_after();
-            issue_pv(j);
-        }
-        mrun = mnew;
-    }
-    if (!named_bar_and(1 + wg, 128, mbar_wait(barO, po, a.status))) return;
-    po ^= 1;
-    tc_fence_after();
-    float o[64];
-    tmem_ld32(tO + lane_off, o);
-    tmem_ld32(tO + lane_off + 32, o + 32);
-    tmem_ld_wait();
-    tc_fence_before();
-    if (t < len) {
-        const float inv = 1.f / lrun;
-        uint4* dst = reinterpret_cast<uint4*>(a.out + (bh * a.N + n) * D);
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-            uint4 pk;
-            __nv_bfloat162* h2 = reinterpret_cast<__nv_bfloat162*>(&pk);
-#pragma unroll
-            for (int u = 0; u < 4; ++u)
-                h2[u] = __floats2bfloat162_rn(o[8 * c + 2 * u] * inv, o[8 * c + 2 * u + 1] * inv);
-            dst[c] = pk;
-        }
-    }
-}
-
-template <int NWG>
-__global__ void __launch_bounds__(NWG * 128) expert_tc_kernel(Args a) {
+__global__ void __launch_bounds__(NT, 1) expert_tc_kernel(Args a) {
     extern __shared__ uint8_t smem_raw[];
-    __shared__ uint64_t barS[NWG], barO[NWG];
+    __shared__ uint64_t kvfull, kvfree, qfull[NWG * 2], qfree[NWG * 2], ofree[NWG];
+    __shared__ uint64_t sfull[NWG * 2], sfree[NWG * 2], pfull[NWG], pvdone[NWG];
     __shared__ uint32_t tmem_base;
-    constexpr int NT = NWG * 128;
-    constexpr uint32_t kCols = NWG == 2 ? 512 : 256;
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t* keys = base;
-    uint8_t* vals = keys + a.nblk * 16384;
-    uint8_t* qbuf = vals + a.nblk * 16384;
-    uint8_t* pbuf = qbuf + NWG * 16384;
+    const Layout S = layout(base, a.nblk);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int nkeys = a.m + a.k;
 
-    const int tid = threadIdx.x, wg = tid >> 7, t = tid & 127;
     if (tid == 0) {
+        mbar_init(&kvfull, 1);
+        mbar_init(&kvfree, NWG);  // one commit per MMA issuer
         for (int w = 0; w < NWG; ++w) {
-            mbar_init(&barS[w], 1);
-            mbar_init(&barO[w], 1);
+            mbar_init(&ofree[w], 128);
+            mbar_init(&pfull[w], 128);
+            mbar_init(&pvdone[w], 1);
+        }
+        for (int b = 0; b < NWG * 2; ++b) {
+            mbar_init(&qfull[b], 1);
+            mbar_init(&qfree[b], 1);
+            mbar_init(&sfull[b], 1);
+            mbar_init(&sfree[b], 128);
         }
         fence_barrier_init();
     }
-    if (tid < 32) tmem_alloc(&tmem_base, kCols);
+    if (warp == 0) tmem_alloc(&tmem_base, 512);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tS = tmem_base + wg * 256, tO = tS + 128;
+    const uint32_t tb = tmem_base;
 
     const int total = *a.nitems;
     const int i0 = static_cast<int>(static_cast<int64_t>(total) * blockIdx.x / gridDim.x);
     const int i1 = static_cast<int>(static_cast<int64_t>(total) * (blockIdx.x + 1) / gridDim.x);
-    int staged_bh = -1, staged_e = -1;
-    uint32_t ps = 0, po = 0;
-    for (int r = i0; r < i1;) {
-        const int4 it0 = a.items[r];
-        int cnt = 1;
-        int4 it1 = it0;
-        if (NWG == 2 && r + 1 < i1) {
-            it1 = a.items[r + 1];
-            if (it1.x == it0.x && it1.w == it0.w) cnt = 2;
+
+    if (warp == 0) {
+        // ------------------------------ producer ------------------------------
+        int64_t cur_bh = -1;
+        int cur_e = -1, changes = 0;
+        uint32_t nq[NWG] = {0, 0};
+        bool ok = true;
+        for (int r = i0; r < i1 && ok;) {
+            int4 it[2];
+            const int cnt = round_size(a, r, i1, it[0], it[1]);
+            if (it[0].w != cur_bh || it[0].x != cur_e) {
+                // wait until the MMAs reading the previous lists are done
+                if (changes > 0) ok = __all_sync(0xffffffffu, mbar_wait(&kvfree, (changes - 1) & 1, a.status));
+                if (!ok) break;
+                const int64_t bh = it[0].w;
+                const int32_t* sel = a.expert_idx + (bh * a.m + it[0].x) * static_cast<int64_t>(a.k);
+                const int r0 = (it[0].w != cur_bh) ? 0 : a.m;  // shared rows only on a new head
+                const uint32_t kb = smem_u32(S.keys), vb = smem_u32(S.vals);
+                for (int x = r0 * 8 + lane; x < a.nblk * KB * 8; x += 32) {
+                    const int row = x >> 3, c = x & 7;
+                    const uint32_t off = swz128(row, c);
+                    if (row < a.m) {
+                        const int64_t src = (bh * a.m + row) * D + c * 8;
+                        cp_async16(kb + off, a.lqhi + src);
+                        cp_async16(vb + off, a.lvbf + src);
+                    } else if (row < nkeys) {
+                        const int64_t src = (bh * a.N + sel[row - a.m]) * D + c * 8;
+                        cp_async16(kb + off, a.K + src);
+                        cp_async16(vb + off, a.V + src);
+                    } else {
+                        zero16(S.keys + off);
+                        zero16(S.vals + off);
+                    }
+                }
+                cp_async_wait_all();
+                fence_proxy_async();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&kvfull);
+                cur_bh = it[0].w;
+                cur_e = it[0].x;
+                ++changes;
+            }
+            for (int w = 0; w < cnt && ok; ++w) {
+                // Q buffer nq&1 of this warpgroup was last used two items back
+                const uint32_t qb = w * 2 + (nq[w] & 1);
+                if (nq[w] >= 2)
+                    ok = __all_sync(0xffffffffu, mbar_wait(&qfree[qb], ((nq[w] >> 1) - 1) & 1, a.status));
+                if (!ok) break;
+                const int64_t bh = it[w].w;
+                const uint32_t qa = smem_u32(S.q + qb * 16384);
+                for (int x = lane; x < 128 * 8; x += 32) {
+                    const int row = x >> 3, c = x & 7;
+                    if (row < it[w].z) {
+                        const int n = a.perm[bh * a.N + it[w].y + row];
+                        cp_async16(qa + swz128(row, c), a.Q + (bh * a.N + n) * D + c * 8);
+                    } else {
+                        zero16(S.q + qb * 16384 + swz128(row, c));
+                    }
+                }
+                cp_async_wait_all();
+                fence_proxy_async();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&qfull[qb]);
+                ++nq[w];
+            }
+            r += cnt;
         }
-        if (it0.w != staged_bh || it0.x != staged_e) {
-            __syncthreads();  // every warpgroup is done with the previous expert
-            stage_expert<NT>(a, it0.w, it0.x, keys, vals);
-            __syncthreads();
-            staged_bh = it0.w;
-            staged_e = it0.x;
+    } else if (warp <= NWG) {
+        // ---------------- MMA issuers: lane 0 of warp 1 + w serves warpgroup w ----------------
+        // (each issuer has a warp of its own: tcgen05.mma is a single-thread instruction)
+        if (lane == 0) {
+            const int w = warp - 1;
+            int64_t cur_bh = -1;
+            int cur_e = -1, changes = 0;
+            uint32_t nq = 0, gb = 0;
+            const uint32_t ka = smem_u32(S.keys), va = smem_u32(S.vals);
+            const uint32_t pa = smem_u32(S.p + w * 16384);
+            const uint32_t tO = tb + w * 256 + 128;
+            bool ok = true;
+            for (int r = i0; r < i1 && ok;) {
+                int4 it[2];
+                const int cnt = round_size(a, r, i1, it[0], it[1]);
+                if (it[0].w != cur_bh || it[0].x != cur_e) {
+                    if (!mbar_wait(&kvfull, changes & 1, a.status)) break;
+                    cur_bh = it[0].w;
+                    cur_e = it[0].x;
+                    ++changes;
+                }
+                r += cnt;
+                if (w < cnt) {
+                    const uint32_t qb = w * 2 + (nq & 1);
+                    if (!mbar_wait(&qfull[qb], (nq >> 1) & 1, a.status)) break;
+                    tc_fence_after();
+                    const uint32_t qa = smem_u32(S.q + qb * 16384);
+                    // S for block j, then P.V for block j-1
+                    for (int j = 0; j <= a.nblk && ok; ++j) {
+                        if (j < a.nblk) {
+                            const uint32_t g = gb + j, sb = g & 1;
+                            if (g >= 2) {
+                                ok = mbar_wait(&sfree[w * 2 + sb], ((g >> 1) - 1) & 1, a.status);
+                                if (!ok) break;
+                                tc_fence_after();
+                            }
+                            const uint32_t tS = tb + w * 256 + sb * KB;
+#pragma unroll
+                            for (int s = 0; s < 4; ++s)
+                                mma_ss(tS, sdesc_sw128(qa + s * 32), sdesc_sw128(ka + j * 8192 + s * 32), kIdescS,
+                                       s > 0);
+                            mma_commit(&sfull[w * 2 + sb]);
+                            if (j == a.nblk - 1) mma_commit(&qfree[qb]);
+                        }
+                        if (j > 0) {
+                            const uint32_t g = gb + j - 1;
+                            // the first P.V of an item overwrites O: the previous
+                            // item's epilogue must have read it
+                            if (j == 1 && nq > 0) ok = mbar_wait(&ofree[w], (nq - 1) & 1, a.status);
+                            if (ok) ok = mbar_wait(&pfull[w], g & 1, a.status);
+                            if (!ok) break;
+                            tc_fence_after();
+#pragma unroll
+                            for (int s = 0; s < 4; ++s)
+                                mma_ss(tO, sdesc_sw128(pa + s * 32), sdesc_sw128(va + (j - 1) * 8192 + s * 2048),
+                                       kIdescPV, (j > 1 || s > 0) ? 1u : 0u);
+                            mma_commit(&pvdone[w]);
+                        }
+                    }
+                    gb += a.nblk;
+                    ++nq;
+                }
+                // the next round needs other lists: let the producer overwrite them
+                int4 n0, n1;
+                if (r >= i1 || (round_size(a, r, i1, n0, n1), n0.w != cur_bh || n0.x != cur_e)) mma_commit(&kvfree);
+            }
         }
-        if (wg < cnt)
-            run_item(a, wg == 0 ? it0 : it1, wg, t, keys, vals, qbuf + wg * 16384, pbuf + wg * 32768, &barS[wg],
-                     &barO[wg], tS, tO, ps, po);
-        r += cnt;
+    } else {
+        // ------------------------------ row warpgroups ------------------------------
+        const int w = (warp - 1 - NWG) >> 2;
+        const int t = (warp & 3) * 32 + lane;  // TMEM lane = query row of the item
+        const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+        const uint32_t tO = tb + w * 256 + 128;
+        uint32_t gb = 0, nitem = 0;
+        bool ok = true;
+        for (int r = i0; r < i1 && ok;) {
+            int4 it[2];
+            const int cnt = round_size(a, r, i1, it[0], it[1]);
+            r += cnt;
+            if (w >= cnt) continue;
+            const int4 item = it[w];
+            const int64_t bh = item.w;
+            const int n = t < item.z ? a.perm[bh * a.N + item.y + t] : 0;
+            float mrun = -INFINITY, lrun = 0.f;
+            for (int j = 0; j < a.nblk; ++j, ++gb) {
+                const uint32_t sb = gb & 1;
+                ok = __all_sync(0xffffffffu, mbar_wait(&sfull[w * 2 + sb], (gb >> 1) & 1, a.status));
+                if (!ok) break;
+                tc_fence_after();
+                float s[KB];
+                tmem_ld32(tb + w * 256 + sb * KB + lane_off, s);
+                tmem_ld32(tb + w * 256 + sb * KB + lane_off + 32, s + 32);
+                tmem_ld_wait();
+                tc_fence_before();
+                mbar_arrive(&sfree[w * 2 + sb]);
+                const int valid = min(KB, nkeys - j * KB);
+                if (valid < KB) {  // last, partial block (warp-uniform)
+#pragma unroll
+                    for (int c = 0; c < KB; ++c) s[c] = c < valid ? s[c] : -INFINITY;
+                }
+                // 8 independent partial maxima / sums: short dependency chains
+                float pm[8], ps[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) pm[u] = s[u];
+#pragma unroll
+                for (int c = 8; c < KB; ++c) pm[c & 7] = fmaxf(pm[c & 7], s[c]);
+                const float bmax =
+                    fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])), fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7]))) *
+                    kC;
+                const float mnew = (bmax > mrun + kLazy) ? bmax : mrun;
+                const float alpha = exp2f(mrun - mnew);  // 0 on the first block, 1 when the max is kept
+#pragma unroll
+                for (int u = 0; u < 8; ++u) ps[u] = 0.f;
+#pragma unroll
+                for (int c = 0; c < KB; ++c) {
+                    s[c] = exp2f(fmaf(s[c], kC, -mnew));
+                    ps[c & 7] += s[c];
+                }
+                const float sum = ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
+                lrun = lrun * alpha + sum;
+                // P.V of the previous block must be done before P is overwritten
+                // (and before O is rescaled, when a running max grew by > 2^8)
+                const bool rescale = j > 0 && __any_sync(0xffffffffu, alpha != 1.f);
+                if (gb >= 1) {
+                    ok = __all_sync(0xffffffffu, mbar_wait(&pvdone[w], (gb - 1) & 1, a.status));
+                    if (!ok) break;
+                }
+                tc_fence_after();
+                if (rescale) {
+                    float o[32];
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        tmem_ld32(tO + lane_off + h * 32, o);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int c = 0; c < 32; ++c) o[c] *= alpha;
+                        tmem_st32(tO + lane_off + h * 32, o);
+                    }
+                    tmem_st_wait();
+                }
+                uint8_t* pdst = S.p + w * 16384;
+#pragma unroll
+                for (int g = 0; g < KB / 8; ++g) {
+                    uint4 pk;
+                    __nv_bfloat162* h2 = reinterpret_cast<__nv_bfloat162*>(&pk);
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) h2[u] = __floats2bfloat162_rn(s[8 * g + 2 * u], s[8 * g + 2 * u + 1]);
+                    *reinterpret_cast<uint4*>(pdst + swz128(t, g)) = pk;
+                }
+                fence_proxy_async();
+                tc_fence_before();
+                mbar_arrive(&pfull[w]);
+                mrun = mnew;
+            }
+            if (!ok) break;
+            // epilogue: the last P.V of the item (and with it every earlier one) is done
+            ok = __all_sync(0xffffffffu, mbar_wait(&pvdone[w], (gb - 1) & 1, a.status));
+            if (!ok) break;
+            tc_fence_after();
+            float o[64];
+            tmem_ld32(tO + lane_off, o);
+            tmem_ld32(tO + lane_off + 32, o + 32);
+            tmem_ld_wait();
+            tc_fence_before();
+            mbar_arrive(&ofree[w]);
+            ++nitem;
+            if (t < item.z) {
+                const float inv = 1.f / lrun;
+                uint4* dst = reinterpret_cast<uint4*>(a.out + (bh * a.N + n) * D);
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    uint4 pk;
+                    __nv_bfloat162* h2 = reinterpret_cast<__nv_bfloat162*>(&pk);
+#pragma unroll
+                    for (int u = 0; u < 4; ++u)
+                        h2[u] = __floats2bfloat162_rn(o[8 * c + 2 * u] * inv, o[8 * c + 2 * u + 1] * inv);
+                    dst[c] = pk;
+                }
+            }
+        }
+        (void)nitem;
     }
     tc_fence_before();
     __syncthreads();
-    if (tid < 32) tmem_free(tmem_base, kCols);
+    if (warp == 0) tmem_free(tb, 512);
 }
 
-template <int NWG>
-size_t smem_bytes(int nblk) {
-    return 1024 + static_cast<size_t>(nblk) * 32768 + NWG * (16384 + 32768);
-}
+size_t smem_bytes(int nblk) { return 1024 + static_cast<size_t>(nblk) * 16384 + NWG * (2 * 16384 + 16384); }
 
 }  // namespace
 
 bool expert_tc_supported(const Plan& p) {
     const int nkeys = p.s.m + p.s.k;
-    return nkeys <= 512 && smem_bytes<2>((nkeys + 127) / 128) <= 232448;
+    return nkeys <= 512 && smem_bytes((nkeys + KB - 1) / KB) <= 232448;
 }
 
 cudaError_t launch_expert_tc(const Plan& p, const Work& w, const __nv_bfloat16* Q, const __nv_bfloat16* K,
@@ -300,22 +411,12 @@ cudaError_t launch_expert_tc(const Plan& p, const Work& w, const __nv_bfloat16* 
     a.N = p.s.N;
     a.m = p.s.m;
     a.k = p.s.k;
-    a.nblk = (p.s.m + p.s.k + 127) / 128;
-    const int sms = device_sms();
-    cudaError_t e;
-    if (a.nblk <= 2) {  // small key lists: one warpgroup per CTA, two CTAs per SM
-        const size_t sm = smem_bytes<1>(a.nblk);
-        if ((e = cudaFuncSetAttribute(expert_tc_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      static_cast<int>(sm))) != cudaSuccess)
-            return e;
-        expert_tc_kernel<1><<<2 * sms, 128, sm, st>>>(a);
-    } else {
-        const size_t sm = smem_bytes<2>(a.nblk);
-        if ((e = cudaFuncSetAttribute(expert_tc_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      static_cast<int>(sm))) != cudaSuccess)
-            return e;
-        expert_tc_kernel<2><<<sms, 256, sm, st>>>(a);
-    }
+    a.nblk = (p.s.m + p.s.k + KB - 1) / KB;
+    const size_t sm = smem_bytes(a.nblk);
+    cudaError_t e = cudaFuncSetAttribute(expert_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(sm));
+    if (e != cudaSuccess) return e;
+    expert_tc_kernel<<<device_sms(), NT, sm, st>>>(a);
     return cudaGetLastError();
 }
 

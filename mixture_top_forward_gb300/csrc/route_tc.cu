@@ -141,20 +141,31 @@ __global__ void __launch_bounds__(160, 1) route_tc_kernel(const __grid_constant_
             }
             tc_fence_after();
             const uint32_t d = tb + (t & 1) * 256 + lane_off;
-            float best = -INFINITY;
-            int arg = 0;
+            // 4 interleaved (value, index) chains; on equal values the lower
+            // index wins, as in a left-to-right scan with a strict comparison
+            float bv[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+            int bi[4] = {0, 1, 2, 3};
             for (int c0 = 0; c0 < a.m_pad; c0 += 32) {
                 float v[32];
                 tmem_ld32(d + c0, v);
                 tmem_ld_wait();
 #pragma unroll
                 for (int j = 0; j < 32; ++j) {
-                    if (c0 + j < a.m && v[j] > best) {
-                        best = v[j];
-                        arg = c0 + j;
+                    const int u = j & 3;
+                    if (c0 + j < a.m && v[j] > bv[u]) {
+                        bv[u] = v[j];
+                        bi[u] = c0 + j;
                     }
                 }
             }
+            float best = bv[0];
+            int arg = bi[0];
+#pragma unroll
+            for (int u = 1; u < 4; ++u)
+                if (bv[u] > best || (bv[u] == best && bi[u] < arg)) {
+                    best = bv[u];
+                    arg = bi[u];
+                }
             tc_fence_before();
             named_bar(1, 128);
             if (tid == 0) mbar_arrive(&dfree[t & 1]);

@@ -273,12 +273,15 @@ __global__ void __launch_bounds__(Cfg<FULL, NL>::NT, 1)
             float gm[KT / 16];
             float bmax = -INFINITY;
 #pragma unroll
-            for (int g = 0; g < KT / 16; ++g) {
-                float x = s[16 * g];
+            for (int g = 0; g < KT / 16; ++g) {  // two interleaved chains per group
+                float x = s[16 * g], y = s[16 * g + 1];
 #pragma unroll
-                for (int j = 1; j < 16; ++j) x = fmaxf(x, s[16 * g + j]);
-                gm[g] = x;
-                bmax = fmaxf(bmax, x);
+                for (int j = 2; j < 16; j += 2) {
+                    x = fmaxf(x, s[16 * g + j]);
+                    y = fmaxf(y, s[16 * g + j + 1]);
+                }
+                gm[g] = fmaxf(x, y);
+                bmax = fmaxf(bmax, gm[g]);
             }
 
             // top-k candidates (compaction first if this tile could overflow a buffer)
@@ -323,12 +326,15 @@ __global__ void __launch_bounds__(Cfg<FULL, NL>::NT, 1)
                 const float bm2 = bmax * kC;
                 const float mnew = (bm2 > mrun + kLazy) ? bm2 : mrun;
                 const float alpha = exp2f(mrun - mnew);
-                float sum = 0.f;
+                float ps[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) ps[u] = 0.f;
 #pragma unroll
                 for (int col = 0; col < KT; ++col) {
                     s[col] = exp2f(fmaf(s[col], kC, -mnew));
-                    sum += s[col];
+                    ps[col & 7] += s[col];
                 }
+                const float sum = ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
                 lrun = lrun * alpha + sum;
                 const int pb = L * 2 + sb;
                 // this warp's rows of O need rescaling only when a running max
