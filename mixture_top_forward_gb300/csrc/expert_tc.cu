@@ -148,20 +148,35 @@ __global__ void __launch_bounds__(NT, 1) expert_tc_kernel(Args a) {
                 const int32_t* sel = a.expert_idx + (bh * a.m + it[0].x) * static_cast<int64_t>(a.k);
                 const int r0 = (it[0].w != cur_bh) ? 0 : a.m;  // shared rows only on a new head
                 const uint32_t kb = smem_u32(S.keys), vb = smem_u32(S.vals);
-                for (int x = r0 * 8 + lane; x < a.nblk * KB * 8; x += 32) {
-                    const int row = x >> 3, c = x & 7;
-                    const uint32_t off = swz128(row, c);
-                    if (row < a.m) {
-                        const int64_t src = (bh * a.m + row) * D + c * 8;
-                        cp_async16(kb + off, a.lqhi + src);
-                        cp_async16(vb + off, a.lvbf + src);
-                    } else if (row < nkeys) {
-                        const int64_t src = (bh * a.N + sel[row - a.m]) * D + c * 8;
-                        cp_async16(kb + off, a.K + src);
-                        cp_async16(vb + off, a.V + src);
-                    } else {
-                        zero16(S.keys + off);
-                        zero16(S.vals + off);
+                // lane l stages rows r0 + l, r0 + l + 32, ...: the row indices of a
+                // batch of 8 rows are loaded first, then all of their copies issued
+                const int rows = a.nblk * KB;
+                for (int rb = r0; rb < rows; rb += 32 * 8) {
+                    int64_t src[8];
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        const int row = rb + u * 32 + lane;
+                        src[u] = -1;
+                        if (row < a.m) src[u] = (bh * a.m + row) * D;
+                        else if (row < nkeys) src[u] = (bh * a.N + sel[row - a.m]) * D;
+                    }
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        const int row = rb + u * 32 + lane;
+                        if (row >= rows) continue;
+                        const __nv_bfloat16* ks = row < a.m ? a.lqhi : a.K;
+                        const __nv_bfloat16* vs = row < a.m ? a.lvbf : a.V;
+#pragma unroll
+                        for (int c = 0; c < 8; ++c) {
+                            const uint32_t off = swz128(row, c);
+                            if (src[u] >= 0) {
+                                cp_async16(kb + off, ks + src[u] + c * 8);
+                                cp_async16(vb + off, vs + src[u] + c * 8);
+                            } else {
+                                zero16(S.keys + off);
+                                zero16(S.vals + off);
+                            }
+                        }
                     }
                 }
                 cp_async_wait_all();
@@ -180,13 +195,22 @@ __global__ void __launch_bounds__(NT, 1) expert_tc_kernel(Args a) {
                 if (!ok) break;
                 const int64_t bh = it[w].w;
                 const uint32_t qa = smem_u32(S.q + qb * 16384);
-                for (int x = lane; x < 128 * 8; x += 32) {
-                    const int row = x >> 3, c = x & 7;
-                    if (row < it[w].z) {
-                        const int n = a.perm[bh * a.N + it[w].y + row];
-                        cp_async16(qa + swz128(row, c), a.Q + (bh * a.N + n) * D + c * 8);
-                    } else {
-                        zero16(S.q + qb * 16384 + swz128(row, c));
+                // lane l gathers rows l, l+32, l+64, l+96: indices first, then copies
+                int n[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int row = u * 32 + lane;
+                    n[u] = row < it[w].z ? a.perm[bh * a.N + it[w].y + row] : -1;
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int row = u * 32 + lane;
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        if (n[u] >= 0)
+                            cp_async16(qa + swz128(row, c), a.Q + (bh * a.N + n[u]) * D + c * 8);
+                        else
+                            zero16(S.q + qb * 16384 + swz128(row, c));
                     }
                 }
                 cp_async_wait_all();
@@ -299,13 +323,15 @@ __global__ void __launch_bounds__(NT, 1) expert_tc_kernel(Args a) {
                 }
                 // 8 independent partial maxima / sums: short dependency chains
                 float pm[8], ps[8];
+                static_assert(KB == 64, "the partial maxima below cover exactly 64 columns");
 #pragma unroll
-                for (int u = 0; u < 8; ++u) pm[u] = s[u];
-#pragma unroll
-                for (int c = 8; c < KB; ++c) pm[c & 7] = fmaxf(pm[c & 7], s[c]);
-                const float bmax =
-                    fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])), fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7]))) *
-                    kC;
+                for (int u = 0; u < 8; ++u) {  // columns u, u+8, ..., u+56
+                    pm[u] = fmax3(s[u], s[u + 8], s[u + 16]);
+                    pm[u] = fmax3(pm[u], s[u + 24], s[u + 32]);
+                    pm[u] = fmax3(pm[u], s[u + 40], s[u + 48]);
+                    pm[u] = fmaxf(pm[u], s[u + 56]);
+                }
+                const float bmax = fmaxf(fmax3(pm[0], pm[1], pm[2]), fmax3(fmax3(pm[3], pm[4], pm[5]), pm[6], pm[7])) * kC;
                 const float mnew = (bmax > mrun + kLazy) ? bmax : mrun;
                 const float alpha = exp2f(mrun - mnew);  // 0 on the first block, 1 when the max is kept
 #pragma unroll

@@ -273,14 +273,11 @@ __global__ void __launch_bounds__(Cfg<FULL, NL>::NT, 1)
             float gm[KT / 16];
             float bmax = -INFINITY;
 #pragma unroll
-            for (int g = 0; g < KT / 16; ++g) {  // two interleaved chains per group
-                float x = s[16 * g], y = s[16 * g + 1];
-#pragma unroll
-                for (int j = 2; j < 16; j += 2) {
-                    x = fmaxf(x, s[16 * g + j]);
-                    y = fmaxf(y, s[16 * g + j + 1]);
-                }
-                gm[g] = fmaxf(x, y);
+            for (int g = 0; g < KT / 16; ++g) {  // three-input maxima, short chains
+                const float* v = s + 16 * g;
+                const float x = fmax3(v[0], v[1], v[2]), y = fmax3(v[3], v[4], v[5]), z = fmax3(v[6], v[7], v[8]);
+                const float u = fmax3(v[9], v[10], v[11]), w2 = fmax3(v[12], v[13], v[14]);
+                gm[g] = fmax3(fmax3(x, y, z), fmax3(u, w2, v[15]), -INFINITY);
                 bmax = fmaxf(bmax, gm[g]);
             }
 
