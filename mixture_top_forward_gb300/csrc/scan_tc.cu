@@ -267,19 +267,17 @@ __global__ void __launch_bounds__(Cfg<FULL, NL>::NT, 1)
 #pragma unroll
                 for (int col = 0; col < KT; ++col) s[col] = col < nvalid ? s[col] : -INFINITY;
             }
-            // raw maxima per 16-column group; a group can only hold a candidate
+            // raw maxima per 8-column group; a group can only hold a candidate
             // if its maximum reaches the threshold (s_raw >= 8 theta_s is exact:
             // tau = 1/8 is a power of two)
-            float gm[KT / 16];
-            float bmax = -INFINITY;
+            static_assert(KT == 64, "eight groups of eight columns");
+            float gm[KT / 8];
 #pragma unroll
-            for (int g = 0; g < KT / 16; ++g) {  // three-input maxima, short chains
-                const float* v = s + 16 * g;
-                const float x = fmax3(v[0], v[1], v[2]), y = fmax3(v[3], v[4], v[5]), z = fmax3(v[6], v[7], v[8]);
-                const float u = fmax3(v[9], v[10], v[11]), w2 = fmax3(v[12], v[13], v[14]);
-                gm[g] = fmax3(fmax3(x, y, z), fmax3(u, w2, v[15]), -INFINITY);
-                bmax = fmaxf(bmax, gm[g]);
+            for (int g = 0; g < KT / 8; ++g) {
+                const float* v = s + 8 * g;
+                gm[g] = fmax3(fmax3(v[0], v[1], v[2]), fmax3(v[3], v[4], v[5]), fmaxf(v[6], v[7]));
             }
+            const float bmax = fmax3(fmax3(gm[0], gm[1], gm[2]), fmax3(gm[3], gm[4], gm[5]), fmaxf(gm[6], gm[7]));
 
             // top-k candidates (compaction first if this tile could overflow a buffer)
             unsigned need = __ballot_sync(0xffffffffu, row_ok && cnt + nvalid > a.cap);
@@ -300,20 +298,25 @@ __global__ void __launch_bounds__(Cfg<FULL, NL>::NT, 1)
             // threshold is still -inf (every finite score passes -FLT_MAX)
             const float thr = fmaxf(theta_s * 8.0f, -3.402823466e38f);
             if (row_ok && bmax >= thr) {
+                // a lane entering a group stashes the group's 8 scores in its own
+                // 32-byte slot of the warp's scratch (the compaction histogram,
+                // idle here), so each hit is one shared-memory load
+                float* slot = reinterpret_cast<float*>(hist) + lane * 8;
 #pragma unroll
-                for (int g = 0; g < KT / 16; ++g) {
+                for (int g = 0; g < KT / 8; ++g) {
                     if (gm[g] >= thr) {
+                        reinterpret_cast<float4*>(slot)[0] =
+                            make_float4(s[8 * g], s[8 * g + 1], s[8 * g + 2], s[8 * g + 3]);
+                        reinterpret_cast<float4*>(slot)[1] =
+                            make_float4(s[8 * g + 4], s[8 * g + 5], s[8 * g + 6], s[8 * g + 7]);
                         unsigned msk = 0;
 #pragma unroll
-                        for (int j = 0; j < 16; ++j) msk |= (s[16 * g + j] >= thr ? 1u : 0u) << j;
+                        for (int j = 0; j < 8; ++j) msk |= (s[8 * g + j] >= thr ? 1u : 0u) << j;
                         while (msk) {
                             const int j = __ffs(msk) - 1;
                             msk &= msk - 1;
-                            float v = s[16 * g];
-#pragma unroll
-                            for (int jj = 1; jj < 16; ++jj) v = (j == jj) ? s[16 * g + jj] : v;
                             const uint64_t key =
-                                topk_key(v * 0.125f, static_cast<uint32_t>((col0 + 16 * g + j) * a.stride));
+                                topk_key(slot[j] * 0.125f, static_cast<uint32_t>((col0 + 8 * g + j) * a.stride));
                             if (key >= theta) buf[cnt++] = key;
                         }
                     }
