@@ -322,7 +322,7 @@ __global__ void __launch_bounds__(NT, 1) expert_tc_kernel(Args a) {
                     for (int c = 0; c < KB; ++c) s[c] = c < valid ? s[c] : -INFINITY;
                 }
                 // 8 independent partial maxima / sums: short dependency chains
-                float pm[8], ps[8];
+                float pm[8];
                 static_assert(KB == 64, "the partial maxima below cover exactly 64 columns");
 #pragma unroll
                 for (int u = 0; u < 8; ++u) {  // columns u, u+8, ..., u+56
@@ -334,14 +334,19 @@ __global__ void __launch_bounds__(NT, 1) expert_tc_kernel(Args a) {
                 const float bmax = fmaxf(fmax3(pm[0], pm[1], pm[2]), fmax3(fmax3(pm[3], pm[4], pm[5]), pm[6], pm[7])) * kC;
                 const float mnew = (bmax > mrun + kLazy) ? bmax : mrun;
                 const float alpha = exp2f(mrun - mnew);  // 0 on the first block, 1 when the max is kept
+                // packed pairs: one f32x2 FMA forms two exponents, one f32x2 add
+                // accumulates two weights
+                const float2 c2 = make_float2(kC, kC), m2 = make_float2(-mnew, -mnew);
+                float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                                 make_float2(0.f, 0.f)};
 #pragma unroll
-                for (int u = 0; u < 8; ++u) ps[u] = 0.f;
-#pragma unroll
-                for (int c = 0; c < KB; ++c) {
-                    s[c] = exp2f(fmaf(s[c], kC, -mnew));
-                    ps[c & 7] += s[c];
+                for (int c = 0; c < KB; c += 2) {
+                    const float2 x = __ffma2_rn(make_float2(s[c], s[c + 1]), c2, m2);
+                    s[c] = exp2f(x.x);
+                    s[c + 1] = exp2f(x.y);
+                    acc[(c >> 1) & 3] = __fadd2_rn(acc[(c >> 1) & 3], make_float2(s[c], s[c + 1]));
                 }
-                const float sum = ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
+                const float sum = ((acc[0].x + acc[0].y) + (acc[1].x + acc[1].y)) + ((acc[2].x + acc[2].y) + (acc[3].x + acc[3].y));
                 lrun = lrun * alpha + sum;
                 // P.V of the previous block must be done before P is overwritten
                 // (and before O is rescaled, when a running max grew by > 2^8)

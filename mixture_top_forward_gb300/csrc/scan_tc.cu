@@ -326,15 +326,19 @@ __global__ void __launch_bounds__(Cfg<FULL, NL>::NT, 1)
                 const float bm2 = bmax * kC;
                 const float mnew = (bm2 > mrun + kLazy) ? bm2 : mrun;
                 const float alpha = exp2f(mrun - mnew);
-                float ps[8];
+                // packed pairs: one f32x2 FMA forms two exponents, one f32x2 add
+                // accumulates two weights
+                const float2 c2 = make_float2(kC, kC), m2 = make_float2(-mnew, -mnew);
+                float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                                 make_float2(0.f, 0.f)};
 #pragma unroll
-                for (int u = 0; u < 8; ++u) ps[u] = 0.f;
-#pragma unroll
-                for (int col = 0; col < KT; ++col) {
-                    s[col] = exp2f(fmaf(s[col], kC, -mnew));
-                    ps[col & 7] += s[col];
+                for (int col = 0; col < KT; col += 2) {
+                    const float2 x = __ffma2_rn(make_float2(s[col], s[col + 1]), c2, m2);
+                    s[col] = exp2f(x.x);
+                    s[col + 1] = exp2f(x.y);
+                    acc[(col >> 1) & 3] = __fadd2_rn(acc[(col >> 1) & 3], make_float2(s[col], s[col + 1]));
                 }
-                const float sum = ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
+                const float sum = ((acc[0].x + acc[0].y) + (acc[1].x + acc[1].y)) + ((acc[2].x + acc[2].y) + (acc[3].x + acc[3].y));
                 lrun = lrun * alpha + sum;
                 const int pb = L * 2 + sb;
                 // this warp's rows of O need rescaling only when a running max

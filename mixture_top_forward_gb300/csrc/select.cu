@@ -19,7 +19,8 @@ namespace mita {
 
 namespace {
 
-constexpr int ST = 256;  // threads per CTA
+constexpr int ST = 256;         // threads per CTA
+constexpr int SEL_CAP = 5120;   // candidates staged in shared memory (40 KB)
 
 template <bool PILOT>
 __global__ void __launch_bounds__(ST) select_kernel(int m, int k, int chunks, int cap,
@@ -30,6 +31,8 @@ __global__ void __launch_bounds__(ST) select_kernel(int m, int k, int chunks, in
                                                     int32_t* __restrict__ expert_idx, uint64_t* __restrict__ theta) {
     __shared__ unsigned hist[256];
     __shared__ int cnts[64];
+    __shared__ int offs[65];
+    __shared__ uint64_t staged[SEL_CAP];
     __shared__ int sel[MITA_SORT_MAX];
     __shared__ int nsel;
     __shared__ int s_digit;
@@ -67,6 +70,39 @@ __global__ void __launch_bounds__(ST) select_kernel(int m, int k, int chunks, in
     auto count_of = [&](int c) { return c < 64 ? cnts[c] : ccount[(bh * chunks + c) * m + i]; };
     auto buf_of = [&](int c) { return cand + ((bh * chunks + c) * m + i) * static_cast<int64_t>(cap); };
 
+    // all of this landmark's candidates in shared memory when they fit
+    const bool in_smem = chunks <= 64 && total <= SEL_CAP;
+    if (in_smem) {
+        if (tid == 0) {
+            int o = 0;
+            for (int c = 0; c < chunks; ++c) {
+                offs[c] = o;
+                o += cnts[c];
+            }
+        }
+        __syncthreads();
+        for (int c = 0; c < chunks; ++c) {
+            const uint64_t* b = buf_of(c);
+            for (int e = tid; e < cnts[c]; e += ST) staged[offs[c] + e] = b[e];
+        }
+        __syncthreads();
+    }
+    auto for_each = [&](auto&& f) {
+        if (in_smem) {
+            for (int e = tid; e < total; e += ST) f(staged[e]);
+        } else {
+            for (int c = 0; c < chunks; ++c) {
+                const uint64_t* b = buf_of(c);
+                const int n = count_of(c);
+                for (int e = tid; e < n; e += ST) f(b[e]);
+            }
+        }
+    };
+
+    // Radix select, 8 bits per pass from the top. It stops early once the bin
+    // holding the k-th largest key holds exactly the keys still needed: then
+    // every key whose leading digits reach the prefix is selected, and the
+    // prefix (lower bits zero) separates them from the rest.
     uint64_t kth = 0;  // keep every key >= kth
     if (total > k || (PILOT && total == k)) {
         uint64_t prefix = 0, mask = 0;
@@ -74,14 +110,9 @@ __global__ void __launch_bounds__(ST) select_kernel(int m, int k, int chunks, in
         for (int shift = 56; shift >= 0; shift -= 8) {
             hist[tid] = 0;
             __syncthreads();
-            for (int c = 0; c < chunks; ++c) {
-                const uint64_t* b = buf_of(c);
-                const int n = count_of(c);
-                for (int e = tid; e < n; e += ST) {
-                    const uint64_t x = b[e];
-                    if ((x & mask) == prefix) atomicAdd(&hist[(x >> shift) & 255u], 1u);
-                }
-            }
+            for_each([&](uint64_t x) {
+                if ((x & mask) == prefix) atomicAdd(&hist[(x >> shift) & 255u], 1u);
+            });
             __syncthreads();
             if (tid < 32) {  // warp 0 finds the digit holding the k-th largest
                 const int lane = tid;
@@ -114,7 +145,9 @@ __global__ void __launch_bounds__(ST) select_kernel(int m, int k, int chunks, in
             remaining -= s_above;
             prefix |= static_cast<uint64_t>(s_digit) << shift;
             mask |= 0xFFull << shift;
+            const bool whole_bin = hist[s_digit] == remaining;
             __syncthreads();
+            if (whole_bin) break;
         }
         kth = prefix;
     }
@@ -129,14 +162,9 @@ __global__ void __launch_bounds__(ST) select_kernel(int m, int k, int chunks, in
     // ---- gather the selected indices and sort them ascending ----------------
     if (tid == 0) nsel = 0;
     __syncthreads();
-    for (int c = 0; c < chunks; ++c) {
-        const uint64_t* b = buf_of(c);
-        const int n = count_of(c);
-        for (int e = tid; e < n; e += ST) {
-            const uint64_t x = b[e];
-            if (x >= kth) sel[atomicAdd(&nsel, 1)] = static_cast<int>(topk_key_index(x));
-        }
-    }
+    for_each([&](uint64_t x) {
+        if (x >= kth) sel[atomicAdd(&nsel, 1)] = static_cast<int>(topk_key_index(x));
+    });
     __syncthreads();
     int n2 = 1;
     while (n2 < k) n2 <<= 1;
