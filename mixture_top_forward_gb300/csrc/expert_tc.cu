@@ -44,8 +44,12 @@ using namespace umma;
 constexpr float kC = 0.125f * kLog2e;  // tau * log2(e), tau = 1/sqrt(64)
 constexpr float kLazy = 8.0f;          // keep the running max while the new one is within 2^8
 constexpr int KB = 64;                 // keys per block
-constexpr int NWG = 2;                 // row warpgroups
+constexpr int NWG = 3;                 // row warpgroups
+constexpr int QB = 1;                  // query-row buffers per warpgroup
+constexpr int SB = 1;                  // TMEM score buffers per warpgroup
 constexpr int NT = 32 * (1 + NWG) + NWG * 128;  // producer, one issuer warp per group, rows
+constexpr uint32_t kTStride = (SB + 1) * 64;    // TMEM columns per warpgroup: SB x S, then O
+static_assert(NWG * kTStride <= 512, "TMEM holds 512 columns");
 constexpr uint32_t kIdescS = idesc_bf16(128, KB, false);
 constexpr uint32_t kIdescPV = idesc_bf16(128, 64, true);
 
@@ -68,7 +72,7 @@ struct Args {
 struct Layout {
     uint8_t* keys;  // nblk * 8 KB
     uint8_t* vals;  // nblk * 8 KB
-    uint8_t* q;     // [NWG][2] * 16 KB: query rows, double-buffered per warpgroup
+    uint8_t* q;     // [NWG][QB] * 16 KB: query rows
     uint8_t* p;     // [NWG] * 16 KB: P of the current block
 };
 
@@ -77,28 +81,29 @@ __device__ __forceinline__ Layout layout(uint8_t* base, int nblk) {
     L.keys = base;
     L.vals = L.keys + nblk * 8192;
     L.q = L.vals + nblk * 8192;
-    L.p = L.q + NWG * 2 * 16384;
+    L.p = L.q + NWG * QB * 16384;
     return L;
 }
 
-// The round starting at item r of [r, i1): one item, or two consecutive items
-// of the same expert.
-__device__ __forceinline__ int round_size(const Args& a, int r, int i1, int4& it0, int4& it1) {
-    it0 = a.items[r];
-    it1 = it0;
-    if (r + 1 < i1) {
-        it1 = a.items[r + 1];
-        if (it1.x == it0.x && it1.w == it0.w) return 2;
+// The round starting at item r of [r, i1): up to NWG consecutive items of
+// the same expert, one per warpgroup.
+__device__ __forceinline__ int round_size(const Args& a, int r, int i1, int4* it) {
+    it[0] = a.items[r];
+    int n = 1;
+    while (n < NWG && r + n < i1) {
+        const int4 x = a.items[r + n];
+        if (x.x != it[0].x || x.w != it[0].w) break;
+        it[n++] = x;
     }
-    return 1;
+    return n;
 }
 
 __device__ __forceinline__ void zero16(uint8_t* p) { *reinterpret_cast<uint4*>(p) = make_uint4(0, 0, 0, 0); }
 
 __global__ void __launch_bounds__(NT, 1) expert_tc_kernel(Args a) {
     extern __shared__ uint8_t smem_raw[];
-    __shared__ uint64_t kvfull, kvfree, qfull[NWG * 2], qfree[NWG * 2], ofree[NWG];
-    __shared__ uint64_t sfull[NWG * 2], sfree[NWG * 2], pfull[NWG], pvdone[NWG];
+    __shared__ uint64_t kvfull, kvfree, qfull[NWG * QB], qfree[NWG * QB], ofree[NWG];
+    __shared__ uint64_t sfull[NWG * SB], sfree[NWG * SB], pfull[NWG], pvdone[NWG];
     __shared__ uint32_t tmem_base;
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const Layout S = layout(base, a.nblk);
@@ -113,9 +118,11 @@ __global__ void __launch_bounds__(NT, 1) expert_tc_kernel(Args a) {
             mbar_init(&pfull[w], 128);
             mbar_init(&pvdone[w], 1);
         }
-        for (int b = 0; b < NWG * 2; ++b) {
+        for (int b = 0; b < NWG * QB; ++b) {
             mbar_init(&qfull[b], 1);
             mbar_init(&qfree[b], 1);
+        }
+        for (int b = 0; b < NWG * SB; ++b) {
             mbar_init(&sfull[b], 1);
             mbar_init(&sfree[b], 128);
         }
@@ -135,11 +142,11 @@ __global__ void __launch_bounds__(NT, 1) expert_tc_kernel(Args a) {
         // ------------------------------ producer ------------------------------
         int64_t cur_bh = -1;
         int cur_e = -1, changes = 0;
-        uint32_t nq[NWG] = {0, 0};
+        uint32_t nq[NWG] = {};
         bool ok = true;
         for (int r = i0; r < i1 && ok;) {
-            int4 it[2];
-            const int cnt = round_size(a, r, i1, it[0], it[1]);
+            int4 it[NWG];
+            const int cnt = round_size(a, r, i1, it);
             if (it[0].w != cur_bh || it[0].x != cur_e) {
                 // wait until the MMAs reading the previous lists are done
                 if (changes > 0) ok = __all_sync(0xffffffffu, mbar_wait(&kvfree, (changes - 1) & 1, a.status));
@@ -188,10 +195,10 @@ __global__ void __launch_bounds__(NT, 1) expert_tc_kernel(Args a) {
                 ++changes;
             }
             for (int w = 0; w < cnt && ok; ++w) {
-                // Q buffer nq&1 of this warpgroup was last used two items back
-                const uint32_t qb = w * 2 + (nq[w] & 1);
-                if (nq[w] >= 2)
-                    ok = __all_sync(0xffffffffu, mbar_wait(&qfree[qb], ((nq[w] >> 1) - 1) & 1, a.status));
+                // this Q buffer of the warpgroup was last used QB items back
+                const uint32_t qb = w * QB + (nq[w] % QB);
+                if (nq[w] >= QB)
+                    ok = __all_sync(0xffffffffu, mbar_wait(&qfree[qb], ((nq[w] / QB) - 1) & 1, a.status));
                 if (!ok) break;
                 const int64_t bh = it[w].w;
                 const uint32_t qa = smem_u32(S.q + qb * 16384);
@@ -231,11 +238,11 @@ __global__ void __launch_bounds__(NT, 1) expert_tc_kernel(Args a) {
             uint32_t nq = 0, gb = 0;
             const uint32_t ka = smem_u32(S.keys), va = smem_u32(S.vals);
             const uint32_t pa = smem_u32(S.p + w * 16384);
-            const uint32_t tO = tb + w * 256 + 128;
+            const uint32_t tO = tb + w * kTStride + SB * 64;
             bool ok = true;
             for (int r = i0; r < i1 && ok;) {
-                int4 it[2];
-                const int cnt = round_size(a, r, i1, it[0], it[1]);
+                int4 it[NWG];
+                const int cnt = round_size(a, r, i1, it);
                 if (it[0].w != cur_bh || it[0].x != cur_e) {
                     if (!mbar_wait(&kvfull, changes & 1, a.status)) break;
                     cur_bh = it[0].w;
@@ -244,25 +251,25 @@ __global__ void __launch_bounds__(NT, 1) expert_tc_kernel(Args a) {
                 }
                 r += cnt;
                 if (w < cnt) {
-                    const uint32_t qb = w * 2 + (nq & 1);
-                    if (!mbar_wait(&qfull[qb], (nq >> 1) & 1, a.status)) break;
+                    const uint32_t qb = w * QB + (nq % QB);
+                    if (!mbar_wait(&qfull[qb], (nq / QB) & 1, a.status)) break;
                     tc_fence_after();
                     const uint32_t qa = smem_u32(S.q + qb * 16384);
                     // S for block j, then P.V for block j-1
                     for (int j = 0; j <= a.nblk && ok; ++j) {
                         if (j < a.nblk) {
-                            const uint32_t g = gb + j, sb = g & 1;
-                            if (g >= 2) {
-                                ok = mbar_wait(&sfree[w * 2 + sb], ((g >> 1) - 1) & 1, a.status);
+                            const uint32_t g = gb + j, sb = g % SB;
+                            if (g >= SB) {  // the rows have read this S buffer (block g - SB)
+                                ok = mbar_wait(&sfree[w * SB + sb], ((g / SB) - 1) & 1, a.status);
                                 if (!ok) break;
                                 tc_fence_after();
                             }
-                            const uint32_t tS = tb + w * 256 + sb * KB;
+                            const uint32_t tS = tb + w * kTStride + sb * KB;
 #pragma unroll
                             for (int s = 0; s < 4; ++s)
                                 mma_ss(tS, sdesc_sw128(qa + s * 32), sdesc_sw128(ka + j * 8192 + s * 32), kIdescS,
                                        s > 0);
-                            mma_commit(&sfull[w * 2 + sb]);
+                            mma_commit(&sfull[w * SB + sb]);
                             if (j == a.nblk - 1) mma_commit(&qfree[qb]);
                         }
                         if (j > 0) {
@@ -284,21 +291,20 @@ __global__ void __launch_bounds__(NT, 1) expert_tc_kernel(Args a) {
                     ++nq;
                 }
                 // the next round needs other lists: let the producer overwrite them
-                int4 n0, n1;
-                if (r >= i1 || (round_size(a, r, i1, n0, n1), n0.w != cur_bh || n0.x != cur_e)) mma_commit(&kvfree);
+                if (r >= i1 || a.items[r].w != cur_bh || a.items[r].x != cur_e) mma_commit(&kvfree);
             }
         }
     } else {
         // ------------------------------ row warpgroups ------------------------------
-        const int w = (warp - 1 - NWG) >> 2;
+        const int w = (warp - 1 - NWG) >> 2;  // 4 consecutive warps cover the 4 TMEM lane quarters
         const int t = (warp & 3) * 32 + lane;  // TMEM lane = query row of the item
         const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-        const uint32_t tO = tb + w * 256 + 128;
+        const uint32_t tO = tb + w * kTStride + SB * 64;
         uint32_t gb = 0, nitem = 0;
         bool ok = true;
         for (int r = i0; r < i1 && ok;) {
-            int4 it[2];
-            const int cnt = round_size(a, r, i1, it[0], it[1]);
+            int4 it[NWG];
+            const int cnt = round_size(a, r, i1, it);
             r += cnt;
             if (w >= cnt) continue;
             const int4 item = it[w];
@@ -306,16 +312,16 @@ __global__ void __launch_bounds__(NT, 1) expert_tc_kernel(Args a) {
             const int n = t < item.z ? a.perm[bh * a.N + item.y + t] : 0;
             float mrun = -INFINITY, lrun = 0.f;
             for (int j = 0; j < a.nblk; ++j, ++gb) {
-                const uint32_t sb = gb & 1;
-                ok = __all_sync(0xffffffffu, mbar_wait(&sfull[w * 2 + sb], (gb >> 1) & 1, a.status));
+                const uint32_t sb = gb % SB;
+                ok = __all_sync(0xffffffffu, mbar_wait(&sfull[w * SB + sb], (gb / SB) & 1, a.status));
                 if (!ok) break;
                 tc_fence_after();
                 float s[KB];
-                tmem_ld32(tb + w * 256 + sb * KB + lane_off, s);
-                tmem_ld32(tb + w * 256 + sb * KB + lane_off + 32, s + 32);
+                tmem_ld32(tb + w * kTStride + sb * KB + lane_off, s);
+                tmem_ld32(tb + w * kTStride + sb * KB + lane_off + 32, s + 32);
                 tmem_ld_wait();
                 tc_fence_before();
-                mbar_arrive(&sfree[w * 2 + sb]);
+                mbar_arrive(&sfree[w * SB + sb]);
                 const int valid = min(KB, nkeys - j * KB);
                 if (valid < KB) {  // last, partial block (warp-uniform)
 #pragma unroll
@@ -357,14 +363,14 @@ __global__ void __launch_bounds__(NT, 1) expert_tc_kernel(Args a) {
                 }
                 tc_fence_after();
                 if (rescale) {
-                    float o[32];
+                    float o[16];
 #pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        tmem_ld32(tO + lane_off + h * 32, o);
+                    for (int h = 0; h < 4; ++h) {
+                        tmem_ld16(tO + lane_off + h * 16, o);
                         tmem_ld_wait();
 #pragma unroll
-                        for (int c = 0; c < 32; ++c) o[c] *= alpha;
-                        tmem_st32(tO + lane_off + h * 32, o);
+                        for (int c = 0; c < 16; ++c) o[c] *= alpha;
+                        tmem_st16(tO + lane_off + h * 16, o);
                     }
                     tmem_st_wait();
                 }
@@ -387,26 +393,30 @@ __global__ void __launch_bounds__(NT, 1) expert_tc_kernel(Args a) {
             ok = __all_sync(0xffffffffu, mbar_wait(&pvdone[w], (gb - 1) & 1, a.status));
             if (!ok) break;
             tc_fence_after();
-            float o[64];
-            tmem_ld32(tO + lane_off, o);
-            tmem_ld32(tO + lane_off + 32, o + 32);
-            tmem_ld_wait();
-            tc_fence_before();
-            mbar_arrive(&ofree[w]);
-            ++nitem;
-            if (t < item.z) {
-                const float inv = 1.f / lrun;
-                uint4* dst = reinterpret_cast<uint4*>(a.out + (bh * a.N + n) * D);
+            const float inv = 1.f / lrun;
+            uint4* dst = reinterpret_cast<uint4*>(a.out + (bh * a.N + n) * D);
 #pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    uint4 pk;
-                    __nv_bfloat162* h2 = reinterpret_cast<__nv_bfloat162*>(&pk);
+            for (int h = 0; h < 2; ++h) {  // two 32-column halves of the output row
+                float o[32];
+                tmem_ld32(tO + lane_off + h * 32, o);
+                tmem_ld_wait();
+                if (h == 1) {
+                    tc_fence_before();
+                    mbar_arrive(&ofree[w]);
+                }
+                if (t < item.z) {
 #pragma unroll
-                    for (int u = 0; u < 4; ++u)
-                        h2[u] = __floats2bfloat162_rn(o[8 * c + 2 * u] * inv, o[8 * c + 2 * u + 1] * inv);
-                    dst[c] = pk;
+                    for (int c = 0; c < 4; ++c) {
+                        uint4 pk;
+                        __nv_bfloat162* h2 = reinterpret_cast<__nv_bfloat162*>(&pk);
+#pragma unroll
+                        for (int u = 0; u < 4; ++u)
+                            h2[u] = __floats2bfloat162_rn(o[8 * c + 2 * u] * inv, o[8 * c + 2 * u + 1] * inv);
+                        dst[h * 4 + c] = pk;
+                    }
                 }
             }
+            ++nitem;
         }
         (void)nitem;
     }
@@ -415,7 +425,7 @@ __global__ void __launch_bounds__(NT, 1) expert_tc_kernel(Args a) {
     if (warp == 0) tmem_free(tb, 512);
 }
 
-size_t smem_bytes(int nblk) { return 1024 + static_cast<size_t>(nblk) * 16384 + NWG * (2 * 16384 + 16384); }
+size_t smem_bytes(int nblk) { return 1024 + static_cast<size_t>(nblk) * 16384 + NWG * (QB * 16384 + 16384); }
 
 }  // namespace
 

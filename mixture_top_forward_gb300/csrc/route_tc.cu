@@ -13,9 +13,11 @@
 //                  the MMAs D = Q Lq_hi^T + Q Lq_lo^T (M = 128, N = m_pad,
 //                  exact to ~2^-16 of the fp32 landmarks) into one of two TMEM
 //                  buffers;
-//   warps 0-3:     one query row per thread: argmax over the m logits, the
-//                  route, and a shared-memory histogram of the head's routes
-//                  that is added to the per-head expert counts.
+//   warps 0-3, 5-8: two argmax warpgroups, one per TMEM buffer (tiles
+//                  alternate): one query row per thread, argmax over the m
+//                  logits, the route, and a shared-memory histogram (one per
+//                  warpgroup) of the head's routes that is added to the
+//                  per-head expert counts.
 // Every wait is bounded (umma.cuh).
 #include <algorithm>
 
@@ -41,13 +43,15 @@ struct RouteArgs {
     int m, m_pad;
 };
 
-__global__ void __launch_bounds__(160, 1) route_tc_kernel(const __grid_constant__ CUtensorMap tq,
+constexpr int RT_THREADS = 288;  // warps 0-3 and 5-8: argmax groups; warp 4: loads and MMAs
+
+__global__ void __launch_bounds__(RT_THREADS, 1) route_tc_kernel(const __grid_constant__ CUtensorMap tq,
                                                           const __grid_constant__ CUtensorMap thi,
                                                           const __grid_constant__ CUtensorMap tlo, RouteArgs a) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ uint64_t qfull[QST], qempty[QST], dfull[2], dfree[2], lqbar;
     __shared__ uint32_t tmem_base;
-    __shared__ int hist[256];
+    __shared__ int hist[2][256];
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int64_t t0 = a.total_tiles * blockIdx.x / gridDim.x;
@@ -61,12 +65,12 @@ __global__ void __launch_bounds__(160, 1) route_tc_kernel(const __grid_constant_
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&dfull[i], 1);
-            mbar_init(&dfree[i], 1);
+            mbar_init(&dfree[i], 128);  // every thread of the buffer's group arrives
         }
         mbar_init(&lqbar, 1);
         fence_barrier_init();
     }
-    for (int e = tid; e < 256; e += blockDim.x) hist[e] = 0;
+    for (int e = tid; e < 512; e += blockDim.x) hist[e >> 8][e & 255] = 0;
     if (warp == 0) tmem_alloc(&tmem_base, 512);
     tc_fence_before();
     __syncthreads();
@@ -120,27 +124,28 @@ __global__ void __launch_bounds__(160, 1) route_tc_kernel(const __grid_constant_
             }
         }
     } else {
-        // ---------------- argmax warpgroup (warps 0-3) ----------------
-        const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+        // ---------------- argmax warpgroups: group b takes the tiles t = b (mod 2) ----------------
+        const int b = warp < 4 ? 0 : 1;
+        const int row = (warp & 3) * 32 + lane;  // TMEM lane quarter = warp % 4
+        const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+        int* h = hist[b];
         int64_t cur = -1;
-        for (int t = 0; t < nt; ++t) {
+        for (int t = b; t < nt; t += 2) {
             const int64_t g = t0 + t;
             const int64_t bh = g / a.tiles_per_head, tile = g % a.tiles_per_head;
             if (bh != cur) {
-                named_bar(1, 128);
+                named_bar(1 + b, 128);
                 if (cur >= 0)
-                    for (int e = tid; e < a.m; e += 128)
-                        if (hist[e]) atomicAdd(&a.counts[cur * a.m + e], hist[e]);
-                named_bar(1, 128);
-                for (int e = tid; e < a.m; e += 128) hist[e] = 0;
+                    for (int e = row; e < a.m; e += 128)
+                        if (h[e]) atomicAdd(&a.counts[cur * a.m + e], h[e]);
+                named_bar(1 + b, 128);
+                for (int e = row; e < a.m; e += 128) h[e] = 0;
+                named_bar(1 + b, 128);
                 cur = bh;
             }
-            if (!named_bar_and(1, 128, mbar_wait(&dfull[t & 1], (t >> 1) & 1, a.status))) {
-                cur = -1;
-                break;
-            }
+            if (!named_bar_and(1 + b, 128, mbar_wait(&dfull[b], (t >> 1) & 1, a.status))) break;
             tc_fence_after();
-            const uint32_t d = tb + (t & 1) * 256 + lane_off;
+            const uint32_t d = tb + b * 256 + lane_off;
             // 4 interleaved (value, index) chains; on equal values the lower
             // index wins, as in a left-to-right scan with a strict comparison
             float bv[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
@@ -158,6 +163,8 @@ __global__ void __launch_bounds__(160, 1) route_tc_kernel(const __grid_constant_
                     }
                 }
             }
+            tc_fence_before();
+            mbar_arrive(&dfree[b]);
             float best = bv[0];
             int arg = bi[0];
 #pragma unroll
@@ -166,19 +173,16 @@ __global__ void __launch_bounds__(160, 1) route_tc_kernel(const __grid_constant_
                     best = bv[u];
                     arg = bi[u];
                 }
-            tc_fence_before();
-            named_bar(1, 128);
-            if (tid == 0) mbar_arrive(&dfree[t & 1]);
-            const int64_t n = tile * 128 + tid;
+            const int64_t n = tile * 128 + row;
             if (n < a.N) {
                 a.route[bh * a.N + n] = arg;
-                atomicAdd(&hist[arg], 1);
+                atomicAdd(&h[arg], 1);
             }
         }
-        named_bar(1, 128);
+        named_bar(1 + b, 128);
         if (cur >= 0)
-            for (int e = tid; e < a.m; e += 128)
-                if (hist[e]) atomicAdd(&a.counts[cur * a.m + e], hist[e]);
+            for (int e = row; e < a.m; e += 128)
+                if (h[e]) atomicAdd(&a.counts[cur * a.m + e], h[e]);
     }
     tc_fence_before();
     __syncthreads();
@@ -208,7 +212,7 @@ cudaError_t launch_route_tc(const Plan& p, const Work& w, const __nv_bfloat16* Q
                                          static_cast<int>(SMEM));
     if (e != cudaSuccess) return e;
     const int64_t grid = std::min<int64_t>(device_sms(), a.total_tiles);
-    route_tc_kernel<<<static_cast<unsigned>(grid), 160, SMEM, st>>>(tq, thi, tlo, a);
+    route_tc_kernel<<<static_cast<unsigned>(grid), RT_THREADS, SMEM, st>>>(tq, thi, tlo, a);
     return cudaGetLastError();
 }
 
