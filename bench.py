@@ -37,9 +37,10 @@ METRIC = "MiTA fwd queries/s at N=4K-1M, d=64; achieved fraction of roofline"
 DEFAULT_CONFIG = "long1m"
 SWEEP = ("lra", "long64k", "long256k")
 PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-STAGES = ("pool", "scan", "select", "route", "group", "expert")
-KERNEL_SOURCES = {"pool": "pool.cu", "scan": "scan_simt.cu", "select": "select.cu", "route": "route_simt.cu",
-                  "group": "group.cu", "expert": "expert_simt.cu"}
+STAGES = ("pool", "pilot", "scan", "select", "route", "group", "expert")
+# the source file of the kernel that runs each stage on the long-sequence workloads
+KERNEL_SOURCES = {"pool": "pool.cu", "pilot": "scan_tc.cu", "scan": "scan_tc.cu", "select": "select.cu",
+                  "route": "route_tc.cu", "group": "group.cu", "expert": "expert_tc.cu"}
 
 
 def describe(name):

@@ -146,12 +146,13 @@ int mita_sync_status(void* stream);
 /*
  * Stage timing (off by default). While enabled on a host thread, every
  * forward call made from that thread records CUDA events on its stream around
- * each stage: 0 landmark pooling, 1 landmark scan, 2 expert merge/selection,
- * 3 routing, 4 grouping, 5 expert attention. mita_profile_read() waits for
+ * each stage: 0 landmark pooling, 1 pilot scans (top-k thresholds from key
+ * samples), 2 landmark scan, 3 expert merge/selection, 4 routing,
+ * 5 grouping, 6 expert attention. mita_profile_read() waits for
  * `stream`, adds the elapsed times of all recorded calls on it to stage_ms
  * and the number of kernels each stage launched to stage_launches (arrays of
  * at least max_stages entries, either may be NULL), forgets those records and
- * returns the number of stages (6), or a MITA_ERR_* code.
+ * returns the number of stages (7), or a MITA_ERR_* code.
  */
 int mita_profile_enable(int on);
 int mita_profile_read(double* stage_ms, int64_t* stage_launches, int max_stages, void* stream);

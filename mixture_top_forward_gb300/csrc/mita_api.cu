@@ -284,8 +284,8 @@ namespace {
 // ---------------------------------------------------------------------------
 // Stage timing: per host thread, events recorded between stages.
 // ---------------------------------------------------------------------------
-constexpr int kStages = 6;
-const char* const kStageNames[kStages] = {"pool", "scan", "select", "route", "group", "expert"};
+constexpr int kStages = 7;
+const char* const kStageNames[kStages] = {"pool", "pilot", "scan", "select", "route", "group", "expert"};
 struct Recorded {
     cudaStream_t stream;
     cudaEvent_t ev[kStages + 1];
@@ -340,22 +340,24 @@ int run_forward(const Plan& P, const Work& W, const __nv_bfloat16* Q, const __nv
             if ((e = launch_scan_tc(P, W, K, V, l, st)) != cudaSuccess) return cuda_fail(e, "pilot scan launch");
             if ((e = launch_pilot_select(P, W, l, st)) != cudaSuccess) return cuda_fail(e, "pilot select launch");
         }
+        marks.mark(2);
         if ((e = launch_scan_tc(P, W, K, V, P.nlev - 1, st)) != cudaSuccess)
             return cuda_fail(e, "landmark scan launch");
-    } else if ((e = launch_scan(P, W, K, V, st)) != cudaSuccess) {
-        return cuda_fail(e, "landmark scan launch");
+    } else {
+        marks.mark(2);
+        if ((e = launch_scan(P, W, K, V, st)) != cudaSuccess) return cuda_fail(e, "landmark scan launch");
     }
-    marks.mark(2);
-    if ((e = launch_select(P, W, expert_idx, st)) != cudaSuccess) return cuda_fail(e, "expert selection launch");
     marks.mark(3);
-    if ((e = launch_route(P, W, Q, route, st)) != cudaSuccess) return cuda_fail(e, "routing launch");
+    if ((e = launch_select(P, W, expert_idx, st)) != cudaSuccess) return cuda_fail(e, "expert selection launch");
     marks.mark(4);
-    if ((e = launch_group(P, W, route, st)) != cudaSuccess) return cuda_fail(e, "grouping launch");
+    if ((e = launch_route(P, W, Q, route, st)) != cudaSuccess) return cuda_fail(e, "routing launch");
     marks.mark(5);
+    if ((e = launch_group(P, W, route, st)) != cudaSuccess) return cuda_fail(e, "grouping launch");
+    marks.mark(6);
     if ((e = launch_expert(P, W, Q, K, V, expert_idx, out, st)) != cudaSuccess)
         return cuda_fail(e, "expert attention launch");
-    marks.mark(6);
-    const int launches[kStages] = {1, P.scan_tc ? 2 * P.nlev - 1 : 1, 1, 1, 2, 1};
+    marks.mark(7);
+    const int launches[kStages] = {1, P.scan_tc ? 2 * (P.nlev - 1) : 0, 1, 1, 1, 2, 1};
     marks.commit(launches);
     if (lq_out && (e = cudaMemcpyAsync(lq_out, W.lq32, mrows * D * sizeof(float), cudaMemcpyDeviceToDevice, st)) !=
                       cudaSuccess)

@@ -64,6 +64,6 @@ def test_workspace_bytes(lib):
 
 
 def test_stage_names(lib):
-    names = [M.mita_stage_name(i) for i in range(6)]
-    assert names == ["pool", "scan", "select", "route", "group", "expert"]
-    assert M.mita_stage_name(6) is None
+    names = [M.mita_stage_name(i) for i in range(7)]
+    assert names == ["pool", "pilot", "scan", "select", "route", "group", "expert"]
+    assert M.mita_stage_name(7) is None
