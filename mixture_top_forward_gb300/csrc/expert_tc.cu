@@ -11,28 +11,30 @@
 // list (<= 128 queries of one expert per item), in rounds of up to two items
 // of the same expert, one per row warpgroup. The expert's key list
 // [Lq_0..Lq_{m-1}, K_e] and value list [LV_0..LV_{m-1}, V_e] (bf16, 128-byte
-// swizzled rows, zero padded to whole 64-row blocks) stay in shared memory
+// swizzled rows, zero padded to whole 128-row blocks) stay in shared memory
 // while consecutive rounds share the expert.
 //   warp 0:         producer: gathers the key/value lists when the expert
 //                   changes (the shared rows only when the head changes) and
-//                   each item's query rows (through the grouping permutation),
-//                   all with cp.async;
-//   warps 1, 2 (lane 0): one MMA issuer per warpgroup: per 64-key block j of its
-//                   item, S = Q keys_j^T into one of two TMEM buffers, and one
-//                   block later O += P_j values_j into the warpgroup's TMEM
-//                   accumulator;
+//                   each item's query rows (through the grouping permutation)
+//                   into the warpgroup's next query buffer, all with cp.async;
+//   warps 1, 2 (lane 0): one MMA issuer per warpgroup: per 128-key block j of
+//                   its item, S = Q keys_j^T (A and B in shared memory) into
+//                   the warpgroup's TMEM score columns, and one block later
+//                   O += P_j values_j with P read from TMEM (A in tensor
+//                   memory, B in shared memory) into its TMEM accumulator;
 //   warps 3-6, 7-10: one warpgroup per item (4 consecutive warps cover the 4
 //                   TMEM lane quarters), one thread per query row: load the
-//                   64 logits, update the running max (kept while it grows by
+//                   128 logits, update the running max (kept while it grows by
 //                   < 2^8, so O rarely needs rescaling), p = 2^(s tau log2e -
-//                   max) in registers, P (bf16) into shared memory once the
+//                   max) in registers, P as bf16 pairs into TMEM once the
 //                   previous block's P.V is done; at the end O / rowsum ->
-//                   bf16 -> the query's row. Query rows are double-buffered, so
-//                   the producer gathers the next item while this one runs.
+//                   bf16 -> the query's row.
+// TMEM per warpgroup: 128 columns of S, 64 of P (bf16 pairs), 64 of O.
 // Handshakes are mbarriers, each completed exactly once per event its waiter
-// consumes; row threads arrive individually (128-arrival barriers) and make
+// consumes; row warps arrive once each (4-arrival barriers) and make
 // their waits warp-uniform, so no named barrier can block forever. Every
 // wait is bounded (umma.cuh).
+#include "tensormap.cuh"
 #include "umma.cuh"
 
 namespace mita {
@@ -43,22 +45,16 @@ using namespace umma;
 
 constexpr float kC = 0.125f * kLog2e;  // tau * log2(e), tau = 1/sqrt(64)
 constexpr float kLazy = 8.0f;          // keep the running max while the new one is within 2^8
-constexpr int KB = 64;                 // keys per block
-constexpr int NWG = 3;                 // row warpgroups
-constexpr int QB = 1;                  // query-row buffers per warpgroup
-constexpr int SB = 1;                  // TMEM score buffers per warpgroup
+constexpr int KB = 128;                // keys per block
+constexpr int NWG = 2;                 // row warpgroups
+constexpr int QB = 2;                  // query-row buffers per warpgroup
 constexpr int NT = 32 * (1 + NWG) + NWG * 128;  // producer, one issuer warp per group, rows
-constexpr uint32_t kTStride = (SB + 1) * 64;    // TMEM columns per warpgroup: SB x S, then O
+constexpr uint32_t kTStride = 256;              // TMEM columns per warpgroup
+constexpr uint32_t kTP = 128, kTO = 192;        // P and O column offsets inside them
 static_assert(NWG * kTStride <= 512, "TMEM holds 512 columns");
-constexpr uint32_t kIdescS = idesc_bf16(128, KB, false);
 constexpr uint32_t kIdescPV = idesc_bf16(128, 64, true);
 
 struct Args {
-    const __nv_bfloat16* Q;
-    const __nv_bfloat16* K;
-    const __nv_bfloat16* V;
-    const __nv_bfloat16* lqhi;
-    const __nv_bfloat16* lvbf;
     const int4* items;
     const int* nitems;
     const int* perm;
@@ -70,18 +66,16 @@ struct Args {
 };
 
 struct Layout {
-    uint8_t* keys;  // nblk * 8 KB
-    uint8_t* vals;  // nblk * 8 KB
+    uint8_t* keys;  // nblk * 16 KB
+    uint8_t* vals;  // nblk * 16 KB
     uint8_t* q;     // [NWG][QB] * 16 KB: query rows
-    uint8_t* p;     // [NWG] * 16 KB: P of the current block
 };
 
 __device__ __forceinline__ Layout layout(uint8_t* base, int nblk) {
     Layout L;
     L.keys = base;
-    L.vals = L.keys + nblk * 8192;
-    L.q = L.vals + nblk * 8192;
-    L.p = L.q + NWG * QB * 16384;
+    L.vals = L.keys + nblk * 16384;
+    L.q = L.vals + nblk * 16384;
     return L;
 }
 
@@ -100,31 +94,42 @@ __device__ __forceinline__ int round_size(const Args& a, int r, int i1, int4* it
 
 __device__ __forceinline__ void zero16(uint8_t* p) { *reinterpret_cast<uint4*>(p) = make_uint4(0, 0, 0, 0); }
 
-__global__ void __launch_bounds__(NT, 1) expert_tc_kernel(Args a) {
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__global__ void __launch_bounds__(NT, 1)
+    expert_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                     const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tlq,
+                     const __grid_constant__ CUtensorMap tlv, Args a) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ uint64_t kvfull, kvfree, qfull[NWG * QB], qfree[NWG * QB], ofree[NWG];
-    __shared__ uint64_t sfull[NWG * SB], sfree[NWG * SB], pfull[NWG], pvdone[NWG];
+    __shared__ uint64_t sfull[NWG], sfree[NWG], pfull[NWG], pvdone[NWG];
     __shared__ uint32_t tmem_base;
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const Layout S = layout(base, a.nblk);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int nkeys = a.m + a.k;
+    // key rows: [0, m) shared, [m, m4) unused, [m4, m4 + k) routed (m4 = m
+    // rounded up to 4, so every 4-row gather starts 512-byte aligned)
+    const int m4 = (a.m + 3) & ~3;
+    const int nkeys = m4 + a.k;
+    // width of the last key block: its rows rounded up to the MMA's N step
+    const int wlast = ((nkeys - (a.nblk - 1) * KB) + 15) & ~15;
 
     if (tid == 0) {
         mbar_init(&kvfull, 1);
         mbar_init(&kvfree, NWG);  // one commit per MMA issuer
         for (int w = 0; w < NWG; ++w) {
-            mbar_init(&ofree[w], 128);
-            mbar_init(&pfull[w], 128);
+            mbar_init(&ofree[w], 4);  // one arrival per row warp
+            mbar_init(&pfull[w], 4);
             mbar_init(&pvdone[w], 1);
+            mbar_init(&sfull[w], 1);
+            mbar_init(&sfree[w], 4);
         }
         for (int b = 0; b < NWG * QB; ++b) {
             mbar_init(&qfull[b], 1);
             mbar_init(&qfree[b], 1);
-        }
-        for (int b = 0; b < NWG * SB; ++b) {
-            mbar_init(&sfull[b], 1);
-            mbar_init(&sfree[b], 128);
         }
         fence_barrier_init();
     }
@@ -140,6 +145,17 @@ __global__ void __launch_bounds__(NT, 1) expert_tc_kernel(Args a) {
 
     if (warp == 0) {
         // ------------------------------ producer ------------------------------
+        // Every row arrives by TMA 4-row gathers that complete on the consumer's
+        // mbarrier: the producer never waits for its own copies. Rows past the
+        // last gather stay zero (their logits are masked; their values must be
+        // finite).
+        const int rows = a.nblk * KB;
+        for (int x = ((nkeys + 3) & ~3) * 8 + lane; x < rows * 8; x += 32) {
+            zero16(S.keys + swz128(x >> 3, x & 7));
+            zero16(S.vals + swz128(x >> 3, x & 7));
+        }
+        fence_proxy_async();
+        __syncwarp();
         int64_t cur_bh = -1;
         int cur_e = -1, changes = 0;
         uint32_t nq[NWG] = {};
@@ -151,45 +167,28 @@ __global__ void __launch_bounds__(NT, 1) expert_tc_kernel(Args a) {
                 // wait until the MMAs reading the previous lists are done
                 if (changes > 0) ok = __all_sync(0xffffffffu, mbar_wait(&kvfree, (changes - 1) & 1, a.status));
                 if (!ok) break;
-                const int64_t bh = it[0].w;
-                const int32_t* sel = a.expert_idx + (bh * a.m + it[0].x) * static_cast<int64_t>(a.k);
-                const int r0 = (it[0].w != cur_bh) ? 0 : a.m;  // shared rows only on a new head
-                const uint32_t kb = smem_u32(S.keys), vb = smem_u32(S.vals);
-                // lane l stages rows r0 + l, r0 + l + 32, ...: the row indices of a
-                // batch of 8 rows are loaded first, then all of their copies issued
-                const int rows = a.nblk * KB;
-                for (int rb = r0; rb < rows; rb += 32 * 8) {
-                    int64_t src[8];
-#pragma unroll
-                    for (int u = 0; u < 8; ++u) {
-                        const int row = rb + u * 32 + lane;
-                        src[u] = -1;
-                        if (row < a.m) src[u] = (bh * a.m + row) * D;
-                        else if (row < nkeys) src[u] = (bh * a.N + sel[row - a.m]) * D;
-                    }
-#pragma unroll
-                    for (int u = 0; u < 8; ++u) {
-                        const int row = rb + u * 32 + lane;
-                        if (row >= rows) continue;
-                        const __nv_bfloat16* ks = row < a.m ? a.lqhi : a.K;
-                        const __nv_bfloat16* vs = row < a.m ? a.lvbf : a.V;
-#pragma unroll
-                        for (int c = 0; c < 8; ++c) {
-                            const uint32_t off = swz128(row, c);
-                            if (src[u] >= 0) {
-                                cp_async16(kb + off, ks + src[u] + c * 8);
-                                cp_async16(vb + off, vs + src[u] + c * 8);
-                            } else {
-                                zero16(S.keys + off);
-                                zero16(S.vals + off);
-                            }
-                        }
-                    }
-                }
-                cp_async_wait_all();
-                fence_proxy_async();
+                const int bh = it[0].w;
+                const int32_t* sel = a.expert_idx + (static_cast<int64_t>(bh) * a.m + it[0].x) * a.k;
+                const int ns = it[0].w != cur_bh ? m4 / 4 : 0;  // shared rows only on a new head
+                const int nr = (a.k + 3) / 4;
+                if (lane == 0) mbar_arrive_expect_tx(&kvfull, static_cast<uint32_t>(ns + nr) * 1024u);
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&kvfull);
+                for (int g = lane; g < ns; g += 32) {  // shared rows 4g..4g+3 (the last ones repeat row m-1)
+                    const int y = bh * a.m;
+                    const int r0 = 4 * g;
+                    const int y0 = y + min(r0, a.m - 1), y1 = y + min(r0 + 1, a.m - 1);
+                    const int y2 = y + min(r0 + 2, a.m - 1), y3 = y + min(r0 + 3, a.m - 1);
+                    tma_gather4(S.keys + r0 * 128, &tlq, 0, y0, y1, y2, y3, &kvfull);
+                    tma_gather4(S.vals + r0 * 128, &tlv, 0, y0, y1, y2, y3, &kvfull);
+                }
+                for (int g = lane; g < nr; g += 32) {  // routed rows m4 + 4g.. (the last ones repeat key k-1)
+                    const int r0 = 4 * g;
+                    const int y = bh * static_cast<int>(a.N);
+                    const int y0 = y + sel[min(r0, a.k - 1)], y1 = y + sel[min(r0 + 1, a.k - 1)];
+                    const int y2 = y + sel[min(r0 + 2, a.k - 1)], y3 = y + sel[min(r0 + 3, a.k - 1)];
+                    tma_gather4(S.keys + (m4 + r0) * 128, &tk, 0, y0, y1, y2, y3, &kvfull);
+                    tma_gather4(S.vals + (m4 + r0) * 128, &tv, 0, y0, y1, y2, y3, &kvfull);
+                }
                 cur_bh = it[0].w;
                 cur_e = it[0].x;
                 ++changes;
@@ -200,30 +199,15 @@ __global__ void __launch_bounds__(NT, 1) expert_tc_kernel(Args a) {
                 if (nq[w] >= QB)
                     ok = __all_sync(0xffffffffu, mbar_wait(&qfree[qb], ((nq[w] / QB) - 1) & 1, a.status));
                 if (!ok) break;
-                const int64_t bh = it[w].w;
-                const uint32_t qa = smem_u32(S.q + qb * 16384);
-                // lane l gathers rows l, l+32, l+64, l+96: indices first, then copies
-                int n[4];
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const int row = u * 32 + lane;
-                    n[u] = row < it[w].z ? a.perm[bh * a.N + it[w].y + row] : -1;
-                }
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const int row = u * 32 + lane;
-#pragma unroll
-                    for (int c = 0; c < 8; ++c) {
-                        if (n[u] >= 0)
-                            cp_async16(qa + swz128(row, c), a.Q + (bh * a.N + n[u]) * D + c * 8);
-                        else
-                            zero16(S.q + qb * 16384 + swz128(row, c));
-                    }
-                }
-                cp_async_wait_all();
-                fence_proxy_async();
+                if (lane == 0) mbar_arrive_expect_tx(&qfull[qb], 16384u);
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&qfull[qb]);
+                // lane l gathers query rows 4l..4l+3; rows past the item repeat its last query
+                const int bh = it[w].w;
+                const int* pp = a.perm + static_cast<int64_t>(bh) * a.N + it[w].y;
+                const int last = it[w].z - 1, r0 = 4 * lane;
+                const int y = bh * static_cast<int>(a.N);
+                tma_gather4(S.q + qb * 16384 + r0 * 128, &tq, 0, y + pp[min(r0, last)], y + pp[min(r0 + 1, last)],
+                            y + pp[min(r0 + 2, last)], y + pp[min(r0 + 3, last)], &qfull[qb]);
                 ++nq[w];
             }
             r += cnt;
@@ -237,8 +221,7 @@ __global__ void __launch_bounds__(NT, 1) expert_tc_kernel(Args a) {
             int cur_e = -1, changes = 0;
             uint32_t nq = 0, gb = 0;
             const uint32_t ka = smem_u32(S.keys), va = smem_u32(S.vals);
-            const uint32_t pa = smem_u32(S.p + w * 16384);
-            const uint32_t tO = tb + w * kTStride + SB * 64;
+            const uint32_t tS = tb + w * kTStride, tP = tS + kTP, tO = tS + kTO;
             bool ok = true;
             for (int r = i0; r < i1 && ok;) {
                 int4 it[NWG];
@@ -258,18 +241,19 @@ __global__ void __launch_bounds__(NT, 1) expert_tc_kernel(Args a) {
                     // S for block j, then P.V for block j-1
                     for (int j = 0; j <= a.nblk && ok; ++j) {
                         if (j < a.nblk) {
-                            const uint32_t g = gb + j, sb = g % SB;
-                            if (g >= SB) {  // the rows have read this S buffer (block g - SB)
-                                ok = mbar_wait(&sfree[w * SB + sb], ((g / SB) - 1) & 1, a.status);
+                            const uint32_t g = gb + j;
+                            if (g >= 1) {  // the rows have read the previous S
+                                ok = mbar_wait(&sfree[w], (g - 1) & 1, a.status);
                                 if (!ok) break;
                                 tc_fence_after();
                             }
-                            const uint32_t tS = tb + w * kTStride + sb * KB;
+                            const int width = j == a.nblk - 1 ? wlast : KB;
+                            const uint32_t idesc = idesc_bf16(128, width, false);
 #pragma unroll
                             for (int s = 0; s < 4; ++s)
-                                mma_ss(tS, sdesc_sw128(qa + s * 32), sdesc_sw128(ka + j * 8192 + s * 32), kIdescS,
+                                mma_ss(tS, sdesc_sw128(qa + s * 32), sdesc_sw128(ka + j * 16384 + s * 32), idesc,
                                        s > 0);
-                            mma_commit(&sfull[w * SB + sb]);
+                            mma_commit(&sfull[w]);
                             if (j == a.nblk - 1) mma_commit(&qfree[qb]);
                         }
                         if (j > 0) {
@@ -280,10 +264,10 @@ __global__ void __launch_bounds__(NT, 1) expert_tc_kernel(Args a) {
                             if (ok) ok = mbar_wait(&pfull[w], g & 1, a.status);
                             if (!ok) break;
                             tc_fence_after();
-#pragma unroll
-                            for (int s = 0; s < 4; ++s)
-                                mma_ss(tO, sdesc_sw128(pa + s * 32), sdesc_sw128(va + (j - 1) * 8192 + s * 2048),
-                                       kIdescPV, (j > 1 || s > 0) ? 1u : 0u);
+                            const int steps = (j == a.nblk ? wlast : KB) / 16;
+                            for (int s = 0; s < steps; ++s)
+                                mma_ts(tO, tP + s * 8, sdesc_sw128(va + (j - 1) * 16384 + s * 2048), kIdescPV,
+                                       (j > 1 || s > 0) ? 1u : 0u);
                             mma_commit(&pvdone[w]);
                         }
                     }
@@ -299,8 +283,8 @@ __global__ void __launch_bounds__(NT, 1) expert_tc_kernel(Args a) {
         const int w = (warp - 1 - NWG) >> 2;  // 4 consecutive warps cover the 4 TMEM lane quarters
         const int t = (warp & 3) * 32 + lane;  // TMEM lane = query row of the item
         const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-        const uint32_t tO = tb + w * kTStride + SB * 64;
-        uint32_t gb = 0, nitem = 0;
+        const uint32_t tS = tb + w * kTStride + lane_off, tP = tS + kTP, tO = tS + kTO;
+        uint32_t gb = 0;
         bool ok = true;
         for (int r = i0; r < i1 && ok;) {
             int4 it[NWG];
@@ -312,45 +296,50 @@ __global__ void __launch_bounds__(NT, 1) expert_tc_kernel(Args a) {
             const int n = t < item.z ? a.perm[bh * a.N + item.y + t] : 0;
             float mrun = -INFINITY, lrun = 0.f;
             for (int j = 0; j < a.nblk; ++j, ++gb) {
-                const uint32_t sb = gb % SB;
-                ok = __all_sync(0xffffffffu, mbar_wait(&sfull[w * SB + sb], (gb / SB) & 1, a.status));
+                ok = __all_sync(0xffffffffu, mbar_wait(&sfull[w], gb & 1, a.status));
                 if (!ok) break;
                 tc_fence_after();
                 float s[KB];
-                tmem_ld32(tb + w * kTStride + sb * KB + lane_off, s);
-                tmem_ld32(tb + w * kTStride + sb * KB + lane_off + 32, s + 32);
+#pragma unroll
+                for (int c = 0; c < KB; c += 32) tmem_ld32(tS + c, s + c);
                 tmem_ld_wait();
                 tc_fence_before();
-                mbar_arrive(&sfree[w * SB + sb]);
-                const int valid = min(KB, nkeys - j * KB);
-                if (valid < KB) {  // last, partial block (warp-uniform)
+                warp_arrive(&sfree[w]);
+                const int k0 = j * KB;  // key row of column 0
+                if (k0 + KB > nkeys || (k0 < m4 && k0 + KB > a.m && m4 > a.m)) {
+                    // (warp-uniform) the block holds the unused rows [m, m4) or
+                    // ends past the key list, where columns are stale
 #pragma unroll
-                    for (int c = 0; c < KB; ++c) s[c] = c < valid ? s[c] : -INFINITY;
+                    for (int c = 0; c < KB; ++c) {
+                        const int g = k0 + c;
+                        s[c] = (g >= nkeys || (g >= a.m && g < m4)) ? -INFINITY : s[c];
+                    }
                 }
-                // 8 independent partial maxima / sums: short dependency chains
+                // 8 independent partial maxima: short dependency chains
                 float pm[8];
-                static_assert(KB == 64, "the partial maxima below cover exactly 64 columns");
+                static_assert(KB == 128, "the partial maxima below cover exactly 128 columns");
 #pragma unroll
-                for (int u = 0; u < 8; ++u) {  // columns u, u+8, ..., u+56
-                    pm[u] = fmax3(s[u], s[u + 8], s[u + 16]);
-                    pm[u] = fmax3(pm[u], s[u + 24], s[u + 32]);
-                    pm[u] = fmax3(pm[u], s[u + 40], s[u + 48]);
-                    pm[u] = fmaxf(pm[u], s[u + 56]);
+                for (int u = 0; u < 8; ++u) {  // columns u, u+8, ..., u+120
+                    float x = fmax3(s[u], s[u + 8], s[u + 16]);
+#pragma unroll
+                    for (int i = 3; i < 15; i += 2) x = fmax3(x, s[u + 8 * i], s[u + 8 * i + 8]);
+                    pm[u] = fmaxf(x, s[u + 120]);
                 }
                 const float bmax = fmaxf(fmax3(pm[0], pm[1], pm[2]), fmax3(fmax3(pm[3], pm[4], pm[5]), pm[6], pm[7])) * kC;
                 const float mnew = (bmax > mrun + kLazy) ? bmax : mrun;
                 const float alpha = exp2f(mrun - mnew);  // 0 on the first block, 1 when the max is kept
                 // packed pairs: one f32x2 FMA forms two exponents, one f32x2 add
-                // accumulates two weights
+                // accumulates two weights; P goes out as bf16 pairs
                 const float2 c2 = make_float2(kC, kC), m2 = make_float2(-mnew, -mnew);
                 float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                                  make_float2(0.f, 0.f)};
+                uint32_t pk[KB / 2];
 #pragma unroll
                 for (int c = 0; c < KB; c += 2) {
                     const float2 x = __ffma2_rn(make_float2(s[c], s[c + 1]), c2, m2);
-                    s[c] = exp2f(x.x);
-                    s[c + 1] = exp2f(x.y);
-                    acc[(c >> 1) & 3] = __fadd2_rn(acc[(c >> 1) & 3], make_float2(s[c], s[c + 1]));
+                    const float2 e = make_float2(exp2f(x.x), exp2f(x.y));
+                    acc[(c >> 1) & 3] = __fadd2_rn(acc[(c >> 1) & 3], e);
+                    pk[c >> 1] = pack_bf16(e.x, e.y);
                 }
                 const float sum = ((acc[0].x + acc[0].y) + (acc[1].x + acc[1].y)) + ((acc[2].x + acc[2].y) + (acc[3].x + acc[3].y));
                 lrun = lrun * alpha + sum;
@@ -366,26 +355,18 @@ __global__ void __launch_bounds__(NT, 1) expert_tc_kernel(Args a) {
                     float o[16];
 #pragma unroll
                     for (int h = 0; h < 4; ++h) {
-                        tmem_ld16(tO + lane_off + h * 16, o);
+                        tmem_ld16(tO + h * 16, o);
                         tmem_ld_wait();
 #pragma unroll
                         for (int c = 0; c < 16; ++c) o[c] *= alpha;
-                        tmem_st16(tO + lane_off + h * 16, o);
+                        tmem_st16(tO + h * 16, o);
                     }
-                    tmem_st_wait();
                 }
-                uint8_t* pdst = S.p + w * 16384;
-#pragma unroll
-                for (int g = 0; g < KB / 8; ++g) {
-                    uint4 pk;
-                    __nv_bfloat162* h2 = reinterpret_cast<__nv_bfloat162*>(&pk);
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) h2[u] = __floats2bfloat162_rn(s[8 * g + 2 * u], s[8 * g + 2 * u + 1]);
-                    *reinterpret_cast<uint4*>(pdst + swz128(t, g)) = pk;
-                }
-                fence_proxy_async();
+                tmem_st32u(tP, pk);
+                tmem_st32u(tP + 32, pk + 32);
+                tmem_st_wait();
                 tc_fence_before();
-                mbar_arrive(&pfull[w]);
+                warp_arrive(&pfull[w]);
                 mrun = mnew;
             }
             if (!ok) break;
@@ -398,51 +379,46 @@ __global__ void __launch_bounds__(NT, 1) expert_tc_kernel(Args a) {
 #pragma unroll
             for (int h = 0; h < 2; ++h) {  // two 32-column halves of the output row
                 float o[32];
-                tmem_ld32(tO + lane_off + h * 32, o);
+                tmem_ld32(tO + h * 32, o);
                 tmem_ld_wait();
                 if (h == 1) {
                     tc_fence_before();
-                    mbar_arrive(&ofree[w]);
+                    warp_arrive(&ofree[w]);
                 }
                 if (t < item.z) {
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
-                        uint4 pk;
-                        __nv_bfloat162* h2 = reinterpret_cast<__nv_bfloat162*>(&pk);
-#pragma unroll
-                        for (int u = 0; u < 4; ++u)
-                            h2[u] = __floats2bfloat162_rn(o[8 * c + 2 * u] * inv, o[8 * c + 2 * u + 1] * inv);
-                        dst[h * 4 + c] = pk;
+                        uint4 q;
+                        q.x = pack_bf16(o[8 * c + 0] * inv, o[8 * c + 1] * inv);
+                        q.y = pack_bf16(o[8 * c + 2] * inv, o[8 * c + 3] * inv);
+                        q.z = pack_bf16(o[8 * c + 4] * inv, o[8 * c + 5] * inv);
+                        q.w = pack_bf16(o[8 * c + 6] * inv, o[8 * c + 7] * inv);
+                        dst[h * 4 + c] = q;
                     }
                 }
             }
-            ++nitem;
         }
-        (void)nitem;
     }
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_free(tb, 512);
 }
 
-size_t smem_bytes(int nblk) { return 1024 + static_cast<size_t>(nblk) * 16384 + NWG * (QB * 16384 + 16384); }
+size_t smem_bytes(int nblk) { return 1024 + static_cast<size_t>(nblk) * 32768 + NWG * QB * 16384; }
+
+int key_rows(const Plan& p) { return ((p.s.m + 3) & ~3) + p.s.k; }
 
 }  // namespace
 
 bool expert_tc_supported(const Plan& p) {
-    const int nkeys = p.s.m + p.s.k;
-    return nkeys <= 512 && smem_bytes((nkeys + KB - 1) / KB) <= 232448;
+    return key_rows(p) <= 512 && p.s.BH * p.s.N < (int64_t(1) << 31) &&
+           smem_bytes((key_rows(p) + KB - 1) / KB) <= 232448;
 }
 
 cudaError_t launch_expert_tc(const Plan& p, const Work& w, const __nv_bfloat16* Q, const __nv_bfloat16* K,
                              const __nv_bfloat16* V, const int32_t* expert_idx, __nv_bfloat16* out,
                              cudaStream_t st) {
     Args a;
-    a.Q = Q;
-    a.K = K;
-    a.V = V;
-    a.lqhi = w.lqhi;
-    a.lvbf = w.lvbf;
     a.items = w.items;
     a.nitems = w.nitems;
     a.perm = w.perm;
@@ -452,12 +428,17 @@ cudaError_t launch_expert_tc(const Plan& p, const Work& w, const __nv_bfloat16* 
     a.N = p.s.N;
     a.m = p.s.m;
     a.k = p.s.k;
-    a.nblk = (p.s.m + p.s.k + KB - 1) / KB;
+    a.nblk = (key_rows(p) + KB - 1) / KB;
+    CUtensorMap tq, tk, tv, tlq, tlv;
+    const uint64_t rows = static_cast<uint64_t>(p.s.BH) * p.s.N, lrows = static_cast<uint64_t>(p.s.BH) * p.s.m;
+    if (!make_row_tmap(&tq, Q, rows, 1) || !make_row_tmap(&tk, K, rows, 1) || !make_row_tmap(&tv, V, rows, 1) ||
+        !make_row_tmap(&tlq, w.lqhi, lrows, 1) || !make_row_tmap(&tlv, w.lvbf, lrows, 1))
+        return cudaErrorInvalidValue;
     const size_t sm = smem_bytes(a.nblk);
     cudaError_t e = cudaFuncSetAttribute(expert_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(sm));
     if (e != cudaSuccess) return e;
-    expert_tc_kernel<<<device_sms(), NT, sm, st>>>(a);
+    expert_tc_kernel<<<device_sms(), NT, sm, st>>>(tq, tk, tv, tlq, tlv, a);
     return cudaGetLastError();
 }
 

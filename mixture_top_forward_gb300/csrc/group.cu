@@ -12,9 +12,10 @@
 //     items (expert, start, length <= qtile, head) for the attention kernel,
 //     appended to one flat list: each head reserves its range with one global
 //     atomic, and keeps its items in expert order inside it;
-//  3. scatter_kernel (one CTA per 256 queries): counts its queries per expert
-//     in shared memory, reserves a range of each expert's segment with one
-//     global atomic per (CTA, expert), and writes the query indices there.
+//  3. scatter_kernel (one CTA per 4096 queries of a head): counts its queries
+//     per expert in shared memory, reserves a range of each expert's segment
+//     with one global atomic per (CTA, expert), and writes the query indices
+//     there (each expert's queries of the CTA land contiguously).
 // The order of queries inside a segment depends on CTA timing; it does not
 // affect any result, because every query's attention is computed on its own.
 #include "mita_internal.cuh"
@@ -24,7 +25,8 @@ namespace mita {
 namespace {
 
 constexpr int GT = 1024;  // threads of the offsets kernel (>= MITA_MAX_M_INTERNAL)
-constexpr int SCT = 256;  // queries per scatter CTA
+constexpr int SCT = 1024;  // threads per scatter CTA
+constexpr int SQT = 4;     // queries per scatter thread
 
 __global__ void __launch_bounds__(GT) offsets_kernel(int m, int64_t N, int qtile, int* __restrict__ counts,
                                                      int* __restrict__ expoff, int* __restrict__ cursor,
@@ -71,20 +73,22 @@ __global__ void __launch_bounds__(SCT) scatter_kernel(const int32_t* __restrict_
     __shared__ int sh[MITA_MAX_M_INTERNAL];
     const int64_t blk = blockIdx.x % nblocks;
     const int64_t bh = blockIdx.x / nblocks;
-    const int64_t n = blk * SCT + threadIdx.x;
-    const bool valid = n < N;
     for (int e = threadIdx.x; e < m; e += SCT) sh[e] = 0;
     __syncthreads();
-    int e = 0, rank = 0;
-    if (valid) {
-        e = route[bh * N + n];
-        rank = atomicAdd(&sh[e], 1);
-    }
+    // query n0 + u * SCT (u < SQT): consecutive threads read consecutive routes
+    const int64_t n0 = blk * (SCT * SQT) + threadIdx.x;
+    int e[SQT], rank[SQT];
+#pragma unroll
+    for (int u = 0; u < SQT; ++u) e[u] = n0 + u * SCT < N ? route[bh * N + n0 + u * SCT] : -1;
+#pragma unroll
+    for (int u = 0; u < SQT; ++u) rank[u] = e[u] >= 0 ? atomicAdd(&sh[e[u]], 1) : 0;
     __syncthreads();
     for (int x = threadIdx.x; x < m; x += SCT)
         if (sh[x]) sh[x] = atomicAdd(&cursor[bh * m + x], sh[x]);
     __syncthreads();
-    if (valid) perm[bh * N + sh[e] + rank] = static_cast<int>(n);
+#pragma unroll
+    for (int u = 0; u < SQT; ++u)
+        if (e[u] >= 0) perm[bh * N + sh[e[u]] + rank[u]] = static_cast<int>(n0 + u * SCT);
 }
 
 }  // namespace
@@ -92,7 +96,7 @@ __global__ void __launch_bounds__(SCT) scatter_kernel(const int32_t* __restrict_
 cudaError_t launch_group(const Plan& p, const Work& w, const int32_t* route, cudaStream_t st) {
     offsets_kernel<<<static_cast<unsigned>(p.s.BH), GT, 0, st>>>(p.s.m, p.s.N, p.qtile, w.counts, w.expoff,
                                                                  w.cursor, w.items, w.nitems);
-    const int64_t nblocks = (p.s.N + SCT - 1) / SCT;
+    const int64_t nblocks = (p.s.N + SCT * SQT - 1) / (SCT * SQT);
     scatter_kernel<<<static_cast<unsigned>(p.s.BH * nblocks), SCT, 0, st>>>(route, p.s.N, p.s.m, nblocks, w.cursor,
                                                                             w.perm);
     return cudaGetLastError();

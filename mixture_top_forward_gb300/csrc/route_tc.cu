@@ -65,7 +65,7 @@ __global__ void __launch_bounds__(RT_THREADS, 1) route_tc_kernel(const __grid_co
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&dfull[i], 1);
-            mbar_init(&dfree[i], 128);  // every thread of the buffer's group arrives
+            mbar_init(&dfree[i], 4);  // every warp of the buffer's group arrives
         }
         mbar_init(&lqbar, 1);
         fence_barrier_init();
@@ -164,7 +164,7 @@ __global__ void __launch_bounds__(RT_THREADS, 1) route_tc_kernel(const __grid_co
                 }
             }
             tc_fence_before();
-            mbar_arrive(&dfree[b]);
+            warp_arrive(&dfree[b]);
             float best = bv[0];
             int arg = bi[0];
 #pragma unroll

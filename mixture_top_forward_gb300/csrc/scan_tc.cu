@@ -142,8 +142,8 @@ __global__ void __launch_bounds__(Cfg<FULL, NL>::NT, 1)
         }
         for (int l = 0; l < NL * 2; ++l) {
             mbar_init(&sfull[l], 1);
-            mbar_init(&sfree[l], 128);  // every row thread arrives after reading S
-            mbar_init(&pfull[l], 128);  // every row thread arrives after writing its P row
+            mbar_init(&sfree[l], 4);  // every row warp arrives after reading S
+            mbar_init(&pfull[l], 4);  // every row warp arrives after writing its P rows
             mbar_init(&pvdone[l], 1);
         }
         fence_barrier_init();
@@ -260,7 +260,7 @@ __global__ void __launch_bounds__(Cfg<FULL, NL>::NT, 1)
             tmem_ld32(tb + L * 256 + sb * KT + lane_off + 32, s + 32);
             tmem_ld_wait();
             tc_fence_before();
-            mbar_arrive(&sfree[L * 2 + sb]);
+            warp_arrive(&sfree[L * 2 + sb]);
             const int64_t col0 = s0 + static_cast<int64_t>(i) * KT;
             const int nvalid = static_cast<int>(s1 - col0 < KT ? s1 - col0 : KT);
             if (nvalid < KT) {  // last, partial tile of the chunk (warp-uniform)
@@ -378,7 +378,7 @@ __global__ void __launch_bounds__(Cfg<FULL, NL>::NT, 1)
                 }
                 fence_proxy_async();
                 tc_fence_before();
-                mbar_arrive(&pfull[pb]);
+                warp_arrive(&pfull[pb]);
                 mrun = mnew;
             }
         }
