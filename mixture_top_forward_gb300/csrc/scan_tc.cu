@@ -15,9 +15,13 @@
 //   warp 0:        TMEM allocation; lane 0: TMA producer of 128-key tiles of
 //                  K (3-4 stage ring); lane 1: TMA producer of V tiles (2-3
 //                  stages; full scans only);
-//   warp 1 lane 0: MMA issuer: S_L = Lq_L K^T into TMEM per landmark tile L,
-//                  and one tile later O_L += P_L V (full scans only);
-//   warps 2..:     one warpgroup (4 consecutive warps: warp w reads TMEM lane
+//   warps 1..NL (lane 0): one MMA issuer per landmark tile L: S_L = Lq_L K^T
+//                  into TMEM (two buffers);
+//   warp NL+1 (lane 0, full scans only): MMA issuer of O_L += P_L V, one tile
+//                  behind (a tcgen05.mma holds its issuing thread for about a
+//                  hundred cycles, so independent chains from separate warps
+//                  keep the tensor pipe busy);
+//   warps NL+2..:  one warpgroup (4 consecutive warps: warp w reads TMEM lane
 //                  quarter w % 4) per landmark tile, one thread per landmark.
 //                  A thread loads its 128 scores, offers them to its
 //                  landmark's candidate buffer (topk.cuh: append when the
@@ -66,7 +70,8 @@ struct Cfg {
     static constexpr int TB = KT * 128;               // bytes of one K or V tile
     static constexpr int KST = 6;                     // K ring stages
     static constexpr int VST = FULL ? 4 : 0;          // V ring stages
-    static constexpr int NT = 64 + NL * 128;
+    static constexpr int NT = 32 * (NL + 2) + NL * 128;  // producer, NL S issuers, P.V issuer, rows
+    static constexpr int ROW0 = NL + 2;                  // first row warp
     static constexpr size_t OFF_LQLO = NL * 16384;
     static constexpr size_t OFF_K = 2 * NL * 16384;
     static constexpr size_t OFF_V = OFF_K + KST * TB;
@@ -92,20 +97,17 @@ struct Bars {
     uint64_t* pvdone;  // [NL][2]
 };
 
-// Issues O_L += P_L(i) V(i) for every landmark tile L of key tile i (MMA thread).
+// Issues O_L += P_L(i) V(i) for every landmark tile L of key tile i (P.V issuer).
 template <class C, int NL>
 __device__ __forceinline__ bool issue_pv(const ScanArgs& a, uint8_t* base, uint32_t tb, int i, const Bars& b) {
     const int vs = i % C::VST, pbuf = i & 1;
     if (!mbar_wait(&b.vfull[vs], (i / C::VST) & 1, a.status)) return false;
-    const uint32_t va = smem_u32(base + C::OFF_V + vs * C::TB);
+    const uint64_t vd = sdesc_sw128(smem_u32(base + C::OFF_V + vs * C::TB));
     for (int l = 0; l < NL; ++l) {
         if (!mbar_wait(&b.pfull[l * 2 + pbuf], (i >> 1) & 1, a.status)) return false;
         tc_fence_after();
-        const uint32_t pa = smem_u32(base + C::OFF_P + (l * 2 + pbuf) * 16384);
-        const uint32_t tO = tb + l * 256 + 128;
-#pragma unroll
-        for (int s = 0; s < 4; ++s)
-            mma_ss(tO, sdesc_sw128(pa + s * 32), sdesc_sw128(va + s * 2048), kIdescPV, (i > 0 || s > 0) ? 1u : 0u);
+        const uint64_t pd = sdesc_sw128(smem_u32(base + C::OFF_P + (l * 2 + pbuf) * 16384));
+        mma_ss_k64_bmn(tb + l * 256 + 128, pd, vd, kIdescPV, i > 0 ? 1u : 0u);
         mma_commit(&b.pvdone[l * 2 + pbuf]);
     }
     mma_commit(&b.vempty[vs]);
@@ -134,7 +136,7 @@ __global__ void __launch_bounds__(Cfg<FULL, NL>::NT, 1)
     if (tid == 0) {
         for (int i = 0; i < C::KST; ++i) {
             mbar_init(&kfull[i], 1);
-            mbar_init(&kempty[i], 1);
+            mbar_init(&kempty[i], NL);  // one commit per S issuer
         }
         for (int i = 0; i < C::VST; ++i) {
             mbar_init(&vfull[i], 1);
@@ -195,46 +197,36 @@ __global__ void __launch_bounds__(Cfg<FULL, NL>::NT, 1)
                 }
             }
         }
-    } else if (warp == 1) {
-        // ---------------- MMA issuer ----------------
+    } else if (warp <= NL) {
+        // ---------------- S issuer of landmark tile L = warp - 1 ----------------
         if (lane == 0) {
-            const uint32_t hi = smem_u32(base), lo = smem_u32(base + C::OFF_LQLO);
-            bool ok = true;
-            for (int i = 0; i < T && ok; ++i) {
+            const int l = warp - 1;
+            const uint64_t hd = sdesc_sw128(smem_u32(base + l * 16384));
+            const uint64_t ld = sdesc_sw128(smem_u32(base + C::OFF_LQLO + l * 16384));
+            for (int i = 0; i < T; ++i) {
                 const int st = i % C::KST, sb = i & 1;
                 if (!mbar_wait(&kfull[st], (i / C::KST) & 1, a.status)) break;
+                // the rows have read S buffer sb of tile i-2
+                if (i >= 2 && !mbar_wait(&sfree[l * 2 + sb], ((i >> 1) - 1) & 1, a.status)) break;
                 tc_fence_after();
-                const uint32_t ka = smem_u32(base + C::OFF_K + st * C::TB);
-                for (int l = 0; l < NL && ok; ++l) {
-                    if (i >= 2) {  // the rows have read S buffer sb of tile i-2
-                        if (!mbar_wait(&sfree[l * 2 + sb], ((i >> 1) - 1) & 1, a.status)) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
-                    }
-                    const uint32_t tS = tb + l * 256 + sb * KT;
-#pragma unroll
-                    for (int s = 0; s < 4; ++s)
-                        mma_ss(tS, sdesc_sw128(hi + l * 16384 + s * 32), sdesc_sw128(ka + s * 32), kIdescS, s > 0);
-#pragma unroll
-                    for (int s = 0; s < 4; ++s)
-                        mma_ss(tS, sdesc_sw128(lo + l * 16384 + s * 32), sdesc_sw128(ka + s * 32), kIdescS, 1u);
-                    mma_commit(&sfull[l * 2 + sb]);
-                }
-                if (!ok) break;
+                const uint64_t kd = sdesc_sw128(smem_u32(base + C::OFF_K + st * C::TB));
+                const uint32_t tS = tb + l * 256 + sb * KT;
+                mma_ss_k64(tS, hd, kd, kIdescS, 0u);
+                mma_ss_k64(tS, ld, kd, kIdescS, 1u);
+                mma_commit(&sfull[l * 2 + sb]);
                 mma_commit(&kempty[st]);
-                if constexpr (FULL) {
-                    if (i > 0) ok = issue_pv<C, NL>(a, base, tb, i - 1, bars);
-                }
             }
-            if constexpr (FULL) {
-                if (ok && T > 0) issue_pv<C, NL>(a, base, tb, T - 1, bars);
-            }
+        }
+    } else if (warp == NL + 1) {
+        // ---------------- P.V issuer ----------------
+        if constexpr (FULL) {
+            if (lane == 0)
+                for (int i = 0; i < T; ++i)
+                    if (!issue_pv<C, NL>(a, base, tb, i, bars)) break;
         }
     } else {
         // ---------------- landmark rows: top-k filter and softmax ----------------
-        const int L = (warp - 2) >> 2;
+        const int L = (warp - C::ROW0) >> 2;
         const int t = (warp & 3) * 32 + lane;  // TMEM lane = landmark row in the tile
         const int li = L * 128 + t;
         const bool row_ok = li < a.m;
@@ -245,7 +237,7 @@ __global__ void __launch_bounds__(Cfg<FULL, NL>::NT, 1)
         uint64_t theta = (a.theta && row_ok) ? a.theta[bh * a.m + li] : 0;
         float theta_s = key_score(theta);
         int cnt = 0;
-        unsigned* hist = reinterpret_cast<unsigned*>(base + C::OFF_HIST + (warp - 2) * 1024);
+        unsigned* hist = reinterpret_cast<unsigned*>(base + C::OFF_HIST + (warp - C::ROW0) * 1024);
         float mrun = -INFINITY, lrun = 0.f;
         bool ok = true;
         for (int i = 0; i < T; ++i) {

@@ -305,6 +305,23 @@ __device__ __forceinline__ void mma_ss_k64(uint32_t d_tmem, uint64_t a_desc, uin
         "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
+// Four K=16 steps of D (+)= A * B, both operands in shared memory with the
+// 128-byte swizzle; A K-major (+32 bytes per step), B MN-major (16 rows =
+// +2048 bytes per step).
+__device__ __forceinline__ void mma_ss_k64_bmn(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                               uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p, t;\n .reg .b64 a1, a2, a3, b1, b2, b3;\n"
+        " setp.ne.b32 p, %4, 0;\n setp.eq.b32 t, %4, %4;\n"
+        " add.s64 a1, %1, 2;\n add.s64 a2, %1, 4;\n add.s64 a3, %1, 6;\n"
+        " add.s64 b1, %2, 128;\n add.s64 b2, %2, 256;\n add.s64 b3, %2, 384;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], a1, b1, %3, t;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], a2, b2, %3, t;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], a3, b3, %3, t;\n}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
 // Four K=16 steps of D (+)= A * B with A (bf16 pairs) in TMEM from column
 // a_tmem (8 columns per step) and B MN-major in shared memory with the 128-byte
 // swizzle (16 rows = +2048 bytes per step).
