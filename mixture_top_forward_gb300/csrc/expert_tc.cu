@@ -52,6 +52,7 @@ constexpr int NT = 32 * (1 + NWG) + NWG * 128;  // producer, one issuer warp per
 constexpr uint32_t kTStride = 256;              // TMEM columns per warpgroup
 constexpr uint32_t kTP = 128, kTO = 192;        // P and O column offsets inside them
 static_assert(NWG * kTStride <= 512, "TMEM holds 512 columns");
+constexpr uint32_t kIdescS = idesc_bf16(128, KB, false);
 constexpr uint32_t kIdescPV = idesc_bf16(128, 64, true);
 
 struct Args {
@@ -79,17 +80,54 @@ __device__ __forceinline__ Layout layout(uint8_t* base, int nblk) {
     return L;
 }
 
-// The round starting at item r of [r, i1): up to NWG consecutive items of
-// the same expert, one per warpgroup.
-__device__ __forceinline__ int round_size(const Args& a, int r, int i1, int4* it) {
-    it[0] = a.items[r];
-    int n = 1;
-    while (n < NWG && r + n < i1) {
-        const int4 x = a.items[r + n];
-        if (x.x != it[0].x || x.w != it[0].w) break;
-        it[n++] = x;
+// The round starting at item r of [r, i1): the item there and, if the next
+// item has the same expert (and head), that one too; one per warpgroup.
+__device__ __forceinline__ int round_items(const Args& a, int r, int i1, int4& x0, int4& x1) {
+    x0 = a.items[r];
+    if (r + 1 < i1) {
+        x1 = a.items[r + 1];
+        if (x1.x == x0.x && x1.w == x0.w) return 2;
     }
-    return n;
+    return 1;
+}
+
+// Walks the rounds from r to the next item of warpgroup w (returned in out).
+// Each list change on the way is first released (kvfree: once this thread's
+// MMAs so far are done) and then waited for (kvfull), strictly in turn, so
+// every issuer sees every phase of both barriers. Returns 1 (item), 0 (none
+// left) or -1 (a wait timed out).
+__device__ __forceinline__ int next_item(const Args& a, int w, int& r, int i1, int& cur_bh, int& cur_e, int& changes,
+                                         uint64_t* kvfull, uint64_t* kvfree, int4& out) {
+    while (r < i1) {
+        int4 x0, x1;
+        const int cnt = round_items(a, r, i1, x0, x1);
+        if (x0.w != cur_bh || x0.x != cur_e) {
+            if (changes > 0) umma::mma_commit(kvfree);
+            if (!umma::mbar_wait(kvfull, changes & 1, a.status)) return -1;
+            umma::tc_fence_after();
+            cur_bh = x0.w;
+            cur_e = x0.x;
+            ++changes;
+        }
+        r += cnt;
+        if (w < cnt) {
+            out = w == 0 ? x0 : x1;
+            return 1;
+        }
+    }
+    return 0;
+}
+
+// Whether warpgroup w has another item before the next list change.
+__device__ __forceinline__ bool next_same(const Args& a, int w, int r, int i1, int cur_bh, int cur_e) {
+    while (r < i1) {
+        int4 x0, x1;
+        const int cnt = round_items(a, r, i1, x0, x1);
+        if (x0.w != cur_bh || x0.x != cur_e) return false;
+        if (w < cnt) return true;
+        r += cnt;
+    }
+    return false;
 }
 
 __device__ __forceinline__ void zero16(uint8_t* p) { *reinterpret_cast<uint4*>(p) = make_uint4(0, 0, 0, 0); }
@@ -114,8 +152,6 @@ __global__ void __launch_bounds__(NT, 1)
     // rounded up to 4, so every 4-row gather starts 512-byte aligned)
     const int m4 = (a.m + 3) & ~3;
     const int nkeys = m4 + a.k;
-    // width of the last key block: its rows rounded up to the MMA's N step
-    const int wlast = ((nkeys - (a.nblk - 1) * KB) + 15) & ~15;
 
     if (tid == 0) {
         mbar_init(&kvfull, 1);
@@ -162,7 +198,7 @@ __global__ void __launch_bounds__(NT, 1)
         bool ok = true;
         for (int r = i0; r < i1 && ok;) {
             int4 it[NWG];
-            const int cnt = round_size(a, r, i1, it);
+            const int cnt = round_items(a, r, i1, it[0], it[1]);
             if (it[0].w != cur_bh || it[0].x != cur_e) {
                 // wait until the MMAs reading the previous lists are done
                 if (changes > 0) ok = __all_sync(0xffffffffu, mbar_wait(&kvfree, (changes - 1) & 1, a.status));
@@ -193,7 +229,9 @@ __global__ void __launch_bounds__(NT, 1)
                 cur_e = it[0].x;
                 ++changes;
             }
-            for (int w = 0; w < cnt && ok; ++w) {
+#pragma unroll
+            for (int w = 0; w < NWG; ++w) {
+                if (w >= cnt || !ok) break;
                 // this Q buffer of the warpgroup was last used QB items back
                 const uint32_t qb = w * QB + (nq[w] % QB);
                 if (nq[w] >= QB)
@@ -215,83 +253,106 @@ __global__ void __launch_bounds__(NT, 1)
     } else if (warp <= NWG) {
         // ---------------- MMA issuers: lane 0 of warp 1 + w serves warpgroup w ----------------
         // (each issuer has a warp of its own: tcgen05.mma is a single-thread instruction)
+        // Per item: S(0), then S(j) and P.V(j - 1) in turn. The next item's
+        // S(0) goes out before this item's last P.V when it keeps the
+        // key/value lists, so the rows find it ready when they start it. Every
+        // MMA covers a whole block: past the key list the logits are masked and
+        // the staged rows are finite (zero or repeated), so P = 0 there.
         if (lane == 0) {
             const int w = warp - 1;
-            int64_t cur_bh = -1;
-            int cur_e = -1, changes = 0;
-            uint32_t nq = 0, gb = 0;
-            const uint32_t ka = smem_u32(S.keys), va = smem_u32(S.vals);
             const uint32_t tS = tb + w * kTStride, tP = tS + kTP, tO = tS + kTO;
-            bool ok = true;
-            for (int r = i0; r < i1 && ok;) {
-                int4 it[NWG];
-                const int cnt = round_size(a, r, i1, it);
-                if (it[0].w != cur_bh || it[0].x != cur_e) {
-                    if (!mbar_wait(&kvfull, changes & 1, a.status)) break;
-                    cur_bh = it[0].w;
-                    cur_e = it[0].x;
-                    ++changes;
+            const uint64_t kd = sdesc_sw128(smem_u32(S.keys)), vd = sdesc_sw128(smem_u32(S.vals));
+            const uint64_t qd = sdesc_sw128(smem_u32(S.q + w * QB * 16384));  // + 1024 per buffer
+            int r = i0, cur_bh = -1, cur_e = -1, changes = 0;
+            uint32_t gs = 0, gp = 0;  // S and P.V blocks issued
+            uint32_t nq = 0;          // items whose S has started (query buffer sequence)
+            uint32_t npv = 0;         // items whose P.V is complete
+            // S of block j of the item in query buffer sequence q
+            auto issue_s = [&](uint32_t q, int j) -> bool {
+                const uint32_t qb = w * QB + q % QB;
+                if (j == 0) {
+                    if (!mbar_wait(&qfull[qb], (q / QB) & 1, a.status)) return false;
                 }
-                r += cnt;
-                if (w < cnt) {
-                    const uint32_t qb = w * QB + (nq % QB);
-                    if (!mbar_wait(&qfull[qb], (nq / QB) & 1, a.status)) break;
-                    tc_fence_after();
-                    const uint32_t qa = smem_u32(S.q + qb * 16384);
-                    // S for block j, then P.V for block j-1
-                    for (int j = 0; j <= a.nblk && ok; ++j) {
-                        if (j < a.nblk) {
-                            const uint32_t g = gb + j;
-                            if (g >= 1) {  // the rows have read the previous S
-                                ok = mbar_wait(&sfree[w], (g - 1) & 1, a.status);
-                                if (!ok) break;
-                                tc_fence_after();
-                            }
-                            const int width = j == a.nblk - 1 ? wlast : KB;
-                            const uint32_t idesc = idesc_bf16(128, width, false);
-#pragma unroll
-                            for (int s = 0; s < 4; ++s)
-                                mma_ss(tS, sdesc_sw128(qa + s * 32), sdesc_sw128(ka + j * 16384 + s * 32), idesc,
-                                       s > 0);
-                            mma_commit(&sfull[w]);
-                            if (j == a.nblk - 1) mma_commit(&qfree[qb]);
-                        }
-                        if (j > 0) {
-                            const uint32_t g = gb + j - 1;
-                            // the first P.V of an item overwrites O: the previous
-                            // item's epilogue must have read it
-                            if (j == 1 && nq > 0) ok = mbar_wait(&ofree[w], (nq - 1) & 1, a.status);
-                            if (ok) ok = mbar_wait(&pfull[w], g & 1, a.status);
-                            if (!ok) break;
-                            tc_fence_after();
-                            const int steps = (j == a.nblk ? wlast : KB) / 16;
-                            for (int s = 0; s < steps; ++s)
-                                mma_ts(tO, tP + s * 8, sdesc_sw128(va + (j - 1) * 16384 + s * 2048), kIdescPV,
-                                       (j > 1 || s > 0) ? 1u : 0u);
-                            mma_commit(&pvdone[w]);
-                        }
-                    }
-                    gb += a.nblk;
-                    ++nq;
-                }
-                // the next round needs other lists: let the producer overwrite them
-                if (r >= i1 || a.items[r].w != cur_bh || a.items[r].x != cur_e) mma_commit(&kvfree);
+                if (gs >= 1 && !mbar_wait(&sfree[w], (gs - 1) & 1, a.status)) return false;  // rows read S(gs - 1)
+                tc_fence_after();
+                mma_ss_k64(tS, qd + (q % QB) * 1024, kd + j * 1024, kIdescS, 0u);
+                mma_commit(&sfull[w]);
+                if (j == a.nblk - 1) mma_commit(&qfree[qb]);
+                ++gs;
+                return true;
+            };
+            // P.V of block j of the current item
+            auto issue_pv = [&](int j) -> bool {
+                // the first P.V of an item overwrites O: the previous item's epilogue must have read it
+                if (j == 0 && npv > 0 && !mbar_wait(&ofree[w], (npv - 1) & 1, a.status)) return false;
+                if (!mbar_wait(&pfull[w], gp & 1, a.status)) return false;
+                tc_fence_after();
+                mma_ts_k64(tO, tP, vd + j * 1024, kIdescPV, j > 0 ? 1u : 0u);
+                mma_ts_k64(tO, tP + 32, vd + j * 1024 + 512, kIdescPV, 1u);
+                mma_commit(&pvdone[w]);
+                ++gp;
+                return true;
+            };
+            int4 cur;
+            int st = next_item(a, w, r, i1, cur_bh, cur_e, changes, &kvfull, &kvfree, cur);
+            bool ok = st >= 0, s0 = false;
+            while (ok && st > 0) {
+                const uint32_t q = nq++;
+                if (!s0) ok = issue_s(q, 0);
+                for (int j = 1; j < a.nblk && ok; ++j) ok = issue_s(q, j) && issue_pv(j - 1);
+                if (!ok) break;
+                s0 = next_same(a, w, r, i1, cur_bh, cur_e);
+                if (s0 && !(ok = issue_s(nq, 0))) break;
+                if (!(ok = issue_pv(a.nblk - 1))) break;
+                ++npv;
+                st = next_item(a, w, r, i1, cur_bh, cur_e, changes, &kvfull, &kvfree, cur);
+                ok = st >= 0;
             }
         }
     } else {
         // ------------------------------ row warpgroups ------------------------------
+        // An item's epilogue (O / rowsum -> its output rows) waits until the
+        // rows have written the next item's first P: by then its last P.V is
+        // done, and the wait for it has overlapped that block's softmax.
         const int w = (warp - 1 - NWG) >> 2;  // 4 consecutive warps cover the 4 TMEM lane quarters
         const int t = (warp & 3) * 32 + lane;  // TMEM lane = query row of the item
         const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
         const uint32_t tS = tb + w * kTStride + lane_off, tP = tS + kTP, tO = tS + kTO;
         uint32_t gb = 0;
         bool ok = true;
+        bool pend = false, pend_row = false;  // an item whose epilogue is pending
+        float pend_inv = 0.f;
+        uint4* pend_dst = nullptr;
+        auto epilogue = [&]() {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {  // two 32-column halves of the output row
+                float o[32];
+                tmem_ld32(tO + h * 32, o);
+                tmem_ld_wait();
+                if (h == 1) {
+                    tc_fence_before();
+                    warp_arrive(&ofree[w]);
+                }
+                if (pend_row) {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        uint4 q;
+                        q.x = pack_bf16(o[8 * c + 0] * pend_inv, o[8 * c + 1] * pend_inv);
+                        q.y = pack_bf16(o[8 * c + 2] * pend_inv, o[8 * c + 3] * pend_inv);
+                        q.z = pack_bf16(o[8 * c + 4] * pend_inv, o[8 * c + 5] * pend_inv);
+                        q.w = pack_bf16(o[8 * c + 6] * pend_inv, o[8 * c + 7] * pend_inv);
+                        pend_dst[h * 4 + c] = q;
+                    }
+                }
+            }
+            pend = false;
+        };
         for (int r = i0; r < i1 && ok;) {
-            int4 it[NWG];
-            const int cnt = round_size(a, r, i1, it);
+            int4 x0, x1;
+            const int cnt = round_items(a, r, i1, x0, x1);
             r += cnt;
             if (w >= cnt) continue;
-            const int4 item = it[w];
+            const int4 item = w == 0 ? x0 : x1;
             const int64_t bh = item.w;
             const int n = t < item.z ? a.perm[bh * a.N + item.y + t] : 0;
             float mrun = -INFINITY, lrun = 0.f;
@@ -308,7 +369,7 @@ __global__ void __launch_bounds__(NT, 1)
                 const int k0 = j * KB;  // key row of column 0
                 if (k0 + KB > nkeys || (k0 < m4 && k0 + KB > a.m && m4 > a.m)) {
                     // (warp-uniform) the block holds the unused rows [m, m4) or
-                    // ends past the key list, where columns are stale
+                    // ends past the key list, where the logits are not keys'
 #pragma unroll
                     for (int c = 0; c < KB; ++c) {
                         const int g = k0 + c;
@@ -343,8 +404,8 @@ __global__ void __launch_bounds__(NT, 1)
                 }
                 const float sum = ((acc[0].x + acc[0].y) + (acc[1].x + acc[1].y)) + ((acc[2].x + acc[2].y) + (acc[3].x + acc[3].y));
                 lrun = lrun * alpha + sum;
-                // P.V of the previous block must be done before P is overwritten
-                // (and before O is rescaled, when a running max grew by > 2^8)
+                // P.V of the previous block (for j = 0 the previous item's last)
+                // must be done before P is overwritten or O rescaled
                 const bool rescale = j > 0 && __any_sync(0xffffffffu, alpha != 1.f);
                 if (gb >= 1) {
                     ok = __all_sync(0xffffffffu, mbar_wait(&pvdone[w], (gb - 1) & 1, a.status));
@@ -367,35 +428,20 @@ __global__ void __launch_bounds__(NT, 1)
                 tmem_st_wait();
                 tc_fence_before();
                 warp_arrive(&pfull[w]);
+                if (pend) epilogue();  // the previous item's O is final (its last P.V is done)
                 mrun = mnew;
             }
             if (!ok) break;
-            // epilogue: the last P.V of the item (and with it every earlier one) is done
+            pend = true;
+            pend_row = t < item.z;
+            pend_inv = 1.f / lrun;
+            pend_dst = reinterpret_cast<uint4*>(a.out + (bh * a.N + n) * D);
+        }
+        if (ok && pend) {  // the last item: wait for its last P.V
             ok = __all_sync(0xffffffffu, mbar_wait(&pvdone[w], (gb - 1) & 1, a.status));
-            if (!ok) break;
-            tc_fence_after();
-            const float inv = 1.f / lrun;
-            uint4* dst = reinterpret_cast<uint4*>(a.out + (bh * a.N + n) * D);
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {  // two 32-column halves of the output row
-                float o[32];
-                tmem_ld32(tO + h * 32, o);
-                tmem_ld_wait();
-                if (h == 1) {
-                    tc_fence_before();
-                    warp_arrive(&ofree[w]);
-                }
-                if (t < item.z) {
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        uint4 q;
-                        q.x = pack_bf16(o[8 * c + 0] * inv, o[8 * c + 1] * inv);
-                        q.y = pack_bf16(o[8 * c + 2] * inv, o[8 * c + 3] * inv);
-                        q.z = pack_bf16(o[8 * c + 4] * inv, o[8 * c + 5] * inv);
-                        q.w = pack_bf16(o[8 * c + 6] * inv, o[8 * c + 7] * inv);
-                        dst[h * 4 + c] = q;
-                    }
-                }
+            if (ok) {
+                tc_fence_after();
+                epilogue();
             }
         }
     }

@@ -190,7 +190,8 @@ bool make_plan(const Shape& s, Plan* p) {
             while (P.nlev < 3) {
                 const int64_t stride = s.N / t;
                 const int64_t S = cdiv(s.N, stride);
-                P.lev[P.nlev++] = scan_level(s, S, stride, prevS, 512, sms);
+                // the unfiltered first level keeps every sampled key: small chunks spread it over the SMs
+                P.lev[P.nlev++] = scan_level(s, S, stride, prevS, prevS == 0 ? 128 : 512, sms);
                 prevS = S;
                 const int64_t next = std::min<int64_t>(16 * t, s.N / 8);
                 if (next <= t) break;
