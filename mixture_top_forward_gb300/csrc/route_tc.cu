@@ -154,10 +154,14 @@ __global__ void __launch_bounds__(RT_THREADS, 1) route_tc_kernel(const __grid_co
                 float v[32];
                 tmem_ld32(d + c0, v);
                 tmem_ld_wait();
+                if (c0 + 32 > a.m) {  // (uniform) the last chunk: columns past m are another head's
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) v[j] = c0 + j < a.m ? v[j] : -INFINITY;
+                }
 #pragma unroll
                 for (int j = 0; j < 32; ++j) {
                     const int u = j & 3;
-                    if (c0 + j < a.m && v[j] > bv[u]) {
+                    if (v[j] > bv[u]) {
                         bv[u] = v[j];
                         bi[u] = c0 + j;
                     }
