@@ -27,7 +27,7 @@
 //                  landmark's candidate buffer (topk.cuh: append when the
 //                  64-bit order key reaches the threshold, warp-cooperative
 //                  compaction on overflow) and, in full scans, runs the online
-//                  softmax (lazy running max), writes P (bf16) and leaves a
+//                  softmax (lazy running max), writes P (bf16) into TMEM and leaves a
 //                  (max, sum, o[64]) partial at the end of the chunk.
 // Keys are read through a 3-D tensor map (row, head) whose row stride may be
 // > 1: a pilot scan reads every stride-th key of each head. A pilot does only
@@ -75,10 +75,10 @@ struct Cfg {
     static constexpr size_t OFF_LQLO = NL * 16384;
     static constexpr size_t OFF_K = 2 * NL * 16384;
     static constexpr size_t OFF_V = OFF_K + KST * TB;
-    static constexpr size_t OFF_P = OFF_V + VST * TB;  // [NL][2] tiles of 128 x 64 bf16
-    static constexpr size_t OFF_HIST = OFF_P + (FULL ? NL * 2 * 16384 : 0);
+    static constexpr size_t OFF_HIST = OFF_V + VST * TB;
     static constexpr size_t SMEM = OFF_HIST + NL * 4 * 1024 + 1024;
-    // TMEM per landmark tile L (256 columns apart): S buffers at +0 and +64, O at +128
+    // TMEM per landmark tile L (256 columns apart): S buffers at +0 and +64, O at +128,
+    // P (bf16 pairs) buffers at +192 and +224
     static constexpr uint32_t TCOLS = NL * 256;
 };
 
@@ -106,8 +106,7 @@ __device__ __forceinline__ bool issue_pv(const ScanArgs& a, uint8_t* base, uint3
     for (int l = 0; l < NL; ++l) {
         if (!mbar_wait(&b.pfull[l * 2 + pbuf], (i >> 1) & 1, a.status)) return false;
         tc_fence_after();
-        const uint64_t pd = sdesc_sw128(smem_u32(base + C::OFF_P + (l * 2 + pbuf) * 16384));
-        mma_ss_k64_bmn(tb + l * 256 + 128, pd, vd, kIdescPV, i > 0 ? 1u : 0u);
+        mma_ts_k64(tb + l * 256 + 128, tb + l * 256 + 192 + pbuf * 32, vd, kIdescPV, i > 0 ? 1u : 0u);
         mma_commit(&b.pvdone[l * 2 + pbuf]);
     }
     mma_commit(&b.vempty[vs]);
@@ -358,17 +357,14 @@ __global__ void __launch_bounds__(Cfg<FULL, NL>::NT, 1)
                     }
                     tmem_st_wait();
                 }
-                uint8_t* pdst = base + C::OFF_P + pb * 16384;
+                uint32_t pk[KT / 2];
 #pragma unroll
-                for (int g = 0; g < KT / 8; ++g) {
-                    uint4 pk;
-                    __nv_bfloat162* h2 = reinterpret_cast<__nv_bfloat162*>(&pk);
-#pragma unroll
-                    for (int u = 0; u < 4; ++u)
-                        h2[u] = __floats2bfloat162_rn(s[8 * g + 2 * u], s[8 * g + 2 * u + 1]);
-                    *reinterpret_cast<uint4*>(pdst + swz128(t, g)) = pk;
+                for (int q = 0; q < KT / 2; ++q) {
+                    __nv_bfloat162 h2 = __floats2bfloat162_rn(s[2 * q], s[2 * q + 1]);
+                    pk[q] = *reinterpret_cast<uint32_t*>(&h2);
                 }
-                fence_proxy_async();
+                tmem_st32u(tb + L * 256 + 192 + sb * 32 + lane_off, pk);
+                tmem_st_wait();
                 tc_fence_before();
                 warp_arrive(&pfull[pb]);
                 mrun = mnew;
