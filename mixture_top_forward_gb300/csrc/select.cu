@@ -6,7 +6,8 @@
 //  * routed expert: the k largest top-k keys over all chunks' candidate
 //    buffers, found by radix select on the 64-bit keys (8 bits per pass,
 //    256-bin shared-memory histogram), then written as key indices in
-//    ascending order (bitonic sort in shared memory).
+//    ascending order (each selected index placed by counting the selected
+//    indices below it).
 // Each chunk's buffer holds at least min(chunk length, k) of its best keys,
 // so the union always contains the global top k.
 //
@@ -20,7 +21,7 @@ namespace mita {
 namespace {
 
 constexpr int ST = 256;         // threads per CTA
-constexpr int SEL_CAP = 5120;   // candidates staged in shared memory (40 KB)
+constexpr int SEL_CAP = 4608;   // candidates staged in shared memory (36 KB)
 
 template <bool PILOT>
 __global__ void __launch_bounds__(ST) select_kernel(int m, int k, int chunks, int cap,
@@ -30,8 +31,10 @@ __global__ void __launch_bounds__(ST) select_kernel(int m, int k, int chunks, in
                                                     __nv_bfloat16* __restrict__ lvbf,
                                                     int32_t* __restrict__ expert_idx, uint64_t* __restrict__ theta) {
     __shared__ unsigned hist[256];
-    __shared__ int cnts[64];
-    __shared__ int offs[65];
+    __shared__ int offs[ST + 1];        // chunk offsets into staged[] (chunks <= ST)
+    __shared__ float red[ST / 32 + 1];  // block reductions
+    __shared__ float fac[ST];           // LV merge: per-chunk rescale factors
+    __shared__ float osum[4][D];
     __shared__ uint64_t staged[SEL_CAP];
     __shared__ int sel[MITA_SORT_MAX];
     __shared__ int nsel;
@@ -40,50 +43,93 @@ __global__ void __launch_bounds__(ST) select_kernel(int m, int k, int chunks, in
 
     const int i = static_cast<int>(blockIdx.x % static_cast<unsigned>(m));
     const int64_t bh = blockIdx.x / static_cast<unsigned>(m);
-    const int tid = threadIdx.x;
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    const bool small = chunks <= ST;  // per-chunk values fit the shared arrays
+    auto part_of = [&](int c) { return part + ((bh * chunks + c) * m + i) * 68; };
 
     // ---- shared-expert value ------------------------------------------------
-    if (!PILOT && tid < D) {
-        float M = -INFINITY;
-        for (int c = 0; c < chunks; ++c) M = fmaxf(M, part[((bh * chunks + c) * m + i) * 68]);
-        float L = 0.f, O = 0.f;
-        for (int c = 0; c < chunks; ++c) {
-            const float* pp = part + ((bh * chunks + c) * m + i) * 68;
-            const float f = exp2f((pp[0] - M) * kLog2e);
-            L += pp[1] * f;
-            O += pp[4 + tid] * f;
+    if (!PILOT) {
+        if (small) {
+            // M = max of the chunks' maxima; factors exp(max_c - M); L = sum sum_c f_c
+            const float mc = tid < chunks ? part_of(tid)[0] : -INFINITY;
+            const float lc = tid < chunks ? part_of(tid)[1] : 0.f;
+            float x = mc;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+            if (lane == 0) red[wid] = x;
+            __syncthreads();
+            float M = red[0];
+            for (int w = 1; w < ST / 32; ++w) M = fmaxf(M, red[w]);
+            const float f = tid < chunks ? exp2f((mc - M) * kLog2e) : 0.f;
+            if (tid < chunks) fac[tid] = f;
+            float y = lc * f;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) y += __shfl_xor_sync(0xffffffffu, y, o);
+            __syncthreads();
+            if (lane == 0) red[wid] = y;
+            __syncthreads();
+            float L = 0.f;
+            for (int w = 0; w < ST / 32; ++w) L += red[w];
+            // O_d = sum_c o_c[d] f_c: four threads per column d, chunks q, q+4, ...
+            const int dd = tid & (D - 1), q = tid >> 6;
+            float acc = 0.f;
+            for (int c = q; c < chunks; c += ST / D) acc += part_of(c)[4 + dd] * fac[c];
+            osum[q][dd] = acc;
+            __syncthreads();
+            if (tid < D) {
+                const float v = (osum[0][tid] + osum[1][tid] + osum[2][tid] + osum[3][tid]) / L;
+                lv32[(bh * m + i) * D + tid] = v;
+                lvbf[(bh * m + i) * D + tid] = __float2bfloat16_rn(v);
+            }
+        } else if (tid < D) {
+            float M = -INFINITY;
+            for (int c = 0; c < chunks; ++c) M = fmaxf(M, part_of(c)[0]);
+            float L = 0.f, O = 0.f;
+            for (int c = 0; c < chunks; ++c) {
+                const float* pp = part_of(c);
+                const float f = exp2f((pp[0] - M) * kLog2e);
+                L += pp[1] * f;
+                O += pp[4 + tid] * f;
+            }
+            const float v = O / L;
+            lv32[(bh * m + i) * D + tid] = v;
+            lvbf[(bh * m + i) * D + tid] = __float2bfloat16_rn(v);
         }
-        const float v = O / L;
-        lv32[(bh * m + i) * D + tid] = v;
-        lvbf[(bh * m + i) * D + tid] = __float2bfloat16_rn(v);
     }
 
     // ---- routed expert: k largest keys over all chunk buffers ---------------
-    // chunk counts (chunks may exceed 64: then they are re-read from global)
-    int total = 0;
-    for (int c = 0; c < chunks; ++c) {
-        const int n = ccount[(bh * chunks + c) * m + i];
-        if (c < 64 && tid == 0) cnts[c] = n;
-        total += n;
-    }
-    __syncthreads();
-    auto count_of = [&](int c) { return c < 64 ? cnts[c] : ccount[(bh * chunks + c) * m + i]; };
     auto buf_of = [&](int c) { return cand + ((bh * chunks + c) * m + i) * static_cast<int64_t>(cap); };
-
-    // all of this landmark's candidates in shared memory when they fit
-    const bool in_smem = chunks <= 64 && total <= SEL_CAP;
-    if (in_smem) {
-        if (tid == 0) {
-            int o = 0;
-            for (int c = 0; c < chunks; ++c) {
-                offs[c] = o;
-                o += cnts[c];
-            }
+    auto count_of = [&](int c) { return ccount[(bh * chunks + c) * m + i]; };
+    int total = 0;
+    if (small) {
+        // chunk counts, one per thread, and their exclusive prefix sums
+        const int n = tid < chunks ? count_of(tid) : 0;
+        int incl = n;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
         }
         __syncthreads();
-        for (int c = 0; c < chunks; ++c) {
+        if (lane == 31) red[wid] = __int_as_float(incl);
+        __syncthreads();
+        int base = 0;
+        for (int w = 0; w < wid; ++w) base += __float_as_int(red[w]);
+        offs[tid] = base + incl - n;
+        if (tid == ST - 1) offs[ST] = base + incl;
+        __syncthreads();
+        total = offs[ST];
+    } else {
+        for (int c = 0; c < chunks; ++c) total += count_of(c);
+    }
+
+    // all of this landmark's candidates in shared memory when they fit
+    const bool in_smem = small && total <= SEL_CAP;
+    if (in_smem) {  // one warp per chunk buffer, so the chunks' loads overlap
+        for (int c = wid; c < chunks; c += ST / 32) {
             const uint64_t* b = buf_of(c);
-            for (int e = tid; e < cnts[c]; e += ST) staged[offs[c] + e] = b[e];
+            const int o = offs[c], n = offs[c + 1] - o;
+            for (int e = lane; e < n; e += 32) staged[o + e] = b[e];
         }
         __syncthreads();
     }
@@ -166,27 +212,15 @@ __global__ void __launch_bounds__(ST) select_kernel(int m, int k, int chunks, in
         if (x >= kth) sel[atomicAdd(&nsel, 1)] = static_cast<int>(topk_key_index(x));
     });
     __syncthreads();
-    int n2 = 1;
-    while (n2 < k) n2 <<= 1;
-    for (int t = k + tid; t < n2; t += ST) sel[t] = 0x7FFFFFFF;
-    __syncthreads();
-    for (int size = 2; size <= n2; size <<= 1) {
-        for (int stride = size >> 1; stride > 0; stride >>= 1) {
-            for (int t = tid; t < n2 / 2; t += ST) {
-                const int lo = 2 * t - (t & (stride - 1));
-                const int hi = lo + stride;
-                const bool up = (lo & size) == 0;
-                const int a = sel[lo], b = sel[hi];
-                if ((a > b) == up) {
-                    sel[lo] = b;
-                    sel[hi] = a;
-                }
-            }
-            __syncthreads();
-        }
-    }
+    // ascending order: each selected index (all distinct) goes to the place
+    // given by the number of selected indices below it
     int32_t* dst = expert_idx + (bh * m + i) * static_cast<int64_t>(k);
-    for (int t = tid; t < k; t += ST) dst[t] = sel[t];
+    for (int t = tid; t < k; t += ST) {
+        const int x = sel[t];
+        int r = 0;
+        for (int u = 0; u < k; ++u) r += sel[u] < x ? 1 : 0;
+        dst[r] = x;
+    }
 }
 
 }  // namespace
