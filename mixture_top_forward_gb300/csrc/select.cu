@@ -212,13 +212,18 @@ __global__ void __launch_bounds__(ST) select_kernel(int m, int k, int chunks, in
         if (x >= kth) sel[atomicAdd(&nsel, 1)] = static_cast<int>(topk_key_index(x));
     });
     __syncthreads();
-    // ascending order: each selected index (all distinct) goes to the place
-    // given by the number of selected indices below it
+    // Exactly k keys reach kth (every landmark has at least k candidates). If
+    // that were ever not so, the missing entries become key 0, so every index
+    // written is in range.
+    for (int t = nsel + tid; t < k; t += ST) sel[t] = 0;
+    __syncthreads();
+    // ascending order: each selected index goes to the place given by the
+    // number of selected indices below it (equal ones ordered by position)
     int32_t* dst = expert_idx + (bh * m + i) * static_cast<int64_t>(k);
     for (int t = tid; t < k; t += ST) {
         const int x = sel[t];
         int r = 0;
-        for (int u = 0; u < k; ++u) r += sel[u] < x ? 1 : 0;
+        for (int u = 0; u < k; ++u) r += (sel[u] < x || (sel[u] == x && u < t)) ? 1 : 0;
         dst[r] = x;
     }
 }
