@@ -198,7 +198,19 @@ bool make_plan(const Shape& s, Plan* p) {
                 t = next;
             }
         }
+        // Dense top-k when the last sample could only pass more than one key in
+        // 16 to the main scan (or there is no sample at all) and the logit rows
+        // stay small: appending that many candidates one by one costs more than
+        // writing every logit and ranking whole rows.
+        const int64_t dense_bytes = s.BH * s.m * round_up(s.N, 4) * 4;
+        if ((prevS == 0 || 16LL * s.k > prevS) && s.N <= 65536 && dense_bytes <= (1LL << 30)) {
+            P.dense = true;
+            P.dense_ld = round_up(s.N, 4);
+            P.nlev = 0;
+            prevS = 1;  // chunking as for a filtered scan; no candidate buffers
+        }
         P.lev[P.nlev++] = scan_level(s, s.N, 1, prevS, 512, sms);
+        if (P.dense) P.lev[0].cap = 0;
     } else {
         // CUDA-core scan: 32 landmarks per CTA, ~8 CTAs per SM, >= 1024 keys per chunk
         const int64_t ltiles = cdiv(s.m, 32);
@@ -250,6 +262,7 @@ bool make_plan(const Shape& s, Plan* p) {
     P.off_perm = take(BH * static_cast<size_t>(s.N) * sizeof(int));
     P.off_items = take(BH * static_cast<size_t>(P.max_items) * sizeof(int4));
     P.off_nitems = take(sizeof(int));
+    P.off_dense = take(P.dense ? BH * m * static_cast<size_t>(P.dense_ld) * sizeof(float) : 0);
     P.total = off;
     if (P.max_items * s.BH > 0x7FFFFFFFLL || s.BH * P.nrblocks > 0x7FFFFFFFLL) return false;
     for (int l = 0; l < P.nlev; ++l)
@@ -277,6 +290,7 @@ Work carve(const Plan& p, void* base) {
     w.perm = reinterpret_cast<int*>(b + p.off_perm);
     w.items = reinterpret_cast<int4*>(b + p.off_items);
     w.nitems = reinterpret_cast<int*>(b + p.off_nitems);
+    w.dense = p.dense ? reinterpret_cast<float*>(b + p.off_dense) : nullptr;
     return w;
 }
 

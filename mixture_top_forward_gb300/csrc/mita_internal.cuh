@@ -41,6 +41,11 @@ struct Plan {
     bool scan_tc;
     int nlev;
     ScanLevel lev[4];
+    // dense top-k: when no sample threshold could keep the main scan's
+    // candidates rare, the main scan writes every logit and the select ranks
+    // whole rows (no pilots, no candidate buffers)
+    bool dense;
+    int64_t dense_ld;  // row stride of the dense logits (N rounded up to 4)
     // routing / grouping
     int rblock;         // queries per routing CTA
     int64_t nrblocks;   // routing CTAs per head
@@ -49,7 +54,7 @@ struct Plan {
     int64_t max_items;  // work items per head, upper bound
     // workspace layout (byte offsets)
     size_t off_status, off_lq32, off_lqhi, off_lqlo, off_lv32, off_lvbf, off_part, off_cand, off_ccount, off_theta,
-        off_counts, off_expoff, off_cursor, off_perm, off_items, off_nitems, total;
+        off_counts, off_expoff, off_cursor, off_perm, off_items, off_nitems, off_dense, total;
 };
 
 // Builds the plan; returns false if a size does not fit the int ranges used.
@@ -67,6 +72,7 @@ struct Work {
     uint64_t* cand;         // [BH][chunks][m][cap] composite top-k keys
     int* ccount;            // [BH][chunks][m]
     uint64_t* theta;        // [BH][m] top-k thresholds from the pilot scans
+    float* dense;           // [BH][m][dense_ld] raw logits <Lq_i, K_j> (dense top-k only)
     int* counts;            // [BH][m] queries routed to each expert
     int* expoff;            // [BH][m+1] exclusive prefix of counts
     int* cursor;            // [BH][m] scatter cursors

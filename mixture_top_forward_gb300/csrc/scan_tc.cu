@@ -57,6 +57,8 @@ struct ScanArgs {
     float* part;            // [BH][chunks][m][68], full scans only
     uint64_t* cand;         // [BH][chunks][m][cap]
     int* ccount;            // [BH][chunks][m]
+    float* dense;           // dense top-k: [BH][m][ld] raw logits, else null
+    int64_t ld;             // row stride of dense
     int* status;
     int64_t S;          // keys (samples) per head in this scan
     int64_t stride;     // key index of sample s is s * stride
@@ -270,6 +272,20 @@ __global__ void __launch_bounds__(Cfg<FULL, NL>::NT, 1)
             }
             const float bmax = fmax3(fmax3(gm[0], gm[1], gm[2]), fmax3(gm[3], gm[4], gm[5]), fmaxf(gm[6], gm[7]));
 
+            if (a.dense) {  // (uniform) dense top-k: every logit of the row goes out
+                if (row_ok) {
+                    float* dst = a.dense + (bh * a.m + li) * a.ld + col0;
+                    if (nvalid == KT) {
+#pragma unroll
+                        for (int q = 0; q < KT; q += 4)
+                            *reinterpret_cast<float4*>(dst + q) = make_float4(s[q], s[q + 1], s[q + 2], s[q + 3]);
+                    } else {
+#pragma unroll
+                        for (int q = 0; q < KT; ++q)
+                            if (q < nvalid) dst[q] = s[q];
+                    }
+                }
+            } else {
             // top-k candidates (compaction first if this tile could overflow a buffer)
             unsigned need = __ballot_sync(0xffffffffu, row_ok && cnt + nvalid > a.cap);
             while (need) {
@@ -312,6 +328,7 @@ __global__ void __launch_bounds__(Cfg<FULL, NL>::NT, 1)
                         }
                     }
                 }
+            }
             }
             if constexpr (FULL) {
                 const float bm2 = bmax * kC;
@@ -391,7 +408,7 @@ __global__ void __launch_bounds__(Cfg<FULL, NL>::NT, 1)
                 }
             }
         }
-        if (row_ok) a.ccount[slot] = cnt;
+        if (row_ok && !a.dense) a.ccount[slot] = cnt;
     }
     tc_fence_before();
     __syncthreads();
@@ -434,6 +451,8 @@ cudaError_t launch_scan_tc(const Plan& p, const Work& w, const __nv_bfloat16* K,
     a.part = w.part;
     a.cand = w.cand;
     a.ccount = w.ccount;
+    a.dense = full ? w.dense : nullptr;
+    a.ld = p.dense_ld;
     a.status = w.status;
     a.S = L.S;
     a.stride = L.stride;

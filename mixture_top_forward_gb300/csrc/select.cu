@@ -11,10 +11,13 @@
 // Each chunk's buffer holds at least min(chunk length, k) of its best keys,
 // so the union always contains the global top k.
 //
+// Dense top-k (shapes whose sample thresholds would pass too many keys): the
+// candidates are the landmark's whole row of logits, written by the scan.
+//
 // The pilot variant (after a scan of a strided key sample) only finds each
 // landmark's k-th largest sample key and raises the landmark's threshold to
 // it: k keys of the head reach that value, so the true k-th best does too.
-#include "mita_internal.cuh"
+#include "topk.cuh"
 
 namespace mita {
 
@@ -29,7 +32,8 @@ __global__ void __launch_bounds__(ST) select_kernel(int m, int k, int chunks, in
                                                     const uint64_t* __restrict__ cand,
                                                     const int* __restrict__ ccount, float* __restrict__ lv32,
                                                     __nv_bfloat16* __restrict__ lvbf,
-                                                    int32_t* __restrict__ expert_idx, uint64_t* __restrict__ theta) {
+                                                    int32_t* __restrict__ expert_idx, uint64_t* __restrict__ theta,
+                                                    const float* __restrict__ dense, int64_t N, int64_t ld) {
     __shared__ unsigned hist[256];
     __shared__ int offs[ST + 1];        // chunk offsets into staged[] (chunks <= ST)
     __shared__ float red[ST / 32 + 1];  // block reductions
@@ -100,8 +104,12 @@ __global__ void __launch_bounds__(ST) select_kernel(int m, int k, int chunks, in
     // ---- routed expert: k largest keys over all chunk buffers ---------------
     auto buf_of = [&](int c) { return cand + ((bh * chunks + c) * m + i) * static_cast<int64_t>(cap); };
     auto count_of = [&](int c) { return ccount[(bh * chunks + c) * m + i]; };
+    // dense top-k: the landmark's whole row of logits, as order keys
+    const float* drow = dense ? dense + (bh * m + i) * ld : nullptr;
     int total = 0;
-    if (small) {
+    if (drow) {
+        total = static_cast<int>(N);
+    } else if (small) {
         // chunk counts, one per thread, and their exclusive prefix sums
         const int n = tid < chunks ? count_of(tid) : 0;
         int incl = n;
@@ -124,8 +132,11 @@ __global__ void __launch_bounds__(ST) select_kernel(int m, int k, int chunks, in
     }
 
     // all of this landmark's candidates in shared memory when they fit
-    const bool in_smem = small && total <= SEL_CAP;
-    if (in_smem) {  // one warp per chunk buffer, so the chunks' loads overlap
+    const bool in_smem = (drow || small) && total <= SEL_CAP;
+    if (in_smem && drow) {
+        for (int e = tid; e < total; e += ST) staged[e] = topk_key(drow[e] * 0.125f, static_cast<uint32_t>(e));
+        __syncthreads();
+    } else if (in_smem) {  // one warp per chunk buffer, so the chunks' loads overlap
         for (int c = wid; c < chunks; c += ST / 32) {
             const uint64_t* b = buf_of(c);
             const int o = offs[c], n = offs[c + 1] - o;
@@ -136,6 +147,8 @@ __global__ void __launch_bounds__(ST) select_kernel(int m, int k, int chunks, in
     auto for_each = [&](auto&& f) {
         if (in_smem) {
             for (int e = tid; e < total; e += ST) f(staged[e]);
+        } else if (drow) {
+            for (int e = tid; e < total; e += ST) f(topk_key(drow[e] * 0.125f, static_cast<uint32_t>(e)));
         } else {
             for (int c = 0; c < chunks; ++c) {
                 const uint64_t* b = buf_of(c);
@@ -234,7 +247,7 @@ cudaError_t launch_select(const Plan& p, const Work& w, int32_t* expert_idx, cud
     const unsigned grid = static_cast<unsigned>(p.s.BH * p.s.m);
     const ScanLevel& L = p.lev[p.nlev - 1];
     select_kernel<false><<<grid, ST, 0, st>>>(p.s.m, p.s.k, L.chunks, L.cap, w.part, w.cand, w.ccount, w.lv32,
-                                             w.lvbf, expert_idx, nullptr);
+                                             w.lvbf, expert_idx, nullptr, w.dense, p.s.N, p.dense_ld);
     return cudaGetLastError();
 }
 
@@ -242,7 +255,7 @@ cudaError_t launch_pilot_select(const Plan& p, const Work& w, int level, cudaStr
     const unsigned grid = static_cast<unsigned>(p.s.BH * p.s.m);
     const ScanLevel& L = p.lev[level];
     select_kernel<true><<<grid, ST, 0, st>>>(p.s.m, p.s.k, L.chunks, L.cap, nullptr, w.cand, w.ccount, nullptr,
-                                            nullptr, nullptr, w.theta);
+                                            nullptr, nullptr, w.theta, nullptr, 0, 0);
     return cudaGetLastError();
 }
 
