@@ -122,21 +122,11 @@ __device__ __forceinline__ void tma_gather4(void* dst, const CUtensorMap* map, i
         "l"(map), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3), "r"(smem_u32(bar))
         : "memory");
 }
-__device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
-    asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
-}
-
 // Ampere-style 16-byte asynchronous copy (used for row gathers).
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
-// Makes this thread's completed cp.async writes count as an arrival on `bar`.
-__device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {
-    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-
 // max(a, b, c) in one instruction (three-input max.f32, sm_100 family).
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
     float r;
@@ -230,14 +220,6 @@ __device__ __forceinline__ void tmem_st32u(uint32_t taddr, const uint32_t* v) {
         "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
         : "memory");
 }
-__device__ __forceinline__ void tmem_st16u(uint32_t taddr, const uint32_t* v) {
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
-            taddr),
-        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]),
-        "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
-        : "memory");
-}
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
     uint32_t r[16];
     asm volatile(
@@ -300,17 +282,6 @@ __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_
         "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
-// D[tmem] (+)= A[tmem] * B[smem]: A (M rows = TMEM lanes, K along the
-// columns, two bf16 per 32-bit column, the lower K index in the low half) is
-// read from tensor memory at column address a_tmem.
-__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
-                                       uint32_t accumulate) {
-    asm volatile(
-        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-        " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
 // Four K=16 steps of D (+)= A * B over a 64-wide K dimension, both operands
 // K-major in shared memory with the 128-byte swizzle (descriptor start +32
 // bytes per step). accumulate = 0 overwrites D with the first product.
@@ -321,23 +292,6 @@ __device__ __forceinline__ void mma_ss_k64(uint32_t d_tmem, uint64_t a_desc, uin
         " setp.ne.b32 p, %4, 0;\n setp.eq.b32 t, %4, %4;\n"
         " add.s64 a1, %1, 2;\n add.s64 a2, %1, 4;\n add.s64 a3, %1, 6;\n"
         " add.s64 b1, %2, 2;\n add.s64 b2, %2, 4;\n add.s64 b3, %2, 6;\n"
-        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n"
-        " tcgen05.mma.cta_group::1.kind::f16 [%0], a1, b1, %3, t;\n"
-        " tcgen05.mma.cta_group::1.kind::f16 [%0], a2, b2, %3, t;\n"
-        " tcgen05.mma.cta_group::1.kind::f16 [%0], a3, b3, %3, t;\n}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-// Four K=16 steps of D (+)= A * B, both operands in shared memory with the
-// 128-byte swizzle; A K-major (+32 bytes per step), B MN-major (16 rows =
-// +2048 bytes per step).
-__device__ __forceinline__ void mma_ss_k64_bmn(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                               uint32_t accumulate) {
-    asm volatile(
-        "{\n .reg .pred p, t;\n .reg .b64 a1, a2, a3, b1, b2, b3;\n"
-        " setp.ne.b32 p, %4, 0;\n setp.eq.b32 t, %4, %4;\n"
-        " add.s64 a1, %1, 2;\n add.s64 a2, %1, 4;\n add.s64 a3, %1, 6;\n"
-        " add.s64 b1, %2, 128;\n add.s64 b2, %2, 256;\n add.s64 b3, %2, 384;\n"
         " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n"
         " tcgen05.mma.cta_group::1.kind::f16 [%0], a1, b1, %3, t;\n"
         " tcgen05.mma.cta_group::1.kind::f16 [%0], a2, b2, %3, t;\n"
@@ -386,14 +340,6 @@ __device__ __forceinline__ bool named_bar_and(int id, int nthreads, bool v) {
         : "r"(static_cast<uint32_t>(v)), "r"(id), "r"(nthreads)
         : "memory");
     return r != 0;
-}
-
-__device__ __forceinline__ bool elect_one() {
-    uint32_t pred = 0;
-    asm volatile(
-        "{\n .reg .b32 r;\n .reg .pred p;\n elect.sync r|p, 0xffffffff;\n selp.u32 %0, 1, 0, p;\n}"
-        : "=r"(pred));
-    return pred != 0;
 }
 
 }  // namespace umma
