@@ -8,28 +8,30 @@
 // implementation groups queries by expert and combines by online softmax.
 //
 // Persistent CTAs walk a contiguous range of the flat, expert-ordered item
-// list (<= 128 queries of one expert per item), in rounds of up to two items
+// list (<= 128 queries of one expert per item), in rounds of up to three items
 // of the same expert, one per row warpgroup. The expert's key list
 // [Lq_0..Lq_{m-1}, K_e] and value list [LV_0..LV_{m-1}, V_e] (bf16, 128-byte
-// swizzled rows, zero padded to whole 128-row blocks) stay in shared memory
+// swizzled rows, zero padded to whole 64-row blocks) stay in shared memory
 // while consecutive rounds share the expert.
 //   warp 0:         producer: gathers the key/value lists when the expert
 //                   changes (the shared rows only when the head changes) and
 //                   each item's query rows (through the grouping permutation)
-//                   into the warpgroup's next query buffer, all with cp.async;
-//   warps 1, 2 (lane 0): one MMA issuer per warpgroup: per 128-key block j of
+//                   into the warpgroup's next query buffer, all with TMA 4-row
+//                   gathers that complete on the consumer's mbarrier;
+//   warps 1-3 (lane 0): one MMA issuer per warpgroup: per 64-key block j of
 //                   its item, S = Q keys_j^T (A and B in shared memory) into
 //                   the warpgroup's TMEM score columns, and one block later
 //                   O += P_j values_j with P read from TMEM (A in tensor
 //                   memory, B in shared memory) into its TMEM accumulator;
-//   warps 3-6, 7-10: one warpgroup per item (4 consecutive warps cover the 4
-//                   TMEM lane quarters), one thread per query row: load the
-//                   128 logits, update the running max (kept while it grows by
-//                   < 2^8, so O rarely needs rescaling), p = 2^(s tau log2e -
-//                   max) in registers, P as bf16 pairs into TMEM once the
+//   warps 4-7, 8-11, 12-15: one warpgroup per item (4 consecutive warps cover
+//                   the 4 TMEM lane quarters), one thread per query row: load
+//                   the 64 logits, update the running max (kept while it grows
+//                   by < 2^8, so O rarely needs rescaling), p = 2^(s tau log2e
+//                   - max) in registers, P as bf16 pairs into TMEM once the
 //                   previous block's P.V is done; at the end O / rowsum ->
 //                   bf16 -> the query's row.
-// TMEM per warpgroup: 128 columns of S, 64 of P (bf16 pairs), 64 of O.
+// TMEM per warpgroup: 64 columns of S, 32 of P (bf16 pairs), 64 of O, so three
+// warpgroups (three row warps per SM sub-partition) fit in the 512 columns.
 // Handshakes are mbarriers, each completed exactly once per event its waiter
 // consumes; row warps arrive once each (4-arrival barriers) and make
 // their waits warp-uniform, so no named barrier can block forever. Every
@@ -45,13 +47,17 @@ using namespace umma;
 
 constexpr float kC = 0.125f * kLog2e;  // tau * log2(e), tau = 1/sqrt(64)
 constexpr float kLazy = 8.0f;          // keep the running max while the new one is within 2^8
-constexpr int KB = 128;                // keys per block
-constexpr int NWG = 2;                 // row warpgroups
+constexpr int KB = 64;                 // keys per block
+constexpr int NWG = 3;                 // row warpgroups
 constexpr int QB = 2;                  // query-row buffers per warpgroup
 constexpr int NT = 32 * (1 + NWG) + NWG * 128;  // producer, one issuer warp per group, rows
-constexpr uint32_t kTStride = 256;              // TMEM columns per warpgroup
-constexpr uint32_t kTP = 128, kTO = 192;        // P and O column offsets inside them
-static_assert(NWG * kTStride <= 512, "TMEM holds 512 columns");
+// TMEM columns of warpgroup w: S (64) at 64 w, O (64) at 192 + 64 w, P (32,
+// bf16 pairs) at 384 + 32 w; every S and O starts on a multiple of 64
+__host__ __device__ constexpr uint32_t tcol_s(int w) { return 64u * w; }
+__host__ __device__ constexpr uint32_t tcol_o(int w) { return 192u + 64u * w; }
+__host__ __device__ constexpr uint32_t tcol_p(int w) { return 384u + 32u * w; }
+static_assert(tcol_p(NWG - 1) + 32 <= 512 && tcol_s(NWG - 1) + 64 <= tcol_o(0) && tcol_o(NWG - 1) + 64 <= tcol_p(0),
+              "TMEM holds 512 columns");
 constexpr uint32_t kIdescS = idesc_bf16(128, KB, false);
 constexpr uint32_t kIdescPV = idesc_bf16(128, 64, true);
 
@@ -67,28 +73,32 @@ struct Args {
 };
 
 struct Layout {
-    uint8_t* keys;  // nblk * 16 KB
-    uint8_t* vals;  // nblk * 16 KB
+    uint8_t* keys;  // nblk * 8 KB
+    uint8_t* vals;  // nblk * 8 KB
     uint8_t* q;     // [NWG][QB] * 16 KB: query rows
 };
 
 __device__ __forceinline__ Layout layout(uint8_t* base, int nblk) {
     Layout L;
     L.keys = base;
-    L.vals = L.keys + nblk * 16384;
-    L.q = L.vals + nblk * 16384;
+    L.vals = L.keys + nblk * 8192;
+    L.q = L.vals + nblk * 8192;
     return L;
 }
 
 // The round starting at item r of [r, i1): the item there and, if the next
 // item has the same expert (and head), that one too; one per warpgroup.
-__device__ __forceinline__ int round_items(const Args& a, int r, int i1, int4& x0, int4& x1) {
+__device__ __forceinline__ int round_items(const Args& a, int r, int i1, int4& x0, int4& x1, int4& x2) {
     x0 = a.items[r];
-    if (r + 1 < i1) {
-        x1 = a.items[r + 1];
-        if (x1.x == x0.x && x1.w == x0.w) return 2;
-    }
-    return 1;
+    if (r + 1 >= i1) return 1;
+    x1 = a.items[r + 1];
+    if (x1.x != x0.x || x1.w != x0.w) return 1;
+    if (r + 2 >= i1) return 2;
+    x2 = a.items[r + 2];
+    return (x2.x == x0.x && x2.w == x0.w) ? 3 : 2;
+}
+__device__ __forceinline__ int4 pick(int w, const int4& x0, const int4& x1, const int4& x2) {
+    return w == 0 ? x0 : (w == 1 ? x1 : x2);
 }
 
 // Walks the rounds from r to the next item of warpgroup w (returned in out).
@@ -99,8 +109,8 @@ __device__ __forceinline__ int round_items(const Args& a, int r, int i1, int4& x
 __device__ __forceinline__ int next_item(const Args& a, int w, int& r, int i1, int& cur_bh, int& cur_e, int& changes,
                                          uint64_t* kvfull, uint64_t* kvfree, int4& out) {
     while (r < i1) {
-        int4 x0, x1;
-        const int cnt = round_items(a, r, i1, x0, x1);
+        int4 x0, x1, x2;
+        const int cnt = round_items(a, r, i1, x0, x1, x2);
         if (x0.w != cur_bh || x0.x != cur_e) {
             if (changes > 0) umma::mma_commit(kvfree);
             if (!umma::mbar_wait(kvfull, changes & 1, a.status)) return -1;
@@ -111,7 +121,7 @@ __device__ __forceinline__ int next_item(const Args& a, int w, int& r, int i1, i
         }
         r += cnt;
         if (w < cnt) {
-            out = w == 0 ? x0 : x1;
+            out = pick(w, x0, x1, x2);
             return 1;
         }
     }
@@ -121,8 +131,8 @@ __device__ __forceinline__ int next_item(const Args& a, int w, int& r, int i1, i
 // Whether warpgroup w has another item before the next list change.
 __device__ __forceinline__ bool next_same(const Args& a, int w, int r, int i1, int cur_bh, int cur_e) {
     while (r < i1) {
-        int4 x0, x1;
-        const int cnt = round_items(a, r, i1, x0, x1);
+        int4 x0, x1, x2;
+        const int cnt = round_items(a, r, i1, x0, x1, x2);
         if (x0.w != cur_bh || x0.x != cur_e) return false;
         if (w < cnt) return true;
         r += cnt;
@@ -198,7 +208,7 @@ __global__ void __launch_bounds__(NT, 1)
         bool ok = true;
         for (int r = i0; r < i1 && ok;) {
             int4 it[NWG];
-            const int cnt = round_items(a, r, i1, it[0], it[1]);
+            const int cnt = round_items(a, r, i1, it[0], it[1], it[2]);
             if (it[0].w != cur_bh || it[0].x != cur_e) {
                 // wait until the MMAs reading the previous lists are done
                 if (changes > 0) ok = __all_sync(0xffffffffu, mbar_wait(&kvfree, (changes - 1) & 1, a.status));
@@ -260,7 +270,7 @@ __global__ void __launch_bounds__(NT, 1)
         // the staged rows are finite (zero or repeated), so P = 0 there.
         if (lane == 0) {
             const int w = warp - 1;
-            const uint32_t tS = tb + w * kTStride, tP = tS + kTP, tO = tS + kTO;
+            const uint32_t tS = tb + tcol_s(w), tP = tb + tcol_p(w), tO = tb + tcol_o(w);
             const uint64_t kd = sdesc_sw128(smem_u32(S.keys)), vd = sdesc_sw128(smem_u32(S.vals));
             const uint64_t qd = sdesc_sw128(smem_u32(S.q + w * QB * 16384));  // + 1024 per buffer
             int r = i0, cur_bh = -1, cur_e = -1, changes = 0;
@@ -275,7 +285,7 @@ __global__ void __launch_bounds__(NT, 1)
                 }
                 if (gs >= 1 && !mbar_wait(&sfree[w], (gs - 1) & 1, a.status)) return false;  // rows read S(gs - 1)
                 tc_fence_after();
-                mma_ss_k64(tS, qd + (q % QB) * 1024, kd + j * 1024, kIdescS, 0u);
+                mma_ss_k64(tS, qd + (q % QB) * 1024, kd + j * 512, kIdescS, 0u);
                 mma_commit(&sfull[w]);
                 if (j == a.nblk - 1) mma_commit(&qfree[qb]);
                 ++gs;
@@ -287,8 +297,7 @@ __global__ void __launch_bounds__(NT, 1)
                 if (j == 0 && npv > 0 && !mbar_wait(&ofree[w], (npv - 1) & 1, a.status)) return false;
                 if (!mbar_wait(&pfull[w], gp & 1, a.status)) return false;
                 tc_fence_after();
-                mma_ts_k64(tO, tP, vd + j * 1024, kIdescPV, j > 0 ? 1u : 0u);
-                mma_ts_k64(tO, tP + 32, vd + j * 1024 + 512, kIdescPV, 1u);
+                mma_ts_k64(tO, tP, vd + j * 512, kIdescPV, j > 0 ? 1u : 0u);
                 mma_commit(&pvdone[w]);
                 ++gp;
                 return true;
@@ -317,7 +326,7 @@ __global__ void __launch_bounds__(NT, 1)
         const int w = (warp - 1 - NWG) >> 2;  // 4 consecutive warps cover the 4 TMEM lane quarters
         const int t = (warp & 3) * 32 + lane;  // TMEM lane = query row of the item
         const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-        const uint32_t tS = tb + w * kTStride + lane_off, tP = tS + kTP, tO = tS + kTO;
+        const uint32_t tS = tb + tcol_s(w) + lane_off, tP = tb + tcol_p(w) + lane_off, tO = tb + tcol_o(w) + lane_off;
         uint32_t gb = 0;
         bool ok = true;
         bool pend = false, pend_row = false;  // an item whose epilogue is pending
@@ -348,11 +357,11 @@ __global__ void __launch_bounds__(NT, 1)
             pend = false;
         };
         for (int r = i0; r < i1 && ok;) {
-            int4 x0, x1;
-            const int cnt = round_items(a, r, i1, x0, x1);
+            int4 x0, x1, x2;
+            const int cnt = round_items(a, r, i1, x0, x1, x2);
             r += cnt;
             if (w >= cnt) continue;
-            const int4 item = w == 0 ? x0 : x1;
+            const int4 item = pick(w, x0, x1, x2);
             const int64_t bh = item.w;
             const int n = t < item.z ? a.perm[bh * a.N + item.y + t] : 0;
             float mrun = -INFINITY, lrun = 0.f;
@@ -378,14 +387,11 @@ __global__ void __launch_bounds__(NT, 1)
                 }
                 // 8 independent partial maxima: short dependency chains
                 float pm[8];
-                static_assert(KB == 128, "the partial maxima below cover exactly 128 columns");
+                static_assert(KB == 64, "the partial maxima below cover exactly 64 columns");
 #pragma unroll
-                for (int u = 0; u < 8; ++u) {  // columns u, u+8, ..., u+120
-                    float x = fmax3(s[u], s[u + 8], s[u + 16]);
-#pragma unroll
-                    for (int i = 3; i < 15; i += 2) x = fmax3(x, s[u + 8 * i], s[u + 8 * i + 8]);
-                    pm[u] = fmaxf(x, s[u + 120]);
-                }
+                for (int u = 0; u < 8; ++u)  // columns u, u+8, ..., u+56
+                    pm[u] = fmax3(fmax3(s[u], s[u + 8], s[u + 16]), fmax3(s[u + 24], s[u + 32], s[u + 40]),
+                                  fmaxf(s[u + 48], s[u + 56]));
                 const float bmax = fmaxf(fmax3(pm[0], pm[1], pm[2]), fmax3(fmax3(pm[3], pm[4], pm[5]), pm[6], pm[7])) * kC;
                 const float mnew = (bmax > mrun + kLazy) ? bmax : mrun;
                 const float alpha = exp2f(mrun - mnew);  // 0 on the first block, 1 when the max is kept
@@ -425,7 +431,6 @@ __global__ void __launch_bounds__(NT, 1)
                     }
                 }
                 tmem_st32u(tP, pk);
-                tmem_st32u(tP + 32, pk + 32);
                 tmem_st_wait();
                 tc_fence_before();
                 warp_arrive(&pfull[w]);
@@ -451,7 +456,7 @@ __global__ void __launch_bounds__(NT, 1)
     if (warp == 0) tmem_free(tb, 512);
 }
 
-size_t smem_bytes(int nblk) { return 1024 + static_cast<size_t>(nblk) * 32768 + NWG * QB * 16384; }
+size_t smem_bytes(int nblk) { return 1024 + static_cast<size_t>(nblk) * 16384 + NWG * QB * 16384; }
 
 int key_rows(const Plan& p) { return ((p.s.m + 3) & ~3) + p.s.k; }
 
