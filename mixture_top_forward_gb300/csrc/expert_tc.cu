@@ -404,8 +404,7 @@ __global__ void __launch_bounds__(NT, 1)
 #pragma unroll
                 for (int c = 0; c < KB; c += 2) {
                     const float2 x = __ffma2_rn(make_float2(s[c], s[c + 1]), c2, m2);
-                    // one pair in four on the FMA pipe, the rest on the MUFU unit
-                    const float2 e = (c & 6) == 0 ? exp2_fma2(x) : make_float2(exp2f(x.x), exp2f(x.y));
+                    const float2 e = make_float2(exp2f(x.x), exp2f(x.y));
                     acc[(c >> 1) & 3] = __fadd2_rn(acc[(c >> 1) & 3], e);
                     pk[c >> 1] = pack_bf16(e.x, e.y);
                 }

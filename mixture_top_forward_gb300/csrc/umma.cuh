@@ -134,29 +134,6 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
     return r;
 }
 
-// 2^x for a pair of values on the FMA pipe (to take load off the MUFU unit,
-// which the softmax loops saturate). Cody-Waite split x = n + f, n = round(x)
-// (adding 1.5 * 2^23 rounds to an integer in the low mantissa bits),
-// f in [-1/2, 1/2]; 2^f by a cubic fitted to 2^f on [-1/2, 1/2] (least squares
-// at Chebyshev nodes, refined toward minimax relative error: |rel err| <
-// 7.5e-5, far below the 2^-9 of the bf16 weights it feeds); 2^n added to the
-// exponent field: with t = x + 1.5 * 2^23, (bits(t) << 23) = n << 23 modulo
-// 2^32. x is clamped to >= -126, so -inf gives 2^-126 (negligible next to the
-// block maximum's weight, >= 2^-8), not 0.
-__device__ __forceinline__ float2 exp2_fma2(float2 x) {
-    constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23
-    x = make_float2(fmaxf(x.x, -126.0f), fmaxf(x.y, -126.0f));
-    const float2 t = __fadd2_rn(x, make_float2(kMagic, kMagic));
-    const float2 n = __fadd2_rn(t, make_float2(-kMagic, -kMagic));
-    const float2 f = __fadd2_rn(x, make_float2(-n.x, -n.y));
-    float2 p = __ffma2_rn(make_float2(0.0551716648f, 0.0551716648f), f, make_float2(0.2426111251f, 0.2426111251f));
-    p = __ffma2_rn(p, f, make_float2(0.6932609677f, 0.6932609677f));
-    p = __ffma2_rn(p, f, make_float2(0.9999280572f, 0.9999280572f));
-    const int ex = __float_as_int(p.x) + (__float_as_int(t.x) << 23);
-    const int ey = __float_as_int(p.y) + (__float_as_int(t.y) << 23);
-    return make_float2(__int_as_float(ex), __int_as_float(ey));
-}
-
 // Orders this thread's generic-proxy shared-memory writes before later
 // async-proxy reads (tensor core, TMA).
 __device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
