@@ -25,11 +25,16 @@
 //                   memory, B in shared memory) into its TMEM accumulator;
 //   warps 4-7, 8-11, 12-15: one warpgroup per item (4 consecutive warps cover
 //                   the 4 TMEM lane quarters), one thread per query row: load
-//                   the 64 logits, update the running max (kept while it grows
-//                   by < 2^8, so O rarely needs rescaling), p = 2^(s tau log2e
+//                   the 64 logits, update the running max, p = 2^(s tau log2e
 //                   - max) in registers, P as bf16 pairs into TMEM once the
 //                   previous block's P.V is done; at the end O / rowsum ->
-//                   bf16 -> the query's row.
+//                   bf16 -> the query's row. The row sum takes each block's
+//                   largest weight as rounded to bf16 for the P.V product, so
+//                   a dominant key's rounding cancels in O / rowsum.
+// The running max is kept while a new block maximum stays within 2^32 of it,
+// so O is rescaled (after the block's P.V wait) only for extreme logit
+// ranges. Weights up to 2^32 stay far inside the bf16/fp32 range; O overflows
+// only for values beyond ~2^86 in magnitude.
 // TMEM per warpgroup: 64 columns of S, 32 of P (bf16 pairs), 64 of O, so three
 // warpgroups (three row warps per SM sub-partition) fit in the 512 columns.
 // Handshakes are mbarriers, each completed exactly once per event its waiter
@@ -46,7 +51,7 @@ namespace {
 using namespace umma;
 
 constexpr float kC = 0.125f * kLog2e;  // tau * log2(e), tau = 1/sqrt(64)
-constexpr float kLazy = 8.0f;          // keep the running max while the new one is within 2^8
+constexpr float kLazy = 32.0f;         // keep the running max while the new one is within 2^32
 constexpr int KB = 64;                 // keys per block
 constexpr int NWG = 3;                 // row warpgroups
 constexpr int QB = 2;                  // query-row buffers per warpgroup
@@ -392,9 +397,16 @@ __global__ void __launch_bounds__(NT, 1)
                 for (int u = 0; u < 8; ++u)  // columns u, u+8, ..., u+56
                     pm[u] = fmax3(fmax3(s[u], s[u + 8], s[u + 16]), fmax3(s[u + 24], s[u + 32], s[u + 40]),
                                   fmaxf(s[u + 48], s[u + 56]));
-                const float bmax = fmaxf(fmax3(pm[0], pm[1], pm[2]), fmax3(fmax3(pm[3], pm[4], pm[5]), pm[6], pm[7])) * kC;
+                const float smax = fmaxf(fmax3(pm[0], pm[1], pm[2]), fmax3(fmax3(pm[3], pm[4], pm[5]), pm[6], pm[7]));
+                const float bmax = smax * kC;
                 const float mnew = (bmax > mrun + kLazy) ? bmax : mrun;
                 const float alpha = exp2f(mrun - mnew);  // 0 on the first block, 1 when the max is kept
+                // The P.V product sees the weights rounded to bf16, the row sum
+                // below adds them unrounded; the block's largest weight
+                // dominates the difference, so the sum takes its rounding
+                // (computed exactly as in the loop: same fused multiply-add).
+                const float emax = exp2f(fmaf(smax, kC, -mnew));
+                const float corr = __bfloat162float(__float2bfloat16_rn(emax)) - emax;
                 // packed pairs: one f32x2 FMA forms two exponents, one f32x2 add
                 // accumulates two weights; P goes out as bf16 pairs
                 const float2 c2 = make_float2(kC, kC), m2 = make_float2(-mnew, -mnew);
@@ -409,7 +421,7 @@ __global__ void __launch_bounds__(NT, 1)
                     pk[c >> 1] = pack_bf16(e.x, e.y);
                 }
                 const float sum = ((acc[0].x + acc[0].y) + (acc[1].x + acc[1].y)) + ((acc[2].x + acc[2].y) + (acc[3].x + acc[3].y));
-                lrun = lrun * alpha + sum;
+                lrun = lrun * alpha + (sum + corr);
                 // P.V of the previous block (for j = 0 the previous item's last)
                 // must be done before P is overwritten or O rescaled
                 const bool rescale = j > 0 && __any_sync(0xffffffffu, alpha != 1.f);
