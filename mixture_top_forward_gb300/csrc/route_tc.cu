@@ -9,15 +9,16 @@
 // Persistent CTAs, each over a contiguous range of 128-query tiles (so the
 // head, and with it the landmark operand, changes rarely).
 //   warp 4 lane 0: TMA loads of Q tiles (4-stage ring) and of the head's
-//                  landmark queries (bf16 hi/lo pair, m_pad <= 256 rows), and
-//                  the MMAs D = Q Lq_hi^T + Q Lq_lo^T (M = 128, N = m_pad,
-//                  exact to ~2^-16 of the fp32 landmarks) into one of two TMEM
-//                  buffers;
-//   warps 0-3, 5-8: two argmax warpgroups, one per TMEM buffer (tiles
-//                  alternate): one query row per thread, argmax over the m
-//                  logits, the route, and a shared-memory histogram (one per
-//                  warpgroup) of the head's routes that is added to the
-//                  per-head expert counts.
+//                  landmark queries (bf16 hi/lo pair, m_pad <= 256 rows);
+//   warps 9, 10 (lane 0): MMA issuers, one per TMEM buffer b (tiles t = b mod
+//                  2): D = Q Lq_hi^T + Q Lq_lo^T (M = 128, N = m_pad, exact to
+//                  ~2^-16 of the fp32 landmarks); a tcgen05.mma holds its
+//                  issuing thread about as long as it runs, so the two
+//                  buffers' MMAs come from separate threads;
+//   warps 0-3, 5-8: two argmax warpgroups, one per TMEM buffer: one query row
+//                  per thread, argmax over the m logits, the route, and a
+//                  shared-memory histogram (one per warpgroup) of the head's
+//                  routes that is added to the per-head expert counts.
 // Every wait is bounded (umma.cuh).
 #include <algorithm>
 
@@ -43,13 +44,13 @@ struct RouteArgs {
     int m, m_pad;
 };
 
-constexpr int RT_THREADS = 288;  // warps 0-3 and 5-8: argmax groups; warp 4: loads and MMAs
+constexpr int RT_THREADS = 352;  // warps 0-3 and 5-8: argmax groups; 4: loads; 9, 10: MMA issuers
 
 __global__ void __launch_bounds__(RT_THREADS, 1) route_tc_kernel(const __grid_constant__ CUtensorMap tq,
                                                           const __grid_constant__ CUtensorMap thi,
                                                           const __grid_constant__ CUtensorMap tlo, RouteArgs a) {
     extern __shared__ uint8_t smem_raw[];
-    __shared__ uint64_t qfull[QST], qempty[QST], dfull[2], dfree[2], lqbar;
+    __shared__ uint64_t qfull[QST], qempty[QST], dfull[2], dfree[2], lqfull, lqfree;
     __shared__ uint32_t tmem_base;
     __shared__ int hist[2][256];
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -67,7 +68,8 @@ __global__ void __launch_bounds__(RT_THREADS, 1) route_tc_kernel(const __grid_co
             mbar_init(&dfull[i], 1);
             mbar_init(&dfree[i], 4);  // every warp of the buffer's group arrives
         }
-        mbar_init(&lqbar, 1);
+        mbar_init(&lqfull, 1);
+        mbar_init(&lqfree, 2);  // one commit per MMA issuer
         fence_barrier_init();
     }
     for (int e = tid; e < 512; e += blockDim.x) hist[e >> 8][e & 255] = 0;
@@ -78,9 +80,8 @@ __global__ void __launch_bounds__(RT_THREADS, 1) route_tc_kernel(const __grid_co
     const uint32_t tb = tmem_base;
 
     if (warp == 4) {
+        // ---------------- loads (lane 0) ----------------
         if (lane == 0) {
-            const uint32_t idesc = idesc_bf16(128, a.m_pad, false);
-            const uint32_t hi = smem_u32(base), lo = smem_u32(base + OFF_LO);
             auto load_q = [&](int t) {
                 const int st = t % QST;
                 const int64_t g = t0 + t;
@@ -90,37 +91,57 @@ __global__ void __launch_bounds__(RT_THREADS, 1) route_tc_kernel(const __grid_co
             };
             for (int t = 0; t < nt && t < QST; ++t) load_q(t);
             int64_t cur = -1;
-            uint32_t lq_phase = 0;
+            int changes = 0;
             for (int t = 0; t < nt; ++t) {
                 const int64_t bh = (t0 + t) / a.tiles_per_head;
                 if (bh != cur) {  // restage the landmarks once the MMAs reading them are done
-                    if (t > 0 && !mbar_wait(&dfull[(t - 1) & 1], ((t - 1) >> 1) & 1, a.status)) break;
-                    mbar_arrive_expect_tx(&lqbar, 2u * a.m_pad * 128u);
-                    tma_load_2d(base, &thi, 0, static_cast<int>(bh * a.m), &lqbar);
-                    tma_load_2d(base + OFF_LO, &tlo, 0, static_cast<int>(bh * a.m), &lqbar);
-                    if (!mbar_wait(&lqbar, lq_phase, a.status)) break;
-                    lq_phase ^= 1;
+                    if (changes > 0 && !mbar_wait(&lqfree, (changes - 1) & 1, a.status)) break;
+                    mbar_arrive_expect_tx(&lqfull, 2u * a.m_pad * 128u);
+                    tma_load_2d(base, &thi, 0, static_cast<int>(bh * a.m), &lqfull);
+                    tma_load_2d(base + OFF_LO, &tlo, 0, static_cast<int>(bh * a.m), &lqfull);
+                    ++changes;
                     cur = bh;
                 }
+                // refill the stage of tile t once its MMAs are done
+                if (t + QST < nt) {
+                    if (!mbar_wait(&qempty[t % QST], (t / QST) & 1, a.status)) break;
+                    load_q(t + QST);
+                }
+            }
+        }
+    } else if (warp >= 9) {
+        // ---------------- MMA issuer of TMEM buffer b (lane 0) ----------------
+        // Walks every tile to follow the landmark restages (each head change
+        // is released, then waited for), and issues the tiles t = b mod 2.
+        if (lane == 0) {
+            const int b = warp - 9;
+            const uint32_t idesc = idesc_bf16(128, a.m_pad, false);
+            const uint32_t hi = smem_u32(base), lo = smem_u32(base + OFF_LO);
+            const uint32_t d = tb + b * 256;
+            int64_t cur = -1;
+            int changes = 0;
+            for (int t = 0; t < nt; ++t) {
+                const int64_t bh = (t0 + t) / a.tiles_per_head;
+                if (bh != cur) {
+                    if (changes > 0) mma_commit(&lqfree);  // once this thread's MMAs on the old landmarks are done
+                    if (!mbar_wait(&lqfull, changes & 1, a.status)) break;
+                    ++changes;
+                    cur = bh;
+                }
+                if ((t & 1) != b) continue;
                 const int st = t % QST;
                 if (!mbar_wait(&qfull[st], (t / QST) & 1, a.status)) break;
-                if (t >= 2 && !mbar_wait(&dfree[t & 1], ((t >> 1) - 1) & 1, a.status)) break;
+                // the argmax group has read this buffer's previous tile (t - 2)
+                if (t >= 2 && !mbar_wait(&dfree[b], ((t >> 1) - 1) & 1, a.status)) break;
                 tc_fence_after();
                 const uint32_t qa = smem_u32(base + OFF_Q + st * 16384);
-                const uint32_t d = tb + (t & 1) * 256;
 #pragma unroll
                 for (int s = 0; s < 4; ++s)
                     mma_ss(d, sdesc_sw128(qa + s * 32), sdesc_sw128(hi + s * 32), idesc, s > 0);
 #pragma unroll
                 for (int s = 0; s < 4; ++s) mma_ss(d, sdesc_sw128(qa + s * 32), sdesc_sw128(lo + s * 32), idesc, 1u);
-                mma_commit(&dfull[t & 1]);
+                mma_commit(&dfull[b]);
                 mma_commit(&qempty[st]);
-                // refill the stage of the previous tile (its MMAs were issued earlier)
-                if (t >= 1 && t - 1 + QST < nt) {
-                    const int ps = (t - 1) % QST;
-                    if (!mbar_wait(&qempty[ps], ((t - 1) / QST) & 1, a.status)) break;
-                    load_q(t - 1 + QST);
-                }
             }
         }
     } else {
@@ -177,6 +198,7 @@ __global__ void __launch_bounds__(RT_THREADS, 1) route_tc_kernel(const __grid_co
                     best = bv[u];
                     arg = bi[u];
                 }
+            arg = min(arg, a.m - 1);  // in range whatever the logits (non-finite ones are out of contract)
             const int64_t n = tile * 128 + row;
             if (n < a.N) {
                 a.route[bh * a.N + n] = arg;
