@@ -209,6 +209,32 @@ def cpu_baseline(name, q, k, v, heads=2):
 # ---------------------------------------------------------------------------
 # GPU arm.
 # ---------------------------------------------------------------------------
+def rank_barrier(world):
+    """All ranks meet here (N > 1 only)."""
+    if world > 1:
+        import torch
+
+        torch.distributed.barrier()
+
+
+def max_over_ranks(ms, world, device=None):
+    """The slowest rank's time; every rank gets it. The replicas are
+    independent, so the job is done when the last one is."""
+    if world == 1:
+        return ms
+    import torch
+
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(queries_per_rank, world, ms_step):
+    """Queries of all ranks per second (weak scaling: each rank has its own
+    full problem), over the slowest rank's step time."""
+    return queries_per_rank * world / (ms_step / 1e3)
+
+
 def run_gpu(args, rank, world):
     import torch
 
@@ -242,8 +268,7 @@ def run_gpu(args, rank, world):
     clocks = Clocks(dev.index) if rank == 0 else None
     time.sleep(0.3 if clocks else 0)
     M.mita_profile_enable(True)
-    if world > 1:
-        torch.distributed.barrier()
+    rank_barrier(world)
     torch.cuda.synchronize()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     ev0.record(stream)
@@ -251,20 +276,16 @@ def run_gpu(args, rank, world):
         step()
     ev1.record(stream)
     torch.cuda.synchronize()
-    if world > 1:
-        torch.distributed.barrier()
+    rank_barrier(world)
     M.mita_profile_enable(False)
     ms = ev0.elapsed_time(ev1)
     stages = M.mita_profile_read(stream)
     clk = clocks.stop() if clocks else None
     assert M.mita_sync_status(stream) == 0, M.mita_last_error()
-    if world > 1:
-        t = torch.tensor([ms], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, world, dev)
     ms_step = ms / args.steps
     queries = B * H * N
-    value = queries * world / (ms_step / 1e3)
+    value = job_throughput(queries, world, ms_step)
 
     peaks, peak_src = load_peaks()
     w = work(c)
@@ -304,8 +325,10 @@ def run_gpu(args, rank, world):
     del Q, K, V, out
     torch.cuda.empty_cache()
 
-    if rank == 0 and not args.no_e2e:
-        res["e2e"] = e2e(args, M, q, k, v, c, stream)
+    if not args.no_e2e:  # every rank: the job's end-to-end rate
+        e = e2e(args, M, q, k, v, c, stream, world, dev)
+        if rank == 0:
+            res["e2e"] = e
     if rank == 0 and not args.no_sweep:
         res["sweep"] = sweep(args, M, dev, stream, peaks)
     if rank == 0 and not args.no_cpu and world == 1:
@@ -313,9 +336,10 @@ def run_gpu(args, rank, world):
     return res
 
 
-def e2e(args, M, q, k, v, c, stream):
+def e2e(args, M, q, k, v, c, stream, world=1, dev=None):
     """Same metric through the host-buffer entry point: each step copies the
-    inputs from pinned host memory and the results back."""
+    inputs from pinned host memory and the results back. With N ranks each
+    runs its replica; the time is the slowest rank's."""
     import torch
 
     pin = lambda a: torch.from_numpy(a).pin_memory().numpy()
@@ -327,11 +351,12 @@ def e2e(args, M, q, k, v, c, stream):
     for _ in range(max(1, min(args.warmup, 3))):
         M.mita_forward_host(qh, kh, vh, *args_, out=out, expert_idx=eidx, route=route, stream=stream.cuda_stream)
     n = max(3, min(args.steps, 10))
+    rank_barrier(world)
     t0 = time.perf_counter()
     for _ in range(n):
         M.mita_forward_host(qh, kh, vh, *args_, out=out, expert_idx=eidx, route=route, stream=stream.cuda_stream)
-    dt = (time.perf_counter() - t0) / n
-    return {"value": c["B"] * c["H"] * c["N"] / dt, "unit": "queries/s",
+    dt = max_over_ranks((time.perf_counter() - t0) * 1e3, world, dev) / 1e3 / n
+    return {"value": job_throughput(c["B"] * c["H"] * c["N"], world, dt * 1e3), "unit": "queries/s",
             "h2d_bytes_per_step": int(qh.nbytes + kh.nbytes + vh.nbytes),
             "d2h_bytes_per_step": int(out.nbytes + eidx.nbytes + route.nbytes), "steps": n,
             "ms_per_step": dt * 1e3}
