@@ -89,9 +89,14 @@ int mita_forward_aux(const void* Q, const void* K, const void* V, int B, int H, 
 /*
  * mita_forward on HOST buffers (same shapes and dtypes; bf16 as uint16 bit
  * patterns). Copies the inputs to the device, runs the forward pass on
- * `stream`, copies out, expert_idx and route back, and returns after the
- * stream has finished. Host buffers may be pageable; pinned buffers copy
- * faster. Device staging buffers are part of the cached workspace.
+ * `stream`, copies out, expert_idx and route back, and returns once every
+ * copy has finished (also on error: no copy touches the caller's buffers
+ * after the call returns). When Q, K and V together reach 256 MiB the heads
+ * go in up to 8 groups: one group's inputs are copied in while the previous
+ * group runs on `stream` and the one before is copied out, on two copy
+ * streams the library creates per (device, stream) and keeps until
+ * mita_release_workspace. Host buffers may be pageable; pinned buffers copy
+ * faster and overlap. Device staging buffers are part of the cached workspace.
  */
 int mita_forward_host(const uint16_t* Q, const uint16_t* K, const uint16_t* V, int B, int H, int N, int d,
                       int grid_h, int grid_w, int m, int k, uint16_t* out, int32_t* expert_idx, int32_t* route,

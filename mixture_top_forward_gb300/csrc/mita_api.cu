@@ -35,6 +35,11 @@ int cuda_fail(cudaError_t e, const char* what) {
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
+// The host entry point pipelines up to kHostGroups head groups once Q, K and V
+// together reach kHostPipelineBytes.
+constexpr int kHostGroups = 8;
+constexpr size_t kHostPipelineBytes = size_t(256) << 20;
+
 int isqrt_exact(int m) {
     int p = 0;
     while ((p + 1) * (p + 1) <= m) ++p;
@@ -417,6 +422,43 @@ extern "C" int mita_forward(const void* Q, const void* K, const void* V, int B, 
                             stream);
 }
 
+namespace {
+
+// Copy streams of the host entry point, one pair per (device, caller stream),
+// with their events; created on first use and kept (guarded by g_ws_mu).
+struct HostStreams {
+    cudaStream_t in = nullptr, out = nullptr;
+    cudaEvent_t start = nullptr;
+    cudaEvent_t ready[kHostGroups] = {}, done[kHostGroups] = {};
+};
+std::map<std::pair<int, uintptr_t>, HostStreams> g_hs;
+
+int host_streams(cudaStream_t st, HostStreams** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    std::lock_guard<std::mutex> lk(g_ws_mu);
+    HostStreams& h = g_hs[{dev, reinterpret_cast<uintptr_t>(st)}];
+    if (!h.in) {
+        if ((e = cudaStreamCreateWithFlags(&h.in, cudaStreamNonBlocking)) != cudaSuccess ||
+            (e = cudaStreamCreateWithFlags(&h.out, cudaStreamNonBlocking)) != cudaSuccess ||
+            (e = cudaEventCreateWithFlags(&h.start, cudaEventDisableTiming)) != cudaSuccess)
+            return cuda_fail(e, "copy stream creation");
+        for (int g = 0; g < kHostGroups; ++g)
+            if ((e = cudaEventCreateWithFlags(&h.ready[g], cudaEventDisableTiming)) != cudaSuccess ||
+                (e = cudaEventCreateWithFlags(&h.done[g], cudaEventDisableTiming)) != cudaSuccess)
+                return cuda_fail(e, "copy event creation");
+    }
+    *out = &h;
+    return MITA_OK;
+}
+
+}  // namespace
+
+// Pipelined by groups of heads (the heads are independent problems): group
+// g's inputs are copied in on one stream while group g-1 runs on the
+// caller's stream and group g-2's results are copied out on a third, so the
+// forward pass and the outgoing copies hide under the incoming copies.
 extern "C" int mita_forward_host(const uint16_t* Q, const uint16_t* K, const uint16_t* V, int B, int H, int N, int d,
                                  int grid_h, int grid_w, int m, int k, uint16_t* out, int32_t* expert_idx,
                                  int32_t* route, void* stream) {
@@ -428,9 +470,12 @@ extern "C" int mita_forward_host(const uint16_t* Q, const uint16_t* K, const uin
     if (!Q || !K || !V || !out || !expert_idx || !route)
         return fail(MITA_ERR_INVALID_ARG, "a required pointer is NULL");
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    const size_t tok = static_cast<size_t>(s.BH) * s.N * D * 2;
-    const size_t eb = static_cast<size_t>(s.BH) * s.m * s.k * sizeof(int32_t);
-    const size_t rb = static_cast<size_t>(s.BH) * s.N * sizeof(int32_t);
+    const size_t head_tok = static_cast<size_t>(s.N) * D * 2;  // bytes of one head's Q (K, V, out)
+    const size_t head_e = static_cast<size_t>(s.m) * s.k * sizeof(int32_t);
+    const size_t head_r = static_cast<size_t>(s.N) * sizeof(int32_t);
+    const size_t tok = static_cast<size_t>(s.BH) * head_tok;
+    const size_t eb = static_cast<size_t>(s.BH) * head_e;
+    const size_t rb = static_cast<size_t>(s.BH) * head_r;
     size_t off = 0;
     const size_t oq = off; off += align256(tok);
     const size_t ok_ = off; off += align256(tok);
@@ -441,20 +486,50 @@ extern "C" int mita_forward_host(const uint16_t* Q, const uint16_t* K, const uin
     void* stage = nullptr;
     if ((rc = workspace(st, 1, off, &stage)) != MITA_OK) return rc;
     char* sb = static_cast<char*>(stage);
-    cudaError_t e;
-    if ((e = cudaMemcpyAsync(sb + oq, Q, tok, cudaMemcpyHostToDevice, st)) != cudaSuccess ||
-        (e = cudaMemcpyAsync(sb + ok_, K, tok, cudaMemcpyHostToDevice, st)) != cudaSuccess ||
-        (e = cudaMemcpyAsync(sb + ov, V, tok, cudaMemcpyHostToDevice, st)) != cudaSuccess)
-        return cuda_fail(e, "host-to-device copy");
-    rc = mita_forward_aux(sb + oq, sb + ok_, sb + ov, B, H, N, d, grid_h, grid_w, m, k, sb + oo,
-                          reinterpret_cast<int32_t*>(sb + oe), reinterpret_cast<int32_t*>(sb + orr), nullptr, nullptr,
-                          stream);
+    HostStreams* hs = nullptr;
+    if ((rc = host_streams(st, &hs)) != MITA_OK) return rc;
+    // groups: one per head up to kHostGroups, when the inputs are large
+    // enough for the overlap to outweigh the extra launches
+    int64_t groups = 3 * tok >= kHostPipelineBytes ? std::min<int64_t>(s.BH, kHostGroups) : 1;
+    const int64_t per = cdiv(s.BH, groups);
+    groups = cdiv(s.BH, per);
+    cudaError_t e = cudaEventRecord(hs->start, st);  // after the caller's earlier work on `stream`
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(hs->in, hs->start, 0);
+    for (int64_t g = 0; g < groups && e == cudaSuccess && rc == MITA_OK; ++g) {
+        const int64_t h0 = g * per, nh = std::min<int64_t>(per, s.BH - h0);
+        const size_t t0 = h0 * head_tok, tn = nh * head_tok;
+        const uint16_t* src[3] = {Q, K, V};
+        const size_t dst[3] = {oq, ok_, ov};
+        for (int i = 0; i < 3 && e == cudaSuccess; ++i)
+            e = cudaMemcpyAsync(sb + dst[i] + t0, reinterpret_cast<const char*>(src[i]) + t0, tn,
+                                cudaMemcpyHostToDevice, hs->in);
+        if (e == cudaSuccess) e = cudaEventRecord(hs->ready[g], hs->in);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(st, hs->ready[g], 0);
+        if (e != cudaSuccess) break;
+        rc = mita_forward_aux(sb + oq + t0, sb + ok_ + t0, sb + ov + t0, 1, static_cast<int>(nh), N, d, grid_h,
+                              grid_w, m, k, sb + oo + t0, reinterpret_cast<int32_t*>(sb + oe + h0 * head_e),
+                              reinterpret_cast<int32_t*>(sb + orr + h0 * head_r), nullptr, nullptr, stream);
+        if (rc != MITA_OK) break;
+        e = cudaEventRecord(hs->done[g], st);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(hs->out, hs->done[g], 0);
+        if (e == cudaSuccess)
+            e = cudaMemcpyAsync(reinterpret_cast<char*>(out) + t0, sb + oo + t0, tn, cudaMemcpyDeviceToHost, hs->out);
+        if (e == cudaSuccess)
+            e = cudaMemcpyAsync(reinterpret_cast<char*>(expert_idx) + h0 * head_e, sb + oe + h0 * head_e, nh * head_e,
+                                cudaMemcpyDeviceToHost, hs->out);
+        if (e == cudaSuccess)
+            e = cudaMemcpyAsync(reinterpret_cast<char*>(route) + h0 * head_r, sb + orr + h0 * head_r, nh * head_r,
+                                cudaMemcpyDeviceToHost, hs->out);
+    }
+    // every copy touching the caller's host buffers is finished before returning, error or not
+    const cudaError_t e_in = cudaStreamSynchronize(hs->in);
+    const cudaError_t e_st = cudaStreamSynchronize(st);
+    const cudaError_t e_out = cudaStreamSynchronize(hs->out);
     if (rc != MITA_OK) return rc;
-    if ((e = cudaMemcpyAsync(out, sb + oo, tok, cudaMemcpyDeviceToHost, st)) != cudaSuccess ||
-        (e = cudaMemcpyAsync(expert_idx, sb + oe, eb, cudaMemcpyDeviceToHost, st)) != cudaSuccess ||
-        (e = cudaMemcpyAsync(route, sb + orr, rb, cudaMemcpyDeviceToHost, st)) != cudaSuccess)
-        return cuda_fail(e, "device-to-host copy");
-    if ((e = cudaStreamSynchronize(st)) != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+    if (e != cudaSuccess) return cuda_fail(e, "host copy pipeline");
+    if (e_in != cudaSuccess) return cuda_fail(e_in, "host-to-device copies");
+    if (e_st != cudaSuccess) return cuda_fail(e_st, "cudaStreamSynchronize");
+    if (e_out != cudaSuccess) return cuda_fail(e_out, "device-to-host copies");
     return MITA_OK;
 }
 
@@ -544,6 +619,20 @@ extern "C" void mita_release_workspace(void) {
         kv.second.bytes = 0;
     }
     g_ws.clear();
+    for (auto& kv : g_hs) {
+        HostStreams& h = kv.second;
+        cudaSetDevice(kv.first.first);
+        if (h.in) cudaStreamSynchronize(h.in);
+        if (h.out) cudaStreamSynchronize(h.out);
+        for (int g = 0; g < kHostGroups; ++g) {
+            if (h.ready[g]) cudaEventDestroy(h.ready[g]);
+            if (h.done[g]) cudaEventDestroy(h.done[g]);
+        }
+        if (h.start) cudaEventDestroy(h.start);
+        if (h.in) cudaStreamDestroy(h.in);
+        if (h.out) cudaStreamDestroy(h.out);
+    }
+    g_hs.clear();
     cudaSetDevice(cur);
 }
 
