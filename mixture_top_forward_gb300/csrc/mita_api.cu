@@ -192,14 +192,28 @@ bool make_plan(const Shape& s, Plan* p) {
         const int64_t K8 = 8LL * s.k;
         int64_t t = std::max<int64_t>(2LL * s.k, std::min<int64_t>(s.N / 8, K8));
         if (8 * t <= s.N) {
+            // The first level has no threshold. When a 4x larger sample still
+            // fits below N/8 (and its logits in 1 GB), it writes every logit of
+            // that sample and its select ranks whole rows (dense): appending
+            // each sampled key as a candidate costs more, and the 4x larger
+            // sample makes the next level's threshold 4x tighter.
+            const int64_t t0 = 4 * t;
+            const bool dense0 = t0 <= s.N / 8 && s.BH * s.m * round_up(t0, 4) * 4 <= (1LL << 30);
             while (P.nlev < 3) {
-                const int64_t stride = s.N / t;
+                const int64_t ts = (P.nlev == 0 && dense0) ? t0 : t;
+                const int64_t stride = s.N / ts;
                 const int64_t S = cdiv(s.N, stride);
                 // the unfiltered first level keeps every sampled key: small chunks spread it over the SMs
-                P.lev[P.nlev++] = scan_level(s, S, stride, prevS, prevS == 0 ? 128 : 512, sms);
+                ScanLevel L = scan_level(s, S, stride, prevS, prevS == 0 ? 128 : 512, sms);
+                if (P.nlev == 0 && dense0) {
+                    L.dense = true;
+                    L.ld = round_up(S, 4);
+                    L.cap = 0;
+                }
+                P.lev[P.nlev++] = L;
                 prevS = S;
                 const int64_t next = std::min<int64_t>(16 * t, s.N / 8);
-                if (next <= t) break;
+                if (next <= S) break;
                 t = next;
             }
         }
@@ -215,7 +229,11 @@ bool make_plan(const Shape& s, Plan* p) {
             prevS = 1;  // chunking as for a filtered scan; no candidate buffers
         }
         P.lev[P.nlev++] = scan_level(s, s.N, 1, prevS, 512, sms);
-        if (P.dense) P.lev[0].cap = 0;
+        if (P.dense) {
+            P.lev[0].cap = 0;
+            P.lev[0].dense = true;
+            P.lev[0].ld = P.dense_ld;
+        }
     } else {
         // CUDA-core scan: 32 landmarks per CTA, ~8 CTAs per SM, >= 1024 keys per chunk
         const int64_t ltiles = cdiv(s.m, 32);
@@ -267,7 +285,10 @@ bool make_plan(const Shape& s, Plan* p) {
     P.off_perm = take(BH * static_cast<size_t>(s.N) * sizeof(int));
     P.off_items = take(BH * static_cast<size_t>(P.max_items) * sizeof(int4));
     P.off_nitems = take(sizeof(int));
-    P.off_dense = take(P.dense ? BH * m * static_cast<size_t>(P.dense_ld) * sizeof(float) : 0);
+    size_t dense_floats = 0;  // the largest dense level's logits
+    for (int l = 0; l < P.nlev; ++l)
+        if (P.lev[l].dense) dense_floats = std::max(dense_floats, BH * m * static_cast<size_t>(P.lev[l].ld));
+    P.off_dense = take(dense_floats * sizeof(float));
     P.total = off;
     if (P.max_items * s.BH > 0x7FFFFFFFLL || s.BH * P.nrblocks > 0x7FFFFFFFLL) return false;
     for (int l = 0; l < P.nlev; ++l)
@@ -295,7 +316,9 @@ Work carve(const Plan& p, void* base) {
     w.perm = reinterpret_cast<int*>(b + p.off_perm);
     w.items = reinterpret_cast<int4*>(b + p.off_items);
     w.nitems = reinterpret_cast<int*>(b + p.off_nitems);
-    w.dense = p.dense ? reinterpret_cast<float*>(b + p.off_dense) : nullptr;
+    bool any_dense = false;
+    for (int l = 0; l < p.nlev; ++l) any_dense = any_dense || p.lev[l].dense;
+    w.dense = any_dense ? reinterpret_cast<float*>(b + p.off_dense) : nullptr;
     return w;
 }
 

@@ -32,6 +32,8 @@ struct ScanLevel {
     int64_t chunk_len;  // samples per chunk (last one may be shorter)
     int chunks;         // chunks per head (one CTA each)
     int cap;            // candidate slots per (head, chunk, landmark)
+    bool dense;         // write every logit ([BH][m][ld] floats) instead of candidates
+    int64_t ld;         // row stride of those logits (S rounded up to 4)
 };
 
 struct Plan {

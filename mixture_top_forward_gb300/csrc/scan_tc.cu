@@ -451,8 +451,8 @@ cudaError_t launch_scan_tc(const Plan& p, const Work& w, const __nv_bfloat16* K,
     a.part = w.part;
     a.cand = w.cand;
     a.ccount = w.ccount;
-    a.dense = full ? w.dense : nullptr;
-    a.ld = p.dense_ld;
+    a.dense = L.dense ? w.dense : nullptr;
+    a.ld = L.ld;
     a.status = w.status;
     a.S = L.S;
     a.stride = L.stride;

@@ -33,7 +33,8 @@ __global__ void __launch_bounds__(ST) select_kernel(int m, int k, int chunks, in
                                                     const int* __restrict__ ccount, float* __restrict__ lv32,
                                                     __nv_bfloat16* __restrict__ lvbf,
                                                     int32_t* __restrict__ expert_idx, uint64_t* __restrict__ theta,
-                                                    const float* __restrict__ dense, int64_t N, int64_t ld) {
+                                                    const float* __restrict__ dense, int64_t N, int64_t ld,
+                                                    int64_t stride) {
     __shared__ unsigned hist[256];
     __shared__ int offs[ST + 1];        // chunk offsets into staged[] (chunks <= ST)
     __shared__ float red[ST / 32 + 1];  // block reductions
@@ -134,7 +135,7 @@ __global__ void __launch_bounds__(ST) select_kernel(int m, int k, int chunks, in
     // all of this landmark's candidates in shared memory when they fit
     const bool in_smem = (drow || small) && total <= SEL_CAP;
     if (in_smem && drow) {
-        for (int e = tid; e < total; e += ST) staged[e] = topk_key(drow[e] * 0.125f, static_cast<uint32_t>(e));
+        for (int e = tid; e < total; e += ST) staged[e] = topk_key(drow[e] * 0.125f, static_cast<uint32_t>(e * stride));
         __syncthreads();
     } else if (in_smem) {  // one warp per chunk buffer, so the chunks' loads overlap
         for (int c = wid; c < chunks; c += ST / 32) {
@@ -148,7 +149,7 @@ __global__ void __launch_bounds__(ST) select_kernel(int m, int k, int chunks, in
         if (in_smem) {
             for (int e = tid; e < total; e += ST) f(staged[e]);
         } else if (drow) {
-            for (int e = tid; e < total; e += ST) f(topk_key(drow[e] * 0.125f, static_cast<uint32_t>(e)));
+            for (int e = tid; e < total; e += ST) f(topk_key(drow[e] * 0.125f, static_cast<uint32_t>(e * stride)));
         } else {
             for (int c = 0; c < chunks; ++c) {
                 const uint64_t* b = buf_of(c);
@@ -247,7 +248,8 @@ cudaError_t launch_select(const Plan& p, const Work& w, int32_t* expert_idx, cud
     const unsigned grid = static_cast<unsigned>(p.s.BH * p.s.m);
     const ScanLevel& L = p.lev[p.nlev - 1];
     select_kernel<false><<<grid, ST, 0, st>>>(p.s.m, p.s.k, L.chunks, L.cap, w.part, w.cand, w.ccount, w.lv32,
-                                             w.lvbf, expert_idx, nullptr, w.dense, p.s.N, p.dense_ld);
+                                             w.lvbf, expert_idx, nullptr, L.dense ? w.dense : nullptr, p.s.N, L.ld,
+                                             1);
     return cudaGetLastError();
 }
 
@@ -255,7 +257,8 @@ cudaError_t launch_pilot_select(const Plan& p, const Work& w, int level, cudaStr
     const unsigned grid = static_cast<unsigned>(p.s.BH * p.s.m);
     const ScanLevel& L = p.lev[level];
     select_kernel<true><<<grid, ST, 0, st>>>(p.s.m, p.s.k, L.chunks, L.cap, nullptr, w.cand, w.ccount, nullptr,
-                                            nullptr, nullptr, w.theta, nullptr, 0, 0);
+                                            nullptr, nullptr, w.theta, L.dense ? w.dense : nullptr, L.S, L.ld,
+                                            L.stride);
     return cudaGetLastError();
 }
 
