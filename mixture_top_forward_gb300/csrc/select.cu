@@ -132,9 +132,19 @@ __global__ void __launch_bounds__(ST) select_kernel(int m, int k, int chunks, in
         for (int c = 0; c < chunks; ++c) total += count_of(c);
     }
 
-    // all of this landmark's candidates in shared memory when they fit
-    const bool in_smem = (drow || small) && total <= SEL_CAP;
-    if (in_smem && drow) {
+    // all of this landmark's candidates in shared memory when they fit. A
+    // dense pilot row only needs its k-th largest score: its scores go in as
+    // the upper 32 bits of their keys (index bits zero), twice as many fit,
+    // and the k-th largest of those keys is still at or below the true k-th
+    // largest key of the head.
+    uint32_t* staged32 = reinterpret_cast<uint32_t*>(staged);
+    const bool in_smem32 = PILOT && drow && total <= 2 * SEL_CAP;
+    const bool in_smem = !in_smem32 && (drow || small) && total <= SEL_CAP;
+    if (in_smem32) {
+        for (int e = tid; e < total; e += ST)
+            staged32[e] = static_cast<uint32_t>(topk_key(drow[e] * 0.125f, 0xFFFFFFFFu) >> 32);
+        __syncthreads();
+    } else if (in_smem && drow) {
         for (int e = tid; e < total; e += ST) staged[e] = topk_key(drow[e] * 0.125f, static_cast<uint32_t>(e * stride));
         __syncthreads();
     } else if (in_smem) {  // one warp per chunk buffer, so the chunks' loads overlap
@@ -146,7 +156,9 @@ __global__ void __launch_bounds__(ST) select_kernel(int m, int k, int chunks, in
         __syncthreads();
     }
     auto for_each = [&](auto&& f) {
-        if (in_smem) {
+        if (in_smem32) {
+            for (int e = tid; e < total; e += ST) f(static_cast<uint64_t>(staged32[e]) << 32);
+        } else if (in_smem) {
             for (int e = tid; e < total; e += ST) f(staged[e]);
         } else if (drow) {
             for (int e = tid; e < total; e += ST) f(topk_key(drow[e] * 0.125f, static_cast<uint32_t>(e * stride)));
