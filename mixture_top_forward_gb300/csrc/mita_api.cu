@@ -258,9 +258,14 @@ bool make_plan(const Shape& s, Plan* p) {
     P.max_items = (s.N + P.qtile - 1) / P.qtile + s.m;
 
     const size_t BH = static_cast<size_t>(s.BH), m = static_cast<size_t>(s.m);
-    size_t cand = 0, cnts = 0;
+    size_t cand = 0, cnts = 0, recs = 0;
     for (int l = 0; l < P.nlev; ++l) {
+        // the tensor-core pilot scans append 8-column groups as records first
+        // (keys only once a landmark's records are full), as many records as
+        // key slots; the main scan appends keys
+        if (P.scan_tc && !P.lev[l].dense && l + 1 < P.nlev) P.lev[l].rcap = P.lev[l].cap;
         cand = std::max(cand, BH * P.lev[l].chunks * m * static_cast<size_t>(P.lev[l].cap));
+        recs = std::max(recs, BH * P.lev[l].chunks * m * static_cast<size_t>(P.lev[l].rcap));
         cnts = std::max(cnts, BH * P.lev[l].chunks * m);
     }
     size_t off = 0;
@@ -289,6 +294,9 @@ bool make_plan(const Shape& s, Plan* p) {
     for (int l = 0; l < P.nlev; ++l)
         if (P.lev[l].dense) dense_floats = std::max(dense_floats, BH * m * static_cast<size_t>(P.lev[l].ld));
     P.off_dense = take(dense_floats * sizeof(float));
+    P.off_ridx = take(recs * sizeof(uint32_t));
+    P.off_rval = take(recs * 8 * sizeof(float));
+    P.off_rcount = take(recs ? cnts * sizeof(int) : 0);
     P.total = off;
     if (P.max_items * s.BH > 0x7FFFFFFFLL || s.BH * P.nrblocks > 0x7FFFFFFFLL) return false;
     for (int l = 0; l < P.nlev; ++l)
@@ -309,6 +317,9 @@ Work carve(const Plan& p, void* base) {
     w.part = reinterpret_cast<float*>(b + p.off_part);
     w.cand = reinterpret_cast<uint64_t*>(b + p.off_cand);
     w.ccount = reinterpret_cast<int*>(b + p.off_ccount);
+    w.ridx = reinterpret_cast<uint32_t*>(b + p.off_ridx);
+    w.rval = reinterpret_cast<float*>(b + p.off_rval);
+    w.rcount = reinterpret_cast<int*>(b + p.off_rcount);
     w.theta = reinterpret_cast<uint64_t*>(b + p.off_theta);
     w.counts = reinterpret_cast<int*>(b + p.off_counts);
     w.expoff = reinterpret_cast<int*>(b + p.off_expoff);

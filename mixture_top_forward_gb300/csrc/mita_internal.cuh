@@ -32,6 +32,7 @@ struct ScanLevel {
     int64_t chunk_len;  // samples per chunk (last one may be shorter)
     int chunks;         // chunks per head (one CTA each)
     int cap;            // candidate slots per (head, chunk, landmark)
+    int rcap;           // group records per (head, chunk, landmark) (tensor-core scans; 0: none)
     bool dense;         // write every logit ([BH][m][ld] floats) instead of candidates
     int64_t ld;         // row stride of those logits (S rounded up to 4)
 };
@@ -56,7 +57,8 @@ struct Plan {
     int64_t max_items;  // work items per head, upper bound
     // workspace layout (byte offsets)
     size_t off_status, off_lq32, off_lqhi, off_lqlo, off_lv32, off_lvbf, off_part, off_cand, off_ccount, off_theta,
-        off_counts, off_expoff, off_cursor, off_perm, off_items, off_nitems, off_dense, total;
+        off_counts, off_expoff, off_cursor, off_perm, off_items, off_nitems, off_dense, off_ridx, off_rval, off_rcount,
+        total;
 };
 
 // Builds the plan; returns false if a size does not fit the int ranges used.
@@ -73,6 +75,9 @@ struct Work {
     float* part;            // [BH][chunks][m][68]: max, sum, -, -, o[64]
     uint64_t* cand;         // [BH][chunks][m][cap] composite top-k keys
     int* ccount;            // [BH][chunks][m]
+    uint32_t* ridx;         // [BH][chunks][m][rcap] group records: sample index of the group's first key
+    float* rval;            // [BH][chunks][m][rcap][8] group records: the group's 8 raw logits
+    int* rcount;            // [BH][chunks][m]
     uint64_t* theta;        // [BH][m] top-k thresholds from the pilot scans
     float* dense;           // [BH][m][dense_ld] raw logits <Lq_i, K_j> (dense top-k only)
     int* counts;            // [BH][m] queries routed to each expert

@@ -57,13 +57,16 @@ struct ScanArgs {
     float* part;            // [BH][chunks][m][68], full scans only
     uint64_t* cand;         // [BH][chunks][m][cap]
     int* ccount;            // [BH][chunks][m]
+    uint32_t* ridx;         // [BH][chunks][m][rcap] group records: sample index of column 0 of the group
+    float* rval;            // [BH][chunks][m][rcap][8] group records: the group's raw logits
+    int* rcount;            // [BH][chunks][m]
     float* dense;           // dense top-k: [BH][m][ld] raw logits, else null
     int64_t ld;             // row stride of dense
     int* status;
     int64_t S;          // keys (samples) per head in this scan
     int64_t stride;     // key index of sample s is s * stride
     int64_t chunk_len;  // multiple of 128
-    int chunks, cap, m, k;
+    int chunks, cap, rcap, m, k;
 };
 
 template <bool FULL, int NL>
@@ -235,6 +238,9 @@ __global__ void __launch_bounds__(Cfg<FULL, NL>::NT, 1)
         const uint32_t tO = tb + L * 256 + 128;
         const int64_t slot = (bh * a.chunks + c) * a.m + (row_ok ? li : 0);
         uint64_t* buf = a.cand + slot * static_cast<int64_t>(a.cap);
+        uint32_t* rix = a.ridx + slot * static_cast<int64_t>(a.rcap);
+        float4* rvl = reinterpret_cast<float4*>(a.rval) + slot * static_cast<int64_t>(a.rcap) * 2;
+        int rc = 0;  // records so far
         uint64_t theta = (a.theta && row_ok) ? a.theta[bh * a.m + li] : 0;
         float theta_s = key_score(theta);
         int cnt = 0;
@@ -305,13 +311,22 @@ __global__ void __launch_bounds__(Cfg<FULL, NL>::NT, 1)
             // threshold is still -inf (every finite score passes -FLT_MAX)
             const float thr = fmaxf(theta_s * 8.0f, -3.402823466e38f);
             if (row_ok && bmax >= thr) {
-                // a lane entering a group stashes the group's 8 scores in its own
+                // A group whose maximum reaches the threshold goes out whole as
+                // a record (its first sample index and its 8 raw logits; the
+                // select keeps the ones at or above the threshold). Once the
+                // landmark's records are full, its keys go one by one: a lane
+                // entering a group stashes the group's 8 scores in its own
                 // 32-byte slot of the warp's scratch (the compaction histogram,
-                // idle here), so each hit is one shared-memory load
+                // idle here), so each hit is one shared-memory load.
                 float* slot = reinterpret_cast<float*>(hist) + lane * 8;
 #pragma unroll
                 for (int g = 0; g < KT / 8; ++g) {
-                    if (gm[g] >= thr) {
+                    if (!FULL && gm[g] >= thr && rc < a.rcap) {  // (pilot scans only)
+                        rix[rc] = static_cast<uint32_t>(col0 + 8 * g);
+                        rvl[2 * rc] = make_float4(s[8 * g], s[8 * g + 1], s[8 * g + 2], s[8 * g + 3]);
+                        rvl[2 * rc + 1] = make_float4(s[8 * g + 4], s[8 * g + 5], s[8 * g + 6], s[8 * g + 7]);
+                        ++rc;
+                    } else if (gm[g] >= thr) {
                         reinterpret_cast<float4*>(slot)[0] =
                             make_float4(s[8 * g], s[8 * g + 1], s[8 * g + 2], s[8 * g + 3]);
                         reinterpret_cast<float4*>(slot)[1] =
@@ -409,6 +424,7 @@ __global__ void __launch_bounds__(Cfg<FULL, NL>::NT, 1)
             }
         }
         if (row_ok && !a.dense) a.ccount[slot] = cnt;
+        if (!FULL && row_ok && a.rcap > 0) a.rcount[slot] = rc;
     }
     tc_fence_before();
     __syncthreads();
@@ -459,6 +475,10 @@ cudaError_t launch_scan_tc(const Plan& p, const Work& w, const __nv_bfloat16* K,
     a.chunk_len = L.chunk_len;
     a.chunks = L.chunks;
     a.cap = L.cap;
+    a.rcap = L.rcap;
+    a.ridx = w.ridx;
+    a.rval = w.rval;
+    a.rcount = w.rcount;
     a.m = p.s.m;
     a.k = p.s.k;
     const bool two = p.s.m > 128;

@@ -34,7 +34,9 @@ __global__ void __launch_bounds__(ST) select_kernel(int m, int k, int chunks, in
                                                     __nv_bfloat16* __restrict__ lvbf,
                                                     int32_t* __restrict__ expert_idx, uint64_t* __restrict__ theta,
                                                     const float* __restrict__ dense, int64_t N, int64_t ld,
-                                                    int64_t stride) {
+                                                    int64_t stride, const uint32_t* __restrict__ ridx,
+                                                    const float* __restrict__ rval, const int* __restrict__ rcount,
+                                                    int rcap, const uint64_t* __restrict__ thr_in) {
     __shared__ unsigned hist[256];
     __shared__ int offs[ST + 1];        // chunk offsets into staged[] (chunks <= ST)
     __shared__ float red[ST / 32 + 1];  // block reductions
@@ -43,6 +45,7 @@ __global__ void __launch_bounds__(ST) select_kernel(int m, int k, int chunks, in
     __shared__ uint64_t staged[SEL_CAP];
     __shared__ int sel[MITA_SORT_MAX];
     __shared__ int nsel;
+    __shared__ int nst;  // keys staged (records expanded); counts past SEL_CAP too
     __shared__ int s_digit;
     __shared__ unsigned s_above;
 
@@ -107,6 +110,25 @@ __global__ void __launch_bounds__(ST) select_kernel(int m, int k, int chunks, in
     auto count_of = [&](int c) { return ccount[(bh * chunks + c) * m + i]; };
     // dense top-k: the landmark's whole row of logits, as order keys
     const float* drow = dense ? dense + (bh * m + i) * ld : nullptr;
+    // group records (tensor-core scans): each record's logits at or above the
+    // landmark's threshold key become keys, as the scan's own key appends
+    // would have made them (non-finite logits are masked columns: dropped)
+    const uint64_t thr_key = thr_in ? thr_in[bh * m + i] : 0;
+    auto recs_of = [&](int c) { return rcap > 0 ? rcount[(bh * chunks + c) * m + i] : 0; };
+    auto rec_keys = [&](int c, int r, auto&& f) {
+        const int64_t at = ((bh * chunks + c) * m + i) * static_cast<int64_t>(rcap) + r;
+        const uint32_t b0 = ridx[at];
+        const float4 v0 = reinterpret_cast<const float4*>(rval)[2 * at];
+        const float4 v1 = reinterpret_cast<const float4*>(rval)[2 * at + 1];
+        const float sc[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            if (sc[j] >= -3.402823466e38f && sc[j] <= 3.402823466e38f) {
+                const uint64_t key = topk_key(sc[j] * 0.125f, static_cast<uint32_t>((b0 + j) * stride));
+                if (key >= thr_key) f(key);
+            }
+        }
+    };
     int total = 0;
     if (drow) {
         total = static_cast<int>(N);
@@ -126,10 +148,39 @@ __global__ void __launch_bounds__(ST) select_kernel(int m, int k, int chunks, in
         for (int w = 0; w < wid; ++w) base += __float_as_int(red[w]);
         offs[tid] = base + incl - n;
         if (tid == ST - 1) offs[ST] = base + incl;
+        if (tid == 0) nst = 0;
         __syncthreads();
         total = offs[ST];
+        // the records' keys go after the plain keys (one warp per chunk);
+        // the count stays exact past SEL_CAP
+        if (rcap > 0) {
+            if (tid == 0) nst = total;
+            __syncthreads();
+            for (int c = wid; c < chunks; c += ST / 32) {
+                const int nr = recs_of(c);
+                for (int r = lane; r < nr; r += 32)
+                    rec_keys(c, r, [&](uint64_t key) {
+                        const int pos = atomicAdd(&nst, 1);
+                        if (pos < SEL_CAP) staged[pos] = key;
+                    });
+            }
+            __syncthreads();
+            total = nst;
+        }
     } else {
         for (int c = 0; c < chunks; ++c) total += count_of(c);
+        if (rcap > 0) {  // count the records' keys
+            int mine = 0;
+            for (int c = 0; c < chunks; ++c)
+                for (int r = tid; r < recs_of(c); r += ST) rec_keys(c, r, [&](uint64_t) { ++mine; });
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) mine += __shfl_xor_sync(0xffffffffu, mine, o);
+            __syncthreads();
+            if (lane == 0) red[wid] = __int_as_float(mine);
+            __syncthreads();
+            for (int w = 0; w < ST / 32; ++w) total += __float_as_int(red[w]);
+            __syncthreads();
+        }
     }
 
     // all of this landmark's candidates in shared memory when they fit. A
@@ -148,6 +199,7 @@ __global__ void __launch_bounds__(ST) select_kernel(int m, int k, int chunks, in
         for (int e = tid; e < total; e += ST) staged[e] = topk_key(drow[e] * 0.125f, static_cast<uint32_t>(e * stride));
         __syncthreads();
     } else if (in_smem) {  // one warp per chunk buffer, so the chunks' loads overlap
+        // (the records' keys are already in place after the plain keys)
         for (int c = wid; c < chunks; c += ST / 32) {
             const uint64_t* b = buf_of(c);
             const int o = offs[c], n = offs[c + 1] - o;
@@ -167,6 +219,8 @@ __global__ void __launch_bounds__(ST) select_kernel(int m, int k, int chunks, in
                 const uint64_t* b = buf_of(c);
                 const int n = count_of(c);
                 for (int e = tid; e < n; e += ST) f(b[e]);
+                const int nr = recs_of(c);
+                for (int r = tid; r < nr; r += ST) rec_keys(c, r, f);
             }
         }
     };
@@ -261,7 +315,7 @@ cudaError_t launch_select(const Plan& p, const Work& w, int32_t* expert_idx, cud
     const ScanLevel& L = p.lev[p.nlev - 1];
     select_kernel<false><<<grid, ST, 0, st>>>(p.s.m, p.s.k, L.chunks, L.cap, w.part, w.cand, w.ccount, w.lv32,
                                              w.lvbf, expert_idx, nullptr, L.dense ? w.dense : nullptr, p.s.N, L.ld,
-                                             1);
+                                             1, w.ridx, w.rval, w.rcount, L.rcap, p.nlev > 1 ? w.theta : nullptr);
     return cudaGetLastError();
 }
 
@@ -270,7 +324,8 @@ cudaError_t launch_pilot_select(const Plan& p, const Work& w, int level, cudaStr
     const ScanLevel& L = p.lev[level];
     select_kernel<true><<<grid, ST, 0, st>>>(p.s.m, p.s.k, L.chunks, L.cap, nullptr, w.cand, w.ccount, nullptr,
                                             nullptr, nullptr, w.theta, L.dense ? w.dense : nullptr, L.S, L.ld,
-                                            L.stride);
+                                            L.stride, w.ridx, w.rval, w.rcount, L.rcap,
+                                            level > 0 ? w.theta : nullptr);
     return cudaGetLastError();
 }
 
