@@ -175,3 +175,21 @@ def test_pilot_blind_spot_forces_compaction(orc):
     v = synth.normal_bf16((B, H, N, 64), 41, 2)
     rep = parity.full_parity(orc, q, kk_, v, 0, 0, m, k)
     print(rep)
+
+
+def test_pilot_records_overflow_to_keys(orc):
+    """Keys at indices 8, 16, 24 (mod 32) outscore the rest. At N = 65536 the
+    first pilot level samples every 32nd key and sees only weak ones, so the
+    second level (every 8th key) finds three quarters of its samples above
+    that threshold: its group records fill, the rest go out as keys and
+    compact, and the result must still be exact."""
+    B, H, N, m, k = 1, 1, 65536, 4, 64
+    noise = synth.bf16_to_f64(synth.normal_bf16((B, H, N, 64), 43, 0))
+    q = synth.f64_to_bf16(1.0 + 0.1 * noise)
+    idx = np.arange(N) % 32
+    sign = np.where((idx == 8) | (idx == 16) | (idx == 24), 1.0, -1.0)[None, None, :, None]
+    kn = synth.bf16_to_f64(synth.normal_bf16((B, H, N, 64), 43, 1))
+    kk_ = synth.f64_to_bf16(0.5 * sign + 0.05 * kn)
+    v = synth.normal_bf16((B, H, N, 64), 43, 2)
+    rep = parity.full_parity(orc, q, kk_, v, 0, 0, m, k)
+    print(rep)
