@@ -79,8 +79,9 @@ __device__ __forceinline__ uint64_t warp_kth_largest(const uint64_t* buf, int cn
 }
 
 // Keeps the k largest keys of buf[0..cnt) (cnt >= k) in buf[0..k), in place.
-// Returns the k-th largest key, the buffer's new threshold.
-__device__ __forceinline__ uint64_t warp_compact_topk(uint64_t* buf, int cnt, int k, unsigned* hist) {
+// Returns the k-th largest key, the buffer's new threshold. Not inlined: it runs
+// rarely, and inlined it would add its registers to its callers' hot loops.
+static __device__ __noinline__ uint64_t warp_compact_topk(uint64_t* buf, int cnt, int k, unsigned* hist) {
     const int lane = threadIdx.x & 31;
     const uint64_t kth = warp_kth_largest(buf, cnt, k, hist);
     int out = 0;
