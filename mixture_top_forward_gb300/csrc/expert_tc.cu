@@ -430,17 +430,7 @@ __global__ void __launch_bounds__(NT, 1)
                     if (!ok) break;
                 }
                 tc_fence_after();
-                if (rescale) {
-                    float o[16];
-#pragma unroll
-                    for (int h = 0; h < 4; ++h) {
-                        tmem_ld16(tO + h * 16, o);
-                        tmem_ld_wait();
-#pragma unroll
-                        for (int c = 0; c < 16; ++c) o[c] *= alpha;
-                        tmem_st16(tO + h * 16, o);
-                    }
-                }
+                if (rescale) tmem_scale64(tO, alpha);
                 tmem_st32u(tP, pk);
                 tmem_st_wait();
                 tc_fence_before();

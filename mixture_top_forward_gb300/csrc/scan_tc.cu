@@ -377,18 +377,7 @@ __global__ void __launch_bounds__(Cfg<FULL, NL>::NT, 1)
                     if (!ok) break;
                 }
                 tc_fence_after();
-                if (rescale) {
-                    float o[32];
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        tmem_ld32(tO + lane_off + h * 32, o);
-                        tmem_ld_wait();
-#pragma unroll
-                        for (int q = 0; q < 32; ++q) o[q] *= alpha;
-                        tmem_st32(tO + lane_off + h * 32, o);
-                    }
-                    tmem_st_wait();
-                }
+                if (rescale) tmem_scale64(tO + lane_off, alpha);
                 uint32_t pk[KT / 2];
 #pragma unroll
                 for (int q = 0; q < KT / 2; ++q) {

@@ -238,6 +238,24 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
     return d;
 }
 
+// Multiplies 64 consecutive fp32 TMEM columns of this warp's lanes by a
+// per-lane factor (rescaling an online-softmax accumulator). Not inlined:
+// callers take it rarely, and inlined its registers would count in their
+// hot loops.
+static __device__ __noinline__ void tmem_scale64(uint32_t taddr, float f) {
+    float o[16];
+#pragma unroll 1
+    for (int h = 0; h < 4; ++h) {
+        tmem_ld16(taddr + h * 16, o);
+        tmem_ld_wait();
+#pragma unroll
+        for (int c = 0; c < 16; ++c) o[c] *= f;
+        tmem_st16(taddr + h * 16, o);
+    }
+    tmem_st_wait();
+}
+
+
 // Instruction descriptor: D fp32, A and B bf16, dense, M x N tile.
 // b_mn_major: B is MN-major (its N index is the contiguous one).
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool b_mn_major) {
