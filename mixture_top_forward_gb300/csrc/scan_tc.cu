@@ -23,12 +23,17 @@
 //                  keep the tensor pipe busy);
 //   warps NL+2..:  one warpgroup (4 consecutive warps: warp w reads TMEM lane
 //                  quarter w % 4) per landmark tile, one thread per landmark.
-//                  A thread loads its 128 scores, offers them to its
-//                  landmark's candidate buffer (topk.cuh: append when the
-//                  64-bit order key reaches the threshold, warp-cooperative
-//                  compaction on overflow) and, in full scans, runs the online
-//                  softmax (lazy running max), writes P (bf16) into TMEM and leaves a
-//                  (max, sum, o[64]) partial at the end of the chunk.
+//                  Per 64-key tile a thread loads its 64 scores and offers
+//                  them to its landmark's candidate buffers: an 8-column
+//                  group whose maximum reaches the threshold goes out whole
+//                  as a record in pilot scans (the select expands it), and
+//                  key by key otherwise, or once the records are full
+//                  (topk.cuh: append when the 64-bit order key reaches the
+//                  threshold, warp-cooperative compaction on overflow); in
+//                  full scans it also runs the online softmax (lazy running
+//                  max), writes P (bf16) into TMEM and leaves a (max, sum,
+//                  o[64]) partial at the end of the chunk. Dense levels
+//                  write every raw logit instead of candidates.
 // Keys are read through a 3-D tensor map (row, head) whose row stride may be
 // > 1: a pilot scan reads every stride-th key of each head. A pilot does only
 // the top-k part; its k-th best order key (select.cu) is a lower bound of the
