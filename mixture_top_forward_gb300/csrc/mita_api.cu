@@ -167,12 +167,17 @@ ScanLevel scan_level(const Shape& s, int64_t S, int64_t stride, int64_t prevS, i
     // room for k plus one 128-key tile).
     const int64_t room = round_up(std::min(L.chunk_len, S), 32);
     int64_t cap = room;
+    // group records (pilot scans) overflow into the key buffer, so they need
+    // room for the expected groups only: each holds at least one survivor
+    int64_t rcap = cdiv(room, 8);
     if (prevS > 0) {
         const int64_t expect = cdiv(static_cast<int64_t>(s.k) * L.chunk_len, prevS);
         cap = std::max<int64_t>(round_up(expect + expect / 2 + 64, 32), s.k + 128);
         cap = std::min(cap, room);
+        rcap = std::min(round_up(expect + expect / 2 + 64, 32), cap);
     }
     L.cap = static_cast<int>(cap);
+    L.rcap = static_cast<int>(rcap);  // (kept only for the tensor-core pilot levels: make_plan)
     return L;
 }
 
@@ -261,9 +266,9 @@ bool make_plan(const Shape& s, Plan* p) {
     size_t cand = 0, cnts = 0, recs = 0;
     for (int l = 0; l < P.nlev; ++l) {
         // the tensor-core pilot scans append 8-column groups as records first
-        // (keys only once a landmark's records are full), as many records as
-        // key slots; the main scan appends keys
-        if (P.scan_tc && !P.lev[l].dense && l + 1 < P.nlev) P.lev[l].rcap = P.lev[l].cap;
+        // (keys only once a landmark's records are full); the main scan and
+        // the CUDA-core scan append keys
+        if (!(P.scan_tc && !P.lev[l].dense && l + 1 < P.nlev)) P.lev[l].rcap = 0;
         cand = std::max(cand, BH * P.lev[l].chunks * m * static_cast<size_t>(P.lev[l].cap));
         recs = std::max(recs, BH * P.lev[l].chunks * m * static_cast<size_t>(P.lev[l].rcap));
         cnts = std::max(cnts, BH * P.lev[l].chunks * m);
