@@ -46,8 +46,8 @@ def _bind(path: str):
     lib.oracle_scores.argtypes = [vp, vp, i64, i64, ci, ci, i64, ci, vp]
     lib.oracle_scan.argtypes = [vp, vp, vp, i64, i64, ci, ci, ci, vp, i64, vp, vp, vp]
     lib.oracle_route.argtypes = [vp, vp, i64, i64, ci, ci, vp, i64, vp, vp]
-    lib.oracle_attend.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i64, ci, ci, ci, vp, i64, vp, vp]
-    lib.oracle_forward.argtypes = [vp, vp, vp, i64, i64, i64, ci, ci, ci, ci, ci] + [vp] * 8
+    lib.oracle_attend.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i64, ci, ci, ci, vp, i64, ci, vp, vp]
+    lib.oracle_forward.argtypes = [vp, vp, vp, i64, i64, i64, ci, ci, ci, ci, ci, ci] + [vp] * 8
     return lib
 
 
@@ -145,10 +145,11 @@ class Oracle:
         _check(self.lib.oracle_route(_p(q), _p(lq), BH, N, d, m, _p(which), n, _p(r), _p(g)), "route")
         return r, g
 
-    def attend(self, q, lq, lv, k, v, eidx, route_, which=None):
+    def attend(self, q, lq, lv, k, v, eidx, route_, which=None, shared: bool = True):
         """Query-expert attention conditioned on the given routes and experts.
 
-        Returns (out, wsum) for the queries in `which` (global ids) or all queries.
+        Returns (out, wsum) for the queries in `which` (global ids) or all
+        queries. shared=False: the routing-only ablation (no shared pairs).
         """
         q, k, v = _u16(q), _u16(k), _u16(v)
         *lead, N, d = q.shape
@@ -167,11 +168,12 @@ class Oracle:
         out = np.empty(shp + (d,), np.float64)
         ws = np.empty(shp, np.float64)
         _check(self.lib.oracle_attend(_p(q), _p(lq), _p(lv), _p(k), _p(v), _p(eidx), _p(route_), BH, N, d, m, kk,
-                                     _p(which), n, _p(out), _p(ws)), "attend")
+                                     _p(which), n, int(shared), _p(out), _p(ws)), "attend")
         return out, ws
 
-    def forward(self, q, k, v, grid_h: int, grid_w: int, m: int, kk: int):
-        """Full forward with the oracle's own routes/experts.
+    def forward(self, q, k, v, grid_h: int, grid_w: int, m: int, kk: int, shared: bool = True):
+        """Full forward with the oracle's own routes/experts (shared=False: the
+        routing-only ablation, no shared pairs).
 
         q,k,v: [B,H,N,d] bf16 (uint16). Returns a dict of float64/int32 arrays:
         out [B,H,N,d], expert_idx [B,H,m,kk], route [B,H,N], lq, lv [B,H,m,d],
@@ -182,7 +184,7 @@ class Oracle:
         r = dict(out=np.empty((B, H, N, d)), expert_idx=np.empty((B, H, m, kk), np.int32),
                  route=np.empty((B, H, N), np.int32), lq=np.empty((B, H, m, d)), lv=np.empty((B, H, m, d)),
                  gap=np.empty((B, H, m)), rgap=np.empty((B, H, N)), wsum=np.empty((B, H, N)))
-        _check(self.lib.oracle_forward(_p(q), _p(k), _p(v), B, H, N, d, grid_h, grid_w, m, kk, _p(r["out"]),
+        _check(self.lib.oracle_forward(_p(q), _p(k), _p(v), B, H, N, d, grid_h, grid_w, m, kk, int(shared), _p(r["out"]),
                                       _p(r["expert_idx"]), _p(r["route"]), _p(r["lq"]), _p(r["lv"]), _p(r["gap"]),
                                       _p(r["rgap"]), _p(r["wsum"])), "forward")
         return r

@@ -245,9 +245,12 @@ int oracle_route(const uint16_t* q, const double* lq, int64_t BH, int64_t N, int
 // [BH][m][kk] expert array the output is conditioned on; `lv` is [BH][m][d].
 // out[it][:] is the attention output of query which[it]; wsum[it] the sum of its
 // m+k softmax weights (1 up to rounding). Null `which` means every query.
+// shared = 0 gives the routing-only ablation the pages compare MiTA with
+// ([P2] results section; [P3] Figure 4): no shared pairs, one softmax over
+// the k routed logits alone.
 int oracle_attend(const uint16_t* q, const double* lq, const double* lv, const uint16_t* k, const uint16_t* v,
                   const int32_t* eidx, const int32_t* route, int64_t BH, int64_t N, int d, int m, int kk,
-                  const int64_t* which, int64_t n_which, double* out, double* wsum) {
+                  const int64_t* which, int64_t n_which, int shared, double* out, double* wsum) {
     if (N < 1 || d < 1 || m < 1 || kk < 1 || kk > N) return -1;
     const int64_t n_items = which ? n_which : BH * N;
     const double tau = 1.0 / std::sqrt(static_cast<double>(d));
@@ -262,9 +265,10 @@ int oracle_attend(const uint16_t* q, const double* lq, const double* lv, const u
             continue;
         }
         const int32_t* sel = eidx + (bh * m + e) * static_cast<int64_t>(kk);
-        std::vector<double> qd(d), logit(m + kk);
+        const int ms = shared ? m : 0;  // shared pairs taken
+        std::vector<double> qd(d), logit(ms + kk);
         for (int c = 0; c < d; ++c) qd[c] = widen(q[qi * d + c]);
-        for (int i = 0; i < m; ++i) {
+        for (int i = 0; i < ms; ++i) {
             const double* a = lq + (bh * m + i) * d;
             double t = 0.0;
             for (int c = 0; c < d; ++c) t += qd[c] * a[c];
@@ -273,26 +277,26 @@ int oracle_attend(const uint16_t* q, const double* lq, const double* lv, const u
         for (int j = 0; j < kk; ++j) {
             if (sel[j] < 0 || sel[j] >= N) {
                 bad |= 1;
-                logit[m + j] = 0.0;
+                logit[ms + j] = 0.0;
                 continue;
             }
             const uint16_t* row = k + (bh * N + sel[j]) * d;
             double t = 0.0;
             for (int c = 0; c < d; ++c) t += qd[c] * widen(row[c]);
-            logit[m + j] = tau * t;
+            logit[ms + j] = tau * t;
         }
         double mx = -std::numeric_limits<double>::infinity();
         for (double t : logit) mx = std::max(mx, t);
         std::vector<double> acc(d, 0.0);
         double z = 0.0;
-        for (int i = 0; i < m; ++i) {
+        for (int i = 0; i < ms; ++i) {
             double w = std::exp(logit[i] - mx);
             z += w;
             const double* val = lv + (bh * m + i) * d;
             for (int c = 0; c < d; ++c) acc[c] += w * val[c];
         }
         for (int j = 0; j < kk; ++j) {
-            double w = std::exp(logit[m + j] - mx);
+            double w = std::exp(logit[ms + j] - mx);
             z += w;
             int64_t jj = (sel[j] >= 0 && sel[j] < N) ? sel[j] : 0;
             const uint16_t* row = v + (bh * N + jj) * d;
@@ -311,10 +315,10 @@ int oracle_attend(const uint16_t* q, const double* lq, const double* lv, const u
 // The whole forward pass, stages 1-4 in order, with the oracle's own routes
 // and experts. Buffers: out [BH][N][d], eidx [BH][m][kk], route [BH][N],
 // lq/lv [BH][m][d], gap [BH][m], rgap [BH][N], wsum [BH][N]; the last five
-// may be null.
+// may be null. shared = 0: the routing-only ablation (see oracle_attend).
 int oracle_forward(const uint16_t* q, const uint16_t* k, const uint16_t* v, int64_t B, int64_t H, int64_t N, int d,
-                   int gh, int gw, int m, int kk, double* out, int32_t* eidx, int32_t* route, double* lq_out,
-                   double* lv_out, double* gap, double* rgap, double* wsum) {
+                   int gh, int gw, int m, int kk, int shared, double* out, int32_t* eidx, int32_t* route,
+                   double* lq_out, double* lv_out, double* gap, double* rgap, double* wsum) {
     if (B < 0 || H < 0) return -1;
     const int64_t BH = B * H;
     if (BH == 0) return 0;
@@ -325,7 +329,7 @@ int oracle_forward(const uint16_t* q, const uint16_t* k, const uint16_t* v, int6
     if (oracle_landmarks(q, BH, N, d, gh, gw, m, L)) return -1;
     if (oracle_scan(L, k, v, BH, N, d, m, kk, nullptr, 0, LV, eidx, gap)) return -1;
     if (oracle_route(q, L, BH, N, d, m, nullptr, 0, route, rgap)) return -1;
-    return oracle_attend(q, L, LV, k, v, eidx, route, BH, N, d, m, kk, nullptr, 0, out, wsum);
+    return oracle_attend(q, L, LV, k, v, eidx, route, BH, N, d, m, kk, nullptr, 0, shared, out, wsum);
 }
 
 }  // extern "C"

@@ -176,6 +176,31 @@ def pin_attention_k_equals_n(o):
     assert np.max(np.abs(out2 - r["out"].reshape(2, N, 64))) < 1e-12
 
 
+def pin_routing_only(o):
+    """The routing-only ablation (no shared pairs): with k = N every query
+    attends to all keys, so the output is plain softmax attention over K, V
+    (whatever the routes); with k < N it is softmax attention over the routed
+    expert's keys alone, and its weights sum to 1."""
+    N, m = 60, 4
+    q, k, v = _rand((1, 2, N, 64), 23, 0, 2.0), _rand((1, 2, N, 64), 23, 1), _rand((1, 2, N, 64), 23, 2)
+    r = o.forward(q, k, v, 0, 0, m, N, shared=False)
+    Q, K, V = _f64(q)[0], _f64(k)[0], _f64(v)[0]
+    for h in range(2):
+        w = softmax(Q[h] @ K[h].T / 8.0, axis=-1)
+        assert np.max(np.abs(r["out"][0, h] - w @ V[h])) < 1e-12
+    assert np.max(np.abs(r["wsum"] - 1.0)) < 1e-12
+    kk = 7
+    r = o.forward(q, k, v, 0, 0, m, kk, shared=False)
+    for h in range(2):
+        for n in (0, 17, 59):
+            sel = r["expert_idx"][0, h, r["route"][0, h, n]]
+            w = softmax(Q[h, n] @ K[h, sel].T / 8.0)
+            assert np.max(np.abs(r["out"][0, h, n] - w @ V[h, sel])) < 1e-12
+    # the shared branch does change the result
+    full = o.forward(q, k, v, 0, 0, m, kk)
+    assert np.max(np.abs(full["out"] - r["out"])) > 1e-3
+
+
 def pin_weights_sum_to_one(o):
     q, k, v = synth.make_inputs("tiny")
     r = o.forward(q, k, v, 14, 14, 25, 25)
@@ -239,6 +264,7 @@ def pin_hand_example(o):
 
 
 ALL_PINS = [
+    pin_routing_only,
     pin_window_tables,
     pin_landmarks_adaptive_pool,
     pin_landmarks_special,

@@ -30,7 +30,8 @@ MUTANTS = [
     ("shared branch dropped", "double w = std::exp(logit[i] - mx);", "double w = 0.0 * std::exp(logit[i] - mx);"),
     ("shared values are Lq", "const double* val = lv + (bh * m + i) * d;", "const double* val = lq + (bh * m + i) * d;"),
     ("expert of landmark 0", "eidx + (bh * m + e) * static_cast<int64_t>(kk);", "eidx + (bh * m + 0) * static_cast<int64_t>(kk);"),
-    ("attend drops tau on routed logits", "logit[m + j] = tau * t;", "logit[m + j] = t;"),
+    ("attend drops tau on routed logits", "logit[ms + j] = tau * t;", "logit[ms + j] = t;"),
+    ("routing-only keeps the shared pairs", "const int ms = shared ? m : 0;", "const int ms = m;"),
 ]
 
 
