@@ -58,9 +58,19 @@ def describe(name):
 # Whole pass: FLOPs = B*H*(4 m N d + 4 N (m+k) d); bytes = B*H*(3 N d + N d)*2
 # + B*H*m*k*2*d*2 (Q,K,V read once, gathered expert rows, output written).
 # ---------------------------------------------------------------------------
-def work(c):
+def work(c, shared=True):
+    """shared=False: the routing-only ablation, whose scan forms only the
+    logits (no shared-expert values) and whose experts hold k keys alone."""
     BH, N, d, m, k = c["B"] * c["H"], c["N"], 64, c["m"], c["k"]
     row = N * d * 2
+    if not shared:
+        return {
+            "total": {"flops": BH * (2 * m * N * d + 4 * N * k * d), "bytes": BH * (4 * row + m * k * 2 * d * 2)},
+            "pool": {"flops": 0, "bytes": BH * row},
+            "scan": {"flops": BH * 2 * m * N * d, "bytes": BH * row},
+            "route": {"flops": BH * 2 * N * m * d, "bytes": BH * row},
+            "expert": {"flops": BH * 4 * N * k * d, "bytes": BH * (2 * row + m * k * 2 * d * 2)},
+        }
     return {
         "total": {"flops": BH * (4 * m * N * d + 4 * N * (m + k) * d),
                   "bytes": BH * (4 * row + m * k * 2 * d * 2)},
@@ -331,6 +341,7 @@ def run_gpu(args, rank, world):
             res["e2e"] = e
     if rank == 0 and not args.no_sweep:
         res["sweep"] = sweep(args, M, dev, stream, peaks)
+        res["routed_only"] = routed_only(args, M, dev, stream, peaks)
     if rank == 0 and not args.no_cpu and world == 1:
         res["cpu_baseline"] = cpu_baseline(name, q, k, v)
     return res
@@ -395,6 +406,50 @@ def sweep(args, M, dev, stream, peaks):
         del Q, K, V, out
         torch.cuda.empty_cache()
     return res
+
+
+def routed_only(args, M, dev, stream, peaks):
+    """The routing-only ablation on the timed workload at the same budget:
+    no shared pairs, each expert holds k' = m + k keys. Device-resident
+    inputs, per-stage times from the library's stage profile."""
+    import torch
+
+    c = dict(synth.CONFIGS[args.config])
+    q, k, v = synth.make_inputs(c)
+    c["k"] = min(c["m"] + c["k"], c["N"])
+    to = lambda a: torch.from_numpy(a.view(np.int16)).to(dev).view(torch.bfloat16)
+    Q, K, V = to(q), to(k), to(v)
+    out = torch.empty_like(Q)
+    e = torch.empty((c["B"], c["H"], c["m"], c["k"]), dtype=torch.int32, device=dev)
+    r = torch.empty((c["B"], c["H"], c["N"]), dtype=torch.int32, device=dev)
+    a = (c["grid_h"], c["grid_w"], c["m"], c["k"])
+    for _ in range(3):
+        M.mita_forward_routed(Q, K, V, *a, out=out, expert_idx=e, route=r, stream=stream)
+    torch.cuda.synchronize()
+    assert M.mita_sync_status(stream) == 0, M.mita_last_error()
+    M.mita_profile_read(stream)
+    M.mita_profile_enable(True)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    n = 10
+    ev0.record(stream)
+    for _ in range(n):
+        M.mita_forward_routed(Q, K, V, *a, out=out, expert_idx=e, route=r, stream=stream)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    M.mita_profile_enable(False)
+    stages = M.mita_profile_read(stream)
+    assert M.mita_sync_status(stream) == 0, M.mita_last_error()
+    ms = ev0.elapsed_time(ev1) / n
+    w = work(c, shared=False)
+    stage_ms = {s: stages[s][0] / n for s in STAGES}
+    t_exp = stage_ms["expert"] / 1e3
+    del Q, K, V, out
+    torch.cuda.empty_cache()
+    exp_tf = w["expert"]["flops"] / t_exp / 1e12 if t_exp > 0 else None
+    return {"k_routed": c["k"], "queries_per_s": c["B"] * c["H"] * c["N"] / (ms / 1e3), "ms_per_step": ms,
+            "roofline_frac": roofline_time(w["total"], peaks, sustained=True) / (ms / 1e3),
+            "expert_tflops": exp_tf, "expert_frac": exp_tf / peaks["bf16_tflops_sustained"] if exp_tf else None,
+            "stage_ms": stage_ms}
 
 
 # ---------------------------------------------------------------------------

@@ -78,6 +78,19 @@ int mita_forward(const void* Q, const void* K, const void* V, int B, int H, int 
                  int m, int k, void* out, int32_t* expert_idx, int32_t* route, void* stream);
 
 /*
+ * The routing-only ablation of MiTA ("NeurIPS 2026 | Mixture-of-Top-k 注意力"
+ * (shuwu5.cn), results section, and Figure 4 of "And attention is also FFN?
+ * …" (en.roboind.com): routed experts alone, without the shared branch).
+ * Stages 1-3 as in mita_forward (landmarks, top-k experts, routing); in
+ * stage 4 each query attends only to the k pairs (K_j, V_j) of its routed
+ * expert, under one softmax over those k logits. The pages compare it with
+ * MiTA at k' = m + k routed pairs: pass that k'. Arguments, layouts, errors
+ * and asynchrony as for mita_forward.
+ */
+int mita_forward_routed(const void* Q, const void* K, const void* V, int B, int H, int N, int d, int grid_h,
+                        int grid_w, int m, int k, void* out, int32_t* expert_idx, int32_t* route, void* stream);
+
+/*
  * mita_forward with two optional extra device outputs (either may be NULL):
  * lq, float32 [B][H][m][d], the landmark queries of stage 1, and lv,
  * float32 [B][H][m][d], the shared-expert values LV of stage 2.

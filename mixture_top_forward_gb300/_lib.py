@@ -55,6 +55,8 @@ def load(path: str | None = None, build_if_missing: bool = True) -> ctypes.CDLL:
                                     ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_uint16))
         lib.mita_forward.argtypes = [vp, vp, vp] + [ci] * 8 + [vp, vp, vp, vp]
         lib.mita_forward.restype = ci
+        lib.mita_forward_routed.argtypes = [vp, vp, vp] + [ci] * 8 + [vp, vp, vp, vp]
+        lib.mita_forward_routed.restype = ci
         lib.mita_forward_aux.argtypes = [vp, vp, vp] + [ci] * 8 + [vp, vp, vp, vp, vp, vp]
         lib.mita_forward_aux.restype = ci
         lib.mita_forward_noalloc.argtypes = [vp, vp, vp] + [ci] * 8 + [vp, vp, vp, vp]
@@ -113,7 +115,7 @@ def _shape(Q, m, k, grid_h, grid_w):
 
 
 def mita_forward(Q, K, V, grid_h: int, grid_w: int, m: int, k: int, out=None, expert_idx=None, route=None,
-                 stream=None):
+                 stream=None, _entry="mita_forward"):
     """MiTA forward on device tensors (torch, bf16 [B,H,N,d]).
 
     Returns (out bf16 [B,H,N,d], expert_idx int32 [B,H,m,k], route int32
@@ -128,12 +130,21 @@ def mita_forward(Q, K, V, grid_h: int, grid_w: int, m: int, k: int, out=None, ex
     out = torch.empty_like(Q) if out is None else out
     expert_idx = torch.empty((B, H, m, k), dtype=torch.int32, device=Q.device) if expert_idx is None else expert_idx
     route = torch.empty((B, H, N), dtype=torch.int32, device=Q.device) if route is None else route
-    rc = load().mita_forward(_dev_ptr(Q, "torch.bfloat16", "Q"), _dev_ptr(K, "torch.bfloat16", "K"),
-                             _dev_ptr(V, "torch.bfloat16", "V"), B, H, N, d, grid_h, grid_w, m, k,
-                             _dev_ptr(out, "torch.bfloat16", "out"), _dev_ptr(expert_idx, "torch.int32", "expert_idx"),
-                             _dev_ptr(route, "torch.int32", "route"), _stream(stream))
+    rc = getattr(load(), _entry)(_dev_ptr(Q, "torch.bfloat16", "Q"), _dev_ptr(K, "torch.bfloat16", "K"),
+                                 _dev_ptr(V, "torch.bfloat16", "V"), B, H, N, d, grid_h, grid_w, m, k,
+                                 _dev_ptr(out, "torch.bfloat16", "out"),
+                                 _dev_ptr(expert_idx, "torch.int32", "expert_idx"),
+                                 _dev_ptr(route, "torch.int32", "route"), _stream(stream))
     _raise(rc)
     return out, expert_idx, route
+
+
+def mita_forward_routed(Q, K, V, grid_h: int, grid_w: int, m: int, k: int, out=None, expert_idx=None, route=None,
+                        stream=None):
+    """The routing-only ablation (no shared pairs; each query attends to the
+    k pairs of its routed expert alone), on device tensors; arguments and
+    results as mita_forward."""
+    return mita_forward(Q, K, V, grid_h, grid_w, m, k, out, expert_idx, route, stream, _entry="mita_forward_routed")
 
 
 def mita_forward_noalloc(Q, K, V, grid_h: int, grid_w: int, m: int, k: int, out, expert_idx, route, stream=None):

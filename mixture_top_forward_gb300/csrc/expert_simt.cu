@@ -23,7 +23,7 @@ constexpr int EB = 32;   // keys per staged block
 
 __global__ void __launch_bounds__(ET) expert_simt_kernel(
     const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restrict__ K, const __nv_bfloat16* __restrict__ V,
-    int64_t N, int m, int k, const int4* __restrict__ items, const int* __restrict__ nitems,
+    int64_t N, int m, int ms, int k, const int4* __restrict__ items, const int* __restrict__ nitems,
     const int* __restrict__ perm, const int32_t* __restrict__ expert_idx, const float* __restrict__ lq32,
     const float* __restrict__ lv32, __nv_bfloat16* __restrict__ out) {
     __shared__ __align__(16) float Ks[EB][D];
@@ -45,7 +45,7 @@ __global__ void __launch_bounds__(ET) expert_simt_kernel(
 #pragma unroll
     for (int c = 0; c < D; ++c) o[c] = 0.f;
     float mx = -INFINITY, l = 0.f;
-    const int total = m + k;
+    const int total = ms + k;  // ms = m shared pairs, or 0 (routing-only)
     const int32_t* sel = expert_idx + (bh * m + e) * static_cast<int64_t>(k);
 
     for (int j0 = 0; j0 < total; j0 += EB) {
@@ -55,7 +55,7 @@ __global__ void __launch_bounds__(ET) expert_simt_kernel(
             const int r = t >> 2, c0 = (t & 3) * 16;
             const int j = j0 + r;
             if (r < nb) {
-                if (j < m) {
+                if (j < ms) {
                     const float* kr = lq32 + (bh * m + j) * D + c0;
                     const float* vr = lv32 + (bh * m + j) * D + c0;
 #pragma unroll
@@ -64,7 +64,7 @@ __global__ void __launch_bounds__(ET) expert_simt_kernel(
                         Vs[r][c0 + c] = vr[c];
                     }
                 } else {
-                    const int64_t row = bh * N + sel[j - m];
+                    const int64_t row = bh * N + sel[j - ms];
                     unpack_bf16x8(ldg_nc_v4(K + row * D + c0), &Ks[r][c0]);
                     unpack_bf16x8(ldg_nc_v4(K + row * D + c0 + 8), &Ks[r][c0 + 8]);
                     unpack_bf16x8(ldg_nc_v4(V + row * D + c0), &Vs[r][c0]);
@@ -136,7 +136,8 @@ __global__ void __launch_bounds__(ET) expert_simt_kernel(
 cudaError_t launch_expert_simt(const Plan& p, const Work& w, const __nv_bfloat16* Q, const __nv_bfloat16* K,
                           const __nv_bfloat16* V, const int32_t* expert_idx, __nv_bfloat16* out, cudaStream_t st) {
     const unsigned grid = static_cast<unsigned>(p.s.BH * p.max_items);
-    expert_simt_kernel<<<grid, ET, 0, st>>>(Q, K, V, p.s.N, p.s.m, p.s.k, w.items, w.nitems, w.perm,
+    expert_simt_kernel<<<grid, ET, 0, st>>>(Q, K, V, p.s.N, p.s.m, p.shared ? p.s.m : 0, p.s.k, w.items, w.nitems,
+                                            w.perm,
                                             expert_idx, w.lq32, w.lv32, out);
     return cudaGetLastError();
 }

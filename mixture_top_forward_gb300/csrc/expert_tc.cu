@@ -74,7 +74,7 @@ struct Args {
     __nv_bfloat16* out;
     int* status;
     int64_t N;
-    int m, k, nblk;
+    int m, msh, k, nblk;  // msh: shared pairs taken (m, or 0 for the routing-only ablation)
 };
 
 struct Layout {
@@ -163,9 +163,11 @@ __global__ void __launch_bounds__(NT, 1)
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const Layout S = layout(base, a.nblk);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    // key rows: [0, m) shared, [m, m4) unused, [m4, m4 + k) routed (m4 = m
-    // rounded up to 4, so every 4-row gather starts 512-byte aligned)
-    const int m4 = (a.m + 3) & ~3;
+    // key rows: [0, msh) shared, [msh, m4) unused, [m4, m4 + k) routed (m4 =
+    // msh rounded up to 4, so every 4-row gather starts 512-byte aligned);
+    // msh = m, or 0 in the routing-only ablation (no shared pairs)
+    const int msh = a.msh;
+    const int m4 = (msh + 3) & ~3;
     const int nkeys = m4 + a.k;
 
     if (tid == 0) {
@@ -220,7 +222,7 @@ __global__ void __launch_bounds__(NT, 1)
                 if (!ok) break;
                 const int bh = it[0].w;
                 const int32_t* sel = a.expert_idx + (static_cast<int64_t>(bh) * a.m + it[0].x) * a.k;
-                const int ns = it[0].w != cur_bh ? m4 / 4 : 0;  // shared rows only on a new head
+                const int ns = it[0].w != cur_bh ? m4 / 4 : 0;  // shared rows (if any) only on a new head
                 const int nr = (a.k + 3) / 4;
                 if (lane == 0) mbar_arrive_expect_tx(&kvfull, static_cast<uint32_t>(ns + nr) * 1024u);
                 __syncwarp();
@@ -381,13 +383,13 @@ __global__ void __launch_bounds__(NT, 1)
                 tc_fence_before();
                 warp_arrive(&sfree[w]);
                 const int k0 = j * KB;  // key row of column 0
-                if (k0 + KB > nkeys || (k0 < m4 && k0 + KB > a.m && m4 > a.m)) {
+                if (k0 + KB > nkeys || (k0 < m4 && k0 + KB > msh && m4 > msh)) {
                     // (warp-uniform) the block holds the unused rows [m, m4) or
                     // ends past the key list, where the logits are not keys'
 #pragma unroll
                     for (int c = 0; c < KB; ++c) {
                         const int g = k0 + c;
-                        s[c] = (g >= nkeys || (g >= a.m && g < m4)) ? -INFINITY : s[c];
+                        s[c] = (g >= nkeys || (g >= msh && g < m4)) ? -INFINITY : s[c];
                     }
                 }
                 // 8 independent partial maxima: short dependency chains
@@ -459,7 +461,7 @@ __global__ void __launch_bounds__(NT, 1)
 
 size_t smem_bytes(int nblk) { return 1024 + static_cast<size_t>(nblk) * 16384 + NWG * QB * 16384; }
 
-int key_rows(const Plan& p) { return ((p.s.m + 3) & ~3) + p.s.k; }
+int key_rows(const Plan& p) { return (p.shared ? (p.s.m + 3) & ~3 : 0) + p.s.k; }
 
 }  // namespace
 
@@ -480,6 +482,7 @@ cudaError_t launch_expert_tc(const Plan& p, const Work& w, const __nv_bfloat16* 
     a.status = w.status;
     a.N = p.s.N;
     a.m = p.s.m;
+    a.msh = p.shared ? p.s.m : 0;
     a.k = p.s.k;
     a.nblk = (key_rows(p) + KB - 1) / KB;
     CUtensorMap tq, tk, tv, tlq, tlv;

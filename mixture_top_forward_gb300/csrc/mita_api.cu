@@ -183,9 +183,10 @@ ScanLevel scan_level(const Shape& s, int64_t S, int64_t stride, int64_t prevS, i
 
 }  // namespace
 
-bool make_plan(const Shape& s, Plan* p) {
+bool make_plan(const Shape& s, Plan* p, bool shared) {
     Plan P{};
     P.s = s;
+    P.shared = shared;
     const int sms = device_sms();
     P.scan_tc = s.m <= 256;
     if (P.scan_tc) {
@@ -432,9 +433,13 @@ int run_forward(const Plan& P, const Work& W, const __nv_bfloat16* Q, const __nv
 
 using namespace mita;
 
-extern "C" int mita_forward_aux(const void* Q, const void* K, const void* V, int B, int H, int N, int d, int grid_h,
-                                int grid_w, int m, int k, void* out, int32_t* expert_idx, int32_t* route, float* lq,
-                                float* lv, void* stream) {
+namespace {
+
+// The device-buffer entry points: MiTA (shared = true) or its routing-only
+// ablation.
+int forward_device(const void* Q, const void* K, const void* V, int B, int H, int N, int d, int grid_h, int grid_w,
+                   int m, int k, void* out, int32_t* expert_idx, int32_t* route, float* lq, float* lv, void* stream,
+                   bool shared) {
     g_err[0] = 0;
     Shape s;
     bool empty;
@@ -445,7 +450,7 @@ extern "C" int mita_forward_aux(const void* Q, const void* K, const void* V, int
     if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(out))
         return fail(MITA_ERR_INVALID_ARG, "Q, K, V and out must be 16-byte aligned");
     Plan P;
-    if (!make_plan(s, &P)) return fail(MITA_ERR_UNSUPPORTED, "problem too large for the launch grids");
+    if (!make_plan(s, &P, shared)) return fail(MITA_ERR_UNSUPPORTED, "problem too large for the launch grids");
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     void* base = nullptr;
     if ((rc = workspace(st, 0, P.total, &base)) != MITA_OK) return rc;
@@ -453,6 +458,21 @@ extern "C" int mita_forward_aux(const void* Q, const void* K, const void* V, int
     return run_forward(P, W, static_cast<const __nv_bfloat16*>(Q), static_cast<const __nv_bfloat16*>(K),
                        static_cast<const __nv_bfloat16*>(V), static_cast<__nv_bfloat16*>(out), expert_idx, route, lq,
                        lv, st);
+}
+
+}  // namespace
+
+extern "C" int mita_forward_aux(const void* Q, const void* K, const void* V, int B, int H, int N, int d, int grid_h,
+                                int grid_w, int m, int k, void* out, int32_t* expert_idx, int32_t* route, float* lq,
+                                float* lv, void* stream) {
+    return forward_device(Q, K, V, B, H, N, d, grid_h, grid_w, m, k, out, expert_idx, route, lq, lv, stream, true);
+}
+
+extern "C" int mita_forward_routed(const void* Q, const void* K, const void* V, int B, int H, int N, int d, int grid_h,
+                                   int grid_w, int m, int k, void* out, int32_t* expert_idx, int32_t* route,
+                                   void* stream) {
+    return forward_device(Q, K, V, B, H, N, d, grid_h, grid_w, m, k, out, expert_idx, route, nullptr, nullptr, stream,
+                          false);
 }
 
 extern "C" int mita_forward(const void* Q, const void* K, const void* V, int B, int H, int N, int d, int grid_h,

@@ -42,6 +42,9 @@ struct Plan {
     // landmark scan: pilot levels on strided samples, then the main scan
     // (lev[nlev-1], stride 1); scan_tc selects the tensor-core kernels
     bool scan_tc;
+    // false: the routing-only ablation (no shared pairs in the attention; the
+    // main scan then computes no LV)
+    bool shared;
     int nlev;
     ScanLevel lev[4];
     // dense top-k: when no sample threshold could keep the main scan's
@@ -62,7 +65,7 @@ struct Plan {
 };
 
 // Builds the plan; returns false if a size does not fit the int ranges used.
-bool make_plan(const Shape& s, Plan* p);
+bool make_plan(const Shape& s, Plan* p, bool shared = true);
 
 // Workspace pointers derived from a plan.
 struct Work {

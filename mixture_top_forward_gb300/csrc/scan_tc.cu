@@ -442,7 +442,7 @@ cudaError_t launch_one(const CUtensorMap& tk, const CUtensorMap& tv, const ScanA
 cudaError_t launch_scan_tc(const Plan& p, const Work& w, const __nv_bfloat16* K, const __nv_bfloat16* V, int level,
                            cudaStream_t st) {
     const ScanLevel& L = p.lev[level];
-    const bool full = level == p.nlev - 1;
+    const bool full = level == p.nlev - 1 && p.shared;  // (no LV without the shared branch)
     CUtensorMap tk, tv;
     if (!make_head_tmap(&tk, K, static_cast<uint64_t>(L.S), static_cast<uint64_t>(p.s.BH),
                         static_cast<uint64_t>(L.stride), static_cast<uint64_t>(p.s.N), 64))

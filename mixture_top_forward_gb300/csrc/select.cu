@@ -56,7 +56,7 @@ __global__ void __launch_bounds__(ST) select_kernel(int m, int k, int chunks, in
     auto part_of = [&](int c) { return part + ((bh * chunks + c) * m + i) * 68; };
 
     // ---- shared-expert value ------------------------------------------------
-    if (!PILOT) {
+    if (!PILOT && part) {
         if (small) {
             // M = max of the chunks' maxima; factors exp(max_c - M); L = sum sum_c f_c
             const float mc = tid < chunks ? part_of(tid)[0] : -INFINITY;
@@ -313,7 +313,8 @@ __global__ void __launch_bounds__(ST) select_kernel(int m, int k, int chunks, in
 cudaError_t launch_select(const Plan& p, const Work& w, int32_t* expert_idx, cudaStream_t st) {
     const unsigned grid = static_cast<unsigned>(p.s.BH * p.s.m);
     const ScanLevel& L = p.lev[p.nlev - 1];
-    select_kernel<false><<<grid, ST, 0, st>>>(p.s.m, p.s.k, L.chunks, L.cap, w.part, w.cand, w.ccount, w.lv32,
+    select_kernel<false><<<grid, ST, 0, st>>>(p.s.m, p.s.k, L.chunks, L.cap, p.shared ? w.part : nullptr, w.cand,
+                                             w.ccount, w.lv32,
                                              w.lvbf, expert_idx, nullptr, L.dense ? w.dense : nullptr, p.s.N, L.ld,
                                              1, w.ridx, w.rval, w.rcount, L.rcap, p.nlev > 1 ? w.theta : nullptr);
     return cudaGetLastError();

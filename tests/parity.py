@@ -42,22 +42,29 @@ def out_rows(out_dev, rows):
     return synth.bf16_to_f64(sel.view(torch.int16).cpu().numpy().view(np.uint16))
 
 
-def run_gpu(q, k, v, gh, gw, m, kk, full_out=True):
+def run_gpu(q, k, v, gh, gw, m, kk, full_out=True, shared=True):
     """Runs the library on device copies. Small results come back as numpy;
-    `out` stays on the device unless full_out (then float64 numpy)."""
+    `out` stays on the device unless full_out (then float64 numpy).
+    shared=False runs the routing-only ablation, which returns no Lq or LV."""
     import torch
 
     import mixture_top_forward_gb300 as M
 
     Q, K, V = to_device(q), to_device(k), to_device(v)
-    out, eidx, route, lq, lv = M.mita_forward_aux(Q, K, V, gh, gw, m, kk)
+    if shared:
+        out, eidx, route, lq, lv = M.mita_forward_aux(Q, K, V, gh, gw, m, kk)
+    else:
+        out, eidx, route = M.mita_forward_routed(Q, K, V, gh, gw, m, kk)
+        lq = lv = None
     torch.cuda.synchronize()
     assert M.mita_sync_status() == 0
     del Q, K, V
     if full_out:
         out = synth.bf16_to_f64(out.view(torch.int16).cpu().numpy().view(np.uint16))
-    return dict(out=out, expert_idx=eidx.cpu().numpy(), route=route.cpu().numpy(),
-                lq=lq.cpu().numpy().astype(np.float64), lv=lv.cpu().numpy().astype(np.float64))
+    res = dict(out=out, expert_idx=eidx.cpu().numpy(), route=route.cpu().numpy(), lq=None, lv=None)
+    if shared:
+        res.update(lq=lq.cpu().numpy().astype(np.float64), lv=lv.cpu().numpy().astype(np.float64))
+    return res
 
 
 def check_experts(orc, lq_o, k, gpu_e, ora_e, gap, report):
@@ -113,31 +120,34 @@ def check_outputs(gpu_out, cond_out, report):
     assert mean <= OUT_MEAN, f"mean-abs output error {mean:.3g} > {OUT_MEAN}"
 
 
-def full_parity(orc, q, k, v, gh, gw, m, kk, gpu=None):
-    """Every element against the full oracle (small problems)."""
+def full_parity(orc, q, k, v, gh, gw, m, kk, gpu=None, shared=True):
+    """Every element against the full oracle (small problems). shared=False:
+    the routing-only ablation (no Lq/LV diagnostics: that path returns none)."""
     B, H, N, d = q.shape
-    gpu = gpu or run_gpu(q, k, v, gh, gw, m, kk)
-    ora = orc.forward(q, k, v, gh, gw, m, kk)
+    gpu = gpu or run_gpu(q, k, v, gh, gw, m, kk, shared=shared)
+    ora = orc.forward(q, k, v, gh, gw, m, kk, shared=shared)
     rep = {}
     BH = B * H
     lq_o = ora["lq"].reshape(BH, m, d)
-    assert np.max(np.abs(gpu["lq"].reshape(BH, m, d) - lq_o)) <= LQ_TOL, "Lq differs"
-    rep["lv_max_abs"] = float(np.max(np.abs(gpu["lv"].reshape(BH, m, d) - ora["lv"].reshape(BH, m, d))))
-    assert rep["lv_max_abs"] <= LV_TOL, f"LV differs by {rep['lv_max_abs']:.3g}"
+    if shared:
+        assert np.max(np.abs(gpu["lq"].reshape(BH, m, d) - lq_o)) <= LQ_TOL, "Lq differs"
+        rep["lv_max_abs"] = float(np.max(np.abs(gpu["lv"].reshape(BH, m, d) - ora["lv"].reshape(BH, m, d))))
+        assert rep["lv_max_abs"] <= LV_TOL, f"LV differs by {rep['lv_max_abs']:.3g}"
     kf = k.reshape(BH, N, d)
     check_experts(orc, lq_o, kf, gpu["expert_idx"].reshape(BH, m, kk), ora["expert_idx"].reshape(BH, m, kk),
                   ora["gap"].reshape(BH, m), rep)
     which = np.arange(BH * N)
     check_routes(q, lq_o, gpu["route"].reshape(-1), ora["route"].reshape(-1), ora["rgap"].reshape(-1), which, rep)
-    cond, ws = orc.attend(q, ora["lq"], ora["lv"], k, v, gpu["expert_idx"], gpu["route"])
+    cond, ws = orc.attend(q, ora["lq"], ora["lv"], k, v, gpu["expert_idx"], gpu["route"], shared=shared)
     assert np.max(np.abs(ws - 1.0)) < 1e-9
     check_outputs(gpu["out"].reshape(BH, N, d), cond.reshape(BH, N, d), rep)
     rep["out_max_abs_unconditioned"] = float(np.max(np.abs(gpu["out"] - ora["out"])))
     return rep
 
 
-def sampled_parity(orc, q, k, v, gh, gw, m, kk, gpu, heads, queries_per_head, seed=0):
-    """Full checks on a few heads; routes and outputs on sampled queries."""
+def sampled_parity(orc, q, k, v, gh, gw, m, kk, gpu, heads, queries_per_head, seed=0, shared=True):
+    """Full checks on a few heads; routes and outputs on sampled queries.
+    shared=False: the routing-only ablation (no Lq/LV diagnostics)."""
     B, H, N, d = q.shape
     BH = B * H
     rng = np.random.default_rng(seed)
@@ -146,11 +156,12 @@ def sampled_parity(orc, q, k, v, gh, gw, m, kk, gpu, heads, queries_per_head, se
     for bh in heads:
         qs, ks, vs = qf[bh:bh + 1][None], kf[bh:bh + 1][None], vf[bh:bh + 1][None]
         lq_o = orc.landmarks(qs, gh, gw, m)  # [1,1,m,d]
-        assert np.max(np.abs(gpu["lq"].reshape(BH, m, d)[bh] - lq_o[0, 0])) <= LQ_TOL, f"Lq differs in head {bh}"
         lv_o, e_o, gap = orc.scan(lq_o, ks, vs, kk)
-        lv_err = float(np.max(np.abs(gpu["lv"].reshape(BH, m, d)[bh] - lv_o[0])))
-        rep["lv_max_abs"] = max(rep.get("lv_max_abs", 0.0), lv_err)
-        assert lv_err <= LV_TOL, f"LV differs by {lv_err:.3g} in head {bh}"
+        if shared:
+            assert np.max(np.abs(gpu["lq"].reshape(BH, m, d)[bh] - lq_o[0, 0])) <= LQ_TOL, f"Lq differs in head {bh}"
+            lv_err = float(np.max(np.abs(gpu["lv"].reshape(BH, m, d)[bh] - lv_o[0])))
+            rep["lv_max_abs"] = max(rep.get("lv_max_abs", 0.0), lv_err)
+            assert lv_err <= LV_TOL, f"LV differs by {lv_err:.3g} in head {bh}"
         g_e = gpu["expert_idx"].reshape(BH, m, kk)[bh:bh + 1]
         check_experts(orc, lq_o.reshape(1, m, d), ks.reshape(1, N, d), g_e, e_o, gap, rep)
         n_s = min(N, queries_per_head)
@@ -159,6 +170,6 @@ def sampled_parity(orc, q, k, v, gh, gw, m, kk, gpu, heads, queries_per_head, se
         g_r = gpu["route"].reshape(BH, N)[bh]
         check_routes(qs, lq_o, g_r[which], r_o, rg, which, rep)
         cond, ws = orc.attend(qs, lq_o, lv_o.reshape(1, 1, m, d), ks, vs, g_e.reshape(1, 1, m, kk),
-                              g_r.reshape(1, 1, N), which=which)
+                              g_r.reshape(1, 1, N), which=which, shared=shared)
         check_outputs(out_rows(gpu["out"], bh * N + which), cond, rep)
     return rep

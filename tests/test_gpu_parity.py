@@ -72,6 +72,63 @@ def test_edge_shapes(orc, B, H, N, gh, gw, m, k):
     print(rep)
 
 
+def _routed_args(name):
+    """The routing-only ablation at the MiTA config's budget: each expert
+    holds k' = m + k keys (the shared pairs' share goes to routed keys)."""
+    gh, gw, m, k = _cfg_args(name)
+    return gh, gw, m, min(m + k, synth.CONFIGS[name]["N"])
+
+
+@pytest.mark.parametrize("name", ["tiny", "deit", "seg1024"])
+def test_routed_config_full_oracle(orc, name):
+    q, k, v = synth.make_inputs(name)
+    rep = parity.full_parity(orc, q, k, v, *_routed_args(name), shared=False)
+    print(name, rep)
+
+
+@pytest.mark.parametrize("name,heads,nq", [
+    ("long64k", (0, 7), 8192),
+    ("long1m", (3,), 8192),
+])
+def test_routed_config_sampled(orc, name, heads, nq):
+    q, k, v = synth.make_inputs(name)
+    args = _routed_args(name)
+    gpu = parity.run_gpu(q, k, v, *args, full_out=False, shared=False)
+    rep = parity.sampled_parity(orc, q, k, v, *args, gpu, heads, nq, shared=False)
+    print(name, rep)
+
+
+@pytest.mark.parametrize("B,H,N,gh,gw,m,k", [
+    (2, 3, 1000, 0, 0, 7, 13),      # ragged windows and tiles
+    (1, 2, 196, 14, 14, 25, 196),   # k = N: full softmax attention for every query
+    (2, 2, 300, 0, 0, 1, 5),        # m = 1: every query in one expert
+    (1, 3, 777, 0, 0, 33, 1),       # k = 1: each output is one value row
+    (1, 1, 1, 0, 0, 1, 1),          # a single token
+    (3, 1, 2500, 50, 50, 16, 1024), # k = MITA_MAX_K
+])
+def test_routed_edge_shapes(orc, B, H, N, gh, gw, m, k):
+    q, kk_, v = _rand(B, H, N, 300 + N + m + k, 2.0)
+    rep = parity.full_parity(orc, q, kk_, v, gh, gw, m, k, shared=False)
+    print(rep)
+
+
+def test_routed_differs_from_mita(orc):
+    """Same experts and routes on both entry points; the outputs differ (the
+    shared pairs are gone), so the ablation is not MiTA under another name."""
+    import torch
+
+    import mixture_top_forward_gb300 as M
+
+    q, k, v = synth.make_inputs("seg1024")
+    Q, K, V = parity.to_device(q), parity.to_device(k), parity.to_device(v)
+    a = M.mita_forward(Q, K, V, 32, 32, 49, 49)
+    b = M.mita_forward_routed(Q, K, V, 32, 32, 49, 49)
+    torch.cuda.synchronize()
+    assert torch.equal(a[1], b[1]) and torch.equal(a[2], b[2])
+    diff = (a[0].float() - b[0].float()).abs().mean().item()
+    assert diff > 1e-2, diff
+
+
 def test_ascending_scores_force_compaction(orc):
     """Scores that grow along the sequence make every key beat the running
     threshold, so every chunk buffer overflows and compacts repeatedly."""
