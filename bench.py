@@ -342,6 +342,9 @@ def run_gpu(args, rank, world):
     if rank == 0 and not args.no_sweep:
         res["sweep"] = sweep(args, M, dev, stream, peaks)
         res["routed_only"] = routed_only(args, M, dev, stream, peaks)
+        mita_ms = {n: r["ms_per_step"] for n, r in res["sweep"].items()}
+        mita_ms[name] = ms_step
+        res["full_attention"] = full_attention(args, dev, stream, mita_ms)
     if rank == 0 and not args.no_cpu and world == 1:
         res["cpu_baseline"] = cpu_baseline(name, q, k, v)
     return res
@@ -450,6 +453,68 @@ def routed_only(args, M, dev, stream, peaks):
             "roofline_frac": roofline_time(w["total"], peaks, sustained=True) / (ms / 1e3),
             "expert_tflops": exp_tf, "expert_frac": exp_tf / peaks["bf16_tflops_sustained"] if exp_tf else None,
             "stage_ms": stage_ms}
+
+
+# ---------------------------------------------------------------------------
+# Full-attention comparator: plain softmax attention over all N keys by
+# PyTorch's fused SDPA (a library kernel, not this library's), the baseline
+# the pages' speedups are quoted against.
+# ---------------------------------------------------------------------------
+SDPA_BACKENDS = ("CUDNN_ATTENTION", "FLASH_ATTENTION", "EFFICIENT_ATTENTION")
+
+
+def sdpa_full(Q, K, V, backend=None):
+    """softmax(Q K^T / sqrt(d)) V on [B,H,N,d] bf16 device tensors through
+    the first fused SDPA backend that accepts the shapes (or `backend`).
+    Returns (out, backend name)."""
+    import torch
+    from torch.nn.attention import SDPBackend, sdpa_kernel
+
+    last = None
+    for name in ((backend,) if backend else SDPA_BACKENDS):
+        try:
+            with sdpa_kernel(getattr(SDPBackend, name)):
+                return torch.nn.functional.scaled_dot_product_attention(Q, K, V), name
+        except RuntimeError as e:  # backend refuses the shape or the device
+            last = e
+    raise RuntimeError(f"no fused SDPA backend ran: {last}")
+
+
+def full_attention(args, dev, stream, mita_ms, max_queries=65536):
+    """Full attention at the long-sequence workloads. Above max_queries the
+    timed call takes the first max_queries queries against all N keys and the
+    time is scaled by N / max_queries (each query's cost is the same, so the
+    pass is linear in the number of queries)."""
+    import torch
+
+    res = {}
+    for name in ("long64k", "long256k", args.config):
+        if name in res or name not in mita_ms:
+            continue
+        c = synth.CONFIGS[name]
+        q, k, v = synth.make_inputs(c)
+        to = lambda a: torch.from_numpy(a.view(np.int16)).to(dev).view(torch.bfloat16)
+        K, V = to(k), to(v)
+        nq = min(c["N"], max_queries)
+        Q = to(np.ascontiguousarray(q[:, :, :nq]))
+        _, backend = sdpa_full(Q, K, V)
+        for _ in range(2):
+            sdpa_full(Q, K, V, backend)
+        torch.cuda.synchronize()
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        n = 3
+        ev0.record(torch.cuda.current_stream(dev))
+        for _ in range(n):
+            sdpa_full(Q, K, V, backend)
+        ev1.record(torch.cuda.current_stream(dev))
+        torch.cuda.synchronize()
+        ms = ev0.elapsed_time(ev1) / n * c["N"] / nq
+        flops = 4 * c["B"] * c["H"] * c["N"] * c["N"] * 64
+        res[name] = {"backend": backend, "ms_per_pass": ms, "queries_timed": nq * c["B"] * c["H"],
+                     "tflops": flops / (ms / 1e3) / 1e12, "mita_speedup": ms / mita_ms[name]}
+        del Q, K, V
+        torch.cuda.empty_cache()
+    return res
 
 
 # ---------------------------------------------------------------------------

@@ -129,6 +129,29 @@ def test_routed_differs_from_mita(orc):
     assert diff > 1e-2, diff
 
 
+@pytest.mark.parametrize("name", ["seg1024", "ragged"])
+def test_full_attention_comparator(orc, name):
+    """The fused-SDPA baseline bench.py times is plain softmax attention: the
+    oracle's routing-only mode with one landmark and k = N (every query
+    attends to every key) gives the same outputs."""
+    import torch
+
+    import bench
+
+    if name == "ragged":
+        q, k, v = _rand(1, 3, 1000, 77, 2.0)
+    else:
+        q, k, v = synth.make_inputs(name)
+    out, backend = bench.sdpa_full(parity.to_device(q), parity.to_device(k), parity.to_device(v))
+    torch.cuda.synchronize()
+    got = synth.bf16_to_f64(out.contiguous().view(torch.int16).cpu().numpy().view(np.uint16))
+    N = q.shape[2]
+    ref = orc.forward(q, k, v, 0, 0, 1, N, shared=False)["out"]
+    rep = {"backend": backend}
+    parity.check_outputs(got, ref, rep)
+    print(name, rep)
+
+
 def test_ascending_scores_force_compaction(orc):
     """Scores that grow along the sequence make every key beat the running
     threshold, so every chunk buffer overflows and compacts repeatedly."""
