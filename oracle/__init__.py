@@ -48,6 +48,8 @@ def _bind(path: str):
     lib.oracle_route.argtypes = [vp, vp, i64, i64, ci, ci, vp, i64, vp, vp]
     lib.oracle_attend.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i64, ci, ci, ci, vp, i64, ci, vp, vp]
     lib.oracle_forward.argtypes = [vp, vp, vp, i64, i64, i64, ci, ci, ci, ci, ci, ci] + [vp] * 8
+    lib.oracle_route_multi.argtypes = [vp, vp, i64, i64, ci, ci, ci, vp, i64, vp, vp]
+    lib.oracle_attend_multi.argtypes = [vp, vp, vp, vp, vp, vp, vp, i64, i64, ci, ci, ci, ci, vp, i64, vp, vp]
     return lib
 
 
@@ -190,6 +192,64 @@ class Oracle:
         return r
 
 
+    def route_multi(self, q, lq, s: int, which=None):
+        """Top-s routes (highest logit first, ties to the lower landmark) and
+        the margin between the s-th and (s+1)-th logits, for the queries in
+        `which` (global ids) or all: ([..., s] int32, [...] float64)."""
+        q = _u16(q)
+        *lead, N, d = q.shape
+        BH = int(np.prod(lead)) if lead else 1
+        lq = np.ascontiguousarray(lq, dtype=np.float64).reshape(BH, -1, d)
+        m = lq.shape[1]
+        if which is not None:
+            which = np.ascontiguousarray(which, dtype=np.int64)
+            n, shp = which.shape[0], (which.shape[0],)
+        else:
+            n, shp = BH * N, (BH, N)
+        r = np.empty(shp + (s,), np.int32)
+        g = np.empty(shp, np.float64)
+        _check(self.lib.oracle_route_multi(_p(q), _p(lq), BH, N, d, m, s, _p(which), n, _p(r), _p(g)), "route_multi")
+        return r, g
+
+    def attend_multi(self, q, lq, lv, k, v, eidx, route_, which=None):
+        """Attention over the shared pairs and the union of each query's s
+        routed experts (route_ [B,H,N,s]); returns (out, wsum) like attend."""
+        q, k, v = _u16(q), _u16(k), _u16(v)
+        *lead, N, d = q.shape
+        BH = int(np.prod(lead)) if lead else 1
+        lq = np.ascontiguousarray(lq, dtype=np.float64).reshape(BH, -1, d)
+        lv = np.ascontiguousarray(lv, dtype=np.float64).reshape(BH, -1, d)
+        m = lq.shape[1]
+        eidx = np.ascontiguousarray(eidx, dtype=np.int32).reshape(BH, m, -1)
+        kk = eidx.shape[2]
+        s = int(np.asarray(route_).shape[-1])
+        route_ = np.ascontiguousarray(route_, dtype=np.int32).reshape(BH * N, s)
+        if which is not None:
+            which = np.ascontiguousarray(which, dtype=np.int64)
+            n, shp = which.shape[0], (which.shape[0],)
+        else:
+            n, shp = BH * N, (BH, N)
+        out = np.empty(shp + (d,), np.float64)
+        ws = np.empty(shp, np.float64)
+        _check(self.lib.oracle_attend_multi(_p(q), _p(lq), _p(lv), _p(k), _p(v), _p(eidx), _p(route_), BH, N, d, m,
+                                           kk, s, _p(which), n, _p(out), _p(ws)), "attend_multi")
+        return out, ws
+
+    def forward_multi(self, q, k, v, grid_h: int, grid_w: int, m: int, kk: int, s: int):
+        """The forward pass with s routed experts per query: landmarks, scan,
+        top-s routes, attention over the shared pairs and the union of the s
+        experts. Same keys as forward; route is [B,H,N,s]."""
+        q, k, v = _u16(q), _u16(k), _u16(v)
+        B, H, N, d = q.shape
+        lq = self.landmarks(q, grid_h, grid_w, m)
+        lv, e, gap = self.scan(lq, k, v, kk)
+        r, rg = self.route_multi(q, lq, s)
+        out, ws = self.attend_multi(q, lq, lv, k, v, e, r)
+        return dict(out=out.reshape(B, H, N, d), expert_idx=e.reshape(B, H, m, kk), route=r.reshape(B, H, N, s),
+                    lq=lq.reshape(B, H, m, d), lv=lv.reshape(B, H, m, d), gap=gap.reshape(B, H, m),
+                    rgap=rg.reshape(B, H, N), wsum=ws.reshape(B, H, N))
+
+
 def _default() -> Oracle:
     global _lib
     with _lock:
@@ -228,3 +288,15 @@ def attend(*a, **kw):
 
 def forward(*a, **kw):
     return _default().forward(*a, **kw)
+
+
+def route_multi(*a, **kw):
+    return _default().route_multi(*a, **kw)
+
+
+def attend_multi(*a, **kw):
+    return _default().attend_multi(*a, **kw)
+
+
+def forward_multi(*a, **kw):
+    return _default().forward_multi(*a, **kw)

@@ -61,6 +61,12 @@ double dot_bf16(const double* a, const uint16_t* b, int d) {
     return s;
 }
 
+double dot_f64(const double* a, const double* b, int d) {
+    double s = 0.0;
+    for (int c = 0; c < d; ++c) s += a[c] * b[c];
+    return s;
+}
+
 int isqrt_exact(int m) {
     int p = static_cast<int>(std::lround(std::sqrt(static_cast<double>(m))));
     while (p * p > m) --p;
@@ -301,6 +307,104 @@ int oracle_attend(const uint16_t* q, const double* lq, const double* lv, const u
             int64_t jj = (sel[j] >= 0 && sel[j] < N) ? sel[j] : 0;
             const uint16_t* row = v + (bh * N + jj) * d;
             for (int c = 0; c < d; ++c) acc[c] += w * widen(row[c]);
+        }
+        for (int c = 0; c < d; ++c) out[it * d + c] = acc[c] / z;
+        if (wsum) {
+            double ws = 0.0;
+            for (double t : logit) ws += std::exp(t - mx) / z;
+            wsum[it] = ws;
+        }
+    }
+    return bad ? -1 : 0;
+}
+
+// Stage 3 with s experts per query. The pages use one routed expert per
+// query and call that "the s = 1 configuration" ([P2], end of section
+// "MiTA：…"), which names the general form without describing it. Reading
+// taken: a query takes the s landmarks with the highest logits tau <q, Lq_i>,
+// listed highest first, ties to the lower landmark index (s = 1 is
+// oracle_route). route is [n_items][s]; rgap[it] is the s-th highest logit
+// minus the (s+1)-th (+inf when s = m), the margin that decides the set.
+int oracle_route_multi(const uint16_t* q, const double* lq, int64_t BH, int64_t N, int d, int m, int s,
+                       const int64_t* which, int64_t n_which, int32_t* route, double* rgap) {
+    if (N < 1 || d < 1 || m < 1 || s < 1 || s > m) return -1;
+    const int64_t n_items = which ? n_which : BH * N;
+    const double tau = 1.0 / std::sqrt(static_cast<double>(d));
+#pragma omp parallel for schedule(dynamic, 256)
+    for (int64_t it = 0; it < n_items; ++it) {
+        const int64_t qi = which ? which[it] : it;
+        const int64_t bh = qi / N;
+        std::vector<double> qd(d), sc(m);
+        for (int c = 0; c < d; ++c) qd[c] = widen(q[qi * d + c]);
+        for (int i = 0; i < m; ++i) sc[i] = tau * dot_f64(lq + (bh * m + i) * d, qd.data(), d);
+        std::vector<int> order(m);
+        for (int i = 0; i < m; ++i) order[i] = i;
+        // highest logit first; a stable sort keeps equal logits in index order
+        std::stable_sort(order.begin(), order.end(), [&](int x, int y) { return sc[x] > sc[y]; });
+        for (int u = 0; u < s; ++u) route[it * s + u] = order[u];
+        if (rgap) rgap[it] = s < m ? sc[order[s - 1]] - sc[order[s]] : std::numeric_limits<double>::infinity();
+    }
+    return 0;
+}
+
+// Stage 4 with s experts per query: the m shared pairs and the keys of the s
+// routed experts under ONE softmax, as for s = 1 ([P2] "MiTA：…", unified
+// softmax). Reading taken: the routed part is the UNION of the s experts' key
+// sets, so a key that two of the chosen experts hold enters once (attention
+// over a set of keys; counting it twice would weight it twice). route is the
+// full [BH][N][s] array; everything else as in oracle_attend (shared = 1).
+int oracle_attend_multi(const uint16_t* q, const double* lq, const double* lv, const uint16_t* k, const uint16_t* v,
+                        const int32_t* eidx, const int32_t* route, int64_t BH, int64_t N, int d, int m, int kk, int s,
+                        const int64_t* which, int64_t n_which, double* out, double* wsum) {
+    if (N < 1 || d < 1 || m < 1 || kk < 1 || kk > N || s < 1 || s > m) return -1;
+    const int64_t n_items = which ? n_which : BH * N;
+    const double tau = 1.0 / std::sqrt(static_cast<double>(d));
+    int bad = 0;
+#pragma omp parallel for schedule(dynamic, 64) reduction(| : bad)
+    for (int64_t it = 0; it < n_items; ++it) {
+        const int64_t qi = which ? which[it] : it;
+        const int64_t bh = qi / N;
+        std::vector<int32_t> keys;
+        for (int u = 0; u < s; ++u) {
+            const int e = route[qi * s + u];
+            if (e < 0 || e >= m) {
+                bad |= 1;
+                continue;
+            }
+            const int64_t row0 = (bh * m + e) * static_cast<int64_t>(kk);  // expert e's kk key indices
+            for (int j = 0; j < kk; ++j) {
+                if (eidx[row0 + j] < 0 || eidx[row0 + j] >= N)
+                    bad |= 1;
+                else
+                    keys.push_back(eidx[row0 + j]);
+            }
+        }
+        std::sort(keys.begin(), keys.end());
+        keys.erase(std::unique(keys.begin(), keys.end()), keys.end());
+        const int64_t nk = static_cast<int64_t>(keys.size());
+        std::vector<double> qd(d), logit(m + nk);
+        for (int c = 0; c < d; ++c) qd[c] = widen(q[qi * d + c]);
+        for (int i = 0; i < m; ++i) logit[i] = tau * dot_f64(lq + (bh * m + i) * d, qd.data(), d);
+        for (int64_t j = 0; j < nk; ++j) {
+            const uint16_t* row = k + (bh * N + keys[j]) * d;
+            double t = 0.0;
+            for (int c = 0; c < d; ++c) t += qd[c] * widen(row[c]);
+            logit[m + j] = tau * t;
+        }
+        double mx = -std::numeric_limits<double>::infinity();
+        for (double t : logit) mx = std::max(mx, t);
+        std::vector<double> acc(d, 0.0);
+        double z = 0.0;
+        for (int64_t j = 0; j < m + nk; ++j) {  // shared pairs first, then the union's keys
+            const double p = std::exp(logit[j] - mx);
+            z += p;
+            if (j < m) {
+                const double* lvj = lv + (bh * m + j) * d;
+                for (int c = 0; c < d; ++c) acc[c] += p * lvj[c];
+            } else {
+                const uint16_t* vrow = v + (bh * N + keys[j - m]) * d;
+                for (int c = 0; c < d; ++c) acc[c] += p * widen(vrow[c]);
+            }
         }
         for (int c = 0; c < d; ++c) out[it * d + c] = acc[c] / z;
         if (wsum) {

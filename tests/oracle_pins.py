@@ -18,6 +18,13 @@ What pins what:
   * permutation        permuting K,V rows permutes the experts' indices and
                        leaves LV, routes and outputs unchanged
   * hand example       a 4-token, d=2 case worked out in closed form
+  * routing-only       k=N gives plain softmax attention over K, V; k<N
+                       gives softmax attention over the routed keys alone
+  * s experts/query    top-s routes against a stable numpy argsort (planted
+                       exact tie); outputs against a brute-force softmax over
+                       the shared pairs and the Python set union of the s
+                       experts; s=1 is the one-expert forward; s=m with k=N
+                       is plain softmax attention over [Lq; K]
 """
 from __future__ import annotations
 
@@ -201,6 +208,70 @@ def pin_routing_only(o):
     assert np.max(np.abs(full["out"] - r["out"])) > 1e-3
 
 
+def pin_route_multi(o):
+    """Top-s routes: the first s entries of a stable descending sort of the
+    logits (equal logits keep index order), and the s-th/(s+1)-th margin."""
+    q = _rand((2, 2, 150, 64), 31, 0)
+    lq = o.landmarks(q, 0, 0, 9)
+    lq[:, :, 6] = lq[:, :, 2]  # an exact tie between landmarks 2 and 6 for every query
+    t = np.einsum("bhnc,bhic->bhni", _f64(q), lq) / 8.0
+    order = np.argsort(-t, axis=-1, kind="stable")
+    ts = -np.sort(-t, axis=-1)
+    for s_ in (1, 2, 3, 9):
+        r, g = o.route_multi(q, lq, s_)
+        assert np.array_equal(r.reshape(2, 2, 150, s_), order[..., :s_])
+        want = ts[..., s_ - 1] - ts[..., s_] if s_ < 9 else np.full((2, 2, 150), np.inf)
+        assert np.all(g.reshape(2, 2, 150) == want) or np.max(np.abs(g.reshape(2, 2, 150) - want)) < 1e-12
+    # where landmark 2 or 6 is taken and the other falls inside the cut too,
+    # 2 comes first
+    r, _ = o.route_multi(q, lq, 9)
+    pos = {i: np.argmax(r == i, axis=-1) for i in (2, 6)}
+    assert np.all(pos[2] < pos[6])
+    r1, _ = o.route_multi(q, lq, 1)
+    r0, _ = o.route(q, lq)
+    assert np.array_equal(r1[..., 0], r0)
+
+
+def pin_attend_multi_union(o):
+    """s experts per query: one softmax over the m shared pairs and the set
+    union of the s experts' keys, computed here by brute force (Python sets,
+    numpy softmax). The inputs make the experts overlap, so counting a shared
+    key twice would fail."""
+    N, m, kk, s_ = 48, 6, 8, 3
+    q, k, v = synth.make_inputs(dict(B=1, H=2, N=N, d=64, grid_h=0, grid_w=0, m=m, k=kk, recipe="clusters",
+                                     clusters=3))
+    r = o.forward_multi(q, k, v, 0, 0, m, kk, s_)
+    Q, K, V = _f64(q)[0], _f64(k)[0], _f64(v)[0]
+    overlaps = 0
+    for h in range(2):
+        for n in range(N):
+            union = sorted(set(int(j) for u in range(s_) for j in r["expert_idx"][0, h, r["route"][0, h, n, u]]))
+            overlaps += len(union) < s_ * kk
+            keys = np.concatenate([r["lq"][0, h], K[h, union]])
+            vals = np.concatenate([r["lv"][0, h], V[h, union]])
+            w = softmax(keys @ Q[h, n] / 8.0)
+            assert np.max(np.abs(r["out"][0, h, n] - w @ vals)) < 1e-12
+    assert overlaps > N // 2, overlaps
+    assert np.max(np.abs(r["wsum"] - 1.0)) < 1e-12
+
+
+def pin_multi_reductions(o):
+    """s = 1 is the one-expert forward pass; s = m with k = N takes every key
+    once, which is plain softmax attention over [Lq; K] with values [LV; V]."""
+    q, k, v = synth.make_inputs("tiny")
+    one = o.forward(q, k, v, 14, 14, 25, 25)
+    mul = o.forward_multi(q, k, v, 14, 14, 25, 25, 1)
+    assert np.array_equal(mul["route"][..., 0], one["route"])
+    assert np.max(np.abs(mul["out"] - one["out"])) < 1e-12
+    N, m = 40, 4
+    q, k, v = _rand((1, 2, N, 64), 37, 0, 2.0), _rand((1, 2, N, 64), 37, 1), _rand((1, 2, N, 64), 37, 2)
+    r = o.forward_multi(q, k, v, 0, 0, m, N, m)
+    Q, K, V = _f64(q)[0], _f64(k)[0], _f64(v)[0]
+    for h in range(2):
+        w = softmax(Q[h] @ np.concatenate([r["lq"][0, h], K[h]]).T / 8.0, axis=-1)
+        assert np.max(np.abs(r["out"][0, h] - w @ np.concatenate([r["lv"][0, h], V[h]]))) < 1e-12
+
+
 def pin_weights_sum_to_one(o):
     q, k, v = synth.make_inputs("tiny")
     r = o.forward(q, k, v, 14, 14, 25, 25)
@@ -264,6 +335,9 @@ def pin_hand_example(o):
 
 
 ALL_PINS = [
+    pin_route_multi,
+    pin_attend_multi_union,
+    pin_multi_reductions,
     pin_routing_only,
     pin_window_tables,
     pin_landmarks_adaptive_pool,

@@ -32,6 +32,13 @@ MUTANTS = [
     ("expert of landmark 0", "eidx + (bh * m + e) * static_cast<int64_t>(kk);", "eidx + (bh * m + 0) * static_cast<int64_t>(kk);"),
     ("attend drops tau on routed logits", "logit[ms + j] = tau * t;", "logit[ms + j] = t;"),
     ("routing-only keeps the shared pairs", "const int ms = shared ? m : 0;", "const int ms = m;"),
+    ("s experts: union keeps duplicates", "keys.erase(std::unique(keys.begin(), keys.end()), keys.end());",
+     "(void)0;"),
+    ("s experts: lowest logits taken", "return sc[x] > sc[y]; });", "return sc[x] < sc[y]; });"),
+    ("s experts: ties to the higher landmark", "return sc[x] > sc[y]; });",
+     "return sc[x] > sc[y] || (sc[x] == sc[y] && x > y); });"),
+    ("s experts: only the first expert attended", "for (int u = 0; u < s; ++u) {\n            const int e",
+     "for (int u = 0; u < 1; ++u) {\n            const int e"),
 ]
 
 
