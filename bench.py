@@ -342,6 +342,7 @@ def run_gpu(args, rank, world):
     if rank == 0 and not args.no_sweep:
         res["sweep"] = sweep(args, M, dev, stream, peaks)
         res["routed_only"] = routed_only(args, M, dev, stream, peaks)
+        res["multi_expert"] = multi_expert(args, M, dev, stream)
         mita_ms = {n: r["ms_per_step"] for n, r in res["sweep"].items()}
         mita_ms[name] = ms_step
         res["full_attention"] = full_attention(args, dev, stream, mita_ms)
@@ -453,6 +454,54 @@ def routed_only(args, M, dev, stream, peaks):
             "roofline_frac": roofline_time(w["total"], peaks, sustained=True) / (ms / 1e3),
             "expert_tflops": exp_tf, "expert_frac": exp_tf / peaks["bf16_tflops_sustained"] if exp_tf else None,
             "stage_ms": stage_ms}
+
+
+# fp32 FMA peak of the CUDA cores: 152 SMs x 128 FMA lanes x 2 FLOP x 2.07 GHz
+# (the clock the bench's clock record shows under load)
+SIMT_FP32_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
+
+
+def multi_expert(args, M, dev, stream, s=2):
+    """s routed experts per query on the timed workload (device-resident
+    inputs; the attention passes run on the CUDA cores). The expert stage's
+    FLOPs count s*k routed keys per query, an upper bound (a key shared by
+    two chosen experts is attended once)."""
+    import torch
+
+    c = synth.CONFIGS[args.config]
+    q, k, v = synth.make_inputs(c)
+    to = lambda a: torch.from_numpy(a.view(np.int16)).to(dev).view(torch.bfloat16)
+    Q, K, V = to(q), to(k), to(v)
+    out = torch.empty_like(Q)
+    e = torch.empty((c["B"], c["H"], c["m"], c["k"]), dtype=torch.int32, device=dev)
+    r = torch.empty((c["B"], c["H"], c["N"], s), dtype=torch.int32, device=dev)
+    a = (c["grid_h"], c["grid_w"], c["m"], c["k"], s)
+    for _ in range(3):
+        M.mita_forward_multi(Q, K, V, *a, out=out, expert_idx=e, route=r, stream=stream)
+    torch.cuda.synchronize()
+    assert M.mita_sync_status(stream) == 0, M.mita_last_error()
+    M.mita_profile_read(stream)
+    M.mita_profile_enable(True)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    n = 5
+    ev0.record(stream)
+    for _ in range(n):
+        M.mita_forward_multi(Q, K, V, *a, out=out, expert_idx=e, route=r, stream=stream)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    M.mita_profile_enable(False)
+    stages = M.mita_profile_read(stream)
+    assert M.mita_sync_status(stream) == 0, M.mita_last_error()
+    ms = ev0.elapsed_time(ev1) / n
+    stage_ms = {x: stages[x][0] / n for x in STAGES}
+    BH, N, m, kk = c["B"] * c["H"], c["N"], c["m"], c["k"]
+    exp_flops = BH * 4 * N * (m + s * kk) * 64
+    exp_tf = exp_flops / (stage_ms["expert"] / 1e3) / 1e12
+    del Q, K, V, out
+    torch.cuda.empty_cache()
+    return {"s": s, "queries_per_s": BH * N / (ms / 1e3), "ms_per_step": ms, "stage_ms": stage_ms,
+            "expert": {"bound": "alu", "achieved": exp_tf, "peak": SIMT_FP32_TFLOPS, "unit": "TFLOP/s",
+                       "frac": exp_tf / SIMT_FP32_TFLOPS, "flops": "4 N (m + s k) d per head (upper bound)"}}
 
 
 # ---------------------------------------------------------------------------

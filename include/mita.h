@@ -67,6 +67,7 @@ extern "C" {
 
 #define MITA_MAX_M 1024
 #define MITA_MAX_K 1024
+#define MITA_MAX_S 8 /* routed experts per query (mita_forward_multi) */
 
 /*
  * The MiTA forward pass, stages 1-4 above, on device buffers.
@@ -89,6 +90,23 @@ int mita_forward(const void* Q, const void* K, const void* V, int B, int H, int 
  */
 int mita_forward_routed(const void* Q, const void* K, const void* V, int B, int H, int N, int d, int grid_h,
                         int grid_w, int m, int k, void* out, int32_t* expert_idx, int32_t* route, void* stream);
+
+/*
+ * MiTA with s routed experts per query. The pages run what they call the
+ * s = 1 configuration ("NeurIPS 2026 | Mixture-of-Top-k 注意力"
+ * (shuwu5.cn), end of section "MiTA：用少量地标查询，同时完成压缩与专家构造") and do
+ * not describe s > 1; this entry point takes the plain generalisation:
+ * stage 3 gives each query the s landmarks with the highest logits
+ * tau <q, Lq_i> (highest first, ties to the lower landmark index), and stage
+ * 4 attends, under ONE softmax, to the m shared pairs and the union of the s
+ * experts' keys (a key held by several of them enters once).
+ * route: device, int32 [B][H][N][s], each query's landmarks highest first.
+ * 1 <= s <= min(m, MITA_MAX_S). s = 1 is exactly mita_forward. Other
+ * arguments, layouts, errors and asynchrony as for mita_forward. The extra
+ * workspace is an fp32 state row of 272 bytes per query (s > 1).
+ */
+int mita_forward_multi(const void* Q, const void* K, const void* V, int B, int H, int N, int d, int grid_h,
+                       int grid_w, int m, int k, int s, void* out, int32_t* expert_idx, int32_t* route, void* stream);
 
 /*
  * mita_forward with two optional extra device outputs (either may be NULL):

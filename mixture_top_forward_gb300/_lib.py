@@ -59,6 +59,8 @@ def load(path: str | None = None, build_if_missing: bool = True) -> ctypes.CDLL:
         lib.mita_forward_routed.restype = ci
         lib.mita_forward_aux.argtypes = [vp, vp, vp] + [ci] * 8 + [vp, vp, vp, vp, vp, vp]
         lib.mita_forward_aux.restype = ci
+        lib.mita_forward_multi.argtypes = [vp, vp, vp] + [ci] * 9 + [vp, vp, vp, vp]
+        lib.mita_forward_multi.restype = ci
         lib.mita_forward_noalloc.argtypes = [vp, vp, vp] + [ci] * 8 + [vp, vp, vp, vp]
         lib.mita_forward_noalloc.restype = ci
         lib.mita_forward_host.argtypes = [vp, vp, vp] + [ci] * 8 + [vp, vp, vp, vp]
@@ -145,6 +147,31 @@ def mita_forward_routed(Q, K, V, grid_h: int, grid_w: int, m: int, k: int, out=N
     k pairs of its routed expert alone), on device tensors; arguments and
     results as mita_forward."""
     return mita_forward(Q, K, V, grid_h, grid_w, m, k, out, expert_idx, route, stream, _entry="mita_forward_routed")
+
+
+def mita_forward_multi(Q, K, V, grid_h: int, grid_w: int, m: int, k: int, s: int, out=None, expert_idx=None,
+                       route=None, stream=None):
+    """MiTA with s routed experts per query, on device tensors. Returns (out,
+    expert_idx, route int32 [B,H,N,s], each query's landmarks highest first);
+    other arguments and results as mita_forward."""
+    import torch
+
+    B, H, N, d = _shape(Q, m, k, grid_h, grid_w)
+    for t, n in ((K, "K"), (V, "V")):
+        if tuple(t.shape) != (B, H, N, d):
+            raise ValueError(f"{n} must have the shape of Q")
+    out = torch.empty_like(Q) if out is None else out
+    expert_idx = torch.empty((B, H, m, k), dtype=torch.int32, device=Q.device) if expert_idx is None else expert_idx
+    route = torch.empty((B, H, N, s), dtype=torch.int32, device=Q.device) if route is None else route
+    if route.numel() != B * H * N * max(s, 0):
+        raise ValueError("route must hold B*H*N*s entries")
+    rc = load().mita_forward_multi(_dev_ptr(Q, "torch.bfloat16", "Q"), _dev_ptr(K, "torch.bfloat16", "K"),
+                                   _dev_ptr(V, "torch.bfloat16", "V"), B, H, N, d, grid_h, grid_w, m, k, s,
+                                   _dev_ptr(out, "torch.bfloat16", "out"),
+                                   _dev_ptr(expert_idx, "torch.int32", "expert_idx"),
+                                   _dev_ptr(route, "torch.int32", "route"), _stream(stream))
+    _raise(rc)
+    return out, expert_idx, route
 
 
 def mita_forward_noalloc(Q, K, V, grid_h: int, grid_w: int, m: int, k: int, out, expert_idx, route, stream=None):

@@ -67,8 +67,8 @@ __global__ void __launch_bounds__(GT) offsets_kernel(int m, int64_t N, int qtile
     }
 }
 
-__global__ void __launch_bounds__(SCT) scatter_kernel(const int32_t* __restrict__ route, int64_t N, int m,
-                                                      int64_t nblocks, int* __restrict__ cursor,
+__global__ void __launch_bounds__(SCT) scatter_kernel(const int32_t* __restrict__ route, int64_t N, int m, int s,
+                                                      int j, int64_t nblocks, int* __restrict__ cursor,
                                                       int* __restrict__ perm) {
     __shared__ int sh[MITA_MAX_M_INTERNAL];
     const int64_t blk = blockIdx.x % nblocks;
@@ -79,7 +79,7 @@ __global__ void __launch_bounds__(SCT) scatter_kernel(const int32_t* __restrict_
     const int64_t n0 = blk * (SCT * SQT) + threadIdx.x;
     int e[SQT], rank[SQT];
 #pragma unroll
-    for (int u = 0; u < SQT; ++u) e[u] = n0 + u * SCT < N ? route[bh * N + n0 + u * SCT] : -1;
+    for (int u = 0; u < SQT; ++u) e[u] = n0 + u * SCT < N ? route[(bh * N + n0 + u * SCT) * s + j] : -1;
 #pragma unroll
     for (int u = 0; u < SQT; ++u) rank[u] = e[u] >= 0 ? atomicAdd(&sh[e[u]], 1) : 0;
     __syncthreads();
@@ -93,12 +93,17 @@ __global__ void __launch_bounds__(SCT) scatter_kernel(const int32_t* __restrict_
 
 }  // namespace
 
-cudaError_t launch_group(const Plan& p, const Work& w, const int32_t* route, cudaStream_t st) {
-    offsets_kernel<<<static_cast<unsigned>(p.s.BH), GT, 0, st>>>(p.s.m, p.s.N, p.qtile, w.counts, w.expoff,
-                                                                 w.cursor, w.items, w.nitems);
+// Groups the queries by the j-th entry of their routes (route is [BH][N][s];
+// s = 1, j = 0 for one expert per query) into plane j of perm and items.
+cudaError_t launch_group(const Plan& p, const Work& w, const int32_t* route, int j, cudaStream_t st) {
+    const size_t mrows = static_cast<size_t>(p.s.BH) * p.s.m;
+    int* perm = w.perm + static_cast<size_t>(j) * p.s.BH * p.s.N;
+    int4* items = w.items + static_cast<size_t>(j) * p.s.BH * p.max_items;
+    offsets_kernel<<<static_cast<unsigned>(p.s.BH), GT, 0, st>>>(p.s.m, p.s.N, p.qtile, w.counts + j * mrows,
+                                                                 w.expoff, w.cursor, items, w.nitems + j);
     const int64_t nblocks = (p.s.N + SCT * SQT - 1) / (SCT * SQT);
-    scatter_kernel<<<static_cast<unsigned>(p.s.BH * nblocks), SCT, 0, st>>>(route, p.s.N, p.s.m, nblocks, w.cursor,
-                                                                            w.perm);
+    scatter_kernel<<<static_cast<unsigned>(p.s.BH * nblocks), SCT, 0, st>>>(route, p.s.N, p.s.m, p.s.s_route, j,
+                                                                            nblocks, w.cursor, perm);
     return cudaGetLastError();
 }
 

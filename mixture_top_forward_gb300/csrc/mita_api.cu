@@ -72,7 +72,7 @@ int check_shape(int B, int H, int N, int d, int gh, int gw, int m, int k, Shape*
     const int64_t BH = static_cast<int64_t>(B) * H;
     if (BH * N > (static_cast<int64_t>(1) << 40))
         return fail(MITA_ERR_UNSUPPORTED, "B*H*N=%lld is too large", static_cast<long long>(BH * N));
-    *s = Shape{BH, N, gh, gw, p, m, k};
+    *s = Shape{BH, N, gh, gw, p, m, k, 1};
     return MITA_OK;
 }
 
@@ -290,12 +290,13 @@ bool make_plan(const Shape& s, Plan* p, bool shared) {
     P.off_cand = take(cand * sizeof(uint64_t));
     P.off_ccount = take(cnts * sizeof(int));
     P.off_theta = take(BH * m * sizeof(uint64_t));
-    P.off_counts = take(BH * m * sizeof(int));
+    const size_t sr = static_cast<size_t>(s.s_route);  // one grouping plane per rank of the routes
+    P.off_counts = take(sr * BH * m * sizeof(int));
     P.off_expoff = take(BH * (m + 1) * sizeof(int));
     P.off_cursor = take(BH * m * sizeof(int));
-    P.off_perm = take(BH * static_cast<size_t>(s.N) * sizeof(int));
-    P.off_items = take(BH * static_cast<size_t>(P.max_items) * sizeof(int4));
-    P.off_nitems = take(sizeof(int));
+    P.off_perm = take(sr * BH * static_cast<size_t>(s.N) * sizeof(int));
+    P.off_items = take(sr * BH * static_cast<size_t>(P.max_items) * sizeof(int4));
+    P.off_nitems = take(sr * sizeof(int));
     size_t dense_floats = 0;  // the largest dense level's logits
     for (int l = 0; l < P.nlev; ++l)
         if (P.lev[l].dense) dense_floats = std::max(dense_floats, BH * m * static_cast<size_t>(P.lev[l].ld));
@@ -303,6 +304,7 @@ bool make_plan(const Shape& s, Plan* p, bool shared) {
     P.off_ridx = take(recs * sizeof(uint32_t));
     P.off_rval = take(recs * 8 * sizeof(float));
     P.off_rcount = take(recs ? cnts * sizeof(int) : 0);
+    P.off_state = take(expert_multi_state_bytes(P));
     P.total = off;
     if (P.max_items * s.BH > 0x7FFFFFFFLL || s.BH * P.nrblocks > 0x7FFFFFFFLL) return false;
     for (int l = 0; l < P.nlev; ++l)
@@ -333,6 +335,7 @@ Work carve(const Plan& p, void* base) {
     w.perm = reinterpret_cast<int*>(b + p.off_perm);
     w.items = reinterpret_cast<int4*>(b + p.off_items);
     w.nitems = reinterpret_cast<int*>(b + p.off_nitems);
+    w.state = reinterpret_cast<float*>(b + p.off_state);
     bool any_dense = false;
     for (int l = 0; l < p.nlev; ++l) any_dense = any_dense || p.lev[l].dense;
     w.dense = any_dense ? reinterpret_cast<float*>(b + p.off_dense) : nullptr;
@@ -386,8 +389,9 @@ int run_forward(const Plan& P, const Work& W, const __nv_bfloat16* Q, const __nv
                 float* lv_out, cudaStream_t st) {
     cudaError_t e;
     const size_t mrows = static_cast<size_t>(P.s.BH) * P.s.m;
-    if ((e = cudaMemsetAsync(W.counts, 0, mrows * sizeof(int), st)) != cudaSuccess ||
-        (e = cudaMemsetAsync(W.nitems, 0, sizeof(int), st)) != cudaSuccess)
+    const int sr = P.s.s_route;
+    if ((e = cudaMemsetAsync(W.counts, 0, sr * mrows * sizeof(int), st)) != cudaSuccess ||
+        (e = cudaMemsetAsync(W.nitems, 0, sr * sizeof(int), st)) != cudaSuccess)
         return cuda_fail(e, "cudaMemsetAsync");
     StageMarks marks(st);
     marks.mark(0);
@@ -410,14 +414,22 @@ int run_forward(const Plan& P, const Work& W, const __nv_bfloat16* Q, const __nv
     marks.mark(3);
     if ((e = launch_select(P, W, expert_idx, st)) != cudaSuccess) return cuda_fail(e, "expert selection launch");
     marks.mark(4);
-    if ((e = launch_route(P, W, Q, route, st)) != cudaSuccess) return cuda_fail(e, "routing launch");
+    e = sr > 1 ? launch_route_multi(P, W, Q, route, st) : launch_route(P, W, Q, route, st);
+    if (e != cudaSuccess) return cuda_fail(e, "routing launch");
     marks.mark(5);
-    if ((e = launch_group(P, W, route, st)) != cudaSuccess) return cuda_fail(e, "grouping launch");
+    for (int j = 0; j < sr; ++j)
+        if ((e = launch_group(P, W, route, j, st)) != cudaSuccess) return cuda_fail(e, "grouping launch");
     marks.mark(6);
-    if ((e = launch_expert(P, W, Q, K, V, expert_idx, out, st)) != cudaSuccess)
-        return cuda_fail(e, "expert attention launch");
+    if (sr == 1) {
+        if ((e = launch_expert(P, W, Q, K, V, expert_idx, out, st)) != cudaSuccess)
+            return cuda_fail(e, "expert attention launch");
+    } else {  // one pass per rank of the routes
+        for (int j = 0; j < sr; ++j)
+            if ((e = launch_expert_multi(P, W, Q, K, V, expert_idx, route, j, out, st)) != cudaSuccess)
+                return cuda_fail(e, "expert attention launch");
+    }
     marks.mark(7);
-    const int launches[kStages] = {1, P.scan_tc ? 2 * (P.nlev - 1) : 0, 1, 1, 1, 2, 1};
+    const int launches[kStages] = {1, P.scan_tc ? 2 * (P.nlev - 1) : 0, 1, 1, 1, 2 * sr, sr};
     marks.commit(launches);
     if (lq_out && (e = cudaMemcpyAsync(lq_out, W.lq32, mrows * D * sizeof(float), cudaMemcpyDeviceToDevice, st)) !=
                       cudaSuccess)
@@ -439,12 +451,15 @@ namespace {
 // ablation.
 int forward_device(const void* Q, const void* K, const void* V, int B, int H, int N, int d, int grid_h, int grid_w,
                    int m, int k, void* out, int32_t* expert_idx, int32_t* route, float* lq, float* lv, void* stream,
-                   bool shared) {
+                   bool shared, int s_route = 1) {
     g_err[0] = 0;
     Shape s;
     bool empty;
     int rc = check_shape(B, H, N, d, grid_h, grid_w, m, k, &s, &empty);
     if (rc != MITA_OK || empty) return rc;
+    if (s_route < 1 || s_route > m || s_route > MITA_MAX_S)
+        return fail(MITA_ERR_INVALID_ARG, "s=%d must be in [1, min(m=%d, MITA_MAX_S=%d)]", s_route, m, MITA_MAX_S);
+    s.s_route = s_route;
     if (!Q || !K || !V || !out || !expert_idx || !route)
         return fail(MITA_ERR_INVALID_ARG, "a required pointer is NULL");
     if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(out))
@@ -473,6 +488,13 @@ extern "C" int mita_forward_routed(const void* Q, const void* K, const void* V, 
                                    void* stream) {
     return forward_device(Q, K, V, B, H, N, d, grid_h, grid_w, m, k, out, expert_idx, route, nullptr, nullptr, stream,
                           false);
+}
+
+extern "C" int mita_forward_multi(const void* Q, const void* K, const void* V, int B, int H, int N, int d, int grid_h,
+                                  int grid_w, int m, int k, int s, void* out, int32_t* expert_idx, int32_t* route,
+                                  void* stream) {
+    return forward_device(Q, K, V, B, H, N, d, grid_h, grid_w, m, k, out, expert_idx, route, nullptr, nullptr, stream,
+                          true, s);
 }
 
 extern "C" int mita_forward(const void* Q, const void* K, const void* V, int B, int H, int N, int d, int grid_h,

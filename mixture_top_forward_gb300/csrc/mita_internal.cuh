@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "mita.h"
+
 // Largest m and k the kernels' shared-memory tables hold (the public limits
 // MITA_MAX_M / MITA_MAX_K in mita.h must not exceed these).
 #define MITA_MAX_M_INTERNAL 1024
@@ -23,6 +25,7 @@ struct Shape {
     int gh, gw;     // token grid (0,0 = 1-D)
     int p;          // landmark grid side for 2-D (m = p*p), 0 for 1-D
     int m, k;       // landmarks, keys per routed expert
+    int s_route;    // routed experts per query (s)
 };
 
 // One scan over (a sample of) every head's keys.
@@ -61,7 +64,7 @@ struct Plan {
     // workspace layout (byte offsets)
     size_t off_status, off_lq32, off_lqhi, off_lqlo, off_lv32, off_lvbf, off_part, off_cand, off_ccount, off_theta,
         off_counts, off_expoff, off_cursor, off_perm, off_items, off_nitems, off_dense, off_ridx, off_rval, off_rcount,
-        total;
+        off_state, total;
 };
 
 // Builds the plan; returns false if a size does not fit the int ranges used.
@@ -83,12 +86,13 @@ struct Work {
     int* rcount;            // [BH][chunks][m]
     uint64_t* theta;        // [BH][m] top-k thresholds from the pilot scans
     float* dense;           // [BH][m][dense_ld] raw logits <Lq_i, K_j> (dense top-k only)
-    int* counts;            // [BH][m] queries routed to each expert
+    int* counts;            // [s][BH][m] queries routed to each expert (per rank of the routes)
     int* expoff;            // [BH][m+1] exclusive prefix of counts
     int* cursor;            // [BH][m] scatter cursors
-    int* perm;              // [BH][N] queries grouped by expert
-    int4* items;            // [BH*max_items] flat list: (expert, start, len, head)
-    int* nitems;            // number of items in the flat list
+    int* perm;              // [s][BH][N] queries grouped by expert (rank j of the routes: plane j)
+    int4* items;            // [s][BH*max_items] flat lists: (expert, start, len, head)
+    int* nitems;            // [s] number of items in each flat list
+    float* state;           // [BH][N][68] running softmax state between the passes of s > 1 routing
 };
 
 Work carve(const Plan& p, void* base);
@@ -155,7 +159,13 @@ cudaError_t launch_route_simt(const Plan& p, const Work& w, const __nv_bfloat16*
                               cudaStream_t st);
 cudaError_t launch_route_tc(const Plan& p, const Work& w, const __nv_bfloat16* Q, int32_t* route, cudaStream_t st);
 bool route_tc_supported(const Plan& p);
-cudaError_t launch_group(const Plan& p, const Work& w, const int32_t* route, cudaStream_t st);
+cudaError_t launch_group(const Plan& p, const Work& w, const int32_t* route, int j, cudaStream_t st);
+cudaError_t launch_route_multi(const Plan& p, const Work& w, const __nv_bfloat16* Q, int32_t* route,
+                               cudaStream_t st);
+cudaError_t launch_expert_multi(const Plan& p, const Work& w, const __nv_bfloat16* Q, const __nv_bfloat16* K,
+                                const __nv_bfloat16* V, const int32_t* expert_idx, const int32_t* route, int j,
+                                __nv_bfloat16* out, cudaStream_t st);
+size_t expert_multi_state_bytes(const Plan& p);
 cudaError_t launch_expert(const Plan& p, const Work& w, const __nv_bfloat16* Q, const __nv_bfloat16* K,
                           const __nv_bfloat16* V, const int32_t* expert_idx, __nv_bfloat16* out, cudaStream_t st);
 cudaError_t launch_expert_simt(const Plan& p, const Work& w, const __nv_bfloat16* Q, const __nv_bfloat16* K,

@@ -5,7 +5,11 @@
   GPU set must still be a valid top-k: k distinct ascending indices whose
   smallest oracle logit is within 1e-3 of the largest logit left out.
 * Routes: identical wherever the oracle's top-2 margin is >= 1e-3; otherwise
-  the GPU's landmark must score within 1e-3 of the best.
+  the GPU's landmark must score within 1e-3 of the best. With s routed
+  experts per query: s distinct landmarks, the same set as the oracle's
+  wherever its s-th/(s+1)-th margin is >= 1e-3 (else every chosen landmark
+  within 1e-3 of every one left out), in descending order up to 1e-3, and in
+  the oracle's exact order wherever all its margins are >= 1e-3.
 * Outputs: compared with the oracle conditioned on the GPU's own routes and
   expert sets (so legal near-tie choices cost nothing): max-abs <= 2e-2 and
   mean-abs <= 2e-3 over all compared elements.
@@ -171,5 +175,95 @@ def sampled_parity(orc, q, k, v, gh, gw, m, kk, gpu, heads, queries_per_head, se
         check_routes(qs, lq_o, g_r[which], r_o, rg, which, rep)
         cond, ws = orc.attend(qs, lq_o, lv_o.reshape(1, 1, m, d), ks, vs, g_e.reshape(1, 1, m, kk),
                               g_r.reshape(1, 1, N), which=which, shared=shared)
+        check_outputs(out_rows(gpu["out"], bh * N + which), cond, rep)
+    return rep
+
+
+# ---------------------------------------------------------------------------
+# s routed experts per query
+# ---------------------------------------------------------------------------
+def run_gpu_multi(q, k, v, gh, gw, m, kk, s, full_out=True):
+    import torch
+
+    import mixture_top_forward_gb300 as M
+
+    Q, K, V = to_device(q), to_device(k), to_device(v)
+    out, eidx, route = M.mita_forward_multi(Q, K, V, gh, gw, m, kk, s)
+    torch.cuda.synchronize()
+    assert M.mita_sync_status() == 0
+    del Q, K, V
+    if full_out:
+        out = synth.bf16_to_f64(out.view(torch.int16).cpu().numpy().view(np.uint16))
+    return dict(out=out, expert_idx=eidx.cpu().numpy(), route=route.cpu().numpy())
+
+
+def check_routes_multi(q, lq_o, gpu_r, ora_r, rgap, which, report):
+    """gpu_r/ora_r [n, s] and rgap [n] indexed like `which` (global query ids)."""
+    d = q.shape[-1]
+    N = q.shape[-2]
+    qf = q.reshape(-1, d)
+    m = lq_o.shape[-2]
+    lqf = lq_o.reshape(-1, m, d)
+    n, s = gpu_r.shape
+    exact = near = 0
+    for t in range(n):
+        g, o = gpu_r[t], ora_r[t]
+        qi = which[t]
+        assert np.all((g >= 0) & (g < m)) and len(set(g.tolist())) == s, f"routes of query {qi} not {s} distinct"
+        lg = lqf[qi // N] @ synth.bf16_to_f64(qf[qi]) / np.sqrt(d)
+        assert np.all(np.diff(lg[g]) <= GAP), f"routes of query {qi} not in descending order"
+        if rgap[t] >= GAP:
+            assert set(g.tolist()) == set(o.tolist()), f"route set of query {qi} differs (margin {rgap[t]:.3g})"
+            if np.all(-np.diff(lg[o]) >= GAP):
+                assert np.array_equal(g, o), f"route order of query {qi} differs"
+            exact += 1
+        else:
+            out_mask = np.ones(m, bool)
+            out_mask[g] = False
+            best_out = lg[out_mask].max() if s < m else -np.inf
+            assert lg[g].min() >= best_out - GAP, f"routes of query {qi} are not a 1e-3 top-{s}"
+            near += 1
+    report["routes_exact"] = report.get("routes_exact", 0) + exact
+    report["routes_near_tie"] = report.get("routes_near_tie", 0) + near
+
+
+def full_parity_multi(orc, q, k, v, gh, gw, m, kk, s, gpu=None):
+    """Every element against the oracle's s-expert forward (small problems)."""
+    B, H, N, d = q.shape
+    BH = B * H
+    gpu = gpu or run_gpu_multi(q, k, v, gh, gw, m, kk, s)
+    ora = orc.forward_multi(q, k, v, gh, gw, m, kk, s)
+    rep = {}
+    lq_o = ora["lq"].reshape(BH, m, d)
+    check_experts(orc, lq_o, k.reshape(BH, N, d), gpu["expert_idx"].reshape(BH, m, kk),
+                  ora["expert_idx"].reshape(BH, m, kk), ora["gap"].reshape(BH, m), rep)
+    check_routes_multi(q, lq_o, gpu["route"].reshape(-1, s), ora["route"].reshape(-1, s), ora["rgap"].reshape(-1),
+                       np.arange(BH * N), rep)
+    cond, ws = orc.attend_multi(q, ora["lq"], ora["lv"], k, v, gpu["expert_idx"], gpu["route"])
+    assert np.max(np.abs(ws - 1.0)) < 1e-9
+    check_outputs(gpu["out"].reshape(BH, N, d), cond.reshape(BH, N, d), rep)
+    return rep
+
+
+def sampled_parity_multi(orc, q, k, v, gh, gw, m, kk, s, gpu, heads, queries_per_head, seed=0):
+    """Experts of a few heads in full; routes and outputs of sampled queries."""
+    B, H, N, d = q.shape
+    BH = B * H
+    rng = np.random.default_rng(seed)
+    rep = {"heads": list(map(int, heads))}
+    qf, kf, vf = q.reshape(BH, N, d), k.reshape(BH, N, d), v.reshape(BH, N, d)
+    for bh in heads:
+        qs, ks, vs = qf[bh:bh + 1][None], kf[bh:bh + 1][None], vf[bh:bh + 1][None]
+        lq_o = orc.landmarks(qs, gh, gw, m)
+        lv_o, e_o, gap = orc.scan(lq_o, ks, vs, kk)
+        g_e = gpu["expert_idx"].reshape(BH, m, kk)[bh:bh + 1]
+        check_experts(orc, lq_o.reshape(1, m, d), ks.reshape(1, N, d), g_e, e_o, gap, rep)
+        n_s = min(N, queries_per_head)
+        which = np.sort(rng.choice(N, size=n_s, replace=False)) if n_s < N else np.arange(N)
+        r_o, rg = orc.route_multi(qs, lq_o, s, which=which)
+        g_r = gpu["route"].reshape(BH, N, s)[bh]
+        check_routes_multi(qs, lq_o, g_r[which], r_o, rg, which, rep)
+        cond, ws = orc.attend_multi(qs, lq_o, lv_o.reshape(1, 1, m, d), ks, vs, g_e.reshape(1, 1, m, kk),
+                                    g_r.reshape(1, 1, N, s), which=which)
         check_outputs(out_rows(gpu["out"], bh * N + which), cond, rep)
     return rep

@@ -152,6 +152,68 @@ def test_full_attention_comparator(orc, name):
     print(name, rep)
 
 
+@pytest.mark.parametrize("name,s", [("tiny", 2), ("deit", 2), ("seg1024", 3)])
+def test_multi_config_full_oracle(orc, name, s):
+    q, k, v = synth.make_inputs(name)
+    rep = parity.full_parity_multi(orc, q, k, v, *_cfg_args(name), s)
+    print(name, s, rep)
+
+
+@pytest.mark.parametrize("name,s,heads,nq", [
+    ("long64k", 2, (0, 7), 4096),
+    ("long1m", 2, (3,), 4096),
+])
+def test_multi_config_sampled(orc, name, s, heads, nq):
+    q, k, v = synth.make_inputs(name)
+    args = _cfg_args(name)
+    gpu = parity.run_gpu_multi(q, k, v, *args, s, full_out=False)
+    rep = parity.sampled_parity_multi(orc, q, k, v, *args, s, gpu, heads, nq)
+    print(name, rep)
+
+
+@pytest.mark.parametrize("B,H,N,gh,gw,m,k,s", [
+    (2, 3, 1000, 0, 0, 7, 13, 3),      # ragged windows and tiles
+    (1, 2, 196, 14, 14, 25, 196, 2),   # k = N: both experts hold every key (all duplicates)
+    (2, 2, 300, 0, 0, 4, 5, 4),        # s = m: every expert for every query
+    (1, 1, 1, 0, 0, 1, 1, 1),          # a single token
+    (3, 1, 2500, 50, 50, 16, 1024, 2), # k = MITA_MAX_K
+    (1, 2, 5000, 0, 0, 300, 70, 8),    # s = MITA_MAX_S, several landmark tiles
+])
+def test_multi_edge_shapes(orc, B, H, N, gh, gw, m, k, s):
+    q, kk_, v = _rand(B, H, N, 500 + N + m + k + s, 2.0)
+    rep = parity.full_parity_multi(orc, q, kk_, v, gh, gw, m, k, s)
+    print(rep)
+
+
+def test_multi_s1_is_mita():
+    """s = 1 through the s-expert entry point is the one-expert forward pass."""
+    import torch
+
+    import mixture_top_forward_gb300 as M
+
+    q, k, v = synth.make_inputs("seg1024")
+    Q, K, V = parity.to_device(q), parity.to_device(k), parity.to_device(v)
+    a = M.mita_forward(Q, K, V, 32, 32, 49, 49)
+    b = M.mita_forward_multi(Q, K, V, 32, 32, 49, 49, 1)
+    torch.cuda.synchronize()
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1]) and torch.equal(a[2], b[2].reshape(a[2].shape))
+
+
+def test_multi_rejects_bad_s():
+    import torch
+
+    import mixture_top_forward_gb300 as M
+
+    Q = torch.zeros((1, 1, 64, 64), dtype=torch.bfloat16, device="cuda")
+    for s in (0, 5, M_MAX_S + 1):
+        with pytest.raises(M.MitaError) as ei:
+            M.mita_forward_multi(Q, Q, Q, 0, 0, 4 if s == 5 else 16, 8, s)
+        assert ei.value.code == M.MITA_ERR_INVALID_ARG
+
+
+M_MAX_S = 8  # MITA_MAX_S in mita.h
+
+
 def test_ascending_scores_force_compaction(orc):
     """Scores that grow along the sequence make every key beat the running
     threshold, so every chunk buffer overflows and compacts repeatedly."""
