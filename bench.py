@@ -342,7 +342,7 @@ def run_gpu(args, rank, world):
     if rank == 0 and not args.no_sweep:
         res["sweep"] = sweep(args, M, dev, stream, peaks)
         res["routed_only"] = routed_only(args, M, dev, stream, peaks)
-        res["multi_expert"] = multi_expert(args, M, dev, stream)
+        res["multi_expert"] = multi_expert(args, M, dev, stream, peaks)
         mita_ms = {n: r["ms_per_step"] for n, r in res["sweep"].items()}
         mita_ms[name] = ms_step
         res["full_attention"] = full_attention(args, dev, stream, mita_ms)
@@ -456,16 +456,11 @@ def routed_only(args, M, dev, stream, peaks):
             "stage_ms": stage_ms}
 
 
-# fp32 FMA peak of the CUDA cores: 152 SMs x 128 FMA lanes x 2 FLOP x 2.07 GHz
-# (the clock the bench's clock record shows under load)
-SIMT_FP32_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
-
-
-def multi_expert(args, M, dev, stream, s=2):
+def multi_expert(args, M, dev, stream, peaks, s=2):
     """s routed experts per query on the timed workload (device-resident
-    inputs; the attention passes run on the CUDA cores). The expert stage's
-    FLOPs count s*k routed keys per query, an upper bound (a key shared by
-    two chosen experts is attended once)."""
+    inputs; one tensor-core attention pass per rank of the routes). The
+    expert stage's FLOPs count s*k routed keys per query, an upper bound (a
+    key shared by two chosen experts is attended once)."""
     import torch
 
     c = synth.CONFIGS[args.config]
@@ -499,9 +494,10 @@ def multi_expert(args, M, dev, stream, s=2):
     exp_tf = exp_flops / (stage_ms["expert"] / 1e3) / 1e12
     del Q, K, V, out
     torch.cuda.empty_cache()
+    pk = peaks["bf16_tflops_sustained"]
     return {"s": s, "queries_per_s": BH * N / (ms / 1e3), "ms_per_step": ms, "stage_ms": stage_ms,
-            "expert": {"bound": "alu", "achieved": exp_tf, "peak": SIMT_FP32_TFLOPS, "unit": "TFLOP/s",
-                       "frac": exp_tf / SIMT_FP32_TFLOPS, "flops": "4 N (m + s k) d per head (upper bound)"}}
+            "expert": {"bound": "tensor", "achieved": exp_tf, "peak": pk, "unit": "TFLOP/s", "frac": exp_tf / pk,
+                       "flops": "4 N (m + s k) d per head (upper bound)"}}
 
 
 # ---------------------------------------------------------------------------

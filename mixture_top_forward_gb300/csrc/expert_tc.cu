@@ -41,6 +41,16 @@
 // consumes; row warps arrive once each (4-arrival barriers) and make
 // their waits warp-uniform, so no named barrier can block forever. Every
 // wait is bounded (umma.cuh).
+//
+// s routed experts per query (MULTI; the pages' setting is s = 1): one launch
+// per rank j of the routes, over the queries grouped by their j-th expert.
+// Pass 0 takes the shared pairs and the expert's keys, later passes the
+// expert's keys alone, with the keys an earlier-ranked expert of the query
+// already held masked out (their logits set to -inf, from the expert overlap
+// table), so the union of the s experts enters the softmax once. Each pass
+// runs its own online softmax; the epilogue merges it with the query's fp32
+// state row of the earlier passes (log-sum-exp merge of (max, sum, O)) and
+// either stores the merged state or, in the last pass, the normalised output.
 #include "tensormap.cuh"
 #include "umma.cuh"
 
@@ -74,7 +84,11 @@ struct Args {
     __nv_bfloat16* out;
     int* status;
     int64_t N;
-    int m, msh, k, nblk;  // msh: shared pairs taken (m, or 0 for the routing-only ablation)
+    int m, msh, k, nblk;  // msh: shared pairs taken (m, or 0 for the routing-only ablation / passes j > 0)
+    // s > 1 routing (MULTI): this launch is the pass of rank j of s
+    const uint64_t* mask;  // j > 0: [BH][N][nbw] per grouping slot, bit c of word b: key c of block b counted before
+    float* state;          // [BH][N][68]: O[64] (unnormalised), max (log2 units), sum
+    int s, j, nbw;
 };
 
 struct Layout {
@@ -152,6 +166,7 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     return *reinterpret_cast<uint32_t*>(&h);
 }
 
+template <bool MULTI>
 __global__ void __launch_bounds__(NT, 1)
     expert_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                      const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tlq,
@@ -339,27 +354,80 @@ __global__ void __launch_bounds__(NT, 1)
         bool pend = false, pend_row = false;  // an item whose epilogue is pending
         float pend_inv = 0.f;
         uint4* pend_dst = nullptr;
+        float pend_m = 0.f, pend_l = 0.f;  // MULTI: the pass's running max and sum
+        float* pend_state = nullptr;       // MULTI: the query's state row
         auto epilogue = [&]() {
+            if constexpr (!MULTI) {
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {  // two 32-column halves of the output row
-                float o[32];
-                tmem_ld32(tO + h * 32, o);
-                tmem_ld_wait();
-                if (h == 1) {
-                    tc_fence_before();
-                    warp_arrive(&ofree[w]);
-                }
-                if (pend_row) {
+                for (int h = 0; h < 2; ++h) {  // two 32-column halves of the output row
+                    float o[32];
+                    tmem_ld32(tO + h * 32, o);
+                    tmem_ld_wait();
+                    if (h == 1) {
+                        tc_fence_before();
+                        warp_arrive(&ofree[w]);
+                    }
+                    if (pend_row) {
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        uint4 q;
-                        q.x = pack_bf16(o[8 * c + 0] * pend_inv, o[8 * c + 1] * pend_inv);
-                        q.y = pack_bf16(o[8 * c + 2] * pend_inv, o[8 * c + 3] * pend_inv);
-                        q.z = pack_bf16(o[8 * c + 4] * pend_inv, o[8 * c + 5] * pend_inv);
-                        q.w = pack_bf16(o[8 * c + 6] * pend_inv, o[8 * c + 7] * pend_inv);
-                        pend_dst[h * 4 + c] = q;
+                        for (int c = 0; c < 4; ++c) {
+                            uint4 q;
+                            q.x = pack_bf16(o[8 * c + 0] * pend_inv, o[8 * c + 1] * pend_inv);
+                            q.y = pack_bf16(o[8 * c + 2] * pend_inv, o[8 * c + 3] * pend_inv);
+                            q.z = pack_bf16(o[8 * c + 4] * pend_inv, o[8 * c + 5] * pend_inv);
+                            q.w = pack_bf16(o[8 * c + 6] * pend_inv, o[8 * c + 7] * pend_inv);
+                            pend_dst[h * 4 + c] = q;
+                        }
                     }
                 }
+            } else {
+                // merge (pend_m, pend_l, O of this pass) with the state of the
+                // earlier passes (none in pass 0); max -inf: nothing there
+                float ms = -INFINITY, ls = 0.f;
+                if (pend_row && a.j > 0) {
+                    const float2 ml = *reinterpret_cast<const float2*>(pend_state + D);
+                    ms = ml.x;
+                    ls = ml.y;
+                }
+                const float mt = fmaxf(ms, pend_m);
+                const float fs = ms == -INFINITY ? 0.f : exp2f(ms - mt);
+                const float fp = pend_m == -INFINITY ? 0.f : exp2f(pend_m - mt);
+                const float lt = ls * fs + pend_l * fp;
+                const bool last = a.j == a.s - 1;
+                const float inv = last ? 1.f / lt : 1.f;
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    float o[32];
+                    tmem_ld32(tO + h * 32, o);
+                    tmem_ld_wait();
+                    if (h == 1) {
+                        tc_fence_before();
+                        warp_arrive(&ofree[w]);
+                    }
+                    if (pend_row) {
+                        float4* sr = reinterpret_cast<float4*>(pend_state + h * 32);
+#pragma unroll
+                        for (int c = 0; c < 8; ++c) {
+                            float4 x = make_float4(o[4 * c] * fp, o[4 * c + 1] * fp, o[4 * c + 2] * fp,
+                                                   o[4 * c + 3] * fp);
+                            if (a.j > 0) {
+                                const float4 y = sr[c];
+                                x.x = fmaf(y.x, fs, x.x);
+                                x.y = fmaf(y.y, fs, x.y);
+                                x.z = fmaf(y.z, fs, x.z);
+                                x.w = fmaf(y.w, fs, x.w);
+                            }
+                            if (last) {
+                                uint2 q;
+                                q.x = pack_bf16(x.x * inv, x.y * inv);
+                                q.y = pack_bf16(x.z * inv, x.w * inv);
+                                reinterpret_cast<uint2*>(pend_dst)[h * 8 + c] = q;
+                            } else {
+                                sr[c] = x;
+                            }
+                        }
+                    }
+                }
+                if (pend_row && !last) *reinterpret_cast<float2*>(pend_state + D) = make_float2(mt, lt);
             }
             pend = false;
         };
@@ -372,7 +440,32 @@ __global__ void __launch_bounds__(NT, 1)
             const int64_t bh = item.w;
             const int n = t < item.z ? a.perm[bh * a.N + item.y + t] : 0;
             float mrun = -INFINITY, lrun = 0.f;
+            float* srow = nullptr;
+            const uint64_t* mrow = nullptr;  // MULTI, passes j > 0: this row's masks, one word per block
+            uint64_t dm0 = 0;                // the word of the next block (first: loaded with the item)
+            if constexpr (MULTI) {
+                if (a.j > 0 && t < item.z) {
+                    mrow = a.mask + (bh * a.N + item.y + t) * static_cast<int64_t>(a.nbw);
+                    dm0 = mrow[0];
+                }
+                srow = a.state + (bh * a.N + n) * 68;
+                if (a.j > 0 && t < item.z) {  // the epilogue reads it: start bringing it in
+                    const char* p0 = reinterpret_cast<const char*>(srow);
+#pragma unroll
+                    for (int x = 0; x < 4; ++x)
+                        asm volatile("prefetch.global.L2 [%0];" ::"l"(p0 + (x < 3 ? 128 * x : 271)));
+                }
+            }
             for (int j = 0; j < a.nblk; ++j, ++gb) {
+                // MULTI, passes j > 0: the block's keys an earlier-ranked expert
+                // of the query holds (bit c: key column c)
+                uint64_t dm = 0;
+                if constexpr (MULTI) {
+                    if (mrow) {  // this block's word; the next one loads during this block
+                        dm = dm0;
+                        if (j + 1 < a.nblk) dm0 = mrow[j + 1];
+                    }
+                }
                 ok = __all_sync(0xffffffffu, mbar_wait(&sfull[w], gb & 1, a.status));
                 if (!ok) break;
                 tc_fence_after();
@@ -392,6 +485,12 @@ __global__ void __launch_bounds__(NT, 1)
                         s[c] = (g >= nkeys || (g >= msh && g < m4)) ? -INFINITY : s[c];
                     }
                 }
+                if constexpr (MULTI) {
+                    if (dm) {
+#pragma unroll
+                        for (int c = 0; c < KB; ++c) s[c] = ((dm >> c) & 1) ? -INFINITY : s[c];
+                    }
+                }
                 // 8 independent partial maxima: short dependency chains
                 float pm[8];
                 static_assert(KB == 64, "the partial maxima below cover exactly 64 columns");
@@ -402,16 +501,19 @@ __global__ void __launch_bounds__(NT, 1)
                 const float smax = fmaxf(fmax3(pm[0], pm[1], pm[2]), fmax3(fmax3(pm[3], pm[4], pm[5]), pm[6], pm[7]));
                 const float bmax = smax * kC;
                 const float mnew = (bmax > mrun + kLazy) ? bmax : mrun;
-                const float alpha = exp2f(mrun - mnew);  // 0 on the first block, 1 when the max is kept
+                // 0 on the first block, 1 when the max is kept. MULTI: a row
+                // may have no key yet (max -inf): then every weight is 0
+                const float alpha = (MULTI && mnew == -INFINITY) ? 1.f : exp2f(mrun - mnew);
+                const float mexp = (MULTI && mnew == -INFINITY) ? 0.f : mnew;
                 // The P.V product sees the weights rounded to bf16, the row sum
                 // below adds them unrounded; the block's largest weight
                 // dominates the difference, so the sum takes its rounding
                 // (computed exactly as in the loop: same fused multiply-add).
-                const float emax = exp2f(fmaf(smax, kC, -mnew));
+                const float emax = exp2f(fmaf(smax, kC, -mexp));
                 const float corr = __bfloat162float(__float2bfloat16_rn(emax)) - emax;
                 // packed pairs: one f32x2 FMA forms two exponents, one f32x2 add
                 // accumulates two weights; P goes out as bf16 pairs
-                const float2 c2 = make_float2(kC, kC), m2 = make_float2(-mnew, -mnew);
+                const float2 c2 = make_float2(kC, kC), m2 = make_float2(-mexp, -mexp);
                 float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                                  make_float2(0.f, 0.f)};
                 uint32_t pk[KB / 2];
@@ -445,6 +547,9 @@ __global__ void __launch_bounds__(NT, 1)
             pend_row = t < item.z;
             pend_inv = 1.f / lrun;
             pend_dst = reinterpret_cast<uint4*>(a.out + (bh * a.N + n) * D);
+            pend_m = mrun;
+            pend_l = lrun;
+            pend_state = srow;
         }
         if (ok && pend) {  // the last item: wait for its last P.V
             ok = __all_sync(0xffffffffu, mbar_wait(&pvdone[w], (gb - 1) & 1, a.status));
@@ -471,30 +576,37 @@ bool expert_tc_supported(const Plan& p) {
 }
 
 cudaError_t launch_expert_tc(const Plan& p, const Work& w, const __nv_bfloat16* Q, const __nv_bfloat16* K,
-                             const __nv_bfloat16* V, const int32_t* expert_idx, __nv_bfloat16* out,
-                             cudaStream_t st) {
+                             const __nv_bfloat16* V, const int32_t* expert_idx, __nv_bfloat16* out, cudaStream_t st,
+                             const int32_t* route, int j) {
+    (void)route;  // the passes read the per-slot masks built from it
+    const bool multi = p.s.s_route > 1;
     Args a;
-    a.items = w.items;
-    a.nitems = w.nitems;
-    a.perm = w.perm;
+    a.items = w.items + static_cast<size_t>(j) * p.s.BH * p.max_items;  // the plane of rank j
+    a.nitems = w.nitems + j;
+    a.perm = w.perm + static_cast<size_t>(j) * p.s.BH * p.s.N;
     a.expert_idx = expert_idx;
     a.out = out;
     a.status = w.status;
     a.N = p.s.N;
     a.m = p.s.m;
-    a.msh = p.shared ? p.s.m : 0;
+    a.msh = p.shared && j == 0 ? p.s.m : 0;
     a.k = p.s.k;
-    a.nblk = (key_rows(p) + KB - 1) / KB;
+    a.nblk = ((a.msh + 3) / 4 * 4 + a.k + KB - 1) / KB;
+    a.mask = j > 0 ? w.mask + static_cast<size_t>(j - 1) * p.s.BH * p.s.N * ((p.s.k + 63) / 64) : nullptr;
+    a.state = w.state;
+    a.s = p.s.s_route;
+    a.j = j;
+    a.nbw = (p.s.k + 63) / 64;
     CUtensorMap tq, tk, tv, tlq, tlv;
     const uint64_t rows = static_cast<uint64_t>(p.s.BH) * p.s.N, lrows = static_cast<uint64_t>(p.s.BH) * p.s.m;
     if (!make_row_tmap(&tq, Q, rows, 1) || !make_row_tmap(&tk, K, rows, 1) || !make_row_tmap(&tv, V, rows, 1) ||
         !make_row_tmap(&tlq, w.lqhi, lrows, 1) || !make_row_tmap(&tlv, w.lvbf, lrows, 1))
         return cudaErrorInvalidValue;
     const size_t sm = smem_bytes(a.nblk);
-    cudaError_t e = cudaFuncSetAttribute(expert_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(sm));
+    auto kern = multi ? expert_tc_kernel<true> : expert_tc_kernel<false>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(sm));
     if (e != cudaSuccess) return e;
-    expert_tc_kernel<<<device_sms(), NT, sm, st>>>(tq, tk, tv, tlq, tlv, a);
+    kern<<<device_sms(), NT, sm, st>>>(tq, tk, tv, tlq, tlv, a);
     return cudaGetLastError();
 }
 

@@ -134,7 +134,8 @@ int device_sms() {
 }
 
 cudaError_t launch_route(const Plan& p, const Work& w, const __nv_bfloat16* Q, int32_t* route, cudaStream_t st) {
-    if (route_tc_supported(p)) return launch_route_tc(p, w, Q, route, st);
+    if (route_tc_supported(p)) return launch_route_tc(p, w, Q, route, st);  // any s
+    if (p.s.s_route > 1) return launch_route_multi(p, w, Q, route, st);
     return launch_route_simt(p, w, Q, route, st);
 }
 
@@ -305,6 +306,12 @@ bool make_plan(const Shape& s, Plan* p, bool shared) {
     P.off_rval = take(recs * 8 * sizeof(float));
     P.off_rcount = take(recs ? cnts * sizeof(int) : 0);
     P.off_state = take(expert_multi_state_bytes(P));
+    // s > 1: tensor-core passes where the one-expert kernel applies (same
+    // conditions as launch_expert) and the overlap table stays below 1 GB
+    P.multi_tc = s.s_route > 1 && expert_tc_supported(P) && s.N >= 32LL * s.m && s.m <= 256 &&
+                 overlap_bytes(s) <= (size_t(1) << 30) && pass_mask_bytes(s) <= (size_t(4) << 30);
+    P.off_ovl = take(P.multi_tc ? overlap_bytes(s) : 0);
+    P.off_mask = take(P.multi_tc ? pass_mask_bytes(s) : 0);
     P.total = off;
     if (P.max_items * s.BH > 0x7FFFFFFFLL || s.BH * P.nrblocks > 0x7FFFFFFFLL) return false;
     for (int l = 0; l < P.nlev; ++l)
@@ -336,6 +343,8 @@ Work carve(const Plan& p, void* base) {
     w.items = reinterpret_cast<int4*>(b + p.off_items);
     w.nitems = reinterpret_cast<int*>(b + p.off_nitems);
     w.state = reinterpret_cast<float*>(b + p.off_state);
+    w.ovl = reinterpret_cast<uint64_t*>(b + p.off_ovl);
+    w.mask = reinterpret_cast<uint64_t*>(b + p.off_mask);
     bool any_dense = false;
     for (int l = 0; l < p.nlev; ++l) any_dense = any_dense || p.lev[l].dense;
     w.dense = any_dense ? reinterpret_cast<float*>(b + p.off_dense) : nullptr;
@@ -414,22 +423,25 @@ int run_forward(const Plan& P, const Work& W, const __nv_bfloat16* Q, const __nv
     marks.mark(3);
     if ((e = launch_select(P, W, expert_idx, st)) != cudaSuccess) return cuda_fail(e, "expert selection launch");
     marks.mark(4);
-    e = sr > 1 ? launch_route_multi(P, W, Q, route, st) : launch_route(P, W, Q, route, st);
-    if (e != cudaSuccess) return cuda_fail(e, "routing launch");
+    if ((e = launch_route(P, W, Q, route, st)) != cudaSuccess) return cuda_fail(e, "routing launch");
     marks.mark(5);
     for (int j = 0; j < sr; ++j)
         if ((e = launch_group(P, W, route, j, st)) != cudaSuccess) return cuda_fail(e, "grouping launch");
+    if (P.multi_tc && (e = launch_overlap(P, W, expert_idx, route, st)) != cudaSuccess)
+        return cuda_fail(e, "expert overlap launch");
     marks.mark(6);
     if (sr == 1) {
         if ((e = launch_expert(P, W, Q, K, V, expert_idx, out, st)) != cudaSuccess)
             return cuda_fail(e, "expert attention launch");
     } else {  // one pass per rank of the routes
-        for (int j = 0; j < sr; ++j)
-            if ((e = launch_expert_multi(P, W, Q, K, V, expert_idx, route, j, out, st)) != cudaSuccess)
-                return cuda_fail(e, "expert attention launch");
+        for (int j = 0; j < sr; ++j) {
+            e = P.multi_tc ? launch_expert_tc(P, W, Q, K, V, expert_idx, out, st, route, j)
+                           : launch_expert_multi(P, W, Q, K, V, expert_idx, route, j, out, st);
+            if (e != cudaSuccess) return cuda_fail(e, "expert attention launch");
+        }
     }
     marks.mark(7);
-    const int launches[kStages] = {1, P.scan_tc ? 2 * (P.nlev - 1) : 0, 1, 1, 1, 2 * sr, sr};
+    const int launches[kStages] = {1, P.scan_tc ? 2 * (P.nlev - 1) : 0, 1, 1, 1, 2 * sr + (P.multi_tc ? sr : 0), sr};
     marks.commit(launches);
     if (lq_out && (e = cudaMemcpyAsync(lq_out, W.lq32, mrows * D * sizeof(float), cudaMemcpyDeviceToDevice, st)) !=
                       cudaSuccess)

@@ -61,10 +61,13 @@ struct Plan {
     // expert attention
     int qtile;          // queries per expert work item
     int64_t max_items;  // work items per head, upper bound
+    // s > 1 routing: the attention passes run on the tensor cores (with the
+    // expert overlap table) or, where that kernel does not apply, on the CUDA cores
+    bool multi_tc;
     // workspace layout (byte offsets)
     size_t off_status, off_lq32, off_lqhi, off_lqlo, off_lv32, off_lvbf, off_part, off_cand, off_ccount, off_theta,
         off_counts, off_expoff, off_cursor, off_perm, off_items, off_nitems, off_dense, off_ridx, off_rval, off_rcount,
-        off_state, total;
+        off_state, off_ovl, off_mask, total;
 };
 
 // Builds the plan; returns false if a size does not fit the int ranges used.
@@ -93,6 +96,8 @@ struct Work {
     int4* items;            // [s][BH*max_items] flat lists: (expert, start, len, head)
     int* nitems;            // [s] number of items in each flat list
     float* state;           // [BH][N][68] running softmax state between the passes of s > 1 routing
+    uint64_t* ovl;          // [BH][m][m][ceil(k/64)] expert overlap bit masks (s > 1, tensor cores)
+    uint64_t* mask;         // [s-1][BH][N][ceil(k/64)] per grouping slot of ranks 1..s-1: keys already counted
 };
 
 Work carve(const Plan& p, void* base);
@@ -166,14 +171,19 @@ cudaError_t launch_expert_multi(const Plan& p, const Work& w, const __nv_bfloat1
                                 const __nv_bfloat16* V, const int32_t* expert_idx, const int32_t* route, int j,
                                 __nv_bfloat16* out, cudaStream_t st);
 size_t expert_multi_state_bytes(const Plan& p);
+size_t overlap_bytes(const Shape& s);
+size_t pass_mask_bytes(const Shape& s);
+cudaError_t launch_overlap(const Plan& p, const Work& w, const int32_t* expert_idx, const int32_t* route,
+                           cudaStream_t st);
 cudaError_t launch_expert(const Plan& p, const Work& w, const __nv_bfloat16* Q, const __nv_bfloat16* K,
                           const __nv_bfloat16* V, const int32_t* expert_idx, __nv_bfloat16* out, cudaStream_t st);
 cudaError_t launch_expert_simt(const Plan& p, const Work& w, const __nv_bfloat16* Q, const __nv_bfloat16* K,
                                const __nv_bfloat16* V, const int32_t* expert_idx, __nv_bfloat16* out,
                                cudaStream_t st);
+// route/j: s > 1 routing, the pass of rank j (route is [BH][N][s]); s = 1: nullptr, 0
 cudaError_t launch_expert_tc(const Plan& p, const Work& w, const __nv_bfloat16* Q, const __nv_bfloat16* K,
-                             const __nv_bfloat16* V, const int32_t* expert_idx, __nv_bfloat16* out,
-                             cudaStream_t st);
+                             const __nv_bfloat16* V, const int32_t* expert_idx, __nv_bfloat16* out, cudaStream_t st,
+                             const int32_t* route = nullptr, int j = 0);
 bool expert_tc_supported(const Plan& p);
 
 // Number of SMs of the current device (cached per device).

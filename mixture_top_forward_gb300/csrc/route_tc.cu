@@ -19,6 +19,10 @@
 //                  per thread, argmax over the m logits, the route, and a
 //                  shared-memory histogram (one per warpgroup) of the head's
 //                  routes that is added to the per-head expert counts.
+// With s routed experts per query (MULTI; the pages' setting is s = 1, the
+// general form takes the s highest logits, highest first, ties to the lower
+// landmark) each row keeps its s best (logit, landmark) pairs as a sorted
+// list instead of the argmax, and the histograms count per rank of the list.
 // Every wait is bounded (umma.cuh).
 #include <algorithm>
 
@@ -37,22 +41,24 @@ constexpr size_t OFF_Q = 65536;
 constexpr size_t SMEM = OFF_Q + QST * 16384 + 1024;
 
 struct RouteArgs {
-    int32_t* route;
-    int* counts;
+    int32_t* route;  // [BH][N][s]
+    int* counts;     // [s][BH][m]
     int* status;
-    int64_t N, tiles_per_head, total_tiles;
-    int m, m_pad;
+    int64_t N, BH, tiles_per_head, total_tiles;
+    int m, m_pad, s;
 };
 
 constexpr int RT_THREADS = 352;  // warps 0-3 and 5-8: argmax groups; 4: loads; 9, 10: MMA issuers
 
+template <bool MULTI>
 __global__ void __launch_bounds__(RT_THREADS, 1) route_tc_kernel(const __grid_constant__ CUtensorMap tq,
                                                           const __grid_constant__ CUtensorMap thi,
                                                           const __grid_constant__ CUtensorMap tlo, RouteArgs a) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ uint64_t qfull[QST], qempty[QST], dfull[2], dfree[2], lqfull, lqfree;
     __shared__ uint32_t tmem_base;
-    __shared__ int hist[2][256];
+    constexpr int HS = MULTI ? MITA_MAX_S : 1;  // histogram planes (ranks)
+    __shared__ int hist[2][HS][256];
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int64_t t0 = a.total_tiles * blockIdx.x / gridDim.x;
@@ -72,7 +78,7 @@ __global__ void __launch_bounds__(RT_THREADS, 1) route_tc_kernel(const __grid_co
         mbar_init(&lqfree, 2);  // one commit per MMA issuer
         fence_barrier_init();
     }
-    for (int e = tid; e < 512; e += blockDim.x) hist[e >> 8][e & 255] = 0;
+    for (int e = tid; e < 2 * HS * 256; e += blockDim.x) (&hist[0][0][0])[e] = 0;
     if (warp == 0) tmem_alloc(&tmem_base, 512);
     tc_fence_before();
     __syncthreads();
@@ -149,7 +155,8 @@ __global__ void __launch_bounds__(RT_THREADS, 1) route_tc_kernel(const __grid_co
         const int b = warp < 4 ? 0 : 1;
         const int row = (warp & 3) * 32 + lane;  // TMEM lane quarter = warp % 4
         const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-        int* h = hist[b];
+        int(*h)[256] = hist[b];
+        const int ns = MULTI ? a.s : 1;
         int64_t cur = -1;
         for (int t = b; t < nt; t += 2) {
             const int64_t g = t0 + t;
@@ -157,58 +164,121 @@ __global__ void __launch_bounds__(RT_THREADS, 1) route_tc_kernel(const __grid_co
             if (bh != cur) {
                 named_bar(1 + b, 128);
                 if (cur >= 0)
-                    for (int e = row; e < a.m; e += 128)
-                        if (h[e]) atomicAdd(&a.counts[cur * a.m + e], h[e]);
+                    for (int j = 0; j < ns; ++j)
+                        for (int e = row; e < a.m; e += 128)
+                            if (h[j][e]) atomicAdd(&a.counts[(j * a.BH + cur) * a.m + e], h[j][e]);
                 named_bar(1 + b, 128);
-                for (int e = row; e < a.m; e += 128) h[e] = 0;
+                for (int j = 0; j < ns; ++j)
+                    for (int e = row; e < a.m; e += 128) h[j][e] = 0;
                 named_bar(1 + b, 128);
                 cur = bh;
             }
             if (!named_bar_and(1 + b, 128, mbar_wait(&dfull[b], (t >> 1) & 1, a.status))) break;
             tc_fence_after();
             const uint32_t d = tb + b * 256 + lane_off;
-            // 4 interleaved (value, index) chains; on equal values the lower
-            // index wins, as in a left-to-right scan with a strict comparison
-            float bv[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-            int bi[4] = {0, 1, 2, 3};
-            for (int c0 = 0; c0 < a.m_pad; c0 += 32) {
-                float v[32];
-                tmem_ld32(d + c0, v);
-                tmem_ld_wait();
-                if (c0 + 32 > a.m) {  // (uniform) the last chunk: columns past m are another head's
+            const int64_t n = tile * 128 + row;
+            if constexpr (!MULTI) {
+                // 4 interleaved (value, index) chains; on equal values the lower
+                // index wins, as in a left-to-right scan with a strict comparison
+                float bv[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+                int bi[4] = {0, 1, 2, 3};
+                for (int c0 = 0; c0 < a.m_pad; c0 += 32) {
+                    float v[32];
+                    tmem_ld32(d + c0, v);
+                    tmem_ld_wait();
+                    if (c0 + 32 > a.m) {  // (uniform) the last chunk: columns past m are another head's
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) v[j] = c0 + j < a.m ? v[j] : -INFINITY;
-                }
+                        for (int j = 0; j < 32; ++j) v[j] = c0 + j < a.m ? v[j] : -INFINITY;
+                    }
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const int u = j & 3;
-                    if (v[j] > bv[u]) {
-                        bv[u] = v[j];
-                        bi[u] = c0 + j;
+                    for (int j = 0; j < 32; ++j) {
+                        const int u = j & 3;
+                        if (v[j] > bv[u]) {
+                            bv[u] = v[j];
+                            bi[u] = c0 + j;
+                        }
                     }
                 }
-            }
-            tc_fence_before();
-            warp_arrive(&dfree[b]);
-            float best = bv[0];
-            int arg = bi[0];
+                tc_fence_before();
+                warp_arrive(&dfree[b]);
+                float best = bv[0];
+                int arg = bi[0];
 #pragma unroll
-            for (int u = 1; u < 4; ++u)
-                if (bv[u] > best || (bv[u] == best && bi[u] < arg)) {
-                    best = bv[u];
-                    arg = bi[u];
+                for (int u = 1; u < 4; ++u)
+                    if (bv[u] > best || (bv[u] == best && bi[u] < arg)) {
+                        best = bv[u];
+                        arg = bi[u];
+                    }
+                arg = min(arg, a.m - 1);  // in range whatever the logits (non-finite ones are out of contract)
+                if (n < a.N) {
+                    a.route[bh * a.N + n] = arg;
+                    atomicAdd(&h[0][arg], 1);
                 }
-            arg = min(arg, a.m - 1);  // in range whatever the logits (non-finite ones are out of contract)
-            const int64_t n = tile * 128 + row;
-            if (n < a.N) {
-                a.route[bh * a.N + n] = arg;
-                atomicAdd(&h[arg], 1);
+            } else {
+                // s rounds of the argmax above, each over the columns not
+                // taken by an earlier round (those read as -inf): round u
+                // gives the u-th entry in the order (logit descending,
+                // landmark ascending). The winners so far are kept as bytes
+                // (m <= 256 here) in two words; the rounds stay a loop.
+                uint32_t won0 = 0u, won1 = 0u;  // winners 0-3 and 4-7, one byte each
+#pragma unroll 1
+                for (int u = 0; u < ns; ++u) {
+                    float bv[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+                    int bi[4] = {a.m, a.m, a.m, a.m};
+                    for (int c0 = 0; c0 < a.m_pad; c0 += 32) {
+                        float v[32];
+                        tmem_ld32(d + c0, v);
+                        tmem_ld_wait();
+                        if (c0 + 32 > a.m) {
+#pragma unroll
+                            for (int jj = 0; jj < 32; ++jj) v[jj] = c0 + jj < a.m ? v[jj] : -INFINITY;
+                        }
+                        uint32_t ex = 0;  // columns of this chunk taken before
+                        for (int x = 0; x < u; ++x) {
+                            const int wc = static_cast<int>(((x < 4 ? won0 : won1) >> (8 * (x & 3))) & 255u);
+                            if ((wc >> 5) == (c0 >> 5)) ex |= 1u << (wc & 31);
+                        }
+                        if (ex) {
+#pragma unroll
+                            for (int jj = 0; jj < 32; ++jj) v[jj] = ((ex >> jj) & 1u) ? -INFINITY : v[jj];
+                        }
+#pragma unroll
+                        for (int jj = 0; jj < 32; ++jj) {
+                            const int ch = jj & 3;
+                            if (v[jj] > bv[ch]) {
+                                bv[ch] = v[jj];
+                                bi[ch] = c0 + jj;
+                            }
+                        }
+                    }
+                    float best = bv[0];
+                    int arg = bi[0];
+#pragma unroll
+                    for (int c = 1; c < 4; ++c)
+                        if (bv[c] > best || (bv[c] == best && bi[c] < arg)) {
+                            best = bv[c];
+                            arg = bi[c];
+                        }
+                    // in range whatever the logits (non-finite ones are out of contract)
+                    const int r = min(max(arg, 0), a.m - 1);
+                    if (u < 4)
+                        won0 |= static_cast<uint32_t>(r) << (8 * u);
+                    else
+                        won1 |= static_cast<uint32_t>(r) << (8 * (u - 4));
+                    if (n < a.N) {
+                        a.route[(bh * a.N + n) * ns + u] = r;
+                        atomicAdd(&h[u][r], 1);
+                    }
+                }
+                tc_fence_before();
+                warp_arrive(&dfree[b]);
             }
         }
         named_bar(1 + b, 128);
         if (cur >= 0)
-            for (int e = row; e < a.m; e += 128)
-                if (h[e]) atomicAdd(&a.counts[cur * a.m + e], h[e]);
+            for (int j = 0; j < ns; ++j)
+                for (int e = row; e < a.m; e += 128)
+                    if (h[j][e]) atomicAdd(&a.counts[(j * a.BH + cur) * a.m + e], h[j][e]);
     }
     tc_fence_before();
     __syncthreads();
@@ -219,12 +289,16 @@ __global__ void __launch_bounds__(RT_THREADS, 1) route_tc_kernel(const __grid_co
 
 bool route_tc_supported(const Plan& p) { return p.s.m <= 256 && p.s.BH * p.s.N < (int64_t(1) << 31); }
 
+// The route of each query (s = 1: [BH][N]) or its s best landmarks ([BH][N][s]).
+
 cudaError_t launch_route_tc(const Plan& p, const Work& w, const __nv_bfloat16* Q, int32_t* route, cudaStream_t st) {
     RouteArgs a;
     a.route = route;
     a.counts = w.counts;
     a.status = w.status;
     a.N = p.s.N;
+    a.BH = p.s.BH;
+    a.s = p.s.s_route;
     a.tiles_per_head = (p.s.N + 127) / 128;
     a.total_tiles = a.tiles_per_head * p.s.BH;
     a.m = p.s.m;
@@ -234,11 +308,11 @@ cudaError_t launch_route_tc(const Plan& p, const Work& w, const __nv_bfloat16* Q
     if (!make_row_tmap(&tq, Q, static_cast<uint64_t>(p.s.BH * p.s.N), 128) ||
         !make_row_tmap(&thi, w.lqhi, mrows, a.m_pad) || !make_row_tmap(&tlo, w.lqlo, mrows, a.m_pad))
         return cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(route_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(SMEM));
+    auto kern = a.s > 1 ? route_tc_kernel<true> : route_tc_kernel<false>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(SMEM));
     if (e != cudaSuccess) return e;
     const int64_t grid = std::min<int64_t>(device_sms(), a.total_tiles);
-    route_tc_kernel<<<static_cast<unsigned>(grid), RT_THREADS, SMEM, st>>>(tq, thi, tlo, a);
+    kern<<<static_cast<unsigned>(grid), RT_THREADS, SMEM, st>>>(tq, thi, tlo, a);
     return cudaGetLastError();
 }
 

@@ -185,6 +185,16 @@ def test_multi_edge_shapes(orc, B, H, N, gh, gw, m, k, s):
     print(rep)
 
 
+@pytest.mark.parametrize("s", [2, 3])
+def test_multi_tensor_core_clustered(orc, s):
+    """Clustered keys make the experts of nearby landmarks overlap heavily, so
+    the later passes mask many keys; N >= 32 m takes the tensor-core passes."""
+    cfg = dict(B=2, H=2, N=8192, d=64, grid_h=0, grid_w=0, m=64, k=64, recipe="clusters", clusters=8)
+    q, k, v = synth.make_inputs(cfg, seed=5)
+    rep = parity.full_parity_multi(orc, q, k, v, 0, 0, 64, 64, s)
+    print(s, rep)
+
+
 def test_multi_s1_is_mita():
     """s = 1 through the s-expert entry point is the one-expert forward pass."""
     import torch
