@@ -58,11 +58,23 @@ def describe(name):
 # Whole pass: FLOPs = B*H*(4 m N d + 4 N (m+k) d); bytes = B*H*(3 N d + N d)*2
 # + B*H*m*k*2*d*2 (Q,K,V read once, gathered expert rows, output written).
 # ---------------------------------------------------------------------------
-def work(c, shared=True):
+def work(c, shared=True, s=1):
     """shared=False: the routing-only ablation, whose scan forms only the
-    logits (no shared-expert values) and whose experts hold k keys alone."""
+    logits (no shared-expert values) and whose experts hold k keys alone.
+    s > 1: s routed experts per query; the attention counts m + s k keys per
+    query (an upper bound: shared keys of two experts are attended once) and
+    reads s expert row sets per query group."""
     BH, N, d, m, k = c["B"] * c["H"], c["N"], 64, c["m"], c["k"]
     row = N * d * 2
+    if s > 1:
+        return {
+            "total": {"flops": BH * (4 * m * N * d + 4 * N * (m + s * k) * d),
+                      "bytes": BH * (4 * row + m * k * 2 * d * 2)},
+            "pool": {"flops": 0, "bytes": BH * row},
+            "scan": {"flops": BH * 4 * m * N * d, "bytes": BH * 2 * row},
+            "route": {"flops": BH * 2 * N * m * d, "bytes": BH * row},
+            "expert": {"flops": BH * 4 * N * (m + s * k) * d, "bytes": BH * (s * 2 * row + s * m * k * 2 * d * 2)},
+        }
     if not shared:
         return {
             "total": {"flops": BH * (2 * m * N * d + 4 * N * k * d), "bytes": BH * (4 * row + m * k * 2 * d * 2)},
@@ -264,11 +276,15 @@ def run_gpu(args, rank, world):
     Q, K, V = dev_bf16(q), dev_bf16(k), dev_bf16(v)
     out = torch.empty_like(Q)
     eidx = torch.empty((B, H, m, kk), dtype=torch.int32, device=dev)
-    route = torch.empty((B, H, N), dtype=torch.int32, device=dev)
+    sr = args.s_route
+    route = torch.empty((B, H, N) if sr == 1 else (B, H, N, sr), dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream(dev)
 
     def step():
-        M.mita_forward(Q, K, V, gh, gw, m, kk, out=out, expert_idx=eidx, route=route, stream=stream)
+        if sr == 1:
+            M.mita_forward(Q, K, V, gh, gw, m, kk, out=out, expert_idx=eidx, route=route, stream=stream)
+        else:
+            M.mita_forward_multi(Q, K, V, gh, gw, m, kk, sr, out=out, expert_idx=eidx, route=route, stream=stream)
 
     for _ in range(args.warmup):
         step()
@@ -298,7 +314,7 @@ def run_gpu(args, rank, world):
     value = job_throughput(queries, world, ms_step)
 
     peaks, peak_src = load_peaks()
-    w = work(c)
+    w = work(c, s=sr)
     t_roof = roofline_time(w["total"], peaks, sustained=True)
     stage_ms = {s: stages[s][0] / args.steps for s in STAGES}
     launches = sum(stages[s][1] for s in STAGES)
@@ -313,7 +329,7 @@ def run_gpu(args, rank, world):
         ach = wd["bytes"] / t_dom / 1e9
         roof = {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
     roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = kernel_traffic(dom, name)
+    roof["traffic"] = kernel_traffic(dom, name) if sr == 1 else None  # the counters are the one-expert kernels'
     roof["kernel"] = dom
     roof["peak_source"] = f"{peak_src} ({'sustained bf16' if tensor else 'copy bandwidth'})"
 
@@ -321,7 +337,8 @@ def run_gpu(args, rank, world):
         "metric": METRIC, "value": value, "unit": "queries/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": describe(name), "B": B, "H": H, "N": N, "d": 64, "m": m, "k": kk,
+        "config": {"workload": describe(name) + (f"; s={sr} routed experts per query" if sr > 1 else ""),
+                   "B": B, "H": H, "N": N, "d": 64, "m": m, "k": kk, "s": sr,
                    "l2": f"inputs ({3 * Q.numel() * 2 / 1e9:.2f} GB) larger than L2, no flush",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "roofline": roof,
@@ -335,7 +352,7 @@ def run_gpu(args, rank, world):
     del Q, K, V, out
     torch.cuda.empty_cache()
 
-    if not args.no_e2e:  # every rank: the job's end-to-end rate
+    if not args.no_e2e and sr == 1:  # every rank: the job's end-to-end rate (the host entry point is s = 1)
         e = e2e(args, M, q, k, v, c, stream, world, dev)
         if rank == 0:
             res["e2e"] = e
@@ -346,7 +363,7 @@ def run_gpu(args, rank, world):
         mita_ms = {n: r["ms_per_step"] for n, r in res["sweep"].items()}
         mita_ms[name] = ms_step
         res["full_attention"] = full_attention(args, dev, stream, mita_ms)
-    if rank == 0 and not args.no_cpu and world == 1:
+    if rank == 0 and not args.no_cpu and world == 1 and sr == 1:
         res["cpu_baseline"] = cpu_baseline(name, q, k, v)
     return res
 
@@ -603,6 +620,7 @@ def main():
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--s-route", type=int, default=1, help="routed experts per query (1: the pages' configuration)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "mita":
         ap.error("--warmup must be >= 3")
