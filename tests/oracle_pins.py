@@ -25,6 +25,9 @@ What pins what:
                        the shared pairs and the Python set union of the s
                        experts; s=1 is the one-expert forward; s=m with k=N
                        is plain softmax attention over [Lq; K]
+  * gradients          the torch restatement of the forward pass equals the
+                       C++ oracle; its autograd gradients match central
+                       finite differences (torch.autograd.gradcheck)
 """
 from __future__ import annotations
 
@@ -272,6 +275,38 @@ def pin_multi_reductions(o):
         assert np.max(np.abs(r["out"][0, h] - w @ np.concatenate([r["lv"][0, h], V[h]]))) < 1e-12
 
 
+def pin_grad_forward_matches(o):
+    """The differentiable restatement of the forward pass used for gradients
+    (oracle/mita_grad.py, torch float64) gives the C++ oracle's outputs for
+    the C++ oracle's own experts and routes, 1-D and 2-D."""
+    from oracle import mita_grad
+
+    for cfg in ("tiny", dict(B=1, H=2, N=300, d=64, grid_h=0, grid_w=0, m=7, k=11, recipe="iid")):
+        c = synth.CONFIGS[cfg] if isinstance(cfg, str) else cfg
+        q, k, v = synth.make_inputs(c)
+        r = o.forward(q, k, v, c["grid_h"], c["grid_w"], c["m"], c["k"])
+        out = mita_grad.forward(o, q, k, v, c["grid_h"], c["grid_w"], c["m"], r["expert_idx"], r["route"])
+        assert np.max(np.abs(out - r["out"])) < 1e-12
+
+
+def pin_grad_finite_differences(o):
+    """Gradients of the restated forward pass against central finite
+    differences (torch.autograd.gradcheck) on a small problem with fixed,
+    overlapping experts and every expert routed to."""
+    import torch
+
+    from oracle import mita_grad
+
+    rng = np.random.default_rng(3)
+    N, d, m, kk = 12, 4, 3, 5
+    W = mita_grad.pooling_matrix(o, N, 0, 0, m)
+    eidx = np.sort(np.stack([rng.choice(N, kk, replace=False) for _ in range(m)]), axis=1)[None]
+    route = (np.arange(N) % m)[None]
+    Q, K, V = (torch.from_numpy(rng.standard_normal((1, N, d))).requires_grad_(True) for _ in range(3))
+    assert torch.autograd.gradcheck(lambda a, b, c: mita_grad.forward_fixed(W, a, b, c, eidx, route), (Q, K, V),
+                                    eps=1e-6, atol=1e-7, rtol=1e-6)
+
+
 def pin_weights_sum_to_one(o):
     q, k, v = synth.make_inputs("tiny")
     r = o.forward(q, k, v, 14, 14, 25, 25)
@@ -335,6 +370,8 @@ def pin_hand_example(o):
 
 
 ALL_PINS = [
+    pin_grad_forward_matches,
+    pin_grad_finite_differences,
     pin_route_multi,
     pin_attend_multi_union,
     pin_multi_reductions,

@@ -6,6 +6,7 @@ import os
 import subprocess
 from concurrent.futures import ThreadPoolExecutor
 
+import numpy as np
 import pytest
 
 import oracle
@@ -70,3 +71,39 @@ def test_pins_catch_mutant(mutant_libs, idx):
         except (AssertionError, ValueError):
             caught.append(pin.__name__)
     assert caught, f"no pin caught mutant {MUTANTS[idx][0]!r}"
+
+
+GRAD_MUTANTS = [
+    ("landmark values detached", "lv = torch.softmax(tau * (lq @ k.T), dim=-1) @ v",
+     "lv = (torch.softmax(tau * (lq @ k.T), dim=-1) @ v).detach()"),
+    ("landmarks detached", "lq = W @ q", "lq = (W @ q).detach()"),
+    ("routed keys detached", "qi @ k[sel].T", "qi @ k[sel].detach().T"),
+    ("shared values dropped from the gradient", "vals.append(p[:, :m] @ lv + p[:, m:] @ v[sel])",
+     "vals.append(p[:, :m] @ lv.detach() + p[:, m:] @ v[sel])"),
+]
+
+
+@pytest.mark.parametrize("idx", range(len(GRAD_MUTANTS)), ids=[g[0] for g in GRAD_MUTANTS])
+def test_grad_pin_catches_mutant(idx):
+    """A copy of the gradient oracle with one dependence cut must fail the
+    finite-difference pin (its values are unchanged, its gradients are not)."""
+    import types
+
+    import torch
+
+    from oracle import mita_grad
+
+    _, old, new = GRAD_MUTANTS[idx]
+    src = open(mita_grad.__file__).read()
+    assert src.count(old) == 1, f"mutation anchor not unique/not found: {old!r}"
+    mod = types.ModuleType("mita_grad_mutant")
+    exec(compile(src.replace(old, new), "mita_grad_mutant", "exec"), mod.__dict__)
+    rng = np.random.default_rng(3)
+    N, d, m, kk = 12, 4, 3, 5
+    W = mita_grad.pooling_matrix(oracle.Oracle(), N, 0, 0, m)
+    eidx = np.sort(np.stack([rng.choice(N, kk, replace=False) for _ in range(m)]), axis=1)[None]
+    route = (np.arange(N) % m)[None]
+    Q, K, V = (torch.from_numpy(rng.standard_normal((1, N, d))).requires_grad_(True) for _ in range(3))
+    ok = torch.autograd.gradcheck(lambda a, b, c: mod.forward_fixed(W, a, b, c, eidx, route), (Q, K, V), eps=1e-6,
+                                  atol=1e-7, rtol=1e-6, raise_exception=False)
+    assert not ok, "the finite-difference pin did not catch the mutant"
