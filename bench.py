@@ -360,6 +360,7 @@ def run_gpu(args, rank, world):
         res["sweep"] = sweep(args, M, dev, stream, peaks)
         res["routed_only"] = routed_only(args, M, dev, stream, peaks)
         res["multi_expert"] = multi_expert(args, M, dev, stream, peaks)
+        res["backward"] = backward(args, M, dev, stream)
         mita_ms = {n: r["ms_per_step"] for n, r in res["sweep"].items()}
         mita_ms[name] = ms_step
         res["full_attention"] = full_attention(args, dev, stream, mita_ms)
@@ -471,6 +472,49 @@ def routed_only(args, M, dev, stream, peaks):
             "roofline_frac": roofline_time(w["total"], peaks, sustained=True) / (ms / 1e3),
             "expert_tflops": exp_tf, "expert_frac": exp_tf / peaks["bf16_tflops_sustained"] if exp_tf else None,
             "stage_ms": stage_ms}
+
+
+# fp32 FMA peak of the CUDA cores: 152 SMs x 128 FMA lanes x 2 FLOP x 2.07 GHz
+# (the SM clock the clock record shows under load)
+SIMT_FP32_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
+
+
+def backward(args, M, dev, stream):
+    """mita_backward on the timed workload (device-resident inputs and dO,
+    the forward pass's experts and routes). FLOPs: 2.5x the forward pass's
+    (the usual count for an attention backward: recomputed logits, dP, dS
+    products for dQ, dK, dV). The kernels run on the CUDA cores in fp32."""
+    import torch
+
+    c = synth.CONFIGS[args.config]
+    q, k, v = synth.make_inputs(c)
+    to = lambda a: torch.from_numpy(a.view(np.int16)).to(dev).view(torch.bfloat16)
+    Q, K, V = to(q), to(k), to(v)
+    dO = to(synth.normal_bf16(q.shape, 11, 7))
+    a = (c["grid_h"], c["grid_w"], c["m"], c["k"])
+    _, e, r = M.mita_forward(Q, K, V, *a, stream=stream)
+    dq = torch.empty(Q.shape, dtype=torch.float32, device=dev)
+    dk, dv = torch.empty_like(dq), torch.empty_like(dq)
+    for _ in range(3):
+        M.mita_backward(Q, K, V, dO, *a, e, r, dq, dk, dv, stream=stream)
+    torch.cuda.synchronize()
+    assert M.mita_sync_status(stream) == 0, M.mita_last_error()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    n = 3
+    ev0.record(stream)
+    for _ in range(n):
+        M.mita_backward(Q, K, V, dO, *a, e, r, dq, dk, dv, stream=stream)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    assert M.mita_sync_status(stream) == 0, M.mita_last_error()
+    ms = ev0.elapsed_time(ev1) / n
+    flops = 2.5 * work(c)["total"]["flops"]
+    tf = flops / (ms / 1e3) / 1e12
+    del Q, K, V, dO, dq, dk, dv
+    torch.cuda.empty_cache()
+    return {"queries_per_s": c["B"] * c["H"] * c["N"] / (ms / 1e3), "ms_per_step": ms,
+            "roofline": {"bound": "alu", "achieved": tf, "peak": SIMT_FP32_TFLOPS, "unit": "TFLOP/s",
+                         "frac": tf / SIMT_FP32_TFLOPS, "flops": "2.5 x the forward pass's"}}
 
 
 def multi_expert(args, M, dev, stream, peaks, s=2):

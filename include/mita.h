@@ -109,6 +109,26 @@ int mita_forward_multi(const void* Q, const void* K, const void* V, int B, int H
                        int grid_w, int m, int k, int s, void* out, int32_t* expert_idx, int32_t* route, void* stream);
 
 /*
+ * Backward pass: dQ, dK, dV of sum(out * dO) for the MiTA forward pass
+ * (mita_forward; one routed expert per query, with the shared pairs), with
+ * each landmark's top-k key set and each query's route held fixed -- they
+ * are piecewise constant in the inputs, so their derivative is zero almost
+ * everywhere. The pages train MiTA models ("NeurIPS 2026 | Mixture-of-Top-k
+ * 注意力" (shuwu5.cn), results section: Long Range Arena training times) but
+ * do not describe the backward pass; this is the derivative of the forward
+ * pass of section "MiTA：用少量地标查询，同时完成压缩与专家构造" through the pooling,
+ * the landmark attention (LV) and the query-expert attention.
+ * Q, K, V, dO: device, bf16 [B][H][N][d] (read only). expert_idx, route:
+ * device, int32, as returned by mita_forward for the same Q, K, V (read only;
+ * an entry out of range is left out and makes mita_sync_status report
+ * MITA_ERR_INVALID_ARG). dQ, dK, dV: device, float32 [B][H][N][d], overwritten.
+ * Returns MITA_OK or a MITA_ERR_* code; asynchronous on `stream`.
+ */
+int mita_backward(const void* Q, const void* K, const void* V, const void* dO, int B, int H, int N, int d,
+                  int grid_h, int grid_w, int m, int k, const int32_t* expert_idx, const int32_t* route, float* dQ,
+                  float* dK, float* dV, void* stream);
+
+/*
  * mita_forward with two optional extra device outputs (either may be NULL):
  * lq, float32 [B][H][m][d], the landmark queries of stage 1, and lv,
  * float32 [B][H][m][d], the shared-expert values LV of stage 2.

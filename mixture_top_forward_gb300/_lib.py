@@ -59,6 +59,8 @@ def load(path: str | None = None, build_if_missing: bool = True) -> ctypes.CDLL:
         lib.mita_forward_routed.restype = ci
         lib.mita_forward_aux.argtypes = [vp, vp, vp] + [ci] * 8 + [vp, vp, vp, vp, vp, vp]
         lib.mita_forward_aux.restype = ci
+        lib.mita_backward.argtypes = [vp, vp, vp, vp] + [ci] * 8 + [vp] * 6
+        lib.mita_backward.restype = ci
         lib.mita_forward_multi.argtypes = [vp, vp, vp] + [ci] * 9 + [vp, vp, vp, vp]
         lib.mita_forward_multi.restype = ci
         lib.mita_forward_noalloc.argtypes = [vp, vp, vp] + [ci] * 8 + [vp, vp, vp, vp]
@@ -172,6 +174,30 @@ def mita_forward_multi(Q, K, V, grid_h: int, grid_w: int, m: int, k: int, s: int
                                    _dev_ptr(route, "torch.int32", "route"), _stream(stream))
     _raise(rc)
     return out, expert_idx, route
+
+
+def mita_backward(Q, K, V, dO, grid_h: int, grid_w: int, m: int, k: int, expert_idx, route, dQ=None, dK=None,
+                  dV=None, stream=None):
+    """Gradients (float32 [B,H,N,d]) of sum(out * dO) for mita_forward's
+    output, with its experts and routes held fixed. Q, K, V, dO: bf16 device
+    tensors; expert_idx, route: as returned by mita_forward."""
+    import torch
+
+    B, H, N, d = _shape(Q, m, k, grid_h, grid_w)
+    for t, n in ((K, "K"), (V, "V"), (dO, "dO")):
+        if tuple(t.shape) != (B, H, N, d):
+            raise ValueError(f"{n} must have the shape of Q")
+    dQ = torch.empty((B, H, N, d), dtype=torch.float32, device=Q.device) if dQ is None else dQ
+    dK = torch.empty_like(dQ) if dK is None else dK
+    dV = torch.empty_like(dQ) if dV is None else dV
+    rc = load().mita_backward(_dev_ptr(Q, "torch.bfloat16", "Q"), _dev_ptr(K, "torch.bfloat16", "K"),
+                              _dev_ptr(V, "torch.bfloat16", "V"), _dev_ptr(dO, "torch.bfloat16", "dO"), B, H, N, d,
+                              grid_h, grid_w, m, k, _dev_ptr(expert_idx, "torch.int32", "expert_idx"),
+                              _dev_ptr(route, "torch.int32", "route"), _dev_ptr(dQ, "torch.float32", "dQ"),
+                              _dev_ptr(dK, "torch.float32", "dK"), _dev_ptr(dV, "torch.float32", "dV"),
+                              _stream(stream))
+    _raise(rc)
+    return dQ, dK, dV
 
 
 def mita_forward_noalloc(Q, K, V, grid_h: int, grid_w: int, m: int, k: int, out, expert_idx, route, stream=None):

@@ -509,6 +509,36 @@ extern "C" int mita_forward_multi(const void* Q, const void* K, const void* V, i
                           true, s);
 }
 
+extern "C" int mita_backward(const void* Q, const void* K, const void* V, const void* dO, int B, int H, int N, int d,
+                             int grid_h, int grid_w, int m, int k, const int32_t* expert_idx, const int32_t* route,
+                             float* dQ, float* dK, float* dV, void* stream) {
+    g_err[0] = 0;
+    Shape s;
+    bool empty;
+    int rc = check_shape(B, H, N, d, grid_h, grid_w, m, k, &s, &empty);
+    if (rc != MITA_OK || empty) return rc;
+    if (!Q || !K || !V || !dO || !expert_idx || !route || !dQ || !dK || !dV)
+        return fail(MITA_ERR_INVALID_ARG, "a required pointer is NULL");
+    if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(dO) || !aligned16(dQ) || !aligned16(dK) ||
+        !aligned16(dV))
+        return fail(MITA_ERR_INVALID_ARG, "Q, K, V, dO, dQ, dK and dV must be 16-byte aligned");
+    Plan P;
+    if (!make_plan(s, &P)) return fail(MITA_ERR_UNSUPPORTED, "problem too large for the launch grids");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    void* base = nullptr;
+    if ((rc = workspace(st, 0, P.total, &base)) != MITA_OK) return rc;
+    Work W = carve(P, base);
+    const BwdLayout L = backward_layout(P);
+    void* bbase = nullptr;
+    if ((rc = workspace(st, 2, L.total, &bbase)) != MITA_OK) return rc;
+    const cudaError_t e =
+        launch_backward(P, W, L, bbase, static_cast<const __nv_bfloat16*>(Q), static_cast<const __nv_bfloat16*>(K),
+                        static_cast<const __nv_bfloat16*>(V), static_cast<const __nv_bfloat16*>(dO), expert_idx,
+                        route, dQ, dK, dV, st);
+    if (e != cudaSuccess) return cuda_fail(e, "backward launch");
+    return MITA_OK;
+}
+
 extern "C" int mita_forward(const void* Q, const void* K, const void* V, int B, int H, int N, int d, int grid_h,
                             int grid_w, int m, int k, void* out, int32_t* expert_idx, int32_t* route, void* stream) {
     return mita_forward_aux(Q, K, V, B, H, N, d, grid_h, grid_w, m, k, out, expert_idx, route, nullptr, nullptr,
@@ -660,7 +690,11 @@ extern "C" int mita_sync_status(void* stream) {
             cudaMemcpy(kv.second.ptr, &zero, sizeof(int), cudaMemcpyHostToDevice);
         }
     }
-    if (status != MITA_OK) return fail(status, "a bounded device-side wait gave up (status %d)", status);
+    if (status != MITA_OK)
+        return fail(status, "%s (status %d)",
+                    status == MITA_ERR_TIMEOUT ? "a bounded device-side wait gave up"
+                                               : "a device-side check found an index out of range",
+                    status);
     return MITA_OK;
 }
 

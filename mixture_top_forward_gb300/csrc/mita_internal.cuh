@@ -186,6 +186,21 @@ cudaError_t launch_expert_tc(const Plan& p, const Work& w, const __nv_bfloat16* 
                              const int32_t* route = nullptr, int j = 0);
 bool expert_tc_supported(const Plan& p);
 
+// Backward pass: its own workspace (byte offsets) next to the forward plan's.
+struct BwdLayout {
+    int ltiles, chunks;      // landmark tiles of 128; key chunks of the landmark-side kernels
+    int64_t chunk_len;
+    size_t off_lv, off_lse, off_part, off_dlq, off_dlv, off_dlt, off_route, total;
+};
+BwdLayout backward_layout(const Plan& p);
+// Gradients dQ, dK, dV (fp32, [BH][N][64], overwritten) of sum(out * dO) with
+// the given experts and routes held fixed; uses the forward plan's workspace
+// for pooling and grouping and `bbase` (BwdLayout::total bytes) for the rest.
+cudaError_t launch_backward(const Plan& p, const Work& w, const BwdLayout& L, void* bbase, const __nv_bfloat16* Q,
+                            const __nv_bfloat16* K, const __nv_bfloat16* V, const __nv_bfloat16* dO,
+                            const int32_t* expert_idx, const int32_t* route, float* dQ, float* dK, float* dV,
+                            cudaStream_t st);
+
 // Number of SMs of the current device (cached per device).
 int device_sms();
 
