@@ -524,6 +524,10 @@ extern "C" int mita_backward(const void* Q, const void* K, const void* V, const 
         return fail(MITA_ERR_INVALID_ARG, "Q, K, V, dO, dQ, dK and dV must be 16-byte aligned");
     Plan P;
     if (!make_plan(s, &P)) return fail(MITA_ERR_UNSUPPORTED, "problem too large for the launch grids");
+    // the key-side kernel runs one CTA per 128 keys of every head (the
+    // landmark-side grids are no larger)
+    if (s.BH * ((s.N + 127) / 128) > 0x7FFFFFFFLL)
+        return fail(MITA_ERR_UNSUPPORTED, "problem too large for the backward launch grids");
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     void* base = nullptr;
     if ((rc = workspace(st, 0, P.total, &base)) != MITA_OK) return rc;
