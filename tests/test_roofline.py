@@ -30,3 +30,22 @@ def test_bytes_formula():
     # Q, K, V read once and O written (4 x 128 MiB per head) plus m*k gathered K and V rows
     assert w["bytes"] == 8 * (4 * (1 << 20) * 128 + 256 * 256 * 2 * 128)
     assert w["flops"] == 8 * (4 * 256 * (1 << 20) * 64 + 4 * (1 << 20) * 512 * 64)
+
+
+def test_variant_numerators():
+    """The routing-only ablation's scan forms logits only (2 m N d) and its
+    experts hold k keys (4 N k d); s routed experts count m + s k keys per
+    query (an upper bound); s = 1 and shared are the headline numerator."""
+    c = dict(B=1, H=2, N=4096, m=64, k=128)
+    BH, N, m, k, d = 2, 4096, 64, 128, 64
+    base = bench.work(c)
+    assert bench.work(c, s=1) == base and bench.work(c, shared=True) == base
+    r = bench.work(c, shared=False)
+    assert r["scan"]["flops"] == BH * 2 * m * N * d
+    assert r["expert"]["flops"] == BH * 4 * N * k * d
+    assert r["total"]["flops"] == r["scan"]["flops"] + r["expert"]["flops"]
+    for s in (2, 3):
+        w = bench.work(c, s=s)
+        assert w["expert"]["flops"] == BH * 4 * N * (m + s * k) * d
+        assert w["total"]["flops"] == w["scan"]["flops"] + w["expert"]["flops"]
+        assert w["expert"]["flops"] > base["expert"]["flops"]
