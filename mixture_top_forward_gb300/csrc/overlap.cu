@@ -7,7 +7,8 @@
 // set of keys). The pass of rank j skips the keys of its expert e that an
 // earlier-ranked expert of the query already held; this table gives them as
 // bit masks: ovl[bh][a][b][w] bit c is set iff key E_b[64 w + c] is also in
-// E_a (E_a[a] = all ones; a query's experts are distinct, so it is unused).
+// E_a (the entry (a, a) is all ones; a query's experts are distinct, so it
+// is never read).
 //
 // Membership in E_a is a lookup in a hash table of its keys in shared memory
 // (open addressing, linear probing, at most half full: about 1.5 probes per
