@@ -67,3 +67,44 @@ def test_stage_names(lib):
     names = [M.mita_stage_name(i) for i in range(7)]
     assert names == ["pool", "pilot", "scan", "select", "route", "group", "expert"]
     assert M.mita_stage_name(7) is None
+
+
+def _multi(lib, s, B=1, H=1, N=196, d=64, gh=14, gw=14, m=25, k=25, q=FAKE, out=FAKE):
+    return lib.mita_forward_multi(q, FAKE, FAKE, B, H, N, d, gh, gw, m, k, s, out, FAKE, FAKE, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(s=0), M.MITA_ERR_INVALID_ARG),
+    (dict(s=26), M.MITA_ERR_INVALID_ARG),               # s > m
+    (dict(s=9, N=4096, gh=0, gw=0, m=64), M.MITA_ERR_INVALID_ARG),  # s > MITA_MAX_S
+    (dict(s=2, d=32), M.MITA_ERR_UNSUPPORTED),
+    (dict(s=2, q=0), M.MITA_ERR_INVALID_ARG),
+    (dict(s=2, out=FAKE + 4), M.MITA_ERR_INVALID_ARG),  # misaligned
+])
+def test_multi_rejects_bad_arguments(lib, kw, code):
+    assert _multi(lib, **kw) == code
+    assert M.mita_last_error() != ""
+
+
+def _bwd(lib, B=1, H=1, N=196, d=64, gh=14, gw=14, m=25, k=25, dO=FAKE, e=FAKE, dq=FAKE):
+    return lib.mita_backward(FAKE, FAKE, FAKE, dO, B, H, N, d, gh, gw, m, k, e, FAKE, dq, FAKE, FAKE, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(d=128), M.MITA_ERR_UNSUPPORTED),
+    (dict(m=0), M.MITA_ERR_INVALID_ARG),
+    (dict(k=197), M.MITA_ERR_INVALID_ARG),
+    (dict(m=24), M.MITA_ERR_UNSUPPORTED),
+    (dict(dO=0), M.MITA_ERR_INVALID_ARG),
+    (dict(e=0), M.MITA_ERR_INVALID_ARG),
+    (dict(dq=FAKE + 8), M.MITA_ERR_INVALID_ARG),       # misaligned
+])
+def test_backward_rejects_bad_arguments(lib, kw, code):
+    assert _bwd(lib, **kw) == code
+    assert M.mita_last_error() != ""
+
+
+def test_variants_empty_problem_is_a_no_op(lib):
+    assert _multi(lib, 2, B=0) == M.MITA_OK
+    assert _bwd(lib, B=0) == M.MITA_OK
+    assert lib.mita_forward_routed(FAKE, FAKE, FAKE, 0, 1, 196, 64, 14, 14, 25, 25, FAKE, FAKE, FAKE, None) == M.MITA_OK
