@@ -357,13 +357,21 @@ def run_gpu(args, rank, world):
         if rank == 0:
             res["e2e"] = e
     if rank == 0 and not args.no_sweep:
-        res["sweep"] = sweep(args, M, dev, stream, peaks)
-        res["routed_only"] = routed_only(args, M, dev, stream, peaks)
-        res["multi_expert"] = multi_expert(args, M, dev, stream, peaks)
-        res["backward"] = backward(args, M, dev, stream)
-        mita_ms = {n: r["ms_per_step"] for n, r in res["sweep"].items()}
+        # the side measurements: a failure is recorded in the line, never
+        # loses the headline numbers above
+        def leg(key, fn):
+            try:
+                res[key] = fn()
+            except Exception as ex:  # noqa: BLE001 (reported, not hidden)
+                res[key] = {"error": f"{type(ex).__name__}: {ex}"[:400]}
+
+        leg("sweep", lambda: sweep(args, M, dev, stream, peaks))
+        leg("routed_only", lambda: routed_only(args, M, dev, stream, peaks))
+        leg("multi_expert", lambda: multi_expert(args, M, dev, stream, peaks))
+        leg("backward", lambda: backward(args, M, dev, stream))
+        mita_ms = {n: r["ms_per_step"] for n, r in res["sweep"].items()} if "error" not in res["sweep"] else {}
         mita_ms[name] = ms_step
-        res["full_attention"] = full_attention(args, dev, stream, mita_ms)
+        leg("full_attention", lambda: full_attention(args, dev, stream, mita_ms))
     if rank == 0 and not args.no_cpu and world == 1 and sr == 1:
         res["cpu_baseline"] = cpu_baseline(name, q, k, v)
     return res
