@@ -35,18 +35,26 @@
  *   B*H == 0      is an empty problem: nothing is read or written, MITA_OK.
  *   Ownership     the caller owns every buffer passed in; the library never
  *                 frees or retains them. The library owns a cached scratch
- *                 workspace per (device, stream), grown on demand with
- *                 cudaMalloc and freed by mita_release_workspace().
+ *                 workspace per (device, stream), grown on demand in stream
+ *                 order (cudaMallocAsync / cudaFreeAsync on `stream`, from the
+ *                 device's default memory pool) and freed by
+ *                 mita_release_workspace().
  *   Streams       device entry points enqueue all work on `stream` (a
  *                 cudaStream_t; NULL = the legacy default stream) and return
- *                 without synchronising, except when the workspace must grow.
- *                 Calls on different streams use different workspaces.
+ *                 without synchronising the host, also when the workspace
+ *                 grows. Calls on different streams use different workspaces.
  *   Errors        a negative MITA_ERR_* code; mita_last_error() gives the
  *                 message. Argument errors are found before anything is
  *                 launched. A fault inside a kernel surfaces, as with any CUDA
  *                 call, at the caller's next synchronisation; waits inside the
  *                 kernels are bounded and report MITA_ERR_TIMEOUT through
- *                 mita_sync_status() instead of hanging.
+ *                 mita_sync_status() instead of hanging. A timeout stays
+ *                 recorded in the stream's workspace until mita_sync_status()
+ *                 reports and clears it; until then the kernels of later calls
+ *                 on that stream give up at their first wait that does not
+ *                 complete at once, so their outputs are not valid. Other
+ *                 codes in the status word (mita_backward's index check) do
+ *                 not affect later calls.
  */
 #ifndef MITA_H
 #define MITA_H
@@ -172,13 +180,16 @@ int mita_forward_host(const uint16_t* Q, const uint16_t* K, const uint16_t* V, i
  * (N up to a few thousand tokens, m and k in the tens) fit.
  *
  * The first call on a device looks up the array's device address with
- * cudaGetSymbolAddress (with that device current); make that first call
- * before any stream capture. Every call on a device shares the one array and
- * finds the previous call's contents in it (it clears what must start at
- * zero), so calls whose work overlaps on the GPU -- concurrent streams, or
- * several host threads -- race; order them on one stream. Stage timing is
- * not recorded for these calls, and a device-side timeout in them is not
- * reported by mita_sync_status (the kernels still exit instead of hanging).
+ * cudaGetSymbolAddress (with that device current) and clears the array's
+ * status word on `stream`; make that first call before any stream capture.
+ * Every call on a device shares the one array and finds the previous call's
+ * contents in it (it clears what must start at zero), so calls whose work
+ * overlaps on the GPU -- concurrent streams, or several host threads -- race;
+ * order them on one stream. Stage timing is not recorded for these calls. A
+ * device-side timeout in them is recorded in the array's status word and
+ * reported (and cleared) by mita_sync_status called with any stream of the
+ * device; as for the other entry points, the outputs of a call that timed
+ * out, and of later calls until the timeout is cleared, are not valid.
  */
 #define MITA_NOALLOC_SCRATCH_BYTES (64 << 20)
 int mita_forward_noalloc(const void* Q, const void* K, const void* V, int B, int H, int N, int d, int grid_h,
@@ -192,12 +203,27 @@ int mita_forward_noalloc(const void* Q, const void* K, const void* V, int B, int
 size_t mita_workspace_bytes(int B, int H, int N, int d, int grid_h, int grid_w, int m, int k);
 
 /*
- * Waits for `stream`, then reports and clears the device-side status word of
- * the current device: MITA_OK, MITA_ERR_TIMEOUT when a bounded wait inside a
- * kernel gave up since the last check, or MITA_ERR_CUDA when the stream
- * itself failed.
+ * Waits for `stream`, then reports and clears the device-side status words of
+ * the current device that calls on `stream` write (its workspace's, and the
+ * no-allocation scratch's): MITA_OK, MITA_ERR_TIMEOUT when a bounded wait
+ * inside a kernel gave up since the last check, MITA_ERR_INVALID_ARG when
+ * mita_backward found a route or expert index out of range, or MITA_ERR_CUDA
+ * when the stream itself failed.
  */
 int mita_sync_status(void* stream);
+
+/*
+ * Diagnostic (no counterpart in the method): enqueues on `stream` one kernel
+ * whose single thread waits, with the same bounded wait the forward kernels
+ * use for their handshakes, on a barrier that nothing completes. After
+ * limit_us microseconds (1 <= limit_us <= 2000000, else MITA_ERR_INVALID_ARG)
+ * the wait gives up, records MITA_ERR_TIMEOUT in the stream's workspace status
+ * word and the kernel exits. The next mita_sync_status(stream) then reports
+ * MITA_ERR_TIMEOUT and clears it; the call after that reports MITA_OK. It
+ * lets a caller check that the timeout path works on its GPU: nothing hangs,
+ * traps or faults. Asynchronous; returns MITA_OK or a MITA_ERR_* code.
+ */
+int mita_selftest_wait(int64_t limit_us, void* stream);
 
 /*
  * Stage timing (off by default). While enabled on a host thread, every

@@ -69,6 +69,8 @@ def load(path: str | None = None, build_if_missing: bool = True) -> ctypes.CDLL:
         lib.mita_forward_host.restype = ci
         lib.mita_workspace_bytes.argtypes = [ci] * 8
         lib.mita_workspace_bytes.restype = ctypes.c_size_t
+        lib.mita_selftest_wait.argtypes = [ctypes.c_int64, vp]
+        lib.mita_selftest_wait.restype = ci
         lib.mita_sync_status.argtypes = [vp]
         lib.mita_sync_status.restype = ci
         lib.mita_last_error.argtypes = []
@@ -261,6 +263,13 @@ def mita_workspace_bytes(B, H, N, d, grid_h, grid_w, m, k) -> int:
 
 def mita_sync_status(stream=None) -> int:
     return int(load().mita_sync_status(_stream(stream)))
+
+
+def mita_selftest_wait(limit_us: int, stream=None) -> None:
+    """Enqueues the bounded-wait self-test kernel (a wait nothing completes,
+    given up after limit_us microseconds); mita_sync_status then reports
+    MITA_ERR_TIMEOUT once."""
+    _raise(load().mita_selftest_wait(int(limit_us), _stream(stream)))
 
 
 def mita_profile_enable(on: bool = True) -> None:

@@ -173,7 +173,7 @@ __global__ void __launch_bounds__(NT, 1)
                      const __grid_constant__ CUtensorMap tlv, Args a) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ uint64_t kvfull, kvfree, qfull[NWG * QB], qfree[NWG * QB], ofree[NWG];
-    __shared__ uint64_t sfull[NWG], sfree[NWG], pfull[NWG], pvdone[NWG];
+    __shared__ uint64_t sfull[NWG], sfree[NWG], pfull[NWG], pvdone[NWG], drain;
     __shared__ uint32_t tmem_base;
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const Layout S = layout(base, a.nblk);
@@ -199,6 +199,7 @@ __global__ void __launch_bounds__(NT, 1)
             mbar_init(&qfull[b], 1);
             mbar_init(&qfree[b], 1);
         }
+        mbar_init(&drain, NWG);  // exit path: one commit per MMA issuer
         fence_barrier_init();
     }
     if (warp == 0) tmem_alloc(&tmem_base, 512);
@@ -282,6 +283,15 @@ __global__ void __launch_bounds__(NT, 1)
             }
             r += cnt;
         }
+        // exit: the last phase of every barrier this warp armed has landed
+        if (lane == 0) {
+            if (changes > 0) mbar_drain(&kvfull, (changes - 1) & 1);
+            for (int w = 0; w < NWG; ++w)
+                for (uint32_t b = 0; b < QB; ++b) {
+                    const uint32_t arms = nq[w] > b ? (nq[w] - b + QB - 1) / QB : 0;
+                    if (arms > 0) mbar_drain(&qfull[w * QB + b], (arms - 1) & 1);
+                }
+        }
     } else if (warp <= NWG) {
         // ---------------- MMA issuers: lane 0 of warp 1 + w serves warpgroup w ----------------
         // (each issuer has a warp of its own: tcgen05.mma is a single-thread instruction)
@@ -339,6 +349,7 @@ __global__ void __launch_bounds__(NT, 1)
                 st = next_item(a, w, r, i1, cur_bh, cur_e, changes, &kvfull, &kvfree, cur);
                 ok = st >= 0;
             }
+            mma_drain(&drain);  // exit: this issuer's MMAs are done
         }
     } else {
         // ------------------------------ row warpgroups ------------------------------

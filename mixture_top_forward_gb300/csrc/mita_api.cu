@@ -88,6 +88,11 @@ struct Slot {
 std::mutex g_ws_mu;
 std::map<std::pair<int, std::pair<uintptr_t, int>>, Slot> g_ws;
 
+// Grows in stream order: the old buffer is released with cudaFreeAsync and
+// the new one taken with cudaMallocAsync, both on `st`, so the work already
+// queued on `st` finishes with the old buffer before the pool hands its
+// memory out again, and the host never waits. The status word travels with
+// the workspace: a code still pending in the old buffer is carried over.
 int workspace(cudaStream_t st, int purpose, size_t bytes, void** out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -95,23 +100,24 @@ int workspace(cudaStream_t st, int purpose, size_t bytes, void** out) {
     std::lock_guard<std::mutex> lk(g_ws_mu);
     Slot& s = g_ws[{dev, {reinterpret_cast<uintptr_t>(st), purpose}}];
     if (s.bytes < bytes) {
-        if (s.ptr) {
-            e = cudaStreamSynchronize(st);
-            if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
-            cudaFree(s.ptr);
-            s.ptr = nullptr;
-            s.bytes = 0;
-        }
         const size_t want = bytes + bytes / 8;  // some headroom for growth
-        e = cudaMalloc(&s.ptr, want);
+        void* p = nullptr;
+        e = cudaMallocAsync(&p, want, st);
         if (e != cudaSuccess) {
             cudaGetLastError();
-            s.ptr = nullptr;
-            return fail(MITA_ERR_ALLOC, "cudaMalloc(%zu) for the workspace: %s", want, cudaGetErrorString(e));
+            return fail(MITA_ERR_ALLOC, "cudaMallocAsync(%zu) for the workspace: %s", want, cudaGetErrorString(e));
         }
+        e = cudaMemsetAsync(p, 0, want, st);
+        // the forward workspace's status word sits at offset 0 of every plan
+        if (e == cudaSuccess && s.ptr && purpose == 0)
+            e = cudaMemcpyAsync(p, s.ptr, sizeof(int), cudaMemcpyDeviceToDevice, st);
+        if (e == cudaSuccess && s.ptr) e = cudaFreeAsync(s.ptr, st);
+        if (e != cudaSuccess) {
+            cudaFreeAsync(p, st);
+            return cuda_fail(e, "workspace growth");
+        }
+        s.ptr = p;
         s.bytes = want;
-        e = cudaMemsetAsync(s.ptr, 0, want, st);
-        if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
     }
     *out = s.ptr;
     return MITA_OK;
@@ -673,6 +679,8 @@ extern "C" size_t mita_workspace_bytes(int B, int H, int N, int d, int grid_h, i
     return P.total;
 }
 
+static int* noalloc_status(int dev);
+
 extern "C" int mita_sync_status(void* stream) {
     g_err[0] = 0;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -694,11 +702,35 @@ extern "C" int mita_sync_status(void* stream) {
             cudaMemcpy(kv.second.ptr, &zero, sizeof(int), cudaMemcpyHostToDevice);
         }
     }
+    // the no-allocation entry point's scratch (shared by every stream of the device)
+    if (int* nw = noalloc_status(dev)) {
+        int word = 0;
+        if ((e = cudaMemcpy(&word, nw, sizeof(int), cudaMemcpyDeviceToHost)) != cudaSuccess)
+            return cuda_fail(e, "status read");
+        if (word != 0) {
+            if (status == MITA_OK || word == MITA_ERR_TIMEOUT) status = word;
+            const int zero = 0;
+            cudaMemcpy(nw, &zero, sizeof(int), cudaMemcpyHostToDevice);
+        }
+    }
     if (status != MITA_OK)
         return fail(status, "%s (status %d)",
                     status == MITA_ERR_TIMEOUT ? "a bounded device-side wait gave up"
                                                : "a device-side check found an index out of range",
                     status);
+    return MITA_OK;
+}
+
+extern "C" int mita_selftest_wait(int64_t limit_us, void* stream) {
+    g_err[0] = 0;
+    if (limit_us < 1 || limit_us > 2000000)
+        return fail(MITA_ERR_INVALID_ARG, "limit_us=%lld must be in [1, 2000000]", static_cast<long long>(limit_us));
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    void* base = nullptr;
+    int rc = workspace(st, 0, 256, &base);  // the status word at offset 0 (any plan's)
+    if (rc != MITA_OK) return rc;
+    const cudaError_t e = launch_wait_selftest(static_cast<int*>(base), static_cast<uint64_t>(limit_us) * 1000u, st);
+    if (e != cudaSuccess) return cuda_fail(e, "self-test launch");
     return MITA_OK;
 }
 
@@ -745,7 +777,10 @@ extern "C" void mita_release_workspace(void) {
         if (!kv.second.ptr) continue;
         cudaSetDevice(kv.first.first);
         cudaDeviceSynchronize();
-        cudaFree(kv.second.ptr);
+        // stream-ordered memory: freed on the legacy stream (the caller's may be
+        // gone) once the device is idle
+        cudaFreeAsync(kv.second.ptr, nullptr);
+        cudaDeviceSynchronize();
         kv.second.ptr = nullptr;
         kv.second.bytes = 0;
     }
@@ -781,8 +816,9 @@ std::map<int, void*> g_noalloc_addr;  // device -> device address of g_noalloc_s
 
 // Device address of the static scratch on the current device. In host code
 // the array's name is only a host-side stand-in, so the address is asked
-// from the runtime once per device, with that device current.
-int noalloc_scratch(void** out) {
+// from the runtime once per device, with that device current; the same
+// set-up clears the array's status word (offset 0 of every plan) on `st`.
+int noalloc_scratch(cudaStream_t st, void** out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
@@ -794,11 +830,24 @@ int noalloc_scratch(void** out) {
         if (e != cudaSuccess || p == nullptr)
             return fail(MITA_ERR_CUDA, "cudaGetSymbolAddress of the static scratch on device %d: %s", dev,
                         cudaGetErrorString(e));
+        if ((e = cudaMemsetAsync(p, 0, sizeof(int), st)) != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
         it = g_noalloc_addr.emplace(dev, p).first;
     }
     *out = it->second;
     return MITA_OK;
 }
+
+}  // namespace
+
+// The status word of the static scratch of device `dev` (nullptr before the
+// first mita_forward_noalloc call there).
+static int* noalloc_status(int dev) {
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    auto it = g_noalloc_addr.find(dev);
+    return it == g_noalloc_addr.end() ? nullptr : static_cast<int*>(it->second);
+}
+
+namespace {
 
 }  // namespace
 
@@ -820,14 +869,13 @@ extern "C" int mita_forward_noalloc(const void* Q, const void* K, const void* V,
         return fail(MITA_ERR_UNSUPPORTED,
                     "this shape needs %zu bytes of scratch; mita_forward_noalloc has %d (MITA_NOALLOC_SCRATCH_BYTES)",
                     P.total, MITA_NOALLOC_SCRATCH_BYTES);
-    void* base = nullptr;
-    if ((rc = noalloc_scratch(&base)) != MITA_OK) return rc;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    void* base = nullptr;
+    if ((rc = noalloc_scratch(st, &base)) != MITA_OK) return rc;
+    // The array keeps the previous call's contents: the forward sequence clears
+    // what must start at zero (the per-expert counters); the status word keeps
+    // a timeout until mita_sync_status reports and clears it.
     Work W = carve(P, base);
-    // The array keeps the previous call's contents; the status word must start
-    // at zero (the per-expert counters are cleared by the forward sequence).
-    cudaError_t e = cudaMemsetAsync(W.status, 0, sizeof(int), st);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
     const bool prof = t_profile;  // stage timing would create events: keep it off here
     t_profile = false;
     rc = run_forward(P, W, static_cast<const __nv_bfloat16*>(Q), static_cast<const __nv_bfloat16*>(K),

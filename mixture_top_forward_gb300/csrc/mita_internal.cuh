@@ -201,6 +201,10 @@ cudaError_t launch_backward(const Plan& p, const Work& w, const BwdLayout& L, vo
                             const int32_t* expert_idx, const int32_t* route, float* dQ, float* dK, float* dV,
                             cudaStream_t st);
 
+// One thread waits, with the kernels' bounded wait and the given limit, on an
+// mbarrier nothing completes; records MITA_ERR_TIMEOUT in *status.
+cudaError_t launch_wait_selftest(int* status, uint64_t limit_ns, cudaStream_t st);
+
 // Number of SMs of the current device (cached per device).
 int device_sms();
 

@@ -55,7 +55,7 @@ __global__ void __launch_bounds__(RT_THREADS, 1) route_tc_kernel(const __grid_co
                                                           const __grid_constant__ CUtensorMap thi,
                                                           const __grid_constant__ CUtensorMap tlo, RouteArgs a) {
     extern __shared__ uint8_t smem_raw[];
-    __shared__ uint64_t qfull[QST], qempty[QST], dfull[2], dfree[2], lqfull, lqfree;
+    __shared__ uint64_t qfull[QST], qempty[QST], dfull[2], dfree[2], lqfull, lqfree, drain;
     __shared__ uint32_t tmem_base;
     constexpr int HS = MULTI ? MITA_MAX_S : 1;  // histogram planes (ranks)
     __shared__ int hist[2][HS][256];
@@ -76,6 +76,7 @@ __global__ void __launch_bounds__(RT_THREADS, 1) route_tc_kernel(const __grid_co
         }
         mbar_init(&lqfull, 1);
         mbar_init(&lqfree, 2);  // one commit per MMA issuer
+        mbar_init(&drain, 2);   // exit path: one commit per MMA issuer
         fence_barrier_init();
     }
     for (int e = tid; e < 2 * HS * 256; e += blockDim.x) (&hist[0][0][0])[e] = 0;
@@ -95,7 +96,8 @@ __global__ void __launch_bounds__(RT_THREADS, 1) route_tc_kernel(const __grid_co
                 mbar_arrive_expect_tx(&qfull[st], 16384);
                 tma_load_2d(base + OFF_Q + st * 16384, &tq, 0, static_cast<int>(bh * a.N + tile * 128), &qfull[st]);
             };
-            for (int t = 0; t < nt && t < QST; ++t) load_q(t);
+            int loaded = 0;
+            for (int t = 0; t < nt && t < QST; ++t, ++loaded) load_q(t);
             int64_t cur = -1;
             int changes = 0;
             for (int t = 0; t < nt; ++t) {
@@ -112,7 +114,14 @@ __global__ void __launch_bounds__(RT_THREADS, 1) route_tc_kernel(const __grid_co
                 if (t + QST < nt) {
                     if (!mbar_wait(&qempty[t % QST], (t / QST) & 1, a.status)) break;
                     load_q(t + QST);
+                    ++loaded;
                 }
+            }
+            // exit: the last load of every barrier armed here has landed
+            if (changes > 0) mbar_drain(&lqfull, (changes - 1) & 1);
+            for (int st = 0; st < QST; ++st) {
+                const int arms = loaded > st ? (loaded - st + QST - 1) / QST : 0;
+                if (arms > 0) mbar_drain(&qfull[st], (arms - 1) & 1);
             }
         }
     } else if (warp >= 9) {
@@ -149,6 +158,7 @@ __global__ void __launch_bounds__(RT_THREADS, 1) route_tc_kernel(const __grid_co
                 mma_commit(&dfull[b]);
                 mma_commit(&qempty[st]);
             }
+            mma_drain(&drain);  // exit: this issuer's MMAs are done
         }
     } else {
         // ---------------- argmax warpgroups: group b takes the tiles t = b (mod 2) ----------------

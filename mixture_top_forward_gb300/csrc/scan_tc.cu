@@ -131,7 +131,7 @@ __global__ void __launch_bounds__(Cfg<FULL, NL>::NT, 1)
     extern __shared__ uint8_t smem_raw[];
     __shared__ uint64_t kfull[C::KST], kempty[C::KST];
     __shared__ uint64_t vfull[C::VST > 0 ? C::VST : 1], vempty[C::VST > 0 ? C::VST : 1];
-    __shared__ uint64_t sfull[NL * 2], sfree[NL * 2], pfull[NL * 2], pvdone[NL * 2];
+    __shared__ uint64_t sfull[NL * 2], sfree[NL * 2], pfull[NL * 2], pvdone[NL * 2], drain;
     __shared__ uint32_t tmem_base;
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
@@ -157,6 +157,7 @@ __global__ void __launch_bounds__(Cfg<FULL, NL>::NT, 1)
             mbar_init(&pfull[l], 4);  // every row warp arrives after writing its P rows
             mbar_init(&pvdone[l], 1);
         }
+        mbar_init(&drain, FULL ? NL + 1 : NL);  // exit path: one commit per MMA issuer
         fence_barrier_init();
     }
     if (warp == 0) tmem_alloc(&tmem_base, C::TCOLS);
@@ -186,23 +187,35 @@ __global__ void __launch_bounds__(Cfg<FULL, NL>::NT, 1)
     if (warp == 0) {
         // ---------------- K producer (lane 0) ----------------
         if (lane == 0) {
+            int issued = 0;
             for (int i = 0; i < T; ++i) {
                 const int st = i % C::KST;
                 if (i >= C::KST && !mbar_wait(&kempty[st], ((i / C::KST) & 1) ^ 1, a.status)) break;
                 mbar_arrive_expect_tx(&kfull[st], C::TB);
                 tma_load_3d(base + C::OFF_K + st * C::TB, &tk, 0, static_cast<int>(s0 + i * KT),
                             static_cast<int>(bh), &kfull[st]);
+                ++issued;
+            }
+            for (int st = 0; st < C::KST; ++st) {  // exit: the last load of every stage has landed
+                const int arms = issued > st ? (issued - st + C::KST - 1) / C::KST : 0;
+                if (arms > 0) mbar_drain(&kfull[st], (arms - 1) & 1);
             }
         }
         if constexpr (FULL) {
             // ---------------- V producer (lane 1) ----------------
             if (lane == 1) {
+                int issued = 0;
                 for (int i = 0; i < T; ++i) {
                     const int st = i % C::VST;
                     if (i >= C::VST && !mbar_wait(&vempty[st], ((i / C::VST) & 1) ^ 1, a.status)) break;
                     mbar_arrive_expect_tx(&vfull[st], C::TB);
                     tma_load_3d(base + C::OFF_V + st * C::TB, &tv, 0, static_cast<int>(s0 + i * KT),
                                 static_cast<int>(bh), &vfull[st]);
+                    ++issued;
+                }
+                for (int st = 0; st < C::VST; ++st) {
+                    const int arms = issued > st ? (issued - st + C::VST - 1) / C::VST : 0;
+                    if (arms > 0) mbar_drain(&vfull[st], (arms - 1) & 1);
                 }
             }
         }
@@ -225,13 +238,16 @@ __global__ void __launch_bounds__(Cfg<FULL, NL>::NT, 1)
                 mma_commit(&sfull[l * 2 + sb]);
                 mma_commit(&kempty[st]);
             }
+            mma_drain(&drain);  // exit: this issuer's MMAs are done
         }
     } else if (warp == NL + 1) {
         // ---------------- P.V issuer ----------------
         if constexpr (FULL) {
-            if (lane == 0)
+            if (lane == 0) {
                 for (int i = 0; i < T; ++i)
                     if (!issue_pv<C, NL>(a, base, tb, i, bars)) break;
+                mma_drain(&drain);
+            }
         }
     } else {
         // ---------------- landmark rows: top-k filter and softmax ----------------

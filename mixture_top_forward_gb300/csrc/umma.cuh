@@ -78,21 +78,41 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
-// Waits for the phase of parity `parity` to complete. Returns false (and sets
-// *status) on timeout; once *status is set, waits give up immediately.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* status) {
+// Waits for the phase of parity `parity` to complete. Returns false (and
+// records MITA_ERR_TIMEOUT in *status) once `limit_ns` of wall time have
+// passed. A timeout already recorded in *status (by any CTA, this call or an
+// earlier one on the same workspace) makes the wait give up early; any other
+// code in the status word (an input check of another entry point) does not.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* status,
+                                          uint64_t limit_ns = kWaitLimitNs) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_ns();
     for (uint32_t i = 1;; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((i & 63u) == 0) {
-            if (*reinterpret_cast<volatile int*>(status) != 0) return false;
-            if (global_ns() - t0 > kWaitLimitNs) {
+            if (*reinterpret_cast<volatile int*>(status) == -5 /* MITA_ERR_TIMEOUT */) return false;
+            if (global_ns() - t0 > limit_ns) {
                 atomicExch(status, -5 /* MITA_ERR_TIMEOUT */);
                 return false;
             }
         }
     }
+}
+
+// Exit path: waits, for at most kDrainLimitNs and whatever the status word
+// says, for the phase of parity `parity` of `bar`. A producer calls it for the
+// last phase of every barrier it armed, and an MMA issuer for a commit of its
+// own MMAs, so that no TMA copy or tensor-core operation a CTA started is
+// still in flight when the CTA frees its tensor memory and exits (after a
+// wait gave up, the consumers of those phases may never have waited). On the
+// normal path every such phase has completed already and this returns at once.
+constexpr uint64_t kDrainLimitNs = 200000000ull;  // 0.2 s
+
+__device__ __forceinline__ void mbar_drain(uint64_t* bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return;
+    const uint64_t t0 = global_ns();
+    while (!mbar_try_wait(bar, parity))
+        if (global_ns() - t0 > kDrainLimitNs) return;
 }
 
 // ---------------------------------------------------------------------------
@@ -315,6 +335,12 @@ __device__ __forceinline__ void mma_ts_k64(uint32_t d_tmem, uint32_t a_tmem, uin
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
                  : "memory");
+}
+// Exit path of an MMA issuer: `bar` (initialised with one arrival per issuer
+// of the CTA) completes its phase 0 once every issuer's MMAs are done.
+__device__ __forceinline__ void mma_drain(uint64_t* bar) {
+    mma_commit(bar);
+    mbar_drain(bar, 0);
 }
 
 // ---------------------------------------------------------------------------

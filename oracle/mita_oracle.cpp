@@ -20,7 +20,7 @@
 // double), tau = 1/sqrt(d) scales every logit, m landmarks, k keys per routed
 // expert. Everything is computed in double; nothing is rounded to bf16.
 //
-// Readings taken where the prose is silent (each is listed in the design doc):
+// Readings taken where the prose is silent (the readings below):
 //  * landmark windows: 1-D contiguous [floor(i N/m), ceil((i+1) N/m));
 //    2-D adaptive pooling over a p x p landmark grid (m = p^2), rows
 //    [floor(r gh/p), ceil((r+1) gh/p)), columns likewise with gw, landmarks and

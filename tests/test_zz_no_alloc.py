@@ -32,6 +32,11 @@ def M():
 
 @pytest.mark.parametrize("name", ["deit", "seg1600", "tiny"])
 def test_noalloc_matches_forward_on_two_calls(M, name):
+    """Also checks the property the entry point exists for: with every buffer
+    made beforehand and the library's own workspace released, two calls leave
+    the device's free memory (cudaMemGetInfo) exactly as it was. One call
+    runs first, since the static array itself is placed on the device when
+    the library's module is first used there."""
     import torch
 
     c = synth.CONFIGS[name]
@@ -42,16 +47,23 @@ def test_noalloc_matches_forward_on_two_calls(M, name):
     out = torch.empty_like(Q)
     e = torch.empty_like(ref_e)
     r = torch.empty_like(ref_r)
+    M.mita_forward_noalloc(Q, K, V, *args, out=out, expert_idx=e, route=r)
+    torch.cuda.synchronize()
+    M.mita_release_workspace()
     for _ in range(2):
         out.fill_(0)
         e.fill_(-1)
         r.fill_(-1)
+        torch.cuda.synchronize()
+        free0 = torch.cuda.mem_get_info()[0]
         M.mita_forward_noalloc(Q, K, V, *args, out=out, expert_idx=e, route=r)
         torch.cuda.synchronize()
+        assert torch.cuda.mem_get_info()[0] == free0
         assert torch.equal(e, ref_e)
         assert torch.equal(r, ref_r)
         err = (out.float() - ref_out.float()).abs()
         assert err.max().item() <= parity.OUT_MAX and err.mean().item() <= parity.OUT_MEAN
+    assert M.mita_sync_status() == 0
 
 
 def test_noalloc_refuses_shapes_beyond_its_scratch(M):
