@@ -393,6 +393,7 @@ def run_gpu(args, rank, world):
 
         leg("sweep", lambda: sweep(args, M, dev, stream, peaks, peak_src, with_cpu=not args.no_cpu))
         leg("routed_only", lambda: routed_only(args, M, dev, stream, peaks))
+        leg("split_shared", lambda: split_shared(args, M, dev, stream, peaks))
         leg("multi_expert", lambda: multi_expert(args, M, dev, stream, peaks))
         leg("backward", lambda: backward(args, M, dev, stream))
         mita_ms = {n: r["ms_per_step"] for n, r in res["sweep"].items()} if "error" not in res["sweep"] else {}
@@ -568,6 +569,46 @@ def routed_only(args, M, dev, stream, peaks):
             "expert_tflops": exp_tf, "expert_frac": exp_tf / peaks["bf16_tflops"] if exp_tf else None,
             "peak": "burst bf16",
             "stage_ms": stage_ms}
+
+
+def split_shared(args, M, dev, stream, peaks):
+    """mita_forward_split on the timed workload: the shared branch folded into
+    the routing kernel (the routing stage then also forms each query's
+    softmax over its landmark logits, and the expert stage attends to the k
+    routed keys alone). Device-resident inputs, stage times from the
+    library's profile; the same FLOP count as the headline pass."""
+    import torch
+
+    c = synth.CONFIGS[args.config]
+    q, k, v = synth.make_inputs(c)
+    to = lambda a: torch.from_numpy(a.view(np.int16)).to(dev).view(torch.bfloat16)
+    Q, K, V = to(q), to(k), to(v)
+    out = torch.empty_like(Q)
+    e = torch.empty((c["B"], c["H"], c["m"], c["k"]), dtype=torch.int32, device=dev)
+    r = torch.empty((c["B"], c["H"], c["N"]), dtype=torch.int32, device=dev)
+    a = (c["grid_h"], c["grid_w"], c["m"], c["k"])
+    for _ in range(3):
+        M.mita_forward_split(Q, K, V, *a, out=out, expert_idx=e, route=r, stream=stream)
+    torch.cuda.synchronize()
+    assert M.mita_sync_status(stream) == 0, M.mita_last_error()
+    M.mita_profile_read(stream)
+    M.mita_profile_enable(True)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    n = 10
+    ev0.record(stream)
+    for _ in range(n):
+        M.mita_forward_split(Q, K, V, *a, out=out, expert_idx=e, route=r, stream=stream)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    M.mita_profile_enable(False)
+    stages = M.mita_profile_read(stream)
+    assert M.mita_sync_status(stream) == 0, M.mita_last_error()
+    ms = ev0.elapsed_time(ev1) / n
+    del Q, K, V, out
+    torch.cuda.empty_cache()
+    return {"queries_per_s": c["B"] * c["H"] * c["N"] / (ms / 1e3), "ms_per_step": ms,
+            "roofline_frac": roofline_time(work(c)["total"], peaks, sustained=False) / (ms / 1e3),
+            "stage_ms": {x: stages[x][0] / n for x in STAGES}}
 
 
 # fp32 FMA peak of the CUDA cores: 152 SMs x 128 FMA lanes x 2 FLOP x 2.07 GHz

@@ -100,6 +100,25 @@ int mita_forward_routed(const void* Q, const void* K, const void* V, int B, int 
                         int grid_w, int m, int k, void* out, int32_t* expert_idx, int32_t* route, void* stream);
 
 /*
+ * mita_forward computed the other way the pages allow: the Algorithm 1
+ * caption of "And attention is also FFN? …" (en.roboind.com) combines the
+ * shared and routed branches by online softmax, and "NeurIPS 2026 |
+ * Mixture-of-Top-k 注意力" (shuwu5.cn), section "MiTA：用少量地标查询，同时完成
+ * 压缩与专家构造", reuses the query-to-landmark logits for routing. Here the
+ * routing kernel keeps each query's m landmark logits and also forms the
+ * shared branch's softmax over them (its log-sum-exp and normalised output);
+ * the expert attention then runs over the k routed keys alone, starting its
+ * online softmax from that partial. Same results as mita_forward up to
+ * rounding (same routes and expert sets; outputs within the same
+ * tolerances). Measured slower than mita_forward on GB300, so mita_forward
+ * does not use it; shapes where its kernels do not apply (m > 256, large k)
+ * run mita_forward's sequence. Arguments, layouts, errors and asynchrony as
+ * for mita_forward; the workspace adds 132 bytes per query.
+ */
+int mita_forward_split(const void* Q, const void* K, const void* V, int B, int H, int N, int d, int grid_h,
+                       int grid_w, int m, int k, void* out, int32_t* expert_idx, int32_t* route, void* stream);
+
+/*
  * MiTA with s routed experts per query. The pages run what they call the
  * s = 1 configuration ("NeurIPS 2026 | Mixture-of-Top-k 注意力"
  * (shuwu5.cn), end of section "MiTA：用少量地标查询，同时完成压缩与专家构造") and do

@@ -55,6 +55,8 @@ def load(path: str | None = None, build_if_missing: bool = True) -> ctypes.CDLL:
                                     ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_uint16))
         lib.mita_forward.argtypes = [vp, vp, vp] + [ci] * 8 + [vp, vp, vp, vp]
         lib.mita_forward.restype = ci
+        lib.mita_forward_split.argtypes = [vp, vp, vp] + [ci] * 8 + [vp, vp, vp, vp]
+        lib.mita_forward_split.restype = ci
         lib.mita_forward_routed.argtypes = [vp, vp, vp] + [ci] * 8 + [vp, vp, vp, vp]
         lib.mita_forward_routed.restype = ci
         lib.mita_forward_aux.argtypes = [vp, vp, vp] + [ci] * 8 + [vp, vp, vp, vp, vp, vp]
@@ -151,6 +153,14 @@ def mita_forward_routed(Q, K, V, grid_h: int, grid_w: int, m: int, k: int, out=N
     k pairs of its routed expert alone), on device tensors; arguments and
     results as mita_forward."""
     return mita_forward(Q, K, V, grid_h, grid_w, m, k, out, expert_idx, route, stream, _entry="mita_forward_routed")
+
+
+def mita_forward_split(Q, K, V, grid_h: int, grid_w: int, m: int, k: int, out=None, expert_idx=None, route=None,
+                       stream=None):
+    """mita_forward with the shared branch folded into the routing kernel
+    (online-softmax combine of the two branches); same arguments and
+    results as mita_forward."""
+    return mita_forward(Q, K, V, grid_h, grid_w, m, k, out, expert_idx, route, stream, _entry="mita_forward_split")
 
 
 def mita_forward_multi(Q, K, V, grid_h: int, grid_w: int, m: int, k: int, s: int, out=None, expert_idx=None,

@@ -42,6 +42,17 @@
 // their waits warp-uniform, so no named barrier can block forever. Every
 // wait is bounded (umma.cuh).
 //
+// With the shared branch split off (SPLIT, s = 1: route_shared.cu has already
+// formed each query's softmax partial over the m landmark logits, as the
+// Algorithm 1 caption's online-softmax combine allows), the key list holds
+// the k routed keys alone and each row starts its online softmax from that
+// partial: running max lse_n (log2 units), row sum 1 and O = o_n (the shared
+// output, gathered like the query rows), i.e. one pre-merged pair of logit
+// lse_n and value o_n. Each row thread copies its o_n row into its warpgroup's
+// staging rows with cp.async when its item starts, and writes it, scaled to
+// its first block's running max, into its O accumulator before that block's
+// P.V accumulates (the producer is not involved, so it keeps running ahead).
+//
 // s routed experts per query (MULTI; the pages' setting is s = 1): one launch
 // per rank j of the routes, over the queries grouped by their j-th expert.
 // Pass 0 takes the shared pairs and the expert's keys, later passes the
@@ -74,6 +85,7 @@ __host__ __device__ constexpr uint32_t tcol_p(int w) { return 384u + 32u * w; }
 static_assert(tcol_p(NWG - 1) + 32 <= 512 && tcol_s(NWG - 1) + 64 <= tcol_o(0) && tcol_o(NWG - 1) + 64 <= tcol_p(0),
               "TMEM holds 512 columns");
 constexpr uint32_t kIdescS = idesc_bf16(128, KB, false);
+constexpr int kPlain = 0, kMulti = 1, kSplit = 2;  // kernel modes
 constexpr uint32_t kIdescPV = idesc_bf16(128, 64, true);
 
 struct Args {
@@ -89,12 +101,15 @@ struct Args {
     const uint64_t* mask;  // j > 0: [BH][N][nbw] per grouping slot, bit c of word b: key c of block b counted before
     float* state;          // [BH][N][68]: O[64] (unnormalised), max (log2 units), sum
     int s, j, nbw;
+    const float* lse;             // SPLIT: [BH][N] the shared branch's log-sum-exp (log2 units)
+    const __nv_bfloat16* osh;     // SPLIT: [BH][N][64] its output rows
 };
 
 struct Layout {
     uint8_t* keys;  // nblk * 8 KB
     uint8_t* vals;  // nblk * 8 KB
     uint8_t* q;     // [NWG][QB] * 16 KB: query rows
+    uint8_t* ps;    // SPLIT: [NWG] * 16 KB: the rows' shared-branch outputs (each thread its own row)
 };
 
 __device__ __forceinline__ Layout layout(uint8_t* base, int nblk) {
@@ -102,6 +117,7 @@ __device__ __forceinline__ Layout layout(uint8_t* base, int nblk) {
     L.keys = base;
     L.vals = L.keys + nblk * 8192;
     L.q = L.vals + nblk * 8192;
+    L.ps = L.q + NWG * QB * 16384;
     return L;
 }
 
@@ -166,11 +182,31 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     return *reinterpret_cast<uint32_t*>(&h);
 }
 
-template <bool MULTI>
+// SPLIT: writes row t's shared-branch output (bf16, a 128-byte swizzled row
+// of `rows`), times alpha, into this warp's 64 O columns at tO, and orders
+// the stores before the caller's barrier arrival. Once per item: kept out of
+// line so that its registers do not count in the block loop.
+static __device__ __noinline__ void preload_shared(uint32_t tO, const uint8_t* rows, int t, float alpha) {
+#pragma unroll 1
+    for (int hh = 0; hh < 2; ++hh) {
+        float o[32];
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+            unpack_bf16x8(*reinterpret_cast<const uint4*>(rows + swz128(t, 4 * hh + c)), o + 8 * c);
+#pragma unroll
+        for (int c = 0; c < 32; ++c) o[c] *= alpha;
+        tmem_st32(tO + 32 * hh, o);
+    }
+    tmem_st_wait();
+    tc_fence_before();
+}
+
+template <int MODE>
 __global__ void __launch_bounds__(NT, 1)
     expert_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                      const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tlq,
                      const __grid_constant__ CUtensorMap tlv, Args a) {
+    constexpr bool MULTI = MODE == kMulti, SPLIT = MODE == kSplit;
     extern __shared__ uint8_t smem_raw[];
     __shared__ uint64_t kvfull, kvfree, qfull[NWG * QB], qfree[NWG * QB], ofree[NWG];
     __shared__ uint64_t sfull[NWG], sfree[NWG], pfull[NWG], pvdone[NWG], drain;
@@ -325,11 +361,16 @@ __global__ void __launch_bounds__(NT, 1)
             };
             // P.V of block j of the current item
             auto issue_pv = [&](int j) -> bool {
-                // the first P.V of an item overwrites O: the previous item's epilogue must have read it
-                if (j == 0 && npv > 0 && !mbar_wait(&ofree[w], (npv - 1) & 1, a.status)) return false;
+                // the first P.V of an item overwrites O (SPLIT: adds to the
+                // preloaded shared output): the previous item's epilogue must
+                // have read it (SPLIT: the rows have preloaded this item's)
+                if (j == 0) {
+                    if (SPLIT && !mbar_wait(&ofree[w], npv & 1, a.status)) return false;
+                    if (!SPLIT && npv > 0 && !mbar_wait(&ofree[w], (npv - 1) & 1, a.status)) return false;
+                }
                 if (!mbar_wait(&pfull[w], gp & 1, a.status)) return false;
                 tc_fence_after();
-                mma_ts_k64(tO, tP, vd + j * 512, kIdescPV, j > 0 ? 1u : 0u);
+                mma_ts_k64(tO, tP, vd + j * 512, kIdescPV, (j > 0 || SPLIT) ? 1u : 0u);
                 mma_commit(&pvdone[w]);
                 ++gp;
                 return true;
@@ -374,7 +415,7 @@ __global__ void __launch_bounds__(NT, 1)
                     float o[32];
                     tmem_ld32(tO + h * 32, o);
                     tmem_ld_wait();
-                    if (h == 1) {
+                    if (h == 1 && !SPLIT) {  // (SPLIT: the next item's preload releases O)
                         tc_fence_before();
                         warp_arrive(&ofree[w]);
                     }
@@ -450,7 +491,18 @@ __global__ void __launch_bounds__(NT, 1)
             const int4 item = pick(w, x0, x1, x2);
             const int64_t bh = item.w;
             const int n = t < item.z ? a.perm[bh * a.N + item.y + t] : 0;
+            // SPLIT: the shared branch as one pre-merged pair (logit lse, weight 1);
+            // its output row comes in now, and is read in the first block
             float mrun = -INFINITY, lrun = 0.f;
+            if constexpr (SPLIT) {
+                mrun = t < item.z ? a.lse[bh * a.N + n] : 0.f;
+                lrun = 1.f;
+                const __nv_bfloat16* src = a.osh + (bh * a.N + n) * D;  // (padding rows: query 0's, finite)
+                const uint32_t dst = smem_u32(S.ps + w * 16384);
+#pragma unroll
+                for (int c = 0; c < 8; ++c) cp_async16(dst + swz128(t, c), src + 8 * c);
+                asm volatile("cp.async.commit_group;" ::: "memory");
+            }
             float* srow = nullptr;
             const uint64_t* mrow = nullptr;  // MULTI, passes j > 0: this row's masks, one word per block
             uint64_t dm0 = 0;                // the word of the next block (first: loaded with the item)
@@ -551,6 +603,14 @@ __global__ void __launch_bounds__(NT, 1)
                 tc_fence_before();
                 warp_arrive(&pfull[w]);
                 if (pend) epilogue();  // the previous item's O is final (its last P.V is done)
+                if (SPLIT && j == 0) {
+                    // O := alpha o_n (the shared output at this block's running
+                    // max), before this item's first P.V adds to it; each thread
+                    // reads back only the row it copied itself
+                    cp_async_wait_all();
+                    preload_shared(tO, S.ps + w * 16384, t, alpha);
+                    warp_arrive(&ofree[w]);
+                }
                 mrun = mnew;
             }
             if (!ok) break;
@@ -575,15 +635,24 @@ __global__ void __launch_bounds__(NT, 1)
     if (warp == 0) tmem_free(tb, 512);
 }
 
-size_t smem_bytes(int nblk) { return 1024 + static_cast<size_t>(nblk) * 16384 + NWG * QB * 16384; }
+size_t smem_bytes(int nblk, bool split) {
+    return 1024 + static_cast<size_t>(nblk) * 16384 + NWG * QB * 16384 + (split ? NWG * 16384 : 0);
+}
 
-int key_rows(const Plan& p) { return (p.shared ? (p.s.m + 3) & ~3 : 0) + p.s.k; }
+// the shared pairs enter the key list unless they are absent (routing-only
+// ablation) or already folded into each query's shared-branch partial
+int key_rows(const Plan& p) { return (p.shared && !p.split ? (p.s.m + 3) & ~3 : 0) + p.s.k; }
 
 }  // namespace
 
 bool expert_tc_supported(const Plan& p) {
     return key_rows(p) <= 512 && p.s.BH * p.s.N < (int64_t(1) << 31) &&
-           smem_bytes((key_rows(p) + KB - 1) / KB) <= 232448;
+           smem_bytes((key_rows(p) + KB - 1) / KB, p.split) <= 232448;
+}
+
+bool expert_split_fits(const Plan& p) {
+    const int rows = p.s.k;  // the routed keys alone
+    return rows <= 512 && p.s.BH * p.s.N < (int64_t(1) << 31) && smem_bytes((rows + KB - 1) / KB, true) <= 232448;
 }
 
 cudaError_t launch_expert_tc(const Plan& p, const Work& w, const __nv_bfloat16* Q, const __nv_bfloat16* K,
@@ -600,7 +669,7 @@ cudaError_t launch_expert_tc(const Plan& p, const Work& w, const __nv_bfloat16* 
     a.status = w.status;
     a.N = p.s.N;
     a.m = p.s.m;
-    a.msh = p.shared && j == 0 ? p.s.m : 0;
+    a.msh = p.shared && j == 0 && !p.split ? p.s.m : 0;
     a.k = p.s.k;
     a.nblk = ((a.msh + 3) / 4 * 4 + a.k + KB - 1) / KB;
     a.mask = j > 0 ? w.mask + static_cast<size_t>(j - 1) * p.s.BH * p.s.N * ((p.s.k + 63) / 64) : nullptr;
@@ -608,13 +677,15 @@ cudaError_t launch_expert_tc(const Plan& p, const Work& w, const __nv_bfloat16* 
     a.s = p.s.s_route;
     a.j = j;
     a.nbw = (p.s.k + 63) / 64;
+    a.lse = w.lse;
+    a.osh = w.osh;
     CUtensorMap tq, tk, tv, tlq, tlv;
     const uint64_t rows = static_cast<uint64_t>(p.s.BH) * p.s.N, lrows = static_cast<uint64_t>(p.s.BH) * p.s.m;
     if (!make_row_tmap(&tq, Q, rows, 1) || !make_row_tmap(&tk, K, rows, 1) || !make_row_tmap(&tv, V, rows, 1) ||
         !make_row_tmap(&tlq, w.lqhi, lrows, 1) || !make_row_tmap(&tlv, w.lvbf, lrows, 1))
         return cudaErrorInvalidValue;
-    const size_t sm = smem_bytes(a.nblk);
-    auto kern = multi ? expert_tc_kernel<true> : expert_tc_kernel<false>;
+    const size_t sm = smem_bytes(a.nblk, p.split);
+    auto kern = multi ? expert_tc_kernel<kMulti> : (p.split ? expert_tc_kernel<kSplit> : expert_tc_kernel<kPlain>);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(sm));
     if (e != cudaSuccess) return e;
     kern<<<device_sms(), NT, sm, st>>>(tq, tk, tv, tlq, tlv, a);

@@ -147,8 +147,10 @@ cudaError_t launch_route(const Plan& p, const Work& w, const __nv_bfloat16* Q, i
 
 cudaError_t launch_expert(const Plan& p, const Work& w, const __nv_bfloat16* Q, const __nv_bfloat16* K,
                           const __nv_bfloat16* V, const int32_t* expert_idx, __nv_bfloat16* out, cudaStream_t st) {
-    // tensor cores when the experts hold enough queries to fill 128-row tiles
-    if (expert_tc_supported(p) && p.s.N >= 32LL * p.s.m) return launch_expert_tc(p, w, Q, K, V, expert_idx, out, st);
+    // tensor cores wherever the kernel applies, also for experts with few
+    // queries (the 128-row tiles run part-empty; still several times faster
+    // than the CUDA-core kernel, measured on the ViT shapes)
+    if (expert_tc_supported(p)) return launch_expert_tc(p, w, Q, K, V, expert_idx, out, st);
     return launch_expert_simt(p, w, Q, K, V, expert_idx, out, st);
 }
 
@@ -190,7 +192,7 @@ ScanLevel scan_level(const Shape& s, int64_t S, int64_t stride, int64_t prevS, i
 
 }  // namespace
 
-bool make_plan(const Shape& s, Plan* p, bool shared) {
+bool make_plan(const Shape& s, Plan* p, bool shared, bool split) {
     Plan P{};
     P.s = s;
     P.shared = shared;
@@ -265,6 +267,10 @@ bool make_plan(const Shape& s, Plan* p, bool shared) {
         P.nlev = 1;
         P.lev[0] = L;
     }
+    // on request, the shared branch goes with the routing when the
+    // tensor-core kernels of both sides apply (and the scan is the
+    // tensor-core one)
+    P.split = split && P.scan_tc && route_shared_supported(P) && expert_split_fits(P);
     P.rblock = 256;
     P.nrblocks = (s.N + P.rblock - 1) / P.rblock;
     P.qtile = 128;
@@ -314,10 +320,12 @@ bool make_plan(const Shape& s, Plan* p, bool shared) {
     P.off_state = take(expert_multi_state_bytes(P));
     // s > 1: tensor-core passes where the one-expert kernel applies (same
     // conditions as launch_expert) and the overlap table stays below 1 GB
-    P.multi_tc = s.s_route > 1 && expert_tc_supported(P) && s.N >= 32LL * s.m && s.m <= 256 &&
+    P.multi_tc = s.s_route > 1 && expert_tc_supported(P) && s.m <= 256 &&
                  overlap_bytes(s) <= (size_t(1) << 30) && pass_mask_bytes(s) <= (size_t(4) << 30);
     P.off_ovl = take(P.multi_tc ? overlap_bytes(s) : 0);
     P.off_mask = take(P.multi_tc ? pass_mask_bytes(s) : 0);
+    P.off_osh = take(P.split ? BH * static_cast<size_t>(s.N) * D * 2 : 0);
+    P.off_lse = take(P.split ? BH * static_cast<size_t>(s.N) * sizeof(float) : 0);
     P.total = off;
     if (P.max_items * s.BH > 0x7FFFFFFFLL || s.BH * P.nrblocks > 0x7FFFFFFFLL) return false;
     for (int l = 0; l < P.nlev; ++l)
@@ -351,6 +359,8 @@ Work carve(const Plan& p, void* base) {
     w.state = reinterpret_cast<float*>(b + p.off_state);
     w.ovl = reinterpret_cast<uint64_t*>(b + p.off_ovl);
     w.mask = reinterpret_cast<uint64_t*>(b + p.off_mask);
+    w.osh = reinterpret_cast<__nv_bfloat16*>(b + p.off_osh);
+    w.lse = reinterpret_cast<float*>(b + p.off_lse);
     bool any_dense = false;
     for (int l = 0; l < p.nlev; ++l) any_dense = any_dense || p.lev[l].dense;
     w.dense = any_dense ? reinterpret_cast<float*>(b + p.off_dense) : nullptr;
@@ -429,7 +439,8 @@ int run_forward(const Plan& P, const Work& W, const __nv_bfloat16* Q, const __nv
     marks.mark(3);
     if ((e = launch_select(P, W, expert_idx, st)) != cudaSuccess) return cuda_fail(e, "expert selection launch");
     marks.mark(4);
-    if ((e = launch_route(P, W, Q, route, st)) != cudaSuccess) return cuda_fail(e, "routing launch");
+    e = P.split ? launch_route_shared(P, W, Q, route, st) : launch_route(P, W, Q, route, st);
+    if (e != cudaSuccess) return cuda_fail(e, "routing launch");
     marks.mark(5);
     for (int j = 0; j < sr; ++j)
         if ((e = launch_group(P, W, route, j, st)) != cudaSuccess) return cuda_fail(e, "grouping launch");
@@ -469,7 +480,7 @@ namespace {
 // ablation.
 int forward_device(const void* Q, const void* K, const void* V, int B, int H, int N, int d, int grid_h, int grid_w,
                    int m, int k, void* out, int32_t* expert_idx, int32_t* route, float* lq, float* lv, void* stream,
-                   bool shared, int s_route = 1) {
+                   bool shared, int s_route = 1, bool split = false) {
     g_err[0] = 0;
     Shape s;
     bool empty;
@@ -483,7 +494,7 @@ int forward_device(const void* Q, const void* K, const void* V, int B, int H, in
     if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(out))
         return fail(MITA_ERR_INVALID_ARG, "Q, K, V and out must be 16-byte aligned");
     Plan P;
-    if (!make_plan(s, &P, shared)) return fail(MITA_ERR_UNSUPPORTED, "problem too large for the launch grids");
+    if (!make_plan(s, &P, shared, split)) return fail(MITA_ERR_UNSUPPORTED, "problem too large for the launch grids");
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     void* base = nullptr;
     if ((rc = workspace(st, 0, P.total, &base)) != MITA_OK) return rc;
@@ -506,6 +517,13 @@ extern "C" int mita_forward_routed(const void* Q, const void* K, const void* V, 
                                    void* stream) {
     return forward_device(Q, K, V, B, H, N, d, grid_h, grid_w, m, k, out, expert_idx, route, nullptr, nullptr, stream,
                           false);
+}
+
+extern "C" int mita_forward_split(const void* Q, const void* K, const void* V, int B, int H, int N, int d, int grid_h,
+                                  int grid_w, int m, int k, void* out, int32_t* expert_idx, int32_t* route,
+                                  void* stream) {
+    return forward_device(Q, K, V, B, H, N, d, grid_h, grid_w, m, k, out, expert_idx, route, nullptr, nullptr, stream,
+                          true, 1, true);
 }
 
 extern "C" int mita_forward_multi(const void* Q, const void* K, const void* V, int B, int H, int N, int d, int grid_h,

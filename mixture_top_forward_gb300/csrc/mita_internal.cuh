@@ -64,14 +64,20 @@ struct Plan {
     // s > 1 routing: the attention passes run on the tensor cores (with the
     // expert overlap table) or, where that kernel does not apply, on the CUDA cores
     bool multi_tc;
+    // s = 1 with the shared branch on the tensor cores: the routing kernel also
+    // forms each query's softmax partial over the m landmark logits (o, lse)
+    // and the expert kernel attends to the routed keys alone, continuing it
+    bool split;
     // workspace layout (byte offsets)
     size_t off_status, off_lq32, off_lqhi, off_lqlo, off_lv32, off_lvbf, off_part, off_cand, off_ccount, off_theta,
         off_counts, off_expoff, off_cursor, off_perm, off_items, off_nitems, off_dense, off_ridx, off_rval, off_rcount,
-        off_state, off_ovl, off_mask, total;
+        off_state, off_ovl, off_mask, off_osh, off_lse, total;
 };
 
 // Builds the plan; returns false if a size does not fit the int ranges used.
-bool make_plan(const Shape& s, Plan* p, bool shared = true);
+// split: fold the shared branch into the routing kernel where its kernels
+// apply (mita_forward_split).
+bool make_plan(const Shape& s, Plan* p, bool shared = true, bool split = false);
 
 // Workspace pointers derived from a plan.
 struct Work {
@@ -98,6 +104,8 @@ struct Work {
     float* state;           // [BH][N][68] running softmax state between the passes of s > 1 routing
     uint64_t* ovl;          // [BH][m][m][ceil(k/64)] expert overlap bit masks (s > 1, tensor cores)
     uint64_t* mask;         // [s-1][BH][N][ceil(k/64)] per grouping slot of ranks 1..s-1: keys already counted
+    __nv_bfloat16* osh;     // split: [BH][N][64] each query's shared-branch output (normalised)
+    float* lse;             // split: [BH][N] its log-sum-exp (log2 units of the tau-scaled logits)
 };
 
 Work carve(const Plan& p, void* base);
@@ -164,6 +172,7 @@ cudaError_t launch_route_simt(const Plan& p, const Work& w, const __nv_bfloat16*
                               cudaStream_t st);
 cudaError_t launch_route_tc(const Plan& p, const Work& w, const __nv_bfloat16* Q, int32_t* route, cudaStream_t st);
 bool route_tc_supported(const Plan& p);
+
 cudaError_t launch_group(const Plan& p, const Work& w, const int32_t* route, int j, cudaStream_t st);
 cudaError_t launch_route_multi(const Plan& p, const Work& w, const __nv_bfloat16* Q, int32_t* route,
                                cudaStream_t st);
@@ -185,6 +194,10 @@ cudaError_t launch_expert_tc(const Plan& p, const Work& w, const __nv_bfloat16* 
                              const __nv_bfloat16* V, const int32_t* expert_idx, __nv_bfloat16* out, cudaStream_t st,
                              const int32_t* route = nullptr, int j = 0);
 bool expert_tc_supported(const Plan& p);
+bool expert_split_fits(const Plan& p);
+bool route_shared_supported(const Plan& p);
+cudaError_t launch_route_shared(const Plan& p, const Work& w, const __nv_bfloat16* Q, int32_t* route,
+                                cudaStream_t st);
 
 // Backward pass: its own workspace (byte offsets) next to the forward plan's.
 struct BwdLayout {

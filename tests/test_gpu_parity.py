@@ -345,3 +345,66 @@ def test_pilot_records_overflow_to_keys(orc):
     v = synth.normal_bf16((B, H, N, 64), 43, 2)
     rep = parity.full_parity(orc, q, kk_, v, 0, 0, m, k)
     print(rep)
+
+
+# --- mita_forward_split: the shared branch folded into the routing kernel ---
+def _run_split(q, k, v, gh, gw, m, kk, full_out=True):
+    """mita_forward_split's outputs; Lq and LV (not returned by that entry
+    point) from mita_forward_aux, whose first two stages are the same."""
+    import torch
+
+    import mixture_top_forward_gb300 as M
+
+    Q, K, V = parity.to_device(q), parity.to_device(k), parity.to_device(v)
+    _, _, _, lq, lv = M.mita_forward_aux(Q, K, V, gh, gw, m, kk)
+    out, eidx, route = M.mita_forward_split(Q, K, V, gh, gw, m, kk)
+    torch.cuda.synchronize()
+    assert M.mita_sync_status() == 0
+    if full_out:
+        out = synth.bf16_to_f64(out.view(torch.int16).cpu().numpy().view(np.uint16))
+    return dict(out=out, expert_idx=eidx.cpu().numpy(), route=route.cpu().numpy(),
+                lq=lq.cpu().numpy().astype(np.float64), lv=lv.cpu().numpy().astype(np.float64))
+
+
+@pytest.mark.parametrize("name", ["tiny", "deit", "seg1024", "seg1600"])
+def test_split_config_full_oracle(orc, name):
+    q, k, v = synth.make_inputs(name)
+    rep = parity.full_parity(orc, q, k, v, *_cfg_args(name), gpu=_run_split(q, k, v, *_cfg_args(name)))
+    print(name, rep)
+
+
+@pytest.mark.parametrize("name,heads,nq", [("lra", (0, 200), 4096), ("long64k", (0, 6), 8192)])
+def test_split_config_sampled(orc, name, heads, nq):
+    q, k, v = synth.make_inputs(name)
+    gpu = _run_split(q, k, v, *_cfg_args(name), full_out=False)
+    rep = parity.sampled_parity(orc, q, k, v, *_cfg_args(name), gpu, heads, nq)
+    print(name, rep)
+
+
+@pytest.mark.parametrize("B,H,N,gh,gw,m,k", [
+    (2, 3, 1000, 0, 0, 7, 13),      # ragged windows and tiles, m_pad < m + 16
+    (2, 2, 300, 0, 0, 1, 5),        # one landmark
+    (1, 2, 4096, 0, 0, 200, 100),   # two landmark halves in the shared product
+    (1, 2, 196, 14, 14, 196, 3),    # m = N
+])
+def test_split_edge_shapes(orc, B, H, N, gh, gw, m, k):
+    q, kk_, v = _rand(B, H, N, 300 + N + m + k, 2.0)
+    rep = parity.full_parity(orc, q, kk_, v, gh, gw, m, k, gpu=_run_split(q, kk_, v, gh, gw, m, k))
+    print(rep)
+
+
+def test_split_matches_forward():
+    """Same routes and expert sets as mita_forward, outputs within the
+    parity tolerances of each other."""
+    import torch
+
+    import mixture_top_forward_gb300 as M
+
+    q, k, v = synth.make_inputs("seg1600")
+    Q, K, V = parity.to_device(q), parity.to_device(k), parity.to_device(v)
+    a = M.mita_forward(Q, K, V, *_cfg_args("seg1600"))
+    b = M.mita_forward_split(Q, K, V, *_cfg_args("seg1600"))
+    torch.cuda.synchronize()
+    assert torch.equal(a[1], b[1]) and torch.equal(a[2], b[2])
+    err = (a[0].float() - b[0].float()).abs()
+    assert err.max().item() <= parity.OUT_MAX and err.mean().item() <= parity.OUT_MEAN
