@@ -281,7 +281,9 @@ bool make_plan(const Shape& s, Plan* p, bool shared, bool split) {
     for (int l = 0; l < P.nlev; ++l) {
         // the tensor-core pilot scans append 8-column groups as records first
         // (keys only once a landmark's records are full); the main scan and
-        // the CUDA-core scan append keys
+        // the CUDA-core scan append keys (records in the main scan measured
+        // faster there at 256K and 64K, but the select's expansion of them
+        // costs more than that: a net loss at 1M, even at 64K)
         if (!(P.scan_tc && !P.lev[l].dense && l + 1 < P.nlev)) P.lev[l].rcap = 0;
         cand = std::max(cand, BH * P.lev[l].chunks * m * static_cast<size_t>(P.lev[l].cap));
         recs = std::max(recs, BH * P.lev[l].chunks * m * static_cast<size_t>(P.lev[l].rcap));

@@ -115,7 +115,8 @@ __global__ void __launch_bounds__(ST) select_kernel(int m, int k, int chunks, in
     // would have made them (non-finite logits are masked columns: dropped)
     const uint64_t thr_key = thr_in ? thr_in[bh * m + i] : 0;
     auto recs_of = [&](int c) { return rcap > 0 ? rcount[(bh * chunks + c) * m + i] : 0; };
-    auto rec_keys = [&](int c, int r, auto&& f) {
+    // f(j, key) for each column j (0..7, unrolled) of record r of chunk c that becomes a key
+    auto rec_keys_at = [&](int c, int r, auto&& f) {
         const int64_t at = ((bh * chunks + c) * m + i) * static_cast<int64_t>(rcap) + r;
         const uint32_t b0 = ridx[at];
         const float4 v0 = reinterpret_cast<const float4*>(rval)[2 * at];
@@ -125,10 +126,11 @@ __global__ void __launch_bounds__(ST) select_kernel(int m, int k, int chunks, in
         for (int j = 0; j < 8; ++j) {
             if (sc[j] >= -3.402823466e38f && sc[j] <= 3.402823466e38f) {
                 const uint64_t key = topk_key(sc[j] * 0.125f, static_cast<uint32_t>((b0 + j) * stride));
-                if (key >= thr_key) f(key);
+                if (key >= thr_key) f(j, key);
             }
         }
     };
+    auto rec_keys = [&](int c, int r, auto&& f) { rec_keys_at(c, r, [&](int, uint64_t key) { f(key); }); };
     int total = 0;
     if (drow) {
         total = static_cast<int>(N);
@@ -151,18 +153,39 @@ __global__ void __launch_bounds__(ST) select_kernel(int m, int k, int chunks, in
         if (tid == 0) nst = 0;
         __syncthreads();
         total = offs[ST];
-        // the records' keys go after the plain keys (one warp per chunk);
-        // the count stays exact past SEL_CAP
+        // the records' keys go after the plain keys (one warp per chunk, a
+        // record per lane; one shared-memory atomic per warp and round
+        // reserves the round's slots); the count stays exact past SEL_CAP
         if (rcap > 0) {
             if (tid == 0) nst = total;
             __syncthreads();
             for (int c = wid; c < chunks; c += ST / 32) {
                 const int nr = recs_of(c);
-                for (int r = lane; r < nr; r += 32)
-                    rec_keys(c, r, [&](uint64_t key) {
-                        const int pos = atomicAdd(&nst, 1);
-                        if (pos < SEL_CAP) staged[pos] = key;
-                    });
+                for (int r0 = 0; r0 < nr; r0 += 32) {
+                    uint64_t key[8];
+                    unsigned acc = 0;
+                    if (r0 + lane < nr)
+                        rec_keys_at(c, r0 + lane, [&](int j, uint64_t x) {
+                            key[j] = x;
+                            acc |= 1u << j;
+                        });
+                    const int mine = __popc(acc);
+                    int incl = mine;
+#pragma unroll
+                    for (int o = 1; o < 32; o <<= 1) {
+                        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+                        if (lane >= o) incl += y;
+                    }
+                    int base = 0;
+                    if (lane == 31) base = atomicAdd(&nst, incl);
+                    int pos = __shfl_sync(0xffffffffu, base, 31) + incl - mine;
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        if ((acc >> j) & 1u) {
+                            if (pos < SEL_CAP) staged[pos] = key[j];
+                            ++pos;
+                        }
+                }
             }
             __syncthreads();
             total = nst;
