@@ -26,9 +26,8 @@
 //                  Per 64-key tile a thread loads its 64 scores and offers
 //                  them to its landmark's candidate buffers: an 8-column
 //                  group whose maximum reaches the threshold goes out whole
-//                  as a record when the level has records (three stores;
-//                  the select expands it), and key by key otherwise, or
-//                  once the records are full
+//                  as a record in pilot scans (the select expands it), and
+//                  key by key otherwise, or once the records are full
 //                  (topk.cuh: append when the 64-bit order key reaches the
 //                  threshold, warp-cooperative compaction on overflow); in
 //                  full scans it also runs the online softmax (lazy running
@@ -343,7 +342,7 @@ __global__ void __launch_bounds__(Cfg<FULL, NL>::NT, 1)
                 float* slot = reinterpret_cast<float*>(hist) + lane * 8;
 #pragma unroll
                 for (int g = 0; g < KT / 8; ++g) {
-                    if (gm[g] >= thr && rc < a.rcap) {
+                    if (!FULL && gm[g] >= thr && rc < a.rcap) {  // (pilot scans only)
                         rix[rc] = static_cast<uint32_t>(col0 + 8 * g);
                         rvl[2 * rc] = make_float4(s[8 * g], s[8 * g + 1], s[8 * g + 2], s[8 * g + 3]);
                         rvl[2 * rc + 1] = make_float4(s[8 * g + 4], s[8 * g + 5], s[8 * g + 6], s[8 * g + 7]);
@@ -435,7 +434,7 @@ __global__ void __launch_bounds__(Cfg<FULL, NL>::NT, 1)
             }
         }
         if (row_ok && !a.dense) a.ccount[slot] = cnt;
-        if (row_ok && a.rcap > 0) a.rcount[slot] = rc;
+        if (!FULL && row_ok && a.rcap > 0) a.rcount[slot] = rc;
     }
     tc_fence_before();
     __syncthreads();
