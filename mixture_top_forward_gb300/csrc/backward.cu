@@ -340,6 +340,24 @@ __global__ void __launch_bounds__(BT) exp_bwd_kernel(
     }
 }
 
+// Tensor-core path, per landmark: Delta'_i = dLV_i . LV_i, the log-sum-exp
+// in log2 units, and dLV_i rounded to bf16 (an MMA operand).
+__global__ void __launch_bounds__(BT) lm_prep_kernel(int64_t rows, const float* __restrict__ dlv,
+                                                     const float* __restrict__ lv, const float* __restrict__ lse,
+                                                     float* __restrict__ dlt, float* __restrict__ lse2,
+                                                     __nv_bfloat16* __restrict__ dlvb) {
+    const int64_t x = static_cast<int64_t>(blockIdx.x) * BT + threadIdx.x;
+    if (x >= rows) return;
+    float s = 0.f;
+#pragma unroll
+    for (int c = 0; c < D; ++c) {
+        s = fmaf(dlv[x * D + c], lv[x * D + c], s);
+        dlvb[x * D + c] = __float2bfloat16_rn(dlv[x * D + c]);
+    }
+    dlt[x] = s;
+    lse2[x] = lse[x] * kLog2e;
+}
+
 // Delta'_i = dLV_i . LV_i
 __global__ void __launch_bounds__(BT) lm_delta_kernel(int64_t rows, const float* __restrict__ dlv,
                                                       const float* __restrict__ lv, float* __restrict__ dlt) {
@@ -579,6 +597,12 @@ BwdLayout backward_layout(const Plan& p) {
     L.off_dlv = take(BH * m * D * sizeof(float));
     L.off_dlt = take(BH * m * sizeof(float));
     L.off_route = take(BH * N * sizeof(int32_t));
+    const bool tc = backward_tc_supported(p);
+    L.off_qlse = take(tc ? BH * N * sizeof(float) : 0);
+    L.off_qdelta = take(tc ? BH * N * sizeof(float) : 0);
+    L.off_eidx = take(tc ? BH * m * static_cast<size_t>(p.s.k) * sizeof(int32_t) : 0);
+    L.off_lse2 = take(tc ? BH * m * sizeof(float) : 0);
+    L.off_dlvb = take(tc ? BH * m * D * 2 : 0);
     L.total = off;
     return L;
 }
@@ -607,6 +631,42 @@ cudaError_t launch_backward(const Plan& p, const Work& w, const BwdLayout& L, vo
         (e = cudaMemsetAsync(w.nitems, 0, sizeof(int), st)) != cudaSuccess)
         return e;
     if ((e = launch_pool(p, w, Q, st)) != cudaSuccess) return e;
+    if (backward_tc_supported(p) && expert_tc_supported(p) && p.scan_tc && !p.split) {
+        // Tensor-core path. Landmark statistics: the forward pass's scan and
+        // merge (LV in fp32 and bf16, each landmark's log-sum-exp); the expert
+        // sets it selects go to scratch (the caller's are the ones used).
+        int32_t* eidx = reinterpret_cast<int32_t*>(b + L.off_eidx);
+        float* qlse = reinterpret_cast<float*>(b + L.off_qlse);
+        float* qdelta = reinterpret_cast<float*>(b + L.off_qdelta);
+        float* lse2 = reinterpret_cast<float*>(b + L.off_lse2);
+        __nv_bfloat16* dlvb = reinterpret_cast<__nv_bfloat16*>(b + L.off_dlvb);
+        if (p.nlev > 1 && (e = cudaMemsetAsync(w.theta, 0, mrows * sizeof(uint64_t), st)) != cudaSuccess) return e;
+        for (int l = 0; l + 1 < p.nlev; ++l) {
+            if ((e = launch_scan_tc(p, w, K, V, l, st)) != cudaSuccess) return e;
+            if ((e = launch_pilot_select(p, w, l, st)) != cudaSuccess) return e;
+        }
+        if ((e = launch_scan_tc(p, w, K, V, p.nlev - 1, st)) != cudaSuccess) return e;
+        if ((e = launch_select(p, w, eidx, st, lse)) != cudaSuccess) return e;
+        // routes (checked) and grouping, then each query's statistics
+        const int64_t rb = cdiv64(N, 256);
+        route_count_kernel<<<static_cast<unsigned>(BH * rb), 256, 0, st>>>(route, N, m, rb, route_ok, w.counts,
+                                                                             w.status);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        if ((e = launch_group(p, w, route_ok, 0, st)) != cudaSuccess) return e;
+        if ((e = launch_expert_stats(p, w, Q, K, V, expert_idx, dO, qlse, qdelta, st)) != cudaSuccess) return e;
+        // expert attention: dQ, dK, dV of the routed keys, dLq, dLV of the shared ones
+        if ((e = launch_backward_tc_expert(p, w, Q, K, V, dO, expert_idx, qlse, qdelta, dQ, dK, dV, dlq, dlv, st)) !=
+            cudaSuccess)
+            return e;
+        // landmark attention: dK, dV, dLq
+        lm_prep_kernel<<<static_cast<unsigned>(cdiv64(BH * m, BT)), BT, 0, st>>>(BH * m, dlv, w.lv32, lse, dlt, lse2,
+                                                                                 dlvb);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        if ((e = launch_backward_tc_landmark(p, w, K, V, dlvb, lse2, dlt, dK, dV, dlq, st)) != cudaSuccess) return e;
+        pool_bwd_kernel<<<static_cast<unsigned>(cdiv64(BH * N, 256)), 256, 0, st>>>(BH, N, p.s.gh, p.s.gw, p.s.p, m,
+                                                                                     dlq, dQ);
+        return cudaGetLastError();
+    }
     const unsigned g1 = static_cast<unsigned>(BH * L.ltiles * L.chunks);
     lm_stats_kernel<<<g1, BT, 0, st>>>(K, V, N, m, L.ltiles, L.chunks, L.chunk_len, w.lq32, part);
     lm_merge_kernel<<<static_cast<unsigned>(cdiv64(BH * m, BT)), BT, 0, st>>>(BH, m, L.chunks, part, lv, lse);

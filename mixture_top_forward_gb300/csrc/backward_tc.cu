@@ -1,0 +1,779 @@
+// Backward pass on the tensor cores (tcgen05, TMEM): the four dense products
+// of the two attentions of MiTA, for the gradients declared in backward.cu.
+//
+// The forward pass is written in "NeurIPS 2026 | Mixture-of-Top-k 注意力"
+// (shuwu5.cn), section "MiTA：用少量地标查询，同时完成压缩与专家构造"; the pages
+// train MiTA models (results section) but do not describe their backward
+// pass. With tau = 1/sqrt(64), z = tau <row, key> log2(e), and per row its
+// log-sum-exp L (log2 units) and Delta = dR . out:
+//   p = 2^(z - L),   ds = p (<dR, value> - Delta),
+//   row gradient     G_row = tau sum_key ds key           (rows kernel)
+//   key gradients    dK_key = tau sum_row ds row,  dV_key = sum_row p dR
+//                                                          (keys kernel)
+// Two attentions have this form:
+//   expert attention (EXP): rows = the queries routed to an expert (dR = dO),
+//     keys = its list [Lq_0..Lq_{m-1} (bf16, as the forward pass reads them),
+//     K_j (j in E_e)], values [LV_0..LV_{m-1} (bf16), V_j]: G -> dQ, dK/dV of
+//     the shared keys -> dLq, dLV, of the routed keys -> dK, dV;
+//   landmark attention (LMK): rows = the landmarks (Lq as a bf16 hi/lo pair,
+//     as the forward scan reads them; dR = dLV), keys = all of the head's K,
+//     values V: G -> dLq, dK/dV -> dK, dV.
+//
+// Rows kernel (rows on the MMA's M dimension, one thread per row): per block
+// of 64 keys S = R K^T and dP = dR V^T into TMEM, the rows form ds (bf16) in
+// TMEM, and G += ds K (A in TMEM, the same key rows as the MN-major B). One
+// work unit = 128 rows: an item (<= 128 queries of one expert) or a landmark
+// tile with one chunk of keys.
+// Keys kernel (keys on M, one thread per key): per tile of 128 rows
+// S^T = K R^T and dP^T = V dR^T, the key threads form p^T and ds^T (bf16) in
+// TMEM with each row's L and Delta read from shared memory, then
+// dV += p^T dR and dK += ds^T R (A in TMEM, the row tiles as MN-major B),
+// accumulated over all the rows of the unit. One work unit = 128 keys: a
+// block of an expert's list (rows: that expert's queries) or a tile of the
+// head's keys (rows: its landmarks).
+// Warps: 0-3 the 128 row (or key) threads, 4 the producer (TMA), 5 the MMA
+// issuer. Every wait is bounded (umma.cuh).
+#include <algorithm>
+
+#include "tensormap.cuh"
+#include "umma.cuh"
+
+namespace mita {
+
+namespace {
+
+using namespace umma;
+
+constexpr float kTau = 0.125f;
+constexpr float kC = 0.125f * kLog2e;  // tau * log2(e)
+constexpr int kExp = 0, kLmk = 1;       // expert attention / landmark attention
+constexpr int NTB = 192;               // 4 row warps, producer, issuer
+constexpr int TILE = 16384;            // 128 rows of 64 bf16
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// Problem description shared by both kernels (pointers a mode does not use are null).
+struct BArgs {
+    const int4* items;          // EXP rows kernel: the flat item list and its length
+    const int* nitems;
+    const int* expoff;          // EXP keys kernel: [BH][m+1] each expert's first grouped query
+    const int* perm;            // [BH][N] queries grouped by expert
+    const int32_t* expert_idx;  // [BH][m][k]
+    const float* lse;           // EXP: [BH][N] per query; LMK: [BH][m] per landmark (log2 units)
+    const float* delta;         // same layout: Delta of each row
+    float* gk;                  // keys kernel: dK target ([BH][N][64], += ), rows kernel: G target (EXP: dQ, =)
+    float* gv;                  // keys kernel: dV target ([BH][N][64], +=); LMK rows kernel: dLq (atomic)
+    float* slq;                 // EXP keys kernel: dLq of the shared keys ([BH][m][64], atomic)
+    float* slv;                 // EXP keys kernel: dLV of the shared keys ([BH][m][64], atomic)
+    int* status;
+    int64_t N, units, chunk_len;
+    int m, k, m4, nblk, chunks;
+};
+
+
+// Rows of expert list position x (EXP): the shared rows [0, m) are landmark
+// rows (clamped), positions [m, m4) are unused, [m4, m4 + k) routed keys
+// (clamped to the last). Four consecutive positions never straddle m4.
+__device__ __forceinline__ void list_rows4(const BArgs& a, int64_t bh, const int32_t* sel, int x, int* y, bool* shared) {
+    *shared = x < a.m4;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        const int xx = x + u;
+        y[u] = *shared ? static_cast<int>(bh * a.m + min(xx, a.m - 1))
+                       : static_cast<int>(bh * a.N + sel[min(xx - a.m4, a.k - 1)]);
+    }
+}
+
+// ============================================================================
+// Keys kernel
+// ============================================================================
+// shared memory: KB, VB at 0 and 16 KB; row tile buffers b = 0, 1 at
+// 32 KB + b * 49 KB: R, R_lo (LMK), dR, then L[128] and Delta[128]
+constexpr size_t KOFF_BUF = 32768, KBUF = 3 * TILE + 1024;
+constexpr size_t KSMEM = KOFF_BUF + 2 * KBUF + 1024;
+// TMEM columns
+constexpr uint32_t cS = 0, cDP = 128, cP = 256, cDS = 320, cV = 384, cK = 448;
+
+template <int MODE>
+__device__ __forceinline__ void keys_unit(const BArgs& a, int64_t u, int64_t& bh, int& e, int& b, int& ntiles,
+                                          int& qoff, int& qcnt) {
+    if (MODE == kExp) {
+        bh = u / (static_cast<int64_t>(a.m) * a.nblk);
+        e = static_cast<int>((u / a.nblk) % a.m);
+        b = static_cast<int>(u % a.nblk);
+        const int* eo = a.expoff + bh * (a.m + 1);
+        qoff = eo[e];
+        qcnt = eo[e + 1] - qoff;
+        ntiles = (qcnt + 127) / 128;
+    } else {
+        const int64_t nkt = (a.N + 127) / 128;
+        bh = u / nkt;
+        b = static_cast<int>(u % nkt);
+        e = 0;
+        qoff = 0;
+        qcnt = a.m;
+        ntiles = (a.m + 127) / 128;
+    }
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(NTB, 1)
+    bwd_keys_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
+                    const __grid_constant__ CUtensorMap tsk, const __grid_constant__ CUtensorMap tsv,
+                    const __grid_constant__ CUtensorMap tr, const __grid_constant__ CUtensorMap tdr, BArgs a) {
+    // EXP: tk, tv, tsk, tsv: K, V, Lq (bf16), LV (bf16) rows, one row high
+    //      (gathers); tr, tdr: Q, dO rows, one row high.
+    // LMK: tk, tv: K, V, 128 rows high; tr, tsk: Lq hi, lo; tdr: dLV (bf16),
+    //      128 rows high.
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ uint64_t kvfull, kvfree, rfull[2], rfree[2], sfull, sfree, pfull, pvdone, afree, drain;
+    __shared__ uint32_t tmem_base;
+    uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int64_t u0 = a.units * blockIdx.x / gridDim.x, u1 = a.units * (blockIdx.x + 1) / gridDim.x;
+    if (tid == 0) {
+        mbar_init(&kvfull, 1);
+        mbar_init(&kvfree, 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&rfull[b], 2);  // the loads' transaction count, and the statistics
+            mbar_init(&rfree[b], 1);
+        }
+        mbar_init(&sfull, 1);
+        mbar_init(&sfree, 4);
+        mbar_init(&pfull, 4);
+        mbar_init(&pvdone, 1);
+        mbar_init(&afree, 4);
+        mbar_init(&drain, 1);
+        fence_barrier_init();
+    }
+    if (warp == 0) tmem_alloc(&tmem_base, 512);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tb = tmem_base;
+    uint8_t* KBs = base;
+    uint8_t* VBs = base + TILE;
+    auto rbuf = [&](int b) { return base + KOFF_BUF + b * KBUF; };
+
+    if (warp == 4) {
+        // ---------------------------------- producer ----------------------------------
+        int ucount = 0, tseq = 0;
+        bool ok = true;
+        for (int64_t u = u0; u < u1 && ok; ++u) {
+            int64_t bh;
+            int e, b, ntiles, qoff, qcnt;
+            keys_unit<MODE>(a, u, bh, e, b, ntiles, qoff, qcnt);
+            if (ntiles == 0) continue;
+            if (ucount >= 1) ok = __all_sync(0xffffffffu, mbar_wait(&kvfree, (ucount - 1) & 1, a.status));
+            if (!ok) break;
+            if (lane == 0) mbar_arrive_expect_tx(&kvfull, 2 * TILE);
+            __syncwarp();
+            if (MODE == kExp) {  // list positions 128 b + 4 lane .. + 3
+                const int32_t* sel = a.expert_idx + (bh * a.m + e) * static_cast<int64_t>(a.k);
+                int y[4];
+                bool sh;
+                list_rows4(a, bh, sel, 128 * b + 4 * lane, y, &sh);
+                tma_gather4(KBs + 4 * lane * 128, sh ? &tsk : &tk, 0, y[0], y[1], y[2], y[3], &kvfull);
+                tma_gather4(VBs + 4 * lane * 128, sh ? &tsv : &tv, 0, y[0], y[1], y[2], y[3], &kvfull);
+            } else if (lane == 0) {
+                tma_load_2d(KBs, &tk, 0, static_cast<int>(bh * a.N + 128 * b), &kvfull);
+                tma_load_2d(VBs, &tv, 0, static_cast<int>(bh * a.N + 128 * b), &kvfull);
+            }
+            for (int t = 0; t < ntiles && ok; ++t) {
+                const int buf = tseq & 1;
+                if (tseq >= 2) ok = __all_sync(0xffffffffu, mbar_wait(&rfree[buf], ((tseq >> 1) - 1) & 1, a.status));
+                if (!ok) break;
+                uint8_t* rb = rbuf(buf);
+                float* sl = reinterpret_cast<float*>(rb + 3 * TILE);
+                if (lane == 0) mbar_arrive_expect_tx(&rfull[buf], (MODE == kExp ? 2 : 3) * TILE);
+                __syncwarp();
+                const int r0 = 4 * lane;
+                if (MODE == kExp) {  // the tile's queries (padding repeats the last)
+                    const int* pp = a.perm + bh * a.N + qoff + 128 * t;
+                    const int cnt = min(128, qcnt - 128 * t);
+                    int q[4];
+#pragma unroll
+                    for (int x = 0; x < 4; ++x) q[x] = pp[min(r0 + x, cnt - 1)];
+                    const int y = static_cast<int>(bh * a.N);
+                    tma_gather4(rb + r0 * 128, &tr, 0, y + q[0], y + q[1], y + q[2], y + q[3], &rfull[buf]);
+                    tma_gather4(rb + 2 * TILE + r0 * 128, &tdr, 0, y + q[0], y + q[1], y + q[2], y + q[3], &rfull[buf]);
+#pragma unroll
+                    for (int x = 0; x < 4; ++x) {
+                        const bool v = r0 + x < cnt;
+                        sl[r0 + x] = v ? a.lse[bh * a.N + q[x]] : INFINITY;
+                        sl[128 + r0 + x] = v ? a.delta[bh * a.N + q[x]] : 0.f;
+                    }
+                } else {
+                    if (lane == 0) {
+                        const int y = static_cast<int>(bh * a.m + 128 * t);
+                        tma_load_2d(rb, &tr, 0, y, &rfull[buf]);
+                        tma_load_2d(rb + TILE, &tsk, 0, y, &rfull[buf]);
+                        tma_load_2d(rb + 2 * TILE, &tdr, 0, y, &rfull[buf]);
+                    }
+#pragma unroll
+                    for (int x = 0; x < 4; ++x) {
+                        const int li = 128 * t + r0 + x;
+                        const bool v = li < a.m;
+                        sl[r0 + x] = v ? a.lse[bh * a.m + li] : INFINITY;
+                        sl[128 + r0 + x] = v ? a.delta[bh * a.m + li] : 0.f;
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&rfull[buf]);  // the statistics are in place
+                ++tseq;
+            }
+            ++ucount;
+        }
+        if (lane == 0) {  // exit: the last phase of every barrier armed here has landed
+            if (ucount > 0) mbar_drain(&kvfull, (ucount - 1) & 1);
+            for (int b = 0; b < 2; ++b) {
+                const int arms = tseq > b ? (tseq - b + 1) / 2 : 0;
+                if (arms > 0) mbar_drain(&rfull[b], (arms - 1) & 1);
+            }
+        }
+    } else if (warp == 5) {
+        // ---------------------------------- MMA issuer ----------------------------------
+        if (lane == 0) {
+            const uint32_t idS = idesc_bf16(128, 128, false), idG = idesc_bf16(128, 64, true);
+            const uint64_t kd = sdesc_sw128(smem_u32(KBs)), vd = sdesc_sw128(smem_u32(VBs));
+            int ucount = 0, tseq = 0;
+            bool ok = true;
+            for (int64_t u = u0; u < u1 && ok; ++u) {
+                int64_t bh;
+                int e, b, ntiles, qoff, qcnt;
+                keys_unit<MODE>(a, u, bh, e, b, ntiles, qoff, qcnt);
+                if (ntiles == 0) continue;
+                if (!(ok = mbar_wait(&kvfull, ucount & 1, a.status))) break;
+                for (int t = 0; t < ntiles; ++t) {
+                    const int buf = tseq & 1;
+                    if (!(ok = mbar_wait(&rfull[buf], (tseq >> 1) & 1, a.status))) break;
+                    if (tseq >= 1 && !(ok = mbar_wait(&sfree, (tseq - 1) & 1, a.status))) break;
+                    tc_fence_after();
+                    const uint32_t rs = smem_u32(rbuf(buf));
+                    mma_ss_k64(tb + cS, kd, sdesc_sw128(rs), idS, 0u);
+                    if (MODE == kLmk) mma_ss_k64(tb + cS, kd, sdesc_sw128(rs + TILE), idS, 1u);
+                    mma_ss_k64(tb + cDP, vd, sdesc_sw128(rs + 2 * TILE), idS, 0u);
+                    mma_commit(&sfull);
+                    if (!(ok = mbar_wait(&pfull, tseq & 1, a.status))) break;
+                    // the first products of a unit overwrite the accumulators: the
+                    // key threads have read the previous unit's
+                    if (t == 0 && ucount >= 1 && !(ok = mbar_wait(&afree, (ucount - 1) & 1, a.status))) break;
+                    tc_fence_after();
+                    const uint64_t dr = sdesc_sw128(rs + 2 * TILE), rr = sdesc_sw128(rs);
+#pragma unroll 1
+                    for (int s = 0; s < 8; ++s) {  // K = the tile's 128 rows, 16 per step
+                        const uint32_t acc = (t > 0 || s > 0) ? 1u : 0u;
+                        mma_ts(tb + cV, tb + cP + 8 * s, dr + static_cast<uint64_t>(s) * 128, idG, acc);
+                        mma_ts(tb + cK, tb + cDS + 8 * s, rr + static_cast<uint64_t>(s) * 128, idG, acc);
+                    }
+                    mma_commit(&pvdone);
+                    mma_commit(&rfree[buf]);
+                    ++tseq;
+                }
+                if (!ok) break;
+                mma_commit(&kvfree);
+                ++ucount;
+            }
+            mma_drain(&drain);
+        }
+    } else {
+        // ------------------------------- key threads -------------------------------
+        const int t_ = (warp & 3) * 32 + lane;  // TMEM lane = key row of the unit
+        const uint32_t lo = static_cast<uint32_t>((warp & 3) * 32) << 16;
+        int ucount = 0, tseq = 0;
+        bool ok = true;
+        for (int64_t u = u0; u < u1 && ok; ++u) {
+            int64_t bh;
+            int e, b, ntiles, qoff, qcnt;
+            keys_unit<MODE>(a, u, bh, e, b, ntiles, qoff, qcnt);
+            if (ntiles == 0) continue;
+            for (int t = 0; t < ntiles && ok; ++t) {
+                const int buf = tseq & 1;
+                ok = __all_sync(0xffffffffu, mbar_wait(&sfull, tseq & 1, a.status));
+                if (!ok) break;
+                tc_fence_after();
+                // p^T and ds^T go where the previous tile's products read them
+                if (tseq >= 1) {
+                    ok = __all_sync(0xffffffffu, mbar_wait(&pvdone, (tseq - 1) & 1, a.status));
+                    if (!ok) break;
+                    tc_fence_after();
+                }
+                const float* sl = reinterpret_cast<const float*>(rbuf(buf) + 3 * TILE);
+#pragma unroll 1
+                for (int c = 0; c < 4; ++c) {  // 32 rows of the tile at a time
+                    float sv[32], dv[32];
+                    tmem_ld32(tb + cS + 32 * c + lo, sv);
+                    tmem_ld32(tb + cDP + 32 * c + lo, dv);
+                    tmem_ld_wait();
+                    if (c == 3) {
+                        tc_fence_before();
+                        warp_arrive(&sfree);
+                    }
+                    uint32_t pk[16], dk[16];
+#pragma unroll
+                    for (int j = 0; j < 32; j += 4) {
+                        const float4 L = *reinterpret_cast<const float4*>(sl + 32 * c + j);
+                        const float4 Dl = *reinterpret_cast<const float4*>(sl + 128 + 32 * c + j);
+                        const float p0 = exp2f(fmaf(sv[j], kC, -L.x)), p1 = exp2f(fmaf(sv[j + 1], kC, -L.y));
+                        const float p2 = exp2f(fmaf(sv[j + 2], kC, -L.z)), p3 = exp2f(fmaf(sv[j + 3], kC, -L.w));
+                        pk[j >> 1] = pack_bf16(p0, p1);
+                        pk[(j >> 1) + 1] = pack_bf16(p2, p3);
+                        dk[j >> 1] = pack_bf16(p0 * (dv[j] - Dl.x), p1 * (dv[j + 1] - Dl.y));
+                        dk[(j >> 1) + 1] = pack_bf16(p2 * (dv[j + 2] - Dl.z), p3 * (dv[j + 3] - Dl.w));
+                    }
+                    tmem_st16u(tb + cP + 16 * c + lo, pk);
+                    tmem_st16u(tb + cDS + 16 * c + lo, dk);
+                }
+                tmem_st_wait();
+                tc_fence_before();
+                warp_arrive(&pfull);
+                ++tseq;
+            }
+            if (!ok) break;
+            // the unit's gradients of its 128 keys
+            ok = __all_sync(0xffffffffu, mbar_wait(&pvdone, (tseq - 1) & 1, a.status));
+            if (!ok) break;
+            tc_fence_after();
+            float gvv[64], gkk[64];
+            tmem_ld32(tb + cV + lo, gvv);
+            tmem_ld32(tb + cV + 32 + lo, gvv + 32);
+            tmem_ld32(tb + cK + lo, gkk);
+            tmem_ld32(tb + cK + 32 + lo, gkk + 32);
+            tmem_ld_wait();
+            tc_fence_before();
+            warp_arrive(&afree);
+            float* dkp = nullptr;
+            float* dvp = nullptr;
+            bool atomic = true;
+            if (MODE == kExp) {
+                const int x = 128 * b + t_;
+                if (x < a.m) {
+                    dkp = a.slq + (bh * a.m + x) * D;
+                    dvp = a.slv + (bh * a.m + x) * D;
+                } else if (x >= a.m4 && x < a.m4 + a.k) {
+                    const int j = a.expert_idx[(bh * a.m + e) * static_cast<int64_t>(a.k) + (x - a.m4)];
+                    dkp = a.gk + (bh * a.N + j) * D;
+                    dvp = a.gv + (bh * a.N + j) * D;
+                }
+            } else {
+                const int64_t j = 128LL * b + t_;
+                atomic = false;  // this unit alone writes these keys
+                if (j < a.N) {
+                    dkp = a.gk + (bh * a.N + j) * D;
+                    dvp = a.gv + (bh * a.N + j) * D;
+                }
+            }
+            if (dkp) {
+#pragma unroll
+                for (int c = 0; c < 64; c += 4) {
+                    const float4 kk = make_float4(gkk[c] * kTau, gkk[c + 1] * kTau, gkk[c + 2] * kTau, gkk[c + 3] * kTau);
+                    const float4 vv = make_float4(gvv[c], gvv[c + 1], gvv[c + 2], gvv[c + 3]);
+                    float4* pk4 = reinterpret_cast<float4*>(dkp + c);
+                    float4* pv4 = reinterpret_cast<float4*>(dvp + c);
+                    if (atomic) {
+                        atomicAdd(pk4, kk);
+                        atomicAdd(pv4, vv);
+                    } else {
+                        float4 x = *pk4, y = *pv4;
+                        *pk4 = make_float4(x.x + kk.x, x.y + kk.y, x.z + kk.z, x.w + kk.w);
+                        *pv4 = make_float4(y.x + vv.x, y.y + vv.y, y.z + vv.z, y.w + vv.w);
+                    }
+                }
+            }
+            ++ucount;
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_free(tb, 512);
+}
+
+// ============================================================================
+// Rows kernel
+// ============================================================================
+// shared memory: row buffers b = 0, 1 at 49 KB b: R, R_lo (LMK), dR; then a
+// ring of RST key stages of K (8 KB) and V (8 KB) rows, 64 keys each
+constexpr int RST = 4;
+constexpr size_t RBUF = 3 * TILE + 1024, ROFF_K = 2 * RBUF;
+constexpr size_t RSMEM = ROFF_K + RST * 16384 + 1024;
+// TMEM: S buffers at 0, 64; dP at 128, 192; ds (bf16 pairs) at 256, 288; G at 384
+constexpr uint32_t rS = 0, rDP = 128, rDS = 256, rG = 384;
+
+template <int MODE>
+__device__ __forceinline__ void rows_unit(const BArgs& a, int64_t u, int64_t& bh, int4& item, int& lt, int& nb,
+                                          int64_t& c0, int64_t& c1) {
+    if (MODE == kExp) {
+        item = a.items[u];
+        bh = item.w;
+        lt = 0;
+        nb = a.nblk;
+        c0 = c1 = 0;
+    } else {
+        const int lts = (a.m + 127) / 128;
+        bh = u / (static_cast<int64_t>(lts) * a.chunks);
+        lt = static_cast<int>((u / a.chunks) % lts);
+        const int c = static_cast<int>(u % a.chunks);
+        c0 = static_cast<int64_t>(c) * a.chunk_len;
+        c1 = min(a.N, c0 + a.chunk_len);
+        nb = static_cast<int>((c1 - c0 + 63) / 64);
+        item = make_int4(0, 0, 0, 0);
+    }
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(NTB, 1)
+    bwd_rows_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
+                    const __grid_constant__ CUtensorMap tsk, const __grid_constant__ CUtensorMap tsv,
+                    const __grid_constant__ CUtensorMap tr, const __grid_constant__ CUtensorMap tdr, BArgs a) {
+    // EXP: tk, tv, tsk, tsv: K, V, Lq (bf16), LV (bf16) rows one row high
+    //      (the key list gathers); tr, tdr: Q, dO rows one row high.
+    // LMK: tk, tv: K, V, 64 rows high; tr, tsk: Lq hi, lo; tdr: dLV (bf16),
+    //      128 rows high.
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ uint64_t rfull[2], rfree[2], kfull[RST], kempty[RST], sfull[2], sfree[2], pfull[2], dsfree[2];
+    __shared__ uint64_t gdone, gfree, drain;
+    __shared__ uint32_t tmem_base;
+    uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int64_t total = MODE == kExp ? *a.nitems : a.units;
+    const int64_t u0 = total * blockIdx.x / gridDim.x, u1 = total * (blockIdx.x + 1) / gridDim.x;
+    if (tid == 0) {
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&rfull[b], 1);
+            mbar_init(&rfree[b], 1);
+            mbar_init(&sfull[b], 1);
+            mbar_init(&sfree[b], 4);
+            mbar_init(&pfull[b], 4);
+            mbar_init(&dsfree[b], 1);
+        }
+        for (int s = 0; s < RST; ++s) {
+            mbar_init(&kfull[s], 1);
+            mbar_init(&kempty[s], 1);
+        }
+        mbar_init(&gdone, 1);
+        mbar_init(&gfree, 4);
+        mbar_init(&drain, 1);
+        fence_barrier_init();
+    }
+    if (warp == 0) tmem_alloc(&tmem_base, 512);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tb = tmem_base;
+    auto rbuf = [&](int b) { return base + b * RBUF; };
+    auto kst = [&](int s) { return base + ROFF_K + s * 16384; };  // K rows, then V rows at +8 KB
+
+    if (warp == 4) {
+        // ---------------------------------- producer ----------------------------------
+        int useq = 0, g = 0;
+        bool ok = true;
+        for (int64_t u = u0; u < u1 && ok; ++u) {
+            int64_t bh, c0, c1;
+            int4 item;
+            int lt, nb;
+            rows_unit<MODE>(a, u, bh, item, lt, nb, c0, c1);
+            const int buf = useq & 1;
+            if (useq >= 2) ok = __all_sync(0xffffffffu, mbar_wait(&rfree[buf], ((useq >> 1) - 1) & 1, a.status));
+            if (!ok) break;
+            uint8_t* rb = rbuf(buf);
+            if (lane == 0) mbar_arrive_expect_tx(&rfull[buf], (MODE == kExp ? 2 : 3) * TILE);
+            __syncwarp();
+            if (MODE == kExp) {  // the item's queries (padding repeats the last)
+                const int* pp = a.perm + bh * a.N + item.y;
+                const int r0 = 4 * lane, last = item.z - 1;
+                const int y = static_cast<int>(bh * a.N);
+                const int q0 = y + pp[min(r0, last)], q1 = y + pp[min(r0 + 1, last)];
+                const int q2 = y + pp[min(r0 + 2, last)], q3 = y + pp[min(r0 + 3, last)];
+                tma_gather4(rb + r0 * 128, &tr, 0, q0, q1, q2, q3, &rfull[buf]);
+                tma_gather4(rb + 2 * TILE + r0 * 128, &tdr, 0, q0, q1, q2, q3, &rfull[buf]);
+            } else if (lane == 0) {
+                const int y = static_cast<int>(bh * a.m + 128 * lt);
+                tma_load_2d(rb, &tr, 0, y, &rfull[buf]);
+                tma_load_2d(rb + TILE, &tsk, 0, y, &rfull[buf]);
+                tma_load_2d(rb + 2 * TILE, &tdr, 0, y, &rfull[buf]);
+            }
+            const int32_t* sel = MODE == kExp ? a.expert_idx + (bh * a.m + item.x) * static_cast<int64_t>(a.k) : nullptr;
+            for (int j = 0; j < nb && ok; ++j, ++g) {
+                const int s = g % RST;
+                if (g >= RST) ok = __all_sync(0xffffffffu, mbar_wait(&kempty[s], ((g / RST) - 1) & 1, a.status));
+                if (!ok) break;
+                if (lane == 0) mbar_arrive_expect_tx(&kfull[s], 16384);
+                __syncwarp();
+                uint8_t* ks = kst(s);
+                if (MODE == kExp) {  // list positions 64 j + 4 (lane % 16) .. + 3; lanes 16-31 the values
+                    const int gidx = lane & 15;
+                    int y[4];
+                    bool sh;
+                    list_rows4(a, bh, sel, 64 * j + 4 * gidx, y, &sh);
+                    if (lane < 16)
+                        tma_gather4(ks + 4 * gidx * 128, sh ? &tsk : &tk, 0, y[0], y[1], y[2], y[3], &kfull[s]);
+                    else
+                        tma_gather4(ks + 8192 + 4 * gidx * 128, sh ? &tsv : &tv, 0, y[0], y[1], y[2], y[3], &kfull[s]);
+                } else if (lane == 0) {
+                    const int y = static_cast<int>(bh * a.N + c0 + 64 * j);
+                    tma_load_2d(ks, &tk, 0, y, &kfull[s]);
+                    tma_load_2d(ks + 8192, &tv, 0, y, &kfull[s]);
+                }
+            }
+            ++useq;
+        }
+        if (lane == 0) {
+            for (int b = 0; b < 2; ++b) {
+                const int arms = useq > b ? (useq - b + 1) / 2 : 0;
+                if (arms > 0) mbar_drain(&rfull[b], (arms - 1) & 1);
+            }
+            for (int s = 0; s < RST; ++s) {
+                const int arms = g > s ? (g - s + RST - 1) / RST : 0;
+                if (arms > 0) mbar_drain(&kfull[s], (arms - 1) & 1);
+            }
+        }
+    } else if (warp == 5) {
+        // ---------------------------------- MMA issuer ----------------------------------
+        if (lane == 0) {
+            const uint32_t idS = idesc_bf16(128, 64, false), idG = idesc_bf16(128, 64, true);
+            int useq = 0, g = 0;
+            bool ok = true;
+            // G += ds(h) K(h), the unit's block h (first: overwrite G)
+            auto gstep = [&](int h, bool first) -> bool {
+                const int sb = h & 1;
+                if (!mbar_wait(&pfull[sb], (h >> 1) & 1, a.status)) return false;
+                if (first && useq >= 1 && !mbar_wait(&gfree, (useq - 1) & 1, a.status)) return false;
+                tc_fence_after();
+                const uint64_t kmn = sdesc_sw128(smem_u32(kst(h % RST)));
+                mma_ts_k64(tb + rG, tb + rDS + 32 * sb, kmn, idG, first ? 0u : 1u);
+                mma_commit(&dsfree[sb]);
+                mma_commit(&kempty[h % RST]);
+                return true;
+            };
+            for (int64_t u = u0; u < u1 && ok; ++u) {
+                int64_t bh, c0, c1;
+                int4 item;
+                int lt, nb;
+                rows_unit<MODE>(a, u, bh, item, lt, nb, c0, c1);
+                const int buf = useq & 1;
+                if (!(ok = mbar_wait(&rfull[buf], (useq >> 1) & 1, a.status))) break;
+                const uint32_t rs = smem_u32(rbuf(buf));
+                const int gfirst = g;
+                for (int j = 0; j < nb && ok; ++j, ++g) {
+                    const int s = g % RST, sb = g & 1;
+                    if (!(ok = mbar_wait(&kfull[s], (g / RST) & 1, a.status))) break;
+                    if (g >= 2 && !(ok = mbar_wait(&sfree[sb], ((g >> 1) - 1) & 1, a.status))) break;
+                    tc_fence_after();
+                    const uint32_t ks = smem_u32(kst(s));
+                    mma_ss_k64(tb + rS + 64 * sb, sdesc_sw128(rs), sdesc_sw128(ks), idS, 0u);
+                    if (MODE == kLmk) mma_ss_k64(tb + rS + 64 * sb, sdesc_sw128(rs + TILE), sdesc_sw128(ks), idS, 1u);
+                    mma_ss_k64(tb + rDP + 64 * sb, sdesc_sw128(rs + 2 * TILE), sdesc_sw128(ks + 8192), idS, 0u);
+                    mma_commit(&sfull[sb]);
+                    if (j >= 1) ok = gstep(g - 1, j == 1);
+                }
+                if (!ok) break;
+                if (!(ok = gstep(g - 1, nb == 1))) break;
+                (void)gfirst;
+                mma_commit(&gdone);
+                mma_commit(&rfree[buf]);
+                ++useq;
+            }
+            mma_drain(&drain);
+        }
+    } else {
+        // ------------------------------- row threads -------------------------------
+        const int t = (warp & 3) * 32 + lane;  // TMEM lane = row of the unit
+        const uint32_t lo = static_cast<uint32_t>((warp & 3) * 32) << 16;
+        int useq = 0, g = 0;
+        bool ok = true;
+        for (int64_t u = u0; u < u1 && ok; ++u) {
+            int64_t bh, c0, c1;
+            int4 item;
+            int lt, nb;
+            rows_unit<MODE>(a, u, bh, item, lt, nb, c0, c1);
+            // this row's statistics and where its gradient goes
+            bool row_ok;
+            int64_t orow;
+            if (MODE == kExp) {
+                row_ok = t < item.z;
+                const int n = row_ok ? a.perm[bh * a.N + item.y + t] : 0;
+                orow = bh * a.N + n;
+            } else {
+                const int li = 128 * lt + t;
+                row_ok = li < a.m;
+                orow = bh * a.m + (row_ok ? li : 0);
+            }
+            const float L = row_ok ? a.lse[orow] : INFINITY;
+            const float Dl = row_ok ? a.delta[orow] : 0.f;
+            const int nkeys = MODE == kExp ? a.m4 + a.k : static_cast<int>(c1 - c0);  // valid list positions / keys
+            for (int j = 0; j < nb && ok; ++j, ++g) {
+                const int sb = g & 1;
+                ok = __all_sync(0xffffffffu, mbar_wait(&sfull[sb], (g >> 1) & 1, a.status));
+                if (!ok) break;
+                tc_fence_after();
+                float sv[64], dv[64];
+                tmem_ld32(tb + rS + 64 * sb + lo, sv);
+                tmem_ld32(tb + rS + 64 * sb + 32 + lo, sv + 32);
+                tmem_ld32(tb + rDP + 64 * sb + lo, dv);
+                tmem_ld32(tb + rDP + 64 * sb + 32 + lo, dv + 32);
+                tmem_ld_wait();
+                tc_fence_before();
+                warp_arrive(&sfree[sb]);
+                const int x0 = 64 * j;
+                uint32_t pk[32];
+#pragma unroll
+                for (int c = 0; c < 64; c += 2) {
+                    const int x = x0 + c;
+                    // EXP: the unused positions [m, m4) and those past the list; LMK: past the chunk
+                    const bool v0 = x < nkeys && (MODE == kLmk || x < a.m || x >= a.m4);
+                    const bool v1 = x + 1 < nkeys && (MODE == kLmk || x + 1 < a.m || x + 1 >= a.m4);
+                    const float p0 = v0 ? exp2f(fmaf(sv[c], kC, -L)) : 0.f;
+                    const float p1 = v1 ? exp2f(fmaf(sv[c + 1], kC, -L)) : 0.f;
+                    pk[c >> 1] = pack_bf16(p0 * (dv[c] - Dl), p1 * (dv[c + 1] - Dl));
+                }
+                if (g >= 2) {  // ds buffer sb was last read by G of block g - 2
+                    ok = __all_sync(0xffffffffu, mbar_wait(&dsfree[sb], ((g >> 1) - 1) & 1, a.status));
+                    if (!ok) break;
+                }
+                tc_fence_after();
+                tmem_st16u(tb + rDS + 32 * sb + lo, pk);
+                tmem_st16u(tb + rDS + 32 * sb + 16 + lo, pk + 16);
+                tmem_st_wait();
+                tc_fence_before();
+                warp_arrive(&pfull[sb]);
+            }
+            if (!ok) break;
+            ok = __all_sync(0xffffffffu, mbar_wait(&gdone, useq & 1, a.status));
+            if (!ok) break;
+            tc_fence_after();
+            float gg[64];
+            tmem_ld32(tb + rG + lo, gg);
+            tmem_ld32(tb + rG + 32 + lo, gg + 32);
+            tmem_ld_wait();
+            tc_fence_before();
+            warp_arrive(&gfree);
+            if (row_ok) {
+                if (MODE == kExp) {  // dQ of the query (its first contribution: written)
+                    float4* dst = reinterpret_cast<float4*>(a.gk + orow * D);
+#pragma unroll
+                    for (int c = 0; c < 64; c += 4)
+                        dst[c / 4] = make_float4(gg[c] * kTau, gg[c + 1] * kTau, gg[c + 2] * kTau, gg[c + 3] * kTau);
+                } else {  // dLq of the landmark, summed over the key chunks
+                    float4* dst = reinterpret_cast<float4*>(a.gv + orow * D);
+#pragma unroll
+                    for (int c = 0; c < 64; c += 4)
+                        atomicAdd(dst + c / 4,
+                                  make_float4(gg[c] * kTau, gg[c + 1] * kTau, gg[c + 2] * kTau, gg[c + 3] * kTau));
+                }
+            }
+            ++useq;
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_free(tb, 512);
+}
+
+template <class Kern>
+cudaError_t launch6(Kern kern, size_t smem, int64_t grid, const CUtensorMap* m, const BArgs& a, cudaStream_t st) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    if (grid <= 0) return cudaSuccess;
+    kern<<<static_cast<unsigned>(grid), NTB, smem, st>>>(m[0], m[1], m[2], m[3], m[4], m[5], a);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+bool backward_tc_supported(const Plan& p) {
+    // the key list of an expert fits the key kernel's 128-key blocks and the
+    // rows kernel's staged 64-key blocks; the landmarks fit two 128-row tiles
+    return p.s.m <= 256 && p.s.s_route == 1 && p.s.BH * p.s.N < (int64_t(1) << 31) &&
+           p.s.BH * (p.s.m + 1) < (int64_t(1) << 31);
+}
+
+cudaError_t launch_backward_tc_expert(const Plan& p, const Work& w, const __nv_bfloat16* Q, const __nv_bfloat16* K,
+                                      const __nv_bfloat16* V, const __nv_bfloat16* dO, const int32_t* expert_idx,
+                                      const float* st_lse, const float* st_delta, float* dQ, float* dK, float* dV,
+                                      float* dlq, float* dlv, cudaStream_t st) {
+    BArgs a{};
+    a.items = w.items;
+    a.nitems = w.nitems;
+    a.expoff = w.expoff;
+    a.perm = w.perm;
+    a.expert_idx = expert_idx;
+    a.lse = st_lse;
+    a.delta = st_delta;
+    a.status = w.status;
+    a.N = p.s.N;
+    a.m = p.s.m;
+    a.k = p.s.k;
+    a.m4 = (p.s.m + 3) & ~3;
+    CUtensorMap mk, mv, msk, msv, mq, mdo;
+    const uint64_t rows = static_cast<uint64_t>(p.s.BH) * p.s.N, lrows = static_cast<uint64_t>(p.s.BH) * p.s.m;
+    if (!make_row_tmap(&mk, K, rows, 1) || !make_row_tmap(&mv, V, rows, 1) || !make_row_tmap(&msk, w.lqhi, lrows, 1) ||
+        !make_row_tmap(&msv, w.lvbf, lrows, 1) || !make_row_tmap(&mq, Q, rows, 1) || !make_row_tmap(&mdo, dO, rows, 1))
+        return cudaErrorInvalidValue;
+    const CUtensorMap maps[6] = {mk, mv, msk, msv, mq, mdo};
+    const int sms = device_sms();
+    // dQ: one unit per item (rows kernel), over the expert's list in 64-key blocks
+    a.nblk = (a.m4 + a.k + 63) / 64;
+    a.gk = dQ;
+    cudaError_t e = launch6(bwd_rows_kernel<kExp>, RSMEM, sms, maps, a, st);
+    if (e != cudaSuccess) return e;
+    // dK, dV of the routed keys and dLq, dLV of the shared ones: one unit per
+    // (head, expert, 128-key block of its list)
+    a.nblk = (a.m4 + a.k + 127) / 128;
+    a.units = p.s.BH * static_cast<int64_t>(p.s.m) * a.nblk;
+    a.gk = dK;
+    a.gv = dV;
+    a.slq = dlq;
+    a.slv = dlv;
+    return launch6(bwd_keys_kernel<kExp>, KSMEM, std::min<int64_t>(sms, a.units), maps, a, st);
+}
+
+cudaError_t launch_backward_tc_landmark(const Plan& p, const Work& w, const __nv_bfloat16* K, const __nv_bfloat16* V,
+                                        const __nv_bfloat16* dlv_bf16, const float* lse2, const float* delta,
+                                        float* dK, float* dV, float* dlq, cudaStream_t st) {
+    BArgs a{};
+    a.lse = lse2;
+    a.delta = delta;
+    a.status = w.status;
+    a.N = p.s.N;
+    a.m = p.s.m;
+    a.k = p.s.k;
+    a.m4 = (p.s.m + 3) & ~3;
+    const uint64_t rows = static_cast<uint64_t>(p.s.BH) * p.s.N, lrows = static_cast<uint64_t>(p.s.BH) * p.s.m;
+    const int sms = device_sms();
+    // dK, dV: one unit per (head, 128 keys), rows = the head's landmarks
+    {
+        CUtensorMap mk, mv, mlo, mhi, mdl;
+        if (!make_row_tmap(&mk, K, rows, 128) || !make_row_tmap(&mv, V, rows, 128) ||
+            !make_row_tmap(&mhi, w.lqhi, lrows, 128) || !make_row_tmap(&mlo, w.lqlo, lrows, 128) ||
+            !make_row_tmap(&mdl, dlv_bf16, lrows, 128))
+            return cudaErrorInvalidValue;
+        const CUtensorMap maps[6] = {mk, mv, mlo, mlo, mhi, mdl};
+        a.units = p.s.BH * ((p.s.N + 127) / 128);
+        a.gk = dK;
+        a.gv = dV;
+        cudaError_t e = launch6(bwd_keys_kernel<kLmk>, KSMEM, std::min<int64_t>(sms, a.units), maps, a, st);
+        if (e != cudaSuccess) return e;
+    }
+    // dLq: one unit per (head, 128 landmarks, chunk of keys), about 4 units per SM
+    {
+        CUtensorMap mk, mv, mlo, mhi, mdl;
+        if (!make_row_tmap(&mk, K, rows, 64) || !make_row_tmap(&mv, V, rows, 64) ||
+            !make_row_tmap(&mhi, w.lqhi, lrows, 128) || !make_row_tmap(&mlo, w.lqlo, lrows, 128) ||
+            !make_row_tmap(&mdl, dlv_bf16, lrows, 128))
+            return cudaErrorInvalidValue;
+        const CUtensorMap maps[6] = {mk, mv, mlo, mlo, mhi, mdl};
+        const int lts = (p.s.m + 127) / 128;
+        int64_t chunks = std::max<int64_t>(1, (4LL * sms + p.s.BH * lts - 1) / (p.s.BH * lts));
+        chunks = std::min<int64_t>(chunks, (p.s.N + 63) / 64);
+        a.chunk_len = ((p.s.N + chunks - 1) / chunks + 63) / 64 * 64;
+        a.chunks = static_cast<int>((p.s.N + a.chunk_len - 1) / a.chunk_len);
+        a.units = p.s.BH * lts * static_cast<int64_t>(a.chunks);
+        a.gv = dlq;
+        return launch6(bwd_rows_kernel<kLmk>, RSMEM, std::min<int64_t>(sms, a.units), maps, a, st);
+    }
+}
+
+}  // namespace mita

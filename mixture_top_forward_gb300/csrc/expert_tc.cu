@@ -85,7 +85,9 @@ __host__ __device__ constexpr uint32_t tcol_p(int w) { return 384u + 32u * w; }
 static_assert(tcol_p(NWG - 1) + 32 <= 512 && tcol_s(NWG - 1) + 64 <= tcol_o(0) && tcol_o(NWG - 1) + 64 <= tcol_p(0),
               "TMEM holds 512 columns");
 constexpr uint32_t kIdescS = idesc_bf16(128, KB, false);
-constexpr int kPlain = 0, kMulti = 1, kSplit = 2;  // kernel modes
+// kernel modes; kStats (the backward pass's statistics) runs the plain pass
+// but writes each query's log-sum-exp and Delta = dO . out instead of out
+constexpr int kPlain = 0, kMulti = 1, kSplit = 2, kStats = 3;
 constexpr uint32_t kIdescPV = idesc_bf16(128, 64, true);
 
 struct Args {
@@ -97,13 +99,26 @@ struct Args {
     int* status;
     int64_t N;
     int m, msh, k, nblk;  // msh: shared pairs taken (m, or 0 for the routing-only ablation / passes j > 0)
-    // s > 1 routing (MULTI): this launch is the pass of rank j of s
-    const uint64_t* mask;  // j > 0: [BH][N][nbw] per grouping slot, bit c of word b: key c of block b counted before
-    float* state;          // [BH][N][68]: O[64] (unnormalised), max (log2 units), sum
-    int s, j, nbw;
-    const float* lse;             // SPLIT: [BH][N] the shared branch's log-sum-exp (log2 units)
-    const __nv_bfloat16* osh;     // SPLIT: [BH][N][64] its output rows
+    int s, j, nbw;        // MULTI: this launch is the pass of rank j of s; nbw mask words per row
+    // the pointers only one mode reads share their storage (kept within 128
+    // bytes: a larger argument block made the plain kernel spill registers)
+    union {
+        struct {                   // MULTI (s > 1 routing)
+            const uint64_t* mask;  // j > 0: [BH][N][nbw] per grouping slot, bit c of word b: key c of block b counted before
+            float* state;          // [BH][N][68]: O[64] (unnormalised), max (log2 units), sum
+        };
+        struct {                        // SPLIT
+            const float* lse;           // [BH][N] the shared branch's log-sum-exp (log2 units)
+            const __nv_bfloat16* osh;   // [BH][N][64] its output rows
+        };
+        struct {                        // STATS
+            const __nv_bfloat16* dO;    // [BH][N][64] output gradients
+            float* st_lse;              // [BH][N] log-sum-exp of the m + k logits (log2 units of tau <q, key>)
+            float* st_delta;            // [BH][N] dO . out (out unrounded)
+        };
+    };
 };
+static_assert(sizeof(Args) <= 128, "the kernel argument block stays within 128 bytes");
 
 struct Layout {
     uint8_t* keys;  // nblk * 8 KB
@@ -201,12 +216,35 @@ static __device__ __noinline__ void preload_shared(uint32_t tO, const uint8_t* r
     tc_fence_before();
 }
 
+// STATS: dO_row . (O * inv) over this warp's 64 O columns at tO (row = false:
+// the O columns are still read, the dot is 0). Out of line, like the
+// preload above.
+static __device__ __noinline__ float stats_delta(uint32_t tO, const __nv_bfloat16* g, float inv, bool row) {
+    float dl = 0.f;
+#pragma unroll 1
+    for (int h = 0; h < 2; ++h) {
+        float o[32];
+        tmem_ld32(tO + h * 32, o);
+        tmem_ld_wait();
+        if (row) {
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                float gv[8];
+                unpack_bf16x8(ldg_nc_v4(g + 32 * h + 8 * c), gv);
+#pragma unroll
+                for (int u = 0; u < 8; ++u) dl = fmaf(o[8 * c + u] * inv, gv[u], dl);
+            }
+        }
+    }
+    return dl;
+}
+
 template <int MODE>
 __global__ void __launch_bounds__(NT, 1)
     expert_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                      const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tlq,
                      const __grid_constant__ CUtensorMap tlv, Args a) {
-    constexpr bool MULTI = MODE == kMulti, SPLIT = MODE == kSplit;
+    constexpr bool MULTI = MODE == kMulti, SPLIT = MODE == kSplit, STATS = MODE == kStats;
     extern __shared__ uint8_t smem_raw[];
     __shared__ uint64_t kvfull, kvfree, qfull[NWG * QB], qfree[NWG * QB], ofree[NWG];
     __shared__ uint64_t sfull[NWG], sfree[NWG], pfull[NWG], pvdone[NWG], drain;
@@ -406,10 +444,21 @@ __global__ void __launch_bounds__(NT, 1)
         bool pend = false, pend_row = false;  // an item whose epilogue is pending
         float pend_inv = 0.f;
         uint4* pend_dst = nullptr;
-        float pend_m = 0.f, pend_l = 0.f;  // MULTI: the pass's running max and sum
+        float pend_m = 0.f, pend_l = 0.f;  // MULTI, STATS: the running max and sum
         float* pend_state = nullptr;       // MULTI: the query's state row
         auto epilogue = [&]() {
-            if constexpr (!MULTI) {
+            if constexpr (STATS) {
+                // Delta = dO . (O / rowsum) in fp32, and the log-sum-exp
+                const float dl = stats_delta(tO, reinterpret_cast<const __nv_bfloat16*>(pend_dst), pend_inv,
+                                             pend_row);
+                tc_fence_before();
+                warp_arrive(&ofree[w]);
+                if (pend_row) {
+                    const int64_t qrow = (reinterpret_cast<const __nv_bfloat16*>(pend_dst) - a.dO) / D;
+                    a.st_delta[qrow] = dl;
+                    a.st_lse[qrow] = pend_m + __log2f(pend_l);
+                }
+            } else if constexpr (!MULTI) {
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {  // two 32-column halves of the output row
                     float o[32];
@@ -617,7 +666,8 @@ __global__ void __launch_bounds__(NT, 1)
             pend = true;
             pend_row = t < item.z;
             pend_inv = 1.f / lrun;
-            pend_dst = reinterpret_cast<uint4*>(a.out + (bh * a.N + n) * D);
+            // (STATS: the query's dO row instead of its output row)
+            pend_dst = reinterpret_cast<uint4*>((STATS ? const_cast<__nv_bfloat16*>(a.dO) : a.out) + (bh * a.N + n) * D);
             pend_m = mrun;
             pend_l = lrun;
             pend_state = srow;
@@ -660,7 +710,7 @@ cudaError_t launch_expert_tc(const Plan& p, const Work& w, const __nv_bfloat16* 
                              const int32_t* route, int j) {
     (void)route;  // the passes read the per-slot masks built from it
     const bool multi = p.s.s_route > 1;
-    Args a;
+    Args a{};
     a.items = w.items + static_cast<size_t>(j) * p.s.BH * p.max_items;  // the plane of rank j
     a.nitems = w.nitems + j;
     a.perm = w.perm + static_cast<size_t>(j) * p.s.BH * p.s.N;
@@ -672,13 +722,16 @@ cudaError_t launch_expert_tc(const Plan& p, const Work& w, const __nv_bfloat16* 
     a.msh = p.shared && j == 0 && !p.split ? p.s.m : 0;
     a.k = p.s.k;
     a.nblk = ((a.msh + 3) / 4 * 4 + a.k + KB - 1) / KB;
-    a.mask = j > 0 ? w.mask + static_cast<size_t>(j - 1) * p.s.BH * p.s.N * ((p.s.k + 63) / 64) : nullptr;
-    a.state = w.state;
     a.s = p.s.s_route;
     a.j = j;
     a.nbw = (p.s.k + 63) / 64;
-    a.lse = w.lse;
-    a.osh = w.osh;
+    if (multi) {  // (the union holds one mode's pointers)
+        a.mask = j > 0 ? w.mask + static_cast<size_t>(j - 1) * p.s.BH * p.s.N * ((p.s.k + 63) / 64) : nullptr;
+        a.state = w.state;
+    } else if (p.split) {
+        a.lse = w.lse;
+        a.osh = w.osh;
+    }
     CUtensorMap tq, tk, tv, tlq, tlv;
     const uint64_t rows = static_cast<uint64_t>(p.s.BH) * p.s.N, lrows = static_cast<uint64_t>(p.s.BH) * p.s.m;
     if (!make_row_tmap(&tq, Q, rows, 1) || !make_row_tmap(&tk, K, rows, 1) || !make_row_tmap(&tv, V, rows, 1) ||
@@ -689,6 +742,38 @@ cudaError_t launch_expert_tc(const Plan& p, const Work& w, const __nv_bfloat16* 
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(sm));
     if (e != cudaSuccess) return e;
     kern<<<device_sms(), NT, sm, st>>>(tq, tk, tv, tlq, tlv, a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_expert_stats(const Plan& p, const Work& w, const __nv_bfloat16* Q, const __nv_bfloat16* K,
+                                const __nv_bfloat16* V, const int32_t* expert_idx, const __nv_bfloat16* dO,
+                                float* st_lse, float* st_delta, cudaStream_t st) {
+    Args a{};
+    a.items = w.items;
+    a.nitems = w.nitems;
+    a.perm = w.perm;
+    a.expert_idx = expert_idx;
+    a.out = nullptr;
+    a.status = w.status;
+    a.N = p.s.N;
+    a.m = p.s.m;
+    a.msh = p.s.m;
+    a.k = p.s.k;
+    a.nblk = ((a.msh + 3) / 4 * 4 + a.k + KB - 1) / KB;
+    a.s = 1;
+    a.dO = dO;
+    a.st_lse = st_lse;
+    a.st_delta = st_delta;
+    CUtensorMap tq, tk, tv, tlq, tlv;
+    const uint64_t rows = static_cast<uint64_t>(p.s.BH) * p.s.N, lrows = static_cast<uint64_t>(p.s.BH) * p.s.m;
+    if (!make_row_tmap(&tq, Q, rows, 1) || !make_row_tmap(&tk, K, rows, 1) || !make_row_tmap(&tv, V, rows, 1) ||
+        !make_row_tmap(&tlq, w.lqhi, lrows, 1) || !make_row_tmap(&tlv, w.lvbf, lrows, 1))
+        return cudaErrorInvalidValue;
+    const size_t sm = smem_bytes(a.nblk, false);
+    cudaError_t e = cudaFuncSetAttribute(expert_tc_kernel<kStats>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(sm));
+    if (e != cudaSuccess) return e;
+    expert_tc_kernel<kStats><<<device_sms(), NT, sm, st>>>(tq, tk, tv, tlq, tlv, a);
     return cudaGetLastError();
 }
 

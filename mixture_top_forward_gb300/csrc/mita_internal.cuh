@@ -165,7 +165,9 @@ cudaError_t launch_scan(const Plan& p, const Work& w, const __nv_bfloat16* K, co
                         cudaStream_t st);
 cudaError_t launch_scan_tc(const Plan& p, const Work& w, const __nv_bfloat16* K, const __nv_bfloat16* V, int level,
                            cudaStream_t st);
-cudaError_t launch_select(const Plan& p, const Work& w, int32_t* expert_idx, cudaStream_t st);
+// lse_out (optional): each landmark's log-sum-exp over all keys of tau <Lq_i, K_j>
+cudaError_t launch_select(const Plan& p, const Work& w, int32_t* expert_idx, cudaStream_t st,
+                          float* lse_out = nullptr);
 cudaError_t launch_pilot_select(const Plan& p, const Work& w, int level, cudaStream_t st);
 cudaError_t launch_route(const Plan& p, const Work& w, const __nv_bfloat16* Q, int32_t* route, cudaStream_t st);
 cudaError_t launch_route_simt(const Plan& p, const Work& w, const __nv_bfloat16* Q, int32_t* route,
@@ -194,6 +196,13 @@ cudaError_t launch_expert_tc(const Plan& p, const Work& w, const __nv_bfloat16* 
                              const __nv_bfloat16* V, const int32_t* expert_idx, __nv_bfloat16* out, cudaStream_t st,
                              const int32_t* route = nullptr, int j = 0);
 bool expert_tc_supported(const Plan& p);
+// The backward pass's statistics of the query-expert attention (the plain
+// forward pass's sequence with the shared pairs in the key list): per query
+// the log-sum-exp of its m + k logits (log2 units of tau <q, key>) and
+// Delta = dO . out, into st_lse and st_delta ([BH][N] each).
+cudaError_t launch_expert_stats(const Plan& p, const Work& w, const __nv_bfloat16* Q, const __nv_bfloat16* K,
+                                const __nv_bfloat16* V, const int32_t* expert_idx, const __nv_bfloat16* dO,
+                                float* st_lse, float* st_delta, cudaStream_t st);
 bool expert_split_fits(const Plan& p);
 bool route_shared_supported(const Plan& p);
 cudaError_t launch_route_shared(const Plan& p, const Work& w, const __nv_bfloat16* Q, int32_t* route,
@@ -203,7 +212,10 @@ cudaError_t launch_route_shared(const Plan& p, const Work& w, const __nv_bfloat1
 struct BwdLayout {
     int ltiles, chunks;      // landmark tiles of 128; key chunks of the landmark-side kernels
     int64_t chunk_len;
-    size_t off_lv, off_lse, off_part, off_dlq, off_dlv, off_dlt, off_route, total;
+    size_t off_lv, off_lse, off_part, off_dlq, off_dlv, off_dlt, off_route;
+    // tensor-core path: per-query statistics, the recomputed expert sets, the
+    // landmarks' log-sum-exp (log2 units) and dLV in bf16
+    size_t off_qlse, off_qdelta, off_eidx, off_lse2, off_dlvb, total;
 };
 BwdLayout backward_layout(const Plan& p);
 // Gradients dQ, dK, dV (fp32, [BH][N][64], overwritten) of sum(out * dO) with
@@ -217,6 +229,21 @@ cudaError_t launch_backward(const Plan& p, const Work& w, const BwdLayout& L, vo
 // One thread waits, with the kernels' bounded wait and the given limit, on an
 // mbarrier nothing completes; records MITA_ERR_TIMEOUT in *status.
 cudaError_t launch_wait_selftest(int* status, uint64_t limit_ns, cudaStream_t st);
+
+// Backward pass on the tensor cores (backward_tc.cu). The expert part: dQ
+// (written), dK, dV of the routed keys (added atomically) and dLq, dLV of
+// the shared keys (added atomically), from the statistics of
+// launch_expert_stats. The landmark part: dK, dV (added) and dLq (added
+// atomically), from each landmark's log-sum-exp (log2 units) and
+// Delta' = dLV . LV, with dLV rounded to bf16.
+bool backward_tc_supported(const Plan& p);
+cudaError_t launch_backward_tc_expert(const Plan& p, const Work& w, const __nv_bfloat16* Q, const __nv_bfloat16* K,
+                                      const __nv_bfloat16* V, const __nv_bfloat16* dO, const int32_t* expert_idx,
+                                      const float* st_lse, const float* st_delta, float* dQ, float* dK, float* dV,
+                                      float* dlq, float* dlv, cudaStream_t st);
+cudaError_t launch_backward_tc_landmark(const Plan& p, const Work& w, const __nv_bfloat16* K, const __nv_bfloat16* V,
+                                        const __nv_bfloat16* dlv_bf16, const float* lse2, const float* delta,
+                                        float* dK, float* dV, float* dlq, cudaStream_t st);
 
 // Number of SMs of the current device (cached per device).
 int device_sms();

@@ -36,7 +36,8 @@ __global__ void __launch_bounds__(ST) select_kernel(int m, int k, int chunks, in
                                                     const float* __restrict__ dense, int64_t N, int64_t ld,
                                                     int64_t stride, const uint32_t* __restrict__ ridx,
                                                     const float* __restrict__ rval, const int* __restrict__ rcount,
-                                                    int rcap, const uint64_t* __restrict__ thr_in) {
+                                                    int rcap, const uint64_t* __restrict__ thr_in,
+                                                    float* __restrict__ lse_out) {
     __shared__ unsigned hist[256];
     __shared__ int offs[ST + 1];        // chunk offsets into staged[] (chunks <= ST)
     __shared__ float red[ST / 32 + 1];  // block reductions
@@ -87,6 +88,7 @@ __global__ void __launch_bounds__(ST) select_kernel(int m, int k, int chunks, in
             if (tid < D) {
                 const float v = (osum[0][tid] + osum[1][tid] + osum[2][tid] + osum[3][tid]) / L;
                 lv32[(bh * m + i) * D + tid] = v;
+                if (lse_out && tid == 0) lse_out[bh * m + i] = M + logf(L);
                 lvbf[(bh * m + i) * D + tid] = __float2bfloat16_rn(v);
             }
         } else if (tid < D) {
@@ -101,6 +103,7 @@ __global__ void __launch_bounds__(ST) select_kernel(int m, int k, int chunks, in
             }
             const float v = O / L;
             lv32[(bh * m + i) * D + tid] = v;
+            if (lse_out && tid == 0) lse_out[bh * m + i] = M + logf(L);
             lvbf[(bh * m + i) * D + tid] = __float2bfloat16_rn(v);
         }
     }
@@ -333,13 +336,14 @@ __global__ void __launch_bounds__(ST) select_kernel(int m, int k, int chunks, in
 
 }  // namespace
 
-cudaError_t launch_select(const Plan& p, const Work& w, int32_t* expert_idx, cudaStream_t st) {
+cudaError_t launch_select(const Plan& p, const Work& w, int32_t* expert_idx, cudaStream_t st, float* lse_out) {
     const unsigned grid = static_cast<unsigned>(p.s.BH * p.s.m);
     const ScanLevel& L = p.lev[p.nlev - 1];
     select_kernel<false><<<grid, ST, 0, st>>>(p.s.m, p.s.k, L.chunks, L.cap, p.shared ? w.part : nullptr, w.cand,
                                              w.ccount, w.lv32,
                                              w.lvbf, expert_idx, nullptr, L.dense ? w.dense : nullptr, p.s.N, L.ld,
-                                             1, w.ridx, w.rval, w.rcount, L.rcap, p.nlev > 1 ? w.theta : nullptr);
+                                             1, w.ridx, w.rval, w.rcount, L.rcap, p.nlev > 1 ? w.theta : nullptr,
+                                             lse_out);
     return cudaGetLastError();
 }
 
@@ -349,7 +353,7 @@ cudaError_t launch_pilot_select(const Plan& p, const Work& w, int level, cudaStr
     select_kernel<true><<<grid, ST, 0, st>>>(p.s.m, p.s.k, L.chunks, L.cap, nullptr, w.cand, w.ccount, nullptr,
                                             nullptr, nullptr, w.theta, L.dense ? w.dense : nullptr, L.S, L.ld,
                                             L.stride, w.ridx, w.rval, w.rcount, L.rcap,
-                                            level > 0 ? w.theta : nullptr);
+                                            level > 0 ? w.theta : nullptr, nullptr);
     return cudaGetLastError();
 }
 
