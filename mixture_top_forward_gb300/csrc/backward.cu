@@ -24,6 +24,7 @@
 #include <climits>
 
 #include "mita_internal.cuh"
+#include "pool_grad.cuh"
 
 namespace mita {
 
@@ -514,11 +515,6 @@ __global__ void __launch_bounds__(BT) lm_bwd_lq_kernel(const __nv_bfloat16* __re
 }
 
 // ---- pooling backward: dQ_n += dLq_i / |window i| for every window holding n ----
-__device__ __forceinline__ void win1d(int64_t N, int m, int i, int64_t& a, int64_t& b) {
-    a = (static_cast<int64_t>(i) * N) / m;
-    b = (static_cast<int64_t>(i + 1) * N + m - 1) / m;
-}
-
 __global__ void __launch_bounds__(256) pool_bwd_kernel(int64_t BH, int64_t N, int gh, int gw, int p, int m,
                                                        const float* __restrict__ dlq, float* __restrict__ dQ) {
     const int64_t x = static_cast<int64_t>(blockIdx.x) * 256 + threadIdx.x;
@@ -527,7 +523,7 @@ __global__ void __launch_bounds__(256) pool_bwd_kernel(int64_t BH, int64_t N, in
     float g[D];
 #pragma unroll
     for (int c = 0; c < D; ++c) g[c] = 0.f;
-    auto add = [&](int i, float w) {
+    pool_windows_of(N, gh, gw, p, m, n, [&](int i, float w) {
         const float4* s = reinterpret_cast<const float4*>(dlq + (bh * m + i) * D);
 #pragma unroll
         for (int c = 0; c < D / 4; ++c) {
@@ -537,28 +533,7 @@ __global__ void __launch_bounds__(256) pool_bwd_kernel(int64_t BH, int64_t N, in
             g[4 * c + 2] = fmaf(v.z, w, g[4 * c + 2]);
             g[4 * c + 3] = fmaf(v.w, w, g[4 * c + 3]);
         }
-    };
-    if (p == 0) {
-        const int i0 = static_cast<int>((n * m) / N);  // windows are >= 1 token and overlap by at most one
-        for (int i = max(0, i0 - 2); i <= min(m - 1, i0 + 2); ++i) {
-            int64_t a, b;
-            win1d(N, m, i, a, b);
-            if (a <= n && n < b) add(i, 1.f / static_cast<float>(b - a));
-        }
-    } else {
-        const int64_t y = n / gw, xx = n % gw;
-        const int r0 = static_cast<int>((y * p) / gh), c0 = static_cast<int>((xx * p) / gw);
-        for (int r = max(0, r0 - 2); r <= min(p - 1, r0 + 2); ++r) {
-            int64_t ya, yb;
-            win1d(gh, p, r, ya, yb);
-            if (!(ya <= y && y < yb)) continue;
-            for (int cc = max(0, c0 - 2); cc <= min(p - 1, c0 + 2); ++cc) {
-                int64_t xa, xb;
-                win1d(gw, p, cc, xa, xb);
-                if (xa <= xx && xx < xb) add(r * p + cc, 1.f / static_cast<float>((yb - ya) * (xb - xa)));
-            }
-        }
-    }
+    });
     float4* dst = reinterpret_cast<float4*>(dQ + x * D);
 #pragma unroll
     for (int c = 0; c < D / 4; ++c) {
@@ -654,18 +629,17 @@ cudaError_t launch_backward(const Plan& p, const Work& w, const BwdLayout& L, vo
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         if ((e = launch_group(p, w, route_ok, 0, st)) != cudaSuccess) return e;
         if ((e = launch_expert_stats(p, w, Q, K, V, expert_idx, dO, qlse, qdelta, st)) != cudaSuccess) return e;
-        // expert attention: dQ, dK, dV of the routed keys, dLq, dLV of the shared ones
-        if ((e = launch_backward_tc_expert(p, w, Q, K, V, dO, expert_idx, qlse, qdelta, dQ, dK, dV, dlq, dlv, st)) !=
-            cudaSuccess)
+        // expert attention, key side: dK, dV of the routed keys, dLq, dLV of the shared ones
+        if ((e = launch_backward_tc_expert_keys(p, w, Q, K, V, dO, expert_idx, qlse, qdelta, dK, dV, dlq, dlv,
+                                                st)) != cudaSuccess)
             return e;
         // landmark attention: dK, dV, dLq
         lm_prep_kernel<<<static_cast<unsigned>(cdiv64(BH * m, BT)), BT, 0, st>>>(BH * m, dlv, w.lv32, lse, dlt, lse2,
                                                                                  dlvb);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         if ((e = launch_backward_tc_landmark(p, w, K, V, dlvb, lse2, dlt, dK, dV, dlq, st)) != cudaSuccess) return e;
-        pool_bwd_kernel<<<static_cast<unsigned>(cdiv64(BH * N, 256)), 256, 0, st>>>(BH, N, p.s.gh, p.s.gw, p.s.p, m,
-                                                                                     dlq, dQ);
-        return cudaGetLastError();
+        // expert attention, row side, and the pooling: dQ
+        return launch_backward_tc_expert_rows(p, w, Q, K, V, dO, expert_idx, qlse, qdelta, dlq, dQ, st);
     }
     const unsigned g1 = static_cast<unsigned>(BH * L.ltiles * L.chunks);
     lm_stats_kernel<<<g1, BT, 0, st>>>(K, V, N, m, L.ltiles, L.chunks, L.chunk_len, w.lq32, part);

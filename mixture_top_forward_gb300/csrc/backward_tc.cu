@@ -35,6 +35,7 @@
 // issuer. Every wait is bounded (umma.cuh).
 #include <algorithm>
 
+#include "pool_grad.cuh"
 #include "tensormap.cuh"
 #include "umma.cuh"
 
@@ -62,7 +63,7 @@ struct BArgs {
     const int* expoff;          // EXP keys kernel: [BH][m+1] each expert's first grouped query
     const int* perm;            // [BH][N] queries grouped by expert
     const int32_t* expert_idx;  // [BH][m][k]
-    const float* lse;           // EXP: [BH][N] per query; LMK: [BH][m] per landmark (log2 units)
+    const float* lse;           // EXP: [BH][N] per query in grouped order; LMK: [BH][m] per landmark (log2 units)
     const float* delta;         // same layout: Delta of each row
     float* gk;                  // keys kernel: dK target ([BH][N][64], += ), rows kernel: G target (EXP: dQ, =)
     float* gv;                  // keys kernel: dV target ([BH][N][64], +=); LMK rows kernel: dLq (atomic)
@@ -71,6 +72,7 @@ struct BArgs {
     int* status;
     int64_t N, units, chunk_len;
     int m, k, m4, nblk, chunks;
+    int gh, gw, p;              // EXP rows kernel: the landmark windows (dQ gets the pooling's share of dLq)
 };
 
 
@@ -90,9 +92,9 @@ __device__ __forceinline__ void list_rows4(const BArgs& a, int64_t bh, const int
 // ============================================================================
 // Keys kernel
 // ============================================================================
-// shared memory: KB, VB at 0 and 16 KB; row tile buffers b = 0, 1 at
-// 32 KB + b * 49 KB: R, R_lo (LMK), dR, then L[128] and Delta[128]
-constexpr size_t KOFF_BUF = 32768, KBUF = 3 * TILE + 1024;
+// shared memory: key blocks c = 0, 1 (KB, VB) at 32 KB c; row tile buffers
+// b = 0, 1 at 64 KB + b * 49 KB: R, R_lo (LMK), dR, then L[128], Delta[128]
+constexpr size_t KOFF_BUF = 65536, KBUF = 3 * TILE + 1024;
 constexpr size_t KSMEM = KOFF_BUF + 2 * KBUF + 1024;
 // TMEM columns
 constexpr uint32_t cS = 0, cDP = 128, cP = 256, cDS = 320, cV = 384, cK = 448;
@@ -129,15 +131,15 @@ __global__ void __launch_bounds__(NTB, 1)
     // LMK: tk, tv: K, V, 128 rows high; tr, tsk: Lq hi, lo; tdr: dLV (bf16),
     //      128 rows high.
     extern __shared__ uint8_t smem_raw[];
-    __shared__ uint64_t kvfull, kvfree, rfull[2], rfree[2], sfull, sfree, pfull, pvdone, afree, drain;
+    __shared__ uint64_t kvfull[2], kvfree[2], rfull[2], rfree[2], sfull, sfree, pfull, pvdone, afree, drain;
     __shared__ uint32_t tmem_base;
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int64_t u0 = a.units * blockIdx.x / gridDim.x, u1 = a.units * (blockIdx.x + 1) / gridDim.x;
     if (tid == 0) {
-        mbar_init(&kvfull, 1);
-        mbar_init(&kvfree, 1);
         for (int b = 0; b < 2; ++b) {
+            mbar_init(&kvfull[b], 1);
+            mbar_init(&kvfree[b], 1);
             mbar_init(&rfull[b], 2);  // the loads' transaction count, and the statistics
             mbar_init(&rfree[b], 1);
         }
@@ -154,8 +156,7 @@ __global__ void __launch_bounds__(NTB, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tb = tmem_base;
-    uint8_t* KBs = base;
-    uint8_t* VBs = base + TILE;
+    auto kbuf = [&](int c) { return base + c * 2 * TILE; };  // keys, then values at + TILE
     auto rbuf = [&](int b) { return base + KOFF_BUF + b * KBUF; };
 
     if (warp == 4) {
@@ -167,20 +168,23 @@ __global__ void __launch_bounds__(NTB, 1)
             int e, b, ntiles, qoff, qcnt;
             keys_unit<MODE>(a, u, bh, e, b, ntiles, qoff, qcnt);
             if (ntiles == 0) continue;
-            if (ucount >= 1) ok = __all_sync(0xffffffffu, mbar_wait(&kvfree, (ucount - 1) & 1, a.status));
+            const int kb = ucount & 1;  // this unit's key block buffer, last used two units back
+            if (ucount >= 2) ok = __all_sync(0xffffffffu, mbar_wait(&kvfree[kb], ((ucount >> 1) - 1) & 1, a.status));
             if (!ok) break;
-            if (lane == 0) mbar_arrive_expect_tx(&kvfull, 2 * TILE);
+            uint8_t* KBs = kbuf(kb);
+            uint8_t* VBs = KBs + TILE;
+            if (lane == 0) mbar_arrive_expect_tx(&kvfull[kb], 2 * TILE);
             __syncwarp();
             if (MODE == kExp) {  // list positions 128 b + 4 lane .. + 3
                 const int32_t* sel = a.expert_idx + (bh * a.m + e) * static_cast<int64_t>(a.k);
                 int y[4];
                 bool sh;
                 list_rows4(a, bh, sel, 128 * b + 4 * lane, y, &sh);
-                tma_gather4(KBs + 4 * lane * 128, sh ? &tsk : &tk, 0, y[0], y[1], y[2], y[3], &kvfull);
-                tma_gather4(VBs + 4 * lane * 128, sh ? &tsv : &tv, 0, y[0], y[1], y[2], y[3], &kvfull);
+                tma_gather4(KBs + 4 * lane * 128, sh ? &tsk : &tk, 0, y[0], y[1], y[2], y[3], &kvfull[kb]);
+                tma_gather4(VBs + 4 * lane * 128, sh ? &tsv : &tv, 0, y[0], y[1], y[2], y[3], &kvfull[kb]);
             } else if (lane == 0) {
-                tma_load_2d(KBs, &tk, 0, static_cast<int>(bh * a.N + 128 * b), &kvfull);
-                tma_load_2d(VBs, &tv, 0, static_cast<int>(bh * a.N + 128 * b), &kvfull);
+                tma_load_2d(KBs, &tk, 0, static_cast<int>(bh * a.N + 128 * b), &kvfull[kb]);
+                tma_load_2d(VBs, &tv, 0, static_cast<int>(bh * a.N + 128 * b), &kvfull[kb]);
             }
             for (int t = 0; t < ntiles && ok; ++t) {
                 const int buf = tseq & 1;
@@ -200,11 +204,12 @@ __global__ void __launch_bounds__(NTB, 1)
                     const int y = static_cast<int>(bh * a.N);
                     tma_gather4(rb + r0 * 128, &tr, 0, y + q[0], y + q[1], y + q[2], y + q[3], &rfull[buf]);
                     tma_gather4(rb + 2 * TILE + r0 * 128, &tdr, 0, y + q[0], y + q[1], y + q[2], y + q[3], &rfull[buf]);
+                    const int64_t gp = bh * a.N + qoff + 128 * t + r0;  // statistics in grouped order
 #pragma unroll
                     for (int x = 0; x < 4; ++x) {
                         const bool v = r0 + x < cnt;
-                        sl[r0 + x] = v ? a.lse[bh * a.N + q[x]] : INFINITY;
-                        sl[128 + r0 + x] = v ? a.delta[bh * a.N + q[x]] : 0.f;
+                        sl[r0 + x] = v ? a.lse[gp + x] : INFINITY;
+                        sl[128 + r0 + x] = v ? a.delta[gp + x] : 0.f;
                     }
                 } else {
                     if (lane == 0) {
@@ -228,8 +233,9 @@ __global__ void __launch_bounds__(NTB, 1)
             ++ucount;
         }
         if (lane == 0) {  // exit: the last phase of every barrier armed here has landed
-            if (ucount > 0) mbar_drain(&kvfull, (ucount - 1) & 1);
             for (int b = 0; b < 2; ++b) {
+                const int karms = ucount > b ? (ucount - b + 1) / 2 : 0;
+                if (karms > 0) mbar_drain(&kvfull[b], (karms - 1) & 1);
                 const int arms = tseq > b ? (tseq - b + 1) / 2 : 0;
                 if (arms > 0) mbar_drain(&rfull[b], (arms - 1) & 1);
             }
@@ -238,7 +244,6 @@ __global__ void __launch_bounds__(NTB, 1)
         // ---------------------------------- MMA issuer ----------------------------------
         if (lane == 0) {
             const uint32_t idS = idesc_bf16(128, 128, false), idG = idesc_bf16(128, 64, true);
-            const uint64_t kd = sdesc_sw128(smem_u32(KBs)), vd = sdesc_sw128(smem_u32(VBs));
             int ucount = 0, tseq = 0;
             bool ok = true;
             for (int64_t u = u0; u < u1 && ok; ++u) {
@@ -246,7 +251,9 @@ __global__ void __launch_bounds__(NTB, 1)
                 int e, b, ntiles, qoff, qcnt;
                 keys_unit<MODE>(a, u, bh, e, b, ntiles, qoff, qcnt);
                 if (ntiles == 0) continue;
-                if (!(ok = mbar_wait(&kvfull, ucount & 1, a.status))) break;
+                const int kb = ucount & 1;
+                if (!(ok = mbar_wait(&kvfull[kb], (ucount >> 1) & 1, a.status))) break;
+                const uint64_t kd = sdesc_sw128(smem_u32(kbuf(kb))), vd = sdesc_sw128(smem_u32(kbuf(kb) + TILE));
                 for (int t = 0; t < ntiles; ++t) {
                     const int buf = tseq & 1;
                     if (!(ok = mbar_wait(&rfull[buf], (tseq >> 1) & 1, a.status))) break;
@@ -274,7 +281,7 @@ __global__ void __launch_bounds__(NTB, 1)
                     ++tseq;
                 }
                 if (!ok) break;
-                mma_commit(&kvfree);
+                mma_commit(&kvfree[kb]);
                 ++ucount;
             }
             mma_drain(&drain);
@@ -394,11 +401,16 @@ __global__ void __launch_bounds__(NTB, 1)
 // ============================================================================
 // Rows kernel
 // ============================================================================
-// shared memory: row buffers b = 0, 1 at 49 KB b: R, R_lo (LMK), dR; then a
-// ring of RST key stages of K (8 KB) and V (8 KB) rows, 64 keys each
+// shared memory: row buffers b = 0, 1 at 49 KB b: R, R_lo (LMK), dR; then
+// LMK: a ring of RST key stages of K (8 KB) and V (8 KB) rows, 64 keys each;
+// EXP: the expert's whole key list (nblk blocks of 64 rows) and then its
+// value list, kept while consecutive items share the expert
 constexpr int RST = 4;
 constexpr size_t RBUF = 3 * TILE + 1024, ROFF_K = 2 * RBUF;
 constexpr size_t RSMEM = ROFF_K + RST * 16384 + 1024;
+constexpr int RMAXBLK = 8;  // EXP: list blocks of 64 (m4 + k <= 512)
+// EXP row buffers hold R and dR only (2 x 32 KB)
+constexpr size_t RSMEM_EXP = 2 * 2 * TILE + RMAXBLK * 16384 + 1024;
 // TMEM: S buffers at 0, 64; dP at 128, 192; ds (bf16 pairs) at 256, 288; G at 384
 constexpr uint32_t rS = 0, rDP = 128, rDS = 256, rG = 384;
 
@@ -434,7 +446,7 @@ __global__ void __launch_bounds__(NTB, 1)
     //      128 rows high.
     extern __shared__ uint8_t smem_raw[];
     __shared__ uint64_t rfull[2], rfree[2], kfull[RST], kempty[RST], sfull[2], sfree[2], pfull[2], dsfree[2];
-    __shared__ uint64_t gdone, gfree, drain;
+    __shared__ uint64_t gdone, gfree, drain, kvfull, kvfree;
     __shared__ uint32_t tmem_base;
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -456,6 +468,8 @@ __global__ void __launch_bounds__(NTB, 1)
         mbar_init(&gdone, 1);
         mbar_init(&gfree, 4);
         mbar_init(&drain, 1);
+        mbar_init(&kvfull, 1);
+        mbar_init(&kvfree, 1);
         fence_barrier_init();
     }
     if (warp == 0) tmem_alloc(&tmem_base, 512);
@@ -463,18 +477,41 @@ __global__ void __launch_bounds__(NTB, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tb = tmem_base;
-    auto rbuf = [&](int b) { return base + b * RBUF; };
+    constexpr size_t RB = MODE == kExp ? 2 * TILE : RBUF;    // row buffer stride
+    constexpr size_t DROFF = MODE == kExp ? TILE : 2 * TILE;  // dR within a row buffer
+    auto rbuf = [&](int b) { return base + b * RB; };
     auto kst = [&](int s) { return base + ROFF_K + s * 16384; };  // K rows, then V rows at +8 KB
+    uint8_t* listk = base + 2 * RB;                                  // EXP: list block j at + 8 KB j
+    uint8_t* listv = listk + a.nblk * 8192;
 
     if (warp == 4) {
         // ---------------------------------- producer ----------------------------------
-        int useq = 0, g = 0;
+        int useq = 0, g = 0, changes = 0, cur_e = -1;
+        int64_t cur_bh = -1;
         bool ok = true;
         for (int64_t u = u0; u < u1 && ok; ++u) {
             int64_t bh, c0, c1;
             int4 item;
             int lt, nb;
             rows_unit<MODE>(a, u, bh, item, lt, nb, c0, c1);
+            if (MODE == kExp && (bh != cur_bh || item.x != cur_e)) {
+                // the expert's list, once the MMAs reading the previous one are done
+                if (changes > 0) ok = __all_sync(0xffffffffu, mbar_wait(&kvfree, (changes - 1) & 1, a.status));
+                if (!ok) break;
+                if (lane == 0) mbar_arrive_expect_tx(&kvfull, static_cast<uint32_t>(a.nblk) * 16384u);
+                __syncwarp();
+                const int32_t* sel = a.expert_idx + (bh * a.m + item.x) * static_cast<int64_t>(a.k);
+                for (int gi = lane; gi < a.nblk * 16; gi += 32) {  // list positions 4 gi .. + 3
+                    int y[4];
+                    bool sh;
+                    list_rows4(a, bh, sel, 4 * gi, y, &sh);
+                    tma_gather4(listk + 4 * gi * 128, sh ? &tsk : &tk, 0, y[0], y[1], y[2], y[3], &kvfull);
+                    tma_gather4(listv + 4 * gi * 128, sh ? &tsv : &tv, 0, y[0], y[1], y[2], y[3], &kvfull);
+                }
+                cur_bh = bh;
+                cur_e = item.x;
+                ++changes;
+            }
             const int buf = useq & 1;
             if (useq >= 2) ok = __all_sync(0xffffffffu, mbar_wait(&rfree[buf], ((useq >> 1) - 1) & 1, a.status));
             if (!ok) break;
@@ -488,31 +525,21 @@ __global__ void __launch_bounds__(NTB, 1)
                 const int q0 = y + pp[min(r0, last)], q1 = y + pp[min(r0 + 1, last)];
                 const int q2 = y + pp[min(r0 + 2, last)], q3 = y + pp[min(r0 + 3, last)];
                 tma_gather4(rb + r0 * 128, &tr, 0, q0, q1, q2, q3, &rfull[buf]);
-                tma_gather4(rb + 2 * TILE + r0 * 128, &tdr, 0, q0, q1, q2, q3, &rfull[buf]);
+                tma_gather4(rb + DROFF + r0 * 128, &tdr, 0, q0, q1, q2, q3, &rfull[buf]);
             } else if (lane == 0) {
                 const int y = static_cast<int>(bh * a.m + 128 * lt);
                 tma_load_2d(rb, &tr, 0, y, &rfull[buf]);
                 tma_load_2d(rb + TILE, &tsk, 0, y, &rfull[buf]);
                 tma_load_2d(rb + 2 * TILE, &tdr, 0, y, &rfull[buf]);
             }
-            const int32_t* sel = MODE == kExp ? a.expert_idx + (bh * a.m + item.x) * static_cast<int64_t>(a.k) : nullptr;
-            for (int j = 0; j < nb && ok; ++j, ++g) {
+            for (int j = 0; j < nb && ok && MODE == kLmk; ++j, ++g) {
                 const int s = g % RST;
                 if (g >= RST) ok = __all_sync(0xffffffffu, mbar_wait(&kempty[s], ((g / RST) - 1) & 1, a.status));
                 if (!ok) break;
                 if (lane == 0) mbar_arrive_expect_tx(&kfull[s], 16384);
                 __syncwarp();
                 uint8_t* ks = kst(s);
-                if (MODE == kExp) {  // list positions 64 j + 4 (lane % 16) .. + 3; lanes 16-31 the values
-                    const int gidx = lane & 15;
-                    int y[4];
-                    bool sh;
-                    list_rows4(a, bh, sel, 64 * j + 4 * gidx, y, &sh);
-                    if (lane < 16)
-                        tma_gather4(ks + 4 * gidx * 128, sh ? &tsk : &tk, 0, y[0], y[1], y[2], y[3], &kfull[s]);
-                    else
-                        tma_gather4(ks + 8192 + 4 * gidx * 128, sh ? &tsv : &tv, 0, y[0], y[1], y[2], y[3], &kfull[s]);
-                } else if (lane == 0) {
+                if (lane == 0) {
                     const int y = static_cast<int>(bh * a.N + c0 + 64 * j);
                     tma_load_2d(ks, &tk, 0, y, &kfull[s]);
                     tma_load_2d(ks + 8192, &tv, 0, y, &kfull[s]);
@@ -521,6 +548,7 @@ __global__ void __launch_bounds__(NTB, 1)
             ++useq;
         }
         if (lane == 0) {
+            if (changes > 0) mbar_drain(&kvfull, (changes - 1) & 1);
             for (int b = 0; b < 2; ++b) {
                 const int arms = useq > b ? (useq - b + 1) / 2 : 0;
                 if (arms > 0) mbar_drain(&rfull[b], (arms - 1) & 1);
@@ -534,18 +562,19 @@ __global__ void __launch_bounds__(NTB, 1)
         // ---------------------------------- MMA issuer ----------------------------------
         if (lane == 0) {
             const uint32_t idS = idesc_bf16(128, 64, false), idG = idesc_bf16(128, 64, true);
-            int useq = 0, g = 0;
+            int useq = 0, g = 0, changes = 0, cur_e = -1;
+            int64_t cur_bh = -1;
             bool ok = true;
-            // G += ds(h) K(h), the unit's block h (first: overwrite G)
-            auto gstep = [&](int h, bool first) -> bool {
+            // G += ds(h) K(h), the unit's block h (list block jb of EXP; first: overwrite G)
+            auto gstep = [&](int h, int jb, bool first) -> bool {
                 const int sb = h & 1;
                 if (!mbar_wait(&pfull[sb], (h >> 1) & 1, a.status)) return false;
                 if (first && useq >= 1 && !mbar_wait(&gfree, (useq - 1) & 1, a.status)) return false;
                 tc_fence_after();
-                const uint64_t kmn = sdesc_sw128(smem_u32(kst(h % RST)));
+                const uint64_t kmn = sdesc_sw128(smem_u32(MODE == kExp ? listk + jb * 8192 : kst(h % RST)));
                 mma_ts_k64(tb + rG, tb + rDS + 32 * sb, kmn, idG, first ? 0u : 1u);
                 mma_commit(&dsfree[sb]);
-                mma_commit(&kempty[h % RST]);
+                if (MODE == kLmk) mma_commit(&kempty[h % RST]);
                 return true;
             };
             for (int64_t u = u0; u < u1 && ok; ++u) {
@@ -554,24 +583,33 @@ __global__ void __launch_bounds__(NTB, 1)
                 int lt, nb;
                 rows_unit<MODE>(a, u, bh, item, lt, nb, c0, c1);
                 const int buf = useq & 1;
+                if (MODE == kExp && (bh != cur_bh || item.x != cur_e)) {
+                    // release the previous list (once this thread's MMAs on it are
+                    // done), then wait for this expert's; before the unit's rows,
+                    // which the producer loads only after the list
+                    if (changes > 0) mma_commit(&kvfree);
+                    if (!(ok = mbar_wait(&kvfull, changes & 1, a.status))) break;
+                    cur_bh = bh;
+                    cur_e = item.x;
+                    ++changes;
+                }
                 if (!(ok = mbar_wait(&rfull[buf], (useq >> 1) & 1, a.status))) break;
                 const uint32_t rs = smem_u32(rbuf(buf));
-                const int gfirst = g;
                 for (int j = 0; j < nb && ok; ++j, ++g) {
                     const int s = g % RST, sb = g & 1;
-                    if (!(ok = mbar_wait(&kfull[s], (g / RST) & 1, a.status))) break;
+                    if (MODE == kLmk && !(ok = mbar_wait(&kfull[s], (g / RST) & 1, a.status))) break;
                     if (g >= 2 && !(ok = mbar_wait(&sfree[sb], ((g >> 1) - 1) & 1, a.status))) break;
                     tc_fence_after();
-                    const uint32_t ks = smem_u32(kst(s));
+                    const uint32_t ks = MODE == kExp ? smem_u32(listk + j * 8192) : smem_u32(kst(s));
+                    const uint32_t vs = MODE == kExp ? smem_u32(listv + j * 8192) : ks + 8192;
                     mma_ss_k64(tb + rS + 64 * sb, sdesc_sw128(rs), sdesc_sw128(ks), idS, 0u);
                     if (MODE == kLmk) mma_ss_k64(tb + rS + 64 * sb, sdesc_sw128(rs + TILE), sdesc_sw128(ks), idS, 1u);
-                    mma_ss_k64(tb + rDP + 64 * sb, sdesc_sw128(rs + 2 * TILE), sdesc_sw128(ks + 8192), idS, 0u);
+                    mma_ss_k64(tb + rDP + 64 * sb, sdesc_sw128(rs + DROFF), sdesc_sw128(vs), idS, 0u);
                     mma_commit(&sfull[sb]);
-                    if (j >= 1) ok = gstep(g - 1, j == 1);
+                    if (j >= 1) ok = gstep(g - 1, j - 1, j == 1);
                 }
                 if (!ok) break;
-                if (!(ok = gstep(g - 1, nb == 1))) break;
-                (void)gfirst;
+                if (!(ok = gstep(g - 1, nb - 1, nb == 1))) break;
                 mma_commit(&gdone);
                 mma_commit(&rfree[buf]);
                 ++useq;
@@ -592,17 +630,20 @@ __global__ void __launch_bounds__(NTB, 1)
             // this row's statistics and where its gradient goes
             bool row_ok;
             int64_t orow;
+            int64_t srow;  // where its statistics are (EXP: grouped order)
             if (MODE == kExp) {
                 row_ok = t < item.z;
                 const int n = row_ok ? a.perm[bh * a.N + item.y + t] : 0;
                 orow = bh * a.N + n;
+                srow = bh * a.N + item.y + (row_ok ? t : 0);
             } else {
                 const int li = 128 * lt + t;
                 row_ok = li < a.m;
                 orow = bh * a.m + (row_ok ? li : 0);
+                srow = orow;
             }
-            const float L = row_ok ? a.lse[orow] : INFINITY;
-            const float Dl = row_ok ? a.delta[orow] : 0.f;
+            const float L = row_ok ? a.lse[srow] : INFINITY;
+            const float Dl = row_ok ? a.delta[srow] : 0.f;
             const int nkeys = MODE == kExp ? a.m4 + a.k : static_cast<int>(c1 - c0);  // valid list positions / keys
             for (int j = 0; j < nb && ok; ++j, ++g) {
                 const int sb = g & 1;
@@ -651,11 +692,25 @@ __global__ void __launch_bounds__(NTB, 1)
             tc_fence_before();
             warp_arrive(&gfree);
             if (row_ok) {
-                if (MODE == kExp) {  // dQ of the query (its first contribution: written)
+                if (MODE == kExp) {
+                    // dQ of the query: its expert attention's share and the
+                    // pooling's share of the (complete) dLq of its windows
+#pragma unroll
+                    for (int c = 0; c < 64; ++c) gg[c] *= kTau;
+                    pool_windows_of(a.N, a.gh, a.gw, a.p, a.m, orow - bh * a.N, [&](int i, float wgt) {
+                        const float4* s4 = reinterpret_cast<const float4*>(a.slq + (bh * a.m + i) * D);
+#pragma unroll
+                        for (int c = 0; c < 16; ++c) {
+                            const float4 v = s4[c];
+                            gg[4 * c] = fmaf(v.x, wgt, gg[4 * c]);
+                            gg[4 * c + 1] = fmaf(v.y, wgt, gg[4 * c + 1]);
+                            gg[4 * c + 2] = fmaf(v.z, wgt, gg[4 * c + 2]);
+                            gg[4 * c + 3] = fmaf(v.w, wgt, gg[4 * c + 3]);
+                        }
+                    });
                     float4* dst = reinterpret_cast<float4*>(a.gk + orow * D);
 #pragma unroll
-                    for (int c = 0; c < 64; c += 4)
-                        dst[c / 4] = make_float4(gg[c] * kTau, gg[c + 1] * kTau, gg[c + 2] * kTau, gg[c + 3] * kTau);
+                    for (int c = 0; c < 64; c += 4) dst[c / 4] = make_float4(gg[c], gg[c + 1], gg[c + 2], gg[c + 3]);
                 } else {  // dLq of the landmark, summed over the key chunks
                     float4* dst = reinterpret_cast<float4*>(a.gv + orow * D);
 #pragma unroll
@@ -690,11 +745,11 @@ bool backward_tc_supported(const Plan& p) {
            p.s.BH * (p.s.m + 1) < (int64_t(1) << 31);
 }
 
-cudaError_t launch_backward_tc_expert(const Plan& p, const Work& w, const __nv_bfloat16* Q, const __nv_bfloat16* K,
-                                      const __nv_bfloat16* V, const __nv_bfloat16* dO, const int32_t* expert_idx,
-                                      const float* st_lse, const float* st_delta, float* dQ, float* dK, float* dV,
-                                      float* dlq, float* dlv, cudaStream_t st) {
-    BArgs a{};
+// EXP maps and arguments shared by the two expert-side launches
+static int exp_setup(const Plan& p, const Work& w, const __nv_bfloat16* Q, const __nv_bfloat16* K,
+                     const __nv_bfloat16* V, const __nv_bfloat16* dO, const int32_t* expert_idx, const float* st_lse,
+                     const float* st_delta, CUtensorMap* maps, BArgs& a) {
+    a = BArgs{};
     a.items = w.items;
     a.nitems = w.nitems;
     a.expoff = w.expoff;
@@ -707,27 +762,44 @@ cudaError_t launch_backward_tc_expert(const Plan& p, const Work& w, const __nv_b
     a.m = p.s.m;
     a.k = p.s.k;
     a.m4 = (p.s.m + 3) & ~3;
-    CUtensorMap mk, mv, msk, msv, mq, mdo;
+    a.gh = p.s.gh;
+    a.gw = p.s.gw;
+    a.p = p.s.p;
     const uint64_t rows = static_cast<uint64_t>(p.s.BH) * p.s.N, lrows = static_cast<uint64_t>(p.s.BH) * p.s.m;
-    if (!make_row_tmap(&mk, K, rows, 1) || !make_row_tmap(&mv, V, rows, 1) || !make_row_tmap(&msk, w.lqhi, lrows, 1) ||
-        !make_row_tmap(&msv, w.lvbf, lrows, 1) || !make_row_tmap(&mq, Q, rows, 1) || !make_row_tmap(&mdo, dO, rows, 1))
-        return cudaErrorInvalidValue;
-    const CUtensorMap maps[6] = {mk, mv, msk, msv, mq, mdo};
-    const int sms = device_sms();
-    // dQ: one unit per item (rows kernel), over the expert's list in 64-key blocks
-    a.nblk = (a.m4 + a.k + 63) / 64;
-    a.gk = dQ;
-    cudaError_t e = launch6(bwd_rows_kernel<kExp>, RSMEM, sms, maps, a, st);
-    if (e != cudaSuccess) return e;
-    // dK, dV of the routed keys and dLq, dLV of the shared ones: one unit per
-    // (head, expert, 128-key block of its list)
+    return make_row_tmap(&maps[0], K, rows, 1) && make_row_tmap(&maps[1], V, rows, 1) &&
+           make_row_tmap(&maps[2], w.lqhi, lrows, 1) && make_row_tmap(&maps[3], w.lvbf, lrows, 1) &&
+           make_row_tmap(&maps[4], Q, rows, 1) && make_row_tmap(&maps[5], dO, rows, 1);
+}
+
+cudaError_t launch_backward_tc_expert_keys(const Plan& p, const Work& w, const __nv_bfloat16* Q,
+                                           const __nv_bfloat16* K, const __nv_bfloat16* V, const __nv_bfloat16* dO,
+                                           const int32_t* expert_idx, const float* st_lse, const float* st_delta,
+                                           float* dK, float* dV, float* dlq, float* dlv, cudaStream_t st) {
+    BArgs a;
+    CUtensorMap maps[6];
+    if (!exp_setup(p, w, Q, K, V, dO, expert_idx, st_lse, st_delta, maps, a)) return cudaErrorInvalidValue;
+    // one unit per (head, expert, 128-key block of its list)
     a.nblk = (a.m4 + a.k + 127) / 128;
     a.units = p.s.BH * static_cast<int64_t>(p.s.m) * a.nblk;
     a.gk = dK;
     a.gv = dV;
     a.slq = dlq;
     a.slv = dlv;
-    return launch6(bwd_keys_kernel<kExp>, KSMEM, std::min<int64_t>(sms, a.units), maps, a, st);
+    return launch6(bwd_keys_kernel<kExp>, KSMEM, std::min<int64_t>(device_sms(), a.units), maps, a, st);
+}
+
+cudaError_t launch_backward_tc_expert_rows(const Plan& p, const Work& w, const __nv_bfloat16* Q,
+                                           const __nv_bfloat16* K, const __nv_bfloat16* V, const __nv_bfloat16* dO,
+                                           const int32_t* expert_idx, const float* st_lse, const float* st_delta,
+                                           const float* dlq, float* dQ, cudaStream_t st) {
+    BArgs a;
+    CUtensorMap maps[6];
+    if (!exp_setup(p, w, Q, K, V, dO, expert_idx, st_lse, st_delta, maps, a)) return cudaErrorInvalidValue;
+    // one unit per item, over the expert's list in 64-key blocks
+    a.nblk = (a.m4 + a.k + 63) / 64;
+    a.gk = dQ;
+    a.slq = const_cast<float*>(dlq);  // (read: the pooling's share)
+    return launch6(bwd_rows_kernel<kExp>, RSMEM_EXP, device_sms(), maps, a, st);
 }
 
 cudaError_t launch_backward_tc_landmark(const Plan& p, const Work& w, const __nv_bfloat16* K, const __nv_bfloat16* V,

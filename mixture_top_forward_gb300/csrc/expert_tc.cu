@@ -114,33 +114,38 @@ struct Args {
         struct {                        // STATS
             const __nv_bfloat16* dO;    // [BH][N][64] output gradients
             float* st_lse;              // [BH][N] log-sum-exp of the m + k logits (log2 units of tau <q, key>)
-            float* st_delta;            // [BH][N] dO . out (out unrounded)
+            float* st_delta;            // [BH][N] dO . out (out unrounded); both in grouped order
         };
     };
 };
 static_assert(sizeof(Args) <= 128, "the kernel argument block stays within 128 bytes");
 
 struct Layout {
-    uint8_t* keys;  // nblk * 8 KB
-    uint8_t* vals;  // nblk * 8 KB
-    uint8_t* q;     // [NWG][QB] * 16 KB: query rows
-    uint8_t* ps;    // SPLIT: [NWG] * 16 KB: the rows' shared-branch outputs (each thread its own row)
+    uint8_t* keys;    // nblk * 8 KB (IND: warpgroup w's at + w * kvstride)
+    uint8_t* vals;    // nblk * 8 KB (likewise)
+    uint32_t kvstride;  // bytes between the warpgroups' lists (0: one shared list)
+    uint8_t* q;       // [NWG][QB] * 16 KB: query rows
+    uint8_t* ps;      // SPLIT: [NWG] * 16 KB: the rows' shared-branch outputs (each thread its own row)
 };
 
-__device__ __forceinline__ Layout layout(uint8_t* base, int nblk) {
+__device__ __forceinline__ Layout layout(uint8_t* base, int nblk, bool ind) {
     Layout L;
     L.keys = base;
     L.vals = L.keys + nblk * 8192;
-    L.q = L.vals + nblk * 8192;
+    L.kvstride = ind ? static_cast<uint32_t>(nblk) * 16384u : 0u;
+    L.q = base + (ind ? NWG : 1) * nblk * 16384;
     L.ps = L.q + NWG * QB * 16384;
     return L;
 }
 
 // The round starting at item r of [r, i1): the item there and, if the next
-// item has the same expert (and head), that one too; one per warpgroup.
-__device__ __forceinline__ int round_items(const Args& a, int r, int i1, int4& x0, int4& x1, int4& x2) {
+// item has the same expert (and head), that one too; one per warpgroup. With
+// independent warpgroups (one = true) every round is one item of the
+// warpgroup's own range.
+__device__ __forceinline__ int round_items(const Args& a, int r, int i1, int4& x0, int4& x1, int4& x2,
+                                           bool one = false) {
     x0 = a.items[r];
-    if (r + 1 >= i1) return 1;
+    if (one || r + 1 >= i1) return 1;
     x1 = a.items[r + 1];
     if (x1.x != x0.x || x1.w != x0.w) return 1;
     if (r + 2 >= i1) return 2;
@@ -157,10 +162,10 @@ __device__ __forceinline__ int4 pick(int w, const int4& x0, const int4& x1, cons
 // every issuer sees every phase of both barriers. Returns 1 (item), 0 (none
 // left) or -1 (a wait timed out).
 __device__ __forceinline__ int next_item(const Args& a, int w, int& r, int i1, int& cur_bh, int& cur_e, int& changes,
-                                         uint64_t* kvfull, uint64_t* kvfree, int4& out) {
+                                         uint64_t* kvfull, uint64_t* kvfree, int4& out, bool one) {
     while (r < i1) {
         int4 x0, x1, x2;
-        const int cnt = round_items(a, r, i1, x0, x1, x2);
+        const int cnt = round_items(a, r, i1, x0, x1, x2, one);
         if (x0.w != cur_bh || x0.x != cur_e) {
             if (changes > 0) umma::mma_commit(kvfree);
             if (!umma::mbar_wait(kvfull, changes & 1, a.status)) return -1;
@@ -179,10 +184,10 @@ __device__ __forceinline__ int next_item(const Args& a, int w, int& r, int i1, i
 }
 
 // Whether warpgroup w has another item before the next list change.
-__device__ __forceinline__ bool next_same(const Args& a, int w, int r, int i1, int cur_bh, int cur_e) {
+__device__ __forceinline__ bool next_same(const Args& a, int w, int r, int i1, int cur_bh, int cur_e, bool one) {
     while (r < i1) {
         int4 x0, x1, x2;
-        const int cnt = round_items(a, r, i1, x0, x1, x2);
+        const int cnt = round_items(a, r, i1, x0, x1, x2, one);
         if (x0.w != cur_bh || x0.x != cur_e) return false;
         if (w < cnt) return true;
         r += cnt;
@@ -239,18 +244,22 @@ static __device__ __noinline__ float stats_delta(uint32_t tO, const __nv_bfloat1
     return dl;
 }
 
-template <int MODE>
+// IND (independent warpgroups, short lists only): each warpgroup takes a
+// contiguous third of the CTA's items with a key/value list of its own, so
+// experts of one item each (short sequences, ViT shapes) run three at a time
+// instead of one per round.
+template <int MODE, bool IND>
 __global__ void __launch_bounds__(NT, 1)
     expert_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                      const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tlq,
                      const __grid_constant__ CUtensorMap tlv, Args a) {
     constexpr bool MULTI = MODE == kMulti, SPLIT = MODE == kSplit, STATS = MODE == kStats;
     extern __shared__ uint8_t smem_raw[];
-    __shared__ uint64_t kvfull, kvfree, qfull[NWG * QB], qfree[NWG * QB], ofree[NWG];
+    __shared__ uint64_t kvfull[NWG], kvfree[NWG], qfull[NWG * QB], qfree[NWG * QB], ofree[NWG];
     __shared__ uint64_t sfull[NWG], sfree[NWG], pfull[NWG], pvdone[NWG], drain;
     __shared__ uint32_t tmem_base;
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const Layout S = layout(base, a.nblk);
+    const Layout S = layout(base, a.nblk, IND);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     // key rows: [0, msh) shared, [msh, m4) unused, [m4, m4 + k) routed (m4 =
     // msh rounded up to 4, so every 4-row gather starts 512-byte aligned);
@@ -260,8 +269,10 @@ __global__ void __launch_bounds__(NT, 1)
     const int nkeys = m4 + a.k;
 
     if (tid == 0) {
-        mbar_init(&kvfull, 1);
-        mbar_init(&kvfree, NWG);  // one commit per MMA issuer
+        for (int w = 0; w < NWG; ++w) {
+            mbar_init(&kvfull[w], 1);
+            mbar_init(&kvfree[w], IND ? 1 : NWG);  // shared lists: one commit per MMA issuer
+        }
         for (int w = 0; w < NWG; ++w) {
             mbar_init(&ofree[w], 4);  // one arrival per row warp
             mbar_init(&pfull[w], 4);
@@ -285,6 +296,8 @@ __global__ void __launch_bounds__(NT, 1)
     const int total = *a.nitems;
     const int i0 = static_cast<int>(static_cast<int64_t>(total) * blockIdx.x / gridDim.x);
     const int i1 = static_cast<int>(static_cast<int64_t>(total) * (blockIdx.x + 1) / gridDim.x);
+    // IND: warpgroup w's items [j0(w), j0(w + 1))
+    auto j0 = [&](int w) { return i0 + static_cast<int>(static_cast<int64_t>(i1 - i0) * w / NWG); };
 
     if (warp == 0) {
         // ------------------------------ producer ------------------------------
@@ -293,78 +306,118 @@ __global__ void __launch_bounds__(NT, 1)
         // last gather stay zero (their logits are masked; their values must be
         // finite).
         const int rows = a.nblk * KB;
-        for (int x = ((nkeys + 3) & ~3) * 8 + lane; x < rows * 8; x += 32) {
-            zero16(S.keys + swz128(x >> 3, x & 7));
-            zero16(S.vals + swz128(x >> 3, x & 7));
-        }
+        for (int w = 0; w < (IND ? NWG : 1); ++w)
+            for (int x = ((nkeys + 3) & ~3) * 8 + lane; x < rows * 8; x += 32) {
+                zero16(S.keys + w * S.kvstride + swz128(x >> 3, x & 7));
+                zero16(S.vals + w * S.kvstride + swz128(x >> 3, x & 7));
+            }
         fence_proxy_async();
         __syncwarp();
-        int64_t cur_bh = -1;
-        int cur_e = -1, changes = 0;
-        uint32_t nq[NWG] = {};
-        bool ok = true;
-        for (int r = i0; r < i1 && ok;) {
-            int4 it[NWG];
-            const int cnt = round_items(a, r, i1, it[0], it[1], it[2]);
-            if (it[0].w != cur_bh || it[0].x != cur_e) {
-                // wait until the MMAs reading the previous lists are done
-                if (changes > 0) ok = __all_sync(0xffffffffu, mbar_wait(&kvfree, (changes - 1) & 1, a.status));
-                if (!ok) break;
-                const int bh = it[0].w;
-                const int32_t* sel = a.expert_idx + (static_cast<int64_t>(bh) * a.m + it[0].x) * a.k;
-                const int ns = it[0].w != cur_bh ? m4 / 4 : 0;  // shared rows (if any) only on a new head
-                const int nr = (a.k + 3) / 4;
-                if (lane == 0) mbar_arrive_expect_tx(&kvfull, static_cast<uint32_t>(ns + nr) * 1024u);
-                __syncwarp();
-                for (int g = lane; g < ns; g += 32) {  // shared rows 4g..4g+3 (the last ones repeat row m-1)
-                    const int y = bh * a.m;
-                    const int r0 = 4 * g;
-                    const int y0 = y + min(r0, a.m - 1), y1 = y + min(r0 + 1, a.m - 1);
-                    const int y2 = y + min(r0 + 2, a.m - 1), y3 = y + min(r0 + 3, a.m - 1);
-                    tma_gather4(S.keys + r0 * 128, &tlq, 0, y0, y1, y2, y3, &kvfull);
-                    tma_gather4(S.vals + r0 * 128, &tlv, 0, y0, y1, y2, y3, &kvfull);
-                }
-                for (int g = lane; g < nr; g += 32) {  // routed rows m4 + 4g.. (the last ones repeat key k-1)
-                    const int r0 = 4 * g;
-                    const int y = bh * static_cast<int>(a.N);
-                    const int y0 = y + sel[min(r0, a.k - 1)], y1 = y + sel[min(r0 + 1, a.k - 1)];
-                    const int y2 = y + sel[min(r0 + 2, a.k - 1)], y3 = y + sel[min(r0 + 3, a.k - 1)];
-                    tma_gather4(S.keys + (m4 + r0) * 128, &tk, 0, y0, y1, y2, y3, &kvfull);
-                    tma_gather4(S.vals + (m4 + r0) * 128, &tv, 0, y0, y1, y2, y3, &kvfull);
-                }
-                cur_bh = it[0].w;
-                cur_e = it[0].x;
-                ++changes;
+        // the key/value list of item `it` into list copy w (the shared rows
+        // only when the copy held another head's list)
+        auto gather_list = [&](const int4& it, int w, bool new_head) {
+            uint8_t* keys = S.keys + w * S.kvstride;
+            uint8_t* vals = S.vals + w * S.kvstride;
+            uint64_t* bar = &kvfull[w];
+            const int bh = it.w;
+            const int32_t* sel = a.expert_idx + (static_cast<int64_t>(bh) * a.m + it.x) * a.k;
+            const int ns = new_head ? m4 / 4 : 0;
+            const int nr = (a.k + 3) / 4;
+            if (lane == 0) mbar_arrive_expect_tx(bar, static_cast<uint32_t>(ns + nr) * 1024u);
+            __syncwarp();
+            for (int g = lane; g < ns; g += 32) {  // shared rows 4g..4g+3 (the last ones repeat row m-1)
+                const int y = bh * a.m;
+                const int r0 = 4 * g;
+                const int y0 = y + min(r0, a.m - 1), y1 = y + min(r0 + 1, a.m - 1);
+                const int y2 = y + min(r0 + 2, a.m - 1), y3 = y + min(r0 + 3, a.m - 1);
+                tma_gather4(keys + r0 * 128, &tlq, 0, y0, y1, y2, y3, bar);
+                tma_gather4(vals + r0 * 128, &tlv, 0, y0, y1, y2, y3, bar);
             }
-#pragma unroll
-            for (int w = 0; w < NWG; ++w) {
-                if (w >= cnt || !ok) break;
-                // this Q buffer of the warpgroup was last used QB items back
-                const uint32_t qb = w * QB + (nq[w] % QB);
-                if (nq[w] >= QB)
-                    ok = __all_sync(0xffffffffu, mbar_wait(&qfree[qb], ((nq[w] / QB) - 1) & 1, a.status));
-                if (!ok) break;
-                if (lane == 0) mbar_arrive_expect_tx(&qfull[qb], 16384u);
-                __syncwarp();
-                // lane l gathers query rows 4l..4l+3; rows past the item repeat its last query
-                const int bh = it[w].w;
-                const int* pp = a.perm + static_cast<int64_t>(bh) * a.N + it[w].y;
-                const int last = it[w].z - 1, r0 = 4 * lane;
+            for (int g = lane; g < nr; g += 32) {  // routed rows m4 + 4g.. (the last ones repeat key k-1)
+                const int r0 = 4 * g;
                 const int y = bh * static_cast<int>(a.N);
-                tma_gather4(S.q + qb * 16384 + r0 * 128, &tq, 0, y + pp[min(r0, last)], y + pp[min(r0 + 1, last)],
-                            y + pp[min(r0 + 2, last)], y + pp[min(r0 + 3, last)], &qfull[qb]);
-                ++nq[w];
+                const int y0 = y + sel[min(r0, a.k - 1)], y1 = y + sel[min(r0 + 1, a.k - 1)];
+                const int y2 = y + sel[min(r0 + 2, a.k - 1)], y3 = y + sel[min(r0 + 3, a.k - 1)];
+                tma_gather4(keys + (m4 + r0) * 128, &tk, 0, y0, y1, y2, y3, bar);
+                tma_gather4(vals + (m4 + r0) * 128, &tv, 0, y0, y1, y2, y3, bar);
             }
-            r += cnt;
+        };
+        uint32_t nq[NWG] = {};
+        // the query rows of item `it` into warpgroup w's next query buffer
+        auto gather_q = [&](const int4& it, int w) -> bool {
+            // this Q buffer of the warpgroup was last used QB items back
+            const uint32_t qb = w * QB + (nq[w] % QB);
+            if (nq[w] >= QB && !__all_sync(0xffffffffu, mbar_wait(&qfree[qb], ((nq[w] / QB) - 1) & 1, a.status)))
+                return false;
+            if (lane == 0) mbar_arrive_expect_tx(&qfull[qb], 16384u);
+            __syncwarp();
+            // lane l gathers query rows 4l..4l+3; rows past the item repeat its last query
+            const int bh = it.w;
+            const int* pp = a.perm + static_cast<int64_t>(bh) * a.N + it.y;
+            const int last = it.z - 1, r0 = 4 * lane;
+            const int y = bh * static_cast<int>(a.N);
+            tma_gather4(S.q + qb * 16384 + r0 * 128, &tq, 0, y + pp[min(r0, last)], y + pp[min(r0 + 1, last)],
+                        y + pp[min(r0 + 2, last)], y + pp[min(r0 + 3, last)], &qfull[qb]);
+            ++nq[w];
+            return true;
+        };
+        int64_t cur_bh[NWG] = {-1, -1, -1};
+        int cur_e[NWG] = {-1, -1, -1}, changes[NWG] = {0, 0, 0};
+        bool ok = true;
+        if constexpr (IND) {
+            // the warpgroups' ranges, one item of each in turn
+            int pos[NWG];
+            for (int w = 0; w < NWG; ++w) pos[w] = j0(w);
+            for (bool more = true; more && ok;) {
+                more = false;
+                for (int w = 0; w < NWG && ok; ++w) {
+                    if (pos[w] >= j0(w + 1)) continue;
+                    more = true;
+                    const int4 it = a.items[pos[w]++];
+                    if (it.w != cur_bh[w] || it.x != cur_e[w]) {
+                        // wait until this warpgroup's MMAs on its previous list are done
+                        if (changes[w] > 0)
+                            ok = __all_sync(0xffffffffu, mbar_wait(&kvfree[w], (changes[w] - 1) & 1, a.status));
+                        if (!ok) break;
+                        gather_list(it, w, it.w != cur_bh[w]);
+                        cur_bh[w] = it.w;
+                        cur_e[w] = it.x;
+                        ++changes[w];
+                    }
+                    ok = gather_q(it, w);
+                }
+            }
+        } else {
+            for (int r = i0; r < i1 && ok;) {
+                int4 it[NWG];
+                const int cnt = round_items(a, r, i1, it[0], it[1], it[2]);
+                if (it[0].w != cur_bh[0] || it[0].x != cur_e[0]) {
+                    // wait until the MMAs reading the previous lists are done
+                    if (changes[0] > 0)
+                        ok = __all_sync(0xffffffffu, mbar_wait(&kvfree[0], (changes[0] - 1) & 1, a.status));
+                    if (!ok) break;
+                    gather_list(it[0], 0, it[0].w != cur_bh[0]);
+                    cur_bh[0] = it[0].w;
+                    cur_e[0] = it[0].x;
+                    ++changes[0];
+                }
+#pragma unroll
+                for (int w = 0; w < NWG; ++w) {
+                    if (w >= cnt || !ok) break;
+                    ok = gather_q(it[w], w);
+                }
+                r += cnt;
+            }
         }
         // exit: the last phase of every barrier this warp armed has landed
         if (lane == 0) {
-            if (changes > 0) mbar_drain(&kvfull, (changes - 1) & 1);
-            for (int w = 0; w < NWG; ++w)
+            for (int w = 0; w < NWG; ++w) {
+                if (changes[w] > 0) mbar_drain(&kvfull[w], (changes[w] - 1) & 1);
                 for (uint32_t b = 0; b < QB; ++b) {
                     const uint32_t arms = nq[w] > b ? (nq[w] - b + QB - 1) / QB : 0;
                     if (arms > 0) mbar_drain(&qfull[w * QB + b], (arms - 1) & 1);
                 }
+            }
         }
     } else if (warp <= NWG) {
         // ---------------- MMA issuers: lane 0 of warp 1 + w serves warpgroup w ----------------
@@ -377,9 +430,15 @@ __global__ void __launch_bounds__(NT, 1)
         if (lane == 0) {
             const int w = warp - 1;
             const uint32_t tS = tb + tcol_s(w), tP = tb + tcol_p(w), tO = tb + tcol_o(w);
-            const uint64_t kd = sdesc_sw128(smem_u32(S.keys)), vd = sdesc_sw128(smem_u32(S.vals));
+            // IND: this warpgroup's own list, items and list barriers; the rounds
+            // below then hold one item each, all of them this warpgroup's
+            const uint64_t kd = sdesc_sw128(smem_u32(S.keys + w * S.kvstride));
+            const uint64_t vd = sdesc_sw128(smem_u32(S.vals + w * S.kvstride));
             const uint64_t qd = sdesc_sw128(smem_u32(S.q + w * QB * 16384));  // + 1024 per buffer
-            int r = i0, cur_bh = -1, cur_e = -1, changes = 0;
+            const int we = IND ? 0 : w, ie = IND ? j0(w + 1) : i1;
+            uint64_t* kvf = &kvfull[IND ? w : 0];
+            uint64_t* kve = &kvfree[IND ? w : 0];
+            int r = IND ? j0(w) : i0, cur_bh = -1, cur_e = -1, changes = 0;
             uint32_t gs = 0, gp = 0;  // S and P.V blocks issued
             uint32_t nq = 0;          // items whose S has started (query buffer sequence)
             uint32_t npv = 0;         // items whose P.V is complete
@@ -414,18 +473,18 @@ __global__ void __launch_bounds__(NT, 1)
                 return true;
             };
             int4 cur;
-            int st = next_item(a, w, r, i1, cur_bh, cur_e, changes, &kvfull, &kvfree, cur);
+            int st = next_item(a, we, r, ie, cur_bh, cur_e, changes, kvf, kve, cur, IND);
             bool ok = st >= 0, s0 = false;
             while (ok && st > 0) {
                 const uint32_t q = nq++;
                 if (!s0) ok = issue_s(q, 0);
                 for (int j = 1; j < a.nblk && ok; ++j) ok = issue_s(q, j) && issue_pv(j - 1);
                 if (!ok) break;
-                s0 = next_same(a, w, r, i1, cur_bh, cur_e);
+                s0 = next_same(a, we, r, ie, cur_bh, cur_e, IND);
                 if (s0 && !(ok = issue_s(nq, 0))) break;
                 if (!(ok = issue_pv(a.nblk - 1))) break;
                 ++npv;
-                st = next_item(a, w, r, i1, cur_bh, cur_e, changes, &kvfull, &kvfree, cur);
+                st = next_item(a, we, r, ie, cur_bh, cur_e, changes, kvf, kve, cur, IND);
                 ok = st >= 0;
             }
             mma_drain(&drain);  // exit: this issuer's MMAs are done
@@ -445,6 +504,7 @@ __global__ void __launch_bounds__(NT, 1)
         float pend_inv = 0.f;
         uint4* pend_dst = nullptr;
         float pend_m = 0.f, pend_l = 0.f;  // MULTI, STATS: the running max and sum
+        int64_t pend_pos = 0;              // STATS: head * N + the row's position in the grouping
         float* pend_state = nullptr;       // MULTI: the query's state row
         auto epilogue = [&]() {
             if constexpr (STATS) {
@@ -453,10 +513,9 @@ __global__ void __launch_bounds__(NT, 1)
                                              pend_row);
                 tc_fence_before();
                 warp_arrive(&ofree[w]);
-                if (pend_row) {
-                    const int64_t qrow = (reinterpret_cast<const __nv_bfloat16*>(pend_dst) - a.dO) / D;
-                    a.st_delta[qrow] = dl;
-                    a.st_lse[qrow] = pend_m + __log2f(pend_l);
+                if (pend_row) {  // (in grouped order: the row's position in the grouping)
+                    a.st_delta[pend_pos] = dl;
+                    a.st_lse[pend_pos] = pend_m + __log2f(pend_l);
                 }
             } else if constexpr (!MULTI) {
 #pragma unroll
@@ -532,12 +591,14 @@ __global__ void __launch_bounds__(NT, 1)
             }
             pend = false;
         };
-        for (int r = i0; r < i1 && ok;) {
+        // IND: this warpgroup's own range, one item per round
+        const int re = IND ? j0(w + 1) : i1;
+        for (int r = IND ? j0(w) : i0; r < re && ok;) {
             int4 x0, x1, x2;
-            const int cnt = round_items(a, r, i1, x0, x1, x2);
+            const int cnt = round_items(a, r, re, x0, x1, x2, IND);
             r += cnt;
-            if (w >= cnt) continue;
-            const int4 item = pick(w, x0, x1, x2);
+            if (!IND && w >= cnt) continue;
+            const int4 item = IND ? x0 : pick(w, x0, x1, x2);
             const int64_t bh = item.w;
             const int n = t < item.z ? a.perm[bh * a.N + item.y + t] : 0;
             // SPLIT: the shared branch as one pre-merged pair (logit lse, weight 1);
@@ -668,6 +729,7 @@ __global__ void __launch_bounds__(NT, 1)
             pend_inv = 1.f / lrun;
             // (STATS: the query's dO row instead of its output row)
             pend_dst = reinterpret_cast<uint4*>((STATS ? const_cast<__nv_bfloat16*>(a.dO) : a.out) + (bh * a.N + n) * D);
+            if constexpr (STATS) pend_pos = bh * a.N + item.y + t;
             pend_m = mrun;
             pend_l = lrun;
             pend_state = srow;
@@ -685,8 +747,8 @@ __global__ void __launch_bounds__(NT, 1)
     if (warp == 0) tmem_free(tb, 512);
 }
 
-size_t smem_bytes(int nblk, bool split) {
-    return 1024 + static_cast<size_t>(nblk) * 16384 + NWG * QB * 16384 + (split ? NWG * 16384 : 0);
+size_t smem_bytes(int nblk, bool split, bool ind = false) {
+    return 1024 + static_cast<size_t>(nblk) * 16384 * (ind ? NWG : 1) + NWG * QB * 16384 + (split ? NWG * 16384 : 0);
 }
 
 // the shared pairs enter the key list unless they are absent (routing-only
@@ -738,10 +800,15 @@ cudaError_t launch_expert_tc(const Plan& p, const Work& w, const __nv_bfloat16* 
         !make_row_tmap(&tlq, w.lqhi, lrows, 1) || !make_row_tmap(&tlv, w.lvbf, lrows, 1))
         return cudaErrorInvalidValue;
     const size_t sm = smem_bytes(a.nblk, p.split);
-    auto kern = multi ? expert_tc_kernel<kMulti> : (p.split ? expert_tc_kernel<kSplit> : expert_tc_kernel<kPlain>);
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(sm));
+    // short lists (the ViT shapes, short sequences): a list per warpgroup
+    const bool ind = !multi && !p.split && smem_bytes(a.nblk, false, true) <= 232448;
+    const size_t smi = ind ? smem_bytes(a.nblk, false, true) : sm;
+    auto kern = multi ? expert_tc_kernel<kMulti, false>
+                      : (p.split ? expert_tc_kernel<kSplit, false>
+                                 : (ind ? expert_tc_kernel<kPlain, true> : expert_tc_kernel<kPlain, false>));
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smi));
     if (e != cudaSuccess) return e;
-    kern<<<device_sms(), NT, sm, st>>>(tq, tk, tv, tlq, tlv, a);
+    kern<<<device_sms(), NT, smi, st>>>(tq, tk, tv, tlq, tlv, a);
     return cudaGetLastError();
 }
 
@@ -770,10 +837,10 @@ cudaError_t launch_expert_stats(const Plan& p, const Work& w, const __nv_bfloat1
         !make_row_tmap(&tlq, w.lqhi, lrows, 1) || !make_row_tmap(&tlv, w.lvbf, lrows, 1))
         return cudaErrorInvalidValue;
     const size_t sm = smem_bytes(a.nblk, false);
-    cudaError_t e = cudaFuncSetAttribute(expert_tc_kernel<kStats>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(expert_tc_kernel<kStats, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(sm));
     if (e != cudaSuccess) return e;
-    expert_tc_kernel<kStats><<<device_sms(), NT, sm, st>>>(tq, tk, tv, tlq, tlv, a);
+    expert_tc_kernel<kStats, false><<<device_sms(), NT, sm, st>>>(tq, tk, tv, tlq, tlv, a);
     return cudaGetLastError();
 }
 

@@ -165,7 +165,9 @@ cudaError_t launch_scan(const Plan& p, const Work& w, const __nv_bfloat16* K, co
                         cudaStream_t st);
 cudaError_t launch_scan_tc(const Plan& p, const Work& w, const __nv_bfloat16* K, const __nv_bfloat16* V, int level,
                            cudaStream_t st);
-// lse_out (optional): each landmark's log-sum-exp over all keys of tau <Lq_i, K_j>
+// lse_out (optional): each landmark's log-sum-exp over all keys of tau <Lq_i, K_j>.
+// Dense rows of at most 4096 logits take a warp-per-landmark kernel.
+bool dense_row_select_applies(const Plan& p);
 cudaError_t launch_select(const Plan& p, const Work& w, int32_t* expert_idx, cudaStream_t st,
                           float* lse_out = nullptr);
 cudaError_t launch_pilot_select(const Plan& p, const Work& w, int level, cudaStream_t st);
@@ -199,7 +201,8 @@ bool expert_tc_supported(const Plan& p);
 // The backward pass's statistics of the query-expert attention (the plain
 // forward pass's sequence with the shared pairs in the key list): per query
 // the log-sum-exp of its m + k logits (log2 units of tau <q, key>) and
-// Delta = dO . out, into st_lse and st_delta ([BH][N] each).
+// Delta = dO . out, into st_lse and st_delta ([BH][N] each, in the grouped
+// order: entry head * N + p is the query perm[head][p]).
 cudaError_t launch_expert_stats(const Plan& p, const Work& w, const __nv_bfloat16* Q, const __nv_bfloat16* K,
                                 const __nv_bfloat16* V, const int32_t* expert_idx, const __nv_bfloat16* dO,
                                 float* st_lse, float* st_delta, cudaStream_t st);
@@ -230,17 +233,22 @@ cudaError_t launch_backward(const Plan& p, const Work& w, const BwdLayout& L, vo
 // mbarrier nothing completes; records MITA_ERR_TIMEOUT in *status.
 cudaError_t launch_wait_selftest(int* status, uint64_t limit_ns, cudaStream_t st);
 
-// Backward pass on the tensor cores (backward_tc.cu). The expert part: dQ
-// (written), dK, dV of the routed keys (added atomically) and dLq, dLV of
-// the shared keys (added atomically), from the statistics of
-// launch_expert_stats. The landmark part: dK, dV (added) and dLq (added
+// Backward pass on the tensor cores (backward_tc.cu). The expert part: dK,
+// dV of the routed keys (added atomically) and dLq, dLV of the shared keys
+// (added atomically), then dQ, from the statistics of launch_expert_stats. The landmark part: dK, dV (added) and dLq (added
 // atomically), from each landmark's log-sum-exp (log2 units) and
 // Delta' = dLV . LV, with dLV rounded to bf16.
 bool backward_tc_supported(const Plan& p);
-cudaError_t launch_backward_tc_expert(const Plan& p, const Work& w, const __nv_bfloat16* Q, const __nv_bfloat16* K,
-                                      const __nv_bfloat16* V, const __nv_bfloat16* dO, const int32_t* expert_idx,
-                                      const float* st_lse, const float* st_delta, float* dQ, float* dK, float* dV,
-                                      float* dlq, float* dlv, cudaStream_t st);
+cudaError_t launch_backward_tc_expert_keys(const Plan& p, const Work& w, const __nv_bfloat16* Q,
+                                           const __nv_bfloat16* K, const __nv_bfloat16* V, const __nv_bfloat16* dO,
+                                           const int32_t* expert_idx, const float* st_lse, const float* st_delta,
+                                           float* dK, float* dV, float* dlq, float* dlv, cudaStream_t st);
+// dQ (written): the expert attention's share plus the pooling's share of
+// the complete dLq, so it runs after the landmark part
+cudaError_t launch_backward_tc_expert_rows(const Plan& p, const Work& w, const __nv_bfloat16* Q,
+                                           const __nv_bfloat16* K, const __nv_bfloat16* V, const __nv_bfloat16* dO,
+                                           const int32_t* expert_idx, const float* st_lse, const float* st_delta,
+                                           const float* dlq, float* dQ, cudaStream_t st);
 cudaError_t launch_backward_tc_landmark(const Plan& p, const Work& w, const __nv_bfloat16* K, const __nv_bfloat16* V,
                                         const __nv_bfloat16* dlv_bf16, const float* lse2, const float* delta,
                                         float* dK, float* dV, float* dlq, cudaStream_t st);

@@ -334,11 +334,231 @@ __global__ void __launch_bounds__(ST) select_kernel(int m, int k, int chunks, in
     }
 }
 
+// ---------------------------------------------------------------------------
+// Dense rows (short sequences: the dense buffer holds every logit of the
+// landmark's row), one warp per landmark, k <= 32 C. Scores become 32-bit
+// order keys (larger score first). Each lane keeps its C largest keys while
+// the row streams in; theta = the smallest of the lanes' C-th largest is a
+// lower bound on the row's k-th largest key, since every lane holds C keys
+// at or above it (32 C >= k; a lane with fewer than C keys leaves theta = 0,
+// below every key). The keys at or above theta are compacted in index order
+// into shared memory; a radix select over them (8-bit digits, per-warp
+// histogram) finds the k-th largest key, and a walk in index order takes
+// every key above it and, of the keys equal to it, the lowest indices until
+// k are taken: the set ranked by (score desc, index asc), written in
+// ascending index order. More survivors than kSurv (heavy ties) run the same
+// select over the whole row. The warp also merges the landmark's LV partials.
+// ---------------------------------------------------------------------------
+constexpr int DW = 8;        // warps (landmarks) per CTA
+constexpr int kSurv = 512;   // survivors staged per warp
+constexpr int kDenseMaxC = 4;
+
+__device__ __forceinline__ uint32_t score_key32(float raw) {
+    return static_cast<uint32_t>(topk_key(raw * 0.125f, 0u) >> 32);
+}
+
+// k-th largest of `cnt` keys get(e) (e < cnt) by four 8-bit radix passes;
+// returns it and sets *remaining to how many keys equal to it belong to the
+// k largest (warp-uniform results).
+template <class Get>
+__device__ __forceinline__ uint32_t warp_radix_kth(int cnt, unsigned k, unsigned* hist, Get get,
+                                                   unsigned* remaining_out) {
+    const int lane = threadIdx.x & 31;
+    uint32_t prefix = 0, mask = 0;
+    unsigned remaining = k;
+    for (int shift = 24; shift >= 0; shift -= 8) {
+        for (int b = lane; b < 256; b += 32) hist[b] = 0;
+        __syncwarp();
+        for (int e = lane; e < cnt; e += 32) {
+            const uint32_t x = get(e);
+            if ((x & mask) == prefix) atomicAdd(&hist[(x >> shift) & 255u], 1u);
+        }
+        __syncwarp();
+        // lane l holds bins 255-8l .. 248-8l (descending digits)
+        unsigned c[8], tot = 0;
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+            c[t] = hist[255 - 8 * lane - t];
+            tot += c[t];
+        }
+        unsigned incl = tot;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const unsigned y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
+        }
+        const unsigned excl = incl - tot;
+        const bool mine = excl < remaining && remaining <= incl;
+        int digit = 0;
+        unsigned above = 0;
+        if (mine) {
+            unsigned run = excl;
+            for (int t = 0; t < 8; ++t) {
+                if (run + c[t] >= remaining) {
+                    digit = 255 - 8 * lane - t;
+                    above = run;
+                    break;
+                }
+                run += c[t];
+            }
+        }
+        const int src_lane = __ffs(__ballot_sync(0xffffffffu, mine)) - 1;
+        digit = __shfl_sync(0xffffffffu, digit, src_lane);
+        above = __shfl_sync(0xffffffffu, above, src_lane);
+        remaining -= above;
+        prefix |= static_cast<uint32_t>(digit) << shift;
+        mask |= 0xFFu << shift;
+        __syncwarp();
+    }
+    *remaining_out = remaining;
+    return prefix;
+}
+
+// Writes, in ascending order of position e < cnt, idx(e) of every key above
+// kth and of the first `remaining` keys equal to it.
+template <class Get, class Idx>
+__device__ __forceinline__ void warp_take(int cnt, uint32_t kth, unsigned remaining, Get get, Idx idx,
+                                          int32_t* dst) {
+    const int lane = threadIdx.x & 31;
+    const unsigned below = (1u << lane) - 1u;
+    unsigned taken = 0, eq_seen = 0;
+    for (int e0 = 0; e0 < cnt; e0 += 32) {
+        const int e = e0 + lane;
+        const uint32_t x = e < cnt ? get(e) : 0u;
+        const bool gt = e < cnt && x > kth, eq = e < cnt && x == kth;
+        const unsigned eqb = __ballot_sync(0xffffffffu, eq);
+        const bool sel = gt || (eq && eq_seen + __popc(eqb & below) < remaining);
+        const unsigned sb = __ballot_sync(0xffffffffu, sel);
+        if (sel) dst[taken + __popc(sb & below)] = idx(e);
+        taken += __popc(sb);
+        eq_seen += __popc(eqb);
+    }
+}
+
+template <int C>
+__global__ void __launch_bounds__(DW * 32) dense_row_select_kernel(
+    int64_t rows, int m, int k, int chunks, const float* __restrict__ part, float* __restrict__ lv32,
+    __nv_bfloat16* __restrict__ lvbf, int32_t* __restrict__ expert_idx, const float* __restrict__ dense, int n,
+    int64_t ld, float* __restrict__ lse_out) {
+    __shared__ uint32_t s_key[DW][kSurv];
+    __shared__ int32_t s_idx[DW][kSurv];
+    __shared__ unsigned s_hist[DW][256];
+    const int wid = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t row = static_cast<int64_t>(blockIdx.x) * DW + wid;  // (head, landmark)
+    if (row >= rows) return;  // (warp-uniform; no block-wide barrier below)
+
+    // ---- shared-expert value: merge of the chunks' partials ----
+    if (part) {
+        const int64_t bh = row / m, i = row % m;
+        auto part_of = [&](int c) { return part + ((bh * chunks + c) * m + i) * 68; };
+        float M = -INFINITY;
+        for (int c = 0; c < chunks; ++c) M = fmaxf(M, part_of(c)[0]);
+        float L = 0.f, o0 = 0.f, o1 = 0.f;
+        for (int c = 0; c < chunks; ++c) {
+            const float* pp = part_of(c);
+            const float f = exp2f((pp[0] - M) * kLog2e);
+            L += pp[1] * f;
+            o0 += pp[4 + lane] * f;
+            o1 += pp[36 + lane] * f;
+        }
+        o0 /= L;
+        o1 /= L;
+        lv32[row * D + lane] = o0;
+        lv32[row * D + 32 + lane] = o1;
+        lvbf[row * D + lane] = __float2bfloat16_rn(o0);
+        lvbf[row * D + 32 + lane] = __float2bfloat16_rn(o1);
+        if (lse_out && lane == 0) lse_out[row] = M + logf(L);
+    }
+
+    // ---- routed expert: the k best of the row ----
+    const float* src = dense + row * ld;  // ld is a multiple of 4: float4 rows
+    uint32_t t[C];
+#pragma unroll
+    for (int c = 0; c < C; ++c) t[c] = 0u;
+    for (int e0 = 4 * lane; e0 < n; e0 += 128) {
+        const float4 v = __ldg(reinterpret_cast<const float4*>(src + e0));
+        const float f[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            uint32_t x = e0 + j < n ? score_key32(f[j]) : 0u;
+#pragma unroll
+            for (int c = 0; c < C; ++c) {  // insert into t[0] >= t[1] >= ...
+                const uint32_t hi = max(t[c], x);
+                x = min(t[c], x);
+                t[c] = hi;
+            }
+        }
+    }
+    const uint32_t theta = __reduce_min_sync(0xffffffffu, t[C - 1]);
+    // survivors (keys >= theta) in index order
+    const unsigned below = (1u << lane) - 1u;
+    unsigned total = 0;
+    for (int b0 = 0; b0 < n; b0 += 128) {
+        const int e0 = b0 + 4 * lane;
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (e0 < n) v = __ldg(reinterpret_cast<const float4*>(src + e0));
+        const float f[4] = {v.x, v.y, v.z, v.w};
+        uint32_t x[4];
+        unsigned bl[4], before = 0;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            x[j] = e0 + j < n ? score_key32(f[j]) : 0u;
+            bl[j] = __ballot_sync(0xffffffffu, e0 + j < n && x[j] >= theta);
+            before += __popc(bl[j] & below);
+        }
+        unsigned pos = total + before;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            if ((bl[j] >> lane) & 1u) {
+                if (pos < kSurv) {
+                    s_key[wid][pos] = x[j];
+                    s_idx[wid][pos] = e0 + j;
+                }
+                ++pos;
+            }
+        }
+        total += __popc(bl[0]) + __popc(bl[1]) + __popc(bl[2]) + __popc(bl[3]);
+    }
+    __syncwarp();
+    int32_t* dst = expert_idx + row * static_cast<int64_t>(k);
+    unsigned remaining;
+    if (total <= static_cast<unsigned>(kSurv)) {
+        const int cnt = static_cast<int>(total);
+        auto get = [&](int e) { return s_key[wid][e]; };
+        const uint32_t kth = warp_radix_kth(cnt, static_cast<unsigned>(k), s_hist[wid], get, &remaining);
+        warp_take(cnt, kth, remaining, get, [&](int e) { return s_idx[wid][e]; }, dst);
+    } else {
+        auto get = [&](int e) { return score_key32(src[e]); };
+        const uint32_t kth = warp_radix_kth(n, static_cast<unsigned>(k), s_hist[wid], get, &remaining);
+        warp_take(n, kth, remaining, get, [](int e) { return e; }, dst);
+    }
+}
+
 }  // namespace
+
+bool dense_row_select_applies(const Plan& p) {
+    const ScanLevel& L = p.lev[p.nlev - 1];
+    return L.dense && p.s.k <= p.s.N && p.s.k <= 32 * kDenseMaxC;
+}
 
 cudaError_t launch_select(const Plan& p, const Work& w, int32_t* expert_idx, cudaStream_t st, float* lse_out) {
     const unsigned grid = static_cast<unsigned>(p.s.BH * p.s.m);
     const ScanLevel& L = p.lev[p.nlev - 1];
+    if (dense_row_select_applies(p)) {
+        const int64_t rows = p.s.BH * p.s.m;
+        const unsigned grid = static_cast<unsigned>((rows + DW - 1) / DW);
+        auto go = [&](auto kern) {
+            kern<<<grid, DW * 32, 0, st>>>(rows, p.s.m, p.s.k, L.chunks, p.shared ? w.part : nullptr, w.lv32, w.lvbf,
+                                           expert_idx, w.dense, static_cast<int>(p.s.N), L.ld, lse_out);
+        };
+        switch ((p.s.k + 31) / 32) {
+            case 1: go(dense_row_select_kernel<1>); break;
+            case 2: go(dense_row_select_kernel<2>); break;
+            case 3: go(dense_row_select_kernel<3>); break;
+            default: go(dense_row_select_kernel<4>); break;
+        }
+        return cudaGetLastError();
+    }
     select_kernel<false><<<grid, ST, 0, st>>>(p.s.m, p.s.k, L.chunks, L.cap, p.shared ? w.part : nullptr, w.cand,
                                              w.ccount, w.lv32,
                                              w.lvbf, expert_idx, nullptr, L.dense ? w.dense : nullptr, p.s.N, L.ld,

@@ -254,6 +254,19 @@ def test_exact_ties_go_to_lower_index(orc):
     parity.full_parity(orc, q, kk_, v, 0, 0, m, k, gpu=gpu)
 
 
+def test_all_scores_tied_in_dense_rows(orc):
+    """Every key row identical: each landmark's N logits tie exactly, so its
+    expert is the k lowest indices. On this short, ragged sequence the select
+    ranks whole logit rows, and every key survives its threshold (the path
+    that ranks the whole row)."""
+    B, H, N, m, k = 1, 2, 2999, 16, 100
+    q, kk_, v = _rand(B, H, N, 37)
+    kk_ = np.repeat(kk_[:, :, :1], N, axis=2).copy()
+    gpu = parity.run_gpu(q, kk_, v, 0, 0, m, k)
+    assert np.array_equal(gpu["expert_idx"], np.broadcast_to(np.arange(k, dtype=np.int32), (B, H, m, k)))
+    parity.full_parity(orc, q, kk_, v, 0, 0, m, k, gpu=gpu)
+
+
 def test_empty_batch():
     import torch
 
