@@ -31,8 +31,13 @@
 // accumulated over all the rows of the unit. One work unit = 128 keys: a
 // block of an expert's list (rows: that expert's queries) or a tile of the
 // head's keys (rows: its landmarks).
-// Warps: 0-3 the 128 row (or key) threads, 4 the producer (TMA), 5 the MMA
-// issuer. Every wait is bounded (umma.cuh).
+// Warps: 0-15 the row (or key) threads, four per TMEM lane quarter, each
+// taking a quarter of a block's columns (p and ds are elementwise once the
+// row statistics are known, so nothing is reduced across them); 16 the
+// producer (TMA), 17 and 18 the MMA issuers: one for the products that
+// read the rows and keys (S, dP), one for the gradient products (G; dV and
+// dK), so the next block's S and dP run while the threads and G work on
+// this one. Every wait is bounded (umma.cuh).
 #include <algorithm>
 
 #include "pool_grad.cuh"
@@ -48,7 +53,10 @@ using namespace umma;
 constexpr float kTau = 0.125f;
 constexpr float kC = 0.125f * kLog2e;  // tau * log2(e)
 constexpr int kExp = 0, kLmk = 1;       // expert attention / landmark attention
-constexpr int NTB = 192;               // 4 row warps, producer, issuer
+constexpr int RW = 4;                  // row (key) warps per TMEM lane quarter
+constexpr int NRW = 4 * RW;            // row (key) warps: 0 .. NRW - 1
+constexpr int PW = NRW;                // producer warp; the MMA issuers are PW + 1 (S, dP), PW + 2 (G)
+constexpr int NTB = (NRW + 3) * 32;
 constexpr int TILE = 16384;            // 128 rows of 64 bf16
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
@@ -92,10 +100,19 @@ __device__ __forceinline__ void list_rows4(const BArgs& a, int64_t bh, const int
 // ============================================================================
 // Keys kernel
 // ============================================================================
-// shared memory: key blocks c = 0, 1 (KB, VB) at 32 KB c; row tile buffers
-// b = 0, 1 at 64 KB + b * 49 KB: R, R_lo (LMK), dR, then L[128], Delta[128]
-constexpr size_t KOFF_BUF = 65536, KBUF = 3 * TILE + 1024;
-constexpr size_t KSMEM = KOFF_BUF + 2 * KBUF + 1024;
+// shared memory: key blocks c = 0, 1 (KB, VB) at 32 KB c; then the row tile
+// buffers: EXP four of R, dR, L[128], Delta[128] (33 KB each), LMK two of
+// R, R_lo, dR, L, Delta (49 KB each)
+constexpr size_t KOFF_BUF = 65536;
+template <int MODE>
+struct KRow {
+    static constexpr int n = MODE == kExp ? 4 : 2;                         // buffers
+    static constexpr size_t dr = MODE == kExp ? TILE : 2 * TILE;           // dR
+    static constexpr size_t st = MODE == kExp ? 2 * TILE : 3 * TILE;       // L, Delta
+    static constexpr size_t size = st + 1024;
+};
+constexpr size_t KSMEM = KOFF_BUF + 4 * (2 * TILE + 1024) + 1024;
+static_assert(4 * (2 * TILE + 1024) >= 2 * (3 * TILE + 1024), "row buffers of both modes fit");
 // TMEM columns
 constexpr uint32_t cS = 0, cDP = 128, cP = 256, cDS = 320, cV = 384, cK = 448;
 
@@ -131,7 +148,8 @@ __global__ void __launch_bounds__(NTB, 1)
     // LMK: tk, tv: K, V, 128 rows high; tr, tsk: Lq hi, lo; tdr: dLV (bf16),
     //      128 rows high.
     extern __shared__ uint8_t smem_raw[];
-    __shared__ uint64_t kvfull[2], kvfree[2], rfull[2], rfree[2], sfull, sfree, pfull, pvdone, afree, drain;
+    using RB = KRow<MODE>;
+    __shared__ uint64_t kvfull[2], kvfree[2], rfull[4], rfree[4], sfull, sfree, pfull, pvdone, afree, drain[2];
     __shared__ uint32_t tmem_base;
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -140,15 +158,18 @@ __global__ void __launch_bounds__(NTB, 1)
         for (int b = 0; b < 2; ++b) {
             mbar_init(&kvfull[b], 1);
             mbar_init(&kvfree[b], 1);
+        }
+        for (int b = 0; b < RB::n; ++b) {
             mbar_init(&rfull[b], 2);  // the loads' transaction count, and the statistics
             mbar_init(&rfree[b], 1);
         }
         mbar_init(&sfull, 1);
-        mbar_init(&sfree, 4);
-        mbar_init(&pfull, 4);
+        mbar_init(&sfree, NRW);
+        mbar_init(&pfull, NRW);
         mbar_init(&pvdone, 1);
-        mbar_init(&afree, 4);
-        mbar_init(&drain, 1);
+        mbar_init(&afree, NRW);
+        mbar_init(&drain[0], 1);
+        mbar_init(&drain[1], 1);
         fence_barrier_init();
     }
     if (warp == 0) tmem_alloc(&tmem_base, 512);
@@ -157,93 +178,122 @@ __global__ void __launch_bounds__(NTB, 1)
     tc_fence_after();
     const uint32_t tb = tmem_base;
     auto kbuf = [&](int c) { return base + c * 2 * TILE; };  // keys, then values at + TILE
-    auto rbuf = [&](int b) { return base + KOFF_BUF + b * KBUF; };
+    auto rbuf = [&](int b) { return base + KOFF_BUF + b * RB::size; };
 
-    if (warp == 4) {
+    if (warp == PW) {
         // ---------------------------------- producer ----------------------------------
+        // Tiles in order (units with no tiles skipped). The global values a
+        // tile needs (EXP: its queries, the key list rows of a unit's first
+        // tile; both: the rows' statistics) are loaded into registers one tile
+        // ahead, so their latency overlaps the wait for a free buffer.
+        struct Cur {
+            int64_t u, bh;
+            int e, b, ntiles, qoff, qcnt, t;
+        };
+        auto first_of = [&](int64_t u, Cur& c) -> bool {  // the first tile at or after unit u
+            for (; u < u1; ++u) {
+                keys_unit<MODE>(a, u, c.bh, c.e, c.b, c.ntiles, c.qoff, c.qcnt);
+                if (c.ntiles > 0) {
+                    c.u = u;
+                    c.t = 0;
+                    return true;
+                }
+            }
+            return false;
+        };
+        const int r0 = 4 * lane;
+        int q[4], y[4];
+        bool sh = false;
+        float L4[4], D4[4];
+        auto fetch = [&](const Cur& c) {
+            if (MODE == kExp) {
+                const int* pp = a.perm + c.bh * a.N + c.qoff + 128 * c.t;
+                const int cnt = min(128, c.qcnt - 128 * c.t);
+                const int64_t gp = c.bh * a.N + c.qoff + 128 * c.t + r0;  // statistics in grouped order
+#pragma unroll
+                for (int x = 0; x < 4; ++x) {
+                    q[x] = pp[min(r0 + x, cnt - 1)];  // padding repeats the last query
+                    const bool v = r0 + x < cnt;
+                    L4[x] = v ? a.lse[gp + x] : INFINITY;
+                    D4[x] = v ? a.delta[gp + x] : 0.f;
+                }
+                if (c.t == 0) {
+                    const int32_t* sel = a.expert_idx + (c.bh * a.m + c.e) * static_cast<int64_t>(a.k);
+                    list_rows4(a, c.bh, sel, 128 * c.b + r0, y, &sh);
+                }
+            } else {
+#pragma unroll
+                for (int x = 0; x < 4; ++x) {
+                    const int li = 128 * c.t + r0 + x;
+                    const bool v = li < a.m;
+                    L4[x] = v ? a.lse[c.bh * a.m + li] : INFINITY;
+                    D4[x] = v ? a.delta[c.bh * a.m + li] : 0.f;
+                }
+            }
+        };
         int ucount = 0, tseq = 0;
         bool ok = true;
-        for (int64_t u = u0; u < u1 && ok; ++u) {
-            int64_t bh;
-            int e, b, ntiles, qoff, qcnt;
-            keys_unit<MODE>(a, u, bh, e, b, ntiles, qoff, qcnt);
-            if (ntiles == 0) continue;
-            const int kb = ucount & 1;  // this unit's key block buffer, last used two units back
-            if (ucount >= 2) ok = __all_sync(0xffffffffu, mbar_wait(&kvfree[kb], ((ucount >> 1) - 1) & 1, a.status));
-            if (!ok) break;
-            uint8_t* KBs = kbuf(kb);
-            uint8_t* VBs = KBs + TILE;
-            if (lane == 0) mbar_arrive_expect_tx(&kvfull[kb], 2 * TILE);
-            __syncwarp();
-            if (MODE == kExp) {  // list positions 128 b + 4 lane .. + 3
-                const int32_t* sel = a.expert_idx + (bh * a.m + e) * static_cast<int64_t>(a.k);
-                int y[4];
-                bool sh;
-                list_rows4(a, bh, sel, 128 * b + 4 * lane, y, &sh);
-                tma_gather4(KBs + 4 * lane * 128, sh ? &tsk : &tk, 0, y[0], y[1], y[2], y[3], &kvfull[kb]);
-                tma_gather4(VBs + 4 * lane * 128, sh ? &tsv : &tv, 0, y[0], y[1], y[2], y[3], &kvfull[kb]);
-            } else if (lane == 0) {
-                tma_load_2d(KBs, &tk, 0, static_cast<int>(bh * a.N + 128 * b), &kvfull[kb]);
-                tma_load_2d(VBs, &tv, 0, static_cast<int>(bh * a.N + 128 * b), &kvfull[kb]);
-            }
-            for (int t = 0; t < ntiles && ok; ++t) {
-                const int buf = tseq & 1;
-                if (tseq >= 2) ok = __all_sync(0xffffffffu, mbar_wait(&rfree[buf], ((tseq >> 1) - 1) & 1, a.status));
+        Cur c;
+        bool have = first_of(u0, c);
+        if (have) fetch(c);
+        while (have && ok) {
+            if (c.t == 0) {
+                const int kb = ucount & 1;  // this unit's key block buffer, last used two units back
+                if (ucount >= 2) ok = __all_sync(0xffffffffu, mbar_wait(&kvfree[kb], ((ucount >> 1) - 1) & 1, a.status));
                 if (!ok) break;
-                uint8_t* rb = rbuf(buf);
-                float* sl = reinterpret_cast<float*>(rb + 3 * TILE);
-                if (lane == 0) mbar_arrive_expect_tx(&rfull[buf], (MODE == kExp ? 2 : 3) * TILE);
+                uint8_t* KBs = kbuf(kb);
+                uint8_t* VBs = KBs + TILE;
+                if (lane == 0) mbar_arrive_expect_tx(&kvfull[kb], 2 * TILE);
                 __syncwarp();
-                const int r0 = 4 * lane;
-                if (MODE == kExp) {  // the tile's queries (padding repeats the last)
-                    const int* pp = a.perm + bh * a.N + qoff + 128 * t;
-                    const int cnt = min(128, qcnt - 128 * t);
-                    int q[4];
-#pragma unroll
-                    for (int x = 0; x < 4; ++x) q[x] = pp[min(r0 + x, cnt - 1)];
-                    const int y = static_cast<int>(bh * a.N);
-                    tma_gather4(rb + r0 * 128, &tr, 0, y + q[0], y + q[1], y + q[2], y + q[3], &rfull[buf]);
-                    tma_gather4(rb + 2 * TILE + r0 * 128, &tdr, 0, y + q[0], y + q[1], y + q[2], y + q[3], &rfull[buf]);
-                    const int64_t gp = bh * a.N + qoff + 128 * t + r0;  // statistics in grouped order
-#pragma unroll
-                    for (int x = 0; x < 4; ++x) {
-                        const bool v = r0 + x < cnt;
-                        sl[r0 + x] = v ? a.lse[gp + x] : INFINITY;
-                        sl[128 + r0 + x] = v ? a.delta[gp + x] : 0.f;
-                    }
-                } else {
-                    if (lane == 0) {
-                        const int y = static_cast<int>(bh * a.m + 128 * t);
-                        tma_load_2d(rb, &tr, 0, y, &rfull[buf]);
-                        tma_load_2d(rb + TILE, &tsk, 0, y, &rfull[buf]);
-                        tma_load_2d(rb + 2 * TILE, &tdr, 0, y, &rfull[buf]);
-                    }
-#pragma unroll
-                    for (int x = 0; x < 4; ++x) {
-                        const int li = 128 * t + r0 + x;
-                        const bool v = li < a.m;
-                        sl[r0 + x] = v ? a.lse[bh * a.m + li] : INFINITY;
-                        sl[128 + r0 + x] = v ? a.delta[bh * a.m + li] : 0.f;
-                    }
+                if (MODE == kExp) {  // list positions 128 b + 4 lane .. + 3
+                    tma_gather4(KBs + r0 * 128, sh ? &tsk : &tk, 0, y[0], y[1], y[2], y[3], &kvfull[kb]);
+                    tma_gather4(VBs + r0 * 128, sh ? &tsv : &tv, 0, y[0], y[1], y[2], y[3], &kvfull[kb]);
+                } else if (lane == 0) {
+                    tma_load_2d(KBs, &tk, 0, static_cast<int>(c.bh * a.N + 128 * c.b), &kvfull[kb]);
+                    tma_load_2d(VBs, &tv, 0, static_cast<int>(c.bh * a.N + 128 * c.b), &kvfull[kb]);
                 }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&rfull[buf]);  // the statistics are in place
-                ++tseq;
+                ++ucount;
             }
-            ++ucount;
+            const int buf = tseq % RB::n;
+            if (tseq >= RB::n) ok = __all_sync(0xffffffffu, mbar_wait(&rfree[buf], ((tseq / RB::n) - 1) & 1, a.status));
+            if (!ok) break;
+            uint8_t* rb = rbuf(buf);
+            float* sl = reinterpret_cast<float*>(rb + RB::st);
+            if (lane == 0) mbar_arrive_expect_tx(&rfull[buf], (MODE == kExp ? 2 : 3) * TILE);
+            __syncwarp();
+            if (MODE == kExp) {  // the tile's queries
+                const int yb = static_cast<int>(c.bh * a.N);
+                tma_gather4(rb + r0 * 128, &tr, 0, yb + q[0], yb + q[1], yb + q[2], yb + q[3], &rfull[buf]);
+                tma_gather4(rb + RB::dr + r0 * 128, &tdr, 0, yb + q[0], yb + q[1], yb + q[2], yb + q[3], &rfull[buf]);
+            } else if (lane == 0) {
+                const int yl = static_cast<int>(c.bh * a.m + 128 * c.t);
+                tma_load_2d(rb, &tr, 0, yl, &rfull[buf]);
+                tma_load_2d(rb + TILE, &tsk, 0, yl, &rfull[buf]);
+                tma_load_2d(rb + RB::dr, &tdr, 0, yl, &rfull[buf]);
+            }
+            *reinterpret_cast<float4*>(sl + r0) = make_float4(L4[0], L4[1], L4[2], L4[3]);
+            *reinterpret_cast<float4*>(sl + 128 + r0) = make_float4(D4[0], D4[1], D4[2], D4[3]);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&rfull[buf]);  // the statistics are in place
+            ++tseq;
+            // the next tile, and its values
+            if (++c.t == c.ntiles) have = first_of(c.u + 1, c);
+            if (have) fetch(c);
         }
         if (lane == 0) {  // exit: the last phase of every barrier armed here has landed
             for (int b = 0; b < 2; ++b) {
                 const int karms = ucount > b ? (ucount - b + 1) / 2 : 0;
                 if (karms > 0) mbar_drain(&kvfull[b], (karms - 1) & 1);
-                const int arms = tseq > b ? (tseq - b + 1) / 2 : 0;
+            }
+            for (int b = 0; b < RB::n; ++b) {
+                const int arms = tseq > b ? (tseq - b + RB::n - 1) / RB::n : 0;
                 if (arms > 0) mbar_drain(&rfull[b], (arms - 1) & 1);
             }
         }
-    } else if (warp == 5) {
-        // ---------------------------------- MMA issuer ----------------------------------
+    } else if (warp == PW + 1) {
+        // ------------------------------ S, dP issuer ------------------------------
         if (lane == 0) {
-            const uint32_t idS = idesc_bf16(128, 128, false), idG = idesc_bf16(128, 64, true);
+            const uint32_t idS = idesc_bf16(128, 128, false);
             int ucount = 0, tseq = 0;
             bool ok = true;
             for (int64_t u = u0; u < u1 && ok; ++u) {
@@ -255,21 +305,47 @@ __global__ void __launch_bounds__(NTB, 1)
                 if (!(ok = mbar_wait(&kvfull[kb], (ucount >> 1) & 1, a.status))) break;
                 const uint64_t kd = sdesc_sw128(smem_u32(kbuf(kb))), vd = sdesc_sw128(smem_u32(kbuf(kb) + TILE));
                 for (int t = 0; t < ntiles; ++t) {
-                    const int buf = tseq & 1;
-                    if (!(ok = mbar_wait(&rfull[buf], (tseq >> 1) & 1, a.status))) break;
+                    const int buf = tseq % RB::n;
+                    if (!(ok = mbar_wait(&rfull[buf], (tseq / RB::n) & 1, a.status))) break;
+                    // the key threads have read the previous tile's S and dP
                     if (tseq >= 1 && !(ok = mbar_wait(&sfree, (tseq - 1) & 1, a.status))) break;
                     tc_fence_after();
                     const uint32_t rs = smem_u32(rbuf(buf));
                     mma_ss_k64(tb + cS, kd, sdesc_sw128(rs), idS, 0u);
                     if (MODE == kLmk) mma_ss_k64(tb + cS, kd, sdesc_sw128(rs + TILE), idS, 1u);
-                    mma_ss_k64(tb + cDP, vd, sdesc_sw128(rs + 2 * TILE), idS, 0u);
+                    mma_ss_k64(tb + cDP, vd, sdesc_sw128(rs + RB::dr), idS, 0u);
                     mma_commit(&sfull);
+                    ++tseq;
+                }
+                if (!ok) break;
+                mma_commit(&kvfree[kb]);  // the key block is read by S and dP only
+                ++ucount;
+            }
+            mma_drain(&drain[0]);
+        }
+    } else if (warp == PW + 2) {
+        // -------------------------------- G issuer --------------------------------
+        if (lane == 0) {
+            const uint32_t idG = idesc_bf16(128, 64, true);
+            int ucount = 0, tseq = 0;
+            bool ok = true;
+            for (int64_t u = u0; u < u1 && ok; ++u) {
+                int64_t bh;
+                int e, b, ntiles, qoff, qcnt;
+                keys_unit<MODE>(a, u, bh, e, b, ntiles, qoff, qcnt);
+                if (ntiles == 0) continue;
+                for (int t = 0; t < ntiles; ++t) {
+                    const int buf = tseq % RB::n;
+                    // the row tile (for its layout in shared memory) and the
+                    // threads' p^T and ds^T of it
+                    if (!(ok = mbar_wait(&rfull[buf], (tseq / RB::n) & 1, a.status))) break;
                     if (!(ok = mbar_wait(&pfull, tseq & 1, a.status))) break;
                     // the first products of a unit overwrite the accumulators: the
                     // key threads have read the previous unit's
                     if (t == 0 && ucount >= 1 && !(ok = mbar_wait(&afree, (ucount - 1) & 1, a.status))) break;
                     tc_fence_after();
-                    const uint64_t dr = sdesc_sw128(rs + 2 * TILE), rr = sdesc_sw128(rs);
+                    const uint32_t rs = smem_u32(rbuf(buf));
+                    const uint64_t dr = sdesc_sw128(rs + RB::dr), rr = sdesc_sw128(rs);
 #pragma unroll 1
                     for (int s = 0; s < 8; ++s) {  // K = the tile's 128 rows, 16 per step
                         const uint32_t acc = (t > 0 || s > 0) ? 1u : 0u;
@@ -277,18 +353,22 @@ __global__ void __launch_bounds__(NTB, 1)
                         mma_ts(tb + cK, tb + cDS + 8 * s, rr + static_cast<uint64_t>(s) * 128, idG, acc);
                     }
                     mma_commit(&pvdone);
-                    mma_commit(&rfree[buf]);
+                    mma_commit(&rfree[buf]);  // S and dP of the tile completed before pfull
                     ++tseq;
                 }
                 if (!ok) break;
-                mma_commit(&kvfree[kb]);
                 ++ucount;
             }
-            mma_drain(&drain);
+            mma_drain(&drain[1]);
         }
     } else {
         // ------------------------------- key threads -------------------------------
+        // warp w: TMEM lanes 32 (w % 4) .. + 31 (the unit's keys), rows
+        // 32 (w / 4) .. + 31 of each row tile, and accumulator columns
+        // 16 (w / 4) .. + 15
+        static_assert(RW == 4, "one 32-row chunk of the tile per key warp");
         const int t_ = (warp & 3) * 32 + lane;  // TMEM lane = key row of the unit
+        const int cg = warp >> 2;
         const uint32_t lo = static_cast<uint32_t>((warp & 3) * 32) << 16;
         int ucount = 0, tseq = 0;
         bool ok = true;
@@ -298,32 +378,26 @@ __global__ void __launch_bounds__(NTB, 1)
             keys_unit<MODE>(a, u, bh, e, b, ntiles, qoff, qcnt);
             if (ntiles == 0) continue;
             for (int t = 0; t < ntiles && ok; ++t) {
-                const int buf = tseq & 1;
+                const int buf = tseq % RB::n;
                 ok = __all_sync(0xffffffffu, mbar_wait(&sfull, tseq & 1, a.status));
                 if (!ok) break;
                 tc_fence_after();
-                // p^T and ds^T go where the previous tile's products read them
-                if (tseq >= 1) {
-                    ok = __all_sync(0xffffffffu, mbar_wait(&pvdone, (tseq - 1) & 1, a.status));
-                    if (!ok) break;
-                    tc_fence_after();
-                }
-                const float* sl = reinterpret_cast<const float*>(rbuf(buf) + 3 * TILE);
-#pragma unroll 1
-                for (int c = 0; c < 4; ++c) {  // 32 rows of the tile at a time
-                    float sv[32], dv[32];
-                    tmem_ld32(tb + cS + 32 * c + lo, sv);
-                    tmem_ld32(tb + cDP + 32 * c + lo, dv);
+                const float* sl = reinterpret_cast<const float*>(rbuf(buf) + RB::st) + 32 * cg;
+#pragma unroll
+                for (int h = 0; h < 2 && ok; ++h) {  // 16 rows at a time
+                    float sv[16], dv[16];
+                    tmem_ld16(tb + cS + 32 * cg + 16 * h + lo, sv);
+                    tmem_ld16(tb + cDP + 32 * cg + 16 * h + lo, dv);
                     tmem_ld_wait();
-                    if (c == 3) {
+                    if (h == 1) {
                         tc_fence_before();
                         warp_arrive(&sfree);
                     }
-                    uint32_t pk[16], dk[16];
+                    uint32_t pk[8], dk[8];
 #pragma unroll
-                    for (int j = 0; j < 32; j += 4) {
-                        const float4 L = *reinterpret_cast<const float4*>(sl + 32 * c + j);
-                        const float4 Dl = *reinterpret_cast<const float4*>(sl + 128 + 32 * c + j);
+                    for (int j = 0; j < 16; j += 4) {
+                        const float4 L = *reinterpret_cast<const float4*>(sl + 16 * h + j);
+                        const float4 Dl = *reinterpret_cast<const float4*>(sl + 128 + 16 * h + j);
                         const float p0 = exp2f(fmaf(sv[j], kC, -L.x)), p1 = exp2f(fmaf(sv[j + 1], kC, -L.y));
                         const float p2 = exp2f(fmaf(sv[j + 2], kC, -L.z)), p3 = exp2f(fmaf(sv[j + 3], kC, -L.w));
                         pk[j >> 1] = pack_bf16(p0, p1);
@@ -331,30 +405,34 @@ __global__ void __launch_bounds__(NTB, 1)
                         dk[j >> 1] = pack_bf16(p0 * (dv[j] - Dl.x), p1 * (dv[j + 1] - Dl.y));
                         dk[(j >> 1) + 1] = pack_bf16(p2 * (dv[j + 2] - Dl.z), p3 * (dv[j + 3] - Dl.w));
                     }
-                    tmem_st16u(tb + cP + 16 * c + lo, pk);
-                    tmem_st16u(tb + cDS + 16 * c + lo, dk);
+                    // p^T and ds^T go where the previous tile's products read them
+                    if (h == 0 && tseq >= 1) {
+                        ok = __all_sync(0xffffffffu, mbar_wait(&pvdone, (tseq - 1) & 1, a.status));
+                        if (!ok) break;
+                        tc_fence_after();
+                    }
+                    tmem_st8u(tb + cP + 16 * cg + 8 * h + lo, pk);
+                    tmem_st8u(tb + cDS + 16 * cg + 8 * h + lo, dk);
                 }
+                if (!ok) break;
                 tmem_st_wait();
                 tc_fence_before();
                 warp_arrive(&pfull);
                 ++tseq;
             }
             if (!ok) break;
-            // the unit's gradients of its 128 keys
+            // the unit's gradients of its 128 keys, columns 16 cg .. + 15
             ok = __all_sync(0xffffffffu, mbar_wait(&pvdone, (tseq - 1) & 1, a.status));
             if (!ok) break;
             tc_fence_after();
-            float gvv[64], gkk[64];
-            tmem_ld32(tb + cV + lo, gvv);
-            tmem_ld32(tb + cV + 32 + lo, gvv + 32);
-            tmem_ld32(tb + cK + lo, gkk);
-            tmem_ld32(tb + cK + 32 + lo, gkk + 32);
+            float gvv[16], gkk[16];
+            tmem_ld16(tb + cV + 16 * cg + lo, gvv);
+            tmem_ld16(tb + cK + 16 * cg + lo, gkk);
             tmem_ld_wait();
             tc_fence_before();
             warp_arrive(&afree);
             float* dkp = nullptr;
             float* dvp = nullptr;
-            bool atomic = true;
             if (MODE == kExp) {
                 const int x = 128 * b + t_;
                 if (x < a.m) {
@@ -367,7 +445,6 @@ __global__ void __launch_bounds__(NTB, 1)
                 }
             } else {
                 const int64_t j = 128LL * b + t_;
-                atomic = false;  // this unit alone writes these keys
                 if (j < a.N) {
                     dkp = a.gk + (bh * a.N + j) * D;
                     dvp = a.gv + (bh * a.N + j) * D;
@@ -375,19 +452,12 @@ __global__ void __launch_bounds__(NTB, 1)
             }
             if (dkp) {
 #pragma unroll
-                for (int c = 0; c < 64; c += 4) {
+                for (int c = 0; c < 16; c += 4) {
                     const float4 kk = make_float4(gkk[c] * kTau, gkk[c + 1] * kTau, gkk[c + 2] * kTau, gkk[c + 3] * kTau);
                     const float4 vv = make_float4(gvv[c], gvv[c + 1], gvv[c + 2], gvv[c + 3]);
-                    float4* pk4 = reinterpret_cast<float4*>(dkp + c);
-                    float4* pv4 = reinterpret_cast<float4*>(dvp + c);
-                    if (atomic) {
-                        atomicAdd(pk4, kk);
-                        atomicAdd(pv4, vv);
-                    } else {
-                        float4 x = *pk4, y = *pv4;
-                        *pk4 = make_float4(x.x + kk.x, x.y + kk.y, x.z + kk.z, x.w + kk.w);
-                        *pv4 = make_float4(y.x + vv.x, y.y + vv.y, y.z + vv.z, y.w + vv.w);
-                    }
+                    // reductions (no value returned): nothing waits for them
+                    atomicAdd(reinterpret_cast<float4*>(dkp + 16 * cg + c), kk);
+                    atomicAdd(reinterpret_cast<float4*>(dvp + 16 * cg + c), vv);
                 }
             }
             ++ucount;
@@ -446,7 +516,7 @@ __global__ void __launch_bounds__(NTB, 1)
     //      128 rows high.
     extern __shared__ uint8_t smem_raw[];
     __shared__ uint64_t rfull[2], rfree[2], kfull[RST], kempty[RST], sfull[2], sfree[2], pfull[2], dsfree[2];
-    __shared__ uint64_t gdone, gfree, drain, kvfull, kvfree;
+    __shared__ uint64_t gdone, gfree, drain[2], kvfull, kvfree;
     __shared__ uint32_t tmem_base;
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -457,8 +527,8 @@ __global__ void __launch_bounds__(NTB, 1)
             mbar_init(&rfull[b], 1);
             mbar_init(&rfree[b], 1);
             mbar_init(&sfull[b], 1);
-            mbar_init(&sfree[b], 4);
-            mbar_init(&pfull[b], 4);
+            mbar_init(&sfree[b], NRW);
+            mbar_init(&pfull[b], NRW);
             mbar_init(&dsfree[b], 1);
         }
         for (int s = 0; s < RST; ++s) {
@@ -466,10 +536,11 @@ __global__ void __launch_bounds__(NTB, 1)
             mbar_init(&kempty[s], 1);
         }
         mbar_init(&gdone, 1);
-        mbar_init(&gfree, 4);
-        mbar_init(&drain, 1);
+        mbar_init(&gfree, NRW);
+        mbar_init(&drain[0], 1);
+        mbar_init(&drain[1], 1);
         mbar_init(&kvfull, 1);
-        mbar_init(&kvfree, 1);
+        mbar_init(&kvfree, 2);  // both issuers read the expert's list
         fence_barrier_init();
     }
     if (warp == 0) tmem_alloc(&tmem_base, 512);
@@ -484,7 +555,7 @@ __global__ void __launch_bounds__(NTB, 1)
     uint8_t* listk = base + 2 * RB;                                  // EXP: list block j at + 8 KB j
     uint8_t* listv = listk + a.nblk * 8192;
 
-    if (warp == 4) {
+    if (warp == PW) {
         // ---------------------------------- producer ----------------------------------
         int useq = 0, g = 0, changes = 0, cur_e = -1;
         int64_t cur_bh = -1;
@@ -558,25 +629,14 @@ __global__ void __launch_bounds__(NTB, 1)
                 if (arms > 0) mbar_drain(&kfull[s], (arms - 1) & 1);
             }
         }
-    } else if (warp == 5) {
-        // ---------------------------------- MMA issuer ----------------------------------
+    } else if (warp == PW + 1 || warp == PW + 2) {
+        // ------------------- MMA issuers: S and dP (PW + 1), G (PW + 2) -------------------
         if (lane == 0) {
+            const bool gi = warp == PW + 2;
             const uint32_t idS = idesc_bf16(128, 64, false), idG = idesc_bf16(128, 64, true);
             int useq = 0, g = 0, changes = 0, cur_e = -1;
             int64_t cur_bh = -1;
             bool ok = true;
-            // G += ds(h) K(h), the unit's block h (list block jb of EXP; first: overwrite G)
-            auto gstep = [&](int h, int jb, bool first) -> bool {
-                const int sb = h & 1;
-                if (!mbar_wait(&pfull[sb], (h >> 1) & 1, a.status)) return false;
-                if (first && useq >= 1 && !mbar_wait(&gfree, (useq - 1) & 1, a.status)) return false;
-                tc_fence_after();
-                const uint64_t kmn = sdesc_sw128(smem_u32(MODE == kExp ? listk + jb * 8192 : kst(h % RST)));
-                mma_ts_k64(tb + rG, tb + rDS + 32 * sb, kmn, idG, first ? 0u : 1u);
-                mma_commit(&dsfree[sb]);
-                if (MODE == kLmk) mma_commit(&kempty[h % RST]);
-                return true;
-            };
             for (int64_t u = u0; u < u1 && ok; ++u) {
                 int64_t bh, c0, c1;
                 int4 item;
@@ -595,30 +655,50 @@ __global__ void __launch_bounds__(NTB, 1)
                 }
                 if (!(ok = mbar_wait(&rfull[buf], (useq >> 1) & 1, a.status))) break;
                 const uint32_t rs = smem_u32(rbuf(buf));
-                for (int j = 0; j < nb && ok; ++j, ++g) {
-                    const int s = g % RST, sb = g & 1;
-                    if (MODE == kLmk && !(ok = mbar_wait(&kfull[s], (g / RST) & 1, a.status))) break;
-                    if (g >= 2 && !(ok = mbar_wait(&sfree[sb], ((g >> 1) - 1) & 1, a.status))) break;
-                    tc_fence_after();
-                    const uint32_t ks = MODE == kExp ? smem_u32(listk + j * 8192) : smem_u32(kst(s));
-                    const uint32_t vs = MODE == kExp ? smem_u32(listv + j * 8192) : ks + 8192;
-                    mma_ss_k64(tb + rS + 64 * sb, sdesc_sw128(rs), sdesc_sw128(ks), idS, 0u);
-                    if (MODE == kLmk) mma_ss_k64(tb + rS + 64 * sb, sdesc_sw128(rs + TILE), sdesc_sw128(ks), idS, 1u);
-                    mma_ss_k64(tb + rDP + 64 * sb, sdesc_sw128(rs + DROFF), sdesc_sw128(vs), idS, 0u);
-                    mma_commit(&sfull[sb]);
-                    if (j >= 1) ok = gstep(g - 1, j - 1, j == 1);
+                if (!gi) {
+                    for (int j = 0; j < nb && ok; ++j, ++g) {
+                        const int s = g % RST, sb = g & 1;
+                        if (MODE == kLmk && !(ok = mbar_wait(&kfull[s], (g / RST) & 1, a.status))) break;
+                        // the rows have read block g - 2's S and dP
+                        if (g >= 2 && !(ok = mbar_wait(&sfree[sb], ((g >> 1) - 1) & 1, a.status))) break;
+                        tc_fence_after();
+                        const uint32_t ks = MODE == kExp ? smem_u32(listk + j * 8192) : smem_u32(kst(s));
+                        const uint32_t vs = MODE == kExp ? smem_u32(listv + j * 8192) : ks + 8192;
+                        mma_ss_k64(tb + rS + 64 * sb, sdesc_sw128(rs), sdesc_sw128(ks), idS, 0u);
+                        if (MODE == kLmk)
+                            mma_ss_k64(tb + rS + 64 * sb, sdesc_sw128(rs + TILE), sdesc_sw128(ks), idS, 1u);
+                        mma_ss_k64(tb + rDP + 64 * sb, sdesc_sw128(rs + DROFF), sdesc_sw128(vs), idS, 0u);
+                        mma_commit(&sfull[sb]);
+                    }
+                } else {
+                    // G += ds(j) K(j) (the first block of the unit overwrites G)
+                    for (int j = 0; j < nb && ok; ++j, ++g) {
+                        const int s = g % RST, sb = g & 1;
+                        if (!(ok = mbar_wait(&pfull[sb], (g >> 1) & 1, a.status))) break;
+                        if (j == 0 && useq >= 1 && !(ok = mbar_wait(&gfree, (useq - 1) & 1, a.status))) break;
+                        tc_fence_after();
+                        const uint64_t kmn = sdesc_sw128(smem_u32(MODE == kExp ? listk + j * 8192 : kst(s)));
+                        mma_ts_k64(tb + rG, tb + rDS + 32 * sb, kmn, idG, j == 0 ? 0u : 1u);
+                        mma_commit(&dsfree[sb]);
+                        if (MODE == kLmk) mma_commit(&kempty[s]);  // (S and dP of the block completed before pfull)
+                    }
+                    if (!ok) break;
+                    mma_commit(&gdone);
+                    mma_commit(&rfree[buf]);
                 }
                 if (!ok) break;
-                if (!(ok = gstep(g - 1, nb - 1, nb == 1))) break;
-                mma_commit(&gdone);
-                mma_commit(&rfree[buf]);
                 ++useq;
             }
-            mma_drain(&drain);
+            mma_drain(&drain[gi ? 1 : 0]);
         }
     } else {
         // ------------------------------- row threads -------------------------------
+        // warp w: TMEM lanes 32 (w % 4) .. + 31 (the unit's rows), key
+        // columns 16 (w / 4) .. + 15 of each 64-key block, and columns
+        // 16 (w / 4) .. + 15 of G
+        static_assert(RW == 4, "16 of each block's 64 columns per row warp");
         const int t = (warp & 3) * 32 + lane;  // TMEM lane = row of the unit
+        const int cg = warp >> 2;
         const uint32_t lo = static_cast<uint32_t>((warp & 3) * 32) << 16;
         int useq = 0, g = 0;
         bool ok = true;
@@ -650,18 +730,16 @@ __global__ void __launch_bounds__(NTB, 1)
                 ok = __all_sync(0xffffffffu, mbar_wait(&sfull[sb], (g >> 1) & 1, a.status));
                 if (!ok) break;
                 tc_fence_after();
-                float sv[64], dv[64];
-                tmem_ld32(tb + rS + 64 * sb + lo, sv);
-                tmem_ld32(tb + rS + 64 * sb + 32 + lo, sv + 32);
-                tmem_ld32(tb + rDP + 64 * sb + lo, dv);
-                tmem_ld32(tb + rDP + 64 * sb + 32 + lo, dv + 32);
+                float sv[16], dv[16];
+                tmem_ld16(tb + rS + 64 * sb + 16 * cg + lo, sv);
+                tmem_ld16(tb + rDP + 64 * sb + 16 * cg + lo, dv);
                 tmem_ld_wait();
                 tc_fence_before();
                 warp_arrive(&sfree[sb]);
-                const int x0 = 64 * j;
-                uint32_t pk[32];
+                const int x0 = 64 * j + 16 * cg;
+                uint32_t pk[8];
 #pragma unroll
-                for (int c = 0; c < 64; c += 2) {
+                for (int c = 0; c < 16; c += 2) {
                     const int x = x0 + c;
                     // EXP: the unused positions [m, m4) and those past the list; LMK: past the chunk
                     const bool v0 = x < nkeys && (MODE == kLmk || x < a.m || x >= a.m4);
@@ -675,8 +753,7 @@ __global__ void __launch_bounds__(NTB, 1)
                     if (!ok) break;
                 }
                 tc_fence_after();
-                tmem_st16u(tb + rDS + 32 * sb + lo, pk);
-                tmem_st16u(tb + rDS + 32 * sb + 16 + lo, pk + 16);
+                tmem_st8u(tb + rDS + 32 * sb + 8 * cg + lo, pk);
                 tmem_st_wait();
                 tc_fence_before();
                 warp_arrive(&pfull[sb]);
@@ -685,9 +762,8 @@ __global__ void __launch_bounds__(NTB, 1)
             ok = __all_sync(0xffffffffu, mbar_wait(&gdone, useq & 1, a.status));
             if (!ok) break;
             tc_fence_after();
-            float gg[64];
-            tmem_ld32(tb + rG + lo, gg);
-            tmem_ld32(tb + rG + 32 + lo, gg + 32);
+            float gg[16];
+            tmem_ld16(tb + rG + 16 * cg + lo, gg);
             tmem_ld_wait();
             tc_fence_before();
             warp_arrive(&gfree);
@@ -696,11 +772,11 @@ __global__ void __launch_bounds__(NTB, 1)
                     // dQ of the query: its expert attention's share and the
                     // pooling's share of the (complete) dLq of its windows
 #pragma unroll
-                    for (int c = 0; c < 64; ++c) gg[c] *= kTau;
+                    for (int c = 0; c < 16; ++c) gg[c] *= kTau;
                     pool_windows_of(a.N, a.gh, a.gw, a.p, a.m, orow - bh * a.N, [&](int i, float wgt) {
-                        const float4* s4 = reinterpret_cast<const float4*>(a.slq + (bh * a.m + i) * D);
+                        const float4* s4 = reinterpret_cast<const float4*>(a.slq + (bh * a.m + i) * D + 16 * cg);
 #pragma unroll
-                        for (int c = 0; c < 16; ++c) {
+                        for (int c = 0; c < 4; ++c) {
                             const float4 v = s4[c];
                             gg[4 * c] = fmaf(v.x, wgt, gg[4 * c]);
                             gg[4 * c + 1] = fmaf(v.y, wgt, gg[4 * c + 1]);
@@ -708,13 +784,13 @@ __global__ void __launch_bounds__(NTB, 1)
                             gg[4 * c + 3] = fmaf(v.w, wgt, gg[4 * c + 3]);
                         }
                     });
-                    float4* dst = reinterpret_cast<float4*>(a.gk + orow * D);
+                    float4* dst = reinterpret_cast<float4*>(a.gk + orow * D + 16 * cg);
 #pragma unroll
-                    for (int c = 0; c < 64; c += 4) dst[c / 4] = make_float4(gg[c], gg[c + 1], gg[c + 2], gg[c + 3]);
+                    for (int c = 0; c < 16; c += 4) dst[c / 4] = make_float4(gg[c], gg[c + 1], gg[c + 2], gg[c + 3]);
                 } else {  // dLq of the landmark, summed over the key chunks
-                    float4* dst = reinterpret_cast<float4*>(a.gv + orow * D);
+                    float4* dst = reinterpret_cast<float4*>(a.gv + orow * D + 16 * cg);
 #pragma unroll
-                    for (int c = 0; c < 64; c += 4)
+                    for (int c = 0; c < 16; c += 4)
                         atomicAdd(dst + c / 4,
                                   make_float4(gg[c] * kTau, gg[c + 1] * kTau, gg[c + 2] * kTau, gg[c + 3] * kTau));
                 }
