@@ -3,6 +3,7 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl mita|reference]
                     [--config long1m] [--no-sweep] [--no-cpu] [--no-e2e]
+                    [--only backward]
 
 One step = one full forward pass (landmark pooling, landmark scan with expert
 selection, routing, grouping, expert attention) over one synthetic batch
@@ -802,12 +803,25 @@ def main():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--s-route", type=int, default=1, help="routed experts per query (1: the pages' configuration)")
+    ap.add_argument("--only", choices=("backward",),
+                    help="run one side measurement alone on --config and print its JSON (no headline line)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "mita":
         ap.error("--warmup must be >= 3")
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
-    if args.impl == "reference":
+    if args.only == "backward":
+        import torch
+
+        import mixture_top_forward_gb300 as M
+
+        dev = torch.device("cuda", 0)
+        torch.cuda.set_device(dev)
+        M.load(build_if_missing=False)
+        peaks, _ = load_peaks()
+        res = {"only": "backward", "config": args.config,
+               "backward": backward(args, M, dev, torch.cuda.current_stream(dev), peaks)}
+    elif args.impl == "reference":
         res = run_reference(args, rank, world)
     else:
         if world > 1:
