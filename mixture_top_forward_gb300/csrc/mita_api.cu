@@ -380,9 +380,23 @@ struct Recorded {
     cudaStream_t stream;
     cudaEvent_t ev[kStages + 1];
     int launches[kStages];
+    int first;  // stages before `first` ran no kernel (their events are not recorded)
 };
 thread_local bool t_profile = false;
 thread_local std::vector<Recorded> t_records;
+// Events are reused across calls: creating eight per call made the host, not
+// the GPU, set the pace of short passes while profiling.
+thread_local std::vector<cudaEvent_t> t_free_events;
+
+cudaEvent_t take_event() {
+    if (!t_free_events.empty()) {
+        cudaEvent_t e = t_free_events.back();
+        t_free_events.pop_back();
+        return e;
+    }
+    cudaEvent_t e = nullptr;
+    return cudaEventCreate(&e) == cudaSuccess ? e : nullptr;
+}
 
 struct StageMarks {
     Recorded rec{};
@@ -391,22 +405,30 @@ struct StageMarks {
         if (!t_profile) return;
         rec.stream = st;
         for (auto& e : rec.ev)
-            if (cudaEventCreate(&e) != cudaSuccess) return;
+            if (!(e = take_event())) {
+                release();
+                return;
+            }
         on = true;
+    }
+    void release() {
+        for (auto& e : rec.ev)
+            if (e) t_free_events.push_back(e);
+        for (auto& e : rec.ev) e = nullptr;
     }
     void mark(int i) {
         if (on) cudaEventRecord(rec.ev[i], rec.stream);
     }
-    void commit(const int* launches) {
+    void commit(const int* launches, int first = 0) {
         if (on) {
             for (int i = 0; i < kStages; ++i) rec.launches[i] = launches[i];
+            rec.first = first;
             t_records.push_back(rec);
         }
         on = false;
     }
     ~StageMarks() {
-        if (on)
-            for (auto& e : rec.ev) cudaEventDestroy(e);
+        if (on) release();
     }
 };
 
@@ -415,6 +437,16 @@ int run_forward(const Plan& P, const Work& W, const __nv_bfloat16* Q, const __nv
                 const __nv_bfloat16* V, __nv_bfloat16* out, int32_t* expert_idx, int32_t* route, float* lq_out,
                 float* lv_out, cudaStream_t st) {
     cudaError_t e;
+    if (small_fused_applies(P)) {  // a short head: every stage in one kernel (timed as the expert stage)
+        StageMarks marks(st);
+        marks.mark(6);
+        if ((e = launch_small_fused(P, Q, K, V, out, expert_idx, route, lq_out, lv_out, st)) != cudaSuccess)
+            return cuda_fail(e, "fused short-head launch");
+        marks.mark(7);
+        const int launches[kStages] = {0, 0, 0, 0, 0, 0, 1};
+        marks.commit(launches, 6);
+        return MITA_OK;
+    }
     const size_t mrows = static_cast<size_t>(P.s.BH) * P.s.m;
     const int sr = P.s.s_route;
     if ((e = cudaMemsetAsync(W.counts, 0, sr * mrows * sizeof(int), st)) != cudaSuccess ||
@@ -774,12 +806,12 @@ extern "C" int mita_profile_read(double* stage_ms, int64_t* stage_launches, int 
         }
         for (int i = 0; i < n; ++i) {
             float ms = 0.f;
-            if (rc == MITA_OK && (e = cudaEventElapsedTime(&ms, r.ev[i], r.ev[i + 1])) != cudaSuccess)
+            if (i >= r.first && rc == MITA_OK && (e = cudaEventElapsedTime(&ms, r.ev[i], r.ev[i + 1])) != cudaSuccess)
                 rc = cuda_fail(e, "cudaEventElapsedTime");
             if (stage_ms) stage_ms[i] += ms;
             if (stage_launches) stage_launches[i] += r.launches[i];
         }
-        for (auto& ev : r.ev) cudaEventDestroy(ev);
+        for (auto& ev : r.ev) t_free_events.push_back(ev);
     }
     t_records.swap(keep);
     return rc == MITA_OK ? kStages : rc;

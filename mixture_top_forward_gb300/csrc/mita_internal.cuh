@@ -253,6 +253,14 @@ cudaError_t launch_backward_tc_landmark(const Plan& p, const Work& w, const __nv
                                         const __nv_bfloat16* dlv_bf16, const float* lse2, const float* delta,
                                         float* dK, float* dV, float* dlq, cudaStream_t st);
 
+// The whole forward pass of a short head in one kernel (small_fused.cu):
+// N <= 256, m <= 32, s = 1, with the shared branch, not split. Writes out,
+// expert_idx, route and (when not null) Lq, LV [BH][m][64] fp32.
+bool small_fused_applies(const Plan& p);
+cudaError_t launch_small_fused(const Plan& p, const __nv_bfloat16* Q, const __nv_bfloat16* K, const __nv_bfloat16* V,
+                               __nv_bfloat16* out, int32_t* expert_idx, int32_t* route, float* lq_out, float* lv_out,
+                               cudaStream_t st);
+
 // Number of SMs of the current device (cached per device).
 int device_sms();
 

@@ -18,6 +18,7 @@
 // landmark's k-th largest sample key and raises the landmark's threshold to
 // it: k keys of the head reach that value, so the true k-th best does too.
 #include "topk.cuh"
+#include "warp_select.cuh"
 
 namespace mita {
 
@@ -353,88 +354,6 @@ constexpr int DW = 8;        // warps (landmarks) per CTA
 constexpr int kSurv = 512;   // survivors staged per warp
 constexpr int kDenseMaxC = 4;
 
-__device__ __forceinline__ uint32_t score_key32(float raw) {
-    return static_cast<uint32_t>(topk_key(raw * 0.125f, 0u) >> 32);
-}
-
-// k-th largest of `cnt` keys get(e) (e < cnt) by four 8-bit radix passes;
-// returns it and sets *remaining to how many keys equal to it belong to the
-// k largest (warp-uniform results).
-template <class Get>
-__device__ __forceinline__ uint32_t warp_radix_kth(int cnt, unsigned k, unsigned* hist, Get get,
-                                                   unsigned* remaining_out) {
-    const int lane = threadIdx.x & 31;
-    uint32_t prefix = 0, mask = 0;
-    unsigned remaining = k;
-    for (int shift = 24; shift >= 0; shift -= 8) {
-        for (int b = lane; b < 256; b += 32) hist[b] = 0;
-        __syncwarp();
-        for (int e = lane; e < cnt; e += 32) {
-            const uint32_t x = get(e);
-            if ((x & mask) == prefix) atomicAdd(&hist[(x >> shift) & 255u], 1u);
-        }
-        __syncwarp();
-        // lane l holds bins 255-8l .. 248-8l (descending digits)
-        unsigned c[8], tot = 0;
-#pragma unroll
-        for (int t = 0; t < 8; ++t) {
-            c[t] = hist[255 - 8 * lane - t];
-            tot += c[t];
-        }
-        unsigned incl = tot;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const unsigned y = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += y;
-        }
-        const unsigned excl = incl - tot;
-        const bool mine = excl < remaining && remaining <= incl;
-        int digit = 0;
-        unsigned above = 0;
-        if (mine) {
-            unsigned run = excl;
-            for (int t = 0; t < 8; ++t) {
-                if (run + c[t] >= remaining) {
-                    digit = 255 - 8 * lane - t;
-                    above = run;
-                    break;
-                }
-                run += c[t];
-            }
-        }
-        const int src_lane = __ffs(__ballot_sync(0xffffffffu, mine)) - 1;
-        digit = __shfl_sync(0xffffffffu, digit, src_lane);
-        above = __shfl_sync(0xffffffffu, above, src_lane);
-        remaining -= above;
-        prefix |= static_cast<uint32_t>(digit) << shift;
-        mask |= 0xFFu << shift;
-        __syncwarp();
-    }
-    *remaining_out = remaining;
-    return prefix;
-}
-
-// Writes, in ascending order of position e < cnt, idx(e) of every key above
-// kth and of the first `remaining` keys equal to it.
-template <class Get, class Idx>
-__device__ __forceinline__ void warp_take(int cnt, uint32_t kth, unsigned remaining, Get get, Idx idx,
-                                          int32_t* dst) {
-    const int lane = threadIdx.x & 31;
-    const unsigned below = (1u << lane) - 1u;
-    unsigned taken = 0, eq_seen = 0;
-    for (int e0 = 0; e0 < cnt; e0 += 32) {
-        const int e = e0 + lane;
-        const uint32_t x = e < cnt ? get(e) : 0u;
-        const bool gt = e < cnt && x > kth, eq = e < cnt && x == kth;
-        const unsigned eqb = __ballot_sync(0xffffffffu, eq);
-        const bool sel = gt || (eq && eq_seen + __popc(eqb & below) < remaining);
-        const unsigned sb = __ballot_sync(0xffffffffu, sel);
-        if (sel) dst[taken + __popc(sb & below)] = idx(e);
-        taken += __popc(sb);
-        eq_seen += __popc(eqb);
-    }
-}
-
 template <int C>
 __global__ void __launch_bounds__(DW * 32) dense_row_select_kernel(
     int64_t rows, int m, int k, int chunks, const float* __restrict__ part, float* __restrict__ lv32,
@@ -526,11 +445,11 @@ __global__ void __launch_bounds__(DW * 32) dense_row_select_kernel(
         const int cnt = static_cast<int>(total);
         auto get = [&](int e) { return s_key[wid][e]; };
         const uint32_t kth = warp_radix_kth(cnt, static_cast<unsigned>(k), s_hist[wid], get, &remaining);
-        warp_take(cnt, kth, remaining, get, [&](int e) { return s_idx[wid][e]; }, dst);
+        warp_take(cnt, kth, remaining, get, [&](int e) { return s_idx[wid][e]; }, [&](int r, int32_t x) { dst[r] = x; });
     } else {
         auto get = [&](int e) { return score_key32(src[e]); };
         const uint32_t kth = warp_radix_kth(n, static_cast<unsigned>(k), s_hist[wid], get, &remaining);
-        warp_take(n, kth, remaining, get, [](int e) { return e; }, dst);
+        warp_take(n, kth, remaining, get, [](int e) { return e; }, [&](int r, int32_t x) { dst[r] = x; });
     }
 }
 
