@@ -550,6 +550,19 @@ int64_t cdiv64(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 }  // namespace
 
+// Rows of Q and dO in grouped order: row p of head h is query perm[h][p]
+// (16 bytes a thread).
+static __global__ void group_rows_kernel(const __nv_bfloat16* __restrict__ Q, const __nv_bfloat16* __restrict__ dO,
+                                  const int* __restrict__ perm, int64_t rows, int64_t N, __nv_bfloat16* __restrict__ qg,
+                                  __nv_bfloat16* __restrict__ dog) {
+    const int64_t x = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (x >= rows * 8) return;
+    const int64_t r = x >> 3, c = x & 7;
+    const int64_t src = (r / N) * N + perm[r];
+    reinterpret_cast<uint4*>(qg)[r * 8 + c] = __ldg(reinterpret_cast<const uint4*>(Q) + src * 8 + c);
+    reinterpret_cast<uint4*>(dog)[r * 8 + c] = __ldg(reinterpret_cast<const uint4*>(dO) + src * 8 + c);
+}
+
 BwdLayout backward_layout(const Plan& p) {
     BwdLayout L{};
     const int64_t BH = p.s.BH, N = p.s.N, m = p.s.m;
@@ -578,6 +591,8 @@ BwdLayout backward_layout(const Plan& p) {
     L.off_eidx = take(tc ? BH * m * static_cast<size_t>(p.s.k) * sizeof(int32_t) : 0);
     L.off_lse2 = take(tc ? BH * m * sizeof(float) : 0);
     L.off_dlvb = take(tc ? BH * m * D * 2 : 0);
+    L.off_qg = take(tc ? BH * N * D * 2 : 0);
+    L.off_dog = take(tc ? BH * N * D * 2 : 0);
     L.total = off;
     return L;
 }
@@ -629,8 +644,14 @@ cudaError_t launch_backward(const Plan& p, const Work& w, const BwdLayout& L, vo
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         if ((e = launch_group(p, w, route_ok, 0, st)) != cudaSuccess) return e;
         if ((e = launch_expert_stats(p, w, Q, K, V, expert_idx, dO, qlse, qdelta, st)) != cudaSuccess) return e;
-        // expert attention, key side: dK, dV of the routed keys, dLq, dLV of the shared ones
-        if ((e = launch_backward_tc_expert_keys(p, w, Q, K, V, dO, expert_idx, qlse, qdelta, dK, dV, dlq, dlv,
+        // expert attention, key side: dK, dV of the routed keys, dLq, dLV of the
+        // shared ones; its row tiles from copies of Q and dO in grouped order
+        __nv_bfloat16* qg = reinterpret_cast<__nv_bfloat16*>(b + L.off_qg);
+        __nv_bfloat16* dog = reinterpret_cast<__nv_bfloat16*>(b + L.off_dog);
+        group_rows_kernel<<<static_cast<unsigned>(cdiv64(static_cast<int64_t>(rows) * 8, 256)), 256, 0, st>>>(
+            Q, dO, w.perm, static_cast<int64_t>(rows), N, qg, dog);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        if ((e = launch_backward_tc_expert_keys(p, w, qg, K, V, dog, expert_idx, qlse, qdelta, dK, dV, dlq, dlv,
                                                 st)) != cudaSuccess)
             return e;
         // landmark attention: dK, dV, dLq
@@ -639,7 +660,7 @@ cudaError_t launch_backward(const Plan& p, const Work& w, const BwdLayout& L, vo
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
         if ((e = launch_backward_tc_landmark(p, w, K, V, dlvb, lse2, dlt, dK, dV, dlq, st)) != cudaSuccess) return e;
         // expert attention, row side, and the pooling: dQ
-        return launch_backward_tc_expert_rows(p, w, Q, K, V, dO, expert_idx, qlse, qdelta, dlq, dQ, st);
+        return launch_backward_tc_expert_rows(p, w, qg, K, V, dog, expert_idx, qlse, qdelta, dlq, dQ, st);
     }
     const unsigned g1 = static_cast<unsigned>(BH * L.ltiles * L.chunks);
     lm_stats_kernel<<<g1, BT, 0, st>>>(K, V, N, m, L.ltiles, L.chunks, L.chunk_len, w.lq32, part);

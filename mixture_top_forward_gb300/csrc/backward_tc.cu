@@ -202,17 +202,15 @@ __global__ void __launch_bounds__(NTB, 1)
             return false;
         };
         const int r0 = 4 * lane;
-        int q[4], y[4];
+        int y[4];
         bool sh = false;
         float L4[4], D4[4];
         auto fetch = [&](const Cur& c) {
             if (MODE == kExp) {
-                const int* pp = a.perm + c.bh * a.N + c.qoff + 128 * c.t;
                 const int cnt = min(128, c.qcnt - 128 * c.t);
                 const int64_t gp = c.bh * a.N + c.qoff + 128 * c.t + r0;  // statistics in grouped order
 #pragma unroll
                 for (int x = 0; x < 4; ++x) {
-                    q[x] = pp[min(r0 + x, cnt - 1)];  // padding repeats the last query
                     const bool v = r0 + x < cnt;
                     L4[x] = v ? a.lse[gp + x] : INFINITY;
                     D4[x] = v ? a.delta[gp + x] : 0.f;
@@ -261,10 +259,15 @@ __global__ void __launch_bounds__(NTB, 1)
             float* sl = reinterpret_cast<float*>(rb + RB::st);
             if (lane == 0) mbar_arrive_expect_tx(&rfull[buf], (MODE == kExp ? 2 : 3) * TILE);
             __syncwarp();
-            if (MODE == kExp) {  // the tile's queries
-                const int yb = static_cast<int>(c.bh * a.N);
-                tma_gather4(rb + r0 * 128, &tr, 0, yb + q[0], yb + q[1], yb + q[2], yb + q[3], &rfull[buf]);
-                tma_gather4(rb + RB::dr + r0 * 128, &tdr, 0, yb + q[0], yb + q[1], yb + q[2], yb + q[3], &rfull[buf]);
+            if (MODE == kExp) {
+                // the tile's queries and their dO, in grouped order (rows past
+                // the expert's queries belong to the next expert or lie past
+                // the end, zero-filled: their statistics mask them)
+                if (lane == 0) {
+                    const int yg = static_cast<int>(c.bh * a.N + c.qoff + 128 * c.t);
+                    tma_load_2d(rb, &tr, 0, yg, &rfull[buf]);
+                    tma_load_2d(rb + RB::dr, &tdr, 0, yg, &rfull[buf]);
+                }
             } else if (lane == 0) {
                 const int yl = static_cast<int>(c.bh * a.m + 128 * c.t);
                 tma_load_2d(rb, &tr, 0, yl, &rfull[buf]);
@@ -589,14 +592,14 @@ __global__ void __launch_bounds__(NTB, 1)
             uint8_t* rb = rbuf(buf);
             if (lane == 0) mbar_arrive_expect_tx(&rfull[buf], (MODE == kExp ? 2 : 3) * TILE);
             __syncwarp();
-            if (MODE == kExp) {  // the item's queries (padding repeats the last)
-                const int* pp = a.perm + bh * a.N + item.y;
-                const int r0 = 4 * lane, last = item.z - 1;
-                const int y = static_cast<int>(bh * a.N);
-                const int q0 = y + pp[min(r0, last)], q1 = y + pp[min(r0 + 1, last)];
-                const int q2 = y + pp[min(r0 + 2, last)], q3 = y + pp[min(r0 + 3, last)];
-                tma_gather4(rb + r0 * 128, &tr, 0, q0, q1, q2, q3, &rfull[buf]);
-                tma_gather4(rb + DROFF + r0 * 128, &tdr, 0, q0, q1, q2, q3, &rfull[buf]);
+            if (MODE == kExp) {
+                // the item's queries and their dO, in grouped order (rows past
+                // the item are masked: those threads' rows are not the item's)
+                if (lane == 0) {
+                    const int y = static_cast<int>(bh * a.N + item.y);
+                    tma_load_2d(rb, &tr, 0, y, &rfull[buf]);
+                    tma_load_2d(rb + DROFF, &tdr, 0, y, &rfull[buf]);
+                }
             } else if (lane == 0) {
                 const int y = static_cast<int>(bh * a.m + 128 * lt);
                 tma_load_2d(rb, &tr, 0, y, &rfull[buf]);
@@ -847,13 +850,16 @@ static int exp_setup(const Plan& p, const Work& w, const __nv_bfloat16* Q, const
            make_row_tmap(&maps[4], Q, rows, 1) && make_row_tmap(&maps[5], dO, rows, 1);
 }
 
-cudaError_t launch_backward_tc_expert_keys(const Plan& p, const Work& w, const __nv_bfloat16* Q,
-                                           const __nv_bfloat16* K, const __nv_bfloat16* V, const __nv_bfloat16* dO,
+cudaError_t launch_backward_tc_expert_keys(const Plan& p, const Work& w, const __nv_bfloat16* Qg,
+                                           const __nv_bfloat16* K, const __nv_bfloat16* V, const __nv_bfloat16* dOg,
                                            const int32_t* expert_idx, const float* st_lse, const float* st_delta,
                                            float* dK, float* dV, float* dlq, float* dlv, cudaStream_t st) {
     BArgs a;
     CUtensorMap maps[6];
-    if (!exp_setup(p, w, Q, K, V, dO, expert_idx, st_lse, st_delta, maps, a)) return cudaErrorInvalidValue;
+    if (!exp_setup(p, w, Qg, K, V, dOg, expert_idx, st_lse, st_delta, maps, a)) return cudaErrorInvalidValue;
+    // the row tiles: 128 consecutive rows of the grouped copies
+    const uint64_t rows = static_cast<uint64_t>(p.s.BH) * p.s.N;
+    if (!make_row_tmap(&maps[4], Qg, rows, 128) || !make_row_tmap(&maps[5], dOg, rows, 128)) return cudaErrorInvalidValue;
     // one unit per (head, expert, 128-key block of its list)
     a.nblk = (a.m4 + a.k + 127) / 128;
     a.units = p.s.BH * static_cast<int64_t>(p.s.m) * a.nblk;
@@ -864,13 +870,16 @@ cudaError_t launch_backward_tc_expert_keys(const Plan& p, const Work& w, const _
     return launch6(bwd_keys_kernel<kExp>, KSMEM, std::min<int64_t>(device_sms(), a.units), maps, a, st);
 }
 
-cudaError_t launch_backward_tc_expert_rows(const Plan& p, const Work& w, const __nv_bfloat16* Q,
-                                           const __nv_bfloat16* K, const __nv_bfloat16* V, const __nv_bfloat16* dO,
+cudaError_t launch_backward_tc_expert_rows(const Plan& p, const Work& w, const __nv_bfloat16* Qg,
+                                           const __nv_bfloat16* K, const __nv_bfloat16* V, const __nv_bfloat16* dOg,
                                            const int32_t* expert_idx, const float* st_lse, const float* st_delta,
                                            const float* dlq, float* dQ, cudaStream_t st) {
     BArgs a;
     CUtensorMap maps[6];
-    if (!exp_setup(p, w, Q, K, V, dO, expert_idx, st_lse, st_delta, maps, a)) return cudaErrorInvalidValue;
+    if (!exp_setup(p, w, Qg, K, V, dOg, expert_idx, st_lse, st_delta, maps, a)) return cudaErrorInvalidValue;
+    // an item's rows: 128 consecutive rows of the grouped copies
+    const uint64_t rows = static_cast<uint64_t>(p.s.BH) * p.s.N;
+    if (!make_row_tmap(&maps[4], Qg, rows, 128) || !make_row_tmap(&maps[5], dOg, rows, 128)) return cudaErrorInvalidValue;
     // one unit per item, over the expert's list in 64-key blocks
     a.nblk = (a.m4 + a.k + 63) / 64;
     a.gk = dQ;

@@ -218,7 +218,7 @@ struct BwdLayout {
     size_t off_lv, off_lse, off_part, off_dlq, off_dlv, off_dlt, off_route;
     // tensor-core path: per-query statistics, the recomputed expert sets, the
     // landmarks' log-sum-exp (log2 units) and dLV in bf16
-    size_t off_qlse, off_qdelta, off_eidx, off_lse2, off_dlvb, total;
+    size_t off_qlse, off_qdelta, off_eidx, off_lse2, off_dlvb, off_qg, off_dog, total;
 };
 BwdLayout backward_layout(const Plan& p);
 // Gradients dQ, dK, dV (fp32, [BH][N][64], overwritten) of sum(out * dO) with
@@ -239,14 +239,15 @@ cudaError_t launch_wait_selftest(int* status, uint64_t limit_ns, cudaStream_t st
 // atomically), from each landmark's log-sum-exp (log2 units) and
 // Delta' = dLV . LV, with dLV rounded to bf16.
 bool backward_tc_supported(const Plan& p);
-cudaError_t launch_backward_tc_expert_keys(const Plan& p, const Work& w, const __nv_bfloat16* Q,
-                                           const __nv_bfloat16* K, const __nv_bfloat16* V, const __nv_bfloat16* dO,
+// (Qg, dOg: Q and dO rows in grouped order, [BH][N][64] bf16)
+cudaError_t launch_backward_tc_expert_keys(const Plan& p, const Work& w, const __nv_bfloat16* Qg,
+                                           const __nv_bfloat16* K, const __nv_bfloat16* V, const __nv_bfloat16* dOg,
                                            const int32_t* expert_idx, const float* st_lse, const float* st_delta,
                                            float* dK, float* dV, float* dlq, float* dlv, cudaStream_t st);
 // dQ (written): the expert attention's share plus the pooling's share of
 // the complete dLq, so it runs after the landmark part
-cudaError_t launch_backward_tc_expert_rows(const Plan& p, const Work& w, const __nv_bfloat16* Q,
-                                           const __nv_bfloat16* K, const __nv_bfloat16* V, const __nv_bfloat16* dO,
+cudaError_t launch_backward_tc_expert_rows(const Plan& p, const Work& w, const __nv_bfloat16* Qg,
+                                           const __nv_bfloat16* K, const __nv_bfloat16* V, const __nv_bfloat16* dOg,
                                            const int32_t* expert_idx, const float* st_lse, const float* st_delta,
                                            const float* dlq, float* dQ, cudaStream_t st);
 cudaError_t launch_backward_tc_landmark(const Plan& p, const Work& w, const __nv_bfloat16* K, const __nv_bfloat16* V,
