@@ -440,7 +440,7 @@ int run_forward(const Plan& P, const Work& W, const __nv_bfloat16* Q, const __nv
     if (small_fused_applies(P)) {  // a short head: every stage in one kernel (timed as the expert stage)
         StageMarks marks(st);
         marks.mark(6);
-        if ((e = launch_small_fused(P, Q, K, V, out, expert_idx, route, lq_out, lv_out, st)) != cudaSuccess)
+        if ((e = launch_small_fused(P, Q, K, V, out, expert_idx, route, lq_out, lv_out, W.status, st)) != cudaSuccess)
             return cuda_fail(e, "fused short-head launch");
         marks.mark(7);
         const int launches[kStages] = {0, 0, 0, 0, 0, 0, 1};

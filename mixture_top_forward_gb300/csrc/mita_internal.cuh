@@ -260,7 +260,7 @@ cudaError_t launch_backward_tc_landmark(const Plan& p, const Work& w, const __nv
 bool small_fused_applies(const Plan& p);
 cudaError_t launch_small_fused(const Plan& p, const __nv_bfloat16* Q, const __nv_bfloat16* K, const __nv_bfloat16* V,
                                __nv_bfloat16* out, int32_t* expert_idx, int32_t* route, float* lq_out, float* lv_out,
-                               cudaStream_t st);
+                               int* status, cudaStream_t st);
 
 // Number of SMs of the current device (cached per device).
 int device_sms();
