@@ -65,6 +65,11 @@ def _rand(B, H, N, seed, scale=1.0):
     (1, 1, 1, 0, 0, 1, 1),          # a single token
     (1, 2, 5000, 0, 0, 300, 700),   # several landmark tiles, k > 512
     (3, 1, 2500, 50, 50, 16, 1024), # 2-D 4x4 landmarks, k = MITA_MAX_K
+    # heads short enough for the one-kernel-per-head pass (N <= 256, m <= 32)
+    (2, 2, 256, 0, 0, 32, 256),     # its largest N and m, k = N
+    (1, 3, 255, 0, 0, 32, 100),     # ragged key blocks and windows
+    (2, 1, 256, 16, 16, 16, 40),    # 2-D 16x16 grid onto 4x4 landmarks
+    (1, 2, 129, 0, 0, 3, 7),        # a second query tile of one row
 ])
 def test_edge_shapes(orc, B, H, N, gh, gw, m, k):
     q, kk_, v = _rand(B, H, N, 100 + N + m + k, 2.0)
