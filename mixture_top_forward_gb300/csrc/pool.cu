@@ -93,10 +93,82 @@ __global__ void __launch_bounds__(256) pool_kernel(const __nv_bfloat16* __restri
     }
 }
 
+// Small windows (at most 64 tokens): one warp per landmark, 8 CTAs' worth
+// of landmarks per CTA. Lanes 8s .. 8s + 7 cover one query row with 16-byte
+// loads (4 rows per step, all of a window's loads in flight), the 4 row
+// slots are summed by two shuffles in a fixed order.
+__global__ void __launch_bounds__(256) pool_warp_kernel(const __nv_bfloat16* __restrict__ Q, int64_t N, int gh, int gw,
+                                                        int p, int m, int64_t rows, float* __restrict__ lq32,
+                                                        __nv_bfloat16* __restrict__ lqhi,
+                                                        __nv_bfloat16* __restrict__ lqlo) {
+    const int lane = threadIdx.x & 31;
+    const int64_t wg = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+    if (wg >= rows) return;  // (warp-uniform; no block-wide barrier)
+    const int i = static_cast<int>(wg % m);
+    const int64_t bh = wg / m;
+    int64_t t0 = 0, cnt, y0 = 0, x0 = 0, wdt = 1;
+    if (p == 0) {
+        t0 = (static_cast<int64_t>(i) * N) / m;
+        cnt = (static_cast<int64_t>(i + 1) * N + m - 1) / m - t0;
+    } else {
+        const int r = i / p, c = i % p;
+        y0 = (static_cast<int64_t>(r) * gh) / p;
+        const int64_t y1 = (static_cast<int64_t>(r + 1) * gh + p - 1) / p;
+        x0 = (static_cast<int64_t>(c) * gw) / p;
+        wdt = (static_cast<int64_t>(c + 1) * gw + p - 1) / p - x0;
+        cnt = (y1 - y0) * wdt;
+    }
+    const __nv_bfloat16* Qh = Q + bh * N * D;
+    const int col = (lane & 7) * 8, slot = lane >> 3;
+    auto token = [&](int64_t t) -> int64_t { return p == 0 ? t0 + t : (y0 + t / wdt) * gw + x0 + t % wdt; };
+    float acc[8];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) acc[c] = 0.f;
+#pragma unroll 4
+    for (int64_t t = slot; t < cnt; t += 4) {
+        float f[8];
+        unpack_bf16x8(ldg_nc_v4(Qh + token(t) * D + col), f);
+#pragma unroll
+        for (int c = 0; c < 8; ++c) acc[c] += f[c];
+    }
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+        acc[c] += __shfl_xor_sync(0xffffffffu, acc[c], 8);
+        acc[c] += __shfl_xor_sync(0xffffffffu, acc[c], 16);
+    }
+    if (slot == 0) {
+        float v[8];
+        uint32_t hw[4], lw[4];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) v[c] = acc[c] / static_cast<float>(cnt);
+#pragma unroll
+        for (int c = 0; c < 8; c += 2) {
+            const __nv_bfloat162 h2 = __floats2bfloat162_rn(v[c], v[c + 1]);
+            const __nv_bfloat162 l2 = __floats2bfloat162_rn(v[c] - __low2float(h2), v[c + 1] - __high2float(h2));
+            hw[c >> 1] = *reinterpret_cast<const uint32_t*>(&h2);
+            lw[c >> 1] = *reinterpret_cast<const uint32_t*>(&l2);
+        }
+        const int64_t o = (bh * m + i) * D + col;
+        reinterpret_cast<float4*>(lq32 + o)[0] = make_float4(v[0], v[1], v[2], v[3]);
+        reinterpret_cast<float4*>(lq32 + o)[1] = make_float4(v[4], v[5], v[6], v[7]);
+        *reinterpret_cast<uint4*>(lqhi + o) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+        *reinterpret_cast<uint4*>(lqlo + o) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+    }
+}
+
 }  // namespace
 
 cudaError_t launch_pool(const Plan& p, const Work& w, const __nv_bfloat16* Q, cudaStream_t st) {
-    const unsigned grid = static_cast<unsigned>(p.s.BH * p.s.m);
+    // the largest window: 1-D ceil(N / m) + 1 tokens; 2-D (ceil(gh / p) + 1) (ceil(gw / p) + 1)
+    const int64_t win = p.s.p == 0 ? (p.s.N + p.s.m - 1) / p.s.m + 1
+                                   : ((p.s.gh + p.s.p - 1) / p.s.p + 1) * ((p.s.gw + p.s.p - 1) / p.s.p + 1);
+    const int64_t rows = p.s.BH * p.s.m;
+    if (win <= 64) {
+        pool_warp_kernel<<<static_cast<unsigned>((rows + 7) / 8), 256, 0, st>>>(Q, p.s.N, p.s.gh, p.s.gw, p.s.p, p.s.m,
+                                                                             rows, w.lq32, w.lqhi, w.lqlo);
+        return cudaGetLastError();
+    }
+    const unsigned grid = static_cast<unsigned>(rows);
     pool_kernel<<<grid, 256, 0, st>>>(Q, p.s.N, p.s.gh, p.s.gw, p.s.p, p.s.m, w.lq32, w.lqhi, w.lqlo);
     return cudaGetLastError();
 }
