@@ -93,8 +93,8 @@ __global__ void __launch_bounds__(256) pool_kernel(const __nv_bfloat16* __restri
     }
 }
 
-// Small windows (at most 64 tokens): one warp per landmark, 8 CTAs' worth
-// of landmarks per CTA. Lanes 8s .. 8s + 7 cover one query row with 16-byte
+// Small windows (at most 128 tokens): one warp per landmark, 8 landmarks
+// per CTA. Lanes 8s .. 8s + 7 cover one query row with 16-byte
 // loads (4 rows per step, all of a window's loads in flight), the 4 row
 // slots are summed by two shuffles in a fixed order.
 __global__ void __launch_bounds__(256) pool_warp_kernel(const __nv_bfloat16* __restrict__ Q, int64_t N, int gh, int gw,
@@ -159,11 +159,12 @@ __global__ void __launch_bounds__(256) pool_warp_kernel(const __nv_bfloat16* __r
 }  // namespace
 
 cudaError_t launch_pool(const Plan& p, const Work& w, const __nv_bfloat16* Q, cudaStream_t st) {
-    // the largest window: 1-D ceil(N / m) + 1 tokens; 2-D (ceil(gh / p) + 1) (ceil(gw / p) + 1)
+    // the largest window: 1-D ceil(N / m) + 1 tokens; 2-D (ceil(gh / p) + 1) (ceil(gw / p) + 1);
+    // long windows keep a whole CTA per landmark
     const int64_t win = p.s.p == 0 ? (p.s.N + p.s.m - 1) / p.s.m + 1
                                    : ((p.s.gh + p.s.p - 1) / p.s.p + 1) * ((p.s.gw + p.s.p - 1) / p.s.p + 1);
     const int64_t rows = p.s.BH * p.s.m;
-    if (win <= 64) {
+    if (win <= 128) {
         pool_warp_kernel<<<static_cast<unsigned>((rows + 7) / 8), 256, 0, st>>>(Q, p.s.N, p.s.gh, p.s.gw, p.s.p, p.s.m,
                                                                              rows, w.lq32, w.lqhi, w.lqlo);
         return cudaGetLastError();
