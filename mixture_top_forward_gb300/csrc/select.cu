@@ -394,17 +394,27 @@ __global__ void __launch_bounds__(DW * 32) dense_row_select_kernel(
     uint32_t t[C];
 #pragma unroll
     for (int c = 0; c < C; ++c) t[c] = 0u;
-    for (int e0 = 4 * lane; e0 < n; e0 += 128) {
-        const float4 v = __ldg(reinterpret_cast<const float4*>(src + e0));
-        const float f[4] = {v.x, v.y, v.z, v.w};
+    // eight 16-byte loads of the row in flight per lane, then their keys
+    for (int g0 = 0; g0 < n; g0 += 8 * 128) {
+        float4 v[8];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            uint32_t x = e0 + j < n ? score_key32(f[j]) : 0u;
+        for (int u = 0; u < 8; ++u) {
+            const int e0 = g0 + 128 * u + 4 * lane;
+            v[u] = e0 < n ? __ldg(reinterpret_cast<const float4*>(src + e0)) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
 #pragma unroll
-            for (int c = 0; c < C; ++c) {  // insert into t[0] >= t[1] >= ...
-                const uint32_t hi = max(t[c], x);
-                x = min(t[c], x);
-                t[c] = hi;
+        for (int u = 0; u < 8; ++u) {
+            const int e0 = g0 + 128 * u + 4 * lane;
+            const float f[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                uint32_t x = e0 + j < n ? score_key32(f[j]) : 0u;
+#pragma unroll
+                for (int c = 0; c < C; ++c) {  // insert into t[0] >= t[1] >= ...
+                    const uint32_t hi = max(t[c], x);
+                    x = min(t[c], x);
+                    t[c] = hi;
+                }
             }
         }
     }
