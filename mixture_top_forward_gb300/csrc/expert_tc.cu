@@ -306,6 +306,7 @@ __global__ void __launch_bounds__(NT, 1)
         // last gather stay zero (their logits are masked; their values must be
         // finite).
         const int rows = a.nblk * KB;
+        for (int x = lane; x < NWG * QB * 1024; x += 32) zero16(S.q + 16 * x);  // query buffers
         for (int w = 0; w < (IND ? NWG : 1); ++w)
             for (int x = ((nkeys + 3) & ~3) * 8 + lane; x < rows * 8; x += 32) {
                 zero16(S.keys + w * S.kvstride + swz128(x >> 3, x & 7));
@@ -349,15 +350,20 @@ __global__ void __launch_bounds__(NT, 1)
             const uint32_t qb = w * QB + (nq[w] % QB);
             if (nq[w] >= QB && !__all_sync(0xffffffffu, mbar_wait(&qfree[qb], ((nq[w] / QB) - 1) & 1, a.status)))
                 return false;
-            if (lane == 0) mbar_arrive_expect_tx(&qfull[qb], 16384u);
+            // lane l gathers query rows 4l..4l+3 while 4l < z (the last group
+            // repeats the item's last query); the groups after are not copied
+            // (a gather costs the issuing warp about a hundred cycles), so
+            // those rows keep an earlier item's queries or the initial zeros
+            const int ng = (it.z + 3) >> 2;
+            if (lane == 0) mbar_arrive_expect_tx(&qfull[qb], static_cast<uint32_t>(ng) * 512u);
             __syncwarp();
-            // lane l gathers query rows 4l..4l+3; rows past the item repeat its last query
             const int bh = it.w;
             const int* pp = a.perm + static_cast<int64_t>(bh) * a.N + it.y;
             const int last = it.z - 1, r0 = 4 * lane;
             const int y = bh * static_cast<int>(a.N);
-            tma_gather4(S.q + qb * 16384 + r0 * 128, &tq, 0, y + pp[min(r0, last)], y + pp[min(r0 + 1, last)],
-                        y + pp[min(r0 + 2, last)], y + pp[min(r0 + 3, last)], &qfull[qb]);
+            if (lane < ng)
+                tma_gather4(S.q + qb * 16384 + r0 * 128, &tq, 0, y + pp[min(r0, last)], y + pp[min(r0 + 1, last)],
+                            y + pp[min(r0 + 2, last)], y + pp[min(r0 + 3, last)], &qfull[qb]);
             ++nq[w];
             return true;
         };
