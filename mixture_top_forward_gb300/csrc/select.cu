@@ -419,34 +419,42 @@ __global__ void __launch_bounds__(DW * 32) dense_row_select_kernel(
         }
     }
     const uint32_t theta = __reduce_min_sync(0xffffffffu, t[C - 1]);
-    // survivors (keys >= theta) in index order
+    // survivors (keys >= theta) in index order; the second read of the row
+    // also keeps eight 16-byte loads per lane in flight
     const unsigned below = (1u << lane) - 1u;
     unsigned total = 0;
-    for (int b0 = 0; b0 < n; b0 += 128) {
-        const int e0 = b0 + 4 * lane;
-        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (e0 < n) v = __ldg(reinterpret_cast<const float4*>(src + e0));
-        const float f[4] = {v.x, v.y, v.z, v.w};
-        uint32_t x[4];
-        unsigned bl[4], before = 0;
+    for (int g0 = 0; g0 < n; g0 += 8 * 128) {
+        float4 vv[8];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            x[j] = e0 + j < n ? score_key32(f[j]) : 0u;
-            bl[j] = __ballot_sync(0xffffffffu, e0 + j < n && x[j] >= theta);
-            before += __popc(bl[j] & below);
+        for (int u = 0; u < 8; ++u) {
+            const int e0 = g0 + 128 * u + 4 * lane;
+            vv[u] = e0 < n ? __ldg(reinterpret_cast<const float4*>(src + e0)) : make_float4(0.f, 0.f, 0.f, 0.f);
         }
-        unsigned pos = total + before;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            if ((bl[j] >> lane) & 1u) {
-                if (pos < kSurv) {
-                    s_key[wid][pos] = x[j];
-                    s_idx[wid][pos] = e0 + j;
-                }
-                ++pos;
+        for (int u = 0; u < 8; ++u) {
+            const int e0 = g0 + 128 * u + 4 * lane;
+            const float f[4] = {vv[u].x, vv[u].y, vv[u].z, vv[u].w};
+            uint32_t x[4];
+            unsigned bl[4], before = 0;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                x[j] = e0 + j < n ? score_key32(f[j]) : 0u;
+                bl[j] = __ballot_sync(0xffffffffu, e0 + j < n && x[j] >= theta);
+                before += __popc(bl[j] & below);
             }
+            unsigned pos = total + before;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                if ((bl[j] >> lane) & 1u) {
+                    if (pos < kSurv) {
+                        s_key[wid][pos] = x[j];
+                        s_idx[wid][pos] = e0 + j;
+                    }
+                    ++pos;
+                }
+            }
+            total += __popc(bl[0]) + __popc(bl[1]) + __popc(bl[2]) + __popc(bl[3]);
         }
-        total += __popc(bl[0]) + __popc(bl[1]) + __popc(bl[2]) + __popc(bl[3]);
     }
     __syncwarp();
     int32_t* dst = expert_idx + row * static_cast<int64_t>(k);
