@@ -281,12 +281,16 @@ __global__ void __launch_bounds__(NT, 1)
             mbar_init(&sfree[w], 4);
         }
         for (int b = 0; b < NWG * QB; ++b) {
-            mbar_init(&qfull[b], 1);
+            mbar_init(&qfull[b], IND ? 4 : 1);  // IND: the warpgroup's 4 row warps load the rows
             mbar_init(&qfree[b], 1);
         }
         mbar_init(&drain, NWG);  // exit path: one commit per MMA issuer
         fence_barrier_init();
     }
+    // query buffers zeroed before anything copies into them: an item's rows
+    // past its last query keep an earlier item's queries or these zeros
+    for (int x = tid; x < NWG * QB * 1024; x += NT) zero16(S.q + 16 * x);
+    fence_proxy_async();
     if (warp == 0) tmem_alloc(&tmem_base, 512);
     tc_fence_before();
     __syncthreads();
@@ -306,7 +310,6 @@ __global__ void __launch_bounds__(NT, 1)
         // last gather stay zero (their logits are masked; their values must be
         // finite).
         const int rows = a.nblk * KB;
-        for (int x = lane; x < NWG * QB * 1024; x += 32) zero16(S.q + 16 * x);  // query buffers
         for (int w = 0; w < (IND ? NWG : 1); ++w)
             for (int x = ((nkeys + 3) & ~3) * 8 + lane; x < rows * 8; x += 32) {
                 zero16(S.keys + w * S.kvstride + swz128(x >> 3, x & 7));
@@ -390,7 +393,7 @@ __global__ void __launch_bounds__(NT, 1)
                         cur_e[w] = it.x;
                         ++changes[w];
                     }
-                    ok = gather_q(it, w);
+                    // (the query rows: the warpgroup's row warps, below)
                 }
             }
         } else {
@@ -597,8 +600,46 @@ __global__ void __launch_bounds__(NT, 1)
             }
             pend = false;
         };
-        // IND: this warpgroup's own range, one item per round
+        // IND: this warpgroup's own range, one item per round. Its row warps
+        // load the query rows themselves (the producer's TMA gathers are the
+        // bottleneck of short lists, and these warps are mostly waiting):
+        // each warp its 32 rows of the next item, lanes 0-7 one 4-row gather
+        // each, during the current item's first block; the first item's at
+        // the start.
         const int re = IND ? j0(w + 1) : i1;
+        uint32_t qseq = 0;                    // IND: items of this warpgroup so far
+        int qarm_b = -1;                      // IND: the last query buffer this warp armed
+        uint32_t qarm_par = 0;
+        const int qg = 8 * (warp & 3) + lane;  // IND: this lane's 4-row group of an item (lanes 0-7)
+        // IND: the sources of this lane's group of item x (rows past z repeat its last query)
+        auto q_src = [&](const int4& x, int* pq) {
+            const int* pp = a.perm + static_cast<int64_t>(x.w) * a.N + x.y;
+            const int last = x.z - 1, r0 = 4 * qg, y = x.w * static_cast<int>(a.N);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) pq[i] = (lane < 8 && r0 < x.z) ? y + pp[min(r0 + i, last)] : 0;
+        };
+        // IND: item number u of this warpgroup (z queries, rows from pq) into its query buffer
+        auto q_load = [&](int z, uint32_t u, const int* pq) -> bool {
+            const uint32_t qb = w * QB + u % QB;
+            // the buffer's previous item (u - QB) must be done with it (its S products)
+            if (u >= QB && !__all_sync(0xffffffffu, mbar_wait(&qfree[qb], ((u / QB) - 1) & 1, a.status)))
+                return false;
+            const int ng = min(8, max(0, (z - 32 * (warp & 3) + 3) >> 2));  // this warp's groups
+            if (lane == 0) mbar_arrive_expect_tx(&qfull[qb], static_cast<uint32_t>(ng) * 512u);
+            __syncwarp();
+            if (lane < ng) tma_gather4(S.q + qb * 16384 + qg * 512, &tq, 0, pq[0], pq[1], pq[2], pq[3], &qfull[qb]);
+            qarm_b = static_cast<int>(qb);
+            qarm_par = (u / QB) & 1;
+            return true;
+        };
+        if constexpr (IND) {
+            if (j0(w) < re) {
+                const int4 x = a.items[j0(w)];
+                int pq[4];
+                q_src(x, pq);
+                ok = q_load(x.z, 0, pq);
+            }
+        }
         for (int r = IND ? j0(w) : i0; r < re && ok;) {
             int4 x0, x1, x2;
             const int cnt = round_items(a, r, re, x0, x1, x2, IND);
@@ -607,6 +648,8 @@ __global__ void __launch_bounds__(NT, 1)
             const int4 item = IND ? x0 : pick(w, x0, x1, x2);
             const int64_t bh = item.w;
             const int n = t < item.z ? a.perm[bh * a.N + item.y + t] : 0;
+            // IND: the next item's query rows load after this item's first block
+            const bool qnext = IND && r < re;
             // SPLIT: the shared branch as one pre-merged pair (logit lse, weight 1);
             // its output row comes in now, and is read in the first block
             float mrun = -INFINITY, lrun = 0.f;
@@ -719,6 +762,12 @@ __global__ void __launch_bounds__(NT, 1)
                 tc_fence_before();
                 warp_arrive(&pfull[w]);
                 if (pend) epilogue();  // the previous item's O is final (its last P.V is done)
+                if (qnext && j == 0) {
+                    const int4 xn = a.items[r];
+                    int pqn[4];
+                    q_src(xn, pqn);
+                    if (!(ok = q_load(xn.z, qseq + 1, pqn))) break;
+                }
                 if (SPLIT && j == 0) {
                     // O := alpha o_n (the shared output at this block's running
                     // max), before this item's first P.V adds to it; each thread
@@ -730,6 +779,7 @@ __global__ void __launch_bounds__(NT, 1)
                 mrun = mnew;
             }
             if (!ok) break;
+            ++qseq;
             pend = true;
             pend_row = t < item.z;
             pend_inv = 1.f / lrun;
@@ -747,6 +797,9 @@ __global__ void __launch_bounds__(NT, 1)
                 epilogue();
             }
         }
+        // IND exit: this warp's last query copies have landed (on the normal
+        // path the issuer has waited for them already)
+        if (IND && qarm_b >= 0 && lane == 0) mbar_drain(&qfull[qarm_b], qarm_par);
     }
     tc_fence_before();
     __syncthreads();
