@@ -167,7 +167,9 @@ __device__ __forceinline__ int next_item(const Args& a, int w, int& r, int i1, i
         int4 x0, x1, x2;
         const int cnt = round_items(a, r, i1, x0, x1, x2, one);
         if (x0.w != cur_bh || x0.x != cur_e) {
-            if (changes > 0) umma::mma_commit(kvfree);
+            // (IND: the row warps load the next list once they see the last
+            // P.V of the current one done; nothing waits for a release)
+            if (changes > 0 && !one) umma::mma_commit(kvfree);
             if (!umma::mbar_wait(kvfull, changes & 1, a.status)) return -1;
             umma::tc_fence_after();
             cur_bh = x0.w;
@@ -270,7 +272,7 @@ __global__ void __launch_bounds__(NT, 1)
 
     if (tid == 0) {
         for (int w = 0; w < NWG; ++w) {
-            mbar_init(&kvfull[w], 1);
+            mbar_init(&kvfull[w], IND ? 4 : 1);  // IND: the warpgroup's 4 row warps load the list
             mbar_init(&kvfree[w], IND ? 1 : NWG);  // shared lists: one commit per MMA issuer
         }
         for (int w = 0; w < NWG; ++w) {
@@ -290,6 +292,13 @@ __global__ void __launch_bounds__(NT, 1)
     // query buffers zeroed before anything copies into them: an item's rows
     // past its last query keep an earlier item's queries or these zeros
     for (int x = tid; x < NWG * QB * 1024; x += NT) zero16(S.q + 16 * x);
+    // likewise the list rows past the last gather: zero (their logits are
+    // masked; their values must be finite)
+    for (int w = 0; w < (IND ? NWG : 1); ++w)
+        for (int x = ((nkeys + 3) & ~3) * 8 + tid; x < a.nblk * KB * 8; x += NT) {
+            zero16(S.keys + w * S.kvstride + swz128(x >> 3, x & 7));
+            zero16(S.vals + w * S.kvstride + swz128(x >> 3, x & 7));
+        }
     fence_proxy_async();
     if (warp == 0) tmem_alloc(&tmem_base, 512);
     tc_fence_before();
@@ -309,14 +318,6 @@ __global__ void __launch_bounds__(NT, 1)
         // mbarrier: the producer never waits for its own copies. Rows past the
         // last gather stay zero (their logits are masked; their values must be
         // finite).
-        const int rows = a.nblk * KB;
-        for (int w = 0; w < (IND ? NWG : 1); ++w)
-            for (int x = ((nkeys + 3) & ~3) * 8 + lane; x < rows * 8; x += 32) {
-                zero16(S.keys + w * S.kvstride + swz128(x >> 3, x & 7));
-                zero16(S.vals + w * S.kvstride + swz128(x >> 3, x & 7));
-            }
-        fence_proxy_async();
-        __syncwarp();
         // the key/value list of item `it` into list copy w (the shared rows
         // only when the copy held another head's list)
         auto gather_list = [&](const int4& it, int w, bool new_head) {
@@ -374,28 +375,7 @@ __global__ void __launch_bounds__(NT, 1)
         int cur_e[NWG] = {-1, -1, -1}, changes[NWG] = {0, 0, 0};
         bool ok = true;
         if constexpr (IND) {
-            // the warpgroups' ranges, one item of each in turn
-            int pos[NWG];
-            for (int w = 0; w < NWG; ++w) pos[w] = j0(w);
-            for (bool more = true; more && ok;) {
-                more = false;
-                for (int w = 0; w < NWG && ok; ++w) {
-                    if (pos[w] >= j0(w + 1)) continue;
-                    more = true;
-                    const int4 it = a.items[pos[w]++];
-                    if (it.w != cur_bh[w] || it.x != cur_e[w]) {
-                        // wait until this warpgroup's MMAs on its previous list are done
-                        if (changes[w] > 0)
-                            ok = __all_sync(0xffffffffu, mbar_wait(&kvfree[w], (changes[w] - 1) & 1, a.status));
-                        if (!ok) break;
-                        gather_list(it, w, it.w != cur_bh[w]);
-                        cur_bh[w] = it.w;
-                        cur_e[w] = it.x;
-                        ++changes[w];
-                    }
-                    // (the query rows: the warpgroup's row warps, below)
-                }
-            }
+            // (the warpgroups' row warps load their own key lists and query rows)
         } else {
             for (int r = i0; r < i1 && ok;) {
                 int4 it[NWG];
@@ -632,9 +612,45 @@ __global__ void __launch_bounds__(NT, 1)
             qarm_par = (u / QB) & 1;
             return true;
         };
+        // IND: the key/value list of item x into the warpgroup's list (the
+        // head's shared rows too when new_head): its 4-row gathers, keys and
+        // values, spread over the 4 warps (op o: warp o mod 4, lane o / 4);
+        // each warp arrives once on kvfull with its own bytes
+        int karms = 0;  // IND: lists armed by this warp
+        auto l_load = [&](const int4& x, bool new_head) {
+            uint8_t* keys = S.keys + w * S.kvstride;
+            uint8_t* vals = S.vals + w * S.kvstride;
+            const int32_t* sel = a.expert_idx + (static_cast<int64_t>(x.w) * a.m + x.x) * a.k;
+            const int ns = new_head ? m4 / 4 : 0, nr = (a.k + 3) / 4, nops = 2 * (ns + nr);
+            const int wq = warp & 3;
+            const int mine = nops > wq ? (nops - wq + 3) / 4 : 0;  // ops o = wq + 4 i
+            if (lane == 0) mbar_arrive_expect_tx(&kvfull[w], static_cast<uint32_t>(mine) * 512u);
+            __syncwarp();
+            for (int o = wq + 4 * lane; o < nops; o += 128) {
+                const int g = o >> 1;
+                const bool isv = o & 1;
+                if (g < ns) {  // shared rows 4g..4g+3 (the last ones repeat row m-1)
+                    const int y = x.w * a.m, r0 = 4 * g;
+                    tma_gather4((isv ? vals : keys) + r0 * 128, isv ? &tlv : &tlq, 0, y + min(r0, a.m - 1),
+                                y + min(r0 + 1, a.m - 1), y + min(r0 + 2, a.m - 1), y + min(r0 + 3, a.m - 1),
+                                &kvfull[w]);
+                } else {  // routed rows m4 + 4(g - ns).. (the last ones repeat key k-1)
+                    const int r0 = 4 * (g - ns), y = x.w * static_cast<int>(a.N);
+                    tma_gather4((isv ? vals : keys) + (m4 + r0) * 128, isv ? &tv : &tk, 0,
+                                y + sel[min(r0, a.k - 1)], y + sel[min(r0 + 1, a.k - 1)],
+                                y + sel[min(r0 + 2, a.k - 1)], y + sel[min(r0 + 3, a.k - 1)], &kvfull[w]);
+                }
+            }
+            ++karms;
+        };
+        int64_t lbh = -1;  // IND: the head and expert of the list this warpgroup holds
+        int le = -1;
         if constexpr (IND) {
             if (j0(w) < re) {
                 const int4 x = a.items[j0(w)];
+                l_load(x, true);
+                lbh = x.w;
+                le = x.x;
                 int pq[4];
                 q_src(x, pq);
                 ok = q_load(x.z, 0, pq);
@@ -779,6 +795,19 @@ __global__ void __launch_bounds__(NT, 1)
                 mrun = mnew;
             }
             if (!ok) break;
+            if (qnext) {
+                // IND: the next item's list, once this item's last P.V (and
+                // with it every product reading the list) is done
+                const int4 xn = a.items[r];
+                if (xn.w != lbh || xn.x != le) {
+                    ok = __all_sync(0xffffffffu, mbar_wait(&pvdone[w], (gb - 1) & 1, a.status));
+                    if (!ok) break;
+                    tc_fence_after();
+                    l_load(xn, xn.w != lbh);
+                    lbh = xn.w;
+                    le = xn.x;
+                }
+            }
             ++qseq;
             pend = true;
             pend_row = t < item.z;
@@ -800,6 +829,7 @@ __global__ void __launch_bounds__(NT, 1)
         // IND exit: this warp's last query copies have landed (on the normal
         // path the issuer has waited for them already)
         if (IND && qarm_b >= 0 && lane == 0) mbar_drain(&qfull[qarm_b], qarm_par);
+        if (IND && karms > 0 && lane == 0) mbar_drain(&kvfull[w], (karms - 1) & 1);
     }
     tc_fence_before();
     __syncthreads();
