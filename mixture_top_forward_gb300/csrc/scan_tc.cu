@@ -78,8 +78,9 @@ template <bool FULL, int NL>
 struct Cfg {
     static constexpr int KT = 64;                     // keys per tile
     static constexpr int TB = KT * 128;               // bytes of one K or V tile
-    static constexpr int KST = 6;                     // K ring stages
-    static constexpr int VST = FULL ? 4 : 0;          // V ring stages
+    static constexpr int KST = NL == 1 ? 4 : 6;       // K ring stages
+    static constexpr int VST = FULL ? (NL == 1 ? 3 : 4) : 0;  // V ring stages
+    static constexpr int MINB = NL == 1 ? 2 : 1;      // CTAs per SM
     static constexpr int NT = 32 * (NL + 2) + NL * 128;  // producer, NL S issuers, P.V issuer, rows
     static constexpr int ROW0 = NL + 2;                  // first row warp
     static constexpr size_t OFF_LQLO = NL * 16384;
@@ -124,7 +125,7 @@ __device__ __forceinline__ bool issue_pv(const ScanArgs& a, uint8_t* base, uint3
 }
 
 template <bool FULL, int NL>
-__global__ void __launch_bounds__(Cfg<FULL, NL>::NT, 1)
+__global__ void __launch_bounds__(Cfg<FULL, NL>::NT, Cfg<FULL, NL>::MINB)
     scan_tc_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv, ScanArgs a) {
     using C = Cfg<FULL, NL>;
     constexpr int KT = C::KT;

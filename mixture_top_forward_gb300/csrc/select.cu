@@ -391,34 +391,45 @@ __global__ void __launch_bounds__(DW * 32) dense_row_select_kernel(
 
     // ---- routed expert: the k best of the row ----
     const float* src = dense + row * ld;  // ld is a multiple of 4: float4 rows
-    uint32_t t[C];
+    // The per-lane top C runs on the raw logits: tau = 1/8 is exact and the
+    // order key is monotone in the float (with -0 = +0, as a float compare
+    // has it), so comparing raw values orders them as their keys do, and
+    // only the survivors need their keys.
+    float t[C];
 #pragma unroll
-    for (int c = 0; c < C; ++c) t[c] = 0u;
-    // eight 16-byte loads of the row in flight per lane, then their keys
+    for (int c = 0; c < C; ++c) t[c] = -INFINITY;
+    // eight 16-byte loads of the row in flight per lane
     for (int g0 = 0; g0 < n; g0 += 8 * 128) {
         float4 v[8];
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
             const int e0 = g0 + 128 * u + 4 * lane;
-            v[u] = e0 < n ? __ldg(reinterpret_cast<const float4*>(src + e0)) : make_float4(0.f, 0.f, 0.f, 0.f);
+            v[u] = e0 < n ? __ldg(reinterpret_cast<const float4*>(src + e0))
+                          : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
         }
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
-            const int e0 = g0 + 128 * u + 4 * lane;
             const float f[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                uint32_t x = e0 + j < n ? score_key32(f[j]) : 0u;
+                float x = f[j];  // (past the row: -inf, below every logit)
 #pragma unroll
                 for (int c = 0; c < C; ++c) {  // insert into t[0] >= t[1] >= ...
-                    const uint32_t hi = max(t[c], x);
-                    x = min(t[c], x);
+                    const float hi = fmaxf(t[c], x);
+                    x = fminf(t[c], x);
                     t[c] = hi;
                 }
             }
         }
     }
-    const uint32_t theta = __reduce_min_sync(0xffffffffu, t[C - 1]);
+    // theta: the smallest of the lanes' C-th largest keys, and the raw logit
+    // it stands for (-inf when a lane holds fewer than C logits)
+    const uint32_t theta = __reduce_min_sync(0xffffffffu, t[C - 1] == -INFINITY ? 0u : score_key32(t[C - 1]));
+    float thr_raw = -INFINITY;
+    if (theta != 0u) {
+        const uint32_t u = theta;
+        thr_raw = __uint_as_float((u & 0x80000000u) ? (u & 0x7FFFFFFFu) : ~u) * 8.0f;
+    }
     // survivors (keys >= theta) in index order; the second read of the row
     // also keeps eight 16-byte loads per lane in flight
     const unsigned below = (1u << lane) - 1u;
@@ -434,12 +445,10 @@ __global__ void __launch_bounds__(DW * 32) dense_row_select_kernel(
         for (int u = 0; u < 8; ++u) {
             const int e0 = g0 + 128 * u + 4 * lane;
             const float f[4] = {vv[u].x, vv[u].y, vv[u].z, vv[u].w};
-            uint32_t x[4];
             unsigned bl[4], before = 0;
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                x[j] = e0 + j < n ? score_key32(f[j]) : 0u;
-                bl[j] = __ballot_sync(0xffffffffu, e0 + j < n && x[j] >= theta);
+                bl[j] = __ballot_sync(0xffffffffu, e0 + j < n && f[j] >= thr_raw);
                 before += __popc(bl[j] & below);
             }
             unsigned pos = total + before;
@@ -447,7 +456,7 @@ __global__ void __launch_bounds__(DW * 32) dense_row_select_kernel(
             for (int j = 0; j < 4; ++j) {
                 if ((bl[j] >> lane) & 1u) {
                     if (pos < kSurv) {
-                        s_key[wid][pos] = x[j];
+                        s_key[wid][pos] = score_key32(f[j]);
                         s_idx[wid][pos] = e0 + j;
                     }
                     ++pos;
