@@ -124,8 +124,21 @@ __global__ void __launch_bounds__(256) pool_warp_kernel(const __nv_bfloat16* __r
     float acc[8];
 #pragma unroll
     for (int c = 0; c < 8; ++c) acc[c] = 0.f;
-#pragma unroll 4
-    for (int64_t t = slot; t < cnt; t += 4) {
+    // eight 16-byte loads per lane in flight (a 64-token window: two rounds)
+    int64_t t = slot;
+    for (; t + 28 < cnt; t += 32) {
+        uint4 raw[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) raw[u] = ldg_nc_v4(Qh + token(t + 4 * u) * D + col);
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            float f[8];
+            unpack_bf16x8(raw[u], f);
+#pragma unroll
+            for (int c = 0; c < 8; ++c) acc[c] += f[c];
+        }
+    }
+    for (; t < cnt; t += 4) {
         float f[8];
         unpack_bf16x8(ldg_nc_v4(Qh + token(t) * D + col), f);
 #pragma unroll
