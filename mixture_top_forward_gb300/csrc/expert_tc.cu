@@ -17,7 +17,11 @@
 //                   changes (the shared rows only when the head changes) and
 //                   each item's query rows (through the grouping permutation)
 //                   into the warpgroup's next query buffer, all with TMA 4-row
-//                   gathers that complete on the consumer's mbarrier;
+//                   gathers that complete on the consumer's mbarrier. A gather
+//                   costs its issuing warp about a hundred cycles, so where
+//                   lists change often the row warps, idle at a list change,
+//                   load the lists instead (RL: all 12; IND: each warpgroup its
+//                   own list and query rows), and the producer keeps the rest;
 //   warps 1-3 (lane 0): one MMA issuer per warpgroup: per 64-key block j of
 //                   its item, S = Q keys_j^T (A and B in shared memory) into
 //                   the warpgroup's TMEM score columns, and one block later
@@ -250,7 +254,9 @@ static __device__ __noinline__ float stats_delta(uint32_t tO, const __nv_bfloat1
 // contiguous third of the CTA's items with a key/value list of its own, so
 // experts of one item each (short sequences, ViT shapes) run three at a time
 // instead of one per round.
-template <int MODE, bool IND>
+// RL (long lists, few items per expert): the row warps load the CTA's key
+// lists instead of the producer, spread over all of them.
+template <int MODE, bool IND, bool RL = false>
 __global__ void __launch_bounds__(NT, 1)
     expert_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                      const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tlq,
@@ -260,6 +266,9 @@ __global__ void __launch_bounds__(NT, 1)
     __shared__ uint64_t kvfull[NWG], kvfree[NWG], qfull[NWG * QB], qfree[NWG * QB], ofree[NWG];
     __shared__ uint64_t sfull[NWG], sfree[NWG], pfull[NWG], pvdone[NWG], drain;
     __shared__ uint32_t tmem_base;
+    // per row warp: the head and expert of the key list held, lists armed
+    // (read only between items: kept out of the registers of the block loop)
+    __shared__ int s_list[4 * NWG][3];
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const Layout S = layout(base, a.nblk, IND);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -272,7 +281,9 @@ __global__ void __launch_bounds__(NT, 1)
 
     if (tid == 0) {
         for (int w = 0; w < NWG; ++w) {
-            mbar_init(&kvfull[w], IND ? 4 : 1);  // IND: the warpgroup's 4 row warps load the list
+            // the producer loads the lists (one arrival), or the row warps do
+            // (IND: the warpgroup's 4, RL: all of them)
+            mbar_init(&kvfull[w], IND ? 4 : (RL ? 4 * NWG : 1));
             mbar_init(&kvfree[w], IND ? 1 : NWG);  // shared lists: one commit per MMA issuer
         }
         for (int w = 0; w < NWG; ++w) {
@@ -371,24 +382,24 @@ __global__ void __launch_bounds__(NT, 1)
             ++nq[w];
             return true;
         };
-        int64_t cur_bh[NWG] = {-1, -1, -1};
-        int cur_e[NWG] = {-1, -1, -1}, changes[NWG] = {0, 0, 0};
         bool ok = true;
-        if constexpr (IND) {
-            // (the warpgroups' row warps load their own key lists and query rows)
-        } else {
+        // (IND: the row warps load the key lists and their query rows; RL: the
+        // key lists)
+        int64_t cur_bh = -1;
+        int cur_e = -1, changes = 0;
+        if constexpr (!IND) {
             for (int r = i0; r < i1 && ok;) {
                 int4 it[NWG];
                 const int cnt = round_items(a, r, i1, it[0], it[1], it[2]);
-                if (it[0].w != cur_bh[0] || it[0].x != cur_e[0]) {
+                if (!RL && (it[0].w != cur_bh || it[0].x != cur_e)) {
                     // wait until the MMAs reading the previous lists are done
-                    if (changes[0] > 0)
-                        ok = __all_sync(0xffffffffu, mbar_wait(&kvfree[0], (changes[0] - 1) & 1, a.status));
+                    if (changes > 0)
+                        ok = __all_sync(0xffffffffu, mbar_wait(&kvfree[0], (changes - 1) & 1, a.status));
                     if (!ok) break;
-                    gather_list(it[0], 0, it[0].w != cur_bh[0]);
-                    cur_bh[0] = it[0].w;
-                    cur_e[0] = it[0].x;
-                    ++changes[0];
+                    gather_list(it[0], 0, it[0].w != cur_bh);
+                    cur_bh = it[0].w;
+                    cur_e = it[0].x;
+                    ++changes;
                 }
 #pragma unroll
                 for (int w = 0; w < NWG; ++w) {
@@ -400,8 +411,8 @@ __global__ void __launch_bounds__(NT, 1)
         }
         // exit: the last phase of every barrier this warp armed has landed
         if (lane == 0) {
+            if (changes > 0) mbar_drain(&kvfull[0], (changes - 1) & 1);
             for (int w = 0; w < NWG; ++w) {
-                if (changes[w] > 0) mbar_drain(&kvfull[w], (changes[w] - 1) & 1);
                 for (uint32_t b = 0; b < QB; ++b) {
                     const uint32_t arms = nq[w] > b ? (nq[w] - b + QB - 1) / QB : 0;
                     if (arms > 0) mbar_drain(&qfull[w * QB + b], (arms - 1) & 1);
@@ -612,45 +623,60 @@ __global__ void __launch_bounds__(NT, 1)
             qarm_par = (u / QB) & 1;
             return true;
         };
-        // IND: the key/value list of item x into the warpgroup's list (the
-        // head's shared rows too when new_head): its 4-row gathers, keys and
-        // values, spread over the 4 warps (op o: warp o mod 4, lane o / 4);
-        // each warp arrives once on kvfull with its own bytes
-        int karms = 0;  // IND: lists armed by this warp
+        // The key/value list of item x (the head's shared rows too when
+        // new_head) into the warpgroup's list (IND) or the CTA's: its 4-row
+        // gathers, keys and values, spread over the warpgroup's 4 row warps
+        // (IND) or all 4 NWG of them (op o: row warp o mod nw, lane o / nw);
+        // each warp arrives once on kvfull with its own bytes. A TMA gather
+        // costs its issuing warp about a hundred cycles, so one warp alone
+        // would take ~10K cycles per list at k = 256.
+        constexpr int NWL = IND ? 4 : 4 * NWG;  // warps sharing a list's gathers
+        int* ls = s_list[warp - 1 - NWG];        // [0] head, [1] expert of the list held, [2] lists armed
+        if (lane == 0) {
+            ls[0] = -1;
+            ls[1] = -1;
+            ls[2] = 0;
+        }
+        __syncwarp();
         auto l_load = [&](const int4& x, bool new_head) {
-            uint8_t* keys = S.keys + w * S.kvstride;
-            uint8_t* vals = S.vals + w * S.kvstride;
+            const int wl = IND ? (warp & 3) : (warp - 1 - NWG);
+            uint64_t* kvf = &kvfull[IND ? w : 0];
+            uint8_t* keys = S.keys + (IND ? w * S.kvstride : 0);
+            uint8_t* vals = S.vals + (IND ? w * S.kvstride : 0);
             const int32_t* sel = a.expert_idx + (static_cast<int64_t>(x.w) * a.m + x.x) * a.k;
             const int ns = new_head ? m4 / 4 : 0, nr = (a.k + 3) / 4, nops = 2 * (ns + nr);
-            const int wq = warp & 3;
-            const int mine = nops > wq ? (nops - wq + 3) / 4 : 0;  // ops o = wq + 4 i
-            if (lane == 0) mbar_arrive_expect_tx(&kvfull[w], static_cast<uint32_t>(mine) * 512u);
+            const int mine = nops > wl ? (nops - wl + NWL - 1) / NWL : 0;  // ops o = wl + NWL i
+            if (lane == 0) mbar_arrive_expect_tx(kvf, static_cast<uint32_t>(mine) * 512u);
             __syncwarp();
-            for (int o = wq + 4 * lane; o < nops; o += 128) {
+            for (int o = wl + NWL * lane; o < nops; o += 32 * NWL) {
                 const int g = o >> 1;
                 const bool isv = o & 1;
                 if (g < ns) {  // shared rows 4g..4g+3 (the last ones repeat row m-1)
                     const int y = x.w * a.m, r0 = 4 * g;
                     tma_gather4((isv ? vals : keys) + r0 * 128, isv ? &tlv : &tlq, 0, y + min(r0, a.m - 1),
-                                y + min(r0 + 1, a.m - 1), y + min(r0 + 2, a.m - 1), y + min(r0 + 3, a.m - 1),
-                                &kvfull[w]);
+                                y + min(r0 + 1, a.m - 1), y + min(r0 + 2, a.m - 1), y + min(r0 + 3, a.m - 1), kvf);
                 } else {  // routed rows m4 + 4(g - ns).. (the last ones repeat key k-1)
                     const int r0 = 4 * (g - ns), y = x.w * static_cast<int>(a.N);
                     tma_gather4((isv ? vals : keys) + (m4 + r0) * 128, isv ? &tv : &tk, 0,
                                 y + sel[min(r0, a.k - 1)], y + sel[min(r0 + 1, a.k - 1)],
-                                y + sel[min(r0 + 2, a.k - 1)], y + sel[min(r0 + 3, a.k - 1)], &kvfull[w]);
+                                y + sel[min(r0 + 2, a.k - 1)], y + sel[min(r0 + 3, a.k - 1)], kvf);
                 }
             }
-            ++karms;
+            __syncwarp();
+            if (lane == 0) {
+                ls[0] = x.w;
+                ls[1] = x.x;
+                ++ls[2];
+            }
+            __syncwarp();
         };
-        int64_t lbh = -1;  // IND: the head and expert of the list this warpgroup holds
-        int le = -1;
+        if constexpr (RL && !IND) {
+            if (i0 < i1) l_load(a.items[i0], true);  // the first list (every row warp of the CTA)
+        }
         if constexpr (IND) {
             if (j0(w) < re) {
                 const int4 x = a.items[j0(w)];
                 l_load(x, true);
-                lbh = x.w;
-                le = x.x;
                 int pq[4];
                 q_src(x, pq);
                 ok = q_load(x.z, 0, pq);
@@ -660,6 +686,15 @@ __global__ void __launch_bounds__(NT, 1)
             int4 x0, x1, x2;
             const int cnt = round_items(a, r, re, x0, x1, x2, IND);
             r += cnt;
+            if constexpr (RL && !IND) {
+                // a new list: once every MMA issuer has released the old one
+                // (its products are done), every row warp loads its share
+                if (x0.w != ls[0] || x0.x != ls[1]) {
+                    ok = __all_sync(0xffffffffu, mbar_wait(&kvfree[0], (ls[2] - 1) & 1, a.status));
+                    if (!ok) break;
+                    l_load(x0, x0.w != ls[0]);
+                }
+            }
             if (!IND && w >= cnt) continue;
             const int4 item = IND ? x0 : pick(w, x0, x1, x2);
             const int64_t bh = item.w;
@@ -799,13 +834,11 @@ __global__ void __launch_bounds__(NT, 1)
                 // IND: the next item's list, once this item's last P.V (and
                 // with it every product reading the list) is done
                 const int4 xn = a.items[r];
-                if (xn.w != lbh || xn.x != le) {
+                if (xn.w != ls[0] || xn.x != ls[1]) {
                     ok = __all_sync(0xffffffffu, mbar_wait(&pvdone[w], (gb - 1) & 1, a.status));
                     if (!ok) break;
                     tc_fence_after();
-                    l_load(xn, xn.w != lbh);
-                    lbh = xn.w;
-                    le = xn.x;
+                    l_load(xn, xn.w != ls[0]);
                 }
             }
             ++qseq;
@@ -829,7 +862,7 @@ __global__ void __launch_bounds__(NT, 1)
         // IND exit: this warp's last query copies have landed (on the normal
         // path the issuer has waited for them already)
         if (IND && qarm_b >= 0 && lane == 0) mbar_drain(&qfull[qarm_b], qarm_par);
-        if (IND && karms > 0 && lane == 0) mbar_drain(&kvfull[w], (karms - 1) & 1);
+        if ((IND || RL) && ls[2] > 0 && lane == 0) mbar_drain(&kvfull[IND ? w : 0], (ls[2] - 1) & 1);
     }
     tc_fence_before();
     __syncthreads();
@@ -892,9 +925,13 @@ cudaError_t launch_expert_tc(const Plan& p, const Work& w, const __nv_bfloat16* 
     // short lists (the ViT shapes, short sequences): a list per warpgroup
     const bool ind = !multi && !p.split && smem_bytes(a.nblk, false, true) <= 232448;
     const size_t smi = ind ? smem_bytes(a.nblk, false, true) : sm;
+    // the row warps load the key lists when an expert owns few items (its
+    // list is reloaded every few rounds): N / m queries per expert, <= 16 items
+    const bool rl = !multi && !p.split && !ind && p.s.N / p.s.m <= 16 * 128;
     auto kern = multi ? expert_tc_kernel<kMulti, false>
                       : (p.split ? expert_tc_kernel<kSplit, false>
-                                 : (ind ? expert_tc_kernel<kPlain, true> : expert_tc_kernel<kPlain, false>));
+                                 : (ind ? expert_tc_kernel<kPlain, true>
+                                        : (rl ? expert_tc_kernel<kPlain, false, true> : expert_tc_kernel<kPlain, false>)));
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smi));
     if (e != cudaSuccess) return e;
     kern<<<device_sms(), NT, smi, st>>>(tq, tk, tv, tlq, tlv, a);
