@@ -379,6 +379,8 @@ const char* const kStageNames[kStages] = {"pool", "pilot", "scan", "select", "ro
 struct Recorded {
     cudaStream_t stream;
     cudaEvent_t ev[kStages + 1];
+    cudaEvent_t side[2];  // the select stage when it ran on the side stream (else unused)
+    bool side_on;
     int launches[kStages];
     int first;  // stages before `first` ran no kernel (their events are not recorded)
 };
@@ -404,7 +406,13 @@ struct StageMarks {
     explicit StageMarks(cudaStream_t st) {
         if (!t_profile) return;
         rec.stream = st;
+        rec.side_on = false;
         for (auto& e : rec.ev)
+            if (!(e = take_event())) {
+                release();
+                return;
+            }
+        for (auto& e : rec.side)
             if (!(e = take_event())) {
                 release();
                 return;
@@ -414,10 +422,20 @@ struct StageMarks {
     void release() {
         for (auto& e : rec.ev)
             if (e) t_free_events.push_back(e);
+        for (auto& e : rec.side)
+            if (e) t_free_events.push_back(e);
         for (auto& e : rec.ev) e = nullptr;
+        for (auto& e : rec.side) e = nullptr;
     }
     void mark(int i) {
         if (on) cudaEventRecord(rec.ev[i], rec.stream);
+    }
+    // the select stage's own bounds on the side stream
+    void side_mark(int i, cudaStream_t ss) {
+        if (on) {
+            cudaEventRecord(rec.side[i], ss);
+            rec.side_on = true;
+        }
     }
     void commit(const int* launches, int first = 0) {
         if (on) {
@@ -431,6 +449,37 @@ struct StageMarks {
         if (on) release();
     }
 };
+
+// The expert selection needs the scan, routing only Q and the landmarks:
+// the selection runs on a side stream (one per device and caller stream,
+// forked and joined with events) concurrently with routing and grouping.
+struct SideStream {
+    cudaStream_t s = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr;
+};
+std::map<std::pair<int, uintptr_t>, SideStream> g_side;
+
+SideStream* side_stream(cudaStream_t st) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
+    std::lock_guard<std::mutex> lk(g_ws_mu);
+    SideStream& h = g_side[{dev, reinterpret_cast<uintptr_t>(st)}];
+    if (!h.s) {
+        if (cudaStreamCreateWithFlags(&h.s, cudaStreamNonBlocking) != cudaSuccess) {
+            h.s = nullptr;
+            return nullptr;
+        }
+        if (cudaEventCreateWithFlags(&h.fork, cudaEventDisableTiming) != cudaSuccess ||
+            cudaEventCreateWithFlags(&h.join, cudaEventDisableTiming) != cudaSuccess) {
+            if (h.fork) cudaEventDestroy(h.fork);
+            if (h.join) cudaEventDestroy(h.join);
+            cudaStreamDestroy(h.s);
+            h = SideStream{};
+            return nullptr;
+        }
+    }
+    return &h;
+}
 
 // The four stages on a prepared workspace.
 int run_forward(const Plan& P, const Work& W, const __nv_bfloat16* Q, const __nv_bfloat16* K,
@@ -471,13 +520,27 @@ int run_forward(const Plan& P, const Work& W, const __nv_bfloat16* Q, const __nv
         if ((e = launch_scan(P, W, K, V, st)) != cudaSuccess) return cuda_fail(e, "landmark scan launch");
     }
     marks.mark(3);
-    if ((e = launch_select(P, W, expert_idx, st)) != cudaSuccess) return cuda_fail(e, "expert selection launch");
+    // (the split form's routing reads LV from the selection: in order)
+    SideStream* ss = P.split ? nullptr : side_stream(st);
+    if (ss) {
+        if ((e = cudaEventRecord(ss->fork, st)) != cudaSuccess || (e = cudaStreamWaitEvent(ss->s, ss->fork, 0)) != cudaSuccess)
+            return cuda_fail(e, "side stream fork");
+        marks.side_mark(0, ss->s);
+        if ((e = launch_select(P, W, expert_idx, ss->s)) != cudaSuccess)
+            return cuda_fail(e, "expert selection launch");
+        marks.side_mark(1, ss->s);
+        if ((e = cudaEventRecord(ss->join, ss->s)) != cudaSuccess) return cuda_fail(e, "side stream join");
+    } else if ((e = launch_select(P, W, expert_idx, st)) != cudaSuccess) {
+        return cuda_fail(e, "expert selection launch");
+    }
     marks.mark(4);
     e = P.split ? launch_route_shared(P, W, Q, route, st) : launch_route(P, W, Q, route, st);
     if (e != cudaSuccess) return cuda_fail(e, "routing launch");
     marks.mark(5);
     for (int j = 0; j < sr; ++j)
         if ((e = launch_group(P, W, route, j, st)) != cudaSuccess) return cuda_fail(e, "grouping launch");
+    // the expert sets are read from here on
+    if (ss && (e = cudaStreamWaitEvent(st, ss->join, 0)) != cudaSuccess) return cuda_fail(e, "side stream join");
     if (P.multi_tc && (e = launch_overlap(P, W, expert_idx, route, st)) != cudaSuccess)
         return cuda_fail(e, "expert overlap launch");
     marks.mark(6);
@@ -806,12 +869,16 @@ extern "C" int mita_profile_read(double* stage_ms, int64_t* stage_launches, int 
         }
         for (int i = 0; i < n; ++i) {
             float ms = 0.f;
-            if (i >= r.first && rc == MITA_OK && (e = cudaEventElapsedTime(&ms, r.ev[i], r.ev[i + 1])) != cudaSuccess)
+            // (the select stage on the side stream: its own events; it overlaps routing)
+            const bool sel_side = r.side_on && i == 3;
+            cudaEvent_t e0 = sel_side ? r.side[0] : r.ev[i], e1 = sel_side ? r.side[1] : r.ev[i + 1];
+            if (i >= r.first && rc == MITA_OK && (e = cudaEventElapsedTime(&ms, e0, e1)) != cudaSuccess)
                 rc = cuda_fail(e, "cudaEventElapsedTime");
             if (stage_ms) stage_ms[i] += ms;
             if (stage_launches) stage_launches[i] += r.launches[i];
         }
         for (auto& ev : r.ev) t_free_events.push_back(ev);
+        for (auto& ev : r.side) t_free_events.push_back(ev);
     }
     t_records.swap(keep);
     return rc == MITA_OK ? kStages : rc;
@@ -851,6 +918,15 @@ extern "C" void mita_release_workspace(void) {
         if (h.out) cudaStreamDestroy(h.out);
     }
     g_hs.clear();
+    for (auto& kv : g_side) {
+        SideStream& h = kv.second;
+        cudaSetDevice(kv.first.first);
+        if (h.s) cudaStreamSynchronize(h.s);
+        if (h.fork) cudaEventDestroy(h.fork);
+        if (h.join) cudaEventDestroy(h.join);
+        if (h.s) cudaStreamDestroy(h.s);
+    }
+    g_side.clear();
     cudaSetDevice(cur);
 }
 
