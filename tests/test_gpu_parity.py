@@ -65,6 +65,9 @@ def _rand(B, H, N, seed, scale=1.0):
     (1, 1, 1, 0, 0, 1, 1),          # a single token
     (1, 2, 5000, 0, 0, 300, 700),   # several landmark tiles, k > 512
     (3, 1, 2500, 50, 50, 16, 1024), # 2-D 4x4 landmarks, k = MITA_MAX_K
+    # one shared key list per CTA loaded by the row warps (few items per expert)
+    (1, 2, 8192, 0, 0, 128, 128),   # two heads: the shared rows reload
+    (2, 1, 3000, 0, 0, 96, 200),    # ragged: k not a multiple of 4, windows of 31-32
     # heads short enough for the one-kernel-per-head pass (N <= 256, m <= 32)
     (2, 2, 256, 0, 0, 32, 256),     # its largest N and m, k = N
     (1, 3, 255, 0, 0, 32, 100),     # ragged key blocks and windows
