@@ -636,6 +636,7 @@ cudaError_t launch_backward(const Plan& p, const Work& w, const BwdLayout& L, vo
             if ((e = launch_pilot_select(p, w, l, st)) != cudaSuccess) return e;
         }
         if ((e = launch_scan_tc(p, w, K, V, p.nlev - 1, st)) != cudaSuccess) return e;
+        if (p.spec_j && (e = launch_scan_verify(p, w, K, st)) != cudaSuccess) return e;
         if ((e = launch_select(p, w, eidx, st, lse)) != cudaSuccess) return e;
         // routes (checked) and grouping, then each query's statistics
         const int64_t rb = cdiv64(N, 256);

@@ -249,6 +249,17 @@ bool make_plan(const Shape& s, Plan* p, bool shared, bool split) {
             P.lev[0].dense = true;
             P.lev[0].ld = P.dense_ld;
         }
+        // The last pilot's k-th best sample key is a safe main-scan threshold
+        // but a loose one: with a sample of S of the N keys, about k S / N
+        // sample keys are among the head's k best, so about k N / S keys pass
+        // it. Its j-th best with j = 2 k S / N + 8 keeps about 2k + 8 N / S
+        // and still lies below the head's k-th best unless the sample holds
+        // j of the head's best k (the main scan's candidate counts tell; a
+        // head where that happened is scanned again from the k-th).
+        if (P.nlev > 1) {
+            const int64_t j = cdiv(2 * static_cast<int64_t>(s.k) * P.lev[P.nlev - 2].S, s.N) + 8;
+            if (j < s.k) P.spec_j = static_cast<int>(j);
+        }
     } else {
         // CUDA-core scan: 32 landmarks per CTA, ~8 CTAs per SM, >= 1024 keys per chunk
         const int64_t ltiles = cdiv(s.m, 32);
@@ -328,6 +339,8 @@ bool make_plan(const Shape& s, Plan* p, bool shared, bool split) {
     P.off_mask = take(P.multi_tc ? pass_mask_bytes(s) : 0);
     P.off_osh = take(P.split ? BH * static_cast<size_t>(s.N) * D * 2 : 0);
     P.off_lse = take(P.split ? BH * static_cast<size_t>(s.N) * sizeof(float) : 0);
+    P.off_theta_safe = take(P.spec_j ? BH * m * sizeof(uint64_t) : 0);
+    P.off_hflag = take(P.spec_j ? BH * sizeof(int) : 0);
     P.total = off;
     if (P.max_items * s.BH > 0x7FFFFFFFLL || s.BH * P.nrblocks > 0x7FFFFFFFLL) return false;
     for (int l = 0; l < P.nlev; ++l)
@@ -352,6 +365,8 @@ Work carve(const Plan& p, void* base) {
     w.rval = reinterpret_cast<float*>(b + p.off_rval);
     w.rcount = reinterpret_cast<int*>(b + p.off_rcount);
     w.theta = reinterpret_cast<uint64_t*>(b + p.off_theta);
+    w.theta_safe = reinterpret_cast<uint64_t*>(b + p.off_theta_safe);
+    w.hflag = reinterpret_cast<int*>(b + p.off_hflag);
     w.counts = reinterpret_cast<int*>(b + p.off_counts);
     w.expoff = reinterpret_cast<int*>(b + p.off_expoff);
     w.cursor = reinterpret_cast<int*>(b + p.off_cursor);
@@ -515,6 +530,8 @@ int run_forward(const Plan& P, const Work& W, const __nv_bfloat16* Q, const __nv
         marks.mark(2);
         if ((e = launch_scan_tc(P, W, K, V, P.nlev - 1, st)) != cudaSuccess)
             return cuda_fail(e, "landmark scan launch");
+        if (P.spec_j && (e = launch_scan_verify(P, W, K, st)) != cudaSuccess)
+            return cuda_fail(e, "landmark scan check launch");
     } else {
         marks.mark(2);
         if ((e = launch_scan(P, W, K, V, st)) != cudaSuccess) return cuda_fail(e, "landmark scan launch");
@@ -555,7 +572,8 @@ int run_forward(const Plan& P, const Work& W, const __nv_bfloat16* Q, const __nv
         }
     }
     marks.mark(7);
-    const int launches[kStages] = {1, P.scan_tc ? 2 * (P.nlev - 1) : 0, 1, 1, 1, 2 * sr + (P.multi_tc ? sr : 0), sr};
+    const int launches[kStages] = {1, P.scan_tc ? 2 * (P.nlev - 1) : 0, 1 + (P.spec_j ? 2 : 0), 1, 1,
+                                   2 * sr + (P.multi_tc ? sr : 0), sr};
     marks.commit(launches);
     if (lq_out && (e = cudaMemcpyAsync(lq_out, W.lq32, mrows * D * sizeof(float), cudaMemcpyDeviceToDevice, st)) !=
                       cudaSuccess)

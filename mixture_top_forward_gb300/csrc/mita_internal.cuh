@@ -55,6 +55,11 @@ struct Plan {
     // whole rows (no pilots, no candidate buffers)
     bool dense;
     int64_t dense_ld;  // row stride of the dense logits (N rounded up to 4)
+    // speculative main-scan threshold (0: off): the last pilot passes the
+    // spec_j-th best key of its sample instead of the k-th; a head where a
+    // landmark then keeps fewer than k candidates is scanned again from the
+    // k-th (safe) thresholds
+    int spec_j;
     // routing / grouping
     int rblock;         // queries per routing CTA
     int64_t nrblocks;   // routing CTAs per head
@@ -71,7 +76,7 @@ struct Plan {
     // workspace layout (byte offsets)
     size_t off_status, off_lq32, off_lqhi, off_lqlo, off_lv32, off_lvbf, off_part, off_cand, off_ccount, off_theta,
         off_counts, off_expoff, off_cursor, off_perm, off_items, off_nitems, off_dense, off_ridx, off_rval, off_rcount,
-        off_state, off_ovl, off_mask, off_osh, off_lse, total;
+        off_state, off_ovl, off_mask, off_osh, off_lse, off_theta_safe, off_hflag, total;
 };
 
 // Builds the plan; returns false if a size does not fit the int ranges used.
@@ -94,6 +99,8 @@ struct Work {
     float* rval;            // [BH][chunks][m][rcap][8] group records: the group's 8 raw logits
     int* rcount;            // [BH][chunks][m]
     uint64_t* theta;        // [BH][m] top-k thresholds from the pilot scans
+    uint64_t* theta_safe;   // [BH][m] spec_j: the last pilot's k-th best keys (the fallback thresholds)
+    int* hflag;             // [BH] spec_j: heads to scan again from theta_safe
     float* dense;           // [BH][m][dense_ld] raw logits <Lq_i, K_j> (dense top-k only)
     int* counts;            // [s][BH][m] queries routed to each expert (per rank of the routes)
     int* expoff;            // [BH][m+1] exclusive prefix of counts
@@ -165,6 +172,10 @@ cudaError_t launch_scan(const Plan& p, const Work& w, const __nv_bfloat16* K, co
                         cudaStream_t st);
 cudaError_t launch_scan_tc(const Plan& p, const Work& w, const __nv_bfloat16* K, const __nv_bfloat16* V, int level,
                            cudaStream_t st);
+// After the main scan from a speculative threshold (p.spec_j): flags every
+// head with a landmark that kept fewer than k candidates and scans those
+// heads' keys again, candidates only, from the safe thresholds.
+cudaError_t launch_scan_verify(const Plan& p, const Work& w, const __nv_bfloat16* K, cudaStream_t st);
 // lse_out (optional): each landmark's log-sum-exp over all keys of tau <Lq_i, K_j>.
 // Dense rows of at most 4096 logits take a warp-per-landmark kernel.
 bool dense_row_select_applies(const Plan& p);

@@ -68,6 +68,7 @@ struct ScanArgs {
     float* dense;           // dense top-k: [BH][m][ld] raw logits, else null
     int64_t ld;             // row stride of dense
     int* status;
+    const int* skip;    // [BH] or null: a head whose entry is 0 is not scanned (its CTAs return at once)
     int64_t S;          // keys (samples) per head in this scan
     int64_t stride;     // key index of sample s is s * stride
     int64_t chunk_len;  // multiple of 128
@@ -139,6 +140,7 @@ __global__ void __launch_bounds__(Cfg<FULL, NL>::NT, Cfg<FULL, NL>::MINB)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int c = static_cast<int>(blockIdx.x % static_cast<unsigned>(a.chunks));
     const int64_t bh = blockIdx.x / static_cast<unsigned>(a.chunks);
+    if (a.skip && a.skip[bh] == 0) return;  // (uniform: before any barrier or TMEM allocation)
     const int64_t s0 = static_cast<int64_t>(c) * a.chunk_len;
     const int64_t s1 = min(a.S, s0 + a.chunk_len);
     const int T = static_cast<int>((s1 - s0 + KT - 1) / KT);
@@ -454,6 +456,47 @@ cudaError_t launch_one(const CUtensorMap& tk, const CUtensorMap& tv, const ScanA
     return cudaGetLastError();
 }
 
+// One thread per landmark: the candidates its chunks kept; a head with a
+// landmark below k is flagged (every head's flag is written).
+__global__ void __launch_bounds__(256) scan_check_kernel(const int* __restrict__ ccount, int chunks, int m, int k,
+                                                         int* __restrict__ hflag) {
+    const int64_t bh = blockIdx.x;
+    bool bad = false;
+    for (int i = threadIdx.x; i < m; i += 256) {
+        int n = 0;
+        for (int c = 0; c < chunks; ++c) n += ccount[(bh * chunks + c) * m + i];
+        bad = bad || n < k;
+    }
+    bad = __syncthreads_or(bad);
+    if (threadIdx.x == 0) hflag[bh] = bad ? 1 : 0;
+}
+
+ScanArgs scan_args(const Plan& p, const Work& w, const ScanLevel& L) {
+    ScanArgs a;
+    a.lqhi = w.lqhi;
+    a.lqlo = w.lqlo;
+    a.theta = w.theta;
+    a.part = w.part;
+    a.cand = w.cand;
+    a.ccount = w.ccount;
+    a.dense = L.dense ? w.dense : nullptr;
+    a.ld = L.ld;
+    a.status = w.status;
+    a.skip = nullptr;
+    a.S = L.S;
+    a.stride = L.stride;
+    a.chunk_len = L.chunk_len;
+    a.chunks = L.chunks;
+    a.cap = L.cap;
+    a.rcap = L.rcap;
+    a.ridx = w.ridx;
+    a.rval = w.rval;
+    a.rcount = w.rcount;
+    a.m = p.s.m;
+    a.k = p.s.k;
+    return a;
+}
+
 }  // namespace
 
 cudaError_t launch_scan_tc(const Plan& p, const Work& w, const __nv_bfloat16* K, const __nv_bfloat16* V, int level,
@@ -471,30 +514,28 @@ cudaError_t launch_scan_tc(const Plan& p, const Work& w, const __nv_bfloat16* K,
     } else {
         tv = tk;
     }
-    ScanArgs a;
-    a.lqhi = w.lqhi;
-    a.lqlo = w.lqlo;
+    ScanArgs a = scan_args(p, w, L);
     a.theta = level > 0 ? w.theta : nullptr;
-    a.part = w.part;
-    a.cand = w.cand;
-    a.ccount = w.ccount;
-    a.dense = L.dense ? w.dense : nullptr;
-    a.ld = L.ld;
-    a.status = w.status;
-    a.S = L.S;
-    a.stride = L.stride;
-    a.chunk_len = L.chunk_len;
-    a.chunks = L.chunks;
-    a.cap = L.cap;
-    a.rcap = L.rcap;
-    a.ridx = w.ridx;
-    a.rval = w.rval;
-    a.rcount = w.rcount;
-    a.m = p.s.m;
-    a.k = p.s.k;
     const bool two = p.s.m > 128;
     if (full) return two ? launch_one<true, 2>(tk, tv, a, p.s.BH, st) : launch_one<true, 1>(tk, tv, a, p.s.BH, st);
     return two ? launch_one<false, 2>(tk, tv, a, p.s.BH, st) : launch_one<false, 1>(tk, tv, a, p.s.BH, st);
+}
+
+cudaError_t launch_scan_verify(const Plan& p, const Work& w, const __nv_bfloat16* K, cudaStream_t st) {
+    const ScanLevel& L = p.lev[p.nlev - 1];
+    scan_check_kernel<<<static_cast<unsigned>(p.s.BH), 256, 0, st>>>(w.ccount, L.chunks, p.s.m, p.s.k, w.hflag);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    CUtensorMap tk;
+    if (!make_head_tmap(&tk, K, static_cast<uint64_t>(L.S), static_cast<uint64_t>(p.s.BH),
+                        static_cast<uint64_t>(L.stride), static_cast<uint64_t>(p.s.N), 64))
+        return cudaErrorInvalidValue;
+    // the flagged heads' candidates again (the same chunks and buffers; LV is
+    // already merged from the main scan's partials), from the k-th best keys
+    ScanArgs a = scan_args(p, w, L);
+    a.theta = w.theta_safe;
+    a.skip = w.hflag;
+    return p.s.m > 128 ? launch_one<false, 2>(tk, tk, a, p.s.BH, st) : launch_one<false, 1>(tk, tk, a, p.s.BH, st);
 }
 
 }  // namespace mita

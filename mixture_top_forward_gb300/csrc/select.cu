@@ -38,15 +38,17 @@ __global__ void __launch_bounds__(ST) select_kernel(int m, int k, int chunks, in
                                                     int64_t stride, const uint32_t* __restrict__ ridx,
                                                     const float* __restrict__ rval, const int* __restrict__ rcount,
                                                     int rcap, const uint64_t* __restrict__ thr_in,
-                                                    float* __restrict__ lse_out) {
+                                                    float* __restrict__ lse_out, int jspec,
+                                                    uint64_t* __restrict__ theta_safe) {
     __shared__ unsigned hist[256];
     __shared__ int offs[ST + 1];        // chunk offsets into staged[] (chunks <= ST)
     __shared__ float red[ST / 32 + 1];  // block reductions
     __shared__ float fac[ST];           // LV merge: per-chunk rescale factors
     __shared__ float osum[4][D];
     __shared__ uint64_t staged[SEL_CAP];
-    __shared__ int sel[MITA_SORT_MAX];
+    __shared__ __align__(8) int sel[MITA_SORT_MAX];  // (the pilot's speculative pass: MITA_SORT_MAX / 2 keys)
     __shared__ int nsel;
+    __shared__ unsigned long long s_kj;
     __shared__ int nst;  // keys staged (records expanded); counts past SEL_CAP too
     __shared__ int s_digit;
     __shared__ unsigned s_above;
@@ -256,14 +258,15 @@ __global__ void __launch_bounds__(ST) select_kernel(int m, int k, int chunks, in
     // holding the k-th largest key holds exactly the keys still needed: then
     // every key whose leading digits reach the prefix is selected, and the
     // prefix (lower bits zero) separates them from the rest.
-    uint64_t kth = 0;  // keep every key >= kth
-    if (total > k || (PILOT && total == k)) {
+    // (each: the key set, as for_each; returns a value with exactly `target`
+    // of the keys at or above it)
+    auto radix_select = [&](unsigned target, auto&& each) -> uint64_t {
         uint64_t prefix = 0, mask = 0;
-        unsigned remaining = static_cast<unsigned>(k);
+        unsigned remaining = target;
         for (int shift = 56; shift >= 0; shift -= 8) {
             hist[tid] = 0;
             __syncthreads();
-            for_each([&](uint64_t x) {
+            each([&](uint64_t x) {
                 if ((x & mask) == prefix) atomicAdd(&hist[(x >> shift) & 255u], 1u);
             });
             __syncthreads();
@@ -302,12 +305,45 @@ __global__ void __launch_bounds__(ST) select_kernel(int m, int k, int chunks, in
             __syncthreads();
             if (whole_bin) break;
         }
-        kth = prefix;
-    }
+        return prefix;
+    };
+    uint64_t kth = 0;  // keep every key >= kth
+    if (total > k || (PILOT && total == k)) kth = radix_select(static_cast<unsigned>(k), for_each);
     if (PILOT) {
-        if (tid == 0 && total >= k) {
+        // The last pilot of a speculative scan (theta_safe set) also finds the
+        // jspec-th largest key (jspec < k), by the same radix select over the
+        // keys at or above the k-th (at least k of them, gathered in shared
+        // memory when they fit). It becomes the threshold, the k-th the
+        // fallback.
+        bool ranked = false;
+        if (theta_safe && total >= k) {
+            uint64_t* g = reinterpret_cast<uint64_t*>(sel);
+            constexpr int GCAP = MITA_SORT_MAX / 2;
+            if (tid == 0) nsel = 0;
+            __syncthreads();
+            for_each([&](uint64_t x) {
+                if (x >= kth) {
+                    const int p = atomicAdd(&nsel, 1);
+                    if (p < GCAP) g[p] = x;
+                }
+            });
+            __syncthreads();
+            const int n = nsel;
+            if (n > jspec && n <= GCAP) {
+                const uint64_t kj = radix_select(static_cast<unsigned>(jspec), [&](auto&& f) {
+                    for (int e = tid; e < n; e += ST) f(g[e]);
+                });
+                if (tid == 0) s_kj = kj;
+                ranked = true;
+            }
+            __syncthreads();
+        }
+        if (tid == 0) {
             const uint64_t old = theta[bh * m + i];
-            theta[bh * m + i] = kth > old ? kth : old;
+            const uint64_t safe = (total >= k && kth > old) ? kth : old;
+            const uint64_t spec = ranked && s_kj > safe ? static_cast<uint64_t>(s_kj) : safe;
+            theta[bh * m + i] = spec;
+            if (theta_safe) theta_safe[bh * m + i] = safe;
         }
         return;
     }
@@ -509,7 +545,7 @@ cudaError_t launch_select(const Plan& p, const Work& w, int32_t* expert_idx, cud
                                              w.ccount, w.lv32,
                                              w.lvbf, expert_idx, nullptr, L.dense ? w.dense : nullptr, p.s.N, L.ld,
                                              1, w.ridx, w.rval, w.rcount, L.rcap, p.nlev > 1 ? w.theta : nullptr,
-                                             lse_out);
+                                             lse_out, 0, nullptr);
     return cudaGetLastError();
 }
 
@@ -519,7 +555,8 @@ cudaError_t launch_pilot_select(const Plan& p, const Work& w, int level, cudaStr
     select_kernel<true><<<grid, ST, 0, st>>>(p.s.m, p.s.k, L.chunks, L.cap, nullptr, w.cand, w.ccount, nullptr,
                                             nullptr, nullptr, w.theta, L.dense ? w.dense : nullptr, L.S, L.ld,
                                             L.stride, w.ridx, w.rval, w.rcount, L.rcap,
-                                            level > 0 ? w.theta : nullptr, nullptr);
+                                            level > 0 ? w.theta : nullptr, nullptr, p.spec_j,
+                                            p.spec_j && level == p.nlev - 2 ? w.theta_safe : nullptr);
     return cudaGetLastError();
 }
 
