@@ -200,9 +200,11 @@ bool make_plan(const Shape& s, Plan* p, bool shared, bool split) {
     P.scan_tc = s.m <= 256;
     if (P.scan_tc) {
         // Pilots: strided samples, the first of max(2k, min(N/8, 8k)) keys,
-        // then up to 16x larger, the last of about N/8 keys; each starts from
-        // the previous level's threshold. The main scan then keeps about 8k
-        // candidates per landmark and head.
+        // then up to 16x larger while within N/16; each starts from the
+        // previous level's threshold. The main scan starts from the last
+        // level's speculative key (below), which keeps about 2k + 8 N / S
+        // candidates per landmark and head: 2k + 128 after N/16 samples,
+        // against 2k + 64 after N/8, for half the last level's cost.
         int64_t prevS = 0;
         const int64_t K8 = 8LL * s.k;
         int64_t t = std::max<int64_t>(2LL * s.k, std::min<int64_t>(s.N / 8, K8));
@@ -227,7 +229,7 @@ bool make_plan(const Shape& s, Plan* p, bool shared, bool split) {
                 }
                 P.lev[P.nlev++] = L;
                 prevS = S;
-                const int64_t next = std::min<int64_t>(16 * t, s.N / 8);
+                const int64_t next = std::min<int64_t>(16 * t, s.N / 16);
                 if (next <= S) break;
                 t = next;
             }

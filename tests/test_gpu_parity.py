@@ -353,9 +353,9 @@ def test_pilot_blind_spot_forces_compaction(orc):
 def test_pilot_records_overflow_to_keys(orc):
     """Keys at indices 8, 16, 24 (mod 32) outscore the rest. At N = 65536 the
     first pilot level samples every 32nd key and sees only weak ones, so the
-    second level (every 8th key) finds three quarters of its samples above
-    that threshold: its group records fill, the rest go out as keys and
-    compact, and the result must still be exact."""
+    second level (every 16th key) finds half of its samples above that
+    threshold, in every 8-sample group: its group records fill, the rest go
+    out as keys and compact, and the result must still be exact."""
     B, H, N, m, k = 1, 1, 65536, 4, 64
     noise = synth.bf16_to_f64(synth.normal_bf16((B, H, N, 64), 43, 0))
     q = synth.f64_to_bf16(1.0 + 0.1 * noise)
@@ -369,16 +369,16 @@ def test_pilot_records_overflow_to_keys(orc):
 
 
 def test_speculative_threshold_falls_back(orc):
-    """Keys at indices 0 (mod 8), the last pilot's samples at N = 65536,
-    outscore the rest, so the head's best keys are all sample keys: the
-    speculative threshold (a sample key of rank 2 k / 8 + 8 = 24) leaves only
-    24 keys above it, every landmark keeps fewer than k candidates, and the
-    head is scanned again from the k-th best sample key; the result must
-    still be exact."""
+    """Keys at indices 0 (mod 16), the last pilot's samples at N = 65536
+    (levels of 2048 and 4096 samples), outscore the rest, so the head's best
+    keys are all sample keys: the speculative threshold (the sample key of
+    rank 2 k / 16 + 8 = 16) leaves only 16 keys above it, every landmark
+    keeps fewer than k candidates, and the head is scanned again from the
+    k-th best sample key; the result must still be exact."""
     B, H, N, m, k = 1, 2, 65536, 4, 64
     noise = synth.bf16_to_f64(synth.normal_bf16((B, H, N, 64), 47, 0))
     q = synth.f64_to_bf16(1.0 + 0.1 * noise)
-    sign = np.where(np.arange(N) % 8 == 0, 1.0, -1.0)[None, None, :, None]
+    sign = np.where(np.arange(N) % 16 == 0, 1.0, -1.0)[None, None, :, None]
     kn = synth.bf16_to_f64(synth.normal_bf16((B, H, N, 64), 47, 1))
     kk_ = synth.f64_to_bf16(0.5 * sign + 0.05 * kn)
     v = synth.normal_bf16((B, H, N, 64), 47, 2)
