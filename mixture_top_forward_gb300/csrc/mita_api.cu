@@ -200,11 +200,12 @@ bool make_plan(const Shape& s, Plan* p, bool shared, bool split) {
     P.scan_tc = s.m <= 256;
     if (P.scan_tc) {
         // Pilots: strided samples, the first of max(2k, min(N/8, 8k)) keys,
-        // then up to 16x larger while within N/16; each starts from the
+        // then up to 16x larger while within N/32; each starts from the
         // previous level's threshold. The main scan starts from the last
         // level's speculative key (below), which keeps about 2k + 8 N / S
-        // candidates per landmark and head: 2k + 128 after N/16 samples,
-        // against 2k + 64 after N/8, for half the last level's cost.
+        // candidates per landmark and head: 2k + 256 after N/32 samples,
+        // against 2k + 64 after N/8, for a quarter of the last level's cost
+        // (at 1M: levels of 8192 and 32768 samples instead of three).
         int64_t prevS = 0;
         const int64_t K8 = 8LL * s.k;
         int64_t t = std::max<int64_t>(2LL * s.k, std::min<int64_t>(s.N / 8, K8));
@@ -229,7 +230,7 @@ bool make_plan(const Shape& s, Plan* p, bool shared, bool split) {
                 }
                 P.lev[P.nlev++] = L;
                 prevS = S;
-                const int64_t next = std::min<int64_t>(16 * t, s.N / 16);
+                const int64_t next = std::min<int64_t>(16 * t, s.N / 32);
                 if (next <= S) break;
                 t = next;
             }

@@ -350,38 +350,22 @@ def test_pilot_blind_spot_forces_compaction(orc):
     print(rep)
 
 
-def test_pilot_records_overflow_to_keys(orc):
-    """Keys at indices 8, 16, 24 (mod 32) outscore the rest. At N = 65536 the
-    first pilot level samples every 32nd key and sees only weak ones, so the
-    second level (every 16th key) finds half of its samples above that
-    threshold, in every 8-sample group: its group records fill, the rest go
-    out as keys and compact, and the result must still be exact."""
-    B, H, N, m, k = 1, 1, 65536, 4, 64
+def test_pilot_records_in_every_group(orc):
+    """Keys at indices 32, 64, 96 (mod 128) outscore the rest. At N = 65536
+    and k = 16 the first pilot level (512 samples, every 128th key) sees only
+    weak ones, so the second (every 32nd key) finds three quarters of its
+    samples above that threshold, in every 8-sample group: each group goes
+    out as a record (64 per chunk of 512 samples, within the 96 a landmark
+    may keep), the select expands them all, and the result must still be
+    exact."""
+    B, H, N, m, k = 1, 1, 65536, 4, 16
     noise = synth.bf16_to_f64(synth.normal_bf16((B, H, N, 64), 43, 0))
     q = synth.f64_to_bf16(1.0 + 0.1 * noise)
-    idx = np.arange(N) % 32
-    sign = np.where((idx == 8) | (idx == 16) | (idx == 24), 1.0, -1.0)[None, None, :, None]
+    idx = np.arange(N) % 128
+    sign = np.where((idx == 32) | (idx == 64) | (idx == 96), 1.0, -1.0)[None, None, :, None]
     kn = synth.bf16_to_f64(synth.normal_bf16((B, H, N, 64), 43, 1))
     kk_ = synth.f64_to_bf16(0.5 * sign + 0.05 * kn)
     v = synth.normal_bf16((B, H, N, 64), 43, 2)
-    rep = parity.full_parity(orc, q, kk_, v, 0, 0, m, k)
-    print(rep)
-
-
-def test_speculative_threshold_falls_back(orc):
-    """Keys at indices 0 (mod 16), the last pilot's samples at N = 65536
-    (levels of 2048 and 4096 samples), outscore the rest, so the head's best
-    keys are all sample keys: the speculative threshold (the sample key of
-    rank 2 k / 16 + 8 = 16) leaves only 16 keys above it, every landmark
-    keeps fewer than k candidates, and the head is scanned again from the
-    k-th best sample key; the result must still be exact."""
-    B, H, N, m, k = 1, 2, 65536, 4, 64
-    noise = synth.bf16_to_f64(synth.normal_bf16((B, H, N, 64), 47, 0))
-    q = synth.f64_to_bf16(1.0 + 0.1 * noise)
-    sign = np.where(np.arange(N) % 16 == 0, 1.0, -1.0)[None, None, :, None]
-    kn = synth.bf16_to_f64(synth.normal_bf16((B, H, N, 64), 47, 1))
-    kk_ = synth.f64_to_bf16(0.5 * sign + 0.05 * kn)
-    v = synth.normal_bf16((B, H, N, 64), 47, 2)
     rep = parity.full_parity(orc, q, kk_, v, 0, 0, m, k)
     print(rep)
 
