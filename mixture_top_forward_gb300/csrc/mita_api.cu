@@ -210,13 +210,15 @@ bool make_plan(const Shape& s, Plan* p, bool shared, bool split) {
         const int64_t K8 = 8LL * s.k;
         int64_t t = std::max<int64_t>(2LL * s.k, std::min<int64_t>(s.N / 8, K8));
         if (8 * t <= s.N) {
-            // The first level has no threshold. When a 4x larger sample still
-            // fits below N/8 (and its logits in 1 GB), it writes every logit of
-            // that sample and its select ranks whole rows (dense): appending
-            // each sampled key as a candidate costs more, and the 4x larger
-            // sample makes the next level's threshold 4x tighter.
-            const int64_t t0 = 4 * t;
-            const bool dense0 = t0 <= s.N / 8 && s.BH * s.m * round_up(t0, 4) * 4 <= (1LL << 30);
+            // The first level has no threshold. When a sample up to 4x larger
+            // (within N/16: as the last level it is the speculative threshold's
+            // sample, see above) still fits below N/8 and its logits in 1 GB,
+            // it writes every logit of that sample and its select ranks whole
+            // rows (dense): appending each sampled key as a candidate costs
+            // more, and the larger sample makes the next level's threshold
+            // tighter.
+            const int64_t t0 = std::min<int64_t>(4 * t, s.N / 16);
+            const bool dense0 = t0 >= t && t0 <= s.N / 8 && s.BH * s.m * round_up(t0, 4) * 4 <= (1LL << 30);
             while (P.nlev < 3) {
                 const int64_t ts = (P.nlev == 0 && dense0) ? t0 : t;
                 const int64_t stride = s.N / ts;

@@ -370,6 +370,24 @@ def test_pilot_records_in_every_group(orc):
     print(rep)
 
 
+def test_speculative_threshold_falls_back(orc):
+    """Keys at indices 0 (mod 32), the pilot's samples at N = 65536 (one
+    level of 2048 samples), outscore the rest, so the head's best keys are
+    all sample keys: the speculative threshold (the sample key of rank
+    2 k / 32 + 8 = 12) leaves only 12 keys above it, every landmark keeps
+    fewer than k candidates, and the head is scanned again from the k-th
+    best sample key; the result must still be exact."""
+    B, H, N, m, k = 1, 2, 65536, 4, 64
+    noise = synth.bf16_to_f64(synth.normal_bf16((B, H, N, 64), 47, 0))
+    q = synth.f64_to_bf16(1.0 + 0.1 * noise)
+    sign = np.where(np.arange(N) % 32 == 0, 1.0, -1.0)[None, None, :, None]
+    kn = synth.bf16_to_f64(synth.normal_bf16((B, H, N, 64), 47, 1))
+    kk_ = synth.f64_to_bf16(0.5 * sign + 0.05 * kn)
+    v = synth.normal_bf16((B, H, N, 64), 47, 2)
+    rep = parity.full_parity(orc, q, kk_, v, 0, 0, m, k)
+    print(rep)
+
+
 # --- mita_forward_split: the shared branch folded into the routing kernel ---
 def _run_split(q, k, v, gh, gw, m, kk, full_out=True):
     """mita_forward_split's outputs; Lq and LV (not returned by that entry
