@@ -115,6 +115,10 @@ struct Args {
             const float* lse;           // [BH][N] the shared branch's log-sum-exp (log2 units)
             const __nv_bfloat16* osh;   // [BH][N][64] its output rows
         };
+        struct {                        // plain: the key and value rows (L2 prefetches of the next list)
+            const __nv_bfloat16* kp;    // [BH][N][64]
+            const __nv_bfloat16* vp;    // [BH][N][64]
+        };
         struct {                        // STATS
             const __nv_bfloat16* dO;    // [BH][N][64] output gradients
             float* st_lse;              // [BH][N] log-sum-exp of the m + k logits (log2 units of tau <q, key>)
@@ -407,6 +411,24 @@ __global__ void __launch_bounds__(NT, 1)
                     ok = gather_q(it[w], w);
                 }
                 r += cnt;
+                if constexpr (MODE == kPlain) {
+                    // the next round's expert, if it is another one: its routed
+                    // key and value rows into L2 now (a round or two before
+                    // its list is gathered), so that the gathers at the list
+                    // change find them there instead of in DRAM
+                    if (r < i1) {
+                        const int4 nx = a.items[r];
+                        if (nx.w != it[0].w || nx.x != it[0].x) {
+                            const int32_t* sel = a.expert_idx + (static_cast<int64_t>(nx.w) * a.m + nx.x) * a.k;
+                            const int64_t hb = static_cast<int64_t>(nx.w) * a.N;
+                            for (int i = lane; i < a.k; i += 32) {
+                                const int64_t row = hb + sel[i];
+                                asm volatile("prefetch.global.L2 [%0];" ::"l"(a.kp + row * D));
+                                asm volatile("prefetch.global.L2 [%0];" ::"l"(a.vp + row * D));
+                            }
+                        }
+                    }
+                }
             }
         }
         // exit: the last phase of every barrier this warp armed has landed
@@ -915,6 +937,9 @@ cudaError_t launch_expert_tc(const Plan& p, const Work& w, const __nv_bfloat16* 
     } else if (p.split) {
         a.lse = w.lse;
         a.osh = w.osh;
+    } else {
+        a.kp = K;
+        a.vp = V;
     }
     CUtensorMap tq, tk, tv, tlq, tlv;
     const uint64_t rows = static_cast<uint64_t>(p.s.BH) * p.s.N, lrows = static_cast<uint64_t>(p.s.BH) * p.s.m;
