@@ -48,6 +48,7 @@ __global__ void __launch_bounds__(ST) select_kernel(int m, int k, int chunks, in
     __shared__ uint64_t staged[SEL_CAP];
     __shared__ __align__(8) int sel[MITA_SORT_MAX];  // (the pilot's speculative pass: MITA_SORT_MAX / 2 keys)
     __shared__ int nsel;
+    __shared__ int wcnt[ST / 32];  // ordered take: selected keys per warp in the round
     __shared__ unsigned long long s_kj;
     __shared__ int nst;  // keys staged (records expanded); counts past SEL_CAP too
     __shared__ int s_digit;
@@ -348,7 +349,39 @@ __global__ void __launch_bounds__(ST) select_kernel(int m, int k, int chunks, in
         return;
     }
 
-    // ---- gather the selected indices and sort them ascending ----------------
+    int32_t* dst = expert_idx + (bh * m + i) * static_cast<int64_t>(k);
+    if (in_smem) {
+        // ---- the selected indices, ascending, by an ordered take ----------
+        // The staged keys are in ascending index order: the chunks cover the
+        // keys in order, each appends its candidates in key order and its
+        // compaction keeps their order (a dense row is staged in order).
+        // Round by round (ST keys), each selected key goes to the number of
+        // selected keys before it. Exactly k keys reach kth (every landmark
+        // keeps at least k candidates); were it ever fewer, the rest become
+        // key 0, so every index written is in range.
+        int base = 0;  // selected in earlier rounds (block-uniform)
+        for (int e0 = 0; e0 < total; e0 += ST) {
+            const int e = e0 + tid;
+            const bool f = e < total && staged[e] >= kth;
+            const unsigned bal = __ballot_sync(0xffffffffu, f);
+            if (lane == 0) wcnt[wid] = __popc(bal);
+            __syncthreads();
+            int before = 0, all = 0;
+#pragma unroll
+            for (int w = 0; w < ST / 32; ++w) {
+                const int c = wcnt[w];
+                before += w < wid ? c : 0;
+                all += c;
+            }
+            const int pos = base + before + __popc(bal & lanemask_lt());
+            if (f && pos < k) dst[pos] = static_cast<int>(topk_key_index(staged[e]));
+            base += all;
+            __syncthreads();  // (wcnt is rewritten next round)
+        }
+        for (int t = base + tid; t < k; t += ST) dst[t] = 0;
+        return;
+    }
+    // ---- otherwise: gather the selected indices and sort them ascending -----
     if (tid == 0) nsel = 0;
     __syncthreads();
     for_each([&](uint64_t x) {
@@ -362,7 +395,6 @@ __global__ void __launch_bounds__(ST) select_kernel(int m, int k, int chunks, in
     __syncthreads();
     // ascending order: each selected index goes to the place given by the
     // number of selected indices below it (equal ones ordered by position)
-    int32_t* dst = expert_idx + (bh * m + i) * static_cast<int64_t>(k);
     for (int t = tid; t < k; t += ST) {
         const int x = sel[t];
         int r = 0;
