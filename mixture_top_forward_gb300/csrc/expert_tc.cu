@@ -265,6 +265,7 @@ __global__ void __launch_bounds__(NT, 1)
     expert_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                      const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tlq,
                      const __grid_constant__ CUtensorMap tlv, Args a) {
+    dep_entry();  // (launched by launch_dep: the kernel before may still be finishing)
     constexpr bool MULTI = MODE == kMulti, SPLIT = MODE == kSplit, STATS = MODE == kStats;
     extern __shared__ uint8_t smem_raw[];
     __shared__ uint64_t kvfull[NWG], kvfree[NWG], qfull[NWG * QB], qfree[NWG * QB], ofree[NWG];
@@ -959,8 +960,7 @@ cudaError_t launch_expert_tc(const Plan& p, const Work& w, const __nv_bfloat16* 
                                         : (rl ? expert_tc_kernel<kPlain, false, true> : expert_tc_kernel<kPlain, false>)));
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smi));
     if (e != cudaSuccess) return e;
-    kern<<<device_sms(), NT, smi, st>>>(tq, tk, tv, tlq, tlv, a);
-    return cudaGetLastError();
+    return launch_dep(kern, dim3(device_sms()), dim3(NT), smi, st, tq, tk, tv, tlq, tlv, a);
 }
 
 cudaError_t launch_expert_stats(const Plan& p, const Work& w, const __nv_bfloat16* Q, const __nv_bfloat16* K,
@@ -991,8 +991,7 @@ cudaError_t launch_expert_stats(const Plan& p, const Work& w, const __nv_bfloat1
     cudaError_t e = cudaFuncSetAttribute(expert_tc_kernel<kStats, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(sm));
     if (e != cudaSuccess) return e;
-    expert_tc_kernel<kStats, false><<<device_sms(), NT, sm, st>>>(tq, tk, tv, tlq, tlv, a);
-    return cudaGetLastError();
+    return launch_dep(expert_tc_kernel<kStats, false>, dim3(device_sms()), dim3(NT), sm, st, tq, tk, tv, tlq, tlv, a);
 }
 
 }  // namespace mita

@@ -31,6 +31,7 @@ constexpr int SQT = 4;     // queries per scatter thread
 __global__ void __launch_bounds__(GT) offsets_kernel(int m, int64_t N, int qtile, int* __restrict__ counts,
                                                      int* __restrict__ expoff, int* __restrict__ cursor,
                                                      int4* __restrict__ items, int* __restrict__ nitems) {
+    dep_entry();  // (launched by launch_dep: the kernel before may still be finishing)
     __shared__ int sc[GT];
     __shared__ int st[GT];
     __shared__ int base;
@@ -70,6 +71,7 @@ __global__ void __launch_bounds__(GT) offsets_kernel(int m, int64_t N, int qtile
 __global__ void __launch_bounds__(SCT) scatter_kernel(const int32_t* __restrict__ route, int64_t N, int m, int s,
                                                       int j, int64_t nblocks, int* __restrict__ cursor,
                                                       int* __restrict__ perm) {
+    dep_entry();  // (launched by launch_dep: the kernel before may still be finishing)
     __shared__ int sh[MITA_MAX_M_INTERNAL];
     const int64_t blk = blockIdx.x % nblocks;
     const int64_t bh = blockIdx.x / nblocks;
@@ -99,12 +101,12 @@ cudaError_t launch_group(const Plan& p, const Work& w, const int32_t* route, int
     const size_t mrows = static_cast<size_t>(p.s.BH) * p.s.m;
     int* perm = w.perm + static_cast<size_t>(j) * p.s.BH * p.s.N;
     int4* items = w.items + static_cast<size_t>(j) * p.s.BH * p.max_items;
-    offsets_kernel<<<static_cast<unsigned>(p.s.BH), GT, 0, st>>>(p.s.m, p.s.N, p.qtile, w.counts + j * mrows,
-                                                                 w.expoff, w.cursor, items, w.nitems + j);
+    cudaError_t e = launch_dep(offsets_kernel, dim3(static_cast<unsigned>(p.s.BH)), dim3(GT), 0, st, p.s.m, p.s.N,
+                               p.qtile, w.counts + j * mrows, w.expoff, w.cursor, items, w.nitems + j);
+    if (e != cudaSuccess) return e;
     const int64_t nblocks = (p.s.N + SCT * SQT - 1) / (SCT * SQT);
-    scatter_kernel<<<static_cast<unsigned>(p.s.BH * nblocks), SCT, 0, st>>>(route, p.s.N, p.s.m, p.s.s_route, j,
-                                                                            nblocks, w.cursor, perm);
-    return cudaGetLastError();
+    return launch_dep(scatter_kernel, dim3(static_cast<unsigned>(p.s.BH * nblocks)), dim3(SCT), 0, st, route, p.s.N,
+                      p.s.m, p.s.s_route, j, nblocks, w.cursor, perm);
 }
 
 }  // namespace mita

@@ -165,6 +165,35 @@ __device__ __forceinline__ float warp_sum(float x) {
 constexpr float kLog2e = 1.4426950408889634f;
 
 // ----------------------------------------------------------------------------
+// Programmatic dependent launch: a kernel launched by launch_dep may be
+// scheduled while the kernel before it in the stream is still finishing, so
+// the launch latency overlaps that kernel's tail (about 2.5 us per kernel
+// boundary, measured on GB300). Such a kernel calls dep_entry() first, before
+// it touches memory or allocates tensor memory: the wait returns once the
+// kernel before has completed and its writes are visible (at once when there
+// is no such dependency), and the trigger lets the next kernel's launch start.
+// ----------------------------------------------------------------------------
+__device__ __forceinline__ void dep_entry() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <typename... P, typename... A>
+cudaError_t launch_dep(void (*kern)(P...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, A&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<P>(args)...);
+}
+
+// ----------------------------------------------------------------------------
 // Launchers (each returns cudaGetLastError() of its launches).
 // ----------------------------------------------------------------------------
 cudaError_t launch_pool(const Plan& p, const Work& w, const __nv_bfloat16* Q, cudaStream_t st);

@@ -22,6 +22,7 @@ __global__ void __launch_bounds__(256) pool_kernel(const __nv_bfloat16* __restri
                                                    int p, int m, float* __restrict__ lq32,
                                                    __nv_bfloat16* __restrict__ lqhi,
                                                    __nv_bfloat16* __restrict__ lqlo) {
+    dep_entry();  // (launched by launch_dep: the kernel before may still be finishing)
     __shared__ float red[32][D + 4];
     const int i = static_cast<int>(blockIdx.x % static_cast<unsigned>(m));
     const int64_t bh = blockIdx.x / static_cast<unsigned>(m);
@@ -101,6 +102,7 @@ __global__ void __launch_bounds__(256) pool_warp_kernel(const __nv_bfloat16* __r
                                                         int p, int m, int64_t rows, float* __restrict__ lq32,
                                                         __nv_bfloat16* __restrict__ lqhi,
                                                         __nv_bfloat16* __restrict__ lqlo) {
+    dep_entry();  // (launched by launch_dep: the kernel before may still be finishing)
     const int lane = threadIdx.x & 31;
     const int64_t wg = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
     if (wg >= rows) return;  // (warp-uniform; no block-wide barrier)
@@ -178,13 +180,12 @@ cudaError_t launch_pool(const Plan& p, const Work& w, const __nv_bfloat16* Q, cu
                                    : ((p.s.gh + p.s.p - 1) / p.s.p + 1) * ((p.s.gw + p.s.p - 1) / p.s.p + 1);
     const int64_t rows = p.s.BH * p.s.m;
     if (win <= 128) {
-        pool_warp_kernel<<<static_cast<unsigned>((rows + 7) / 8), 256, 0, st>>>(Q, p.s.N, p.s.gh, p.s.gw, p.s.p, p.s.m,
-                                                                             rows, w.lq32, w.lqhi, w.lqlo);
-        return cudaGetLastError();
+        return launch_dep(pool_warp_kernel, dim3(static_cast<unsigned>((rows + 7) / 8)), dim3(256), 0, st, Q, p.s.N,
+                          p.s.gh, p.s.gw, p.s.p, p.s.m, rows, w.lq32, w.lqhi, w.lqlo);
     }
     const unsigned grid = static_cast<unsigned>(rows);
-    pool_kernel<<<grid, 256, 0, st>>>(Q, p.s.N, p.s.gh, p.s.gw, p.s.p, p.s.m, w.lq32, w.lqhi, w.lqlo);
-    return cudaGetLastError();
+    return launch_dep(pool_kernel, dim3(grid), dim3(256), 0, st, Q, p.s.N, p.s.gh, p.s.gw, p.s.p, p.s.m, w.lq32,
+                      w.lqhi, w.lqlo);
 }
 
 }  // namespace mita

@@ -54,6 +54,7 @@ template <bool MULTI>
 __global__ void __launch_bounds__(RT_THREADS, 1) route_tc_kernel(const __grid_constant__ CUtensorMap tq,
                                                           const __grid_constant__ CUtensorMap thi,
                                                           const __grid_constant__ CUtensorMap tlo, RouteArgs a) {
+    dep_entry();  // (launched by launch_dep: the kernel before may still be finishing)
     extern __shared__ uint8_t smem_raw[];
     __shared__ uint64_t qfull[QST], qempty[QST], dfull[2], dfree[2], lqfull, lqfree, drain;
     __shared__ uint32_t tmem_base;
@@ -322,8 +323,7 @@ cudaError_t launch_route_tc(const Plan& p, const Work& w, const __nv_bfloat16* Q
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(SMEM));
     if (e != cudaSuccess) return e;
     const int64_t grid = std::min<int64_t>(device_sms(), a.total_tiles);
-    kern<<<static_cast<unsigned>(grid), RT_THREADS, SMEM, st>>>(tq, thi, tlo, a);
-    return cudaGetLastError();
+    return launch_dep(kern, dim3(static_cast<unsigned>(grid)), dim3(RT_THREADS), SMEM, st, tq, thi, tlo, a);
 }
 
 }  // namespace mita

@@ -128,6 +128,7 @@ __device__ __forceinline__ bool issue_pv(const ScanArgs& a, uint8_t* base, uint3
 template <bool FULL, int NL>
 __global__ void __launch_bounds__(Cfg<FULL, NL>::NT, Cfg<FULL, NL>::MINB)
     scan_tc_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv, ScanArgs a) {
+    dep_entry();  // (launched by launch_dep: the kernel before may still be finishing)
     using C = Cfg<FULL, NL>;
     constexpr int KT = C::KT;
     extern __shared__ uint8_t smem_raw[];
@@ -452,14 +453,14 @@ cudaError_t launch_one(const CUtensorMap& tk, const CUtensorMap& tv, const ScanA
                                          static_cast<int>(C::SMEM));
     if (e != cudaSuccess) return e;
     const unsigned grid = static_cast<unsigned>(BH * a.chunks);
-    scan_tc_kernel<FULL, NL><<<grid, C::NT, C::SMEM, st>>>(tk, tv, a);
-    return cudaGetLastError();
+    return launch_dep(scan_tc_kernel<FULL, NL>, dim3(grid), dim3(C::NT), C::SMEM, st, tk, tv, a);
 }
 
 // One thread per landmark: the candidates its chunks kept; a head with a
 // landmark below k is flagged (every head's flag is written).
 __global__ void __launch_bounds__(256) scan_check_kernel(const int* __restrict__ ccount, int chunks, int m, int k,
                                                          int* __restrict__ hflag) {
+    dep_entry();  // (launched by launch_dep: the kernel before may still be finishing)
     const int64_t bh = blockIdx.x;
     bool bad = false;
     for (int i = threadIdx.x; i < m; i += 256) {
@@ -523,8 +524,8 @@ cudaError_t launch_scan_tc(const Plan& p, const Work& w, const __nv_bfloat16* K,
 
 cudaError_t launch_scan_verify(const Plan& p, const Work& w, const __nv_bfloat16* K, cudaStream_t st) {
     const ScanLevel& L = p.lev[p.nlev - 1];
-    scan_check_kernel<<<static_cast<unsigned>(p.s.BH), 256, 0, st>>>(w.ccount, L.chunks, p.s.m, p.s.k, w.hflag);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_dep(scan_check_kernel, dim3(static_cast<unsigned>(p.s.BH)), dim3(256), 0, st, w.ccount,
+                               L.chunks, p.s.m, p.s.k, w.hflag);
     if (e != cudaSuccess) return e;
     CUtensorMap tk;
     if (!make_head_tmap(&tk, K, static_cast<uint64_t>(L.S), static_cast<uint64_t>(p.s.BH),

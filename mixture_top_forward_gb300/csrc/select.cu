@@ -40,6 +40,7 @@ __global__ void __launch_bounds__(ST) select_kernel(int m, int k, int chunks, in
                                                     int rcap, const uint64_t* __restrict__ thr_in,
                                                     float* __restrict__ lse_out, int jspec,
                                                     uint64_t* __restrict__ theta_safe) {
+    dep_entry();  // (launched by launch_dep: the kernel before may still be finishing)
     __shared__ unsigned hist[256];
     __shared__ int offs[ST + 1];        // chunk offsets into staged[] (chunks <= ST)
     __shared__ float red[ST / 32 + 1];  // block reductions
@@ -427,6 +428,7 @@ __global__ void __launch_bounds__(DW * 32) dense_row_select_kernel(
     int64_t rows, int m, int k, int chunks, const float* __restrict__ part, float* __restrict__ lv32,
     __nv_bfloat16* __restrict__ lvbf, int32_t* __restrict__ expert_idx, const float* __restrict__ dense, int n,
     int64_t ld, float* __restrict__ lse_out) {
+    dep_entry();  // (launched by launch_dep: the kernel before may still be finishing)
     __shared__ uint32_t s_key[DW][kSurv];
     __shared__ int32_t s_idx[DW][kSurv];
     __shared__ unsigned s_hist[DW][256];
@@ -562,34 +564,30 @@ cudaError_t launch_select(const Plan& p, const Work& w, int32_t* expert_idx, cud
         const int64_t rows = p.s.BH * p.s.m;
         const unsigned grid = static_cast<unsigned>((rows + DW - 1) / DW);
         auto go = [&](auto kern) {
-            kern<<<grid, DW * 32, 0, st>>>(rows, p.s.m, p.s.k, L.chunks, p.shared ? w.part : nullptr, w.lv32, w.lvbf,
-                                           expert_idx, w.dense, static_cast<int>(p.s.N), L.ld, lse_out);
+            return launch_dep(kern, dim3(grid), dim3(DW * 32), 0, st, rows, p.s.m, p.s.k, L.chunks,
+                              p.shared ? w.part : nullptr, w.lv32, w.lvbf, expert_idx, w.dense,
+                              static_cast<int>(p.s.N), L.ld, lse_out);
         };
         switch ((p.s.k + 31) / 32) {
-            case 1: go(dense_row_select_kernel<1>); break;
-            case 2: go(dense_row_select_kernel<2>); break;
-            case 3: go(dense_row_select_kernel<3>); break;
-            default: go(dense_row_select_kernel<4>); break;
+            case 1: return go(dense_row_select_kernel<1>);
+            case 2: return go(dense_row_select_kernel<2>);
+            case 3: return go(dense_row_select_kernel<3>);
+            default: return go(dense_row_select_kernel<4>);
         }
-        return cudaGetLastError();
     }
-    select_kernel<false><<<grid, ST, 0, st>>>(p.s.m, p.s.k, L.chunks, L.cap, p.shared ? w.part : nullptr, w.cand,
-                                             w.ccount, w.lv32,
-                                             w.lvbf, expert_idx, nullptr, L.dense ? w.dense : nullptr, p.s.N, L.ld,
-                                             1, w.ridx, w.rval, w.rcount, L.rcap, p.nlev > 1 ? w.theta : nullptr,
-                                             lse_out, 0, nullptr);
-    return cudaGetLastError();
+    return launch_dep(select_kernel<false>, dim3(grid), dim3(ST), 0, st, p.s.m, p.s.k, L.chunks, L.cap,
+                      p.shared ? w.part : nullptr, w.cand, w.ccount, w.lv32, w.lvbf, expert_idx, nullptr,
+                      L.dense ? w.dense : nullptr, p.s.N, L.ld, int64_t(1), w.ridx, w.rval, w.rcount, L.rcap,
+                      p.nlev > 1 ? w.theta : nullptr, lse_out, 0, nullptr);
 }
 
 cudaError_t launch_pilot_select(const Plan& p, const Work& w, int level, cudaStream_t st) {
     const unsigned grid = static_cast<unsigned>(p.s.BH * p.s.m);
     const ScanLevel& L = p.lev[level];
-    select_kernel<true><<<grid, ST, 0, st>>>(p.s.m, p.s.k, L.chunks, L.cap, nullptr, w.cand, w.ccount, nullptr,
-                                            nullptr, nullptr, w.theta, L.dense ? w.dense : nullptr, L.S, L.ld,
-                                            L.stride, w.ridx, w.rval, w.rcount, L.rcap,
-                                            level > 0 ? w.theta : nullptr, nullptr, p.spec_j,
-                                            p.spec_j && level == p.nlev - 2 ? w.theta_safe : nullptr);
-    return cudaGetLastError();
+    return launch_dep(select_kernel<true>, dim3(grid), dim3(ST), 0, st, p.s.m, p.s.k, L.chunks, L.cap, nullptr,
+                      w.cand, w.ccount, nullptr, nullptr, nullptr, w.theta, L.dense ? w.dense : nullptr, L.S, L.ld,
+                      L.stride, w.ridx, w.rval, w.rcount, L.rcap, level > 0 ? w.theta : nullptr, nullptr, p.spec_j,
+                      p.spec_j && level == p.nlev - 2 ? w.theta_safe : nullptr);
 }
 
 }  // namespace mita

@@ -101,6 +101,7 @@ constexpr uint32_t kSfIdescPV = umma::idesc_bf16(128, 64, true);   // O += P val
 constexpr uint32_t kSfIdescR = umma::idesc_bf16(128, 32, false);   // routing: Q landmarks^T
 
 __global__ void __launch_bounds__(SF_THREADS, 1) small_fused_kernel(SFArgs a) {
+    dep_entry();  // (launched by launch_dep: the kernel before may still be finishing)
     extern __shared__ uint8_t sm_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(sm_raw) + 1023) & ~uintptr_t(1023));
     __shared__ uint64_t sfull[2], sfree[2], pfull[2], pvdone[2], rfull[2], drain, cfull, cpfull, cvdone;
@@ -553,8 +554,7 @@ cudaError_t launch_small_fused(const Plan& p, const __nv_bfloat16* Q, const __nv
     cudaError_t e =
         cudaFuncSetAttribute(small_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    small_fused_kernel<<<static_cast<unsigned>(p.s.BH), SF_THREADS, smem, st>>>(a);
-    return cudaGetLastError();
+    return launch_dep(small_fused_kernel, dim3(static_cast<unsigned>(p.s.BH)), dim3(SF_THREADS), smem, st, a);
 }
 
 }  // namespace mita
