@@ -960,6 +960,12 @@ cudaError_t launch_expert_tc(const Plan& p, const Work& w, const __nv_bfloat16* 
                                         : (rl ? expert_tc_kernel<kPlain, false, true> : expert_tc_kernel<kPlain, false>)));
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smi));
     if (e != cudaSuccess) return e;
+    if (multi) {
+        // (the s > 1 passes follow each other directly: launched early, the
+        // next pass's attention measured 1.1 ms slower at long1m, s = 2)
+        kern<<<device_sms(), NT, smi, st>>>(tq, tk, tv, tlq, tlv, a);
+        return cudaGetLastError();
+    }
     return launch_dep(kern, dim3(device_sms()), dim3(NT), smi, st, tq, tk, tv, tlq, tlv, a);
 }
 

@@ -518,16 +518,17 @@ int run_forward(const Plan& P, const Work& W, const __nv_bfloat16* Q, const __nv
     }
     const size_t mrows = static_cast<size_t>(P.s.BH) * P.s.m;
     const int sr = P.s.s_route;
+    // (all before the first kernel, so that the kernels that follow each
+    // other in the stream can overlap their launches)
     if ((e = cudaMemsetAsync(W.counts, 0, sr * mrows * sizeof(int), st)) != cudaSuccess ||
-        (e = cudaMemsetAsync(W.nitems, 0, sr * sizeof(int), st)) != cudaSuccess)
+        (e = cudaMemsetAsync(W.nitems, 0, sr * sizeof(int), st)) != cudaSuccess ||
+        (P.scan_tc && P.nlev > 1 && (e = cudaMemsetAsync(W.theta, 0, mrows * sizeof(uint64_t), st)) != cudaSuccess))
         return cuda_fail(e, "cudaMemsetAsync");
     StageMarks marks(st);
     marks.mark(0);
     if ((e = launch_pool(P, W, Q, st)) != cudaSuccess) return cuda_fail(e, "landmark pooling launch");
     marks.mark(1);
     if (P.scan_tc) {
-        if (P.nlev > 1 && (e = cudaMemsetAsync(W.theta, 0, mrows * sizeof(uint64_t), st)) != cudaSuccess)
-            return cuda_fail(e, "cudaMemsetAsync");
         for (int l = 0; l + 1 < P.nlev; ++l) {
             if ((e = launch_scan_tc(P, W, K, V, l, st)) != cudaSuccess) return cuda_fail(e, "pilot scan launch");
             if ((e = launch_pilot_select(P, W, l, st)) != cudaSuccess) return cuda_fail(e, "pilot select launch");
