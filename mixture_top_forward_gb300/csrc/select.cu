@@ -42,15 +42,17 @@ __global__ void __launch_bounds__(ST) select_kernel(int m, int k, int chunks, in
                                                     uint64_t* __restrict__ theta_safe) {
     dep_entry();  // (launched by launch_dep: the kernel before may still be finishing)
     __shared__ unsigned hist[256];
+    __shared__ unsigned hist2[256];     // (two-target radix select: the second target's histogram)
+    __shared__ int s_dg[2];             // (two-target radix select: each target's digit and keys above it)
+    __shared__ unsigned s_ab[2];
     __shared__ int offs[ST + 1];        // chunk offsets into staged[] (chunks <= ST)
     __shared__ float red[ST / 32 + 1];  // block reductions
     __shared__ float fac[ST];           // LV merge: per-chunk rescale factors
     __shared__ float osum[4][D];
     __shared__ uint64_t staged[SEL_CAP];
-    __shared__ __align__(8) int sel[MITA_SORT_MAX];  // (the pilot's speculative pass: MITA_SORT_MAX / 2 keys)
+    __shared__ int sel[MITA_SORT_MAX];
     __shared__ int nsel;
     __shared__ int wcnt[ST / 32];  // ordered take: selected keys per warp in the round
-    __shared__ unsigned long long s_kj;
     __shared__ int nst;  // keys staged (records expanded); counts past SEL_CAP too
     __shared__ int s_digit;
     __shared__ unsigned s_above;
@@ -309,41 +311,97 @@ __global__ void __launch_bounds__(ST) select_kernel(int m, int k, int chunks, in
         }
         return prefix;
     };
-    uint64_t kth = 0;  // keep every key >= kth
-    if (total > k || (PILOT && total == k)) kth = radix_select(static_cast<unsigned>(k), for_each);
-    if (PILOT) {
-        // The last pilot of a speculative scan (theta_safe set) also finds the
-        // jspec-th largest key (jspec < k), by the same radix select over the
-        // keys at or above the k-th (at least k of them, gathered in shared
-        // memory when they fit). It becomes the threshold, the k-th the
-        // fallback.
-        bool ranked = false;
-        if (theta_safe && total >= k) {
-            uint64_t* g = reinterpret_cast<uint64_t*>(sel);
-            constexpr int GCAP = MITA_SORT_MAX / 2;
-            if (tid == 0) nsel = 0;
+    // The k-th and the j-th largest (j < k) in the same passes: one histogram
+    // while both are searching with the same prefix, one each once they
+    // differ (or one of them is done); warp 0 finds the k-th's digit, warp 1
+    // the j-th's.
+    auto radix_select2 = [&](unsigned tk, unsigned tj, auto&& each, uint64_t& out_k, uint64_t& out_j) {
+        uint64_t pk = 0, pj = 0, mask = 0;
+        unsigned rk = tk, rj = tj;
+        bool dk = false, dj = false;
+        for (int shift = 56; shift >= 0; shift -= 8) {
+            const bool same = pk == pj && !dk && !dj;
+            hist[tid] = 0;
+            hist2[tid] = 0;
             __syncthreads();
-            for_each([&](uint64_t x) {
-                if (x >= kth) {
-                    const int p = atomicAdd(&nsel, 1);
-                    if (p < GCAP) g[p] = x;
-                }
+            each([&](uint64_t x) {
+                const uint64_t xm = x & mask;
+                const unsigned dg = (x >> shift) & 255u;
+                if (!dk && xm == pk) atomicAdd(&hist[dg], 1u);
+                if (!dj && !same && xm == pj) atomicAdd(&hist2[dg], 1u);
             });
             __syncthreads();
-            const int n = nsel;
-            if (n > jspec && n <= GCAP) {
-                const uint64_t kj = radix_select(static_cast<unsigned>(jspec), [&](auto&& f) {
-                    for (int e = tid; e < n; e += ST) f(g[e]);
-                });
-                if (tid == 0) s_kj = kj;
-                ranked = true;
+            if (tid < 64) {
+                const int t2 = tid >> 5, ln = tid & 31;
+                if (t2 == 0 ? !dk : !dj) {
+                    const unsigned* h = (t2 == 1 && !same) ? hist2 : hist;
+                    const unsigned remaining = t2 == 0 ? rk : rj;
+                    unsigned cc[8], tot = 0;
+#pragma unroll
+                    for (int t = 0; t < 8; ++t) {
+                        cc[t] = h[255 - 8 * ln - t];
+                        tot += cc[t];
+                    }
+                    unsigned incl = tot;
+#pragma unroll
+                    for (int o = 1; o < 32; o <<= 1) {
+                        const unsigned y = __shfl_up_sync(0xffffffffu, incl, o);
+                        if (ln >= o) incl += y;
+                    }
+                    const unsigned excl = incl - tot;
+                    if (excl < remaining && remaining <= incl) {
+                        unsigned run = excl;
+                        for (int t = 0; t < 8; ++t) {
+                            if (run + cc[t] >= remaining) {
+                                s_dg[t2] = 255 - 8 * ln - t;
+                                s_ab[t2] = run;
+                                break;
+                            }
+                            run += cc[t];
+                        }
+                    }
+                }
             }
             __syncthreads();
+            bool wk = dk, wj = dj;
+            if (!dk) {
+                rk -= s_ab[0];
+                pk |= static_cast<uint64_t>(s_dg[0]) << shift;
+                wk = hist[s_dg[0]] == rk;  // the whole bin is selected: the prefix separates it
+            }
+            if (!dj) {
+                rj -= s_ab[1];
+                pj |= static_cast<uint64_t>(s_dg[1]) << shift;
+                wj = (same ? hist : hist2)[s_dg[1]] == rj;
+            }
+            mask |= 0xFFull << shift;
+            __syncthreads();
+            dk = wk;
+            dj = wj;
+            if (dk && dj) break;
         }
+        out_k = pk;
+        out_j = pj;
+    };
+    uint64_t kth = 0;  // keep every key >= kth
+    uint64_t kj = 0;   // the last speculative pilot: its jspec-th largest key
+    bool ranked = false;
+    if (total > k || (PILOT && total == k)) {
+        if (PILOT && theta_safe && jspec > 0 && jspec < k) {
+            radix_select2(static_cast<unsigned>(k), static_cast<unsigned>(jspec), for_each, kth, kj);
+            ranked = true;
+        } else {
+            kth = radix_select(static_cast<unsigned>(k), for_each);
+        }
+    }
+    if (PILOT) {
+        // The last pilot of a speculative scan (theta_safe set) has also
+        // found the jspec-th largest key (jspec < k, in the same passes): it
+        // becomes the threshold, the k-th the fallback.
         if (tid == 0) {
             const uint64_t old = theta[bh * m + i];
             const uint64_t safe = (total >= k && kth > old) ? kth : old;
-            const uint64_t spec = ranked && s_kj > safe ? static_cast<uint64_t>(s_kj) : safe;
+            const uint64_t spec = ranked && kj > safe ? kj : safe;
             theta[bh * m + i] = spec;
             if (theta_safe) theta_safe[bh * m + i] = safe;
         }
