@@ -222,6 +222,23 @@ int mita_forward_noalloc(const void* Q, const void* K, const void* V, int B, int
 size_t mita_workspace_bytes(int B, int H, int N, int d, int grid_h, int grid_w, int m, int k);
 
 /*
+ * The landmark scan's schedule for one shape: how the k best keys of each
+ * landmark ("NeurIPS 2026 | Mixture-of-Top-k 注意力" (shuwu5.cn), section
+ * "MiTA：用少量地标查询，同时完成压缩与专家构造": each landmark's routed
+ * expert) are found. A diagnostic for library users; host only, it needs
+ * no GPU and launches nothing. Writes at most cap values to info (int64,
+ * caller-owned): the number of scan levels L (the pilot levels on strided
+ * key samples, then the main scan over every key); 1 when the main scan
+ * writes every logit of its rows and ranks whole rows, else 0; the rank j
+ * of the last pilot's speculative threshold key (0: none, the threshold is
+ * the k-th best sample key); then for each level its number of keys S, the
+ * stride between them, and 1 when the level writes every logit, else 0.
+ * Returns the number of values a full answer takes (3 + 3 L; values past
+ * cap are not written), or 0 for an invalid or empty shape (info untouched).
+ */
+int mita_plan_info(int B, int H, int N, int d, int grid_h, int grid_w, int m, int k, int64_t* info, int cap);
+
+/*
  * Waits for `stream`, then reports and clears the device-side status words of
  * the current device that calls on `stream` write (its workspace's, and the
  * no-allocation scratch's): MITA_OK, MITA_ERR_TIMEOUT when a bounded wait

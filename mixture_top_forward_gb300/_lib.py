@@ -71,6 +71,8 @@ def load(path: str | None = None, build_if_missing: bool = True) -> ctypes.CDLL:
         lib.mita_forward_host.restype = ci
         lib.mita_workspace_bytes.argtypes = [ci] * 8
         lib.mita_workspace_bytes.restype = ctypes.c_size_t
+        lib.mita_plan_info.argtypes = [ci] * 8 + [vp, ci]
+        lib.mita_plan_info.restype = ci
         lib.mita_selftest_wait.argtypes = [ctypes.c_int64, vp]
         lib.mita_selftest_wait.restype = ci
         lib.mita_sync_status.argtypes = [vp]
@@ -269,6 +271,19 @@ def mita_forward_host(Q, K, V, grid_h: int, grid_w: int, m: int, k: int, out=Non
 
 def mita_workspace_bytes(B, H, N, d, grid_h, grid_w, m, k) -> int:
     return int(load().mita_workspace_bytes(B, H, N, d, grid_h, grid_w, m, k))
+
+
+def mita_plan_info(B, H, N, d, grid_h, grid_w, m, k) -> dict | None:
+    """The landmark scan's schedule (mita_plan_info in mita.h): the levels as
+    (keys, stride, dense) tuples, whether the main scan ranks whole rows, and
+    the speculative threshold key's rank (0: none). None for an invalid shape."""
+    buf = (ctypes.c_int64 * 32)()
+    n = int(load().mita_plan_info(B, H, N, d, grid_h, grid_w, m, k, ctypes.cast(buf, ctypes.c_void_p), 32))
+    if n == 0:
+        return None
+    v = list(buf[:n])
+    levels = [(int(v[3 + 3 * l]), int(v[4 + 3 * l]), bool(v[5 + 3 * l])) for l in range(int(v[0]))]
+    return {"levels": levels, "dense_main": bool(v[1]), "spec_j": int(v[2])}
 
 
 def mita_sync_status(stream=None) -> int:

@@ -818,6 +818,31 @@ extern "C" size_t mita_workspace_bytes(int B, int H, int N, int d, int grid_h, i
     return P.total;
 }
 
+extern "C" int mita_plan_info(int B, int H, int N, int d, int grid_h, int grid_w, int m, int k, int64_t* info,
+                              int cap) {
+    Shape s;
+    bool empty;
+    char saved[sizeof g_err];
+    memcpy(saved, g_err, sizeof g_err);
+    const int rc = check_shape(B, H, N, d, grid_h, grid_w, m, k, &s, &empty);
+    memcpy(g_err, saved, sizeof g_err);
+    if (rc != MITA_OK || empty) return 0;
+    Plan P;
+    if (!make_plan(s, &P)) return 0;
+    int64_t v[3 + 3 * 4];
+    int n = 0;
+    v[n++] = P.nlev;
+    v[n++] = P.dense ? 1 : 0;
+    v[n++] = P.spec_j;
+    for (int l = 0; l < P.nlev; ++l) {
+        v[n++] = P.lev[l].S;
+        v[n++] = P.lev[l].stride;
+        v[n++] = P.lev[l].dense ? 1 : 0;
+    }
+    for (int i = 0; i < n && i < cap && info; ++i) info[i] = v[i];
+    return n;
+}
+
 static int* noalloc_status(int dev);
 
 extern "C" int mita_sync_status(void* stream) {

@@ -108,3 +108,44 @@ def test_variants_empty_problem_is_a_no_op(lib):
     assert _multi(lib, 2, B=0) == M.MITA_OK
     assert _bwd(lib, B=0) == M.MITA_OK
     assert lib.mita_forward_routed(FAKE, FAKE, FAKE, 0, 1, 196, 64, 14, 14, 25, 25, FAKE, FAKE, FAKE, None) == M.MITA_OK
+
+
+def _ceil(a, b):
+    return -(-a // b)
+
+
+@pytest.mark.parametrize("N,m,k,pilots,dense_main", [
+    # N = 1M: a dense first level of 4 t = 8192 samples (t = 8 k), one
+    # filtered level 16x larger (32768 = N/32, the cap), then every key
+    (1 << 20, 256, 256, [(8192, 128, True), (32768, 32, False)], False),
+    # 256K: the first level (8192 = N/32) is the last one
+    (1 << 18, 256, 256, [(8192, 32, True)], False),
+    # 64K: the dense first level is capped at N/16 = 4096 samples
+    (1 << 16, 256, 256, [(4096, 16, True)], False),
+    # the LRA shape: a sample could only pass one key in 8, so no pilots and
+    # the main scan writes every logit and ranks whole rows
+    (4096, 64, 64, [], True),
+])
+def test_plan_info_pilot_schedule(lib, N, m, k, pilots, dense_main):
+    """The landmark scan's schedule (mita_plan_info): the pilot levels'
+    sample sizes and strides, the main scan over every key, and the
+    speculative threshold's rank j = ceil(2 k S / N) + 8 (S: the last pilot's
+    samples), used only when below k."""
+    info = M.mita_plan_info(1, 8, N, 64, 0, 0, m, k)
+    assert info["levels"][:-1] == pilots
+    assert info["levels"][-1] == (N, 1, dense_main)
+    assert info["dense_main"] == dense_main
+    if pilots:
+        S = pilots[-1][0]
+        j = _ceil(2 * k * S, N) + 8
+        assert info["spec_j"] == (j if j < k else 0)
+        # every level's keys are a strided sample of the head's N keys
+        for s, stride, _ in pilots:
+            assert s == _ceil(N, stride)
+    else:
+        assert info["spec_j"] == 0
+
+
+def test_plan_info_rejects_bad_shapes(lib):
+    assert M.mita_plan_info(1, 1, 196, 65, 14, 14, 25, 25) is None  # d != 64
+    assert M.mita_plan_info(0, 1, 196, 64, 14, 14, 25, 25) is None  # empty
