@@ -149,3 +149,34 @@ def test_plan_info_pilot_schedule(lib, N, m, k, pilots, dense_main):
 def test_plan_info_rejects_bad_shapes(lib):
     assert M.mita_plan_info(1, 1, 196, 65, 14, 14, 25, 25) is None  # d != 64
     assert M.mita_plan_info(0, 1, 196, 64, 14, 14, 25, 25) is None  # empty
+
+
+@pytest.mark.parametrize("N", [1000, 4096, 8192, 40000, 65536, 1 << 18, 1 << 20, 1 << 22])
+@pytest.mark.parametrize("m,k", [(16, 16), (64, 64), (256, 256), (300, 70), (64, 1024)])
+def test_plan_info_invariants(lib, N, m, k):
+    """Over a sweep of shapes: each level samples keys at a stride (the
+    last is the main scan over every key, stride 1), later levels sample
+    more keys at smaller strides, every level holds at least k keys, the
+    filtered pilot levels stay within N/32 and the dense first one within
+    N/8, and the speculative rank follows j = ceil(2 k S / N) + 8 when below
+    k (0 otherwise, and whenever the main scan ranks whole rows)."""
+    if k > N or m > N:
+        return
+    info = M.mita_plan_info(1, 2, N, 64, 0, 0, m, k)
+    assert info is not None
+    lv = info["levels"]
+    assert lv[-1][0] == N and lv[-1][1] == 1
+    for (s, stride, _) in lv:
+        assert s == _ceil(N, stride) and s >= min(k, N)
+    for a, b in zip(lv, lv[1:]):
+        assert a[0] < b[0] and a[1] > b[1]
+    pilots = lv[:-1]
+    for i, (s, stride, dense) in enumerate(pilots):
+        assert s <= N // 8
+        if i > 0:
+            assert not dense and s <= N // 32
+    if info["dense_main"] or not pilots:
+        assert info["spec_j"] == 0
+    else:
+        j = _ceil(2 * k * pilots[-1][0], N) + 8
+        assert info["spec_j"] == (j if j < k else 0)
